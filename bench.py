@@ -1,0 +1,514 @@
+"""Benchmark of the multi-LoRA decode hot path on GB300.
+
+One step = one InvisibleLoRA decode cycle through one transformer block's
+seven projections on the Llama-3-8B-shaped workload (64 requests, 16
+resident rank-16 adapters with Zipf(1.1) popularity, 1 draft token per
+request, vocabulary 128256):
+
+    plan (a1)  ->  draft pass: 7 x base GEMM, M = 64 rows, LoRA off (a3)
+               ->  verify pass: 7 x (shrink a2 + GEMM a3 + fused expand a4), M = 128 rows
+               ->  accept / resample for 64 requests (a5, a6)
+
+`value` is verified tokens (M = 128 per step, summed over ranks) per second
+with every input resident in HBM, from CUDA events around K replays of the
+step captured as one CUDA graph.  The W working set (436 MB per pass, read
+twice per step) is larger than L2, so weights stream from HBM every launch.
+`e2e` is the same metric through the Python C-ABI binding with pinned host
+buffers: each step copies that step's activations and probabilities to the
+device and reads every output back.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own replica on its own requests
+(weak scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as WL  # noqa: E402
+
+CFG = WL.LLAMA8B_R16
+K_DRAFT = 1
+METRIC = "multi-LoRA decode-step tokens/s (draft+verify layer x7 projections + accept)"
+UNIT = "tokens/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work
+# ---------------------------------------------------------------------------
+
+
+def layer_bytes_flops(M, K, N, active_ranks, verify):
+    b = 2 * (N * K + M * K + M * N)
+    f = 2 * M * N * K
+    if verify:
+        b += sum(2 * r * K + 2 * N * r for r in active_ranks)
+        f += 2 * M * int(np.mean(active_ranks) if active_ranks else 0) * (K + N)
+    return b, f
+
+
+def accept_bytes(B, V, accepted, k):
+    # the draw reads p_n (+ q_n when a draft was rejected); gathers are negligible
+    return int(sum(4 * V * (2 if a < k else 1) for a in accepted)) + 8 * B * k
+
+
+# ---------------------------------------------------------------------------
+# Clock sampler (nvidia-smi during the timed region)
+# ---------------------------------------------------------------------------
+
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return out
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return out
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        out.update(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(mx) if mx else None,
+                   reasons=reasons, samples=len(rows))
+        return out
+
+
+# ---------------------------------------------------------------------------
+# Workload on the device
+# ---------------------------------------------------------------------------
+
+
+def _bf16(torch, bits, device):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+class DeviceWorkload:
+    def __init__(self, torch, ml, device, seed):
+        self.torch, self.ml = torch, ml
+        cfg = CFG
+        self.ranks = WL.adapter_ranks(cfg, seed)
+        self.idx_d = WL.row_adapters(cfg, "draft", seed=seed)
+        self.idx_v = WL.row_adapters(cfg, "verify", k=K_DRAFT, seed=seed)
+        self.Md, self.Mv = len(self.idx_d), len(self.idx_v)
+        self.proj = []
+        for p, (name, K, N) in enumerate(cfg.projections):
+            W, A, B, _ = WL.projection_weights(cfg, p, seed=seed)
+            xd = WL.activations(cfg, p, "draft", seed=seed)
+            xv = WL.activations(cfg, p, "verify", k=K_DRAFT, seed=seed)
+            self.proj.append(dict(name=name, K=K, N=N, W=_bf16(torch, W, device), A=_bf16(torch, A, device),
+                                  B=_bf16(torch, B, device), xd=_bf16(torch, xd, device),
+                                  xv=_bf16(torch, xv, device), xd_h=xd, xv_h=xv,
+                                  yd=torch.empty((self.Md, N), dtype=torch.bfloat16, device=device),
+                                  yv=torch.empty((self.Mv, N), dtype=torch.bfloat16, device=device)))
+        self.rank_of = torch.from_numpy(self.ranks).to(device)
+        self.adx_d = torch.from_numpy(self.idx_d).to(device)
+        self.adx_v = torch.from_numpy(self.idx_v).to(device)
+        p, q, tok, u = WL.accept_inputs(cfg.vocab, cfg.n_requests, K_DRAFT, seed=seed)
+        self.acc_h = (p, q, tok, u)
+        self.p, self.q, self.tok, self.u = (torch.from_numpy(a).to(device) for a in (p, q, tok, u))
+        self.out_tok = torch.empty((cfg.n_requests, K_DRAFT + 1), dtype=torch.int32, device=device)
+        self.accepted = torch.empty((cfg.n_requests,), dtype=torch.int32, device=device)
+        ws_bytes = max(ml.linear_workspace_bytes(self.Mv, P["N"], P["K"], cfg.n_adapters) for P in self.proj)
+        ws_bytes = max(ws_bytes, ml.accept_workspace_bytes(cfg.n_requests, K_DRAFT, cfg.vocab))
+        self.ws = ml.Workspace(ws_bytes, device=device)
+        self.seg = None
+
+    # individual ops of one step, in order
+    def ops(self):
+        ml, cfg = self.ml, CFG
+        out = []
+
+        def plan():
+            self.seg, _ = ml.plan_segments(self.adx_v, self.rank_of, cfg.n_adapters, cfg.r_max, self.ws)
+        out.append(("plan", plan))
+        for P in self.proj:
+            out.append((f"draft.{P['name']}", lambda P=P: ml.linear(P["xd"], P["W"], None, None, None, None,
+                                                                     cfg.scale, ml.DRAFT, ws=self.ws, y=P["yd"])))
+        for P in self.proj:
+            out.append((f"verify.{P['name']}", lambda P=P: ml.linear(P["xv"], P["W"], P["A"], P["B"], self.rank_of,
+                                                                      self.adx_v, cfg.scale, ml.VERIFY, ws=self.ws,
+                                                                      y=P["yv"], seg_offsets_ptr=self.seg)))
+        out.append(("accept", lambda: ml.verify_accept(self.p, self.q, self.tok, self.u, ws=self.ws,
+                                                      out_tok=self.out_tok, accepted=self.accepted)))
+        return out
+
+    def step(self):
+        for _, f in self.ops():
+            f()
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the float64 oracle on a bounded sample of the same workload
+# ---------------------------------------------------------------------------
+
+
+def oracle_sample_step(requests, seed=0, prepared=None):
+    """Run the oracle over `requests` requests of the workload (all 7
+    projections, draft and verify rows, then accept).  Returns (seconds,
+    verify tokens)."""
+    from oracle import accept as OA
+    from oracle import layer as OL
+    cfg = CFG
+    if prepared is None:
+        prepared = prepare_oracle(seed)
+    ranks, idx_d, idx_v, proj, acc = prepared
+    rows_d = np.arange(requests)
+    rows_v = np.arange(requests * (K_DRAFT + 1))
+    t0 = time.perf_counter()
+    for (W, A, B, xd, xv) in proj:
+        OL.mlora_linear(xd[rows_d], W, None, None, None, None, cfg.scale, OL.DRAFT)
+        OL.mlora_linear(xv[rows_v], W, A, B, ranks, idx_v[rows_v], cfg.scale, OL.VERIFY)
+    p, q, tok, u = acc
+    OA.verify_accept(p[:requests], q[:requests], tok[:requests], u[:requests])
+    return time.perf_counter() - t0, len(rows_v)
+
+
+def prepare_oracle(seed=0):
+    cfg = CFG
+    f = WL.bf16_to_f64
+    ranks = WL.adapter_ranks(cfg, seed)
+    idx_d = WL.row_adapters(cfg, "draft", seed=seed)
+    idx_v = WL.row_adapters(cfg, "verify", k=K_DRAFT, seed=seed)
+    proj = []
+    for p in range(len(cfg.projections)):
+        W, A, B, _ = WL.projection_weights(cfg, p, seed=seed)
+        proj.append((f(W), f(A), f(B), f(WL.activations(cfg, p, "draft", seed=seed)),
+                     f(WL.activations(cfg, p, "verify", k=K_DRAFT, seed=seed))))
+    acc = WL.accept_inputs(cfg.vocab, 8, K_DRAFT, seed=seed)
+    return ranks, idx_d, idx_v, proj, acc
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the oracle, as it stands, on the host cores
+# ---------------------------------------------------------------------------
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    prepared = prepare_oracle(0)
+    req = 1
+    for _ in range(args.warmup):
+        oracle_sample_step(req, prepared=prepared)
+    times, toks = [], 0
+    for _ in range(args.steps):
+        t, n = oracle_sample_step(req, prepared=prepared)
+        times.append(t)
+        toks += n
+    total = sum(times)
+    value = toks / total
+    cores = cpu_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": CFG.name + f"/k={K_DRAFT}/vocab={CFG.vocab}", "requests_per_step": req},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{req} request per step: 7 projections draft+verify rows + accept, float64 numpy"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    import speculative_lora_decoding_gb300 as ml
+    if not os.path.exists(ml.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    if not ml.device_supported():
+        raise RuntimeError("this benchmark needs a compute capability 10.3 GPU")
+
+    wl = DeviceWorkload(torch, ml, device, seed=rank)
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            wl.step()
+    stream.synchronize()
+    if wl.ws.status() != 0:
+        raise RuntimeError("device status bits raised during warm-up")
+
+    # Whole step as one CUDA graph.
+    graph = torch.cuda.CUDAGraph()
+    n0 = ml.launch_count()
+    with torch.cuda.graph(graph, stream=stream):
+        wl.step()
+    launches_per_step = ml.launch_count() - n0
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    tokens_per_step = wl.Mv * world
+    value = tokens_per_step / (ms_per_step * 1e-3)
+    if wl.ws.status() != 0:
+        raise RuntimeError("device status bits raised during the timed region")
+
+    # Per-op durations: each op of the step captured as its own graph, replayed
+    # back to back with CUDA events between them on the launching stream.
+    op_graphs = []
+    for name, fn in wl.ops():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        op_graphs.append((name, g))
+    torch.cuda.synchronize()
+    reps = max(10, min(args.steps, 200))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(op_graphs) + 1)] for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for r in range(reps):
+            evs[r][0].record(stream)
+            for i, (_, g) in enumerate(op_graphs):
+                g.replay()
+                evs[r][i + 1].record(stream)
+    torch.cuda.synchronize()
+    op_ms = {name: float(np.median([evs[r][i].elapsed_time(evs[r][i + 1]) for r in range(reps)]))
+             for i, (name, _) in enumerate(op_graphs)}
+
+    # Algorithmic work.
+    hbm_gbs, bf16_tf, peak_kind = _peaks()
+    active = sorted(set(int(a) for a in wl.idx_v if a >= 0))
+    active_ranks = [int(wl.ranks[a]) for a in active]
+    draft_b = draft_t = verify_b = verify_t = 0.0
+    draft_f = verify_f = 0.0
+    for P in wl.proj:
+        b, f = layer_bytes_flops(wl.Md, P["K"], P["N"], [], False)
+        draft_b += b
+        draft_f += f
+        draft_t += op_ms[f"draft.{P['name']}"]
+        b, f = layer_bytes_flops(wl.Mv, P["K"], P["N"], active_ranks, True)
+        verify_b += b
+        verify_f += f
+        verify_t += op_ms[f"verify.{P['name']}"]
+    acc_host = wl.accepted.cpu().numpy()
+    acc_b = accept_bytes(CFG.n_requests, CFG.vocab, acc_host, K_DRAFT)
+    gemm_launches = 2 * len(wl.proj)
+    achieved = draft_b / (draft_t * 1e-3) / 1e9          # draft GEMM launches: one kernel each
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
+                "traffic": None, "kernel": "gemm_kernel (draft pass, 7 projections, M=64)",
+                "peak_kind": f"{peak_kind} hbm_gbs",
+                "algorithmic_bytes_per_launch": draft_b / len(wl.proj),
+                "avg_launch_us": 1e3 * draft_t / len(wl.proj)}
+    modes = {
+        "draft_layer": {"us": 1e3 * draft_t, "tokens_per_s": wl.Md / (draft_t * 1e-3),
+                        "GBps": draft_b / (draft_t * 1e-3) / 1e9, "frac_hbm": draft_b / (draft_t * 1e-3) / 1e9 / hbm_gbs},
+        "verify_layer": {"us": 1e3 * verify_t, "tokens_per_s": wl.Mv / (verify_t * 1e-3),
+                         "GBps": verify_b / (verify_t * 1e-3) / 1e9,
+                         "frac_hbm": verify_b / (verify_t * 1e-3) / 1e9 / hbm_gbs,
+                         "TFLOPs": verify_f / (verify_t * 1e-3) / 1e12},
+        "accept": {"us": 1e3 * op_ms["accept"], "rows_per_s": CFG.n_requests / (op_ms["accept"] * 1e-3),
+                   "GBps": acc_b / (op_ms["accept"] * 1e-3) / 1e9,
+                   "mean_accepted": float(acc_host.mean())},
+        "plan_us": 1e3 * op_ms["plan"],
+        "per_op_us": {k: 1e3 * v for k, v in op_ms.items()},
+    }
+
+    # End to end through the binding with pinned host buffers.
+    e2e = run_e2e(torch, ml, wl, stream, args, world)
+
+    cpu = None
+    if rank == 0 and world == 1:
+        try:
+            prepared = prepare_oracle(0)
+            oracle_sample_step(1, prepared=prepared)
+            secs, toks, nrep = 0.0, 0, 0
+            while secs < 10.0 and nrep < 50:
+                t, n = oracle_sample_step(8, prepared=prepared)
+                secs += t
+                toks += n
+                nrep += 1
+            cpu = {"value": toks / secs, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                   "sample": f"{nrep} x 8 requests (16 verify + 8 draft rows) through 7 projections + accept, "
+                             "float64 numpy, BLAS default threads"}
+        except Exception as exc:  # a baseline that fails does not void the GPU number
+            cpu = {"value": None, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": f"failed: {exc}"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": CFG.name + f"/k={K_DRAFT}/vocab={CFG.vocab}", "requests": CFG.n_requests,
+                       "draft_rows": wl.Md, "verify_rows": wl.Mv, "projections": [p["name"] for p in wl.proj],
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: 436 MB of W streamed per pass, two passes per step",
+                       "graph": "one CUDA graph per step"},
+            "gpu_launches": launches_per_step * args.steps,
+            "roofline": roofline,
+            "modes": modes,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                       "samples": clk["samples"]},
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(torch, ml, wl, stream, args, world):
+    """Host buffers in, host buffers out, through the public binding."""
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_x = [(pin(P["xd_h"].view(np.int16)), pin(P["xv_h"].view(np.int16))) for P in wl.proj]
+    p, q, tok, u = wl.acc_h
+    h_acc = [pin(p), pin(q), pin(tok), pin(u)]
+    h_idx = pin(wl.idx_v)
+    h_yd = [torch.empty(tuple(P["yd"].shape), dtype=torch.int16).pin_memory() for P in wl.proj]
+    h_yv = [torch.empty(tuple(P["yv"].shape), dtype=torch.int16).pin_memory() for P in wl.proj]
+    h_out = torch.empty(tuple(wl.out_tok.shape), dtype=torch.int32).pin_memory()
+    h_acc_out = torch.empty(tuple(wl.accepted.shape), dtype=torch.int32).pin_memory()
+    h2d = sum(a.numel() * a.element_size() for pair in h_x for a in pair) + sum(
+        a.numel() * a.element_size() for a in h_acc) + h_idx.numel() * 4
+    d2h = sum(a.numel() * 2 for a in h_yd + h_yv) + h_out.numel() * 4 + h_acc_out.numel() * 4
+
+    def one():
+        for P, (hd, hv) in zip(wl.proj, h_x):
+            P["xd"].view(torch.int16).copy_(hd, non_blocking=True)
+            P["xv"].view(torch.int16).copy_(hv, non_blocking=True)
+        wl.adx_v.copy_(h_idx, non_blocking=True)
+        for d, h in zip((wl.p, wl.q, wl.tok, wl.u), h_acc):
+            d.copy_(h, non_blocking=True)
+        wl.step()
+        for P, hd, hv in zip(wl.proj, h_yd, h_yv):
+            hd.copy_(P["yd"].view(torch.int16), non_blocking=True)
+            hv.copy_(P["yv"].view(torch.int16), non_blocking=True)
+        h_out.copy_(wl.out_tok, non_blocking=True)
+        h_acc_out.copy_(wl.accepted, non_blocking=True)
+
+    steps = max(3, min(args.steps, 50))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=wl.p.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": wl.Mv * world / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,226 @@
+/*
+ * mlora.h - C ABI of the multi-LoRA decode hot path for GB300 (sm_103a).
+ *
+ * Two operations, as the InvisibleLoRA abstract ("InvisibleLoRA: Fast
+ * Multi-LoRA Serving Without Per-Token LoRA Decoding") uses them:
+ *
+ *   mlora_linear         the batched multi-adapter linear layer
+ *                          draft  (LoRA off):  y = W x
+ *                          verify (LoRA on):   y = W x + scale * B_a (A_a x)
+ *                        with a = adapter_idx[row] chosen per token row.  The
+ *                        formula is "output = W·x + scale · B(A·x)" of "Multi-
+ *                        LoRA Serving in Practice", section "Core Principle:
+ *                        Shared Base Model, Per-Request Adapter Selection".
+ *   mlora_verify_accept  the per-request accept / resample step that ends the
+ *                        verify pass and keeps the target distribution
+ *                        (speculative sampling; exact integer residual draw).
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers to caller-owned memory, unless a
+ *     parameter says otherwise.  The library never allocates, frees or keeps
+ *     a pointer past the call.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronises, except mlora_read_device_status.
+ *   - Errors a host can see (null pointers, sizes, alignment, workspace size)
+ *     are returned at once and nothing is launched.  Errors only the device can
+ *     see (bad adapter index, bad rank, NaN probability, timed-out wait) set
+ *     bits in a status word inside the workspace; the affected rows are
+ *     computed by the documented fallback and no kernel traps.
+ *   - bf16 tensors are passed as uint16_t bit patterns (mlora_bf16).
+ *   - Row-major layouts throughout.  Pointers to bf16 matrices read by the
+ *     tensor-memory engine (x, W) must be 16-byte aligned and K % 8 == 0.
+ *
+ * Workspace: one caller-allocated device buffer, at least the size the
+ * matching *_workspace_bytes function returns and 256-byte aligned.  It holds
+ * a status word, zero-initialised arrival counters and scratch.  Call
+ * mlora_workspace_init once after allocating it (and after any call that
+ * returned MLORA_ERR_TIMEOUT).  Kernels leave the counters at zero when they
+ * finish, so one workspace serves any sequence of calls on one stream.  Calls
+ * that use the same workspace must not overlap in time (e.g. on two streams).
+ */
+#ifndef MLORA_H
+#define MLORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLORA_API __attribute__((visibility("default")))
+#else
+#define MLORA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mlora_bf16;   /* bf16 bit pattern */
+typedef void *mlora_stream;    /* cudaStream_t */
+
+typedef enum {
+  MLORA_OK = 0,
+  MLORA_ERR_ARG = 1,           /* null pointer, bad enum, misaligned pointer */
+  MLORA_ERR_SHAPE = 2,         /* a size outside the supported range */
+  MLORA_ERR_WORKSPACE = 3,     /* workspace missing, too small or misaligned */
+  MLORA_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed */
+  MLORA_ERR_DEVICE_STATUS = 5, /* returned by mlora_read_device_status when bits are set */
+  MLORA_ERR_TIMEOUT = 6,       /* returned by mlora_read_device_status when a device wait gave up */
+  MLORA_ERR_UNSUPPORTED = 7    /* current device is not compute capability 10.3 */
+} mlora_status;
+
+typedef enum { MLORA_DRAFT = 0, MLORA_VERIFY = 1 } mlora_mode;
+
+/* Device status bits (mlora_read_device_status). */
+#define MLORA_DEV_BAD_ADAPTER (1u << 0) /* adapter_idx outside [-1, n_adapters): row ran base-only */
+#define MLORA_DEV_BAD_RANK    (1u << 1) /* rank_of[a] outside [0, r_max]: adapter ran base-only   */
+#define MLORA_DEV_BAD_PROB    (1u << 2) /* a probability or uniform read was NaN or outside [0,1] */
+#define MLORA_DEV_BAD_TOKEN   (1u << 3) /* a draft token outside [0, V): rejected at its position */
+#define MLORA_DEV_ZERO_MASS   (1u << 4) /* residual mass 0: drew from p_n, or emitted token 0     */
+#define MLORA_DEV_TIMEOUT     (1u << 5) /* a bounded wait inside a kernel gave up                 */
+
+/* Supported ranges. */
+#define MLORA_MAX_RANK 64          /* r_max <= 64, r_max % 8 == 0 */
+#define MLORA_MAX_ADAPTERS 4096
+#define MLORA_MAX_ROWS 65536
+#define MLORA_MAX_VOCAB (1 << 24)
+
+/* ------------------------------------------------------------------------- */
+/* Workspace                                                                  */
+/* ------------------------------------------------------------------------- */
+
+/* Bytes of workspace mlora_plan_segments / mlora_shrink / mlora_linear need for
+ * M rows, N outputs, K inputs and n_adapters resident adapters, on the
+ * current device.  One workspace sized for the largest (M, N, K) of a set of
+ * projections serves all of them.  Returns 0 for sizes outside the ranges. */
+MLORA_API size_t mlora_linear_workspace_bytes(int M, int N, int K, int n_adapters);
+
+/* Bytes of workspace mlora_verify_accept needs (B requests, k drafts, V vocab). */
+MLORA_API size_t mlora_accept_workspace_bytes(int B, int k, int V);
+
+/* Zero the status word and the arrival counters (asynchronous memset). */
+MLORA_API mlora_status mlora_workspace_init(void *workspace, size_t ws_bytes, mlora_stream stream);
+
+/* Copy the device status bits to *bits (host pointer), optionally clearing
+ * them.  Synchronises `stream`.  Returns MLORA_OK if no bit is set,
+ * MLORA_ERR_TIMEOUT if MLORA_DEV_TIMEOUT is set, else MLORA_ERR_DEVICE_STATUS. */
+MLORA_API mlora_status mlora_read_device_status(void *workspace, uint32_t *bits, int clear, mlora_stream stream);
+
+/* ------------------------------------------------------------------------- */
+/* Segment plan (step a1)                                                     */
+/* ------------------------------------------------------------------------- */
+
+/* Group token rows by adapter: a stable counting sort of adapter_idx.
+ * The InvisibleLoRA abstract notes that requests are partitioned across the
+ * active adapters; "Multi-LoRA Serving in Practice", section "4. Batching:
+ * Heterogeneous LoRAs Break 'Neat' Batches", asks to aggregate requests of
+ * the same adapter.
+ *
+ *   adapter_idx  int32 [M]   adapter of each row; -1 = base only
+ *   rank_of      int32 [n_adapters]  rank of each resident adapter
+ *   r_max        row stride of A_stack / column stride of B_stack (<= 64, % 8 == 0)
+ *
+ * Writes the plan into the workspace and returns device pointers into it:
+ *   *seg_offsets  int32 [n_adapters + 2]: rows of adapter a sit at sorted
+ *                 positions [seg_offsets[a], seg_offsets[a+1]); bucket
+ *                 n_adapters holds rows without a (valid) adapter.
+ *   *perm         int32 [M]: perm[sorted position] = row; increasing within
+ *                 a bucket.
+ * Either output pointer may be NULL.  The plan depends only on adapter_idx,
+ * rank_of, n_adapters and r_max, so one plan serves every projection of a
+ * decode step that shares them (pass *seg_offsets to mlora_linear). */
+MLORA_API mlora_status mlora_plan_segments(const int32_t *adapter_idx, int M, const int32_t *rank_of, int n_adapters,
+                                 int r_max, void *workspace, size_t ws_bytes, const int32_t **seg_offsets,
+                                 const int32_t **perm, mlora_stream stream);
+
+/* ------------------------------------------------------------------------- */
+/* Shrink (step a2)                                                           */
+/* ------------------------------------------------------------------------- */
+
+/* Low-rank activations T[m, j] = sum_k A_a[j, k] x[m, k] for j < rank_of[a],
+ * a = adapter_idx[m] (the inner product A·x of "output = W·x + scale · B(A·x)").
+ *
+ *   x        bf16 [M, K]          A_stack  bf16 [n_adapters, r_max, K]
+ *   T        fp32 [M, r_max] out: zero where j >= rank and on rows without
+ *            a valid adapter; fp32 accumulation.
+ *   seg_offsets  the pointer mlora_plan_segments returned for this workspace.
+ * Rows of A past rank_of[a] are never read. */
+MLORA_API mlora_status mlora_shrink(const mlora_bf16 *x, int M, int K, const mlora_bf16 *A_stack, int n_adapters, int r_max,
+                          const int32_t *seg_offsets, float *T, void *workspace, size_t ws_bytes,
+                          mlora_stream stream);
+
+/* ------------------------------------------------------------------------- */
+/* Multi-adapter linear layer (steps a1-a4)                                   */
+/* ------------------------------------------------------------------------- */
+
+/* y = W x (mode MLORA_DRAFT) or y = W x + scale * B_a[:, :r] (A_a[:r, :] x)
+ * (mode MLORA_VERIFY), per row, a = adapter_idx[row], r = rank_of[a].
+ *
+ *   x        bf16 [M, K]   token rows (verify rows are request-major:
+ *                          row = request * (k+1) + t)
+ *   W        bf16 [N, K]   base weight (out x in)
+ *   A_stack  bf16 [n_adapters, r_max, K]   B_stack  bf16 [n_adapters, N, r_max]
+ *            (only the first rank_of[a] rows of A_a / columns of B_a are read;
+ *            may be NULL in draft mode, as may rank_of and adapter_idx)
+ *   seg_offsets  NULL: plan first (step a1) into the workspace.  Otherwise the
+ *            pointer mlora_plan_segments returned for this workspace and the
+ *            same adapter_idx / rank_of / n_adapters / r_max.
+ *   scale    LoRA scaling (alpha / r), one scalar per call
+ *   y        bf16 [M, N] out, rows in input order; fp32 accumulation, one
+ *            round to nearest even at the end.
+ *
+ * The base product runs on the tcgen05 tensor cores (bf16 in, fp32 in tensor
+ * memory); the low-rank expand is fused into its epilogue.  Results are
+ * deterministic: the same inputs give the same bits on every call. */
+MLORA_API mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W, int N,
+                          const mlora_bf16 *A_stack, const mlora_bf16 *B_stack, int n_adapters, int r_max,
+                          const int32_t *rank_of, const int32_t *adapter_idx, const int32_t *seg_offsets,
+                          float scale, mlora_mode mode, mlora_bf16 *y, void *workspace, size_t ws_bytes,
+                          mlora_stream stream);
+
+/* ------------------------------------------------------------------------- */
+/* Accept / resample (steps a5-a6)                                            */
+/* ------------------------------------------------------------------------- */
+
+/* Speculative verification that keeps the target distribution (InvisibleLoRA
+ * abstract: one LoRA-on pass verifies all proposals and preserves the output
+ * distribution).  Per request b, with p = target, q = draft probabilities:
+ *   1. keep draft x_i while (double)u_i * q_i(x_i) < p_i(x_i); n = first
+ *      failing position (k if none fails);
+ *   2. weights w(v) = max(0, Q(p_n(v)) - Q(q_n(v))) if n < k, else Q(p_k(v)),
+ *      Q(f) = floor(f * 2^40);
+ *   3. S = sum w, U = floor(u_k * 2^32), T = floor(U * S / 2^32); draw the
+ *      smallest v whose running sum of w exceeds T.
+ * Every decision is exact integer / exact float64 arithmetic, so results are
+ * bit-reproducible.
+ *
+ *   p_target  fp32 [B, k+1, V]     q_draft  fp32 [B, k, V]
+ *   draft_tok int32 [B, k]         uniforms fp32 [B, k+1] in [0, 1)
+ *   out_tok   int32 [B, k+1] out:  kept drafts, the drawn token, then -1
+ *   accepted  int32 [B] out:       n in [0, k]
+ * k in [1, 16], V in [1, 2^24].  Fallbacks: probability NaN/negative -> 0,
+ * above 1 -> 1 (MLORA_DEV_BAD_PROB); uniform NaN/negative -> 0, >= 1 -> the
+ * largest float below 1; a draft token outside [0, V) is rejected at its
+ * position (MLORA_DEV_BAD_TOKEN); zero residual mass draws from p_n, and zero
+ * mass there emits token 0 (MLORA_DEV_ZERO_MASS). */
+MLORA_API mlora_status mlora_verify_accept(const float *p_target, const float *q_draft, const int32_t *draft_tok,
+                                 const float *uniforms, int B, int k, int V, int32_t *out_tok, int32_t *accepted,
+                                 void *workspace, size_t ws_bytes, mlora_stream stream);
+
+/* ------------------------------------------------------------------------- */
+/* Misc                                                                       */
+/* ------------------------------------------------------------------------- */
+
+MLORA_API const char *mlora_status_string(mlora_status s);
+
+/* 1 if the current device can run the kernels (compute capability 10.3, the
+ * only target the library is built for), else 0. */
+MLORA_API int mlora_device_supported(void);
+
+/* Number of kernels this library launched since load (all entry points). */
+MLORA_API uint64_t mlora_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLORA_H */

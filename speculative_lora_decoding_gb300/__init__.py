@@ -1,0 +1,247 @@
+"""Multi-LoRA decode hot path for GB300 (sm_103a): Python binding.
+
+A thin ctypes binding of the C ABI declared in ``include/mlora.h``.  It only
+marshals torch tensors into pointers and sizes and passes the current CUDA
+stream; every step of the computation runs in the library's CUDA kernels.
+There is no CPU or PyTorch fallback: if ``libmlora.so`` is missing or the
+device is not compute capability 10.3, the calls raise.
+
+    linear(x, W, A_stack, B_stack, rank_of, adapter_idx, scale, mode)   steps a1-a4
+    verify_accept(p, q, draft_tok, uniforms)                             steps a5-a6
+    plan_segments(...), shrink(...)                                      steps a1, a2 alone
+
+The layer is y = W x (draft, LoRA off) or y = W x + scale * B_a (A_a x)
+(verify, LoRA on), per token row ("Multi-LoRA Serving in Practice", section
+"Core Principle: Shared Base Model, Per-Request Adapter Selection"; the modes
+are the InvisibleLoRA abstract's LoRA-off draft and LoRA-on verify passes).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+DRAFT = 0
+VERIFY = 1
+
+DEV_BAD_ADAPTER = 1 << 0
+DEV_BAD_RANK = 1 << 1
+DEV_BAD_PROB = 1 << 2
+DEV_BAD_TOKEN = 1 << 3
+DEV_ZERO_MASS = 1 << 4
+DEV_TIMEOUT = 1 << 5
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmlora.so")
+HEADER_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mlora.h")
+
+_c_size = ctypes.c_size_t
+_c_int = ctypes.c_int
+_c_ptr = ctypes.c_void_p
+_c_float = ctypes.c_float
+
+_SIGNATURES = {
+    "mlora_linear_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "mlora_accept_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "mlora_workspace_init": (_c_int, [_c_ptr, _c_size, _c_ptr]),
+    "mlora_read_device_status": (_c_int, [_c_ptr, ctypes.POINTER(ctypes.c_uint32), _c_int, _c_ptr]),
+    "mlora_plan_segments": (_c_int, [_c_ptr, _c_int, _c_ptr, _c_int, _c_int, _c_ptr, _c_size,
+                                     ctypes.POINTER(_c_ptr), ctypes.POINTER(_c_ptr), _c_ptr]),
+    "mlora_shrink": (_c_int, [_c_ptr, _c_int, _c_int, _c_ptr, _c_int, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_size,
+                              _c_ptr]),
+    "mlora_linear": (_c_int, [_c_ptr, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_ptr,
+                              _c_ptr, _c_ptr, _c_float, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "mlora_verify_accept": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr, _c_ptr,
+                                     _c_ptr, _c_size, _c_ptr]),
+    "mlora_status_string": (ctypes.c_char_p, [_c_int]),
+    "mlora_device_supported": (_c_int, []),
+    "mlora_launch_count": (ctypes.c_uint64, []),
+}
+
+_lib = None
+
+
+class MLoraError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _load().mlora_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+def header_symbols(path: str = HEADER_PATH) -> list:
+    """Names of the entry points include/mlora.h declares."""
+    text = open(path).read()
+    return re.findall(r"MLORA_API\s+[\w\s\*]*?\b(mlora_\w+)\s*\(", text)
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run __graft_entry__.build() (needs nvcc, targets sm_103a)")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def library():
+    """The loaded ctypes library (raises if it is not built)."""
+    return _load()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise MLoraError(status, where)
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype, dim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dimensions")
+    return t.data_ptr()
+
+
+def device_supported() -> bool:
+    return bool(_load().mlora_device_supported())
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process."""
+    return int(_load().mlora_launch_count())
+
+
+def linear_workspace_bytes(M: int, N: int, K: int, n_adapters: int) -> int:
+    return int(_load().mlora_linear_workspace_bytes(M, N, K, n_adapters))
+
+
+def accept_workspace_bytes(B: int, k: int, V: int) -> int:
+    return int(_load().mlora_accept_workspace_bytes(B, k, V))
+
+
+class Workspace:
+    """A device buffer for the library's scratch, status word and counters."""
+
+    def __init__(self, nbytes: int, device=None, stream=None):
+        if nbytes <= 0:
+            raise ValueError("workspace size must be positive (sizes outside the supported range give 0)")
+        self.nbytes = int(nbytes)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        _check(_load().mlora_workspace_init(self.buf.data_ptr(), self.nbytes, _stream(stream)), "workspace_init")
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def status(self, clear: bool = True, stream=None) -> int:
+        """Device status bits (synchronises the stream)."""
+        bits = ctypes.c_uint32(0)
+        st = _load().mlora_read_device_status(self.ptr, ctypes.byref(bits), 1 if clear else 0, _stream(stream))
+        if st not in (0, 5, 6):
+            raise MLoraError(st, "read_device_status")
+        return int(bits.value)
+
+    def view_int32(self, ptr: int, count: int) -> torch.Tensor:
+        """int32 view of `count` words of this workspace starting at device pointer `ptr`."""
+        off = int(ptr) - self.ptr
+        if off < 0 or off + 4 * count > self.nbytes or off % 4:
+            raise ValueError("pointer is not inside this workspace")
+        return self.buf[off:off + 4 * count].view(torch.int32)
+
+
+def plan_segments(adapter_idx: torch.Tensor, rank_of: torch.Tensor, n_adapters: int, r_max: int, ws: Workspace,
+                  stream=None):
+    """Step a1.  Returns (seg_offsets_ptr, perm_ptr): device pointers into `ws`."""
+    M = adapter_idx.numel()
+    seg = _c_ptr(0)
+    perm = _c_ptr(0)
+    st = _load().mlora_plan_segments(_need(adapter_idx, "adapter_idx", torch.int32, 1), M,
+                                     _need(rank_of, "rank_of", torch.int32, 1), n_adapters, r_max, ws.ptr, ws.nbytes,
+                                     ctypes.byref(seg), ctypes.byref(perm), _stream(stream))
+    _check(st, "plan_segments")
+    return seg.value, perm.value
+
+
+def shrink(x: torch.Tensor, A_stack: torch.Tensor, seg_offsets_ptr: int, ws: Workspace, T: torch.Tensor = None,
+           stream=None) -> torch.Tensor:
+    """Step a2: T[m, j] = A_a[j, :] . x[m, :] for j < rank, fp32 [M, r_max]."""
+    M, K = x.shape
+    n_ad, r_max, K2 = A_stack.shape
+    if K2 != K:
+        raise ValueError("A_stack and x disagree on K")
+    if T is None:
+        T = torch.empty((M, r_max), dtype=torch.float32, device=x.device)
+    st = _load().mlora_shrink(_need(x, "x", torch.bfloat16, 2), M, K, _need(A_stack, "A_stack", torch.bfloat16, 3),
+                              n_ad, r_max, seg_offsets_ptr, _need(T, "T", torch.float32, 2), ws.ptr, ws.nbytes,
+                              _stream(stream))
+    _check(st, "shrink")
+    return T
+
+
+def linear(x: torch.Tensor, W: torch.Tensor, A_stack, B_stack, rank_of, adapter_idx, scale: float, mode: int,
+           ws: Workspace = None, y: torch.Tensor = None, seg_offsets_ptr: int = None, stream=None) -> torch.Tensor:
+    """Steps a1-a4: y = W x (+ scale * B_a (A_a x) in verify mode), bf16 [M, N]."""
+    M, K = x.shape
+    N, K2 = W.shape
+    if K2 != K:
+        raise ValueError("W and x disagree on K")
+    verify = mode == VERIFY
+    n_ad, r_max = 0, 0
+    a_ptr = b_ptr = r_ptr = i_ptr = None
+    if verify:
+        n_ad, r_max, K3 = A_stack.shape
+        if K3 != K or tuple(B_stack.shape) != (n_ad, N, r_max):
+            raise ValueError("A_stack [n_ad, r_max, K] / B_stack [n_ad, N, r_max] shapes disagree")
+        a_ptr = _need(A_stack, "A_stack", torch.bfloat16, 3)
+        b_ptr = _need(B_stack, "B_stack", torch.bfloat16, 3)
+        r_ptr = _need(rank_of, "rank_of", torch.int32, 1)
+        i_ptr = _need(adapter_idx, "adapter_idx", torch.int32, 1)
+        if adapter_idx.numel() != M or rank_of.numel() != n_ad:
+            raise ValueError("adapter_idx must have M entries and rank_of n_adapters entries")
+    if ws is None:
+        ws = Workspace(linear_workspace_bytes(M, N, K, max(n_ad, 1)), device=x.device, stream=stream)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    st = _load().mlora_linear(_need(x, "x", torch.bfloat16, 2), M, K, _need(W, "W", torch.bfloat16, 2), N, a_ptr,
+                              b_ptr, n_ad, r_max, r_ptr, i_ptr, seg_offsets_ptr, float(scale), int(mode),
+                              _need(y, "y", torch.bfloat16, 2), ws.ptr, ws.nbytes, _stream(stream))
+    _check(st, "linear")
+    return y
+
+
+def verify_accept(p: torch.Tensor, q: torch.Tensor, draft_tok: torch.Tensor, uniforms: torch.Tensor,
+                  ws: Workspace = None, out_tok: torch.Tensor = None, accepted: torch.Tensor = None, stream=None):
+    """Steps a5-a6.  Returns (out_tok int32 [B, k+1], accepted int32 [B])."""
+    B, k1, V = p.shape
+    k = k1 - 1
+    if tuple(q.shape) != (B, k, V) or tuple(draft_tok.shape) != (B, k) or tuple(uniforms.shape) != (B, k1):
+        raise ValueError("p [B,k+1,V], q [B,k,V], draft_tok [B,k], uniforms [B,k+1] shapes disagree")
+    if ws is None:
+        ws = Workspace(accept_workspace_bytes(B, k, V), device=p.device, stream=stream)
+    if out_tok is None:
+        out_tok = torch.empty((B, k1), dtype=torch.int32, device=p.device)
+    if accepted is None:
+        accepted = torch.empty((B,), dtype=torch.int32, device=p.device)
+    st = _load().mlora_verify_accept(_need(p, "p", torch.float32, 3), _need(q, "q", torch.float32, 3),
+                                     _need(draft_tok, "draft_tok", torch.int32, 2),
+                                     _need(uniforms, "uniforms", torch.float32, 2), B, k, V,
+                                     _need(out_tok, "out_tok", torch.int32, 2),
+                                     _need(accepted, "accepted", torch.int32, 1), ws.ptr, ws.nbytes, _stream(stream))
+    _check(st, "verify_accept")
+    return out_tok, accepted

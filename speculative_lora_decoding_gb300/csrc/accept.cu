@@ -1,0 +1,334 @@
+// Steps a5 + a6: per-request accept test and residual / bonus draw.
+//
+// The InvisibleLoRA abstract has one LoRA-on pass verify all drafted tokens
+// while keeping the output distribution of plain multi-LoRA decoding.  The
+// rule used is standard speculative sampling (Leviathan et al. 2023; Chen et
+// al. 2023) with exact arithmetic, so that every decision is reproducible:
+//
+//   keep draft x_i while (double)u_i * q_i(x_i) < p_i(x_i)       -> n kept
+//   w(v) = max(0, Q(p_n(v)) - Q(q_n(v)))  if n < k   (residual)
+//   w(v) = Q(p_k(v))                      if n = k   (bonus)      Q(f) = floor(f * 2^40)
+//   token = smallest v with sum_{v' <= v} w(v') > floor(U * S / 2^32),
+//           S = sum_v w(v), U = floor(u_k * 2^32)
+//
+// Layout: each request's vocabulary row is cut into `slices` contiguous
+// slices, one CTA each, so a small batch still spreads over every SM.  A CTA
+// reads its slice once (coalesced 16-byte loads) and publishes two exact
+// uint64 sums (residual mass and target mass).  The last CTA of a request to
+// arrive (atomic counter, no spinning) adds the slice sums in order, picks
+// the slice holding the draw, re-reads only that slice and locates the token
+// with a block-wide prefix scan.  All sums are integers, so the order of
+// addition cannot change a result.
+#include "common.cuh"
+#include "launch.h"
+
+namespace mlora {
+
+constexpr int ACC_THREADS = 256;
+constexpr int ACC_WARPS = ACC_THREADS / 32;
+constexpr int MIN_SLICE = 4096;
+constexpr float TWO_POW_40 = 1099511627776.0f;
+constexpr float TWO_POW_32 = 4294967296.0f;
+
+__device__ __forceinline__ float sanitize_prob(float f, uint32_t &flags) {
+  if (!(f >= 0.f)) {  // NaN or negative
+    flags |= MLORA_DEV_BAD_PROB;
+    return 0.f;
+  }
+  if (f > 1.f) {
+    flags |= MLORA_DEV_BAD_PROB;
+    return 1.f;
+  }
+  return f;
+}
+
+__device__ __forceinline__ float sanitize_uniform(float u, uint32_t &flags) {
+  if (!(u >= 0.f)) {
+    flags |= MLORA_DEV_BAD_PROB;
+    return 0.f;
+  }
+  if (u >= 1.f) {
+    flags |= MLORA_DEV_BAD_PROB;
+    return __uint_as_float(0x3F7FFFFFu);  // largest float below 1
+  }
+  return u;
+}
+
+// Q(f) = floor(f * 2^40) for f in [0, 1]: the scaling is exact in fp32 and
+// the truncating conversion is the floor.
+__device__ __forceinline__ uint64_t fixq(float f) { return __float2ull_rz(f * TWO_POW_40); }
+
+struct Weights {
+  uint64_t res, tgt;
+};
+
+__device__ __forceinline__ Weights weight_of(float p, float q, bool residual, uint32_t &flags) {
+  Weights w;
+  const uint64_t qp = fixq(sanitize_prob(p, flags));
+  w.tgt = qp;
+  if (residual) {
+    const uint64_t qq = fixq(sanitize_prob(q, flags));
+    w.res = qp > qq ? qp - qq : 0ull;
+  } else {
+    w.res = 0ull;
+  }
+  return w;
+}
+
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ uint64_t warp_incl_scan_u64(uint64_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(ACC_THREADS)
+    accept_kernel(const float *__restrict__ p, const float *__restrict__ q, const int32_t *__restrict__ draft_tok,
+                  const float *__restrict__ uni, int B, int k, int V, int slices, int slice_len, int vec,
+                  int32_t *__restrict__ out_tok, int32_t *__restrict__ accepted, uint32_t *counters,
+                  uint64_t *slice_sums, uint32_t *status) {
+  __shared__ uint64_t sh_a[ACC_WARPS], sh_b[ACC_WARPS];
+  __shared__ int sh_n, sh_last, sh_tok;
+  __shared__ uint32_t sh_flags;
+  __shared__ uint64_t sh_T, sh_base;
+  __shared__ int sh_mode, sh_slice;
+
+  const int b = blockIdx.x / slices, g = blockIdx.x % slices;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k1 = k + 1;
+  uint32_t flags = 0;
+
+  // Step a5: accept tests (cheap gathers; every CTA of the request agrees).
+  if (tid == 0) {
+    sh_flags = 0;
+    int n = k;
+    for (int i = 0; i < k; ++i) {
+      const int x = draft_tok[(size_t)b * k + i];
+      if (x < 0 || x >= V) {
+        flags |= MLORA_DEV_BAD_TOKEN;
+        n = i;
+        break;
+      }
+      const float pi = sanitize_prob(p[((size_t)b * k1 + i) * V + x], flags);
+      const float qi = sanitize_prob(q[((size_t)b * k + i) * V + x], flags);
+      const float ui = sanitize_uniform(uni[(size_t)b * k1 + i], flags);
+      if (!((double)ui * (double)qi < (double)pi)) {
+        n = i;
+        break;
+      }
+    }
+    sh_n = n;
+  }
+  __syncthreads();
+  const int n = sh_n;
+  const bool residual = n < k;
+  const float *prow = p + ((size_t)b * k1 + n) * V;
+  const float *qrow = residual ? q + ((size_t)b * k + n) * V : prow;
+
+  // Step a6, pass 1: exact sums over this CTA's slice.
+  const int v0 = g * slice_len, v1 = min(V, v0 + slice_len);
+  uint64_t s_res = 0, s_tgt = 0;
+  if (vec) {
+    const float4 *p4 = reinterpret_cast<const float4 *>(prow);
+    const float4 *q4 = reinterpret_cast<const float4 *>(qrow);
+    const int e0 = v0 >> 2, e1 = v1 >> 2;  // v0, V multiples of 4 on this path
+    int e = e0 + tid;
+    for (; e + 3 * ACC_THREADS < e1; e += 4 * ACC_THREADS) {
+      float4 pv[4], qv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        pv[r] = __ldcs(p4 + e + r * ACC_THREADS);
+        if (residual) qv[r] = __ldcs(q4 + e + r * ACC_THREADS);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float pa[4] = {pv[r].x, pv[r].y, pv[r].z, pv[r].w};
+        const float qa[4] = {residual ? qv[r].x : 0.f, residual ? qv[r].y : 0.f, residual ? qv[r].z : 0.f,
+                             residual ? qv[r].w : 0.f};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const Weights w = weight_of(pa[t], qa[t], residual, flags);
+          s_res += w.res;
+          s_tgt += w.tgt;
+        }
+      }
+    }
+    for (; e < e1; e += ACC_THREADS) {
+      const float4 pv = __ldcs(p4 + e);
+      const float4 qv = residual ? __ldcs(q4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float pa[4] = {pv.x, pv.y, pv.z, pv.w};
+      const float qa[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const Weights w = weight_of(pa[t], qa[t], residual, flags);
+        s_res += w.res;
+        s_tgt += w.tgt;
+      }
+    }
+  } else {
+    for (int v = v0 + tid; v < v1; v += ACC_THREADS) {
+      const Weights w = weight_of(prow[v], residual ? qrow[v] : 0.f, residual, flags);
+      s_res += w.res;
+      s_tgt += w.tgt;
+    }
+  }
+  s_res = warp_sum_u64(s_res);
+  s_tgt = warp_sum_u64(s_tgt);
+  if (lane == 0) {
+    sh_a[warp] = s_res;
+    sh_b[warp] = s_tgt;
+  }
+  if (flags) atomicOr(&sh_flags, flags);
+  __syncthreads();
+  if (tid == 0) {
+    uint64_t a = 0, t = 0;
+    for (int w = 0; w < ACC_WARPS; ++w) {
+      a += sh_a[w];
+      t += sh_b[w];
+    }
+    slice_sums[((size_t)b * slices + g) * 2 + 0] = a;
+    slice_sums[((size_t)b * slices + g) * 2 + 1] = t;
+    __threadfence();
+    const uint32_t old = atomicAdd(&counters[b], 1u);
+    sh_last = (old == (uint32_t)(slices - 1));
+  }
+  __syncthreads();
+  if (!sh_last) {
+    if (tid == 0 && sh_flags) raise_status(status, sh_flags);
+    return;
+  }
+
+  // Last CTA of this request: choose the weights, the draw and its slice.
+  if (tid == 0) {
+    __threadfence();
+    counters[b] = 0u;
+    uint32_t f2 = sh_flags;
+    uint64_t S_res = 0, S_tgt = 0;
+    for (int s = 0; s < slices; ++s) {
+      S_res += __ldcg(&slice_sums[((size_t)b * slices + s) * 2 + 0]);
+      S_tgt += __ldcg(&slice_sums[((size_t)b * slices + s) * 2 + 1]);
+    }
+    int mode = residual ? 0 : 1;  // 0: residual weights, 1: target weights
+    if (residual && S_res == 0) {
+      f2 |= MLORA_DEV_ZERO_MASS;
+      mode = 1;
+    }
+    const uint64_t S = mode == 0 ? S_res : S_tgt;
+    const float uk = sanitize_uniform(uni[(size_t)b * k1 + k], f2);
+    int tok = -1;
+    if (S == 0) {
+      f2 |= MLORA_DEV_ZERO_MASS;
+      tok = 0;
+    } else {
+      const uint64_t U = __float2ull_rz(uk * TWO_POW_32);
+      const uint64_t lo = U * S, hi = __umul64hi(U, S);
+      const uint64_t T = (hi << 32) | (lo >> 32);  // floor(U * S / 2^32)
+      uint64_t run = 0;
+      int sl = slices - 1;
+      for (int s = 0; s < slices; ++s) {
+        const uint64_t w = __ldcg(&slice_sums[((size_t)b * slices + s) * 2 + mode]);
+        if (run + w > T) {
+          sl = s;
+          break;
+        }
+        run += w;
+      }
+      sh_T = T - run;
+      sh_slice = sl;
+    }
+    sh_tok = tok;
+    sh_mode = mode;
+    sh_base = 0;
+    if (f2) raise_status(status, f2);
+  }
+  __syncthreads();
+
+  if (sh_tok < 0) {
+    // Pass 2: prefix scan over the chosen slice, 4 elements per thread per round.
+    const int mode = sh_mode;
+    const uint64_t T = sh_T;
+    const int w0 = sh_slice * slice_len, w1 = min(V, w0 + slice_len);
+    for (int base = w0; base < w1; base += 4 * ACC_THREADS) {
+      uint64_t w[4];
+      uint64_t mine = 0;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int v = base + tid * 4 + t;
+        uint32_t dummy = 0;
+        w[t] = 0;
+        if (v < w1) {
+          const Weights ww = weight_of(prow[v], residual ? qrow[v] : 0.f, mode == 0, dummy);
+          w[t] = mode == 0 ? ww.res : ww.tgt;
+        }
+        mine += w[t];
+      }
+      const uint64_t inc = warp_incl_scan_u64(mine);
+      if (lane == 31) sh_a[warp] = inc;
+      __syncthreads();
+      uint64_t before = sh_base;
+      for (int ww = 0; ww < warp; ++ww) before += sh_a[ww];
+      uint64_t run = before + inc - mine;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (run <= T && T < run + w[t]) sh_tok = base + tid * 4 + t;
+        run += w[t];
+      }
+      __syncthreads();
+      if (sh_tok >= 0) break;
+      if (tid == ACC_THREADS - 1) sh_base = run;
+      __syncthreads();
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int tok = sh_tok;
+    if (tok < 0) tok = 0;  // unreachable when the sums are consistent
+    for (int i = 0; i < k1; ++i) {
+      int v = -1;
+      if (i < n) v = draft_tok[(size_t)b * k + i];
+      else if (i == n) v = tok;
+      out_tok[(size_t)b * k1 + i] = v;
+    }
+    accepted[b] = n;
+  }
+}
+
+AcceptShape accept_shape(int B, int k, int V, int num_sms) {
+  (void)k;
+  AcceptShape s;
+  int want = (2 * num_sms + B - 1) / B;
+  const int max_slices = (V + MIN_SLICE - 1) / MIN_SLICE;
+  if (want > max_slices) want = max_slices;
+  if (want < 1) want = 1;
+  int len = (V + want - 1) / want;
+  len = (len + 3) / 4 * 4;
+  s.slice_len = len;
+  s.slices = (V + len - 1) / len;
+  s.threads = ACC_THREADS;
+  s.scratch_bytes = (size_t)B * s.slices * 2 * sizeof(uint64_t);
+  return s;
+}
+
+cudaError_t launch_accept(const float *p, const float *q, const int32_t *draft_tok, const float *u, int B, int k, int V,
+                          int32_t *out_tok, int32_t *accepted, uint32_t *counters, void *scratch, uint32_t *status,
+                          const AcceptShape &sh, cudaStream_t s) {
+  const int vec = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(p) & 15) == 0) &&
+                  ((reinterpret_cast<uintptr_t>(q) & 15) == 0);
+  const long long grid = (long long)B * sh.slices;
+  accept_kernel<<<(unsigned)grid, ACC_THREADS, 0, s>>>(p, q, draft_tok, u, B, k, V, sh.slices, sh.slice_len, vec,
+                                                       out_tok, accepted, counters,
+                                                       reinterpret_cast<uint64_t *>(scratch), status);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace mlora

@@ -1,0 +1,229 @@
+// C-ABI front end: argument checks, workspace layout and kernel launches.
+// Nothing here computes a result; every step runs in the CUDA kernels.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace mlora {
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct LinearLayout {
+  size_t plan, T, partials, total;
+};
+
+static LinearLayout linear_layout(int M, int N, int K, int n_ad, int sms) {
+  LinearLayout L;
+  const PlanLayout P = plan_layout(M, n_ad);
+  size_t o = WS_SCRATCH_OFF;
+  L.plan = o;
+  o = align_up(o + P.words * 4, 256);
+  L.T = o;
+  o = align_up(o + (size_t)M * T_STRIDE * 4, 256);
+  L.partials = o;
+  const GemmShape sh = gemm_shape(M, N, K, sms);
+  o = align_up(o + sh.partial_floats * 4, 256);
+  L.total = o;
+  return L;
+}
+
+static bool linear_sizes_ok(int M, int N, int K, int n_ad) {
+  if (M < 1 || M > MLORA_MAX_ROWS || N < 1 || K < 8 || (K % 8) != 0) return false;
+  if (n_ad < 0 || n_ad > MLORA_MAX_ADAPTERS) return false;
+  if ((long long)((N + 127) / 128) * ((M + 511) / 512) * 4 > (long long)WS_MAX_COUNTERS) return false;
+  return true;
+}
+
+static mlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLORA_OK : MLORA_ERR_CUDA; }
+
+}  // namespace mlora
+
+using namespace mlora;
+
+extern "C" {
+
+size_t mlora_linear_workspace_bytes(int M, int N, int K, int n_adapters) {
+  if (!linear_sizes_ok(M, N, K, n_adapters)) return 0;
+  int sms = device_sms();
+  if (sms <= 0) sms = 160;
+  return linear_layout(M, N, K, n_adapters, sms).total;
+}
+
+size_t mlora_accept_workspace_bytes(int B, int k, int V) {
+  if (B < 1 || B > (int)WS_MAX_COUNTERS || k < 1 || k > 16 || V < 1 || V > MLORA_MAX_VOCAB) return 0;
+  int sms = device_sms();
+  if (sms <= 0) sms = 160;
+  return align_up(WS_SCRATCH_OFF + accept_shape(B, k, V, sms).scratch_bytes, 256);
+}
+
+mlora_status mlora_workspace_init(void *workspace, size_t ws_bytes, mlora_stream stream) {
+  if (!workspace) return MLORA_ERR_WORKSPACE;
+  if (ws_bytes < WS_INIT_BYTES || !aligned(workspace, 256)) return MLORA_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(workspace, 0, WS_INIT_BYTES, (cudaStream_t)stream));
+}
+
+mlora_status mlora_read_device_status(void *workspace, uint32_t *bits, int clear, mlora_stream stream) {
+  if (!workspace || !bits) return MLORA_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, (uint8_t *)workspace + WS_STATUS_OFF, 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync((uint8_t *)workspace + WS_STATUS_OFF, 0, 4, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return MLORA_ERR_CUDA;
+  *bits = v;
+  if (v & MLORA_DEV_TIMEOUT) return MLORA_ERR_TIMEOUT;
+  return v ? MLORA_ERR_DEVICE_STATUS : MLORA_OK;
+}
+
+mlora_status mlora_plan_segments(const int32_t *adapter_idx, int M, const int32_t *rank_of, int n_adapters,
+                                 int r_max, void *workspace, size_t ws_bytes, const int32_t **seg_offsets,
+                                 const int32_t **perm, mlora_stream stream) {
+  if (!adapter_idx || !rank_of) return MLORA_ERR_ARG;
+  if (M < 1 || M > MLORA_MAX_ROWS || n_adapters < 1 || n_adapters > MLORA_MAX_ADAPTERS) return MLORA_ERR_SHAPE;
+  if (r_max < 8 || r_max > MLORA_MAX_RANK || (r_max % 8) != 0) return MLORA_ERR_SHAPE;
+  if (!workspace || !aligned(workspace, 256)) return MLORA_ERR_WORKSPACE;
+  const PlanLayout P = plan_layout(M, n_adapters);
+  if (ws_bytes < WS_SCRATCH_OFF + P.words * 4) return MLORA_ERR_WORKSPACE;
+  int32_t *plan = reinterpret_cast<int32_t *>((uint8_t *)workspace + WS_SCRATCH_OFF);
+  uint32_t *status = reinterpret_cast<uint32_t *>((uint8_t *)workspace + WS_STATUS_OFF);
+  cudaError_t e = launch_plan(adapter_idx, M, rank_of, n_adapters, r_max, plan, status, (cudaStream_t)stream);
+  if (e != cudaSuccess) return MLORA_ERR_CUDA;
+  if (seg_offsets) *seg_offsets = plan + P.seg_offsets;
+  if (perm) *perm = plan + P.perm;
+  return MLORA_OK;
+}
+
+mlora_status mlora_shrink(const mlora_bf16 *x, int M, int K, const mlora_bf16 *A_stack, int n_adapters, int r_max,
+                          const int32_t *seg_offsets, float *T, void *workspace, size_t ws_bytes,
+                          mlora_stream stream) {
+  if (!x || !A_stack || !T || !seg_offsets) return MLORA_ERR_ARG;
+  if (M < 1 || M > MLORA_MAX_ROWS || K < 8 || (K % 8) != 0 || n_adapters < 1 || n_adapters > MLORA_MAX_ADAPTERS)
+    return MLORA_ERR_SHAPE;
+  if (r_max < 8 || r_max > MLORA_MAX_RANK || (r_max % 8) != 0) return MLORA_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(A_stack, 16)) return MLORA_ERR_ARG;
+  if (!workspace || !aligned(workspace, 256)) return MLORA_ERR_WORKSPACE;
+  const PlanLayout P = plan_layout(M, n_adapters);
+  if (ws_bytes < WS_SCRATCH_OFF + P.words * 4) return MLORA_ERR_WORKSPACE;
+  int32_t *plan = reinterpret_cast<int32_t *>((uint8_t *)workspace + WS_SCRATCH_OFF);
+  if (seg_offsets != plan + P.seg_offsets) return MLORA_ERR_ARG;
+  const int sms = device_sms();
+  if (sms <= 0) return MLORA_ERR_CUDA;
+  cudaError_t e = launch_shrink(x, M, K, A_stack, n_adapters, r_max, plan, T, r_max, true, sms, (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W, int N, const mlora_bf16 *A_stack,
+                          const mlora_bf16 *B_stack, int n_adapters, int r_max, const int32_t *rank_of,
+                          const int32_t *adapter_idx, const int32_t *seg_offsets, float scale, mlora_mode mode,
+                          mlora_bf16 *y, void *workspace, size_t ws_bytes, mlora_stream stream) {
+  if (!x || !W || !y) return MLORA_ERR_ARG;
+  if (mode != MLORA_DRAFT && mode != MLORA_VERIFY) return MLORA_ERR_ARG;
+  const bool verify = mode == MLORA_VERIFY;
+  if (verify && (!A_stack || !B_stack || !rank_of || !adapter_idx)) return MLORA_ERR_ARG;
+  if (!linear_sizes_ok(M, N, K, verify ? n_adapters : 0)) return MLORA_ERR_SHAPE;
+  if (verify && (n_adapters < 1 || r_max < 8 || r_max > MLORA_MAX_RANK || (r_max % 8) != 0)) return MLORA_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(W, 16)) return MLORA_ERR_ARG;
+  if (verify && (!aligned(A_stack, 16) || !aligned(B_stack, 16))) return MLORA_ERR_ARG;
+  if (!workspace || !aligned(workspace, 256)) return MLORA_ERR_WORKSPACE;
+  const int sms = device_sms();
+  if (sms <= 0) return MLORA_ERR_CUDA;
+  const int n_ad = verify ? n_adapters : 0;
+  const LinearLayout L = linear_layout(M, N, K, n_ad, sms);
+  if (ws_bytes < L.total) return MLORA_ERR_WORKSPACE;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t *ws = (uint8_t *)workspace;
+  uint32_t *status = reinterpret_cast<uint32_t *>(ws + WS_STATUS_OFF);
+  uint32_t *counters = reinterpret_cast<uint32_t *>(ws + WS_COUNTERS_OFF);
+  int32_t *plan = reinterpret_cast<int32_t *>(ws + L.plan);
+  float *T = reinterpret_cast<float *>(ws + L.T);
+  cudaError_t e;
+  if (verify) {
+    const PlanLayout P = plan_layout(M, n_ad);
+    if (seg_offsets == nullptr) {
+      e = launch_plan(adapter_idx, M, rank_of, n_ad, r_max, plan, status, s);
+      if (e != cudaSuccess) return MLORA_ERR_CUDA;
+    } else if (seg_offsets != plan + P.seg_offsets) {
+      return MLORA_ERR_ARG;
+    }
+    e = launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, s);
+    if (e != cudaSuccess) return MLORA_ERR_CUDA;
+  }
+  const GemmShape sh = gemm_shape(M, N, K, sms);
+  GemmLaunch g;
+  g.x = x;
+  g.W = W;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.mode = mode;
+  g.scale = scale;
+  g.y = y;
+  g.B_stack = B_stack;
+  g.r_max = r_max;
+  g.n_ad = n_ad;
+  g.T = T;
+  g.plan = plan;
+  g.partials = reinterpret_cast<float *>(ws + L.partials);
+  g.counters = counters;
+  g.status = status;
+  int err = 0;
+  e = launch_gemm(g, sh, s, &err);
+  if (err) return MLORA_ERR_ARG;
+  return cuda_status(e);
+}
+
+mlora_status mlora_verify_accept(const float *p_target, const float *q_draft, const int32_t *draft_tok,
+                                 const float *uniforms, int B, int k, int V, int32_t *out_tok, int32_t *accepted,
+                                 void *workspace, size_t ws_bytes, mlora_stream stream) {
+  if (!p_target || !q_draft || !draft_tok || !uniforms || !out_tok || !accepted) return MLORA_ERR_ARG;
+  if (B < 1 || B > (int)WS_MAX_COUNTERS || k < 1 || k > 16 || V < 1 || V > MLORA_MAX_VOCAB) return MLORA_ERR_SHAPE;
+  if (!workspace || !aligned(workspace, 256)) return MLORA_ERR_WORKSPACE;
+  const int sms = device_sms();
+  if (sms <= 0) return MLORA_ERR_CUDA;
+  const AcceptShape sh = accept_shape(B, k, V, sms);
+  if (ws_bytes < WS_SCRATCH_OFF + sh.scratch_bytes) return MLORA_ERR_WORKSPACE;
+  uint8_t *ws = (uint8_t *)workspace;
+  cudaError_t e = launch_accept(p_target, q_draft, draft_tok, uniforms, B, k, V, out_tok, accepted,
+                                reinterpret_cast<uint32_t *>(ws + WS_COUNTERS_OFF), ws + WS_SCRATCH_OFF,
+                                reinterpret_cast<uint32_t *>(ws + WS_STATUS_OFF), sh, (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+const char *mlora_status_string(mlora_status s) {
+  switch (s) {
+    case MLORA_OK: return "ok";
+    case MLORA_ERR_ARG: return "invalid argument (null pointer, bad mode or misaligned pointer)";
+    case MLORA_ERR_SHAPE: return "size outside the supported range";
+    case MLORA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case MLORA_ERR_CUDA: return "CUDA call failed";
+    case MLORA_ERR_DEVICE_STATUS: return "device raised status bits (bad input rows were handled by the fallback)";
+    case MLORA_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
+    case MLORA_ERR_UNSUPPORTED: return "device is not supported (needs sm_103)";
+  }
+  return "unknown status";
+}
+
+int mlora_device_supported(void) {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return 0;
+  return (major == 10 && minor == 3) ? 1 : 0;
+}
+
+uint64_t mlora_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

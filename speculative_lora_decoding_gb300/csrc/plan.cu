@@ -1,0 +1,177 @@
+// Step a1, the segment plan: a stable counting sort of token rows by adapter.
+//
+// The InvisibleLoRA abstract observes that requests are partitioned across the
+// active adapters, and "Multi-LoRA Serving in Practice" (section "4. Batching:
+// Heterogeneous LoRAs Break 'Neat' Batches") asks to aggregate requests of one
+// adapter.  The plan gives, per adapter, the sorted positions of its rows; the
+// shrink kernel reads each adapter's A once per group and the GEMM epilogue
+// keeps each adapter's B row in registers across its group.
+//
+// One CTA of 1024 threads: histogram in shared memory, block-wide scans for
+// the offsets, the active-adapter list and the shrink work list, then a
+// warp-sequential ranking (match_any within a warp, warps in order) that
+// keeps rows of one bucket in increasing row order.
+#include "common.cuh"
+#include "launch.h"
+
+namespace mlora {
+
+constexpr int PLAN_THREADS = 1024;
+
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// Exclusive scan over the block; every thread calls it.  sh: 33 ints.
+__device__ int block_excl_scan(int v, int *sh, int *total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int inc = warp_incl_scan(v);
+  if (lane == 31) sh[w] = inc;
+  __syncthreads();
+  if (w == 0) {
+    const int s = (lane < (int)(blockDim.x >> 5)) ? sh[lane] : 0;
+    const int si = warp_incl_scan(s);
+    sh[lane] = si - s;
+    if (lane == 31) sh[32] = si;
+  }
+  __syncthreads();
+  const int res = sh[w] + inc - v;
+  *total = sh[32];
+  __syncthreads();
+  return res;
+}
+
+__device__ __forceinline__ int bucket_of(int a, int n_ad) { return (a >= 0 && a < n_ad) ? a : n_ad; }
+
+__global__ void __launch_bounds__(PLAN_THREADS, 1)
+    plan_kernel(const int32_t *__restrict__ adapter_idx, int M, const int32_t *__restrict__ rank_of, int n_ad,
+                int r_max, int32_t *__restrict__ plan, uint32_t *status) {
+  extern __shared__ int sh_dyn[];
+  int *cnt = sh_dyn;                 // [n_ad + 1]: counts, then bucket offsets
+  int *running = sh_dyn + n_ad + 1;  // [n_ad + 1]
+  __shared__ int scan_sh[33];
+  __shared__ uint32_t flags;
+
+  const PlanLayout L = plan_layout(M, n_ad);
+  const int tid = threadIdx.x;
+  const int nb = n_ad + 1;
+  if (tid == 0) flags = 0;
+  for (int b = tid; b < nb; b += PLAN_THREADS) {
+    cnt[b] = 0;
+    running[b] = 0;
+  }
+  __syncthreads();
+
+  // Validated ranks.
+  for (int a = tid; a < n_ad; a += PLAN_THREADS) {
+    int r = rank_of[a];
+    if (r < 0 || r > r_max) {
+      atomicOr(&flags, MLORA_DEV_BAD_RANK);
+      r = 0;
+    }
+    plan[L.rank_eff + a] = r;
+  }
+  // Histogram and validated adapter per row.
+  for (int m = tid; m < M; m += PLAN_THREADS) {
+    const int a = adapter_idx[m];
+    if (a < -1 || a >= n_ad) atomicOr(&flags, MLORA_DEV_BAD_ADAPTER);
+    const int b = bucket_of(a, n_ad);
+    plan[L.row_adapter + m] = (b < n_ad) ? b : -1;
+    atomicAdd(&cnt[b], 1);
+  }
+  __syncthreads();
+
+  // Bucket offsets: exclusive scan of counts, each thread owning a contiguous run.
+  const int per = (nb + PLAN_THREADS - 1) / PLAN_THREADS;
+  const int b0 = min(tid * per, nb), b1 = min(b0 + per, nb);
+  {
+    int local = 0;
+    for (int b = b0; b < b1; ++b) local += cnt[b];
+    int total;
+    int off = block_excl_scan(local, scan_sh, &total);
+    for (int b = b0; b < b1; ++b) {
+      const int c = cnt[b];
+      plan[L.seg_offsets + b] = off;
+      running[b] = c;  // keep the count; `cnt` turns into offsets below
+      cnt[b] = off;
+      off += c;
+    }
+    if (tid == 0) plan[L.seg_offsets + nb] = total;
+  }
+  __syncthreads();
+
+  // Active adapters (rows > 0) and the shrink work list over them.
+  {
+    const int a0 = min(tid * per, n_ad), a1 = min(a0 + per, n_ad);
+    int nact = 0, nitems = 0;
+    for (int a = a0; a < a1; ++a) {
+      const int c = running[a];
+      if (c > 0) {
+        ++nact;
+        const int r = plan[L.rank_eff + a];
+        nitems += ((r + SHRINK_J - 1) / SHRINK_J) * ((c + SHRINK_TOK - 1) / SHRINK_TOK);
+      }
+    }
+    int tot_act, tot_items;
+    int pa = block_excl_scan(nact, scan_sh, &tot_act);
+    int pi = block_excl_scan(nitems, scan_sh, &tot_items);
+    for (int a = a0; a < a1; ++a) {
+      const int c = running[a];
+      if (c > 0) {
+        const int r = plan[L.rank_eff + a];
+        plan[L.active + pa] = a;
+        plan[L.item_off + pa] = pi;
+        ++pa;
+        pi += ((r + SHRINK_J - 1) / SHRINK_J) * ((c + SHRINK_TOK - 1) / SHRINK_TOK);
+      }
+    }
+    if (tid == 0) {
+      plan[L.item_off + tot_act] = tot_items;
+      plan[L.hdr + 0] = tot_act;
+      plan[L.hdr + 1] = tot_items;
+      plan[L.hdr + 2] = M;
+    }
+  }
+  __syncthreads();
+  for (int b = tid; b < nb; b += PLAN_THREADS) running[b] = 0;
+  __syncthreads();
+
+  // Stable ranks: rows in chunks of 1024; within a warp lanes with the same
+  // bucket are ranked by lane order, warps take their turn in order.
+  const int lane = tid & 31, warp = tid >> 5;
+  for (int base = 0; base < M; base += PLAN_THREADS) {
+    const int m = base + tid;
+    const int b = (m < M) ? bucket_of(adapter_idx[m], n_ad) : -1 - lane - 2 * PLAN_THREADS;
+    const unsigned mask = __match_any_sync(0xffffffffu, b);
+    const int leader = __ffs(mask) - 1;
+    const int rank_in_warp = __popc(mask & ((1u << lane) - 1u));
+    int basev = 0;
+    for (int w = 0; w < PLAN_THREADS / 32; ++w) {
+      if (warp == w && m < M && lane == leader) {
+        basev = running[b];
+        running[b] = basev + __popc(mask);
+      }
+      __syncthreads();
+    }
+    basev = __shfl_sync(0xffffffffu, basev, leader);
+    if (m < M) plan[L.perm + cnt[b] + basev + rank_in_warp] = m;
+  }
+  __syncthreads();
+  if (tid == 0 && flags) raise_status(status, flags);
+}
+
+cudaError_t launch_plan(const int32_t *adapter_idx, int M, const int32_t *rank_of, int n_ad, int r_max,
+                        int32_t *plan, uint32_t *status, cudaStream_t s) {
+  const size_t smem = 2 * (size_t)(n_ad + 1) * sizeof(int);  // <= 32.8 KB for n_ad <= 4096
+  plan_kernel<<<1, PLAN_THREADS, smem, s>>>(adapter_idx, M, rank_of, n_ad, r_max, plan, status);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace mlora

@@ -1,0 +1,54 @@
+"""The C-ABI library loads and exports every entry point the header declares.
+No compute call is made here (this runs without a GPU)."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import speculative_lora_decoding_gb300 as ml
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(ml.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return ml.library()
+
+
+def test_header_declares_the_boundary():
+    names = set(ml.header_symbols())
+    for n in ("mlora_linear", "mlora_verify_accept", "mlora_plan_segments", "mlora_shrink",
+              "mlora_linear_workspace_bytes", "mlora_accept_workspace_bytes", "mlora_workspace_init",
+              "mlora_read_device_status", "mlora_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", ml.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in ml.header_symbols():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings_and_host_checks(lib):
+    for s in range(8):
+        assert lib.mlora_status_string(s)
+    # null pointers are rejected before any CUDA call
+    assert lib.mlora_linear(None, 4, 8, None, 8, None, None, 0, 0, None, None, None, 1.0, 0, None, None, 0, None) == 1
+    assert lib.mlora_verify_accept(None, None, None, None, 1, 1, 4, None, None, None, 0, None) == 1
+    # bad mode
+    p = ctypes.c_void_p(16)
+    assert lib.mlora_linear(p, 4, 8, p, 8, None, None, 0, 0, None, None, None, 1.0, 7, p, p, 1 << 20, None) == 1
+
+
+def test_workspace_sizes(lib):
+    a = lib.mlora_linear_workspace_bytes(128, 4096, 4096, 16)
+    b = lib.mlora_linear_workspace_bytes(512, 14336, 4096, 128)
+    assert 0 < a < b
+    assert lib.mlora_linear_workspace_bytes(128, 4096, 4097, 16) == 0      # K % 8 != 0
+    assert lib.mlora_linear_workspace_bytes(0, 4096, 4096, 16) == 0
+    assert lib.mlora_accept_workspace_bytes(256, 4, 128256) > 0
+    assert lib.mlora_accept_workspace_bytes(256, 0, 128256) == 0

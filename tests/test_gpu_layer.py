@@ -1,0 +1,227 @@
+"""GPU parity of the multi-LoRA layer (steps a1-a4) against the float64 oracle.
+
+Tolerance: max |y - y_ref| <= 1e-2 * max |y_ref| per call (bf16 inputs, fp32
+accumulation, one bf16 rounding of the output).  Integer work (the plan) and
+the small-integer case are compared bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as WL
+from oracle import layer as OL
+from tests.gpu_util import dev, dev_bf16, host_bf16_to_f64, needs_gpu
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+def _rel_err(y, y_ref):
+    return float(np.max(np.abs(y - y_ref)) / max(np.max(np.abs(y_ref)), 1e-30))
+
+
+def _random_case(seed, M, N, K, n_ad, ranks, r_max, nan_pad=True, frac_none=0.1):
+    g = np.random.default_rng(seed)
+    x = WL.bf16_bits(g.standard_normal((M, K)).astype(np.float32))
+    W = WL.bf16_bits((g.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32))
+    A = np.full((n_ad, r_max, K), 0x7FC0 if nan_pad else 0, np.uint16)
+    B = np.full((n_ad, N, r_max), 0x7FC0 if nan_pad else 0, np.uint16)
+    for a, r in enumerate(ranks):
+        A[a, :r] = WL.bf16_bits((g.standard_normal((r, K)) / np.sqrt(K)).astype(np.float32))
+        B[a, :, :r] = WL.bf16_bits((g.standard_normal((N, r)) / np.sqrt(max(r, 1))).astype(np.float32))
+    idx = g.integers(0, n_ad, M).astype(np.int32)
+    idx[g.random(M) < frac_none] = -1
+    return x, W, A, B, np.asarray(ranks, np.int32), idx
+
+
+def _oracle(x, W, A, B, ranks, idx, scale, mode):
+    f = WL.bf16_to_f64
+    return OL.mlora_linear(f(x), f(W), f(A), f(B), ranks, idx, scale, mode)
+
+
+def _run(ml, x, W, A, B, ranks, idx, scale, mode, ws=None):
+    return ml.linear(dev_bf16(x), dev_bf16(W), dev_bf16(A), dev_bf16(B), dev(ranks), dev(idx), scale, mode, ws=ws)
+
+
+def test_exact_small_integers_bitwise():
+    ml = needs_gpu()
+    g = np.random.default_rng(13)
+    for (M, K, N, r) in [(5, 8, 8, 2), (19, 16, 24, 2), (33, 72, 130, 1)]:
+        n_ad, r_max = 3, 8
+        x = g.integers(-2, 3, (M, K)).astype(np.float32)
+        W = g.integers(-2, 3, (N, K)).astype(np.float32)
+        A = np.zeros((n_ad, r_max, K), np.float32)
+        B = np.zeros((n_ad, N, r_max), np.float32)
+        A[:, :r] = g.integers(-1, 2, (n_ad, r, K))
+        B[:, :, :r] = g.integers(-1, 2, (n_ad, N, r))
+        idx = g.integers(-1, n_ad, M).astype(np.int32)
+        ranks = np.full(n_ad, r, np.int32)
+        xb, Wb, Ab, Bb = (WL.bf16_bits(v) for v in (x, W, A, B))
+        for mode in (OL.DRAFT, OL.VERIFY):
+            y_ref, _ = _oracle(xb, Wb, Ab, Bb, ranks, idx, 2.0, mode)
+            if np.abs(y_ref).max() > 256:
+                continue
+            y = host_bf16_to_f64(_run(ml, xb, Wb, Ab, Bb, ranks, idx, 2.0, mode))
+            assert np.array_equal(y, y_ref), (M, K, N, mode)
+
+
+def test_tiny_workload_both_modes():
+    ml = needs_gpu()
+    cfg = WL.TINY
+    W, A, B, ranks = WL.projection_weights(cfg, 0)
+    for mode, name in ((OL.DRAFT, "draft"), (OL.VERIFY, "verify")):
+        x = WL.activations(cfg, 0, name)
+        idx = WL.row_adapters(cfg, name)
+        y_ref, _ = _oracle(x, W, A, B, ranks, idx, cfg.scale, mode)
+        y = host_bf16_to_f64(_run(ml, x, W, A, B, ranks, idx, cfg.scale, mode))
+        assert _rel_err(y, y_ref) <= TOL
+
+
+@pytest.mark.parametrize("M,N,K,n_ad,ranks", [
+    (1, 8, 8, 1, (8,)),
+    (5, 130, 72, 3, (8, 0, 16)),
+    (17, 200, 200, 4, (8, 16, 24, 64)),
+    (100, 1000, 520, 8, (8, 16, 32, 64, 8, 16, 32, 64)),
+    (257, 384, 1024, 5, (64, 8, 33, 17, 1)),
+    (513, 256, 256, 6, (16,) * 6),
+    (640, 1024, 384, 64, tuple([8, 16, 32, 64] * 16)),
+    (700, 136, 128, 3, (8, 8, 8)),
+])
+def test_ragged_shapes_against_oracle(M, N, K, n_ad, ranks):
+    ml = needs_gpu()
+    x, W, A, B, rk, idx = _random_case(M * 7 + N, M, N, K, n_ad, ranks, r_max=64)
+    for mode in (OL.DRAFT, OL.VERIFY):
+        y_ref, _ = _oracle(x, W, A, B, rk, idx, 2.0, mode)
+        ws = ml.Workspace(ml.linear_workspace_bytes(M, N, K, n_ad))
+        y = _run(ml, x, W, A, B, rk, idx, 2.0, mode, ws=ws)
+        assert ws.status() == 0
+        assert _rel_err(host_bf16_to_f64(y), y_ref) <= TOL, (M, N, K, mode)
+
+
+def test_plan_is_bit_exact():
+    ml = needs_gpu()
+    g = np.random.default_rng(2)
+    for M, n_ad in [(1, 1), (16, 4), (128, 16), (512, 128), (640, 64), (3000, 4096), (5, 3)]:
+        idx = g.integers(-1, n_ad, M).astype(np.int32)
+        ranks = g.choice([0, 8, 16, 32, 64], n_ad).astype(np.int32)
+        seg_ref, perm_ref, _ = OL.plan_segments(idx, n_ad)
+        ws = ml.Workspace(ml.linear_workspace_bytes(M, 128, 64, n_ad))
+        seg_p, perm_p = ml.plan_segments(dev(idx), dev(ranks), n_ad, 64, ws)
+        seg = ws.view_int32(seg_p, n_ad + 2).cpu().numpy()
+        perm = ws.view_int32(perm_p, M).cpu().numpy()
+        assert np.array_equal(seg, seg_ref) and np.array_equal(perm, perm_ref), (M, n_ad)
+        assert ws.status() == 0
+
+
+def test_shrink_against_oracle():
+    ml = needs_gpu()
+    for (M, K, n_ad, ranks) in [(16, 512, 4, (8, 8, 8, 8)), (512, 4096, 8, (8, 16, 32, 64, 1, 9, 63, 0)),
+                                (37, 14336, 3, (16, 16, 16))]:
+        x, W, A, B, rk, idx = _random_case(K + M, M, 8, K, n_ad, ranks, r_max=64)
+        T_ref, _ = OL.shrink(WL.bf16_to_f64(x), WL.bf16_to_f64(A), rk, idx)
+        ws = ml.Workspace(ml.linear_workspace_bytes(M, 8, K, n_ad))
+        seg_p, _ = ml.plan_segments(dev(idx), dev(rk), n_ad, 64, ws)
+        T = ml.shrink(dev_bf16(x), dev_bf16(A), seg_p, ws).cpu().numpy().astype(np.float64)
+        assert np.isfinite(T).all()
+        assert np.max(np.abs(T - T_ref)) <= 1e-4 * max(np.max(np.abs(T_ref)), 1e-30)
+
+
+def test_zero_B_verify_equals_draft_bitwise():
+    ml = needs_gpu()
+    x, W, A, B, rk, idx = _random_case(5, 128, 1024, 4096, 16, (16,) * 16, r_max=16, nan_pad=False)
+    B[:] = 0
+    yv = _run(ml, x, W, A, B, rk, idx, 2.0, OL.VERIFY)
+    yd = _run(ml, x, W, A, B, rk, idx, 2.0, OL.DRAFT)
+    assert torch.equal(yv.view(torch.int16), yd.view(torch.int16))
+
+
+def test_row_permutation_and_determinism():
+    ml = needs_gpu()
+    x, W, A, B, rk, idx = _random_case(6, 96, 640, 1536, 8, (8, 16, 32, 64) * 2, r_max=64)
+    y1 = _run(ml, x, W, A, B, rk, idx, 2.0, OL.VERIFY)
+    y2 = _run(ml, x, W, A, B, rk, idx, 2.0, OL.VERIFY)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    perm = np.random.default_rng(1).permutation(96)
+    yp = _run(ml, x[perm], W, A, B, rk, idx[perm], 2.0, OL.VERIFY)
+    assert torch.equal(yp.view(torch.int16), y1[torch.from_numpy(perm).cuda()].view(torch.int16))
+
+
+def test_adapter_relabeling_is_bitwise_invariant():
+    ml = needs_gpu()
+    x, W, A, B, rk, idx = _random_case(7, 64, 512, 512, 6, (8, 16, 32, 64, 24, 40), r_max=64, frac_none=0.0)
+    y1 = _run(ml, x, W, A, B, rk, idx, 2.0, OL.VERIFY)
+    relabel = np.array([3, 5, 0, 1, 4, 2])
+    inv = np.argsort(relabel)
+    y2 = _run(ml, x, W, A[inv].copy(), B[inv].copy(), rk[inv].copy(), relabel[idx].astype(np.int32), 2.0, OL.VERIFY)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_invalid_adapter_and_rank_raise_status():
+    ml = needs_gpu()
+    x, W, A, B, rk, idx = _random_case(8, 32, 256, 128, 4, (8, 8, 8, 8), r_max=8, nan_pad=False, frac_none=0.0)
+    bad = idx.copy()
+    bad[3] = 9
+    bad[4] = -7
+    y_ref, st_ref = _oracle(x, W, A, B, rk, bad, 2.0, OL.VERIFY)
+    ws = ml.Workspace(ml.linear_workspace_bytes(32, 256, 128, 4))
+    y = _run(ml, x, W, A, B, rk, bad, 2.0, OL.VERIFY, ws=ws)
+    assert ws.status() == st_ref == ml.DEV_BAD_ADAPTER
+    assert _rel_err(host_bf16_to_f64(y), y_ref) <= TOL
+    rk2 = rk.copy()
+    rk2[1] = 65
+    y_ref, st_ref = _oracle(x, W, A, B, rk2, idx, 2.0, OL.VERIFY)
+    y = _run(ml, x, W, A, B, rk2, idx, 2.0, OL.VERIFY, ws=ws)
+    assert ws.status() == st_ref == ml.DEV_BAD_RANK
+    assert _rel_err(host_bf16_to_f64(y), y_ref) <= TOL
+
+
+def test_one_workspace_and_one_plan_serve_many_projections():
+    """The decode-step usage: one plan, one workspace, several projections."""
+    ml = needs_gpu()
+    cfg = WL.TINY
+    idx = WL.row_adapters(cfg, "verify")
+    ranks = WL.adapter_ranks(cfg)
+    ws = ml.Workspace(ml.linear_workspace_bytes(16, 1024, 1024, 4))
+    seg_p, _ = ml.plan_segments(dev(idx), dev(ranks), 4, 8, ws)
+    for seed in range(3):
+        x, W, A, B, rk, _ = _random_case(seed, 16, 512 + 256 * seed, 512, 4, tuple(ranks), r_max=8, nan_pad=False)
+        y_ref, _ = _oracle(x, W, A, B, rk, idx, 2.0, OL.VERIFY)
+        y = ml.linear(dev_bf16(x), dev_bf16(W), dev_bf16(A), dev_bf16(B), dev(rk), dev(idx), 2.0, ml.VERIFY,
+                      ws=ws, seg_offsets_ptr=seg_p)
+        assert _rel_err(host_bf16_to_f64(y), y_ref) <= TOL
+    assert ws.status() == 0
+
+
+FULL = [
+    (WL.LLAMA8B_R16, None, range(7)),
+    (WL.LLAMA8B_HET, None, (1, 4, 6)),
+    (WL.QWEN32B_R16, 1, (2, 6)),
+    (WL.QWEN32B_R16, 2, (0,)),
+    (WL.QWEN32B_R16, 4, (2, 4)),
+]
+
+
+@pytest.mark.parametrize("cfg,k,projs", FULL, ids=lambda v: getattr(v, "name", str(v)))
+def test_full_size_sampled_outputs(cfg, k, projs):
+    """Workload sizes as benchmarked; 512 sampled outputs per call vs the oracle one by one."""
+    ml = needs_gpu()
+    ranks = WL.adapter_ranks(cfg)
+    for p in projs:
+        _, K, N = cfg.projections[p]
+        W, A, B, _ = WL.projection_weights(cfg, p)
+        Wd, Ad, Bd = dev_bf16(W), dev_bf16(A), dev_bf16(B)
+        for mode, name in ((OL.DRAFT, "draft"), (OL.VERIFY, "verify")):
+            x = WL.activations(cfg, p, name, k=k)
+            idx = WL.row_adapters(cfg, name, k=k)
+            M = x.shape[0]
+            ws = ml.Workspace(ml.linear_workspace_bytes(M, N, K, cfg.n_adapters))
+            y = ml.linear(dev_bf16(x), Wd, Ad, Bd, dev(ranks), dev(idx), cfg.scale, mode, ws=ws)
+            yh = host_bf16_to_f64(y)
+            assert ws.status() == 0
+            g = np.random.default_rng(p)
+            rows, cols = g.integers(0, M, 512), g.integers(0, N, 512)
+            f = WL.bf16_to_f64
+            e = OL.mlora_linear_entries(rows, cols, f(x), f(W), f(A), f(B), ranks, idx, cfg.scale, mode)
+            scale_ref = max(np.max(np.abs(e)), 1e-30)
+            assert np.max(np.abs(yh[rows, cols] - e)) <= TOL * scale_ref, (cfg.name, p, name)
+            assert np.isfinite(yh).all()
