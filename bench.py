@@ -175,10 +175,12 @@ class DeviceWorkload:
         out.append(("plan", plan))
         for P in self.proj:
             out.append((f"draft.{P['name']}", lambda P=P: ml.linear(P["xd"], P["W"], None, None, None, None,
-                                                                     cfg.scale, ml.DRAFT, ws=self.ws, y=P["yd"])))
+                                                                     cfg.scale, ml.DRAFT | ml.PREFETCH_WEIGHTS,
+                                                                     ws=self.ws, y=P["yd"])))
         for P in self.proj:
             out.append((f"verify.{P['name']}", lambda P=P: ml.linear(P["xv"], P["W"], P["A"], P["B"], self.rank_of,
-                                                                      self.adx_v, cfg.scale, ml.VERIFY, ws=self.ws,
+                                                                      self.adx_v, cfg.scale,
+                                                                      ml.VERIFY | ml.PREFETCH_WEIGHTS, ws=self.ws,
                                                                       y=P["yv"], seg_offsets_ptr=self.seg)))
         out.append(("accept", lambda: ml.verify_accept(self.p, self.q, self.tok, self.u, ws=self.ws,
                                                       out_tok=self.out_tok, accepted=self.accepted)))

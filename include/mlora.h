@@ -68,7 +68,15 @@ typedef enum {
   MLORA_ERR_UNSUPPORTED = 7    /* current device is not compute capability 10.3 */
 } mlora_status;
 
-typedef enum { MLORA_DRAFT = 0, MLORA_VERIFY = 1 } mlora_mode;
+typedef enum {
+  MLORA_DRAFT = 0,   /* LoRA off: y = W x */
+  MLORA_VERIFY = 1,  /* LoRA on:  y = W x + scale * B_a (A_a x) */
+  /* Flag, OR-ed into the mode: W is constant while the stream runs (model
+   * weights), so the call may start streaming W before the preceding kernel
+   * on the stream has finished.  Activations, rank_of, adapter_idx, A and B
+   * are still read only after it finishes. */
+  MLORA_PREFETCH_WEIGHTS = 0x100
+} mlora_mode;
 
 /* Device status bits (mlora_read_device_status). */
 #define MLORA_DEV_BAD_ADAPTER (1u << 0) /* adapter_idx outside [-1, n_adapters): row ran base-only */
@@ -174,7 +182,7 @@ MLORA_API mlora_status mlora_shrink(const mlora_bf16 *x, int M, int K, const mlo
 MLORA_API mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W, int N,
                           const mlora_bf16 *A_stack, const mlora_bf16 *B_stack, int n_adapters, int r_max,
                           const int32_t *rank_of, const int32_t *adapter_idx, const int32_t *seg_offsets,
-                          float scale, mlora_mode mode, mlora_bf16 *y, void *workspace, size_t ws_bytes,
+                          float scale, int mode, mlora_bf16 *y, void *workspace, size_t ws_bytes,
                           mlora_stream stream);
 
 /* ------------------------------------------------------------------------- */

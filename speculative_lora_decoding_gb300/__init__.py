@@ -25,6 +25,7 @@ import torch
 
 DRAFT = 0
 VERIFY = 1
+PREFETCH_WEIGHTS = 0x100  # mode flag: W is constant; may be streamed before the preceding kernel ends
 
 DEV_BAD_ADAPTER = 1 << 0
 DEV_BAD_RANK = 1 << 1
@@ -201,7 +202,7 @@ def linear(x: torch.Tensor, W: torch.Tensor, A_stack, B_stack, rank_of, adapter_
     N, K2 = W.shape
     if K2 != K:
         raise ValueError("W and x disagree on K")
-    verify = mode == VERIFY
+    verify = (mode & ~PREFETCH_WEIGHTS) == VERIFY
     n_ad, r_max = 0, 0
     a_ptr = b_ptr = r_ptr = i_ptr = None
     if verify:

@@ -12,13 +12,15 @@
 //           S = sum_v w(v), U = floor(u_k * 2^32)
 //
 // Layout: each request's vocabulary row is cut into `slices` contiguous
-// slices, one CTA each, so a small batch still spreads over every SM.  A CTA
-// reads its slice once (coalesced 16-byte loads) and publishes two exact
-// uint64 sums (residual mass and target mass).  The last CTA of a request to
-// arrive (atomic counter, no spinning) adds the slice sums in order, picks
-// the slice holding the draw, re-reads only that slice and locates the token
-// with a block-wide prefix scan.  All sums are integers, so the order of
-// addition cannot change a result.
+// slices, one CTA each, so a small batch still spreads over every SM; each
+// slice is cut into one contiguous sub-range per warp.  A warp reads its
+// sub-range once (coalesced 16-byte loads) and publishes two exact uint64
+// sums (residual mass and target mass).  The last CTA of a request to arrive
+// (atomic counter, no spinning) scans the per-warp sums in vocabulary order,
+// picks the sub-range holding the draw, re-reads only that sub-range in one
+// round (a contiguous run per thread) and locates the token with a block-wide
+// prefix scan.  All sums are integers, so the order of addition cannot change
+// a result.
 #include "common.cuh"
 #include "launch.h"
 
@@ -91,20 +93,42 @@ __device__ __forceinline__ uint64_t warp_incl_scan_u64(uint64_t v) {
   return v;
 }
 
+// Exclusive block scan of one uint64 per thread; *total gets the sum.
+__device__ __forceinline__ uint64_t block_excl_scan_u64(uint64_t v, uint64_t *sh, uint64_t *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint64_t inc = warp_incl_scan_u64(v);
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  uint64_t before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < ACC_WARPS; ++w) {
+    const uint64_t t = sh[w];
+    if (w < warp) before += t;
+    all += t;
+  }
+  __syncthreads();
+  *total = all;
+  return before + inc - v;
+}
+
+// Vocabulary row of request b: slices of slice_len (one CTA each), each slice
+// cut into ACC_WARPS contiguous sub-ranges of sub_len (one warp each).
 __global__ void __launch_bounds__(ACC_THREADS)
     accept_kernel(const float *__restrict__ p, const float *__restrict__ q, const int32_t *__restrict__ draft_tok,
                   const float *__restrict__ uni, int B, int k, int V, int slices, int slice_len, int vec,
                   int32_t *__restrict__ out_tok, int32_t *__restrict__ accepted, uint32_t *counters,
-                  uint64_t *slice_sums, uint32_t *status) {
-  __shared__ uint64_t sh_a[ACC_WARPS], sh_b[ACC_WARPS];
-  __shared__ int sh_n, sh_last, sh_tok;
+                  uint64_t *sums, uint32_t *status) {
+  __shared__ uint64_t sh_scan[ACC_WARPS];
+  __shared__ int sh_n, sh_last, sh_tok, sh_mode, sh_entry;
   __shared__ uint32_t sh_flags;
-  __shared__ uint64_t sh_T, sh_base;
-  __shared__ int sh_mode, sh_slice;
+  __shared__ uint64_t sh_T, sh_Tloc;
 
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int b = blockIdx.x / slices, g = blockIdx.x % slices;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k1 = k + 1;
+  const int sub_len = slice_len / ACC_WARPS;
   uint32_t flags = 0;
 
   // Step a5: accept tests (cheap gathers; every CTA of the request agrees).
@@ -134,26 +158,25 @@ __global__ void __launch_bounds__(ACC_THREADS)
   const float *prow = p + ((size_t)b * k1 + n) * V;
   const float *qrow = residual ? q + ((size_t)b * k + n) * V : prow;
 
-  // Step a6, pass 1: exact sums over this CTA's slice.
-  const int v0 = g * slice_len, v1 = min(V, v0 + slice_len);
+  // Step a6, pass 1: exact sums over this warp's sub-range.
+  const int w0 = min(V, g * slice_len + warp * sub_len), w1 = min(V, w0 + sub_len);
   uint64_t s_res = 0, s_tgt = 0;
   if (vec) {
     const float4 *p4 = reinterpret_cast<const float4 *>(prow);
     const float4 *q4 = reinterpret_cast<const float4 *>(qrow);
-    const int e0 = v0 >> 2, e1 = v1 >> 2;  // v0, V multiples of 4 on this path
-    int e = e0 + tid;
-    for (; e + 3 * ACC_THREADS < e1; e += 4 * ACC_THREADS) {
+    const int e0 = w0 >> 2, e1 = w1 >> 2;  // w0, V multiples of 4 on this path
+    int e = e0 + lane;
+    for (; e + 96 < e1; e += 128) {
       float4 pv[4], qv[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        pv[r] = __ldcs(p4 + e + r * ACC_THREADS);
-        if (residual) qv[r] = __ldcs(q4 + e + r * ACC_THREADS);
+        pv[r] = __ldcs(p4 + e + 32 * r);
+        qv[r] = residual ? __ldcs(q4 + e + 32 * r) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const float pa[4] = {pv[r].x, pv[r].y, pv[r].z, pv[r].w};
-        const float qa[4] = {residual ? qv[r].x : 0.f, residual ? qv[r].y : 0.f, residual ? qv[r].z : 0.f,
-                             residual ? qv[r].w : 0.f};
+        const float qa[4] = {qv[r].x, qv[r].y, qv[r].z, qv[r].w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const Weights w = weight_of(pa[t], qa[t], residual, flags);
@@ -162,7 +185,7 @@ __global__ void __launch_bounds__(ACC_THREADS)
         }
       }
     }
-    for (; e < e1; e += ACC_THREADS) {
+    for (; e < e1; e += 32) {
       const float4 pv = __ldcs(p4 + e);
       const float4 qv = residual ? __ldcs(q4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
       const float pa[4] = {pv.x, pv.y, pv.z, pv.w};
@@ -175,7 +198,7 @@ __global__ void __launch_bounds__(ACC_THREADS)
       }
     }
   } else {
-    for (int v = v0 + tid; v < v1; v += ACC_THREADS) {
+    for (int v = w0 + lane; v < w1; v += 32) {
       const Weights w = weight_of(prow[v], residual ? qrow[v] : 0.f, residual, flags);
       s_res += w.res;
       s_tgt += w.tgt;
@@ -183,21 +206,16 @@ __global__ void __launch_bounds__(ACC_THREADS)
   }
   s_res = warp_sum_u64(s_res);
   s_tgt = warp_sum_u64(s_tgt);
+  const size_t entries = (size_t)slices * ACC_WARPS;
   if (lane == 0) {
-    sh_a[warp] = s_res;
-    sh_b[warp] = s_tgt;
+    const size_t at = ((size_t)b * entries + (size_t)g * ACC_WARPS + warp) * 2;
+    sums[at + 0] = s_res;
+    sums[at + 1] = s_tgt;
+    __threadfence();
   }
   if (flags) atomicOr(&sh_flags, flags);
   __syncthreads();
   if (tid == 0) {
-    uint64_t a = 0, t = 0;
-    for (int w = 0; w < ACC_WARPS; ++w) {
-      a += sh_a[w];
-      t += sh_b[w];
-    }
-    slice_sums[((size_t)b * slices + g) * 2 + 0] = a;
-    slice_sums[((size_t)b * slices + g) * 2 + 1] = t;
-    __threadfence();
     const uint32_t old = atomicAdd(&counters[b], 1u);
     sh_last = (old == (uint32_t)(slices - 1));
   }
@@ -207,16 +225,22 @@ __global__ void __launch_bounds__(ACC_THREADS)
     return;
   }
 
-  // Last CTA of this request: choose the weights, the draw and its slice.
+  // Last CTA of this request: scan the per-warp sums (vocabulary order),
+  // choose the weights and the draw, and find the sub-range holding it.
+  __threadfence();
+  const int per = (int)((entries + ACC_THREADS - 1) / ACC_THREADS);
+  const int c0 = min((int)entries, tid * per), c1 = min((int)entries, c0 + per);
+  uint64_t my_res = 0, my_tgt = 0;
+  for (int c = c0; c < c1; ++c) {
+    my_res += __ldcg(&sums[((size_t)b * entries + c) * 2 + 0]);
+    my_tgt += __ldcg(&sums[((size_t)b * entries + c) * 2 + 1]);
+  }
+  uint64_t S_res, S_tgt;
+  const uint64_t ex_res = block_excl_scan_u64(my_res, sh_scan, &S_res);
+  const uint64_t ex_tgt = block_excl_scan_u64(my_tgt, sh_scan, &S_tgt);
   if (tid == 0) {
-    __threadfence();
     counters[b] = 0u;
     uint32_t f2 = sh_flags;
-    uint64_t S_res = 0, S_tgt = 0;
-    for (int s = 0; s < slices; ++s) {
-      S_res += __ldcg(&slice_sums[((size_t)b * slices + s) * 2 + 0]);
-      S_tgt += __ldcg(&slice_sums[((size_t)b * slices + s) * 2 + 1]);
-    }
     int mode = residual ? 0 : 1;  // 0: residual weights, 1: target weights
     if (residual && S_res == 0) {
       f2 |= MLORA_DEV_ZERO_MASS;
@@ -224,68 +248,62 @@ __global__ void __launch_bounds__(ACC_THREADS)
     }
     const uint64_t S = mode == 0 ? S_res : S_tgt;
     const float uk = sanitize_uniform(uni[(size_t)b * k1 + k], f2);
-    int tok = -1;
+    sh_tok = -1;
+    sh_entry = -1;
     if (S == 0) {
       f2 |= MLORA_DEV_ZERO_MASS;
-      tok = 0;
+      sh_tok = 0;
     } else {
       const uint64_t U = __float2ull_rz(uk * TWO_POW_32);
       const uint64_t lo = U * S, hi = __umul64hi(U, S);
-      const uint64_t T = (hi << 32) | (lo >> 32);  // floor(U * S / 2^32)
-      uint64_t run = 0;
-      int sl = slices - 1;
-      for (int s = 0; s < slices; ++s) {
-        const uint64_t w = __ldcg(&slice_sums[((size_t)b * slices + s) * 2 + mode]);
-        if (run + w > T) {
-          sl = s;
-          break;
-        }
-        run += w;
-      }
-      sh_T = T - run;
-      sh_slice = sl;
+      sh_T = (hi << 32) | (lo >> 32);  // floor(U * S / 2^32) < S
     }
-    sh_tok = tok;
     sh_mode = mode;
-    sh_base = 0;
     if (f2) raise_status(status, f2);
+  }
+  __syncthreads();
+  const int mode = sh_mode;
+  if (sh_tok < 0) {
+    const uint64_t T = sh_T;
+    uint64_t run = mode == 0 ? ex_res : ex_tgt;
+    for (int c = c0; c < c1; ++c) {
+      const uint64_t w = __ldcg(&sums[((size_t)b * entries + c) * 2 + mode]);
+      if (run <= T && T < run + w) {
+        sh_entry = c;
+        sh_Tloc = T - run;  // the draw inside the entry; exactly one thread gets here
+      }
+      run += w;
+    }
   }
   __syncthreads();
 
   if (sh_tok < 0) {
-    // Pass 2: prefix scan over the chosen slice, 4 elements per thread per round.
-    const int mode = sh_mode;
-    const uint64_t T = sh_T;
-    const int w0 = sh_slice * slice_len, w1 = min(V, w0 + slice_len);
-    for (int base = w0; base < w1; base += 4 * ACC_THREADS) {
-      uint64_t w[4];
-      uint64_t mine = 0;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int v = base + tid * 4 + t;
-        uint32_t dummy = 0;
-        w[t] = 0;
-        if (v < w1) {
-          const Weights ww = weight_of(prow[v], residual ? qrow[v] : 0.f, mode == 0, dummy);
-          w[t] = mode == 0 ? ww.res : ww.tgt;
+    // Pass 2: one round over the chosen sub-range, a contiguous run per thread.
+    const int ent = sh_entry;
+    const uint64_t T = sh_Tloc;
+    const int gs = ent / ACC_WARPS, ws = ent % ACC_WARPS;
+    const int r0 = min(V, gs * slice_len + ws * sub_len), r1 = min(V, r0 + sub_len);
+    const int len = r1 - r0;
+    const int per2 = (len + ACC_THREADS - 1) / ACC_THREADS;
+    const int t0 = min(len, tid * per2), t1 = min(len, t0 + per2);
+    uint64_t mine = 0;
+    uint32_t dummy = 0;
+    for (int v = r0 + t0; v < r0 + t1; ++v) {
+      const Weights w = weight_of(prow[v], residual ? qrow[v] : 0.f, mode == 0, dummy);
+      mine += mode == 0 ? w.res : w.tgt;
+    }
+    uint64_t tot;
+    uint64_t run = block_excl_scan_u64(mine, sh_scan, &tot);
+    if (run <= T && T < run + mine) {
+      for (int v = r0 + t0; v < r0 + t1; ++v) {
+        const Weights w = weight_of(prow[v], residual ? qrow[v] : 0.f, mode == 0, dummy);
+        const uint64_t wv = mode == 0 ? w.res : w.tgt;
+        if (T < run + wv) {
+          sh_tok = v;
+          break;
         }
-        mine += w[t];
+        run += wv;
       }
-      const uint64_t inc = warp_incl_scan_u64(mine);
-      if (lane == 31) sh_a[warp] = inc;
-      __syncthreads();
-      uint64_t before = sh_base;
-      for (int ww = 0; ww < warp; ++ww) before += sh_a[ww];
-      uint64_t run = before + inc - mine;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        if (run <= T && T < run + w[t]) sh_tok = base + tid * 4 + t;
-        run += w[t];
-      }
-      __syncthreads();
-      if (sh_tok >= 0) break;
-      if (tid == ACC_THREADS - 1) sh_base = run;
-      __syncthreads();
     }
   }
   __syncthreads();
@@ -309,12 +327,13 @@ AcceptShape accept_shape(int B, int k, int V, int num_sms) {
   const int max_slices = (V + MIN_SLICE - 1) / MIN_SLICE;
   if (want > max_slices) want = max_slices;
   if (want < 1) want = 1;
+  const int quantum = 4 * ACC_WARPS;  // every warp sub-range starts on a float4
   int len = (V + want - 1) / want;
-  len = (len + 3) / 4 * 4;
+  len = (len + quantum - 1) / quantum * quantum;
   s.slice_len = len;
   s.slices = (V + len - 1) / len;
   s.threads = ACC_THREADS;
-  s.scratch_bytes = (size_t)B * s.slices * 2 * sizeof(uint64_t);
+  s.scratch_bytes = (size_t)B * s.slices * ACC_WARPS * 2 * sizeof(uint64_t);
   return s;
 }
 
@@ -324,11 +343,10 @@ cudaError_t launch_accept(const float *p, const float *q, const int32_t *draft_t
   const int vec = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(p) & 15) == 0) &&
                   ((reinterpret_cast<uintptr_t>(q) & 15) == 0);
   const long long grid = (long long)B * sh.slices;
-  accept_kernel<<<(unsigned)grid, ACC_THREADS, 0, s>>>(p, q, draft_tok, u, B, k, V, sh.slices, sh.slice_len, vec,
-                                                       out_tok, accepted, counters,
-                                                       reinterpret_cast<uint64_t *>(scratch), status);
-  note_launch();
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(accept_kernel, dim3((unsigned)grid), dim3(ACC_THREADS), 0, s, p, q, draft_tok, u, B, k, V,
+                             sh.slices, sh.slice_len, vec, out_tok, accepted, counters,
+                             reinterpret_cast<uint64_t *>(scratch), status);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mlora

@@ -21,7 +21,7 @@ static int device_sms() {
 static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct LinearLayout {
-  size_t plan, T, partials, total;
+  size_t plan, T, total;
 };
 
 static LinearLayout linear_layout(int M, int N, int K, int n_ad, int sms) {
@@ -32,9 +32,9 @@ static LinearLayout linear_layout(int M, int N, int K, int n_ad, int sms) {
   o = align_up(o + P.words * 4, 256);
   L.T = o;
   o = align_up(o + (size_t)M * T_STRIDE * 4, 256);
-  L.partials = o;
-  const GemmShape sh = gemm_shape(M, N, K, sms);
-  o = align_up(o + sh.partial_floats * 4, 256);
+  (void)N;
+  (void)K;
+  (void)sms;
   L.total = o;
   return L;
 }
@@ -126,11 +126,13 @@ mlora_status mlora_shrink(const mlora_bf16 *x, int M, int K, const mlora_bf16 *A
 
 mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W, int N, const mlora_bf16 *A_stack,
                           const mlora_bf16 *B_stack, int n_adapters, int r_max, const int32_t *rank_of,
-                          const int32_t *adapter_idx, const int32_t *seg_offsets, float scale, mlora_mode mode,
+                          const int32_t *adapter_idx, const int32_t *seg_offsets, float scale, int mode,
                           mlora_bf16 *y, void *workspace, size_t ws_bytes, mlora_stream stream) {
   if (!x || !W || !y) return MLORA_ERR_ARG;
-  if (mode != MLORA_DRAFT && mode != MLORA_VERIFY) return MLORA_ERR_ARG;
-  const bool verify = mode == MLORA_VERIFY;
+  const int prefetch_w = (mode & MLORA_PREFETCH_WEIGHTS) ? 1 : 0;
+  const int base_mode = mode & ~MLORA_PREFETCH_WEIGHTS;
+  if (base_mode != MLORA_DRAFT && base_mode != MLORA_VERIFY) return MLORA_ERR_ARG;
+  const bool verify = base_mode == MLORA_VERIFY;
   if (verify && (!A_stack || !B_stack || !rank_of || !adapter_idx)) return MLORA_ERR_ARG;
   if (!linear_sizes_ok(M, N, K, verify ? n_adapters : 0)) return MLORA_ERR_SHAPE;
   if (verify && (n_adapters < 1 || r_max < 8 || r_max > MLORA_MAX_RANK || (r_max % 8) != 0)) return MLORA_ERR_SHAPE;
@@ -146,7 +148,6 @@ mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t *ws = (uint8_t *)workspace;
   uint32_t *status = reinterpret_cast<uint32_t *>(ws + WS_STATUS_OFF);
-  uint32_t *counters = reinterpret_cast<uint32_t *>(ws + WS_COUNTERS_OFF);
   int32_t *plan = reinterpret_cast<int32_t *>(ws + L.plan);
   float *T = reinterpret_cast<float *>(ws + L.T);
   cudaError_t e;
@@ -168,7 +169,8 @@ mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W
   g.M = M;
   g.N = N;
   g.K = K;
-  g.mode = mode;
+  g.mode = base_mode;
+  g.prefetch_w = prefetch_w;
   g.scale = scale;
   g.y = y;
   g.B_stack = B_stack;
@@ -176,8 +178,6 @@ mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W
   g.n_ad = n_ad;
   g.T = T;
   g.plan = plan;
-  g.partials = reinterpret_cast<float *>(ws + L.partials);
-  g.counters = counters;
   g.status = status;
   int err = 0;
   e = launch_gemm(g, sh, s, &err);

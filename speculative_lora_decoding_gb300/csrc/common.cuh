@@ -27,15 +27,27 @@ constexpr int T_STRIDE = 64;                  // row stride of the internal fp32
 
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Shrink work items: (adapter, block of SHRINK_J rank rows, chunk of SHRINK_TOK rows).
+constexpr int SHRINK_J = 8;
+constexpr int SHRINK_TOK = 4;
+constexpr int ITEM_WORDS = 8;  // {adapter, j0, nrow, ntok, row0..row3}
+
+// Upper bound on shrink items for M rows and n_ad adapters (rank <= 64).
+__host__ __device__ inline size_t max_shrink_items(int M, int n_ad) {
+  const int m_ad = M < n_ad ? M : n_ad;
+  return (size_t)(64 / SHRINK_J) * ((M + SHRINK_TOK - 1) / SHRINK_TOK + m_ad);
+}
+
 // Plan layout inside scratch (int32 words), for M rows and n_ad adapters.
 struct PlanLayout {
-  size_t hdr;         // [0] n_active, [1] total shrink items, [2] n_rows_valid
+  size_t hdr;         // [0] n_active, [1] total shrink items, [2] rows
   size_t seg_offsets; // [n_ad + 2]
   size_t perm;        // [M]
   size_t row_adapter; // [M]   validated adapter per row (-1: none)
   size_t rank_eff;    // [n_ad] validated ranks
   size_t active;      // [n_ad] adapters with rows, increasing
   size_t item_off;    // [n_ad + 1] prefix of shrink items over the active list
+  size_t items;       // [max_shrink_items][ITEM_WORDS], 16-byte aligned
   size_t words;       // total int32 words
 };
 
@@ -49,13 +61,10 @@ __host__ __device__ inline PlanLayout plan_layout(int M, int n_ad) {
   L.rank_eff = o;     o += align_up(n_ad, 16);
   L.active = o;       o += align_up(n_ad, 16);
   L.item_off = o;     o += align_up(n_ad + 1, 16);
+  L.items = o;        o += max_shrink_items(M, n_ad) * ITEM_WORDS;
   L.words = o;
   return L;
 }
-
-// Shrink work items: (adapter, block of SHRINK_J rank rows, chunk of SHRINK_TOK rows).
-constexpr int SHRINK_J = 8;
-constexpr int SHRINK_TOK = 4;
 
 // ---------------------------------------------------------------------------
 // Status word
@@ -231,7 +240,51 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters: barrier and distributed shared memory
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Shared-memory address of the same variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t caddr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+  return v;
+}
+
+// Programmatic dependent launch: wait for the preceding grid's memory, and
+// allow the next grid in the stream to begin launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // Named barrier over `nthreads` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

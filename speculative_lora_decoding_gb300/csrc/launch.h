@@ -10,6 +10,28 @@ namespace mlora {
 
 void note_launch();
 
+// Launch with programmatic dependent launch allowed: the kernel may start
+// while the preceding kernel in the stream finishes; every kernel of this
+// library calls griddepcontrol.wait before it reads anything an earlier
+// kernel may have written.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  note_launch();
+  return e;
+}
+
 // Step a1: stable counting sort of rows by adapter into `plan` (int32 words).
 cudaError_t launch_plan(const int32_t *adapter_idx, int M, const int32_t *rank_of, int n_ad, int r_max,
                         int32_t *plan, uint32_t *status, cudaStream_t s);
@@ -22,6 +44,8 @@ cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, in
 // Steps a3 + a4: base GEMM on tcgen05 with the expand epilogue.
 struct GemmShape {
   int Mb, nsub, sub_n, n_tgroups, n_units, kblocks, total_iters, stages, nbuf, tmem_cols, grid;
+  int C;          // CTAs per cluster splitting K (1: no split)
+  int red_bytes;  // shared memory for the cluster reduction
   size_t smem_bytes, partial_floats;
 };
 GemmShape gemm_shape(int M, int N, int K, int num_sms);
@@ -31,14 +55,13 @@ struct GemmLaunch {
   const uint16_t *W;
   int M, N, K;
   int mode;
+  int prefetch_w;  // W may be requested before the preceding kernel finishes
   float scale;
   uint16_t *y;
   const uint16_t *B_stack;
   int r_max, n_ad;
   const float *T;
   const int32_t *plan;
-  float *partials;
-  uint32_t *counters;
   uint32_t *status;
 };
 cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s, int *err_code);

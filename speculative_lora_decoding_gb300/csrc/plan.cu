@@ -7,16 +7,18 @@
 // shrink kernel reads each adapter's A once per group and the GEMM epilogue
 // keeps each adapter's B row in registers across its group.
 //
-// One CTA of 1024 threads: histogram in shared memory, block-wide scans for
+// One CTA of 256 threads: histogram in shared memory, block-wide scans for
 // the offsets, the active-adapter list and the shrink work list, then a
 // warp-sequential ranking (match_any within a warp, warps in order) that
-// keeps rows of one bucket in increasing row order.
+// keeps rows of one bucket in increasing row order, and finally the shrink
+// work items written out in full, so that a shrink CTA finds its adapter,
+// rank rows and token rows with one load.
 #include "common.cuh"
 #include "launch.h"
 
 namespace mlora {
 
-constexpr int PLAN_THREADS = 1024;
+constexpr int PLAN_THREADS = 256;
 
 __device__ __forceinline__ int warp_incl_scan(int v) {
   const int lane = threadIdx.x & 31;
@@ -52,6 +54,8 @@ __device__ __forceinline__ int bucket_of(int a, int n_ad) { return (a >= 0 && a 
 __global__ void __launch_bounds__(PLAN_THREADS, 1)
     plan_kernel(const int32_t *__restrict__ adapter_idx, int M, const int32_t *__restrict__ rank_of, int n_ad,
                 int r_max, int32_t *__restrict__ plan, uint32_t *status) {
+  grid_launch_dependents();
+  grid_dependency_wait();
   extern __shared__ int sh_dyn[];
   int *cnt = sh_dyn;                 // [n_ad + 1]: counts, then bucket offsets
   int *running = sh_dyn + n_ad + 1;  // [n_ad + 1]
@@ -142,8 +146,8 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
   for (int b = tid; b < nb; b += PLAN_THREADS) running[b] = 0;
   __syncthreads();
 
-  // Stable ranks: rows in chunks of 1024; within a warp lanes with the same
-  // bucket are ranked by lane order, warps take their turn in order.
+  // Stable ranks: rows in chunks of PLAN_THREADS; within a warp lanes with
+  // the same bucket are ranked by lane order, warps take their turn in order.
   const int lane = tid & 31, warp = tid >> 5;
   for (int base = 0; base < M; base += PLAN_THREADS) {
     const int m = base + tid;
@@ -163,15 +167,47 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
     if (m < M) plan[L.perm + cnt[b] + basev + rank_in_warp] = m;
   }
   __syncthreads();
+
+  // Shrink work items, one record each: the item's adapter comes from a
+  // binary search of the item offsets (copied to shared memory).
+  const int n_active = plan[L.hdr + 0];
+  const int total_items = plan[L.hdr + 1];
+  int *ioff = running;  // reuse: [n_active + 1] item offsets
+  for (int i = tid; i <= n_active; i += PLAN_THREADS) ioff[i] = plan[L.item_off + i];
+  __syncthreads();
+  for (int it = tid; it < total_items; it += PLAN_THREADS) {
+    int lo = 0, hi = n_active;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (ioff[mid] <= it) lo = mid; else hi = mid;
+    }
+    const int a = plan[L.active + lo];
+    const int r = plan[L.rank_eff + a];
+    const int s0 = plan[L.seg_offsets + a];
+    const int c = plan[L.seg_offsets + a + 1] - s0;
+    const int local = it - ioff[lo];
+    const int nj = (r + SHRINK_J - 1) / SHRINK_J;
+    const int j0 = (local % nj) * SHRINK_J;
+    const int t0 = (local / nj) * SHRINK_TOK;
+    const int ntok = min(SHRINK_TOK, c - t0);
+    int4 w0 = make_int4(a, j0, min(SHRINK_J, r - j0), ntok);
+    int rows[SHRINK_TOK];
+#pragma unroll
+    for (int t = 0; t < SHRINK_TOK; ++t) rows[t] = (t < ntok) ? plan[L.perm + s0 + t0 + t] : 0;
+    int4 *rec = reinterpret_cast<int4 *>(plan + L.items + (size_t)it * ITEM_WORDS);
+    rec[0] = w0;
+    rec[1] = make_int4(rows[0], rows[1], rows[2], rows[3]);
+  }
+  __syncthreads();
   if (tid == 0 && flags) raise_status(status, flags);
 }
 
 cudaError_t launch_plan(const int32_t *adapter_idx, int M, const int32_t *rank_of, int n_ad, int r_max,
                         int32_t *plan, uint32_t *status, cudaStream_t s) {
   const size_t smem = 2 * (size_t)(n_ad + 1) * sizeof(int);  // <= 32.8 KB for n_ad <= 4096
-  plan_kernel<<<1, PLAN_THREADS, smem, s>>>(adapter_idx, M, rank_of, n_ad, r_max, plan, status);
-  note_launch();
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(PLAN_THREADS), smem, s, adapter_idx, M, rank_of, n_ad, r_max,
+                             plan, status);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mlora

@@ -4,8 +4,9 @@
 // Per-Request Adapter Selection").
 //
 // Work item = (adapter a, block of SHRINK_J = 8 rows of A_a, chunk of
-// SHRINK_TOK = 4 rows of the adapter's group).  One CTA of 8 warps takes an
-// item and splits K across its warps; each lane streams 16-byte pieces of
+// SHRINK_TOK = 4 rows of the adapter's group), read as one 32-byte record
+// the plan kernel wrote.  One CTA of 8 warps takes an item and splits K
+// across its warps; each lane streams 16-byte pieces of
 // the 8 A rows (coalesced: a warp reads 512 contiguous bytes per row per
 // step) and of the 4 x rows, and keeps 8 x 4 fp32 partial sums in registers.
 // Every A element is used by exactly one thread, for all 4 tokens, so A goes
@@ -37,44 +38,44 @@ __device__ __forceinline__ uint4 ldg_stream(const uint16_t *p) {
   return v;
 }
 
+// Sums of 32 per-lane values across the warp: after the five exchange rounds
+// lane l holds the warp total of value l (31 shuffles instead of 160).
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return v[0];
+}
+
 __global__ void __launch_bounds__(SHRINK_THREADS)
     shrink_kernel(const uint16_t *__restrict__ x, int M, int K, const uint16_t *__restrict__ A, int n_ad, int r_max,
                   const int32_t *__restrict__ plan, float *__restrict__ T, int t_stride) {
-  __shared__ float red[SHRINK_WARPS][SHRINK_J][SHRINK_TOK];
+  __shared__ float red[SHRINK_WARPS][SHRINK_J * SHRINK_TOK];
+  grid_launch_dependents();
+  grid_dependency_wait();
   const PlanLayout L = plan_layout(M, n_ad);
-  const int n_active = plan[L.hdr + 0];
   const int total_items = plan[L.hdr + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kchunks = K >> 3;  // 16-byte pieces per row
 
   for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-    // Active-list slot holding this item (item_off is increasing).
-    int lo = 0, hi = n_active;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (plan[L.item_off + mid] <= item) lo = mid; else hi = mid;
-    }
-    const int a = plan[L.active + lo];
-    const int r = plan[L.rank_eff + a];
-    const int s0 = plan[L.seg_offsets + a];
-    const int cnt = plan[L.seg_offsets + a + 1] - s0;
-    const int local = item - plan[L.item_off + lo];
-    const int nj = (r + SHRINK_J - 1) / SHRINK_J;
-    const int j0 = (local % nj) * SHRINK_J;
-    const int t0 = (local / nj) * SHRINK_TOK;
-    const int ntok = min(SHRINK_TOK, cnt - t0);
-    const int nrow = min(SHRINK_J, r - j0);
-
-    int rows[SHRINK_TOK];
-#pragma unroll
-    for (int t = 0; t < SHRINK_TOK; ++t) rows[t] = (t < ntok) ? plan[L.perm + s0 + t0 + t] : 0;
+    const int4 *rec = reinterpret_cast<const int4 *>(plan + L.items + (size_t)item * ITEM_WORDS);
+    const int4 h = rec[0], rw = rec[1];
+    const int a = h.x, j0 = h.y, nrow = h.z, ntok = h.w;
+    const int rows[SHRINK_TOK] = {rw.x, rw.y, rw.z, rw.w};
 
     const uint16_t *Abase = A + ((size_t)a * r_max + j0) * (size_t)K;
-    float acc[SHRINK_J][SHRINK_TOK];
+    float acc[SHRINK_J * SHRINK_TOK];
 #pragma unroll
-    for (int j = 0; j < SHRINK_J; ++j)
-#pragma unroll
-      for (int t = 0; t < SHRINK_TOK; ++t) acc[j][t] = 0.f;
+    for (int i = 0; i < SHRINK_J * SHRINK_TOK; ++i) acc[i] = 0.f;
 
     for (int c = warp * 32 + lane; c < kchunks; c += SHRINK_THREADS) {
       float xf[SHRINK_TOK][8];
@@ -92,32 +93,18 @@ __global__ void __launch_bounds__(SHRINK_THREADS)
 #pragma unroll
           for (int t = 0; t < SHRINK_TOK; ++t)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[j][t] = fmaf(af[e], xf[t][e], acc[j][t]);
+            for (int e = 0; e < 8; ++e) acc[j * SHRINK_TOK + t] = fmaf(af[e], xf[t][e], acc[j * SHRINK_TOK + t]);
         }
       }
     }
-    // Warp sums (butterfly), then a fixed-order sum over warps.
-#pragma unroll
-    for (int j = 0; j < SHRINK_J; ++j)
-#pragma unroll
-      for (int t = 0; t < SHRINK_TOK; ++t) {
-        float v = acc[j][t];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        acc[j][t] = v;
-      }
-    if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < SHRINK_J; ++j)
-#pragma unroll
-        for (int t = 0; t < SHRINK_TOK; ++t) red[warp][j][t] = acc[j][t];
-    }
+    // Warp totals (lane l holds value l), then a fixed-order sum over warps.
+    red[warp][lane] = warp_transpose_sum(acc);
     __syncthreads();
     if (threadIdx.x < SHRINK_J * SHRINK_TOK) {
       const int j = threadIdx.x / SHRINK_TOK, t = threadIdx.x % SHRINK_TOK;
       float s = 0.f;
 #pragma unroll
-      for (int w = 0; w < SHRINK_WARPS; ++w) s += red[w][j][t];
+      for (int w = 0; w < SHRINK_WARPS; ++w) s += red[w][threadIdx.x];
       if (t < ntok) T[(size_t)rows[t] * t_stride + j0 + j] = (j < nrow) ? s : 0.f;
     }
     __syncthreads();
@@ -133,10 +120,11 @@ cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, in
   // Upper bound on work items: ceil(r_max/J) * (ceil(M/TOK) + min(M, n_ad)).
   const long long bound =
       (long long)((r_max + SHRINK_J - 1) / SHRINK_J) * ((M + SHRINK_TOK - 1) / SHRINK_TOK + min(M, n_ad));
+  (void)n_ad;
   const int grid = (int)max(1LL, min(bound, (long long)num_sms * 4));
-  shrink_kernel<<<grid, SHRINK_THREADS, 0, s>>>(x, M, K, A, n_ad, r_max, plan, T, t_stride);
-  note_launch();
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(shrink_kernel, dim3(grid), dim3(SHRINK_THREADS), 0, s, x, M, K, A, n_ad, r_max, plan, T,
+                             t_stride);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mlora

@@ -225,3 +225,32 @@ def test_full_size_sampled_outputs(cfg, k, projs):
             scale_ref = max(np.max(np.abs(e)), 1e-30)
             assert np.max(np.abs(yh[rows, cols] - e)) <= TOL * scale_ref, (cfg.name, p, name)
             assert np.isfinite(yh).all()
+
+
+def test_prefetch_weights_flag_gives_identical_bits():
+    ml = needs_gpu()
+    x, W, A, B, rk, idx = _random_case(9, 128, 1024, 4096, 16, (16,) * 16, r_max=16)
+    for mode in (ml.DRAFT, ml.VERIFY):
+        y0 = _run(ml, x, W, A, B, rk, idx, 2.0, mode)
+        y1 = _run(ml, x, W, A, B, rk, idx, 2.0, mode | ml.PREFETCH_WEIGHTS)
+        assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
+def test_back_to_back_projections_on_one_stream():
+    """Calls that follow one another on a stream overlap their prologues
+    (programmatic dependent launch); each still sees its predecessor's output."""
+    ml = needs_gpu()
+    g = np.random.default_rng(10)
+    M, K = 64, 1024
+    Ws = [WL.bf16_bits((g.standard_normal((K, K)) / np.sqrt(K)).astype(np.float32)) for _ in range(4)]
+    x = WL.bf16_bits(g.standard_normal((M, K)).astype(np.float32))
+    ws = ml.Workspace(ml.linear_workspace_bytes(M, K, K, 1))
+    h = dev_bf16(x)
+    Wd = [dev_bf16(Wb) for Wb in Ws]
+    for Wt in Wd:  # y_{i+1} = W_i y_i, each call reading the previous call's output
+        h = ml.linear(h, Wt, None, None, None, None, 1.0, ml.DRAFT | ml.PREFETCH_WEIGHTS, ws=ws)
+    ref = WL.bf16_to_f64(x)
+    for Wb in Ws:
+        ref, _ = OL.mlora_linear(ref, WL.bf16_to_f64(Wb), None, None, None, None, 1.0, OL.DRAFT)
+        ref = WL.bf16_to_f64(WL.bf16_bits(ref.astype(np.float32)))  # the next layer reads bf16 activations
+    assert _rel_err(host_bf16_to_f64(h), ref) <= 2e-2
