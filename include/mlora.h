@@ -185,6 +185,28 @@ MLORA_API mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlo
                           float scale, int mode, mlora_bf16 *y, void *workspace, size_t ws_bytes,
                           mlora_stream stream);
 
+/* Allocation-free variant of mlora_linear.  The paper has no counterpart;
+ * this is for callers that cannot allocate device memory for a workspace (a
+ * plugin inside a host framework that owns every device buffer, or code
+ * whose device memory budget is fixed at start-up and must not call
+ * cudaMalloc).  Same arguments and results as mlora_linear, minus the plan
+ * pointer and the workspace: the scratch (segment plan, low-rank activations
+ * and status word) lives in one 512 KB array compiled into the library, which
+ * every GPU that loads the library holds until the process exits.
+ *   Limits: M <= 1024 rows and, in verify mode, n_adapters <= 256; larger
+ *   sizes return MLORA_ERR_SHAPE and launch nothing.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current and keeps it; make that
+ *   first call before any stream capture.
+ *   It calls no allocating routine.  All calls share the array: calls whose
+ *   work overlaps on the GPU (e.g. on two streams) race.  Device status bits
+ *   (bad adapter index or rank) still select the same fallback but are not
+ *   reported by this variant. */
+MLORA_API mlora_status mlora_linear_noalloc(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W, int N,
+                                            const mlora_bf16 *A_stack, const mlora_bf16 *B_stack, int n_adapters,
+                                            int r_max, const int32_t *rank_of, const int32_t *adapter_idx,
+                                            float scale, int mode, mlora_bf16 *y, mlora_stream stream);
+
 /* ------------------------------------------------------------------------- */
 /* Accept / resample (steps a5-a6)                                            */
 /* ------------------------------------------------------------------------- */

@@ -27,6 +27,10 @@ DRAFT = 0
 VERIFY = 1
 PREFETCH_WEIGHTS = 0x100  # mode flag: W is constant; may be streamed before the preceding kernel ends
 
+# Limits of mlora_linear_noalloc (its scratch is a fixed array in the library).
+NOALLOC_MAX_ROWS = 1024
+NOALLOC_MAX_ADAPTERS = 256
+
 DEV_BAD_ADAPTER = 1 << 0
 DEV_BAD_RANK = 1 << 1
 DEV_BAD_PROB = 1 << 2
@@ -55,6 +59,8 @@ _SIGNATURES = {
                               _c_ptr, _c_ptr, _c_float, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr]),
     "mlora_verify_accept": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr, _c_ptr,
                                      _c_ptr, _c_size, _c_ptr]),
+    "mlora_linear_noalloc": (_c_int, [_c_ptr, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int,
+                                      _c_ptr, _c_ptr, _c_float, _c_int, _c_ptr, _c_ptr]),
     "mlora_status_string": (ctypes.c_char_p, [_c_int]),
     "mlora_device_supported": (_c_int, []),
     "mlora_launch_count": (ctypes.c_uint64, []),
@@ -246,3 +252,34 @@ def verify_accept(p: torch.Tensor, q: torch.Tensor, draft_tok: torch.Tensor, uni
                                      _need(accepted, "accepted", torch.int32, 1), ws.ptr, ws.nbytes, _stream(stream))
     _check(st, "verify_accept")
     return out_tok, accepted
+
+
+def linear_noalloc(x: torch.Tensor, W: torch.Tensor, A_stack, B_stack, rank_of, adapter_idx, scale: float, mode: int,
+                   y: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """mlora_linear_noalloc: the layer without a workspace, for callers that
+    cannot allocate device memory (the library's own fixed scratch array is
+    used instead; M <= NOALLOC_MAX_ROWS, n_adapters <= NOALLOC_MAX_ADAPTERS).
+    The output buffer `y` is the caller's; pass it to avoid the allocation
+    this wrapper would otherwise make for it."""
+    M, K = x.shape
+    N, K2 = W.shape
+    if K2 != K:
+        raise ValueError("W and x disagree on K")
+    verify = (mode & ~PREFETCH_WEIGHTS) == VERIFY
+    n_ad, r_max = 0, 0
+    a_ptr = b_ptr = r_ptr = i_ptr = None
+    if verify:
+        n_ad, r_max, K3 = A_stack.shape
+        if K3 != K or tuple(B_stack.shape) != (n_ad, N, r_max):
+            raise ValueError("A_stack [n_ad, r_max, K] / B_stack [n_ad, N, r_max] shapes disagree")
+        a_ptr = _need(A_stack, "A_stack", torch.bfloat16, 3)
+        b_ptr = _need(B_stack, "B_stack", torch.bfloat16, 3)
+        r_ptr = _need(rank_of, "rank_of", torch.int32, 1)
+        i_ptr = _need(adapter_idx, "adapter_idx", torch.int32, 1)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    st = _load().mlora_linear_noalloc(_need(x, "x", torch.bfloat16, 2), M, K, _need(W, "W", torch.bfloat16, 2), N,
+                                      a_ptr, b_ptr, n_ad, r_max, r_ptr, i_ptr, float(scale), int(mode),
+                                      _need(y, "y", torch.bfloat16, 2), _stream(stream))
+    _check(st, "linear_noalloc")
+    return y
