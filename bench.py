@@ -347,26 +347,7 @@ def run_gpu(args):
     if wl.ws.status() != 0:
         raise RuntimeError("device status bits raised during the timed region")
 
-    # Per-op durations: each op of the step captured as its own graph, replayed
-    # back to back with CUDA events between them on the launching stream.
-    op_graphs = []
-    for name, fn in wl.ops():
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            fn()
-        op_graphs.append((name, g))
-    torch.cuda.synchronize()
-    reps = max(10, min(args.steps, 200))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(op_graphs) + 1)] for _ in range(reps)]
-    with torch.cuda.stream(stream):
-        for r in range(reps):
-            evs[r][0].record(stream)
-            for i, (_, g) in enumerate(op_graphs):
-                g.replay()
-                evs[r][i + 1].record(stream)
-    torch.cuda.synchronize()
-    op_ms = {name: float(np.median([evs[r][i].elapsed_time(evs[r][i + 1]) for r in range(reps)]))
-             for i, (name, _) in enumerate(op_graphs)}
+    op_ms, timing_kind = per_op_durations(torch, wl, stream, args)
 
     # Algorithmic work.
     hbm_gbs, bf16_tf, peak_kind = _peaks()
@@ -403,6 +384,7 @@ def run_gpu(args):
                    "GBps": acc_b / (op_ms["accept"] * 1e-3) / 1e9,
                    "mean_accepted": float(acc_host.mean())},
         "plan_us": 1e3 * op_ms["plan"],
+        "per_op_timing": timing_kind,
         "per_op_us": {k: 1e3 * v for k, v in op_ms.items()},
     }
 
@@ -448,6 +430,50 @@ def run_gpu(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def per_op_durations(torch, wl, stream, args):
+    """Median duration of every op of the step, from CUDA events on the
+    launching stream.  Preferred: one step graph with an event node between
+    consecutive ops (external events), replayed and read back step by step.
+    Fallback: each op in its own graph, replayed back to back."""
+    ops = wl.ops()
+    reps = max(10, min(args.steps, 200))
+    try:
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(ops) + 1)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            evs[0].record(stream)
+            for i, (_, fn) in enumerate(ops):
+                fn()
+                evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        samples = [[] for _ in ops]
+        for _ in range(reps):
+            g.replay()
+            torch.cuda.synchronize()
+            for i in range(len(ops)):
+                samples[i].append(evs[i].elapsed_time(evs[i + 1]))
+        return {name: float(np.median(samples[i])) for i, (name, _) in enumerate(ops)}, "events inside the step graph"
+    except Exception:
+        pass
+    op_graphs = []
+    for name, fn in ops:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        op_graphs.append((name, g))
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(op_graphs) + 1)] for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for r in range(reps):
+            evs[r][0].record(stream)
+            for i, (_, g) in enumerate(op_graphs):
+                g.replay()
+                evs[r][i + 1].record(stream)
+    torch.cuda.synchronize()
+    return ({name: float(np.median([evs[r][i].elapsed_time(evs[r][i + 1]) for r in range(reps)]))
+             for i, (name, _) in enumerate(op_graphs)}, "one graph per op")
 
 
 def run_e2e(torch, ml, wl, stream, args, world):

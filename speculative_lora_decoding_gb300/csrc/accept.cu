@@ -29,7 +29,6 @@ namespace mlora {
 constexpr int ACC_THREADS = 256;
 constexpr int ACC_WARPS = ACC_THREADS / 32;
 constexpr int MIN_SLICE = 4096;
-constexpr float TWO_POW_40 = 1099511627776.0f;
 constexpr float TWO_POW_32 = 4294967296.0f;
 
 __device__ __forceinline__ float sanitize_prob(float f, uint32_t &flags) {
@@ -56,9 +55,20 @@ __device__ __forceinline__ float sanitize_uniform(float u, uint32_t &flags) {
   return u;
 }
 
-// Q(f) = floor(f * 2^40) for f in [0, 1]: the scaling is exact in fp32 and
-// the truncating conversion is the floor.
-__device__ __forceinline__ uint64_t fixq(float f) { return __float2ull_rz(f * TWO_POW_40); }
+// Q(f) = floor(f * 2^40) for f in [0, 1], from the IEEE-754 fields: a normal
+// f is (2^23 + mantissa) * 2^(exponent - 150), so Q(f) is that 24-bit integer
+// shifted left by (exponent - 110) or, for smaller exponents, right by
+// (110 - exponent) (the right shift is the floor).  Below 2^-40 the result
+// is 0; subnormals are far below that.  Integer operations only.
+__device__ __forceinline__ uint64_t fixq(float f) {
+  const uint32_t bits = __float_as_uint(f);
+  const int e = (int)(bits >> 23) & 0xFF;
+  const uint64_t m = (uint64_t)((bits & 0x7FFFFFu) | 0x800000u);
+  const int sh = e - 110;
+  if (sh >= 0) return m << sh;  // e <= 127 for f <= 1, so sh <= 17
+  if (sh <= -24) return 0ull;
+  return m >> (-sh);
+}
 
 struct Weights {
   uint64_t res, tgt;

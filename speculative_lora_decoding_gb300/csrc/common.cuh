@@ -40,7 +40,7 @@ __host__ __device__ inline size_t max_shrink_items(int M, int n_ad) {
 
 // Plan layout inside scratch (int32 words), for M rows and n_ad adapters.
 struct PlanLayout {
-  size_t hdr;         // [0] n_active, [1] total shrink items, [2] rows
+  size_t hdr;         // [0] n_active, [1] total shrink items, [2] rows, [3] largest active rank
   size_t seg_offsets; // [n_ad + 2]
   size_t perm;        // [M]
   size_t row_adapter; // [M]   validated adapter per row (-1: none)
@@ -106,14 +106,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// Test the phase; if it is not complete the thread may be suspended (it does
+// not take issue slots) for up to MBAR_SUSPEND_NS or until the phase completes.
+constexpr uint32_t MBAR_SUSPEND_NS = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(MBAR_SUSPEND_NS)
       : "memory");
   return done != 0;
 }
@@ -289,6 +293,20 @@ __device__ __forceinline__ void grid_launch_dependents() {
 // Named barrier over `nthreads` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ANDs a predicate over its `nthreads` threads.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }

@@ -46,12 +46,13 @@ constexpr int MAX_MB = 512;
 constexpr int CHUNK = 32;                             // accumulator columns per reduction round
 constexpr int RED_BYTES = 2 * CHUNK * BLOCK_N * 4;    // double-buffered reduction tile, 32 KB
 constexpr int MAX_CLUSTER = 16;
+constexpr int MAX_ACC = 1;                            // tensor-memory accumulators per unit
 constexpr size_t SMEM_LIMIT = 227 * 1024;
 constexpr size_t SMEM_FIXED = 1024 + 256;             // alignment slack + barriers
 
 struct GemmArgs {
   int M, N, K;
-  int Mb, nsub, sub_n, n_tgroups, kblocks, C, stages, tmem_cols, red_bytes;
+  int Mb, nsub, sub_n, n_tgroups, kblocks, C, stages, tmem_cols, red_bytes, nacc;
   int mode, prefetch_w;
   float scale;
   uint16_t *y;
@@ -95,54 +96,179 @@ __device__ __forceinline__ void unpack_bf16x2(uint32_t w, float &lo, float &hi) 
   hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
-// B_a[n, 0:64] as packed bf16 pairs; entries at or past rank r are zeroed
-// (the padding is never used, even if it holds NaN).
-__device__ __forceinline__ void load_brow(const GemmArgs &a, int ad, int n, int r, uint32_t (&bp)[32]) {
+// Accumulator columns [taddr, taddr + 32) summed over the first nacc
+// accumulators (stride columns apart), in accumulator order.
+__device__ __forceinline__ void tmem_ld_acc_x32(uint32_t taddr, int nacc, int stride, uint32_t (&r)[32]) {
+  tmem_ld_x32(taddr, r);
+  tmem_ld_wait();
+  for (int a = 1; a < nacc; ++a) {
+    uint32_t t[32];
+    tmem_ld_x32(taddr + (uint32_t)(a * stride), t);
+    tmem_ld_wait();
 #pragma unroll
-  for (int i = 0; i < 32; ++i) bp[i] = 0u;
-  if (r <= 0 || n >= a.N) return;
-  const uint4 *brow = reinterpret_cast<const uint4 *>(a.B_stack + ((size_t)ad * a.N + n) * a.r_max);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    if (q * 8 < r) {
-      const uint4 v = __ldg(brow + q);
-      bp[4 * q + 0] = v.x;
-      bp[4 * q + 1] = v.y;
-      bp[4 * q + 2] = v.z;
-      bp[4 * q + 3] = v.w;
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    if (2 * e >= r) bp[e] &= 0xFFFF0000u;
-    if (2 * e + 1 >= r) bp[e] &= 0x0000FFFFu;
+    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(t[j]));
   }
 }
 
-// sum_{j < r} T[m, j] * B[j], fp32, j in increasing order.
-__device__ __forceinline__ float lowrank_dot(const float *T, int m, const uint32_t (&bp)[32], int r) {
-  const float4 *trow = reinterpret_cast<const float4 *>(T + (size_t)m * T_STRIDE);
-  float dot = 0.f;
+// Tables the verify epilogue reads for every output: the plan's buckets
+// (adapter, first and last sorted position, rank), its permutation and the
+// rows of T.  Staged into shared memory (the freed stage ring) when the unit
+// holds every token row and they fit; otherwise read from global memory.
+struct VerifyTables {
+  const int4 *bk;       // staged buckets, or nullptr
+  const int32_t *perm;  // permutation
+  const float *T;       // T rows: row m at T + (m - t_row0) * t_stride
+  int t_row0, t_stride, nbk;
+};
+
+__device__ __forceinline__ VerifyTables stage_verify_tables(const GemmArgs &a, const PlanLayout &L, uint8_t *base,
+                                                            size_t avail, int m0, int mcount, int et) {
+  const int32_t *plan = a.plan;
+  const int n_active = plan[L.hdr + 0];
+  const int rmax = plan[L.hdr + 3];
+  const int rs = max(8, (rmax + 7) & ~7);
+  VerifyTables v;
+  v.bk = nullptr;
+  v.perm = plan + L.perm;
+  v.T = a.T;
+  v.t_row0 = 0;
+  v.t_stride = T_STRIDE;
+  v.nbk = n_active + 1;
+  const size_t t_bytes = align_up((size_t)mcount * rs * 4, 16);
+  const size_t p_bytes = align_up((size_t)a.M * 4, 16);
+  const size_t need = t_bytes + p_bytes + (size_t)(n_active + 1) * 16;
+  if (!(m0 == 0 && mcount == a.M) || need > avail) return v;
+  float *sT = reinterpret_cast<float *>(base);
+  int32_t *sp = reinterpret_cast<int32_t *>(base + t_bytes);
+  int4 *sb = reinterpret_cast<int4 *>(base + t_bytes + p_bytes);
+  for (int e = et; e < mcount * rs; e += 128) sT[e] = a.T[(size_t)(m0 + e / rs) * T_STRIDE + e % rs];
+  for (int e = et; e < a.M; e += 128) sp[e] = plan[L.perm + e];
+  for (int i = et; i <= n_active; i += 128) {
+    const int b = (i < n_active) ? plan[L.active + i] : a.n_ad;
+    const int r = (b < a.n_ad) ? plan[L.rank_eff + b] : 0;
+    sb[i] = make_int4(b, plan[L.seg_offsets + b], plan[L.seg_offsets + b + 1], r);
+  }
+  named_bar_sync(1, 128);
+  v.bk = sb;
+  v.perm = sp;
+  v.T = sT;
+  v.t_row0 = m0;
+  v.t_stride = rs;
+  return v;
+}
+
+__device__ __forceinline__ int4 bucket_at(const GemmArgs &a, const PlanLayout &L, const VerifyTables &v, int i) {
+  if (v.bk) return v.bk[i];
+  const int32_t *plan = a.plan;
+  const int n_active = v.nbk - 1;
+  const int b = (i < n_active) ? plan[L.active + i] : a.n_ad;
+  const int r = (b < a.n_ad) ? plan[L.rank_eff + b] : 0;
+  return make_int4(b, plan[L.seg_offsets + b], plan[L.seg_offsets + b + 1], r);
+}
+
+// The verify bucket walk.  Each thread owns one output row n and, per bucket
+// (adapter a, sorted positions [s0, s1), rank r), stages its masked row
+// B_a[n, 0:r] into shared memory (one 16-byte slot per 8 ranks, transposed so
+// that lanes touch consecutive slots), then finishes its share of the
+// bucket's columns four at a time:
+//   y[m, n] = bf16(acc[m, n] + scale * sum_{j<r} T[m, j] * B_a[n, j]).
+// The value acc comes from tensor memory (summed over the accumulators) or,
+// after a cluster reduction, from shared memory (fin, column-major [Mb][R]).
+// The loops over rank chunks stay rolled to keep the code small.
+template <bool FROM_TMEM>
+__device__ __forceinline__ void verify_walk(const GemmArgs &a, const PlanLayout &L, const VerifyTables &vt, uint4 *Bs,
+                                            int et, int n, int m0, int mcount, int first, int step, uint32_t taddr,
+                                            int nacc, const float *fin, int R, int i_row) {
+  for (int ai = 0; ai < vt.nbk; ++ai) {
+    const int4 bk = bucket_at(a, L, vt, ai);
+    const int s0 = bk.y, s1 = bk.z, r = bk.w;
+    if (s0 == s1) continue;
+    const int nq = (r + 7) >> 3;
+    if (r > 0 && n < a.N) {
+      const uint4 *brow = reinterpret_cast<const uint4 *>(a.B_stack + ((size_t)bk.x * a.N + n) * a.r_max);
+#pragma unroll 1
+      for (int q = 0; q < nq; ++q) {
+        uint4 v = __ldg(brow + q);
+        if (q * 8 + 8 > r) {
+          uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    if (q * 8 < r) {
-      const float4 t0 = __ldg(trow + 2 * q), t1 = __ldg(trow + 2 * q + 1);
-      float b0, b1, b2, b3, b4, b5, b6, b7;
-      unpack_bf16x2(bp[4 * q + 0], b0, b1);
-      unpack_bf16x2(bp[4 * q + 1], b2, b3);
-      unpack_bf16x2(bp[4 * q + 2], b4, b5);
-      unpack_bf16x2(bp[4 * q + 3], b6, b7);
-      dot = fmaf(t0.x, b0, dot);
-      dot = fmaf(t0.y, b1, dot);
-      dot = fmaf(t0.z, b2, dot);
-      dot = fmaf(t0.w, b3, dot);
-      dot = fmaf(t1.x, b4, dot);
-      dot = fmaf(t1.y, b5, dot);
-      dot = fmaf(t1.z, b6, dot);
-      dot = fmaf(t1.w, b7, dot);
+          for (int e = 0; e < 4; ++e) {
+            if (q * 8 + 2 * e >= r) w[e] &= 0xFFFF0000u;
+            if (q * 8 + 2 * e + 1 >= r) w[e] &= 0x0000FFFFu;
+          }
+          v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        Bs[q * 128 + et] = v;
+      }
+    }
+#pragma unroll 1
+    for (int i = s0 + first; i < s1; i += 4 * step) {
+      int mm[4];
+      float val[4];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int idx = i + jj * step;
+        int m = idx < s1 ? vt.perm[idx] : -1;
+        if (m < m0 || m >= m0 + mcount) m = -1;
+        mm[jj] = m;
+        val[jj] = 0.f;
+      }
+      if (FROM_TMEM) {
+        uint32_t own[4];
+#pragma unroll 1
+        for (int ac = 0; ac < nacc; ++ac) {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            own[jj] = 0u;
+            if (mm[jj] >= 0) tmem_ld_x1(taddr + (uint32_t)(ac * a.Mb + mm[jj] - m0), own[jj]);
+          }
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) val[jj] = (ac == 0) ? __uint_as_float(own[jj]) : val[jj] + __uint_as_float(own[jj]);
+        }
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+          if (mm[jj] >= 0) val[jj] = fin[(mm[jj] - m0) * R + i_row];
+      }
+      if (r > 0) {
+        float dot[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int q = 0; q < nq; ++q) {
+          const uint4 bv = Bs[q * 128 + et];
+          float b0, b1, b2, b3, b4, b5, b6, b7;
+          unpack_bf16x2(bv.x, b0, b1);
+          unpack_bf16x2(bv.y, b2, b3);
+          unpack_bf16x2(bv.z, b4, b5);
+          unpack_bf16x2(bv.w, b6, b7);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            if (mm[jj] >= 0) {
+              const float4 *trow = reinterpret_cast<const float4 *>(vt.T + (size_t)(mm[jj] - vt.t_row0) * vt.t_stride) + 2 * q;
+              const float4 t0 = trow[0], t1 = trow[1];
+              float d = dot[jj];
+              d = fmaf(t0.x, b0, d);
+              d = fmaf(t0.y, b1, d);
+              d = fmaf(t0.z, b2, d);
+              d = fmaf(t0.w, b3, d);
+              d = fmaf(t1.x, b4, d);
+              d = fmaf(t1.y, b5, d);
+              d = fmaf(t1.z, b6, d);
+              d = fmaf(t1.w, b7, d);
+              dot[jj] = d;
+            }
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) val[jj] = fmaf(a.scale, dot[jj], val[jj]);
+      }
+      if (n < a.N) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+          if (mm[jj] >= 0) a.y[(size_t)mm[jj] * a.N + n] = float_to_bf16_bits(val[jj]);
+      }
     }
   }
-  return dot;
 }
 
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
@@ -258,13 +384,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tc_fence_after_sync();
         const uint32_t a_addr = smem_addr(sp.stage0 + (size_t)stage * stage_bytes);
         const uint32_t b_addr = a_addr + W_TILE_BYTES;
+        // The four 16-wide K steps of a stage take turns over nacc
+        // accumulators, so consecutive MMAs do not wait on each other's result.
 #pragma unroll
         for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
+          const int acc = kk % args.nacc;
           const uint64_t adesc = smem_desc_kmajor_sw128(a_addr + kk * 32);
           for (int s = 0; s < args.nsub; ++s) {
             const uint64_t bdesc = smem_desc_kmajor_sw128(b_addr + s * args.sub_n * BLOCK_K * 2 + kk * 32);
-            mma_bf16_ss(tmem_base + (uint32_t)(s * args.sub_n), adesc, bdesc, idesc,
-                        (kb > kb_lo || kk > 0) ? 1u : 0u);
+            mma_bf16_ss(tmem_base + (uint32_t)(acc * args.Mb + s * args.sub_n), adesc, bdesc, idesc,
+                        (kb > kb_lo || kk >= args.nacc) ? 1u : 0u);
           }
         }
         issued_any = true;
@@ -297,11 +426,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (epi) {
     have_acc = mbar_wait_bounded(sp.tfull, 0, abort_flag);
     if (!have_acc) signal_abort(sp, args.status);
+    __syncwarp();
+    have_acc = named_bar_and(1, 128, have_acc);  // one decision for all four epilogue warps
     tc_fence_after_sync();
     grid_dependency_wait();  // the plan and T come from kernels earlier in the stream
   }
   const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
   const int nchunks = (mcount + CHUNK - 1) / CHUNK;
+  const int nacc_eff = kb_hi > kb_lo ? args.nacc : 1;  // every accumulator gets a K step of each k-block
 
   const bool verify = args.mode == MLORA_VERIFY;
 
@@ -311,8 +443,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!verify) {
         for (int ch = 0; ch < nchunks; ++ch) {
           uint32_t r[32];
-          tmem_ld_x32(taddr + ch * CHUNK, r);
-          tmem_ld_wait();
+          tmem_ld_acc_x32(taddr + ch * CHUNK, nacc_eff, args.Mb, r);
           if (n < args.N) {
 #pragma unroll
             for (int j = 0; j < CHUNK; ++j) {
@@ -322,36 +453,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       } else {
-        // Walk the plan's buckets: one B row load per (adapter, output row),
-        // accumulator columns fetched from tensor memory eight at a time.
-        const int32_t *plan = args.plan;
-        const int n_active = plan[L.hdr + 0];
-        for (int ai = 0; ai <= n_active; ++ai) {
-          const int b = (ai < n_active) ? plan[L.active + ai] : args.n_ad;
-          const int s0 = plan[L.seg_offsets + b], s1 = plan[L.seg_offsets + b + 1];
-          if (s0 == s1) continue;
-          const int r = (b < args.n_ad) ? plan[L.rank_eff + b] : 0;
-          uint32_t bp[32];
-          load_brow(args, b, n, r, bp);
-          for (int i = s0; i < s1; i += 8) {
-            int mm[8];
-            uint32_t own[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              mm[j] = (i + j < s1) ? plan[L.perm + i + j] : -1;
-              own[j] = 0u;
-              if (mm[j] >= m0 && mm[j] < m0 + mcount) tmem_ld_x1(taddr + (uint32_t)(mm[j] - m0), own[j]);
-            }
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (mm[j] < m0 || mm[j] >= m0 + mcount) continue;
-              float v = __uint_as_float(own[j]);
-              if (r > 0) v = fmaf(args.scale, lowrank_dot(args.T, mm[j], bp, r), v);
-              if (n < args.N) args.y[(size_t)mm[j] * args.N + n] = float_to_bf16_bits(v);
-            }
-          }
-        }
+        // Walk the plan's buckets (see verify_walk); the B-row slots sit at
+        // the start of the freed stage ring, the staged tables after them.
+        uint4 *Bs = reinterpret_cast<uint4 *>(sp.stage0);
+        const size_t bs_bytes = 8 * 128 * sizeof(uint4);
+        const VerifyTables vt =
+            stage_verify_tables(args, L, sp.stage0 + bs_bytes, (size_t)S * stage_bytes - bs_bytes, m0, mcount, et);
+        verify_walk<true>(args, L, vt, Bs, et, n, m0, mcount, 0, 1, taddr, nacc_eff, nullptr, 0, 0);
       }
     }
     tc_fence_before_sync();
@@ -371,8 +479,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (epi) {
         uint32_t r[32];
         if (have_acc) {
-          tmem_ld_x32(taddr + ch * CHUNK, r);
-          tmem_ld_wait();
+          tmem_ld_acc_x32(taddr + ch * CHUNK, nacc_eff, args.Mb, r);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = 0u;
@@ -406,29 +513,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     if (verify && epi) {
       named_bar_sync(1, 128);
+      // Stage ring after the reduction: fin, then the B-row slots, then the
+      // staged tables when they fit.
+      const size_t fin_bytes = align_up((size_t)args.Mb * R * 4, 16);
+      uint4 *Bs = reinterpret_cast<uint4 *>(sp.stage0 + fin_bytes);
+      const size_t used = fin_bytes + 8 * 128 * sizeof(uint4);
+      const VerifyTables vt =
+          stage_verify_tables(args, L, sp.stage0 + used, (size_t)S * stage_bytes - used, m0, mcount, et);
       // Threads split as (row i, column phase): 128 / R threads share a row.
       const int P = 128 / R;
       const int i = et % R, sub = et / R;
-      const int n = n_tile * BLOCK_N + r0 + i;
-      const int32_t *plan = args.plan;
-      const int n_active = plan[L.hdr + 0];
-      if (sub < P) {
-        for (int ai = 0; ai <= n_active; ++ai) {
-          const int b = (ai < n_active) ? plan[L.active + ai] : args.n_ad;
-          const int s0 = plan[L.seg_offsets + b], s1 = plan[L.seg_offsets + b + 1];
-          if (s0 == s1) continue;
-          const int r = (b < args.n_ad) ? plan[L.rank_eff + b] : 0;
-          uint32_t bp[32];
-          load_brow(args, b, n, r, bp);
-          for (int idx = s0 + sub; idx < s1; idx += P) {
-            const int m = plan[L.perm + idx];
-            if (m < m0 || m >= m0 + mcount) continue;
-            float v = fin[(m - m0) * R + i];
-            if (r > 0) v = fmaf(args.scale, lowrank_dot(args.T, m, bp, r), v);
-            if (n < args.N) args.y[(size_t)m * args.N + n] = float_to_bf16_bits(v);
-          }
-        }
-      }
+      verify_walk<false>(args, L, vt, Bs, et, n_tile * BLOCK_N + r0 + i, m0, mcount, sub, P, 0u, 1, fin, R, i);
     }
     tc_fence_before_sync();
     cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
@@ -514,9 +609,14 @@ GemmShape gemm_shape(int M, int N, int K, int num_sms) {
   s.n_tgroups = tg;
   s.n_units = ((N + BLOCK_N - 1) / BLOCK_N) * tg;
   s.kblocks = (K + BLOCK_K - 1) / BLOCK_K;
+  // Up to four accumulators (the K steps of a stage take turns) while they
+  // fit in the 512 tensor-memory columns.
   int cols = 32;
   while (cols < Mb) cols <<= 1;
-  s.tmem_cols = cols;
+  int nacc = 1;
+  while (nacc < MAX_ACC && 2 * nacc * cols <= 512) nacc *= 2;
+  s.nacc = nacc;
+  s.tmem_cols = nacc * cols;
   s.nbuf = 1;
   s.total_iters = s.n_units * s.kblocks;
   // Split-K factor (a power of two, so each CTA owns 128 / C output rows):
@@ -607,6 +707,7 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
   a.C = sh.C;
   a.stages = sh.stages;
   a.tmem_cols = sh.tmem_cols;
+  a.nacc = sh.nacc;
   a.red_bytes = sh.red_bytes;
   a.mode = g.mode;
   a.prefetch_w = g.prefetch_w;

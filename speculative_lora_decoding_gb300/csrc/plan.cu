@@ -61,11 +61,15 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
   int *running = sh_dyn + n_ad + 1;  // [n_ad + 1]
   __shared__ int scan_sh[33];
   __shared__ uint32_t flags;
+  __shared__ int max_rank;
 
   const PlanLayout L = plan_layout(M, n_ad);
   const int tid = threadIdx.x;
   const int nb = n_ad + 1;
-  if (tid == 0) flags = 0;
+  if (tid == 0) {
+    flags = 0;
+    max_rank = 0;
+  }
   for (int b = tid; b < nb; b += PLAN_THREADS) {
     cnt[b] = 0;
     running[b] = 0;
@@ -113,15 +117,17 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
   // Active adapters (rows > 0) and the shrink work list over them.
   {
     const int a0 = min(tid * per, n_ad), a1 = min(a0 + per, n_ad);
-    int nact = 0, nitems = 0;
+    int nact = 0, nitems = 0, rmax = 0;
     for (int a = a0; a < a1; ++a) {
       const int c = running[a];
       if (c > 0) {
         ++nact;
         const int r = plan[L.rank_eff + a];
+        rmax = max(rmax, r);
         nitems += ((r + SHRINK_J - 1) / SHRINK_J) * ((c + SHRINK_TOK - 1) / SHRINK_TOK);
       }
     }
+    if (rmax > 0) atomicMax(&max_rank, rmax);
     int tot_act, tot_items;
     int pa = block_excl_scan(nact, scan_sh, &tot_act);
     int pi = block_excl_scan(nitems, scan_sh, &tot_items);
@@ -142,6 +148,8 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
       plan[L.hdr + 2] = M;
     }
   }
+  __syncthreads();
+  if (tid == 0) plan[L.hdr + 3] = max_rank;
   __syncthreads();
   for (int b = tid; b < nb; b += PLAN_THREADS) running[b] = 0;
   __syncthreads();
