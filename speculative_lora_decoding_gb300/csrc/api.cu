@@ -171,6 +171,7 @@ mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W
   g.K = K;
   g.mode = base_mode;
   g.prefetch_w = prefetch_w;
+  g.after_shrink = verify ? 1 : 0;
   g.scale = scale;
   g.y = y;
   g.B_stack = B_stack;

@@ -295,6 +295,11 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrive on named barrier `id` without waiting (the waiters use bar.sync).
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Named barrier that also ANDs a predicate over its `nthreads` threads.
 __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
   uint32_t r;

@@ -47,13 +47,14 @@ constexpr int CHUNK = 32;                             // accumulator columns per
 constexpr int RED_BYTES = 2 * CHUNK * BLOCK_N * 4;    // double-buffered reduction tile, 32 KB
 constexpr int MAX_CLUSTER = 16;
 constexpr int MAX_ACC = 1;                            // tensor-memory accumulators per unit
-constexpr size_t SMEM_LIMIT = 227 * 1024;
+constexpr size_t SMEM_LIMIT = 220 * 1024;             // leaves room for a co-resident shrink CTA
 constexpr size_t SMEM_FIXED = 1024 + 256;             // alignment slack + barriers
 
 struct GemmArgs {
   int M, N, K;
   int Mb, nsub, sub_n, n_tgroups, kblocks, C, stages, tmem_cols, red_bytes, nacc;
   int mode, prefetch_w;
+  int after_shrink;  // launched right after this library's shrink kernel: x and W are ready
   float scale;
   uint16_t *y;
   const uint16_t *B_stack;
@@ -69,6 +70,7 @@ struct SmemPtrs {
   uint64_t *full, *empty, *tfull, *drain;
   uint32_t *tmem_slot;
   int *abort_flag;
+  int *acc_ready;
 };
 
 __device__ __forceinline__ SmemPtrs carve_smem(uint8_t *base, int stages, int stage_bytes, int red_bytes) {
@@ -83,6 +85,7 @@ __device__ __forceinline__ SmemPtrs carve_smem(uint8_t *base, int stages, int st
   uint32_t *w = reinterpret_cast<uint32_t *>(bars + 2 * stages + 2);
   p.tmem_slot = w;
   p.abort_flag = reinterpret_cast<int *>(w + 1);
+  p.acc_ready = reinterpret_cast<int *>(w + 2);
   return p;
 }
 
@@ -119,6 +122,7 @@ struct VerifyTables {
   const int32_t *perm;  // permutation
   const float *T;       // T rows: row m at T + (m - t_row0) * t_stride
   int t_row0, t_stride, nbk;
+  size_t bytes;         // shared memory the staged tables occupy (0: not staged)
 };
 
 __device__ __forceinline__ VerifyTables stage_verify_tables(const GemmArgs &a, const PlanLayout &L, uint8_t *base,
@@ -134,6 +138,7 @@ __device__ __forceinline__ VerifyTables stage_verify_tables(const GemmArgs &a, c
   v.t_row0 = 0;
   v.t_stride = T_STRIDE;
   v.nbk = n_active + 1;
+  v.bytes = 0;
   const size_t t_bytes = align_up((size_t)mcount * rs * 4, 16);
   const size_t p_bytes = align_up((size_t)a.M * 4, 16);
   const size_t need = t_bytes + p_bytes + (size_t)(n_active + 1) * 16;
@@ -141,7 +146,21 @@ __device__ __forceinline__ VerifyTables stage_verify_tables(const GemmArgs &a, c
   float *sT = reinterpret_cast<float *>(base);
   int32_t *sp = reinterpret_cast<int32_t *>(base + t_bytes);
   int4 *sb = reinterpret_cast<int4 *>(base + t_bytes + p_bytes);
-  for (int e = et; e < mcount * rs; e += 128) sT[e] = a.T[(size_t)(m0 + e / rs) * T_STRIDE + e % rs];
+  // Four loads in flight per thread before their stores.
+  const int nt = mcount * rs;
+#pragma unroll 1
+  for (int e0 = et; e0 < nt; e0 += 4 * 128) {
+    float v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = e0 + k * 128;
+      v[k] = e < nt ? a.T[(size_t)(m0 + e / rs) * T_STRIDE + e % rs] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (e0 + k * 128 < nt) sT[e0 + k * 128] = v[k];
+  }
+#pragma unroll 4
   for (int e = et; e < a.M; e += 128) sp[e] = plan[L.perm + e];
   for (int i = et; i <= n_active; i += 128) {
     const int b = (i < n_active) ? plan[L.active + i] : a.n_ad;
@@ -154,6 +173,7 @@ __device__ __forceinline__ VerifyTables stage_verify_tables(const GemmArgs &a, c
   v.T = sT;
   v.t_row0 = m0;
   v.t_stride = rs;
+  v.bytes = align_up(need, 16);
   return v;
 }
 
@@ -166,108 +186,152 @@ __device__ __forceinline__ int4 bucket_at(const GemmArgs &a, const PlanLayout &L
   return make_int4(b, plan[L.seg_offsets + b], plan[L.seg_offsets + b + 1], r);
 }
 
-// The verify bucket walk.  Each thread owns one output row n and, per bucket
-// (adapter a, sorted positions [s0, s1), rank r), stages its masked row
-// B_a[n, 0:r] into shared memory (one 16-byte slot per 8 ranks, transposed so
-// that lanes touch consecutive slots), then finishes its share of the
-// bucket's columns four at a time:
+// The verify bucket walk.  Each thread owns one output row n and, for a group
+// of buckets (adapter a, sorted positions [s0, s1), rank r), stages its masked
+// rows B_a[n, 0:r] into shared memory (one 16-byte slot per 8 ranks,
+// transposed so that lanes touch consecutive slots) in one round of loads,
+// then finishes its share of each bucket's columns four at a time:
 //   y[m, n] = bf16(acc[m, n] + scale * sum_{j<r} T[m, j] * B_a[n, j]).
 // The value acc comes from tensor memory (summed over the accumulators) or,
 // after a cluster reduction, from shared memory (fin, column-major [Mb][R]).
 // The loops over rank chunks stay rolled to keep the code small.
 template <bool FROM_TMEM>
 __device__ __forceinline__ void verify_walk(const GemmArgs &a, const PlanLayout &L, const VerifyTables &vt, uint4 *Bs,
-                                            int et, int n, int m0, int mcount, int first, int step, uint32_t taddr,
-                                            int nacc, const float *fin, int R, int i_row) {
-  for (int ai = 0; ai < vt.nbk; ++ai) {
-    const int4 bk = bucket_at(a, L, vt, ai);
-    const int s0 = bk.y, s1 = bk.z, r = bk.w;
-    if (s0 == s1) continue;
-    const int nq = (r + 7) >> 3;
-    if (r > 0 && n < a.N) {
-      const uint4 *brow = reinterpret_cast<const uint4 *>(a.B_stack + ((size_t)bk.x * a.N + n) * a.r_max);
+                                            int slot_cap, int et, int n, int m0, int mcount, int first, int step,
+                                            uint32_t taddr, int nacc, const float *fin, int R, int i_row) {
+  int ai = 0;
+  while (ai < vt.nbk) {
+    // A group of buckets whose B rows fit the slots: stage them all in one
+    // round of independent loads, then finish the group's columns.
+    int aj = ai, used = 0;
+    while (aj < vt.nbk) {
+      const int nq = (bucket_at(a, L, vt, aj).w + 7) >> 3;
+      if (aj > ai && used + nq > slot_cap) break;
+      used += nq;
+      ++aj;
+    }
+    // Staging walks the group's slots (bucket by bucket, 8 ranks per slot)
+    // with a cursor, eight slots per batch: the batch's loads are all issued
+    // before any of them is stored.
+    {
+      int cb = ai, cq = 0;
+      int4 cbk = bucket_at(a, L, vt, cb);
 #pragma unroll 1
-      for (int q = 0; q < nq; ++q) {
-        uint4 v = __ldg(brow + q);
-        if (q * 8 + 8 > r) {
-          uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (int base = 0; base < used; base += 8) {
+        uint4 v[8];
+        int qq[8], rr[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (q * 8 + 2 * e >= r) w[e] &= 0xFFFF0000u;
-            if (q * 8 + 2 * e + 1 >= r) w[e] &= 0x0000FFFFu;
+        for (int k = 0; k < 8; ++k) {
+          v[k] = make_uint4(0u, 0u, 0u, 0u);
+          qq[k] = 0;
+          rr[k] = 0;
+          if (base + k < used) {
+            while (cq >= ((cbk.w + 7) >> 3)) {
+              ++cb;
+              cbk = bucket_at(a, L, vt, cb);
+              cq = 0;
+            }
+            if (n < a.N && cbk.y < cbk.z)
+              v[k] = __ldg(reinterpret_cast<const uint4 *>(a.B_stack + ((size_t)cbk.x * a.N + n) * a.r_max) + cq);
+            qq[k] = cq;
+            rr[k] = cbk.w;
+            ++cq;
           }
-          v = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        Bs[q * 128 + et] = v;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (base + k < used) {
+            uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+            if (qq[k] * 8 + 8 > rr[k]) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if (qq[k] * 8 + 2 * e >= rr[k]) w[e] &= 0xFFFF0000u;
+                if (qq[k] * 8 + 2 * e + 1 >= rr[k]) w[e] &= 0x0000FFFFu;
+              }
+            }
+            Bs[(base + k) * 128 + et] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
       }
     }
+    int slot = 0;
 #pragma unroll 1
-    for (int i = s0 + first; i < s1; i += 4 * step) {
-      int mm[4];
-      float val[4];
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int idx = i + jj * step;
-        int m = idx < s1 ? vt.perm[idx] : -1;
-        if (m < m0 || m >= m0 + mcount) m = -1;
-        mm[jj] = m;
-        val[jj] = 0.f;
-      }
-      if (FROM_TMEM) {
-        uint32_t own[4];
+    for (int b = ai; b < aj; ++b) {
+      const int4 bk = bucket_at(a, L, vt, b);
+      const int s0 = bk.y, s1 = bk.z, r = bk.w, nq = (r + 7) >> 3;
+      const uint4 *bs = Bs + (size_t)slot * 128 + et;
+      slot += nq;
 #pragma unroll 1
-        for (int ac = 0; ac < nacc; ++ac) {
+      for (int i = s0 + first; i < s1; i += 4 * step) {
+        int mm[4];
+        float val[4];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            own[jj] = 0u;
-            if (mm[jj] >= 0) tmem_ld_x1(taddr + (uint32_t)(ac * a.Mb + mm[jj] - m0), own[jj]);
-          }
-          tmem_ld_wait();
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) val[jj] = (ac == 0) ? __uint_as_float(own[jj]) : val[jj] + __uint_as_float(own[jj]);
+        for (int jj = 0; jj < 4; ++jj) {
+          const int idx = i + jj * step;
+          int m = idx < s1 ? vt.perm[idx] : -1;
+          if (m < m0 || m >= m0 + mcount) m = -1;
+          mm[jj] = m;
+          val[jj] = 0.f;
         }
-      } else {
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-          if (mm[jj] >= 0) val[jj] = fin[(mm[jj] - m0) * R + i_row];
-      }
-      if (r > 0) {
-        float dot[4] = {0.f, 0.f, 0.f, 0.f};
+        if (FROM_TMEM) {
+          uint32_t own[4];
 #pragma unroll 1
-        for (int q = 0; q < nq; ++q) {
-          const uint4 bv = Bs[q * 128 + et];
-          float b0, b1, b2, b3, b4, b5, b6, b7;
-          unpack_bf16x2(bv.x, b0, b1);
-          unpack_bf16x2(bv.y, b2, b3);
-          unpack_bf16x2(bv.z, b4, b5);
-          unpack_bf16x2(bv.w, b6, b7);
+          for (int ac = 0; ac < nacc; ++ac) {
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            if (mm[jj] >= 0) {
-              const float4 *trow = reinterpret_cast<const float4 *>(vt.T + (size_t)(mm[jj] - vt.t_row0) * vt.t_stride) + 2 * q;
-              const float4 t0 = trow[0], t1 = trow[1];
-              float d = dot[jj];
-              d = fmaf(t0.x, b0, d);
-              d = fmaf(t0.y, b1, d);
-              d = fmaf(t0.z, b2, d);
-              d = fmaf(t0.w, b3, d);
-              d = fmaf(t1.x, b4, d);
-              d = fmaf(t1.y, b5, d);
-              d = fmaf(t1.z, b6, d);
-              d = fmaf(t1.w, b7, d);
-              dot[jj] = d;
+            for (int jj = 0; jj < 4; ++jj) {
+              own[jj] = 0u;
+              if (mm[jj] >= 0) tmem_ld_x1(taddr + (uint32_t)(ac * a.Mb + mm[jj] - m0), own[jj]);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+              val[jj] = (ac == 0) ? __uint_as_float(own[jj]) : val[jj] + __uint_as_float(own[jj]);
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            if (mm[jj] >= 0) val[jj] = fin[(mm[jj] - m0) * R + i_row];
+        }
+        if (r > 0) {
+          float dot[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+          for (int q = 0; q < nq; ++q) {
+            const uint4 bv = bs[q * 128];
+            float b0, b1, b2, b3, b4, b5, b6, b7;
+            unpack_bf16x2(bv.x, b0, b1);
+            unpack_bf16x2(bv.y, b2, b3);
+            unpack_bf16x2(bv.z, b4, b5);
+            unpack_bf16x2(bv.w, b6, b7);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              if (mm[jj] >= 0) {
+                const float4 *trow =
+                    reinterpret_cast<const float4 *>(vt.T + (size_t)(mm[jj] - vt.t_row0) * vt.t_stride) + 2 * q;
+                const float4 t0 = trow[0], t1 = trow[1];
+                float d = dot[jj];
+                d = fmaf(t0.x, b0, d);
+                d = fmaf(t0.y, b1, d);
+                d = fmaf(t0.z, b2, d);
+                d = fmaf(t0.w, b3, d);
+                d = fmaf(t1.x, b4, d);
+                d = fmaf(t1.y, b5, d);
+                d = fmaf(t1.z, b6, d);
+                d = fmaf(t1.w, b7, d);
+                dot[jj] = d;
+              }
             }
           }
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) val[jj] = fmaf(a.scale, dot[jj], val[jj]);
         }
+        if (n < a.N) {
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) val[jj] = fmaf(a.scale, dot[jj], val[jj]);
-      }
-      if (n < a.N) {
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-          if (mm[jj] >= 0) a.y[(size_t)mm[jj] * a.N + n] = float_to_bf16_bits(val[jj]);
+          for (int jj = 0; jj < 4; ++jj)
+            if (mm[jj] >= 0) a.y[(size_t)mm[jj] * a.N + n] = float_to_bf16_bits(val[jj]);
+        }
       }
     }
+    ai = aj;
   }
 }
 
@@ -323,13 +387,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int nkb = kb_hi - kb_lo;
       // With static weights, the first ring of W tiles is requested before the
       // wait for the preceding kernel; x always comes after it.
-      const int early = args.prefetch_w ? min(nkb, S) : 0;
+      const int early = (args.prefetch_w && !args.after_shrink) ? min(nkb, S) : 0;
       for (int i = 0; i < early; ++i) {
         mbar_arrive_expect_tx(&sp.full[i], (uint32_t)stage_bytes);
         tma_load_2d(sp.stage0 + (size_t)i * stage_bytes, &tmap_w, &sp.full[i], (kb_lo + i) * BLOCK_K,
                     n_tile * BLOCK_N, pol_w);
       }
-      grid_dependency_wait();
+      // After this library's shrink kernel nothing the mainloop reads can
+      // still be in flight (the shrink released this grid only after its own
+      // predecessor had finished), so only the epilogue waits for T.
+      if (!args.after_shrink) grid_dependency_wait();
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -370,6 +437,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    bool mma_ok = false;
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(BLOCK_N, args.sub_n);
       int stage = 0;
@@ -411,7 +479,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         volatile int never = 0;
         mbar_wait_bounded(sp.drain, 0, &never);
       }
+      mma_ok = ok;
     }
+    // Accumulator handoff: this thread waits for the last MMA, then the warp
+    // releases the epilogue warps through named barrier 2, so they sleep in
+    // hardware instead of polling while the mainloop runs.
+    __syncwarp();
+    if (lane == 0) {
+      bool ready = mma_ok && mbar_wait_bounded(sp.tfull, 0, abort_flag);
+      if (mma_ok && !ready) signal_abort(sp, args.status);
+      *reinterpret_cast<volatile int *>(sp.acc_ready) = ready ? 1 : 0;
+    }
+    __syncwarp();
+    tc_fence_before_sync();
+    named_bar_arrive(2, 160);
   }
 
   // ------------------------------------------------------------ epilogue
@@ -424,11 +505,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const PlanLayout L = plan_layout(args.M, args.n_ad);
   bool have_acc = false;
   if (epi) {
-    have_acc = mbar_wait_bounded(sp.tfull, 0, abort_flag);
-    if (!have_acc) signal_abort(sp, args.status);
-    __syncwarp();
-    have_acc = named_bar_and(1, 128, have_acc);  // one decision for all four epilogue warps
+    named_bar_sync(2, 160);  // released by the MMA warp once the accumulator is complete
     tc_fence_after_sync();
+    have_acc = *reinterpret_cast<volatile int *>(sp.acc_ready) != 0;
     grid_dependency_wait();  // the plan and T come from kernels earlier in the stream
   }
   const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
@@ -453,13 +532,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       } else {
-        // Walk the plan's buckets (see verify_walk); the B-row slots sit at
-        // the start of the freed stage ring, the staged tables after them.
-        uint4 *Bs = reinterpret_cast<uint4 *>(sp.stage0);
-        const size_t bs_bytes = 8 * 128 * sizeof(uint4);
-        const VerifyTables vt =
-            stage_verify_tables(args, L, sp.stage0 + bs_bytes, (size_t)S * stage_bytes - bs_bytes, m0, mcount, et);
-        verify_walk<true>(args, L, vt, Bs, et, n, m0, mcount, 0, 1, taddr, nacc_eff, nullptr, 0, 0);
+        // Walk the plan's buckets (see verify_walk): the staged tables sit at
+        // the start of the freed stage ring, the B-row slots after them.
+        const size_t ring = (size_t)S * stage_bytes;
+        const VerifyTables vt = stage_verify_tables(args, L, sp.stage0, ring - 8 * 128 * sizeof(uint4), m0, mcount, et);
+        uint4 *Bs = reinterpret_cast<uint4 *>(sp.stage0 + vt.bytes);
+        const int slot_cap = (int)((ring - vt.bytes) / (128 * sizeof(uint4)));
+        verify_walk<true>(args, L, vt, Bs, slot_cap, et, n, m0, mcount, 0, 1, taddr, nacc_eff, nullptr, 0, 0);
       }
     }
     tc_fence_before_sync();
@@ -513,17 +592,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     if (verify && epi) {
       named_bar_sync(1, 128);
-      // Stage ring after the reduction: fin, then the B-row slots, then the
-      // staged tables when they fit.
+      // Stage ring after the reduction: fin, then the staged tables when
+      // they fit, then the B-row slots.
+      const size_t ring = (size_t)S * stage_bytes;
       const size_t fin_bytes = align_up((size_t)args.Mb * R * 4, 16);
-      uint4 *Bs = reinterpret_cast<uint4 *>(sp.stage0 + fin_bytes);
-      const size_t used = fin_bytes + 8 * 128 * sizeof(uint4);
-      const VerifyTables vt =
-          stage_verify_tables(args, L, sp.stage0 + used, (size_t)S * stage_bytes - used, m0, mcount, et);
+      const VerifyTables vt = stage_verify_tables(args, L, sp.stage0 + fin_bytes,
+                                                  ring - fin_bytes - 8 * 128 * sizeof(uint4), m0, mcount, et);
+      uint4 *Bs = reinterpret_cast<uint4 *>(sp.stage0 + fin_bytes + vt.bytes);
+      const int slot_cap = (int)((ring - fin_bytes - vt.bytes) / (128 * sizeof(uint4)));
       // Threads split as (row i, column phase): 128 / R threads share a row.
       const int P = 128 / R;
       const int i = et % R, sub = et / R;
-      verify_walk<false>(args, L, vt, Bs, et, n_tile * BLOCK_N + r0 + i, m0, mcount, sub, P, 0u, 1, fin, R, i);
+      verify_walk<false>(args, L, vt, Bs, slot_cap, et, n_tile * BLOCK_N + r0 + i, m0, mcount, sub, P, 0u, 1, fin, R,
+                         i);
     }
     tc_fence_before_sync();
     cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
@@ -711,6 +792,7 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
   a.red_bytes = sh.red_bytes;
   a.mode = g.mode;
   a.prefetch_w = g.prefetch_w;
+  a.after_shrink = g.after_shrink;
   a.scale = g.scale;
   a.y = g.y;
   a.B_stack = g.B_stack;

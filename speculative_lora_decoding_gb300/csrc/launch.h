@@ -56,7 +56,8 @@ struct GemmLaunch {
   const uint16_t *W;
   int M, N, K;
   int mode;
-  int prefetch_w;  // W may be requested before the preceding kernel finishes
+  int prefetch_w;    // W may be requested before the preceding kernel finishes
+  int after_shrink;  // the preceding kernel on the stream is launch_shrink's
   float scale;
   uint16_t *y;
   const uint16_t *B_stack;

@@ -110,6 +110,7 @@ extern "C" MLORA_API mlora_status mlora_linear_noalloc(const mlora_bf16 *x, int 
   g.K = K;
   g.mode = base_mode;
   g.prefetch_w = prefetch_w;
+  g.after_shrink = verify ? 1 : 0;
   g.scale = scale;
   g.y = y;
   g.B_stack = B_stack;

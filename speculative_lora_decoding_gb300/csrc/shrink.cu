@@ -5,7 +5,7 @@
 //
 // Work item = (adapter a, block of SHRINK_J = 8 rows of A_a, chunk of
 // SHRINK_TOK = 4 rows of the adapter's group), read as one 32-byte record
-// the plan kernel wrote.  One CTA of 8 warps takes an item and splits K
+// the plan kernel wrote.  One CTA of 4 warps takes an item and splits K
 // across its warps; each lane streams 16-byte pieces of
 // the 8 A rows (coalesced: a warp reads 512 contiguous bytes per row per
 // step) and of the 4 x rows, and keeps 8 x 4 fp32 partial sums in registers.
@@ -18,7 +18,7 @@
 
 namespace mlora {
 
-constexpr int SHRINK_THREADS = 256;
+constexpr int SHRINK_THREADS = 128;  // small enough to sit beside a GEMM CTA on one SM
 constexpr int SHRINK_WARPS = SHRINK_THREADS / 32;
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
@@ -59,8 +59,12 @@ __global__ void __launch_bounds__(SHRINK_THREADS)
     shrink_kernel(const uint16_t *__restrict__ x, int M, int K, const uint16_t *__restrict__ A, int n_ad, int r_max,
                   const int32_t *__restrict__ plan, float *__restrict__ T, int t_stride) {
   __shared__ float red[SHRINK_WARPS][SHRINK_J * SHRINK_TOK];
-  grid_launch_dependents();
+  // Wait for the preceding kernel first, then let the GEMM that follows
+  // launch: by then everything the GEMM's mainloop reads (x, W) is complete,
+  // so it may stream while this kernel computes T; the GEMM waits for T only
+  // in its epilogue.
   grid_dependency_wait();
+  grid_launch_dependents();
   const PlanLayout L = plan_layout(M, n_ad);
   const int total_items = plan[L.hdr + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -77,19 +81,40 @@ __global__ void __launch_bounds__(SHRINK_THREADS)
 #pragma unroll
     for (int i = 0; i < SHRINK_J * SHRINK_TOK; ++i) acc[i] = 0.f;
 
-    for (int c = warp * 32 + lane; c < kchunks; c += SHRINK_THREADS) {
-      float xf[SHRINK_TOK][8];
+    // Two 16-byte pieces per row per iteration: all 24 loads of an
+    // iteration are issued before any is used.
+    for (int c = warp * 32 + lane; c < kchunks; c += 2 * SHRINK_THREADS) {
+      const int c2 = c + SHRINK_THREADS;
+      const bool has2 = c2 < kchunks;
+      uint4 xv[2][SHRINK_TOK], av[2][SHRINK_J];
 #pragma unroll
       for (int t = 0; t < SHRINK_TOK; ++t) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (t < ntok) v = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)rows[t] * K) + c);
-        bf16x8_to_f32(v, xf[t]);
+        xv[0][t] = make_uint4(0, 0, 0, 0);
+        xv[1][t] = make_uint4(0, 0, 0, 0);
+        if (t < ntok) {
+          const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)rows[t] * K);
+          xv[0][t] = __ldg(xr + c);
+          if (has2) xv[1][t] = __ldg(xr + c2);
+        }
       }
 #pragma unroll
       for (int j = 0; j < SHRINK_J; ++j) {
+        av[0][j] = make_uint4(0, 0, 0, 0);
+        av[1][j] = make_uint4(0, 0, 0, 0);
         if (j < nrow) {
+          av[0][j] = ldg_stream(Abase + (size_t)j * K + (size_t)c * 8);
+          if (has2) av[1][j] = ldg_stream(Abase + (size_t)j * K + (size_t)c2 * 8);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float xf[SHRINK_TOK][8];
+#pragma unroll
+        for (int t = 0; t < SHRINK_TOK; ++t) bf16x8_to_f32(xv[h][t], xf[t]);
+#pragma unroll
+        for (int j = 0; j < SHRINK_J; ++j) {
           float af[8];
-          bf16x8_to_f32(ldg_stream(Abase + (size_t)j * K + (size_t)c * 8), af);
+          bf16x8_to_f32(av[h][j], af);
 #pragma unroll
           for (int t = 0; t < SHRINK_TOK; ++t)
 #pragma unroll
@@ -121,7 +146,7 @@ cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, in
   const long long bound =
       (long long)((r_max + SHRINK_J - 1) / SHRINK_J) * ((M + SHRINK_TOK - 1) / SHRINK_TOK + min(M, n_ad));
   (void)n_ad;
-  const int grid = (int)max(1LL, min(bound, (long long)num_sms * 4));
+  const int grid = (int)max(1LL, min(bound, (long long)num_sms * 8));
   cudaError_t e = launch_pdl(shrink_kernel, dim3(grid), dim3(SHRINK_THREADS), 0, s, x, M, K, A, n_ad, r_max, plan, T,
                              t_stride);
   return e != cudaSuccess ? e : cudaGetLastError();
