@@ -176,15 +176,17 @@ __global__ void __launch_bounds__(ACC_THREADS)
     const float4 *q4 = reinterpret_cast<const float4 *>(qrow);
     const int e0 = w0 >> 2, e1 = w1 >> 2;  // w0, V multiples of 4 on this path
     int e = e0 + lane;
-    for (; e + 96 < e1; e += 128) {
-      float4 pv[4], qv[4];
+    // Eight 16-byte loads of p (and of q when a draft was rejected) in
+    // flight per lane before any is used.
+    for (; e + 7 * 32 < e1; e += 8 * 32) {
+      float4 pv[8], qv[8];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < 8; ++r) {
         pv[r] = __ldcs(p4 + e + 32 * r);
         qv[r] = residual ? __ldcs(q4 + e + 32 * r) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < 8; ++r) {
         const float pa[4] = {pv[r].x, pv[r].y, pv[r].z, pv[r].w};
         const float qa[4] = {qv[r].x, qv[r].y, qv[r].z, qv[r].w};
 #pragma unroll
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(ACC_THREADS)
 AcceptShape accept_shape(int B, int k, int V, int num_sms) {
   (void)k;
   AcceptShape s;
-  int want = (2 * num_sms + B - 1) / B;
+  int want = (2 * num_sms) / B;  // about two CTAs per SM, all resident in one wave
   const int max_slices = (V + MIN_SLICE - 1) / MIN_SLICE;
   if (want > max_slices) want = max_slices;
   if (want < 1) want = 1;

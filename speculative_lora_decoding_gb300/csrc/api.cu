@@ -21,7 +21,7 @@ static int device_sms() {
 static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct LinearLayout {
-  size_t plan, T, total;
+  size_t plan, T, tw, total;  // tw == 0: no masked operand (tensor-core expand off)
 };
 
 static LinearLayout linear_layout(int M, int N, int K, int n_ad, int sms) {
@@ -32,6 +32,13 @@ static LinearLayout linear_layout(int M, int N, int K, int n_ad, int sms) {
   o = align_up(o + P.words * 4, 256);
   L.T = o;
   o = align_up(o + (size_t)M * T_STRIDE * 4, 256);
+  // Masked low-rank operand of the tensor-core expand (one token group of at
+  // most 256 rows, loaded by a single MMA).
+  L.tw = 0;
+  if (M <= 256 && n_ad > 0) {
+    L.tw = o;
+    o = align_up(o + (size_t)max_expand_slices(M, n_ad) * expand_rows(M) * 32, 256);
+  }
   (void)N;
   (void)K;
   (void)sms;
@@ -98,7 +105,11 @@ mlora_status mlora_plan_segments(const int32_t *adapter_idx, int M, const int32_
   if (ws_bytes < WS_SCRATCH_OFF + P.words * 4) return MLORA_ERR_WORKSPACE;
   int32_t *plan = reinterpret_cast<int32_t *>((uint8_t *)workspace + WS_SCRATCH_OFF);
   uint32_t *status = reinterpret_cast<uint32_t *>((uint8_t *)workspace + WS_STATUS_OFF);
-  cudaError_t e = launch_plan(adapter_idx, M, rank_of, n_adapters, r_max, plan, status, (cudaStream_t)stream);
+  // The masked operand sits after the plan when the workspace is large
+  // enough for the layer (mlora_linear checks that size itself).
+  const LinearLayout LL = linear_layout(M, 1, 8, n_adapters, 1);
+  uint16_t *tw = (LL.tw && ws_bytes >= LL.total) ? reinterpret_cast<uint16_t *>((uint8_t *)workspace + LL.tw) : nullptr;
+  cudaError_t e = launch_plan(adapter_idx, M, rank_of, n_adapters, r_max, plan, status, tw, (cudaStream_t)stream);
   if (e != cudaSuccess) return MLORA_ERR_CUDA;
   if (seg_offsets) *seg_offsets = plan + P.seg_offsets;
   if (perm) *perm = plan + P.perm;
@@ -120,7 +131,8 @@ mlora_status mlora_shrink(const mlora_bf16 *x, int M, int K, const mlora_bf16 *A
   if (seg_offsets != plan + P.seg_offsets) return MLORA_ERR_ARG;
   const int sms = device_sms();
   if (sms <= 0) return MLORA_ERR_CUDA;
-  cudaError_t e = launch_shrink(x, M, K, A_stack, n_adapters, r_max, plan, T, r_max, true, sms, (cudaStream_t)stream);
+  cudaError_t e =
+      launch_shrink(x, M, K, A_stack, n_adapters, r_max, plan, T, r_max, true, sms, nullptr, 1.f, (cudaStream_t)stream);
   return cuda_status(e);
 }
 
@@ -150,16 +162,17 @@ mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W
   uint32_t *status = reinterpret_cast<uint32_t *>(ws + WS_STATUS_OFF);
   int32_t *plan = reinterpret_cast<int32_t *>(ws + L.plan);
   float *T = reinterpret_cast<float *>(ws + L.T);
+  uint16_t *tw = L.tw ? reinterpret_cast<uint16_t *>(ws + L.tw) : nullptr;
   cudaError_t e;
   if (verify) {
     const PlanLayout P = plan_layout(M, n_ad);
     if (seg_offsets == nullptr) {
-      e = launch_plan(adapter_idx, M, rank_of, n_ad, r_max, plan, status, s);
+      e = launch_plan(adapter_idx, M, rank_of, n_ad, r_max, plan, status, tw, s);
       if (e != cudaSuccess) return MLORA_ERR_CUDA;
     } else if (seg_offsets != plan + P.seg_offsets) {
       return MLORA_ERR_ARG;
     }
-    e = launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, s);
+    e = launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, tw, scale, s);
     if (e != cudaSuccess) return MLORA_ERR_CUDA;
   }
   const GemmShape sh = gemm_shape(M, N, K, sms);
@@ -180,6 +193,7 @@ mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W
   g.T = T;
   g.plan = plan;
   g.status = status;
+  g.tw = verify ? tw : nullptr;
   int err = 0;
   e = launch_gemm(g, sh, s, &err);
   if (err) return MLORA_ERR_ARG;

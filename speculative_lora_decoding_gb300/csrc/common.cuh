@@ -38,15 +38,25 @@ __host__ __device__ inline size_t max_shrink_items(int M, int n_ad) {
   return (size_t)(64 / SHRINK_J) * ((M + SHRINK_TOK - 1) / SHRINK_TOK + m_ad);
 }
 
+// Upper bound on (adapter, 16-rank slice) pairs: at most min(M, n_ad) active
+// adapters of rank <= 64.
+__host__ __device__ inline int max_expand_slices(int M, int n_ad) { return (M < n_ad ? M : n_ad) * 4; }
+
+// Rows of the masked low-rank operand (tokens padded to 16).
+__host__ __device__ inline int expand_rows(int M) { return (M + 15) / 16 * 16; }
+
 // Plan layout inside scratch (int32 words), for M rows and n_ad adapters.
 struct PlanLayout {
-  size_t hdr;         // [0] n_active, [1] total shrink items, [2] rows, [3] largest active rank
+  size_t hdr;         // [0] n_active, [1] shrink items, [2] rows, [3] largest active rank,
+                      // [4] expand slices, [5] 1 if the masked operand buffer is zeroed and usable
   size_t seg_offsets; // [n_ad + 2]
   size_t perm;        // [M]
   size_t row_adapter; // [M]   validated adapter per row (-1: none)
   size_t rank_eff;    // [n_ad] validated ranks
   size_t active;      // [n_ad] adapters with rows, increasing
   size_t item_off;    // [n_ad + 1] prefix of shrink items over the active list
+  size_t slice_off;   // [n_ad] first expand slice of each adapter
+  size_t slices;      // [max_expand_slices][2] (adapter, first rank of the slice)
   size_t items;       // [max_shrink_items][ITEM_WORDS], 16-byte aligned
   size_t words;       // total int32 words
 };
@@ -61,6 +71,8 @@ __host__ __device__ inline PlanLayout plan_layout(int M, int n_ad) {
   L.rank_eff = o;     o += align_up(n_ad, 16);
   L.active = o;       o += align_up(n_ad, 16);
   L.item_off = o;     o += align_up(n_ad + 1, 16);
+  L.slice_off = o;    o += align_up(n_ad, 16);
+  L.slices = o;       o += align_up((size_t)max_expand_slices(M, n_ad) * 2, 16);
   L.items = o;        o += max_shrink_items(M, n_ad) * ITEM_WORDS;
   L.words = o;
   return L;
@@ -218,6 +230,20 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
   d |= (uint64_t)(1024 >> 4) << 32;             // stride byte offset
   d |= (uint64_t)1 << 46;                       // descriptor version
   d |= (uint64_t)2 << 61;                       // 128-byte swizzle
+  return d;
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile whose rows are
+// 32 bytes (16 bf16) written by TMA with 32-byte swizzling: groups of 8 rows
+// are 256 bytes apart, descriptor version 1, swizzle mode 6 (32 B).  One MMA
+// K step (16 bf16) spans the whole row.
+__device__ __forceinline__ uint64_t smem_desc_kmajor_sw32(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(256 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)6 << 61;
   return d;
 }
 

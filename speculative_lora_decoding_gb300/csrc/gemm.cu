@@ -55,6 +55,7 @@ struct GemmArgs {
   int Mb, nsub, sub_n, n_tgroups, kblocks, C, stages, tmem_cols, red_bytes, nacc;
   int mode, prefetch_w;
   int after_shrink;  // launched right after this library's shrink kernel: x and W are ready
+  int use_tw, Mpad;  // tensor-core expand allowed (masked operand present), its token rows
   float scale;
   uint16_t *y;
   const uint16_t *B_stack;
@@ -335,8 +336,23 @@ __device__ __forceinline__ void verify_walk(const GemmArgs &a, const PlanLayout 
   }
 }
 
+// Tensor-core expand: after the base K loop, one MMA per (adapter, 16-rank
+// slice) adds B_a[n0:n0+128, slice] x Tmask[:, slice]^T, where Tmask holds
+// scale * T for the adapter's own rows and 0 elsewhere (written by the plan
+// and shrink kernels).  Worth it while the slices' MMA work stays small
+// against the base GEMM (slices * 16 <= K / 8); otherwise the epilogue
+// bucket walk adds the low-rank term on the CUDA cores.
+__device__ __forceinline__ int expand_slices_tc(const GemmArgs &a, const PlanLayout &L) {
+  if (!a.use_tw || a.mode != MLORA_VERIFY) return -1;
+  const int32_t *plan = a.plan;
+  if (plan[L.hdr + 5] != 1) return -1;
+  const int ns = plan[L.hdr + 4];
+  return (ns * 16 * 8 <= a.K) ? ns : -1;
+}
+
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_tw,
                 const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -368,6 +384,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_w);
     tma_prefetch_desc(&tmap_x);
+    if (args.use_tw) {
+      tma_prefetch_desc(&tmap_b);
+      tma_prefetch_desc(&tmap_tw);
+    }
   }
   if (warp == 1) {
     tmem_alloc(sp.tmem_slot, args.tmem_cols);
@@ -418,6 +438,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
+        }
+      }
+      const PlanLayout Lp = plan_layout(args.M, args.n_ad);
+      const int ns = (rank == 0 && !*abort_flag) ? expand_slices_tc(args, Lp) : -1;
+      if (ns > 0) {
+        grid_dependency_wait();  // the masked operand comes from the shrink kernel just before
+        for (int sl = 0; sl < ns; ++sl) {
+          const int ad = args.plan[Lp.slices + 2 * sl], j0 = args.plan[Lp.slices + 2 * sl + 1];
+          if (!mbar_wait_bounded(&sp.empty[stage], phase ^ 1u, abort_flag)) {
+            signal_abort(sp, args.status);
+            break;
+          }
+          uint8_t *st = sp.stage0 + (size_t)stage * stage_bytes;
+          mbar_arrive_expect_tx(&sp.full[stage], (uint32_t)(BLOCK_N * 32 + args.sub_n * 32));
+          tma_load_2d(st, &tmap_b, &sp.full[stage], j0, ad * args.N + n_tile * BLOCK_N, pol_w);
+          tma_load_2d(st + BLOCK_N * 32, &tmap_tw, &sp.full[stage], 0, sl * args.Mpad + m0, pol_x);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
       if (*abort_flag) {
@@ -471,6 +512,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           phase ^= 1u;
         }
       }
+      const PlanLayout Lm = plan_layout(args.M, args.n_ad);
+      const int ns = (ok && rank == 0) ? expand_slices_tc(args, Lm) : -1;
+      for (int sl = 0; sl < ns; ++sl) {
+        if (!mbar_wait_bounded(&sp.full[stage], phase, abort_flag)) {
+          signal_abort(sp, args.status);
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t a_addr = smem_addr(sp.stage0 + (size_t)stage * stage_bytes);
+        mma_bf16_ss(tmem_base, smem_desc_kmajor_sw32(a_addr), smem_desc_kmajor_sw32(a_addr + BLOCK_N * 32), idesc, 1u);
+        mma_commit(&sp.empty[stage]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
       if (ok) {
         mma_commit(sp.tfull);
       } else if (issued_any) {
@@ -504,17 +562,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int et = threadIdx.x - 64;
   const PlanLayout L = plan_layout(args.M, args.n_ad);
   bool have_acc = false;
+  bool expand_done = false;  // the low-rank term is already in the accumulator
   if (epi) {
     named_bar_sync(2, 160);  // released by the MMA warp once the accumulator is complete
     tc_fence_after_sync();
     have_acc = *reinterpret_cast<volatile int *>(sp.acc_ready) != 0;
     grid_dependency_wait();  // the plan and T come from kernels earlier in the stream
+    expand_done = expand_slices_tc(args, L) >= 0;
   }
   const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
   const int nchunks = (mcount + CHUNK - 1) / CHUNK;
   const int nacc_eff = kb_hi > kb_lo ? args.nacc : 1;  // every accumulator gets a K step of each k-block
 
-  const bool verify = args.mode == MLORA_VERIFY;
+  // Verify work left for the epilogue: none once the tensor cores added it.
+  const bool verify = args.mode == MLORA_VERIFY && !expand_done;
 
   if (C == 1) {
     if (epi && have_acc) {
@@ -753,27 +814,39 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows, cols] read in boxes of box_rows x 64 with
-// 128-byte swizzling; out-of-range elements read as zero.
-static bool make_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
+// Row-major bf16 matrix [rows, cols] read in boxes of box_rows x box_cols
+// (64 columns with 128-byte swizzling, or 16 with 32-byte swizzling);
+// out-of-range elements read as zero.
+static bool make_map(CUtensorMap *map, const void *base, long long rows, int cols, int box_rows, int box_cols = BLOCK_K) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BLOCK_K, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = box_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B;
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s, int *err_code) {
   *err_code = 0;
-  CUtensorMap tw, tx;
+  CUtensorMap tw, tx, tb, tt;
   if (!make_map(&tw, g.W, g.N, g.K, BLOCK_N) || !make_map(&tx, g.x, g.M, g.K, sh.sub_n)) {
     *err_code = 1;
     return cudaErrorInvalidValue;
+  }
+  // The tensor-core expand needs one token group loaded by one MMA.
+  const int use_tw = (g.mode == MLORA_VERIFY && g.tw != nullptr && sh.nsub == 1 && sh.n_tgroups == 1) ? 1 : 0;
+  tb = tw;
+  tt = tw;
+  if (use_tw) {
+    if (!make_map(&tb, g.B_stack, (long long)g.n_ad * g.N, g.r_max, BLOCK_N, 16) ||
+        !make_map(&tt, g.tw, (long long)max_expand_slices(g.M, g.n_ad) * expand_rows(g.M), 16, sh.sub_n, 16)) {
+      *err_code = 1;
+      return cudaErrorInvalidValue;
+    }
   }
   if (!ensure_attributes()) return cudaErrorInvalidValue;
   GemmArgs a;
@@ -793,6 +866,8 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
   a.mode = g.mode;
   a.prefetch_w = g.prefetch_w;
   a.after_shrink = g.after_shrink;
+  a.use_tw = use_tw;
+  a.Mpad = expand_rows(g.M);
   a.scale = g.scale;
   a.y = g.y;
   a.B_stack = g.B_stack;
@@ -821,7 +896,7 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel, tw, tx, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel, tw, tx, tb, tt, a);
   note_launch();
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

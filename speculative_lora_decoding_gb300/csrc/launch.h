@@ -33,13 +33,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // Step a1: stable counting sort of rows by adapter into `plan` (int32 words).
+// `tw` (may be null): the masked low-rank operand buffer of the tensor-core
+// expand, [max_expand_slices(M, n_ad)][expand_rows(M)][16] bf16; zeroed here.
 cudaError_t launch_plan(const int32_t *adapter_idx, int M, const int32_t *rank_of, int n_ad, int r_max,
-                        int32_t *plan, uint32_t *status, cudaStream_t s);
+                        int32_t *plan, uint32_t *status, uint16_t *tw, cudaStream_t s);
 
 // Step a2: T[m, j] for j < rank (fp32, row stride t_stride).  `zero_first`
 // clears T first so that padding and rows without an adapter read 0.
+// With `tw` non-null it also writes bf16(scale * T) into the masked operand.
 cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, int n_ad, int r_max,
-                          const int32_t *plan, float *T, int t_stride, bool zero_first, int num_sms, cudaStream_t s);
+                          const int32_t *plan, float *T, int t_stride, bool zero_first, int num_sms, uint16_t *tw,
+                          float scale, cudaStream_t s);
 
 // Steps a3 + a4: base GEMM on tcgen05 with the expand epilogue.
 struct GemmShape {
@@ -65,6 +69,7 @@ struct GemmLaunch {
   const float *T;
   const int32_t *plan;
   uint32_t *status;
+  const uint16_t *tw;  // masked low-rank operand, or null (bucket-walk epilogue only)
 };
 cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s, int *err_code);
 

@@ -98,8 +98,9 @@ extern "C" MLORA_API mlora_status mlora_linear_noalloc(const mlora_bf16 *x, int 
   int32_t *plan = reinterpret_cast<int32_t *>(scratch + plan_off);
   float *T = reinterpret_cast<float *>(scratch + t_off);
   if (verify) {
-    if (launch_plan(adapter_idx, M, rank_of, n_ad, r_max, plan, status, s) != cudaSuccess) return MLORA_ERR_CUDA;
-    if (launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, s) != cudaSuccess)
+    if (launch_plan(adapter_idx, M, rank_of, n_ad, r_max, plan, status, nullptr, s) != cudaSuccess)
+      return MLORA_ERR_CUDA;
+    if (launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, nullptr, 1.f, s) != cudaSuccess)
       return MLORA_ERR_CUDA;
   }
   GemmLaunch g;
@@ -119,6 +120,7 @@ extern "C" MLORA_API mlora_status mlora_linear_noalloc(const mlora_bf16 *x, int 
   g.T = T;
   g.plan = plan;
   g.status = status;
+  g.tw = nullptr;
   int err = 0;
   const cudaError_t e = launch_gemm(g, gemm_shape(M, N, K, sms), s, &err);
   if (err) return MLORA_ERR_ARG;

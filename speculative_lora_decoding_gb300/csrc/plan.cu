@@ -53,7 +53,7 @@ __device__ __forceinline__ int bucket_of(int a, int n_ad) { return (a >= 0 && a 
 
 __global__ void __launch_bounds__(PLAN_THREADS, 1)
     plan_kernel(const int32_t *__restrict__ adapter_idx, int M, const int32_t *__restrict__ rank_of, int n_ad,
-                int r_max, int32_t *__restrict__ plan, uint32_t *status) {
+                int r_max, int32_t *__restrict__ plan, uint32_t *status, uint4 *__restrict__ tw) {
   grid_launch_dependents();
   grid_dependency_wait();
   extern __shared__ int sh_dyn[];
@@ -128,17 +128,27 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
       }
     }
     if (rmax > 0) atomicMax(&max_rank, rmax);
-    int tot_act, tot_items;
+    int nsl = 0;
+    for (int a = a0; a < a1; ++a)
+      if (running[a] > 0) nsl += (plan[L.rank_eff + a] + 15) / 16;
+    int tot_act, tot_items, tot_sl;
     int pa = block_excl_scan(nact, scan_sh, &tot_act);
     int pi = block_excl_scan(nitems, scan_sh, &tot_items);
+    int ps = block_excl_scan(nsl, scan_sh, &tot_sl);
     for (int a = a0; a < a1; ++a) {
       const int c = running[a];
       if (c > 0) {
         const int r = plan[L.rank_eff + a];
         plan[L.active + pa] = a;
         plan[L.item_off + pa] = pi;
+        plan[L.slice_off + a] = ps;
+        for (int j = 0; j * 16 < r; ++j) {
+          plan[L.slices + 2 * (ps + j)] = a;
+          plan[L.slices + 2 * (ps + j) + 1] = 16 * j;
+        }
         ++pa;
         pi += ((r + SHRINK_J - 1) / SHRINK_J) * ((c + SHRINK_TOK - 1) / SHRINK_TOK);
+        ps += (r + 15) / 16;
       }
     }
     if (tid == 0) {
@@ -146,6 +156,16 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
       plan[L.hdr + 0] = tot_act;
       plan[L.hdr + 1] = tot_items;
       plan[L.hdr + 2] = M;
+      plan[L.hdr + 4] = tot_sl;
+      plan[L.hdr + 5] = tw ? 1 : 0;
+    }
+    // The masked low-rank operand: slice s holds, for every token row,
+    // scale * T[row, slice ranks] if the row belongs to the slice's adapter
+    // and 0 otherwise.  Zero it here once per plan; the shrink of each
+    // projection rewrites only the member rows, which the plan fixes.
+    if (tw) {
+      const size_t n16 = (size_t)tot_sl * expand_rows(M) * 2;  // 16-byte pieces (16 bf16 per row)
+      for (size_t e = tid; e < n16; e += PLAN_THREADS) tw[e] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
   __syncthreads();
@@ -211,10 +231,10 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
 }
 
 cudaError_t launch_plan(const int32_t *adapter_idx, int M, const int32_t *rank_of, int n_ad, int r_max,
-                        int32_t *plan, uint32_t *status, cudaStream_t s) {
+                        int32_t *plan, uint32_t *status, uint16_t *tw, cudaStream_t s) {
   const size_t smem = 2 * (size_t)(n_ad + 1) * sizeof(int);  // <= 32.8 KB for n_ad <= 4096
   cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(PLAN_THREADS), smem, s, adapter_idx, M, rank_of, n_ad, r_max,
-                             plan, status);
+                             plan, status, reinterpret_cast<uint4 *>(tw));
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

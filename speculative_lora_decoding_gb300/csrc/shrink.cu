@@ -57,7 +57,8 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[32]) {
 
 __global__ void __launch_bounds__(SHRINK_THREADS)
     shrink_kernel(const uint16_t *__restrict__ x, int M, int K, const uint16_t *__restrict__ A, int n_ad, int r_max,
-                  const int32_t *__restrict__ plan, float *__restrict__ T, int t_stride) {
+                  const int32_t *__restrict__ plan, float *__restrict__ T, int t_stride, uint16_t *__restrict__ tw,
+                  float scale) {
   __shared__ float red[SHRINK_WARPS][SHRINK_J * SHRINK_TOK];
   // Wait for the preceding kernel first, then let the GEMM that follows
   // launch: by then everything the GEMM's mainloop reads (x, W) is complete,
@@ -130,14 +131,23 @@ __global__ void __launch_bounds__(SHRINK_THREADS)
       float s = 0.f;
 #pragma unroll
       for (int w = 0; w < SHRINK_WARPS; ++w) s += red[w][threadIdx.x];
-      if (t < ntok) T[(size_t)rows[t] * t_stride + j0 + j] = (j < nrow) ? s : 0.f;
+      if (t < ntok) {
+        const float v = (j < nrow) ? s : 0.f;
+        T[(size_t)rows[t] * t_stride + j0 + j] = v;
+        if (tw) {
+          // Member row of the masked operand: slice (j0 + j) / 16 of adapter a.
+          const int slice = plan[L.slice_off + a] + (j0 + j) / 16;
+          tw[((size_t)slice * expand_rows(M) + rows[t]) * 16 + (j0 + j) % 16] = float_to_bf16_bits(scale * v);
+        }
+      }
     }
     __syncthreads();
   }
 }
 
 cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, int n_ad, int r_max,
-                          const int32_t *plan, float *T, int t_stride, bool zero_first, int num_sms, cudaStream_t s) {
+                          const int32_t *plan, float *T, int t_stride, bool zero_first, int num_sms, uint16_t *tw,
+                          float scale, cudaStream_t s) {
   if (zero_first) {
     cudaError_t e = cudaMemsetAsync(T, 0, (size_t)M * t_stride * sizeof(float), s);
     if (e != cudaSuccess) return e;
@@ -148,7 +158,7 @@ cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, in
   (void)n_ad;
   const int grid = (int)max(1LL, min(bound, (long long)num_sms * 8));
   cudaError_t e = launch_pdl(shrink_kernel, dim3(grid), dim3(SHRINK_THREADS), 0, s, x, M, K, A, n_ad, r_max, plan, T,
-                             t_stride);
+                             t_stride, tw, scale);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

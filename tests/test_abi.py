@@ -46,8 +46,11 @@ def test_status_strings_and_host_checks(lib):
 
 def test_workspace_sizes(lib):
     a = lib.mlora_linear_workspace_bytes(128, 4096, 4096, 16)
-    b = lib.mlora_linear_workspace_bytes(512, 14336, 4096, 128)
-    assert 0 < a < b
+    b = lib.mlora_linear_workspace_bytes(256, 4096, 4096, 16)
+    c = lib.mlora_linear_workspace_bytes(512, 14336, 4096, 128)
+    assert 0 < a < b and c > 0
+    # one workspace serves every projection of a step: the size depends on M and n_adapters only
+    assert lib.mlora_linear_workspace_bytes(128, 1024, 14336, 16) == a
     assert lib.mlora_linear_workspace_bytes(128, 4096, 4097, 16) == 0      # K % 8 != 0
     assert lib.mlora_linear_workspace_bytes(0, 4096, 4096, 16) == 0
     assert lib.mlora_accept_workspace_bytes(256, 4, 128256) > 0
