@@ -63,11 +63,18 @@ __device__ __forceinline__ float sanitize_uniform(float u, uint32_t &flags) {
 __device__ __forceinline__ uint64_t fixq(float f) {
   const uint32_t bits = __float_as_uint(f);
   const int e = (int)(bits >> 23) & 0xFF;
-  const uint64_t m = (uint64_t)((bits & 0x7FFFFFu) | 0x800000u);
-  const int sh = e - 110;
-  if (sh >= 0) return m << sh;  // e <= 127 for f <= 1, so sh <= 17
-  if (sh <= -24) return 0ull;
-  return m >> (-sh);
+  const uint32_t m = (bits & 0x7FFFFFu) | 0x800000u;
+  const int sh = e - 110;  // e <= 127 for f <= 1, so sh <= 17
+  const uint64_t up = (uint64_t)m << (sh > 0 ? sh : 0);
+  const uint64_t down = (uint64_t)(m >> min(-sh, 31));  // m < 2^24: shifts of 24 or more give 0
+  return sh >= 0 ? up : down;
+}
+
+// Clamp to [0, 1] (NaN and negatives to 0) and note whether the value was
+// out of range.
+__device__ __forceinline__ float clamp_prob(float f, uint32_t &flags) {
+  if (!(f >= 0.f && f <= 1.f)) flags |= MLORA_DEV_BAD_PROB;
+  return fminf(fmaxf(f, 0.f), 1.f);
 }
 
 struct Weights {
@@ -121,6 +128,53 @@ __device__ __forceinline__ uint64_t block_excl_scan_u64(uint64_t v, uint64_t *sh
   return before + inc - v;
 }
 
+// Exact sums over [w0, w1) of one vocabulary row: the target mass sum Q(p)
+// and, when a draft was rejected, the residual mass sum max(0, Q(p) - Q(q)).
+// Eight 16-byte loads per operand are in flight per lane before any is used.
+template <bool RESIDUAL>
+__device__ __forceinline__ void pass1_sums(const float *prow, const float *qrow, int w0, int w1, int lane, int vec,
+                                           uint32_t &flags, uint64_t &s_res, uint64_t &s_tgt) {
+  auto add = [&](float pf, float qf) {
+    const uint64_t qp = fixq(clamp_prob(pf, flags));
+    s_tgt += qp;
+    if (RESIDUAL) {
+      const uint64_t qq = fixq(clamp_prob(qf, flags));
+      s_res += qp > qq ? qp - qq : 0ull;
+    }
+  };
+  if (vec) {
+    const float4 *p4 = reinterpret_cast<const float4 *>(prow);
+    const float4 *q4 = reinterpret_cast<const float4 *>(qrow);
+    const int e0 = w0 >> 2, e1 = w1 >> 2;  // w0, V multiples of 4 on this path
+    int e = e0 + lane;
+    for (; e + 7 * 32 < e1; e += 8 * 32) {
+      float4 pv[8], qv[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        pv[r] = __ldcs(p4 + e + 32 * r);
+        if (RESIDUAL) qv[r] = __ldcs(q4 + e + 32 * r);
+      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        add(pv[r].x, RESIDUAL ? qv[r].x : 0.f);
+        add(pv[r].y, RESIDUAL ? qv[r].y : 0.f);
+        add(pv[r].z, RESIDUAL ? qv[r].z : 0.f);
+        add(pv[r].w, RESIDUAL ? qv[r].w : 0.f);
+      }
+    }
+    for (; e < e1; e += 32) {
+      const float4 pv = __ldcs(p4 + e);
+      const float4 qv = RESIDUAL ? __ldcs(q4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+      add(pv.x, qv.x);
+      add(pv.y, qv.y);
+      add(pv.z, qv.z);
+      add(pv.w, qv.w);
+    }
+  } else {
+    for (int v = w0 + lane; v < w1; v += 32) add(prow[v], RESIDUAL ? qrow[v] : 0.f);
+  }
+}
+
 // Vocabulary row of request b: slices of slice_len (one CTA each), each slice
 // cut into ACC_WARPS contiguous sub-ranges of sub_len (one warp each).
 __global__ void __launch_bounds__(ACC_THREADS)
@@ -171,51 +225,10 @@ __global__ void __launch_bounds__(ACC_THREADS)
   // Step a6, pass 1: exact sums over this warp's sub-range.
   const int w0 = min(V, g * slice_len + warp * sub_len), w1 = min(V, w0 + sub_len);
   uint64_t s_res = 0, s_tgt = 0;
-  if (vec) {
-    const float4 *p4 = reinterpret_cast<const float4 *>(prow);
-    const float4 *q4 = reinterpret_cast<const float4 *>(qrow);
-    const int e0 = w0 >> 2, e1 = w1 >> 2;  // w0, V multiples of 4 on this path
-    int e = e0 + lane;
-    // Eight 16-byte loads of p (and of q when a draft was rejected) in
-    // flight per lane before any is used.
-    for (; e + 7 * 32 < e1; e += 8 * 32) {
-      float4 pv[8], qv[8];
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        pv[r] = __ldcs(p4 + e + 32 * r);
-        qv[r] = residual ? __ldcs(q4 + e + 32 * r) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const float pa[4] = {pv[r].x, pv[r].y, pv[r].z, pv[r].w};
-        const float qa[4] = {qv[r].x, qv[r].y, qv[r].z, qv[r].w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const Weights w = weight_of(pa[t], qa[t], residual, flags);
-          s_res += w.res;
-          s_tgt += w.tgt;
-        }
-      }
-    }
-    for (; e < e1; e += 32) {
-      const float4 pv = __ldcs(p4 + e);
-      const float4 qv = residual ? __ldcs(q4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float pa[4] = {pv.x, pv.y, pv.z, pv.w};
-      const float qa[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const Weights w = weight_of(pa[t], qa[t], residual, flags);
-        s_res += w.res;
-        s_tgt += w.tgt;
-      }
-    }
-  } else {
-    for (int v = w0 + lane; v < w1; v += 32) {
-      const Weights w = weight_of(prow[v], residual ? qrow[v] : 0.f, residual, flags);
-      s_res += w.res;
-      s_tgt += w.tgt;
-    }
-  }
+  if (residual)
+    pass1_sums<true>(prow, qrow, w0, w1, lane, vec, flags, s_res, s_tgt);
+  else
+    pass1_sums<false>(prow, qrow, w0, w1, lane, vec, flags, s_res, s_tgt);
   s_res = warp_sum_u64(s_res);
   s_tgt = warp_sum_u64(s_tgt);
   const size_t entries = (size_t)slices * ACC_WARPS;
@@ -335,7 +348,7 @@ __global__ void __launch_bounds__(ACC_THREADS)
 AcceptShape accept_shape(int B, int k, int V, int num_sms) {
   (void)k;
   AcceptShape s;
-  int want = (2 * num_sms) / B;  // about two CTAs per SM, all resident in one wave
+  int want = (2 * num_sms + B - 1) / B;  // about two CTAs per SM
   const int max_slices = (V + MIN_SLICE - 1) / MIN_SLICE;
   if (want > max_slices) want = max_slices;
   if (want < 1) want = 1;

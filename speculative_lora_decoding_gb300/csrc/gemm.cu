@@ -606,47 +606,105 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncthreads();
   } else {
     const int r0 = rank * BLOCK_N / C, r1 = (rank + 1) * BLOCK_N / C, R = r1 - r0;
-    const uint32_t red_local = smem_addr(sp.red);
+    const size_t ring = (size_t)S * stage_bytes;
     // Verify mode keeps the reduced rows, column-major [Mb][R], in the stage
     // ring (free once the last MMA has completed) for the bucket walk below.
     float *fin = reinterpret_cast<float *>(sp.stage0);
-    uint32_t peer[MAX_CLUSTER];
+    // One round when the whole accumulator fits the freed stage ring and no
+    // bucket walk needs the ring afterwards; otherwise 32 columns at a time
+    // through the double-buffered reduction tile.
+    const bool oneshot = !verify && (size_t)args.Mb * BLOCK_N * 4 <= ring;
+    if (oneshot) {
+      float *acc_all = reinterpret_cast<float *>(sp.stage0);  // [Mb][128], one column of 128 rows after another
+      const uint32_t ring_local = smem_addr(sp.stage0);
+      uint32_t peer[MAX_CLUSTER];
 #pragma unroll
-    for (int p = 0; p < MAX_CLUSTER; ++p) peer[p] = (p < C) ? map_to_rank(red_local, (uint32_t)p) : 0u;
-    for (int ch = 0; ch < nchunks; ++ch) {
-      const int buf = ch & 1;
-      float *red = sp.red + buf * CHUNK * BLOCK_N;
+      for (int p = 0; p < MAX_CLUSTER; ++p) peer[p] = (p < C) ? map_to_rank(ring_local, (uint32_t)p) : 0u;
       if (epi) {
-        uint32_t r[32];
-        if (have_acc) {
-          tmem_ld_acc_x32(taddr + ch * CHUNK, nacc_eff, args.Mb, r);
-        } else {
+        for (int ch = 0; ch < nchunks; ++ch) {
+          uint32_t r[32];
+          if (have_acc) {
+            tmem_ld_acc_x32(taddr + ch * CHUNK, nacc_eff, args.Mb, r);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = 0u;
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+#pragma unroll
+          for (int j = 0; j < CHUNK; ++j) acc_all[(ch * CHUNK + j) * BLOCK_N + quad * 32 + lane] = __uint_as_float(r[j]);
         }
-#pragma unroll
-        for (int j = 0; j < CHUNK; ++j) red[j * BLOCK_N + quad * 32 + lane] = __uint_as_float(r[j]);
       }
       cluster_sync_all();
       if (epi) {
-        for (int e = et; e < R * CHUNK; e += 128) {
-          const int i = e % R, c = e / R;
-          const int col = ch * CHUNK + c;
-          if (col >= mcount) continue;
-          const uint32_t off = (uint32_t)((buf * CHUNK * BLOCK_N + c * BLOCK_N + r0 + i) * 4);
-          float w[MAX_CLUSTER];
+        // Rows [r0, r1) of every column, two elements (2C loads) in flight.
+        const int total = R * mcount;
+#pragma unroll 1
+        for (int e0 = et; e0 < total; e0 += 2 * 128) {
+          float w[2][MAX_CLUSTER];
 #pragma unroll
-          for (int p = 0; p < MAX_CLUSTER; ++p)
-            if (p < C) w[p] = ld_dsmem_f32(peer[p] + off);
-          float v = w[0];
+          for (int u = 0; u < 2; ++u) {
+            const int e = e0 + u * 128;
+            const int i = e % R, c = e / R;
+            const uint32_t off = (uint32_t)((c * BLOCK_N + r0 + i) * 4);
+            if (e < total) {
 #pragma unroll
-          for (int p = 1; p < MAX_CLUSTER; ++p)
-            if (p < C) v += w[p];
-          const int n = n_tile * BLOCK_N + r0 + i;
-          if (verify) {
-            fin[col * R + i] = v;
-          } else if (n < args.N) {
-            args.y[(size_t)(m0 + col) * args.N + n] = float_to_bf16_bits(v);
+              for (int p = 0; p < MAX_CLUSTER; ++p)
+                if (p < C) w[u][p] = ld_dsmem_f32(peer[p] + off);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int e = e0 + u * 128;
+            if (e >= total) continue;
+            const int i = e % R, c = e / R;
+            float v = w[u][0];
+#pragma unroll
+            for (int p = 1; p < MAX_CLUSTER; ++p)
+              if (p < C) v += w[u][p];
+            const int n = n_tile * BLOCK_N + r0 + i;
+            if (n < args.N) args.y[(size_t)(m0 + c) * args.N + n] = float_to_bf16_bits(v);
+          }
+        }
+      }
+    } else {
+      const uint32_t red_local = smem_addr(sp.red);
+      uint32_t peer[MAX_CLUSTER];
+  #pragma unroll
+      for (int p = 0; p < MAX_CLUSTER; ++p) peer[p] = (p < C) ? map_to_rank(red_local, (uint32_t)p) : 0u;
+      for (int ch = 0; ch < nchunks; ++ch) {
+        const int buf = ch & 1;
+        float *red = sp.red + buf * CHUNK * BLOCK_N;
+        if (epi) {
+          uint32_t r[32];
+          if (have_acc) {
+            tmem_ld_acc_x32(taddr + ch * CHUNK, nacc_eff, args.Mb, r);
+          } else {
+  #pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+  #pragma unroll
+          for (int j = 0; j < CHUNK; ++j) red[j * BLOCK_N + quad * 32 + lane] = __uint_as_float(r[j]);
+        }
+        cluster_sync_all();
+        if (epi) {
+          for (int e = et; e < R * CHUNK; e += 128) {
+            const int i = e % R, c = e / R;
+            const int col = ch * CHUNK + c;
+            if (col >= mcount) continue;
+            const uint32_t off = (uint32_t)((buf * CHUNK * BLOCK_N + c * BLOCK_N + r0 + i) * 4);
+            float w[MAX_CLUSTER];
+  #pragma unroll
+            for (int p = 0; p < MAX_CLUSTER; ++p)
+              if (p < C) w[p] = ld_dsmem_f32(peer[p] + off);
+            float v = w[0];
+  #pragma unroll
+            for (int p = 1; p < MAX_CLUSTER; ++p)
+              if (p < C) v += w[p];
+            const int n = n_tile * BLOCK_N + r0 + i;
+            if (verify) {
+              fin[col * R + i] = v;
+            } else if (n < args.N) {
+              args.y[(size_t)(m0 + col) * args.N + n] = float_to_bf16_bits(v);
+            }
           }
         }
       }
@@ -655,7 +713,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       named_bar_sync(1, 128);
       // Stage ring after the reduction: fin, then the staged tables when
       // they fit, then the B-row slots.
-      const size_t ring = (size_t)S * stage_bytes;
       const size_t fin_bytes = align_up((size_t)args.Mb * R * 4, 16);
       const VerifyTables vt = stage_verify_tables(args, L, sp.stage0 + fin_bytes,
                                                   ring - fin_bytes - 8 * 128 * sizeof(uint4), m0, mcount, et);
