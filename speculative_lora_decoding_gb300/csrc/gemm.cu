@@ -46,13 +46,12 @@ constexpr int MAX_MB = 512;
 constexpr int CHUNK = 32;                             // accumulator columns per reduction round
 constexpr int RED_BYTES = 2 * CHUNK * BLOCK_N * 4;    // double-buffered reduction tile, 32 KB
 constexpr int MAX_CLUSTER = 16;
-constexpr int MAX_ACC = 1;                            // tensor-memory accumulators per unit
 constexpr size_t SMEM_LIMIT = 220 * 1024;             // leaves room for a co-resident shrink CTA
 constexpr size_t SMEM_FIXED = 1024 + 256;             // alignment slack + barriers
 
 struct GemmArgs {
   int M, N, K;
-  int Mb, nsub, sub_n, n_tgroups, kblocks, C, stages, tmem_cols, red_bytes, nacc;
+  int Mb, nsub, sub_n, n_tgroups, kblocks, C, stages, tmem_cols, red_bytes;
   int mode, prefetch_w;
   int after_shrink;  // launched right after this library's shrink kernel: x and W are ready
   int use_tw, Mpad;  // tensor-core expand allowed (masked operand present), its token rows
@@ -100,18 +99,10 @@ __device__ __forceinline__ void unpack_bf16x2(uint32_t w, float &lo, float &hi) 
   hi = __uint_as_float(w & 0xFFFF0000u);
 }
 
-// Accumulator columns [taddr, taddr + 32) summed over the first nacc
-// accumulators (stride columns apart), in accumulator order.
-__device__ __forceinline__ void tmem_ld_acc_x32(uint32_t taddr, int nacc, int stride, uint32_t (&r)[32]) {
+// Accumulator columns [taddr, taddr + 32) of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_ld_acc_x32(uint32_t taddr, uint32_t (&r)[32]) {
   tmem_ld_x32(taddr, r);
   tmem_ld_wait();
-  for (int a = 1; a < nacc; ++a) {
-    uint32_t t[32];
-    tmem_ld_x32(taddr + (uint32_t)(a * stride), t);
-    tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(t[j]));
-  }
 }
 
 // Tables the verify epilogue reads for every output: the plan's buckets
@@ -193,13 +184,13 @@ __device__ __forceinline__ int4 bucket_at(const GemmArgs &a, const PlanLayout &L
 // transposed so that lanes touch consecutive slots) in one round of loads,
 // then finishes its share of each bucket's columns four at a time:
 //   y[m, n] = bf16(acc[m, n] + scale * sum_{j<r} T[m, j] * B_a[n, j]).
-// The value acc comes from tensor memory (summed over the accumulators) or,
-// after a cluster reduction, from shared memory (fin, column-major [Mb][R]).
+// The value acc comes from tensor memory or, after a cluster reduction, from
+// shared memory (fin, column-major [Mb][R]).
 // The loops over rank chunks stay rolled to keep the code small.
 template <bool FROM_TMEM>
 __device__ __forceinline__ void verify_walk(const GemmArgs &a, const PlanLayout &L, const VerifyTables &vt, uint4 *Bs,
                                             int slot_cap, int et, int n, int m0, int mcount, int first, int step,
-                                            uint32_t taddr, int nacc, const float *fin, int R, int i_row) {
+                                            uint32_t taddr, const float *fin, int R, int i_row) {
   int ai = 0;
   while (ai < vt.nbk) {
     // A group of buckets whose B rows fit the slots: stage them all in one
@@ -276,18 +267,14 @@ __device__ __forceinline__ void verify_walk(const GemmArgs &a, const PlanLayout 
         }
         if (FROM_TMEM) {
           uint32_t own[4];
-#pragma unroll 1
-          for (int ac = 0; ac < nacc; ++ac) {
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              own[jj] = 0u;
-              if (mm[jj] >= 0) tmem_ld_x1(taddr + (uint32_t)(ac * a.Mb + mm[jj] - m0), own[jj]);
-            }
-            tmem_ld_wait();
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-              val[jj] = (ac == 0) ? __uint_as_float(own[jj]) : val[jj] + __uint_as_float(own[jj]);
+          for (int jj = 0; jj < 4; ++jj) {
+            own[jj] = 0u;
+            if (mm[jj] >= 0) tmem_ld_x1(taddr + (uint32_t)(mm[jj] - m0), own[jj]);
           }
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) val[jj] = __uint_as_float(own[jj]);
         } else {
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj)
@@ -405,13 +392,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       const int nkb = kb_hi - kb_lo;
+      // Loop constants in registers (the copies below are asm with memory
+      // clobbers, after which kernel parameters would be re-read).
+      const bool two = args.nsub == 2;
+      const int w_row = n_tile * BLOCK_N, x_row1 = m0 + args.sub_n;
+      const uint32_t x1_bytes = (uint32_t)(args.sub_n * BLOCK_K * 2);
+      const uint32_t tx_bytes = (uint32_t)stage_bytes;
       // With static weights, the first ring of W tiles is requested before the
       // wait for the preceding kernel; x always comes after it.
       const int early = (args.prefetch_w && !args.after_shrink) ? min(nkb, S) : 0;
       for (int i = 0; i < early; ++i) {
-        mbar_arrive_expect_tx(&sp.full[i], (uint32_t)stage_bytes);
-        tma_load_2d(sp.stage0 + (size_t)i * stage_bytes, &tmap_w, &sp.full[i], (kb_lo + i) * BLOCK_K,
-                    n_tile * BLOCK_N, pol_w);
+        mbar_arrive_expect_tx(&sp.full[i], tx_bytes);
+        tma_load_2d(sp.stage0 + (size_t)i * stage_bytes, &tmap_w, &sp.full[i], (kb_lo + i) * BLOCK_K, w_row, pol_w);
       }
       // After this library's shrink kernel nothing the mainloop reads can
       // still be in flight (the shrink released this grid only after its own
@@ -428,12 +420,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             signal_abort(sp, args.status);
             break;
           }
-          mbar_arrive_expect_tx(&sp.full[stage], (uint32_t)stage_bytes);
-          tma_load_2d(st, &tmap_w, &sp.full[stage], kb * BLOCK_K, n_tile * BLOCK_N, pol_w);
+          mbar_arrive_expect_tx(&sp.full[stage], tx_bytes);
+          tma_load_2d(st, &tmap_w, &sp.full[stage], kb * BLOCK_K, w_row, pol_w);
         }
-        for (int s = 0; s < args.nsub; ++s)
-          tma_load_2d(st + W_TILE_BYTES + (size_t)s * args.sub_n * BLOCK_K * 2, &tmap_x, &sp.full[stage],
-                      kb * BLOCK_K, m0 + s * args.sub_n, pol_x);
+        tma_load_2d(st + W_TILE_BYTES, &tmap_x, &sp.full[stage], kb * BLOCK_K, m0, pol_x);
+        if (two) tma_load_2d(st + W_TILE_BYTES + x1_bytes, &tmap_x, &sp.full[stage], kb * BLOCK_K, x_row1, pol_x);
         ++issued;
         if (++stage == S) {
           stage = 0;
@@ -480,30 +471,36 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     bool mma_ok = false;
     if (lane == 0) {
+      // Everything the loop needs is in registers before it starts: this one
+      // thread issues every MMA of the CTA, so the issue path is kept to a
+      // few integer adds per instruction (descriptor start addresses step by
+      // 32 bytes, i.e. 2 in the descriptor's 16-byte units, per 16-wide K step).
       const uint32_t idesc = idesc_bf16_f32(BLOCK_N, args.sub_n);
+      const bool two = args.nsub == 2;
+      const uint32_t d1 = tmem_base + (uint32_t)args.sub_n;
+      const uint64_t x1_off = (uint64_t)((args.sub_n * BLOCK_K * 2) >> 4);
+      const uint32_t ring0 = smem_addr(sp.stage0);
+      const uint32_t sbytes = (uint32_t)stage_bytes;
+      const int k_lo = kb_lo, k_hi = kb_hi;
       int stage = 0;
       uint32_t phase = 0;
       bool issued_any = false, ok = true;
-      for (int kb = kb_lo; kb < kb_hi; ++kb) {
+      for (int kb = k_lo; kb < k_hi; ++kb) {
         if (!mbar_wait_bounded(&sp.full[stage], phase, abort_flag)) {
           signal_abort(sp, args.status);
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t a_addr = smem_addr(sp.stage0 + (size_t)stage * stage_bytes);
-        const uint32_t b_addr = a_addr + W_TILE_BYTES;
-        // The four 16-wide K steps of a stage take turns over nacc
-        // accumulators, so consecutive MMAs do not wait on each other's result.
+        const uint32_t a_addr = ring0 + (uint32_t)stage * sbytes;
+        const uint64_t ad = smem_desc_kmajor_sw128(a_addr);
+        const uint64_t bd = smem_desc_kmajor_sw128(a_addr + W_TILE_BYTES);
+        const uint32_t first = kb > k_lo ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
-          const int acc = kk % args.nacc;
-          const uint64_t adesc = smem_desc_kmajor_sw128(a_addr + kk * 32);
-          for (int s = 0; s < args.nsub; ++s) {
-            const uint64_t bdesc = smem_desc_kmajor_sw128(b_addr + s * args.sub_n * BLOCK_K * 2 + kk * 32);
-            mma_bf16_ss(tmem_base + (uint32_t)(acc * args.Mb + s * args.sub_n), adesc, bdesc, idesc,
-                        (kb > kb_lo || kk >= args.nacc) ? 1u : 0u);
-          }
+          const uint32_t accum = kk > 0 ? 1u : first;
+          mma_bf16_ss(tmem_base, ad + 2 * kk, bd + 2 * kk, idesc, accum);
+          if (two) mma_bf16_ss(d1, ad + 2 * kk, bd + x1_off + 2 * kk, idesc, accum);
         }
         issued_any = true;
         mma_commit(&sp.empty[stage]);
@@ -572,7 +569,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
   const int nchunks = (mcount + CHUNK - 1) / CHUNK;
-  const int nacc_eff = kb_hi > kb_lo ? args.nacc : 1;  // every accumulator gets a K step of each k-block
 
   // Verify work left for the epilogue: none once the tensor cores added it.
   const bool verify = args.mode == MLORA_VERIFY && !expand_done;
@@ -583,7 +579,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!verify) {
         for (int ch = 0; ch < nchunks; ++ch) {
           uint32_t r[32];
-          tmem_ld_acc_x32(taddr + ch * CHUNK, nacc_eff, args.Mb, r);
+          tmem_ld_acc_x32(taddr + ch * CHUNK, r);
           if (n < args.N) {
 #pragma unroll
             for (int j = 0; j < CHUNK; ++j) {
@@ -599,7 +595,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const VerifyTables vt = stage_verify_tables(args, L, sp.stage0, ring - 8 * 128 * sizeof(uint4), m0, mcount, et);
         uint4 *Bs = reinterpret_cast<uint4 *>(sp.stage0 + vt.bytes);
         const int slot_cap = (int)((ring - vt.bytes) / (128 * sizeof(uint4)));
-        verify_walk<true>(args, L, vt, Bs, slot_cap, et, n, m0, mcount, 0, 1, taddr, nacc_eff, nullptr, 0, 0);
+        verify_walk<true>(args, L, vt, Bs, slot_cap, et, n, m0, mcount, 0, 1, taddr, nullptr, 0, 0);
       }
     }
     tc_fence_before_sync();
@@ -624,7 +620,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int ch = 0; ch < nchunks; ++ch) {
           uint32_t r[32];
           if (have_acc) {
-            tmem_ld_acc_x32(taddr + ch * CHUNK, nacc_eff, args.Mb, r);
+            tmem_ld_acc_x32(taddr + ch * CHUNK, r);
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = 0u;
@@ -676,7 +672,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (epi) {
           uint32_t r[32];
           if (have_acc) {
-            tmem_ld_acc_x32(taddr + ch * CHUNK, nacc_eff, args.Mb, r);
+            tmem_ld_acc_x32(taddr + ch * CHUNK, r);
           } else {
   #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = 0u;
@@ -721,7 +717,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // Threads split as (row i, column phase): 128 / R threads share a row.
       const int P = 128 / R;
       const int i = et % R, sub = et / R;
-      verify_walk<false>(args, L, vt, Bs, slot_cap, et, n_tile * BLOCK_N + r0 + i, m0, mcount, sub, P, 0u, 1, fin, R,
+      verify_walk<false>(args, L, vt, Bs, slot_cap, et, n_tile * BLOCK_N + r0 + i, m0, mcount, sub, P, 0u, fin, R,
                          i);
     }
     tc_fence_before_sync();
@@ -808,14 +804,10 @@ GemmShape gemm_shape(int M, int N, int K, int num_sms) {
   s.n_tgroups = tg;
   s.n_units = ((N + BLOCK_N - 1) / BLOCK_N) * tg;
   s.kblocks = (K + BLOCK_K - 1) / BLOCK_K;
-  // Up to four accumulators (the K steps of a stage take turns) while they
-  // fit in the 512 tensor-memory columns.
+  // Tensor-memory columns: a power of two >= 32 holding Mb fp32 columns.
   int cols = 32;
   while (cols < Mb) cols <<= 1;
-  int nacc = 1;
-  while (nacc < MAX_ACC && 2 * nacc * cols <= 512) nacc *= 2;
-  s.nacc = nacc;
-  s.tmem_cols = nacc * cols;
+  s.tmem_cols = cols;
   s.nbuf = 1;
   s.total_iters = s.n_units * s.kblocks;
   // Split-K factor (a power of two, so each CTA owns 128 / C output rows):
@@ -918,7 +910,6 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
   a.C = sh.C;
   a.stages = sh.stages;
   a.tmem_cols = sh.tmem_cols;
-  a.nacc = sh.nacc;
   a.red_bytes = sh.red_bytes;
   a.mode = g.mode;
   a.prefetch_w = g.prefetch_w;

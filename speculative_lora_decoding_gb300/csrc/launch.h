@@ -50,7 +50,6 @@ struct GemmShape {
   int Mb, nsub, sub_n, n_tgroups, n_units, kblocks, total_iters, stages, nbuf, tmem_cols, grid;
   int C;          // CTAs per cluster splitting K (1: no split)
   int red_bytes;  // shared memory for the cluster reduction
-  int nacc;       // tensor-memory accumulators that k-blocks take turns over
   size_t smem_bytes, partial_floats;
 };
 GemmShape gemm_shape(int M, int N, int K, int num_sms);
