@@ -3,11 +3,13 @@
 One step = one InvisibleLoRA decode cycle through one transformer block's
 seven projections on the Llama-3-8B-shaped workload (64 requests, 16
 resident rank-16 adapters with Zipf(1.1) popularity, 1 draft token per
-request, vocabulary 128256):
+request, vocabulary 128256).  Projections that read the same rows go through
+one sliced layer call (q|k|v, gate|up), as a block computes them:
 
-    plan (a1)  ->  draft pass: 7 x base GEMM, M = 64 rows, LoRA off (a3)
-               ->  verify pass: 7 x (shrink a2 + GEMM a3 + fused expand a4), M = 128 rows
-               ->  accept / resample for 64 requests (a5, a6)
+    plan (a1, on a second stream, beside the draft pass)
+    draft pass:  4 layer calls (q|k|v, o, gate|up, down), M = 64 rows, LoRA off (a3)
+    verify pass: 4 x (shrink a2 + GEMM a3 + fused expand a4), M = 128 rows
+    accept / resample for 64 requests (a5, a6)
 
 `value` is verified tokens (M = 128 per step, summed over ranks) per second
 with every input resident in HBM, from CUDA events around K replays of the
@@ -60,12 +62,14 @@ def _peaks():
 # ---------------------------------------------------------------------------
 
 
-def layer_bytes_flops(M, K, N, active_ranks, verify):
+def layer_bytes_flops(M, K, N, active_ranks, verify, n_proj=1):
+    """Algorithmic HBM bytes and flops of one layer call: W, x and y once; in
+    verify mode each active adapter's A (once per projection slice) and B."""
     b = 2 * (N * K + M * K + M * N)
     f = 2 * M * N * K
     if verify:
-        b += sum(2 * r * K + 2 * N * r for r in active_ranks)
-        f += 2 * M * int(np.mean(active_ranks) if active_ranks else 0) * (K + N)
+        b += sum(2 * r * K * n_proj + 2 * N * r for r in active_ranks)
+        f += 2 * M * int(np.mean(active_ranks) if active_ranks else 0) * (K * n_proj + N)
     return b, f
 
 
@@ -142,14 +146,27 @@ class DeviceWorkload:
         self.idx_d = WL.row_adapters(cfg, "draft", seed=seed)
         self.idx_v = WL.row_adapters(cfg, "verify", k=K_DRAFT, seed=seed)
         self.Md, self.Mv = len(self.idx_d), len(self.idx_v)
+        # One entry per input group: the projections' W stacked along N, their
+        # A stacks side by side, their B stacks along N, the shared rows x.
         self.proj = []
-        for p, (name, K, N) in enumerate(cfg.projections):
-            W, A, B, _ = WL.projection_weights(cfg, p, seed=seed)
-            xd = WL.activations(cfg, p, "draft", seed=seed)
-            xv = WL.activations(cfg, p, "verify", k=K_DRAFT, seed=seed)
-            self.proj.append(dict(name=name, K=K, N=N, W=_bf16(torch, W, device), A=_bf16(torch, A, device),
-                                  B=_bf16(torch, B, device), xd=_bf16(torch, xd, device),
-                                  xv=_bf16(torch, xv, device), xd_h=xd, xv_h=xv,
+        for group in WL.input_groups(cfg):
+            Ws, As, Bs = [], [], []
+            for p in group:
+                W, A, B, _ = WL.projection_weights(cfg, p, seed=seed)
+                Ws.append(W)
+                As.append(A)
+                Bs.append(B)
+            K = cfg.projections[group[0]][1]
+            ends = [int(e) for e in np.cumsum([w.shape[0] for w in Ws])]
+            N = ends[-1]
+            name = "_".join(cfg.projections[p][0] for p in group)
+            xd = WL.activations(cfg, group[0], "draft", seed=seed)
+            xv = WL.activations(cfg, group[0], "verify", k=K_DRAFT, seed=seed)
+            self.proj.append(dict(name=name, K=K, N=N, ends=ends, n_proj=len(group),
+                                  W=_bf16(torch, np.concatenate(Ws, axis=0), device),
+                                  A=_bf16(torch, np.stack(As), device),
+                                  B=_bf16(torch, np.concatenate(Bs, axis=1), device),
+                                  xd=_bf16(torch, xd, device), xv=_bf16(torch, xv, device), xd_h=xd, xv_h=xv,
                                   yd=torch.empty((self.Md, N), dtype=torch.bfloat16, device=device),
                                   yv=torch.empty((self.Mv, N), dtype=torch.bfloat16, device=device)))
         self.rank_of = torch.from_numpy(self.ranks).to(device)
@@ -160,7 +177,8 @@ class DeviceWorkload:
         self.p, self.q, self.tok, self.u = (torch.from_numpy(a).to(device) for a in (p, q, tok, u))
         self.out_tok = torch.empty((cfg.n_requests, K_DRAFT + 1), dtype=torch.int32, device=device)
         self.accepted = torch.empty((cfg.n_requests,), dtype=torch.int32, device=device)
-        ws_bytes = max(ml.linear_workspace_bytes(self.Mv, P["N"], P["K"], cfg.n_adapters) for P in self.proj)
+        ws_bytes = max(ml.linear_sliced_workspace_bytes(self.Mv, P["N"], P["K"], cfg.n_adapters, len(P["ends"]))
+                       for P in self.proj)
         ws_bytes = max(ws_bytes, ml.accept_workspace_bytes(cfg.n_requests, K_DRAFT, cfg.vocab))
         self.ws = ml.Workspace(ws_bytes, device=device)
         self.seg = None
@@ -174,20 +192,35 @@ class DeviceWorkload:
             self.seg, _ = ml.plan_segments(self.adx_v, self.rank_of, cfg.n_adapters, cfg.r_max, self.ws)
         out.append(("plan", plan))
         for P in self.proj:
-            out.append((f"draft.{P['name']}", lambda P=P: ml.linear(P["xd"], P["W"], None, None, None, None,
-                                                                     cfg.scale, ml.DRAFT | ml.PREFETCH_WEIGHTS,
-                                                                     ws=self.ws, y=P["yd"])))
+            out.append((f"draft.{P['name']}", lambda P=P: ml.linear_sliced(
+                P["xd"], P["W"], P["ends"], None, None, None, None, cfg.scale, ml.DRAFT | ml.PREFETCH_WEIGHTS,
+                ws=self.ws, y=P["yd"])))
         for P in self.proj:
-            out.append((f"verify.{P['name']}", lambda P=P: ml.linear(P["xv"], P["W"], P["A"], P["B"], self.rank_of,
-                                                                      self.adx_v, cfg.scale,
-                                                                      ml.VERIFY | ml.PREFETCH_WEIGHTS, ws=self.ws,
-                                                                      y=P["yv"], seg_offsets_ptr=self.seg)))
+            out.append((f"verify.{P['name']}", lambda P=P: ml.linear_sliced(
+                P["xv"], P["W"], P["ends"], P["A"], P["B"], self.rank_of, self.adx_v, cfg.scale,
+                ml.VERIFY | ml.PREFETCH_WEIGHTS, ws=self.ws, y=P["yv"], seg_offsets_ptr=self.seg)))
         out.append(("accept", lambda: ml.verify_accept(self.p, self.q, self.tok, self.u, ws=self.ws,
                                                       out_tok=self.out_tok, accepted=self.accepted)))
         return out
 
-    def step(self):
-        for _, f in self.ops():
+    def step(self, side=None):
+        """One step in stream order.  With `side` (a second stream) the plan,
+        which needs only the adapter indices, runs on it concurrently with the
+        draft pass, and the verify pass waits for it."""
+        ops = self.ops()
+        if side is None:
+            for _, f in ops:
+                f()
+            return
+        torch = self.torch
+        main = torch.cuda.current_stream()
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            ops[0][1]()
+        for name, f in ops[1:]:
+            if name.startswith("verify.") and side is not None:
+                main.wait_stream(side)
+                side = None
             f()
 
 
@@ -299,10 +332,11 @@ def run_gpu(args):
 
     wl = DeviceWorkload(torch, ml, device, seed=rank)
     stream = torch.cuda.Stream(device)
+    side = torch.cuda.Stream(device)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
-            wl.step()
+            wl.step(side)
     stream.synchronize()
     if wl.ws.status() != 0:
         raise RuntimeError("device status bits raised during warm-up")
@@ -311,7 +345,7 @@ def run_gpu(args):
     graph = torch.cuda.CUDAGraph()
     n0 = ml.launch_count()
     with torch.cuda.graph(graph, stream=stream):
-        wl.step()
+        wl.step(side)
     launches_per_step = ml.launch_count() - n0
     for _ in range(3):
         graph.replay()
@@ -360,16 +394,17 @@ def run_gpu(args):
         draft_b += b
         draft_f += f
         draft_t += op_ms[f"draft.{P['name']}"]
-        b, f = layer_bytes_flops(wl.Mv, P["K"], P["N"], active_ranks, True)
+        b, f = layer_bytes_flops(wl.Mv, P["K"], P["N"], active_ranks, True, P["n_proj"])
         verify_b += b
         verify_f += f
         verify_t += op_ms[f"verify.{P['name']}"]
     acc_host = wl.accepted.cpu().numpy()
     acc_b = accept_bytes(CFG.n_requests, CFG.vocab, acc_host, K_DRAFT)
-    gemm_launches = 2 * len(wl.proj)
-    achieved = draft_b / (draft_t * 1e-3) / 1e9          # draft GEMM launches: one kernel each
+    achieved = draft_b / (draft_t * 1e-3) / 1e9          # draft layer calls: one GEMM kernel each
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
-                "traffic": None, "kernel": "gemm_kernel (draft pass, 7 projections, M=64)",
+                "traffic": None,
+                "kernel": f"gemm_kernel (draft pass, {len(wl.proj)} launches: "
+                          + ", ".join(P["name"] for P in wl.proj) + ", M=64)",
                 "peak_kind": f"{peak_kind} hbm_gbs",
                 "algorithmic_bytes_per_launch": draft_b / len(wl.proj),
                 "avg_launch_us": 1e3 * draft_t / len(wl.proj)}
@@ -389,7 +424,7 @@ def run_gpu(args):
     }
 
     # End to end through the binding with pinned host buffers.
-    e2e = run_e2e(torch, ml, wl, stream, args, world)
+    e2e = run_e2e(torch, ml, wl, stream, side, args, world)
 
     cpu = None
     if rank == 0 and world == 1:
@@ -414,10 +449,12 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": CFG.name + f"/k={K_DRAFT}/vocab={CFG.vocab}", "requests": CFG.n_requests,
-                       "draft_rows": wl.Md, "verify_rows": wl.Mv, "projections": [p["name"] for p in wl.proj],
+                       "draft_rows": wl.Md, "verify_rows": wl.Mv,
+                       "projections": [p[0] for p in CFG.projections],
+                       "layer_calls": [p["name"] for p in wl.proj],
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2: 436 MB of W streamed per pass, two passes per step",
-                       "graph": "one CUDA graph per step"},
+                       "graph": "one CUDA graph per step; the plan runs on a second stream beside the draft pass"},
             "gpu_launches": launches_per_step * args.steps,
             "roofline": roofline,
             "modes": modes,
@@ -476,7 +513,7 @@ def per_op_durations(torch, wl, stream, args):
              for i, (name, _) in enumerate(op_graphs)}, "one graph per op")
 
 
-def run_e2e(torch, ml, wl, stream, args, world):
+def run_e2e(torch, ml, wl, stream, side, args, world):
     """Host buffers in, host buffers out, through the public binding."""
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     h_x = [(pin(P["xd_h"].view(np.int16)), pin(P["xv_h"].view(np.int16))) for P in wl.proj]
@@ -498,7 +535,7 @@ def run_e2e(torch, ml, wl, stream, args, world):
         wl.adx_v.copy_(h_idx, non_blocking=True)
         for d, h in zip((wl.p, wl.q, wl.tok, wl.u), h_acc):
             d.copy_(h, non_blocking=True)
-        wl.step()
+        wl.step(side)
         for P, hd, hv in zip(wl.proj, h_yd, h_yv):
             hd.copy_(P["yd"].view(torch.int16), non_blocking=True)
             hv.copy_(P["yv"].view(torch.int16), non_blocking=True)

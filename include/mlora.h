@@ -11,6 +11,8 @@
  *                        formula is "output = W·x + scale · B(A·x)" of "Multi-
  *                        LoRA Serving in Practice", section "Core Principle:
  *                        Shared Base Model, Per-Request Adapter Selection".
+ *   mlora_linear_sliced  the same layer for projections that share their
+ *                        input rows (q/k/v, gate/up), in one launch
  *   mlora_verify_accept  the per-request accept / resample step that ends the
  *                        verify pass and keeps the target distribution
  *                        (speculative sampling; exact integer residual draw).
@@ -36,7 +38,10 @@
  * mlora_workspace_init once after allocating it (and after any call that
  * returned MLORA_ERR_TIMEOUT).  Kernels leave the counters at zero when they
  * finish, so one workspace serves any sequence of calls on one stream.  Calls
- * that use the same workspace must not overlap in time (e.g. on two streams).
+ * that use the same workspace must not overlap in time (e.g. on two streams),
+ * with one exception: draft-mode layer calls touch nothing in the workspace
+ * but the status word, so they may overlap mlora_plan_segments on another
+ * stream (a decode step can plan the verify pass while it drafts).
  */
 #ifndef MLORA_H
 #define MLORA_H
@@ -91,6 +96,7 @@ typedef enum {
 #define MLORA_MAX_ADAPTERS 4096
 #define MLORA_MAX_ROWS 65536
 #define MLORA_MAX_VOCAB (1 << 24)
+#define MLORA_MAX_SLICES 4         /* output slices of one mlora_linear_sliced call */
 
 /* ------------------------------------------------------------------------- */
 /* Workspace                                                                  */
@@ -101,6 +107,10 @@ typedef enum {
  * current device.  One workspace sized for the largest (M, N, K) of a set of
  * projections serves all of them.  Returns 0 for sizes outside the ranges. */
 MLORA_API size_t mlora_linear_workspace_bytes(int M, int N, int K, int n_adapters);
+
+/* Bytes of workspace mlora_linear_sliced needs with n_slices output slices
+ * (1..MLORA_MAX_SLICES); equal to mlora_linear_workspace_bytes for one. */
+MLORA_API size_t mlora_linear_sliced_workspace_bytes(int M, int N, int K, int n_adapters, int n_slices);
 
 /* Bytes of workspace mlora_verify_accept needs (B requests, k drafts, V vocab). */
 MLORA_API size_t mlora_accept_workspace_bytes(int B, int k, int V);
@@ -184,6 +194,36 @@ MLORA_API mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlo
                           const int32_t *rank_of, const int32_t *adapter_idx, const int32_t *seg_offsets,
                           float scale, int mode, mlora_bf16 *y, void *workspace, size_t ws_bytes,
                           mlora_stream stream);
+
+/* The same layer for several projections that read the same rows x, in one
+ * launch of each kernel: q, k and v of an attention block, or gate and up of
+ * its MLP ("Multi-LoRA Serving in Practice" lists q_proj, k_proj, v_proj,
+ * o_proj, gate_proj, up_proj and down_proj as the usual LoRA targets).  The
+ * pages define the layer per projection; fusing projections that share their
+ * input is this library's layout, not the pages'.  Output slice s covers
+ * output features [slice_end[s-1], slice_end[s]) (slice_end[-1] = 0):
+ *
+ *   y[m, n] = sum_k W[n, k] x[m, k]
+ *             + [verify] scale * sum_{j<r} B_a[n, j] * sum_k A_{s,a}[j, k] x[m, k]
+ *
+ *   W        bf16 [N, K]   the projections' weights stacked along N
+ *   slice_end   HOST int32 [n_slices], 1 <= n_slices <= MLORA_MAX_SLICES,
+ *            increasing, each but the last a multiple of 128, the last == N
+ *   A_stack  bf16 [n_slices, n_adapters, r_max, K]   each slice's own A
+ *   B_stack  bf16 [n_adapters, N, r_max]   each adapter's B of every slice,
+ *            stacked along N like W
+ *   rank_of  int32 [n_adapters]: one rank per adapter for all its slices
+ *   y        bf16 [M, N] out
+ * Everything else as mlora_linear; with n_slices = 1 it is mlora_linear.  The
+ * workspace must have mlora_linear_sliced_workspace_bytes(M, N, K, n_adapters,
+ * n_slices) bytes; a plan from mlora_plan_segments on it serves any number of
+ * slices.  Bad slice ends return MLORA_ERR_SHAPE. */
+MLORA_API mlora_status mlora_linear_sliced(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W, int N,
+                                           int n_slices, const int32_t *slice_end, const mlora_bf16 *A_stack,
+                                           const mlora_bf16 *B_stack, int n_adapters, int r_max,
+                                           const int32_t *rank_of, const int32_t *adapter_idx,
+                                           const int32_t *seg_offsets, float scale, int mode, mlora_bf16 *y,
+                                           void *workspace, size_t ws_bytes, mlora_stream stream);
 
 /* Allocation-free variant of mlora_linear.  The paper has no counterpart;
  * this is for callers that cannot allocate device memory for a workspace (a

@@ -7,6 +7,7 @@ There is no CPU or PyTorch fallback: if ``libmlora.so`` is missing or the
 device is not compute capability 10.3, the calls raise.
 
     linear(x, W, A_stack, B_stack, rank_of, adapter_idx, scale, mode)   steps a1-a4
+    linear_sliced(x, W, slice_end, A_stack, B_stack, ...)               the same, projections sharing x
     verify_accept(p, q, draft_tok, uniforms)                             steps a5-a6
     plan_segments(...), shrink(...)                                      steps a1, a2 alone
 
@@ -48,6 +49,7 @@ _c_float = ctypes.c_float
 
 _SIGNATURES = {
     "mlora_linear_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "mlora_linear_sliced_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "mlora_accept_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
     "mlora_workspace_init": (_c_int, [_c_ptr, _c_size, _c_ptr]),
     "mlora_read_device_status": (_c_int, [_c_ptr, ctypes.POINTER(ctypes.c_uint32), _c_int, _c_ptr]),
@@ -57,6 +59,9 @@ _SIGNATURES = {
                               _c_ptr]),
     "mlora_linear": (_c_int, [_c_ptr, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_ptr,
                               _c_ptr, _c_ptr, _c_float, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "mlora_linear_sliced": (_c_int, [_c_ptr, _c_int, _c_int, _c_ptr, _c_int, _c_int, ctypes.POINTER(ctypes.c_int32),
+                                     _c_ptr, _c_ptr, _c_int, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_float, _c_int, _c_ptr,
+                                     _c_ptr, _c_size, _c_ptr]),
     "mlora_verify_accept": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr, _c_ptr,
                                      _c_ptr, _c_size, _c_ptr]),
     "mlora_linear_noalloc": (_c_int, [_c_ptr, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int,
@@ -136,6 +141,10 @@ def launch_count() -> int:
 
 def linear_workspace_bytes(M: int, N: int, K: int, n_adapters: int) -> int:
     return int(_load().mlora_linear_workspace_bytes(M, N, K, n_adapters))
+
+
+def linear_sliced_workspace_bytes(M: int, N: int, K: int, n_adapters: int, n_slices: int) -> int:
+    return int(_load().mlora_linear_sliced_workspace_bytes(M, N, K, n_adapters, n_slices))
 
 
 def accept_workspace_bytes(B: int, k: int, V: int) -> int:
@@ -229,6 +238,45 @@ def linear(x: torch.Tensor, W: torch.Tensor, A_stack, B_stack, rank_of, adapter_
                               b_ptr, n_ad, r_max, r_ptr, i_ptr, seg_offsets_ptr, float(scale), int(mode),
                               _need(y, "y", torch.bfloat16, 2), ws.ptr, ws.nbytes, _stream(stream))
     _check(st, "linear")
+    return y
+
+
+def linear_sliced(x: torch.Tensor, W: torch.Tensor, slice_end, A_stack, B_stack, rank_of, adapter_idx,
+                  scale: float, mode: int, ws: Workspace = None, y: torch.Tensor = None, seg_offsets_ptr: int = None,
+                  stream=None) -> torch.Tensor:
+    """mlora_linear_sliced: projections that read the same rows x in one call.
+
+    W [N, K] stacks the projections along N; `slice_end` (host ints) gives
+    each slice's end row; A_stack is [n_slices, n_ad, r_max, K] and B_stack
+    [n_ad, N, r_max].  Returns y [M, N] (bf16)."""
+    M, K = x.shape
+    N, K2 = W.shape
+    if K2 != K:
+        raise ValueError("W and x disagree on K")
+    ends = [int(e) for e in slice_end]
+    S = len(ends)
+    verify = (mode & ~PREFETCH_WEIGHTS) == VERIFY
+    n_ad, r_max = 0, 0
+    a_ptr = b_ptr = r_ptr = i_ptr = None
+    if verify:
+        S2, n_ad, r_max, K3 = A_stack.shape
+        if S2 != S or K3 != K or tuple(B_stack.shape) != (n_ad, N, r_max):
+            raise ValueError("A_stack [S, n_ad, r_max, K] / B_stack [n_ad, N, r_max] shapes disagree")
+        a_ptr = _need(A_stack, "A_stack", torch.bfloat16, 4)
+        b_ptr = _need(B_stack, "B_stack", torch.bfloat16, 3)
+        r_ptr = _need(rank_of, "rank_of", torch.int32, 1)
+        i_ptr = _need(adapter_idx, "adapter_idx", torch.int32, 1)
+        if adapter_idx.numel() != M or rank_of.numel() != n_ad:
+            raise ValueError("adapter_idx must have M entries and rank_of n_adapters entries")
+    if ws is None:
+        ws = Workspace(linear_sliced_workspace_bytes(M, N, K, max(n_ad, 1), S), device=x.device, stream=stream)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    ends_c = (ctypes.c_int32 * max(S, 1))(*ends)
+    st = _load().mlora_linear_sliced(_need(x, "x", torch.bfloat16, 2), M, K, _need(W, "W", torch.bfloat16, 2), N, S,
+                                     ends_c, a_ptr, b_ptr, n_ad, r_max, r_ptr, i_ptr, seg_offsets_ptr, float(scale),
+                                     int(mode), _need(y, "y", torch.bfloat16, 2), ws.ptr, ws.nbytes, _stream(stream))
+    _check(st, "linear_sliced")
     return y
 
 

@@ -115,7 +115,7 @@ __device__ __forceinline__ uint64_t block_excl_scan_u64(uint64_t v, uint64_t *sh
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint64_t inc = warp_incl_scan_u64(v);
   if (lane == 31) sh[warp] = inc;
-  __syncthreads();
+  block_sync();
   uint64_t before = 0, all = 0;
 #pragma unroll
   for (int w = 0; w < ACC_WARPS; ++w) {
@@ -123,7 +123,7 @@ __device__ __forceinline__ uint64_t block_excl_scan_u64(uint64_t v, uint64_t *sh
     if (w < warp) before += t;
     all += t;
   }
-  __syncthreads();
+  block_sync();
   *total = all;
   return before + inc - v;
 }
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(ACC_THREADS)
     }
     sh_n = n;
   }
-  __syncthreads();
+  block_sync();
   const int n = sh_n;
   const bool residual = n < k;
   const float *prow = p + ((size_t)b * k1 + n) * V;
@@ -239,12 +239,12 @@ __global__ void __launch_bounds__(ACC_THREADS)
     __threadfence();
   }
   if (flags) atomicOr(&sh_flags, flags);
-  __syncthreads();
+  block_sync();
   if (tid == 0) {
     const uint32_t old = atomicAdd(&counters[b], 1u);
     sh_last = (old == (uint32_t)(slices - 1));
   }
-  __syncthreads();
+  block_sync();
   if (!sh_last) {
     if (tid == 0 && sh_flags) raise_status(status, sh_flags);
     return;
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(ACC_THREADS)
     sh_mode = mode;
     if (f2) raise_status(status, f2);
   }
-  __syncthreads();
+  block_sync();
   const int mode = sh_mode;
   if (sh_tok < 0) {
     const uint64_t T = sh_T;
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(ACC_THREADS)
       run += w;
     }
   }
-  __syncthreads();
+  block_sync();
 
   if (sh_tok < 0) {
     // Pass 2: one round over the chosen sub-range, a contiguous run per thread.
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(ACC_THREADS)
       }
     }
   }
-  __syncthreads();
+  block_sync();
   if (tid == 0) {
     int tok = sh_tok;
     if (tok < 0) tok = 0;  // unreachable when the sums are consistent

@@ -21,29 +21,52 @@ static int device_sms() {
 static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct LinearLayout {
-  size_t plan, T, tw, total;  // tw == 0: no masked operand (tensor-core expand off)
+  size_t plan, T, tw, sk, total;  // tw == 0: no masked operand; sk == 0: no stream-K scratch
 };
 
-static LinearLayout linear_layout(int M, int N, int K, int n_ad, int sms) {
+// Flag words of the stream-K GEMM: the upper half of the counter array.
+constexpr size_t SK_FLAGS_OFF = WS_COUNTERS_OFF + 4 * (WS_MAX_COUNTERS / 2);
+
+// Workspace of a layer call with n_slices output slices: the plan (at the
+// same offset for every call, so one plan serves all of them), then T and the
+// masked low-rank operand of the tensor-core expand, one of each per slice.
+static LinearLayout linear_layout(int M, int n_ad, int n_slices, int sms) {
   LinearLayout L;
   const PlanLayout P = plan_layout(M, n_ad);
   size_t o = WS_SCRATCH_OFF;
   L.plan = o;
   o = align_up(o + P.words * 4, 256);
   L.T = o;
-  o = align_up(o + (size_t)M * T_STRIDE * 4, 256);
-  // Masked low-rank operand of the tensor-core expand (one token group of at
-  // most 256 rows, loaded by a single MMA).
+  o = align_up(o + (size_t)n_slices * M * T_STRIDE * 4, 256);
+  // Masked operand: one token group of at most 256 rows, loaded by a single MMA.
   L.tw = 0;
   if (M <= 256 && n_ad > 0) {
     L.tw = o;
-    o = align_up(o + (size_t)max_expand_slices(M, n_ad) * expand_rows(M) * 32, 256);
+    o = align_up(o + (size_t)n_slices * max_expand_slices(M, n_ad) * expand_rows(M) * 32, 256);
   }
-  (void)N;
-  (void)K;
-  (void)sms;
+  // Partial sums of the stream-K GEMM (one tile's worth per SM).
+  L.sk = 0;
+  const size_t skb = sk_partial_bytes(M, sms);
+  if (skb) {
+    L.sk = o;
+    o = align_up(o + skb, 256);
+  }
   L.total = o;
   return L;
+}
+
+// Slice ends: increasing, every one but the last a multiple of 128 (the
+// GEMM's tile height), the last equal to N.
+static bool slices_ok(int N, int n_slices, const int32_t *slice_end) {
+  if (n_slices < 1 || n_slices > MLORA_MAX_SLICES || !slice_end) return false;
+  int prev = 0;
+  for (int i = 0; i < n_slices; ++i) {
+    const int e = slice_end[i];
+    if (e <= prev) return false;
+    if (i + 1 < n_slices && (e % 128) != 0) return false;
+    prev = e;
+  }
+  return prev == N;
 }
 
 static bool linear_sizes_ok(int M, int N, int K, int n_ad) {
@@ -65,7 +88,14 @@ size_t mlora_linear_workspace_bytes(int M, int N, int K, int n_adapters) {
   if (!linear_sizes_ok(M, N, K, n_adapters)) return 0;
   int sms = device_sms();
   if (sms <= 0) sms = 160;
-  return linear_layout(M, N, K, n_adapters, sms).total;
+  return linear_layout(M, n_adapters, 1, sms).total;
+}
+
+size_t mlora_linear_sliced_workspace_bytes(int M, int N, int K, int n_adapters, int n_slices) {
+  if (!linear_sizes_ok(M, N, K, n_adapters) || n_slices < 1 || n_slices > MLORA_MAX_SLICES) return 0;
+  int sms = device_sms();
+  if (sms <= 0) sms = 160;
+  return linear_layout(M, n_adapters, n_slices, sms).total;
 }
 
 size_t mlora_accept_workspace_bytes(int B, int k, int V) {
@@ -105,11 +135,7 @@ mlora_status mlora_plan_segments(const int32_t *adapter_idx, int M, const int32_
   if (ws_bytes < WS_SCRATCH_OFF + P.words * 4) return MLORA_ERR_WORKSPACE;
   int32_t *plan = reinterpret_cast<int32_t *>((uint8_t *)workspace + WS_SCRATCH_OFF);
   uint32_t *status = reinterpret_cast<uint32_t *>((uint8_t *)workspace + WS_STATUS_OFF);
-  // The masked operand sits after the plan when the workspace is large
-  // enough for the layer (mlora_linear checks that size itself).
-  const LinearLayout LL = linear_layout(M, 1, 8, n_adapters, 1);
-  uint16_t *tw = (LL.tw && ws_bytes >= LL.total) ? reinterpret_cast<uint16_t *>((uint8_t *)workspace + LL.tw) : nullptr;
-  cudaError_t e = launch_plan(adapter_idx, M, rank_of, n_adapters, r_max, plan, status, tw, (cudaStream_t)stream);
+  cudaError_t e = launch_plan(adapter_idx, M, rank_of, n_adapters, r_max, plan, status, (cudaStream_t)stream);
   if (e != cudaSuccess) return MLORA_ERR_CUDA;
   if (seg_offsets) *seg_offsets = plan + P.seg_offsets;
   if (perm) *perm = plan + P.perm;
@@ -132,14 +158,15 @@ mlora_status mlora_shrink(const mlora_bf16 *x, int M, int K, const mlora_bf16 *A
   const int sms = device_sms();
   if (sms <= 0) return MLORA_ERR_CUDA;
   cudaError_t e =
-      launch_shrink(x, M, K, A_stack, n_adapters, r_max, plan, T, r_max, true, sms, nullptr, 1.f, (cudaStream_t)stream);
+      launch_shrink(x, M, K, A_stack, n_adapters, r_max, plan, T, r_max, true, sms, nullptr, 1.f, 1, (cudaStream_t)stream);
   return cuda_status(e);
 }
 
-mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W, int N, const mlora_bf16 *A_stack,
-                          const mlora_bf16 *B_stack, int n_adapters, int r_max, const int32_t *rank_of,
-                          const int32_t *adapter_idx, const int32_t *seg_offsets, float scale, int mode,
-                          mlora_bf16 *y, void *workspace, size_t ws_bytes, mlora_stream stream) {
+static mlora_status linear_impl(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W, int N, int n_slices,
+                                const int32_t *slice_end, const mlora_bf16 *A_stack, const mlora_bf16 *B_stack,
+                                int n_adapters, int r_max, const int32_t *rank_of, const int32_t *adapter_idx,
+                                const int32_t *seg_offsets, float scale, int mode, mlora_bf16 *y, void *workspace,
+                                size_t ws_bytes, mlora_stream stream) {
   if (!x || !W || !y) return MLORA_ERR_ARG;
   const int prefetch_w = (mode & MLORA_PREFETCH_WEIGHTS) ? 1 : 0;
   const int base_mode = mode & ~MLORA_PREFETCH_WEIGHTS;
@@ -147,6 +174,7 @@ mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W
   const bool verify = base_mode == MLORA_VERIFY;
   if (verify && (!A_stack || !B_stack || !rank_of || !adapter_idx)) return MLORA_ERR_ARG;
   if (!linear_sizes_ok(M, N, K, verify ? n_adapters : 0)) return MLORA_ERR_SHAPE;
+  if (!slices_ok(N, n_slices, slice_end)) return MLORA_ERR_SHAPE;
   if (verify && (n_adapters < 1 || r_max < 8 || r_max > MLORA_MAX_RANK || (r_max % 8) != 0)) return MLORA_ERR_SHAPE;
   if (!aligned(x, 16) || !aligned(W, 16)) return MLORA_ERR_ARG;
   if (verify && (!aligned(A_stack, 16) || !aligned(B_stack, 16))) return MLORA_ERR_ARG;
@@ -154,7 +182,8 @@ mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W
   const int sms = device_sms();
   if (sms <= 0) return MLORA_ERR_CUDA;
   const int n_ad = verify ? n_adapters : 0;
-  const LinearLayout L = linear_layout(M, N, K, n_ad, sms);
+  const int S = verify ? n_slices : 1;  // the draft pass is one plain GEMM over all slices
+  const LinearLayout L = linear_layout(M, n_ad, S, sms);
   if (ws_bytes < L.total) return MLORA_ERR_WORKSPACE;
 
   cudaStream_t s = (cudaStream_t)stream;
@@ -167,21 +196,22 @@ mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W
   if (verify) {
     const PlanLayout P = plan_layout(M, n_ad);
     if (seg_offsets == nullptr) {
-      e = launch_plan(adapter_idx, M, rank_of, n_ad, r_max, plan, status, tw, s);
+      e = launch_plan(adapter_idx, M, rank_of, n_ad, r_max, plan, status, s);
       if (e != cudaSuccess) return MLORA_ERR_CUDA;
     } else if (seg_offsets != plan + P.seg_offsets) {
       return MLORA_ERR_ARG;
     }
-    e = launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, tw, scale, s);
+    e = launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, tw, scale, S, s);
     if (e != cudaSuccess) return MLORA_ERR_CUDA;
   }
-  const GemmShape sh = gemm_shape(M, N, K, sms);
   GemmLaunch g;
   g.x = x;
   g.W = W;
   g.M = M;
   g.N = N;
   g.K = K;
+  g.n_slices = S;
+  for (int i = 0; i < MLORA_MAX_SLICES; ++i) g.slice_end[i] = (verify && i < S) ? slice_end[i] : N;
   g.mode = base_mode;
   g.prefetch_w = prefetch_w;
   g.after_shrink = verify ? 1 : 0;
@@ -195,9 +225,39 @@ mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W
   g.status = status;
   g.tw = verify ? tw : nullptr;
   int err = 0;
-  e = launch_gemm(g, sh, s, &err);
+  // The persistent stream-K GEMM takes batches of up to 256 rows in draft
+  // mode, and in verify mode when the tensor-core expand is certain to apply
+  // (every (adapter, 16-rank block) pair the plan can list fits the budget
+  // expand blocks x 128 <= K); otherwise the cluster split-K GEMM runs.
+  const SkShape sk = sk_shape(M, N, K, sms);
+  const long long max_blocks = (long long)(M < n_ad ? M : n_ad) * ((r_max + 15) / 16);
+  const bool sk_fits = sk.ok && L.sk != 0 && (!verify || (tw != nullptr && max_blocks * 128 <= K));
+  if (sk_fits) {
+    e = launch_gemm_sk(g, sk, reinterpret_cast<float *>(ws + L.sk), reinterpret_cast<uint32_t *>(ws + SK_FLAGS_OFF), s,
+                       &err);
+  } else {
+    e = launch_gemm(g, gemm_shape(M, N, K, sms), s, &err);
+  }
   if (err) return MLORA_ERR_ARG;
   return cuda_status(e);
+}
+
+mlora_status mlora_linear(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W, int N, const mlora_bf16 *A_stack,
+                          const mlora_bf16 *B_stack, int n_adapters, int r_max, const int32_t *rank_of,
+                          const int32_t *adapter_idx, const int32_t *seg_offsets, float scale, int mode,
+                          mlora_bf16 *y, void *workspace, size_t ws_bytes, mlora_stream stream) {
+  const int32_t end[1] = {N};
+  return linear_impl(x, M, K, W, N, 1, end, A_stack, B_stack, n_adapters, r_max, rank_of, adapter_idx, seg_offsets,
+                     scale, mode, y, workspace, ws_bytes, stream);
+}
+
+mlora_status mlora_linear_sliced(const mlora_bf16 *x, int M, int K, const mlora_bf16 *W, int N, int n_slices,
+                                 const int32_t *slice_end, const mlora_bf16 *A_stack, const mlora_bf16 *B_stack,
+                                 int n_adapters, int r_max, const int32_t *rank_of, const int32_t *adapter_idx,
+                                 const int32_t *seg_offsets, float scale, int mode, mlora_bf16 *y, void *workspace,
+                                 size_t ws_bytes, mlora_stream stream) {
+  return linear_impl(x, M, K, W, N, n_slices, slice_end, A_stack, B_stack, n_adapters, r_max, rank_of, adapter_idx,
+                     seg_offsets, scale, mode, y, workspace, ws_bytes, stream);
 }
 
 mlora_status mlora_verify_accept(const float *p_target, const float *q_draft, const int32_t *draft_tok,

@@ -48,7 +48,9 @@ __host__ __device__ inline int expand_rows(int M) { return (M + 15) / 16 * 16; }
 // Plan layout inside scratch (int32 words), for M rows and n_ad adapters.
 struct PlanLayout {
   size_t hdr;         // [0] n_active, [1] shrink items, [2] rows, [3] largest active rank,
-                      // [4] expand slices, [5] 1 if the masked operand buffer is zeroed and usable
+                      // [4] expand slices (adapter, 16-rank block) over the active adapters,
+                      // [5] 1 if every active rank is a multiple of 16 or r_max (16-wide
+                      //     blocks of B then read no padding column inside r_max)
   size_t seg_offsets; // [n_ad + 2]
   size_t perm;        // [M]
   size_t row_adapter; // [M]   validated adapter per row (-1: none)
@@ -101,6 +103,14 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first 1024-byte aligned byte of a dynamic shared-memory array (the
+// 128-byte swizzle patterns repeat every 1024 bytes).  Offsetting the array
+// itself keeps the pointer in the shared window for the compiler, so
+// accesses through it are shared-memory instructions, not generic ones.
+__device__ __forceinline__ uint8_t *align_smem_1024(uint8_t *smem_base) {
+  return smem_base + ((1024u - (smem_addr(smem_base) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
@@ -151,6 +161,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory; completion as transaction bytes.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(smem_dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+// Generic-proxy accesses to global memory made visible (for example by an
+// acquire) are ordered before this thread's later async-proxy (bulk copy)
+// accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // 2-D tiled load of the box at (c0 = inner coordinate, c1 = row) into shared
@@ -316,6 +342,14 @@ __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// CTA barrier reached by converged warps: bar.sync counts whole warps, so a
+// warp whose lanes are still on different paths (one lane finishing a
+// single-thread block) is first brought back together.
+__device__ __forceinline__ void block_sync() {
+  __syncwarp();
+  __syncthreads();
+}
+
 // Named barrier over `nthreads` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -340,11 +374,30 @@ __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
+// Flags between CTAs of one grid: a release store after the data it
+// publishes, an acquire load before the data is read.
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Shared-memory writes by threads become visible to the tensor cores (the
+// async proxy) that read the same bytes as an MMA operand.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void sleep_ns(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
-  __nv_bfloat16 h = __float2bfloat16_rn(f);
-  return *reinterpret_cast<uint16_t *>(&h);
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
 }  // namespace mlora

@@ -55,14 +55,27 @@ struct GemmArgs {
   int mode, prefetch_w;
   int after_shrink;  // launched right after this library's shrink kernel: x and W are ready
   int use_tw, Mpad;  // tensor-core expand allowed (masked operand present), its token rows
+  int n_slices;      // output slices: tile rows [slice_end[s-1], slice_end[s]) use T and masked operand s
+  int slice_end[MLORA_MAX_SLICES];
+  int tw_slice_rows; // rows of one slice's masked operand (expand slices x Mpad)
   float scale;
   uint16_t *y;
   const uint16_t *B_stack;
   int r_max, n_ad;
-  const float *T;
+  const float *T;  // [n_slices][M][T_STRIDE]
   const int32_t *plan;
   uint32_t *status;
 };
+
+// Output slice of the tile starting at W row n0 (slice boundaries are
+// multiples of the tile height, so a tile never straddles two).
+__device__ __forceinline__ int slice_of(const GemmArgs &a, int n0) {
+  int s = 0;
+#pragma unroll
+  for (int i = 0; i + 1 < MLORA_MAX_SLICES; ++i)
+    if (i + 1 < a.n_slices && n0 >= a.slice_end[i]) s = i + 1;
+  return s;
+}
 
 struct SmemPtrs {
   uint8_t *stage0;
@@ -71,6 +84,7 @@ struct SmemPtrs {
   uint32_t *tmem_slot;
   int *abort_flag;
   int *acc_ready;
+  int *zero_word;  // stays 0: for waits that only a time limit may end
 };
 
 __device__ __forceinline__ SmemPtrs carve_smem(uint8_t *base, int stages, int stage_bytes, int red_bytes) {
@@ -86,6 +100,7 @@ __device__ __forceinline__ SmemPtrs carve_smem(uint8_t *base, int stages, int st
   p.tmem_slot = w;
   p.abort_flag = reinterpret_cast<int *>(w + 1);
   p.acc_ready = reinterpret_cast<int *>(w + 2);
+  p.zero_word = reinterpret_cast<int *>(w + 3);
   return p;
 }
 
@@ -117,8 +132,8 @@ struct VerifyTables {
   size_t bytes;         // shared memory the staged tables occupy (0: not staged)
 };
 
-__device__ __forceinline__ VerifyTables stage_verify_tables(const GemmArgs &a, const PlanLayout &L, uint8_t *base,
-                                                            size_t avail, int m0, int mcount, int et) {
+__device__ __forceinline__ VerifyTables stage_verify_tables(const GemmArgs &a, const PlanLayout &L, const float *Tu,
+                                                            uint8_t *base, size_t avail, int m0, int mcount, int et) {
   const int32_t *plan = a.plan;
   const int n_active = plan[L.hdr + 0];
   const int rmax = plan[L.hdr + 3];
@@ -126,7 +141,7 @@ __device__ __forceinline__ VerifyTables stage_verify_tables(const GemmArgs &a, c
   VerifyTables v;
   v.bk = nullptr;
   v.perm = plan + L.perm;
-  v.T = a.T;
+  v.T = Tu;
   v.t_row0 = 0;
   v.t_stride = T_STRIDE;
   v.nbk = n_active + 1;
@@ -146,7 +161,7 @@ __device__ __forceinline__ VerifyTables stage_verify_tables(const GemmArgs &a, c
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int e = e0 + k * 128;
-      v[k] = e < nt ? a.T[(size_t)(m0 + e / rs) * T_STRIDE + e % rs] : 0.f;
+      v[k] = e < nt ? Tu[(size_t)(m0 + e / rs) * T_STRIDE + e % rs] : 0.f;
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k)
@@ -327,13 +342,15 @@ __device__ __forceinline__ void verify_walk(const GemmArgs &a, const PlanLayout 
 // slice) adds B_a[n0:n0+128, slice] x Tmask[:, slice]^T, where Tmask holds
 // scale * T for the adapter's own rows and 0 elsewhere (written by the plan
 // and shrink kernels).  Worth it while the slices' MMA work stays small
-// against the base GEMM (slices * 16 <= K / 8); otherwise the epilogue
-// bucket walk adds the low-rank term on the CUDA cores.
+// against the base GEMM (slices * 16 <= K / 8), and while every active rank
+// is a multiple of 16 or r_max: a 16-wide block of B columns must not reach
+// the caller's padding inside r_max (it may hold NaN, and NaN * 0 is NaN).
+// Otherwise the epilogue bucket walk adds the low-rank term on the CUDA
+// cores, masking per element.
 __device__ __forceinline__ int expand_slices_tc(const GemmArgs &a, const PlanLayout &L) {
   if (!a.use_tw || a.mode != MLORA_VERIFY) return -1;
-  const int32_t *plan = a.plan;
-  if (plan[L.hdr + 5] != 1) return -1;
-  const int ns = plan[L.hdr + 4];
+  if (a.plan[L.hdr + 5] != 1) return -1;
+  const int ns = a.plan[L.hdr + 4];
   return (ns * 16 * 8 <= a.K) ? ns : -1;
 }
 
@@ -342,7 +359,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_tw,
                 const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t *smem = align_smem_1024(smem_raw);
   const int S = args.stages;
   const int stage_bytes = W_TILE_BYTES + args.Mb * BLOCK_K * 2;
   SmemPtrs sp = carve_smem(smem, S, stage_bytes, args.red_bytes);
@@ -356,6 +373,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int mcount = min(args.Mb, args.M - m0);
   const int kb_lo = (int)((long long)rank * args.kblocks / C);
   const int kb_hi = (int)((long long)(rank + 1) * args.kblocks / C);
+  const int slice = slice_of(args, n_tile * BLOCK_N);
+  const float *T_u = args.T + (size_t)slice * args.M * T_STRIDE;  // this tile's T
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -365,6 +384,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     mbar_init(sp.tfull, 1);
     mbar_init(sp.drain, 1);
     *sp.abort_flag = 0;
+    *sp.zero_word = 0;
     fence_mbar_init();
     grid_launch_dependents();
   }
@@ -381,7 +401,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before_sync();
-  __syncthreads();
+  block_sync();
   tc_fence_after_sync();
   const uint32_t tmem_base = *sp.tmem_slot;
   volatile int *abort_flag = sp.abort_flag;
@@ -444,7 +464,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           uint8_t *st = sp.stage0 + (size_t)stage * stage_bytes;
           mbar_arrive_expect_tx(&sp.full[stage], (uint32_t)(BLOCK_N * 32 + args.sub_n * 32));
           tma_load_2d(st, &tmap_b, &sp.full[stage], j0, ad * args.N + n_tile * BLOCK_N, pol_w);
-          tma_load_2d(st + BLOCK_N * 32, &tmap_tw, &sp.full[stage], 0, sl * args.Mpad + m0, pol_x);
+          tma_load_2d(st + BLOCK_N * 32, &tmap_tw, &sp.full[stage], 0,
+                      slice * args.tw_slice_rows + sl * args.Mpad + m0, pol_x);
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -456,13 +477,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // Let this CTA's own copies land before shared memory goes away.
         const int n = issued < S ? issued : S;
         for (int i = issued - n; i < issued; ++i) {
-          volatile int never = 0;
-          mbar_wait_bounded(&sp.full[i % S], (uint32_t)((i / S) & 1), &never);
+          mbar_wait_bounded(&sp.full[i % S], (uint32_t)((i / S) & 1), sp.zero_word);
         }
         if (early > issued) {
           for (int i = issued; i < early; ++i) {
-            volatile int never = 0;
-            mbar_wait_bounded(&sp.full[i], 0u, &never);  // W half only: never completes, bounded
+            mbar_wait_bounded(&sp.full[i], 0u, sp.zero_word);  // W half only: never completes, bounded
           }
         }
       }
@@ -531,8 +550,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       } else if (issued_any) {
         // Wait for this thread's MMAs before tensor memory is freed.
         mma_commit(sp.drain);
-        volatile int never = 0;
-        mbar_wait_bounded(sp.drain, 0, &never);
+        mbar_wait_bounded(sp.drain, 0, sp.zero_word);
       }
       mma_ok = ok;
     }
@@ -592,14 +610,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // Walk the plan's buckets (see verify_walk): the staged tables sit at
         // the start of the freed stage ring, the B-row slots after them.
         const size_t ring = (size_t)S * stage_bytes;
-        const VerifyTables vt = stage_verify_tables(args, L, sp.stage0, ring - 8 * 128 * sizeof(uint4), m0, mcount, et);
+        const VerifyTables vt =
+            stage_verify_tables(args, L, T_u, sp.stage0, ring - 8 * 128 * sizeof(uint4), m0, mcount, et);
         uint4 *Bs = reinterpret_cast<uint4 *>(sp.stage0 + vt.bytes);
         const int slot_cap = (int)((ring - vt.bytes) / (128 * sizeof(uint4)));
         verify_walk<true>(args, L, vt, Bs, slot_cap, et, n, m0, mcount, 0, 1, taddr, nullptr, 0, 0);
       }
     }
     tc_fence_before_sync();
-    __syncthreads();
+    block_sync();
   } else {
     const int r0 = rank * BLOCK_N / C, r1 = (rank + 1) * BLOCK_N / C, R = r1 - r0;
     const size_t ring = (size_t)S * stage_bytes;
@@ -710,15 +729,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       // Stage ring after the reduction: fin, then the staged tables when
       // they fit, then the B-row slots.
       const size_t fin_bytes = align_up((size_t)args.Mb * R * 4, 16);
-      const VerifyTables vt = stage_verify_tables(args, L, sp.stage0 + fin_bytes,
+      const VerifyTables vt = stage_verify_tables(args, L, T_u, sp.stage0 + fin_bytes,
                                                   ring - fin_bytes - 8 * 128 * sizeof(uint4), m0, mcount, et);
       uint4 *Bs = reinterpret_cast<uint4 *>(sp.stage0 + fin_bytes + vt.bytes);
       const int slot_cap = (int)((ring - fin_bytes - vt.bytes) / (128 * sizeof(uint4)));
-      // Threads split as (row i, column phase): 128 / R threads share a row.
+      // Threads split as (row i, column phase): P = floor(128 / R) threads
+      // share a row; when R does not divide 128 the last 128 - P * R idle.
       const int P = 128 / R;
       const int i = et % R, sub = et / R;
-      verify_walk<false>(args, L, vt, Bs, slot_cap, et, n_tile * BLOCK_N + r0 + i, m0, mcount, sub, P, 0u, fin, R,
-                         i);
+      if (sub < P)
+        verify_walk<false>(args, L, vt, Bs, slot_cap, et, n_tile * BLOCK_N + r0 + i, m0, mcount, sub, P, 0u, fin, R,
+                           i);
     }
     tc_fence_before_sync();
     cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
@@ -810,13 +831,13 @@ GemmShape gemm_shape(int M, int N, int K, int num_sms) {
   s.tmem_cols = cols;
   s.nbuf = 1;
   s.total_iters = s.n_units * s.kblocks;
-  // Split-K factor (a power of two, so each CTA owns 128 / C output rows):
-  // minimise waves x (k-blocks per CTA + fixed cost), with a reduction cost
-  // for C > 1; C = 1 needs no cluster.
+  // Split-K factor C (CTA r of a cluster owns output rows [r*128/C,
+  // (r+1)*128/C) in the reduction): minimise waves x (k-blocks per CTA +
+  // fixed cost), with a reduction cost for C > 1; C = 1 needs no cluster.
   const bool attrs = ensure_attributes();
   int bestC = 1;
   double best = 1e30;
-  for (int C = 1; C <= MAX_CLUSTER && C <= s.kblocks; C <<= 1) {  // powers of two: C divides 128 rows
+  for (int C = 1; C <= MAX_CLUSTER && C <= s.kblocks; ++C) {
     const int red = C > 1 ? RED_BYTES : 0;
     const int st = stages_for(Mb, red);
     if (st < 2) continue;
@@ -892,7 +913,8 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
   tt = tw;
   if (use_tw) {
     if (!make_map(&tb, g.B_stack, (long long)g.n_ad * g.N, g.r_max, BLOCK_N, 16) ||
-        !make_map(&tt, g.tw, (long long)max_expand_slices(g.M, g.n_ad) * expand_rows(g.M), 16, sh.sub_n, 16)) {
+        !make_map(&tt, g.tw, (long long)g.n_slices * max_expand_slices(g.M, g.n_ad) * expand_rows(g.M), 16, sh.sub_n,
+                  16)) {
       *err_code = 1;
       return cudaErrorInvalidValue;
     }
@@ -916,6 +938,9 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
   a.after_shrink = g.after_shrink;
   a.use_tw = use_tw;
   a.Mpad = expand_rows(g.M);
+  a.n_slices = g.n_slices;
+  for (int i = 0; i < MLORA_MAX_SLICES; ++i) a.slice_end[i] = i < g.n_slices ? g.slice_end[i] : g.N;
+  a.tw_slice_rows = max_expand_slices(g.M, g.n_ad) * expand_rows(g.M);
   a.scale = g.scale;
   a.y = g.y;
   a.B_stack = g.B_stack;

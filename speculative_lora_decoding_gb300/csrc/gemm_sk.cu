@@ -1,0 +1,619 @@
+// Steps a3 + a4 as a persistent stream-K kernel: the base GEMM acc = x W^T on
+// the tcgen05 tensor cores with the low-rank expand added by tensor-core MMAs
+// (verify mode), for batches of up to 256 token rows:
+//
+//   draft  (LoRA off): y[m, n] = bf16(acc[m, n])
+//   verify (LoRA on):  y[m, n] = bf16(acc[m, n] + sum_s B_a[n, slice s] . Tmask_s[m, :])
+//
+// where Tmask_s holds scale * T on the rows of adapter a and 0 elsewhere
+// ("output = W·x + scale · B(A·x)", "Multi-LoRA Serving in Practice", section
+// "Core Principle: Shared Base Model, Per-Request Adapter Selection").
+//
+// Work split.  The (tile of 128 W rows, 64-wide k-block) pairs are laid out
+// tile by tile and cut into one contiguous, equal share per CTA, one CTA per
+// SM, so every SM streams the same number of W bytes whatever the tile count
+// (no partial last wave).  A CTA's share is a sequence of segments: the tail
+// of a tile begun by the CTA before it, whole tiles, and the head of a tile
+// that the CTAs after it finish.  The CTA that holds a tile's first k-block
+// owns the tile: it adds the expand MMAs, waits for the fp32 partial sums of
+// the other contributors (each publishes its single non-owned segment first,
+// so by the time the owner reaches the end of its share they are ready) and
+// writes y.  Waits only ever point to CTAs with a larger index, and all CTAs
+// are resident at once, so the waits always end; every wait is bounded
+// nevertheless.  Partials are added in CTA order: results are deterministic.
+//
+// Warp roles: warp 0 issues the TMA loads of W and x tiles (128-byte swizzle)
+// and of the expand operands into a ring of stages that runs across segment
+// boundaries; warp 1 owns tensor memory, issues tcgen05.mma from one thread
+// into two accumulators used alternately, and zeroes B columns past an
+// adapter's rank in shared memory before an expand MMA reads them; warps 2..5
+// drain one accumulator while the MMAs fill the other.
+#include "common.cuh"
+#include "launch.h"
+
+namespace mlora {
+
+constexpr int SK_THREADS = 192;
+constexpr int SK_BN = 128;                       // W rows per tile (MMA M)
+constexpr int SK_BK = 64;                        // K per stage: 128 bytes of bf16
+constexpr int SK_WTILE = SK_BN * SK_BK * 2;      // 16 KB
+constexpr int SK_CHUNK = 32;                     // accumulator columns per tensor-memory load
+constexpr size_t SK_SMEM_LIMIT = 220 * 1024;     // leaves room for a co-resident shrink CTA
+constexpr size_t SK_SMEM_FIXED = 1024 + 256;     // alignment slack + barriers
+constexpr int SK_MIN_SHARE = 8;                  // k-blocks per CTA at least
+constexpr int SK_MAX_PARTIALS = 8;               // contributors per tile besides its owner, at most
+constexpr int SK_MAX_ROWS = 256;                 // token rows: two accumulators fit in tensor memory
+
+struct SkArgs {
+  int M, N, K, Mb, kblocks, total, P, stages, cols;
+  int mode, prefetch_w, after_shrink, use_tw, Mpad;
+  int n_slices, slice_end[MLORA_MAX_SLICES], tw_slice_rows;
+  int n_ad;
+  uint16_t *y;
+  const int32_t *plan;
+  uint32_t *status;
+  float *partials;  // [P][Mb][128]: a contributor's partial sums, token-major
+  uint32_t *flags;  // [P]: 1 once CTA i's partial is written; the owner sets it back to 0
+};
+
+__device__ __forceinline__ int sk_begin(const SkArgs &a, int i) { return (int)((long long)i * a.total / a.P); }
+
+// The CTA whose share holds linear k-block g.
+__device__ __forceinline__ int sk_cta_of(const SkArgs &a, int g) {
+  int i = (int)((long long)g * a.P / a.total);
+  while (i + 1 < a.P && sk_begin(a, i + 1) <= g) ++i;
+  while (i > 0 && sk_begin(a, i) > g) --i;
+  return i;
+}
+
+__device__ __forceinline__ int sk_slice_of(const SkArgs &a, int n0) {
+  int s = 0;
+#pragma unroll
+  for (int i = 0; i + 1 < MLORA_MAX_SLICES; ++i)
+    if (i + 1 < a.n_slices && n0 >= a.slice_end[i]) s = i + 1;
+  return s;
+}
+
+// Zero logical columns [c0, 16) of a 128-row x 16-column bf16 tile written by
+// TMA with 32-byte swizzling (row i at byte 32 i; its two 16-byte halves are
+// swapped when bit 2 of i is set).  Each lane of the warp takes 4 rows.
+__device__ __forceinline__ void zero_tail_columns_sw32(uint8_t *tile, int c0, int lane) {
+#pragma unroll 1
+  for (int q = 0; q < 4; ++q) {
+    const int i = lane * 4 + q;
+    uint8_t *row = tile + i * 32;
+    const int flip = (i >> 2) & 1;
+    for (int c = c0; c < 16; ++c) {
+      const int chunk = (c >> 3) ^ flip;
+      *reinterpret_cast<uint16_t *>(row + chunk * 16 + (c & 7) * 2) = 0;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(SK_THREADS, 1)
+    gemm_sk_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                   const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_tw,
+                   const SkArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *ring = align_smem_1024(smem_raw);
+  const int S = args.stages;
+  const int stage_bytes = SK_WTILE + args.Mb * SK_BK * 2;
+  uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)S * stage_bytes);
+  uint64_t *empty = full + S;
+  uint64_t *acc_full = empty + S;     // [2]: MMA commit -> epilogue
+  uint64_t *acc_empty = acc_full + 2; // [2]: epilogue warps -> MMA issuer
+  uint64_t *drain = acc_empty + 2;
+  uint64_t *fix_bar = drain + 1;      // partial sums copied into the ring (owner fix-up)
+  uint64_t *epi_done = fix_bar + 1;   // every epilogue warp is done with tensor memory
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi_done + 1);
+  int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+  int *zero_word = abort_flag + 1;    // stays 0: for waits that only a time limit may end
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x;
+  const int KB = args.kblocks;
+  const int g0 = sk_begin(args, cta), g1 = sk_begin(args, cta + 1);
+  const bool tc = args.use_tw != 0 && args.mode == MLORA_VERIFY;
+  const PlanLayout L = plan_layout(args.M, args.n_ad);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
+    mbar_init(fix_bar, 1);
+    mbar_init(epi_done, 4);
+    *abort_flag = 0;
+    *zero_word = 0;
+    fence_mbar_init();
+    grid_launch_dependents();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_w);
+    tma_prefetch_desc(&tmap_x);
+    if (tc) {
+      tma_prefetch_desc(&tmap_b);
+      tma_prefetch_desc(&tmap_tw);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 2 * args.cols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  block_sync();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  volatile int *ab = abort_flag;
+  volatile int *never = zero_word;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const uint32_t tx = (uint32_t)stage_bytes;
+      const uint32_t tx_expand = (uint32_t)(SK_BN * 32 + args.Mb * 32);
+      // With static weights the first ring of W tiles is requested before the
+      // wait for the preceding kernel; x always comes after it.  (Not with the
+      // expand: its operands would take ring stages between those k-blocks.)
+      int early = 0;
+      if (args.prefetch_w && !args.after_shrink && !tc) {
+        for (int g = g0; g < g1 && early < S; ++g, ++early) {
+          const int t = g / KB, kb = g - t * KB;
+          mbar_arrive_expect_tx(&full[early], tx);
+          tma_load_2d(ring + (size_t)early * stage_bytes, &tmap_w, &full[early], kb * SK_BK, t * SK_BN, pol_w);
+        }
+      }
+      bool waited = !args.after_shrink;
+      if (waited) grid_dependency_wait();
+      int stage = 0, issued = 0, i = 0, ns = -1;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int g = g0; g < g1 && ok;) {
+        const int t = g / KB, kb0 = g - t * KB, kb1 = min(KB, g1 - t * KB);
+        for (int kb = kb0; kb < kb1; ++kb, ++i) {
+          uint8_t *st = ring + (size_t)stage * stage_bytes;
+          if (i >= early) {
+            if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, ab)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], tx);
+            tma_load_2d(st, &tmap_w, &full[stage], kb * SK_BK, t * SK_BN, pol_w);
+          }
+          tma_load_2d(st + SK_WTILE, &tmap_x, &full[stage], kb * SK_BK, 0, pol_x);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok && tc && kb0 == 0) {
+          if (!waited) {
+            grid_dependency_wait();  // the masked operand comes from the shrink kernel just before
+            waited = true;
+          }
+          if (ns < 0) ns = args.plan[L.hdr + 4];
+          const int row0 = sk_slice_of(args, t * SK_BN) * args.tw_slice_rows;
+          for (int sl = 0; sl < ns; ++sl) {
+            const int ad = args.plan[L.slices + 2 * sl], j0 = args.plan[L.slices + 2 * sl + 1];
+            if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, ab)) {
+              ok = false;
+              break;
+            }
+            uint8_t *st = ring + (size_t)stage * stage_bytes;
+            mbar_arrive_expect_tx(&full[stage], tx_expand);
+            tma_load_2d(st, &tmap_b, &full[stage], j0, ad * args.N + t * SK_BN, pol_w);
+            tma_load_2d(st + SK_BN * 32, &tmap_tw, &full[stage], 0, row0 + sl * args.Mpad, pol_x);
+            ++issued;
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        g = t * KB + kb1;
+      }
+      if (!ok) {
+        *reinterpret_cast<volatile int *>(abort_flag) = 1;
+        raise_status(args.status, MLORA_DEV_TIMEOUT);
+      }
+      if (*ab) {
+        // Let this CTA's own copies land before shared memory goes away.
+        const int n = issued < S ? issued : S;
+        for (int k = issued - n; k < issued; ++k) {
+          mbar_wait_bounded(&full[k % S], (uint32_t)((k / S) & 1), never);
+        }
+        for (int k = issued; k < early; ++k) {
+          mbar_wait_bounded(&full[k], 0u, never);  // W half only: never completes, bounded
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(SK_BN, args.Mb);
+    const uint32_t ring0 = smem_addr(ring);
+    const uint32_t sbytes = (uint32_t)stage_bytes;
+    int stage = 0, seg = 0, ns = -1;
+    uint32_t phase = 0;
+    bool ok = true, issued_any = false;
+    for (int g = g0; g < g1 && ok; ++seg) {
+      const int t = g / KB, kb0 = g - t * KB, kb1 = min(KB, g1 - t * KB);
+      const int buf = seg & 1;
+      const uint32_t acc = tmem_base + (uint32_t)(buf * args.cols);
+      if (lane == 0) {
+        // The accumulator's previous use (segment seg - 2) must be drained.
+        if (seg >= 2 && !mbar_wait_bounded(&acc_empty[buf], (uint32_t)(((seg >> 1) - 1) & 1), ab)) ok = false;
+        tc_fence_after_sync();
+        for (int kb = kb0; kb < kb1 && ok; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_addr = ring0 + (uint32_t)stage * sbytes;
+          const uint64_t ad = smem_desc_kmajor_sw128(a_addr);
+          const uint64_t bd = smem_desc_kmajor_sw128(a_addr + SK_WTILE);
+          const uint32_t first = kb > kb0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < SK_BK / 16; ++kk) mma_bf16_ss(acc, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : first);
+          mma_commit(&empty[stage]);
+          issued_any = true;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      stage = __shfl_sync(0xffffffffu, stage, 0);
+      phase = __shfl_sync(0xffffffffu, phase, 0);
+      if (ok && tc && kb0 == 0) {
+        if (ns < 0) {
+          grid_dependency_wait();  // the plan and the masked operand come from earlier kernels
+          ns = args.plan[L.hdr + 4];
+        }
+        for (int sl = 0; sl < ns && ok; ++sl) {
+          if (lane == 0 && !mbar_wait_bounded(&full[stage], phase, ab)) ok = false;
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          const int ad = args.plan[L.slices + 2 * sl], j0 = args.plan[L.slices + 2 * sl + 1];
+          const int c0 = args.plan[L.rank_eff + ad] - j0;  // rank columns of this 16-wide block
+          uint8_t *st = ring + (size_t)stage * stage_bytes;
+          if (c0 < 16) {
+            // B columns past the rank hold the caller's padding (maybe NaN;
+            // NaN * 0 would still be NaN): zero them before the MMA reads.
+            zero_tail_columns_sw32(st, c0, lane);
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) {
+            tc_fence_after_sync();
+            const uint32_t a_addr = smem_addr(st);
+            mma_bf16_ss(acc, smem_desc_kmajor_sw32(a_addr), smem_desc_kmajor_sw32(a_addr + SK_BN * 32), idesc, 1u);
+            mma_commit(&empty[stage]);
+          }
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (lane == 0 && ok) mma_commit(&acc_full[buf]);
+      __syncwarp();
+      g = t * KB + kb1;
+    }
+    if (lane == 0 && !ok) {
+      *reinterpret_cast<volatile int *>(abort_flag) = 1;
+      raise_status(args.status, MLORA_DEV_TIMEOUT);
+      if (issued_any) {
+        // Wait for this thread's MMAs before tensor memory is freed.
+        mma_commit(drain);
+        mbar_wait_bounded(drain, 0, never);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // Warp w reads tensor-memory lanes 32*(w%4)..+31: tile rows.
+    const int quad = warp & 3, et = threadIdx.x - 64;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    grid_dependency_wait();  // y and the flags may still be in use by the preceding kernel
+    int seg = 0;
+    for (int g = g0; g < g1; ++seg) {
+      const int t = g / KB, kb0 = g - t * KB, kb1 = min(KB, g1 - t * KB);
+      const int buf = seg & 1;
+      // All 128 threads agree on the outcome before any of them branches, so
+      // the named barriers below are always reached by every thread.
+      const bool ready = named_bar_and(1, 128, mbar_wait_bounded(&acc_full[buf], (uint32_t)((seg >> 1) & 1), ab));
+      if (!ready) {
+        if (et == 0) {
+          *reinterpret_cast<volatile int *>(abort_flag) = 1;
+          raise_status(args.status, MLORA_DEV_TIMEOUT);
+        }
+        __syncwarp();
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t acc = tmem_base + (uint32_t)(buf * args.cols) + lane_off;
+      const int nchunks = (args.M + SK_CHUNK - 1) / SK_CHUNK;
+      if (kb0 > 0) {
+        // Contributor: publish this segment's partial sums, then the flag.
+        float *part = args.partials + (size_t)cta * args.Mb * SK_BN;
+        for (int ch = 0; ch < nchunks; ++ch) {
+          uint32_t r[32];
+          tmem_ld_x32(acc + ch * SK_CHUNK, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < SK_CHUNK; ++j) {
+            const int col = ch * SK_CHUNK + j;
+            if (col < args.M) part[(size_t)col * SK_BN + row] = __uint_as_float(r[j]);
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        named_bar_sync(1, 128);
+        if (et == 0) {
+          __threadfence();
+          st_release_gpu(&args.flags[cta], 1u);
+        }
+        __syncwarp();
+      } else {
+        // Owner: wait for the contributors of this tile, add their partials
+        // in CTA order, round once and store y.  A tile with contributors is
+        // always this CTA's last segment, so the stage ring is idle (every
+        // load landed and every MMA that read it completed): the partials
+        // come into it with bulk copies, a round trip for many columns.
+        const int last = kb1 < KB ? sk_cta_of(args, (t + 1) * KB - 1) : cta;
+        const int nc = last - cta;
+        bool have = true;
+        if (nc > 0) {
+          if (et == 0) {
+            for (int j = cta + 1; j <= last; ++j) {
+              bool seen = ld_acquire_gpu(&args.flags[j]) == 1u;
+              if (!seen) {
+                const uint64_t t0 = global_timer_ns();
+                while (!(seen = ld_acquire_gpu(&args.flags[j]) == 1u)) {
+                  if (global_timer_ns() - t0 > WAIT_LIMIT_NS) break;
+                  sleep_ns(64);
+                }
+              }
+              if (seen) {
+                args.flags[j] = 0u;
+              } else {
+                have = false;
+                raise_status(args.status, MLORA_DEV_TIMEOUT);
+              }
+            }
+            fence_proxy_async_global();
+          }
+          __syncwarp();  // warps reach a barrier converged (bar.* counts whole warps)
+          have = named_bar_and(1, 128, have);
+        }
+        const int n = t * SK_BN + row;
+        // Columns per round: every contributor's slice of them fits the ring
+        // (the host bounds nc so that at least SK_CHUNK columns always do).
+        const size_t ring_bytes = (size_t)S * stage_bytes;
+        int per = nc > 0 ? (int)(ring_bytes / ((size_t)nc * SK_BN * 4)) / SK_CHUNK * SK_CHUNK : args.M;
+        if (nc > 0 && per < SK_CHUNK) {
+          per = SK_CHUNK;
+          if (have && et == 0) raise_status(args.status, MLORA_DEV_TIMEOUT);
+          have = false;  // cannot happen within the host's bound; never copy past the ring
+        }
+        const float *sp = reinterpret_cast<const float *>(ring);
+        uint32_t fix_phase = 0;
+        for (int q0 = 0; q0 < args.M; q0 += per) {
+          const int q1 = min(args.M, q0 + per);
+          const int qn = q1 - q0;
+          const bool fetch = nc > 0 && have;
+          if (fetch) {
+            if (et == 0) {
+              const uint32_t bytes = (uint32_t)qn * SK_BN * 4;
+              mbar_arrive_expect_tx(fix_bar, bytes * (uint32_t)nc);
+              for (int c = 0; c < nc; ++c)
+                bulk_load(ring + (size_t)c * qn * SK_BN * 4,
+                          args.partials + ((size_t)(cta + 1 + c) * args.Mb + q0) * SK_BN, bytes, fix_bar);
+            }
+            __syncwarp();
+            // Not cut short by the abort flag: the copies must land before
+            // shared memory is reused or released.
+            const bool landed = named_bar_and(1, 128, mbar_wait_bounded(fix_bar, fix_phase, never));
+            fix_phase ^= 1u;
+            if (!landed) {
+              if (et == 0) raise_status(args.status, MLORA_DEV_TIMEOUT);
+              have = false;
+            }
+          }
+          for (int cb = q0; cb < q1; cb += SK_CHUNK) {
+            uint32_t r[32];
+            tmem_ld_x32(acc + cb, r);
+            tmem_ld_wait();
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < SK_CHUNK; ++j) v[j] = __uint_as_float(r[j]);
+            const bool whole = cb + SK_CHUNK <= q1;  // no column past q1 in this chunk
+            if (fetch && have) {
+              for (int c = 0; c < nc; ++c) {
+                const float *pc = sp + ((size_t)c * qn + (cb - q0)) * SK_BN + row;
+                if (whole) {
+#pragma unroll
+                  for (int j = 0; j < SK_CHUNK; ++j) v[j] += pc[j * SK_BN];
+                } else {
+#pragma unroll
+                  for (int j = 0; j < SK_CHUNK; ++j)
+                    if (cb + j < q1) v[j] += pc[j * SK_BN];
+                }
+              }
+            }
+            if (n < args.N) {
+              uint16_t *yp = args.y + (size_t)cb * args.N + n;
+              if (whole) {
+#pragma unroll
+                for (int j = 0; j < SK_CHUNK; ++j) yp[(size_t)j * args.N] = float_to_bf16_bits(v[j]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < SK_CHUNK; ++j)
+                  if (cb + j < q1) yp[(size_t)j * args.N] = float_to_bf16_bits(v[j]);
+              }
+            }
+          }
+          if (fetch) named_bar_sync(1, 128);  // the ring is refilled only after every thread read it
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      }
+      g = t * KB + kb1;
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(epi_done);
+  }
+
+  // Tensor memory is released only once every epilogue warp has finished
+  // reading it (an mbarrier, so that the release does not rest on a CTA
+  // barrier reached by warps whose lanes took different paths).
+  if (warp == 1) {
+    if (lane == 0) {
+      if (!mbar_wait_bounded(epi_done, 0u, never)) raise_status(args.status, MLORA_DEV_TIMEOUT);
+    }
+    __syncwarp();
+  }
+  tc_fence_before_sync();
+  block_sync();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, 2 * args.cols);
+  }
+}
+
+SkShape sk_shape(int M, int N, int K, int num_sms) {
+  SkShape s = {};
+  s.ok = false;
+  if (M < 1 || M > SK_MAX_ROWS || num_sms <= 0) return s;
+  s.Mb = (M + 15) / 16 * 16;
+  int cols = 32;
+  while (cols < s.Mb) cols <<= 1;
+  s.cols = cols;
+  const int stage_bytes = SK_WTILE + s.Mb * SK_BK * 2;
+  int st = (int)((SK_SMEM_LIMIT - SK_SMEM_FIXED) / stage_bytes);
+  s.stages = st > 8 ? 8 : st;
+  if (s.stages < 2) return s;
+  s.n_tiles = (N + SK_BN - 1) / SK_BN;
+  s.kblocks = (K + SK_BK - 1) / SK_BK;
+  s.total = s.n_tiles * s.kblocks;
+  // Shares of at least ceil(kblocks / SK_MAX_PARTIALS) k-blocks: a tile then
+  // meets at most SK_MAX_PARTIALS + 1 CTAs.
+  int share = (s.kblocks + SK_MAX_PARTIALS - 1) / SK_MAX_PARTIALS;
+  if (share < SK_MIN_SHARE) share = SK_MIN_SHARE;
+  int P = s.total / share;
+  if (P > num_sms) P = num_sms;
+  if (P < 1) P = 1;
+  s.P = P;
+  s.smem_bytes = SK_SMEM_FIXED + (size_t)s.stages * stage_bytes;
+  s.ok = true;
+  return s;
+}
+
+size_t sk_partial_bytes(int M, int num_sms) {
+  if (M < 1 || M > SK_MAX_ROWS) return 0;
+  return (size_t)num_sms * ((M + 15) / 16 * 16) * SK_BN * sizeof(float);
+}
+
+typedef CUresult (*SkEncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                               const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static SkEncodeFn sk_encode_fn() {
+  static SkEncodeFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<SkEncodeFn>(p);
+  }
+  return fn;
+}
+
+// Row-major bf16 [rows, cols] read in boxes of box_rows x box_cols (64 columns
+// with 128-byte swizzling, or 16 with 32-byte swizzling); out of range reads 0.
+static bool sk_map(CUtensorMap *map, const void *base, long long rows, int cols, int box_rows, int box_cols) {
+  SkEncodeFn fn = sk_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = box_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partials, uint32_t *flags, cudaStream_t s,
+                           int *err_code) {
+  *err_code = 0;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidValue;
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(gemm_sk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SK_SMEM_LIMIT) !=
+        cudaSuccess)
+      return cudaErrorInvalidValue;
+    attr_done[dev] = 1;
+  }
+  CUtensorMap tw, tx, tb, tt;
+  if (!sk_map(&tw, g.W, g.N, g.K, SK_BN, SK_BK) || !sk_map(&tx, g.x, g.M, g.K, sh.Mb, SK_BK)) {
+    *err_code = 1;
+    return cudaErrorInvalidValue;
+  }
+  const int use_tw = (g.mode == MLORA_VERIFY && g.tw != nullptr) ? 1 : 0;
+  tb = tw;
+  tt = tw;
+  if (use_tw) {
+    if (!sk_map(&tb, g.B_stack, (long long)g.n_ad * g.N, g.r_max, SK_BN, 16) ||
+        !sk_map(&tt, g.tw, (long long)g.n_slices * max_expand_slices(g.M, g.n_ad) * expand_rows(g.M), 16, sh.Mb,
+                16)) {
+      *err_code = 1;
+      return cudaErrorInvalidValue;
+    }
+  }
+  SkArgs a;
+  a.M = g.M;
+  a.N = g.N;
+  a.K = g.K;
+  a.Mb = sh.Mb;
+  a.kblocks = sh.kblocks;
+  a.total = sh.total;
+  a.P = sh.P;
+  a.stages = sh.stages;
+  a.cols = sh.cols;
+  a.mode = g.mode;
+  a.prefetch_w = g.prefetch_w;
+  a.after_shrink = g.after_shrink;
+  a.use_tw = use_tw;
+  a.Mpad = expand_rows(g.M);
+  a.n_slices = g.n_slices;
+  for (int i = 0; i < MLORA_MAX_SLICES; ++i) a.slice_end[i] = i < g.n_slices ? g.slice_end[i] : g.N;
+  a.tw_slice_rows = max_expand_slices(g.M, g.n_ad) * expand_rows(g.M);
+  a.n_ad = g.n_ad;
+  a.y = g.y;
+  a.plan = g.plan;
+  a.status = g.status;
+  a.partials = partials;
+  a.flags = flags;
+  cudaError_t e = launch_pdl(gemm_sk_kernel, dim3(sh.P), dim3(SK_THREADS), sh.smem_bytes, s, tw, tx, tb, tt, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace mlora

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/mlora.h"
+
 namespace mlora {
 
 void note_launch();
@@ -33,17 +35,18 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // Step a1: stable counting sort of rows by adapter into `plan` (int32 words).
-// `tw` (may be null): the masked low-rank operand buffer of the tensor-core
-// expand, [max_expand_slices(M, n_ad)][expand_rows(M)][16] bf16; zeroed here.
 cudaError_t launch_plan(const int32_t *adapter_idx, int M, const int32_t *rank_of, int n_ad, int r_max,
-                        int32_t *plan, uint32_t *status, uint16_t *tw, cudaStream_t s);
+                        int32_t *plan, uint32_t *status, cudaStream_t s);
 
-// Step a2: T[m, j] for j < rank (fp32, row stride t_stride).  `zero_first`
-// clears T first so that padding and rows without an adapter read 0.
-// With `tw` non-null it also writes bf16(scale * T) into the masked operand.
+// Step a2: T[m, j] for j < rank (fp32, row stride t_stride), for n_slices
+// output slices (A: [n_slices][n_ad][r_max][K]; T: [n_slices][M][t_stride]).
+// `zero_first` clears T first so that padding and rows without an adapter
+// read 0.  With `tw` non-null it also writes the whole masked operand of the
+// tensor-core expand, [n_slices][max_expand_slices(M, n_ad)][expand_rows(M)][16]
+// bf16: scale * T on member rows, 0 elsewhere.
 cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, int n_ad, int r_max,
                           const int32_t *plan, float *T, int t_stride, bool zero_first, int num_sms, uint16_t *tw,
-                          float scale, cudaStream_t s);
+                          float scale, int n_slices, cudaStream_t s);
 
 // Steps a3 + a4: base GEMM on tcgen05 with the expand epilogue.
 struct GemmShape {
@@ -58,6 +61,8 @@ struct GemmLaunch {
   const uint16_t *x;
   const uint16_t *W;
   int M, N, K;
+  int n_slices;                      // output slices, each with its own T and masked operand
+  int slice_end[MLORA_MAX_SLICES];   // end row of each slice in W / y; all but the last multiples of 128
   int mode;
   int prefetch_w;    // W may be requested before the preceding kernel finishes
   int after_shrink;  // the preceding kernel on the stream is launch_shrink's
@@ -65,12 +70,26 @@ struct GemmLaunch {
   uint16_t *y;
   const uint16_t *B_stack;
   int r_max, n_ad;
-  const float *T;
+  const float *T;      // [n_slices][M][T_STRIDE]
   const int32_t *plan;
   uint32_t *status;
-  const uint16_t *tw;  // masked low-rank operand, or null (bucket-walk epilogue only)
+  const uint16_t *tw;  // masked low-rank operand [n_slices][...], or null (bucket-walk epilogue only)
 };
 cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s, int *err_code);
+
+// Steps a3 + a4 as a persistent stream-K kernel (gemm_sk.cu): one CTA per SM,
+// equal shares of the (tile, k-block) pairs, at most 256 token rows, draft mode
+// or verify mode with the tensor-core expand.  Needs sk_partial_bytes(M, SMs)
+// of scratch for partial sums and one flag word per CTA (zero between calls).
+struct SkShape {
+  bool ok;
+  int Mb, cols, stages, n_tiles, kblocks, total, P;
+  size_t smem_bytes;
+};
+SkShape sk_shape(int M, int N, int K, int num_sms);
+size_t sk_partial_bytes(int M, int num_sms);
+cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partials, uint32_t *flags, cudaStream_t s,
+                           int *err_code);
 
 // Steps a5 + a6.
 struct AcceptShape {

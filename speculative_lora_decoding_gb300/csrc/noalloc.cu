@@ -98,9 +98,9 @@ extern "C" MLORA_API mlora_status mlora_linear_noalloc(const mlora_bf16 *x, int 
   int32_t *plan = reinterpret_cast<int32_t *>(scratch + plan_off);
   float *T = reinterpret_cast<float *>(scratch + t_off);
   if (verify) {
-    if (launch_plan(adapter_idx, M, rank_of, n_ad, r_max, plan, status, nullptr, s) != cudaSuccess)
+    if (launch_plan(adapter_idx, M, rank_of, n_ad, r_max, plan, status, s) != cudaSuccess)
       return MLORA_ERR_CUDA;
-    if (launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, nullptr, 1.f, s) != cudaSuccess)
+    if (launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, nullptr, 1.f, 1, s) != cudaSuccess)
       return MLORA_ERR_CUDA;
   }
   GemmLaunch g;
@@ -109,6 +109,8 @@ extern "C" MLORA_API mlora_status mlora_linear_noalloc(const mlora_bf16 *x, int 
   g.M = M;
   g.N = N;
   g.K = K;
+  g.n_slices = 1;
+  for (int i = 0; i < MLORA_MAX_SLICES; ++i) g.slice_end[i] = N;
   g.mode = base_mode;
   g.prefetch_w = prefetch_w;
   g.after_shrink = verify ? 1 : 0;

@@ -35,17 +35,17 @@ __device__ int block_excl_scan(int v, int *sh, int *total) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int inc = warp_incl_scan(v);
   if (lane == 31) sh[w] = inc;
-  __syncthreads();
+  block_sync();
   if (w == 0) {
     const int s = (lane < (int)(blockDim.x >> 5)) ? sh[lane] : 0;
     const int si = warp_incl_scan(s);
     sh[lane] = si - s;
     if (lane == 31) sh[32] = si;
   }
-  __syncthreads();
+  block_sync();
   const int res = sh[w] + inc - v;
   *total = sh[32];
-  __syncthreads();
+  block_sync();
   return res;
 }
 
@@ -53,7 +53,7 @@ __device__ __forceinline__ int bucket_of(int a, int n_ad) { return (a >= 0 && a 
 
 __global__ void __launch_bounds__(PLAN_THREADS, 1)
     plan_kernel(const int32_t *__restrict__ adapter_idx, int M, const int32_t *__restrict__ rank_of, int n_ad,
-                int r_max, int32_t *__restrict__ plan, uint32_t *status, uint4 *__restrict__ tw) {
+                int r_max, int32_t *__restrict__ plan, uint32_t *status) {
   grid_launch_dependents();
   grid_dependency_wait();
   extern __shared__ int sh_dyn[];
@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
   __shared__ int scan_sh[33];
   __shared__ uint32_t flags;
   __shared__ int max_rank;
+  __shared__ int partial_block;  // an active rank reads padding columns in a 16-wide block
 
   const PlanLayout L = plan_layout(M, n_ad);
   const int tid = threadIdx.x;
@@ -69,12 +70,13 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
   if (tid == 0) {
     flags = 0;
     max_rank = 0;
+    partial_block = 0;
   }
   for (int b = tid; b < nb; b += PLAN_THREADS) {
     cnt[b] = 0;
     running[b] = 0;
   }
-  __syncthreads();
+  block_sync();
 
   // Validated ranks.
   for (int a = tid; a < n_ad; a += PLAN_THREADS) {
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
     plan[L.row_adapter + m] = (b < n_ad) ? b : -1;
     atomicAdd(&cnt[b], 1);
   }
-  __syncthreads();
+  block_sync();
 
   // Bucket offsets: exclusive scan of counts, each thread owning a contiguous run.
   const int per = (nb + PLAN_THREADS - 1) / PLAN_THREADS;
@@ -112,7 +114,7 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
     }
     if (tid == 0) plan[L.seg_offsets + nb] = total;
   }
-  __syncthreads();
+  block_sync();
 
   // Active adapters (rows > 0) and the shrink work list over them.
   {
@@ -124,6 +126,9 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
         ++nact;
         const int r = plan[L.rank_eff + a];
         rmax = max(rmax, r);
+        // A 16-wide block of B columns past the rank but inside r_max holds
+        // caller padding (possibly NaN); past r_max it reads as zero.
+        if ((r % 16) != 0 && r != r_max) partial_block = 1;
         nitems += ((r + SHRINK_J - 1) / SHRINK_J) * ((c + SHRINK_TOK - 1) / SHRINK_TOK);
       }
     }
@@ -157,22 +162,15 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
       plan[L.hdr + 1] = tot_items;
       plan[L.hdr + 2] = M;
       plan[L.hdr + 4] = tot_sl;
-      plan[L.hdr + 5] = tw ? 1 : 0;
-    }
-    // The masked low-rank operand: slice s holds, for every token row,
-    // scale * T[row, slice ranks] if the row belongs to the slice's adapter
-    // and 0 otherwise.  Zero it here once per plan; the shrink of each
-    // projection rewrites only the member rows, which the plan fixes.
-    if (tw) {
-      const size_t n16 = (size_t)tot_sl * expand_rows(M) * 2;  // 16-byte pieces (16 bf16 per row)
-      for (size_t e = tid; e < n16; e += PLAN_THREADS) tw[e] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  __syncthreads();
+  block_sync();
+  if (tid == 0) plan[L.hdr + 5] = partial_block ? 0 : 1;
+  block_sync();
   if (tid == 0) plan[L.hdr + 3] = max_rank;
-  __syncthreads();
+  block_sync();
   for (int b = tid; b < nb; b += PLAN_THREADS) running[b] = 0;
-  __syncthreads();
+  block_sync();
 
   // Stable ranks: rows in chunks of PLAN_THREADS; within a warp lanes with
   // the same bucket are ranked by lane order, warps take their turn in order.
@@ -189,12 +187,12 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
         basev = running[b];
         running[b] = basev + __popc(mask);
       }
-      __syncthreads();
+      block_sync();
     }
     basev = __shfl_sync(0xffffffffu, basev, leader);
     if (m < M) plan[L.perm + cnt[b] + basev + rank_in_warp] = m;
   }
-  __syncthreads();
+  block_sync();
 
   // Shrink work items, one record each: the item's adapter comes from a
   // binary search of the item offsets (copied to shared memory).
@@ -202,7 +200,7 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
   const int total_items = plan[L.hdr + 1];
   int *ioff = running;  // reuse: [n_active + 1] item offsets
   for (int i = tid; i <= n_active; i += PLAN_THREADS) ioff[i] = plan[L.item_off + i];
-  __syncthreads();
+  block_sync();
   for (int it = tid; it < total_items; it += PLAN_THREADS) {
     int lo = 0, hi = n_active;
     while (hi - lo > 1) {
@@ -226,15 +224,15 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
     rec[0] = w0;
     rec[1] = make_int4(rows[0], rows[1], rows[2], rows[3]);
   }
-  __syncthreads();
+  block_sync();
   if (tid == 0 && flags) raise_status(status, flags);
 }
 
 cudaError_t launch_plan(const int32_t *adapter_idx, int M, const int32_t *rank_of, int n_ad, int r_max,
-                        int32_t *plan, uint32_t *status, uint16_t *tw, cudaStream_t s) {
+                        int32_t *plan, uint32_t *status, cudaStream_t s) {
   const size_t smem = 2 * (size_t)(n_ad + 1) * sizeof(int);  // <= 32.8 KB for n_ad <= 4096
   cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(PLAN_THREADS), smem, s, adapter_idx, M, rank_of, n_ad, r_max,
-                             plan, status, reinterpret_cast<uint4 *>(tw));
+                             plan, status);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -13,6 +13,17 @@
 // from global memory straight to registers; nothing would be reused from a
 // shared-memory copy.  Warp sums are combined in a fixed order, so T is
 // deterministic.  Rank rows past rank_of[a] are never loaded.
+//
+// Output slices (blockIdx.y): a call may cover several projections that read
+// the same rows x (q, k and v; gate and up), each with its own A stack; slice
+// s reads A + s * n_ad * r_max * K and writes T + s * M * t_stride.
+//
+// The masked operand of the tensor-core expand, when requested: for each
+// expand slice e = (adapter a, 16-rank block j0) and token row m, 16 bf16
+// values scale * T[m, j0:j0+16] if m belongs to a and 0 otherwise.  The work
+// items write the member entries of the rank columns below ceil8(rank); a
+// grid-stride pass writes zeros to exactly the other 16-byte halves, so the
+// two never touch the same bytes and no earlier zeroing is needed.
 #include "common.cuh"
 #include "launch.h"
 
@@ -56,9 +67,9 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[32]) {
 }
 
 __global__ void __launch_bounds__(SHRINK_THREADS)
-    shrink_kernel(const uint16_t *__restrict__ x, int M, int K, const uint16_t *__restrict__ A, int n_ad, int r_max,
-                  const int32_t *__restrict__ plan, float *__restrict__ T, int t_stride, uint16_t *__restrict__ tw,
-                  float scale) {
+    shrink_kernel(const uint16_t *__restrict__ x, int M, int K, const uint16_t *__restrict__ A_all, int n_ad, int r_max,
+                  const int32_t *__restrict__ plan, float *__restrict__ T_all, int t_stride,
+                  uint16_t *__restrict__ tw_all, float scale) {
   __shared__ float red[SHRINK_WARPS][SHRINK_J * SHRINK_TOK];
   // Wait for the preceding kernel first, then let the GEMM that follows
   // launch: by then everything the GEMM's mainloop reads (x, W) is complete,
@@ -70,6 +81,25 @@ __global__ void __launch_bounds__(SHRINK_THREADS)
   const int total_items = plan[L.hdr + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kchunks = K >> 3;  // 16-byte pieces per row
+  const int sl = blockIdx.y;
+  const uint16_t *A = A_all + (size_t)sl * n_ad * r_max * K;
+  float *T = T_all + (size_t)sl * M * t_stride;
+  const int Mpad = expand_rows(M);
+  uint16_t *tw = tw_all ? tw_all + (size_t)sl * max_expand_slices(M, n_ad) * Mpad * 16 : nullptr;
+
+  if (tw) {
+    // Zero halves: (expand slice e, row m, half h) not written by an item.
+    const int n_exp = plan[L.hdr + 4];
+    const int halves = n_exp * Mpad * 2;
+    for (int hh = blockIdx.x * SHRINK_THREADS + threadIdx.x; hh < halves; hh += gridDim.x * SHRINK_THREADS) {
+      const int e = hh / (2 * Mpad), rem = hh - e * 2 * Mpad;
+      const int m = rem >> 1, h = rem & 1;
+      const int a = plan[L.slices + 2 * e], j0 = plan[L.slices + 2 * e + 1];
+      const bool member = m < M && plan[L.row_adapter + m] == a;
+      if (!(member && j0 + 8 * h < plan[L.rank_eff + a]))
+        *reinterpret_cast<uint4 *>(tw + ((size_t)e * Mpad + m) * 16 + 8 * h) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
 
   for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
     const int4 *rec = reinterpret_cast<const int4 *>(plan + L.items + (size_t)item * ITEM_WORDS);
@@ -125,7 +155,7 @@ __global__ void __launch_bounds__(SHRINK_THREADS)
     }
     // Warp totals (lane l holds value l), then a fixed-order sum over warps.
     red[warp][lane] = warp_transpose_sum(acc);
-    __syncthreads();
+    block_sync();
     if (threadIdx.x < SHRINK_J * SHRINK_TOK) {
       const int j = threadIdx.x / SHRINK_TOK, t = threadIdx.x % SHRINK_TOK;
       float s = 0.f;
@@ -137,19 +167,19 @@ __global__ void __launch_bounds__(SHRINK_THREADS)
         if (tw) {
           // Member row of the masked operand: slice (j0 + j) / 16 of adapter a.
           const int slice = plan[L.slice_off + a] + (j0 + j) / 16;
-          tw[((size_t)slice * expand_rows(M) + rows[t]) * 16 + (j0 + j) % 16] = float_to_bf16_bits(scale * v);
+          tw[((size_t)slice * Mpad + rows[t]) * 16 + (j0 + j) % 16] = float_to_bf16_bits(scale * v);
         }
       }
     }
-    __syncthreads();
+    block_sync();
   }
 }
 
 cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, int n_ad, int r_max,
                           const int32_t *plan, float *T, int t_stride, bool zero_first, int num_sms, uint16_t *tw,
-                          float scale, cudaStream_t s) {
+                          float scale, int n_slices, cudaStream_t s) {
   if (zero_first) {
-    cudaError_t e = cudaMemsetAsync(T, 0, (size_t)M * t_stride * sizeof(float), s);
+    cudaError_t e = cudaMemsetAsync(T, 0, (size_t)n_slices * M * t_stride * sizeof(float), s);
     if (e != cudaSuccess) return e;
   }
   // Upper bound on work items: ceil(r_max/J) * (ceil(M/TOK) + min(M, n_ad)).
@@ -157,8 +187,8 @@ cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, in
       (long long)((r_max + SHRINK_J - 1) / SHRINK_J) * ((M + SHRINK_TOK - 1) / SHRINK_TOK + min(M, n_ad));
   (void)n_ad;
   const int grid = (int)max(1LL, min(bound, (long long)num_sms * 8));
-  cudaError_t e = launch_pdl(shrink_kernel, dim3(grid), dim3(SHRINK_THREADS), 0, s, x, M, K, A, n_ad, r_max, plan, T,
-                             t_stride, tw, scale);
+  cudaError_t e = launch_pdl(shrink_kernel, dim3(grid, n_slices), dim3(SHRINK_THREADS), 0, s, x, M, K, A, n_ad, r_max,
+                             plan, T, t_stride, tw, scale);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

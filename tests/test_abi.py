@@ -19,7 +19,7 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = set(ml.header_symbols())
-    for n in ("mlora_linear", "mlora_verify_accept", "mlora_plan_segments", "mlora_shrink",
+    for n in ("mlora_linear", "mlora_linear_sliced", "mlora_verify_accept", "mlora_plan_segments", "mlora_shrink",
               "mlora_linear_workspace_bytes", "mlora_accept_workspace_bytes", "mlora_workspace_init",
               "mlora_read_device_status", "mlora_status_string"):
         assert n in names
@@ -55,3 +55,23 @@ def test_workspace_sizes(lib):
     assert lib.mlora_linear_workspace_bytes(0, 4096, 4096, 16) == 0
     assert lib.mlora_accept_workspace_bytes(256, 4, 128256) > 0
     assert lib.mlora_accept_workspace_bytes(256, 0, 128256) == 0
+
+
+def test_sliced_host_checks(lib):
+    """Slice ends are checked on the host, before any CUDA call."""
+    p = ctypes.c_void_p(256)
+    SHAPE = 2
+
+    def call(ends, N=640, mode=0):
+        arr = (ctypes.c_int32 * max(len(ends), 1))(*ends)
+        return lib.mlora_linear_sliced(p, 4, 8, p, N, len(ends), arr, None, None, 0, 0, None, None, None, 1.0, mode,
+                                       p, p, 1 << 24, None)
+
+    assert call([100, 640]) == SHAPE                 # an inner end that is not a multiple of 128
+    assert call([256, 256, 640]) == SHAPE            # not increasing
+    assert call([256, 512]) == SHAPE                 # last end != N
+    assert call([128, 256, 384, 512, 640]) == SHAPE  # more than MLORA_MAX_SLICES
+    assert call([]) == SHAPE
+    assert lib.mlora_linear_sliced_workspace_bytes(128, 6144, 4096, 16, 3) > \
+        lib.mlora_linear_sliced_workspace_bytes(128, 6144, 4096, 16, 1) == lib.mlora_linear_workspace_bytes(128, 6144, 4096, 16)
+    assert lib.mlora_linear_sliced_workspace_bytes(128, 6144, 4096, 16, 5) == 0

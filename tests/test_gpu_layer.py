@@ -98,6 +98,40 @@ def test_ragged_shapes_against_oracle(M, N, K, n_ad, ranks):
         assert _rel_err(host_bf16_to_f64(y), y_ref) <= TOL, (M, N, K, mode)
 
 
+@pytest.mark.parametrize("M,N,K,n_ad,ranks", [
+    (16, 256, 2048, 4, (8, 16, 24, 0)),    # ranks inside a 16-wide block: CUDA-core expand
+    (64, 384, 4096, 4, (16, 32, 48, 64)),  # multiples of 16: tensor-core expand, padding never read
+    (128, 1024, 4096, 16, (16,) * 15 + (40,)),
+])
+def test_nan_rank_padding_in_expand_shapes(M, N, K, n_ad, ranks):
+    """Shapes where the tensor-core expand is allowed, with NaN in every
+    padding entry of A and B past each adapter's rank."""
+    ml = needs_gpu()
+    x, W, A, B, rk, idx = _random_case(M + N + K, M, N, K, n_ad, ranks, r_max=64, nan_pad=True)
+    y_ref, _ = _oracle(x, W, A, B, rk, idx, 2.0, OL.VERIFY)
+    ws = ml.Workspace(ml.linear_workspace_bytes(M, N, K, n_ad))
+    y = host_bf16_to_f64(_run(ml, x, W, A, B, rk, idx, 2.0, OL.VERIFY, ws=ws))
+    assert ws.status() == 0 and np.isfinite(y).all()
+    assert _rel_err(y, y_ref) <= TOL
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 1024, 8192), (128, 4096, 4096), (200, 640, 2048), (1, 8, 512)])
+def test_split_tiles_oracle_and_determinism(M, N, K):
+    """Shapes whose tiles are shared by many CTAs (up to 16 partial sums per
+    tile): oracle parity, identical bits on repeated calls, and consecutive
+    calls on one workspace (each call consumes the partial-sum flags it sets)."""
+    ml = needs_gpu()
+    x, W, A, B, rk, idx = _random_case(M + N + K, M, N, K, 4, (16, 16, 8, 12), r_max=16, nan_pad=True)
+    ws = ml.Workspace(ml.linear_workspace_bytes(M, N, K, 4))
+    for mode in (OL.DRAFT, OL.VERIFY):
+        y_ref, _ = _oracle(x, W, A, B, rk, idx, 2.0, mode)
+        ys = [_run(ml, x, W, A, B, rk, idx, 2.0, mode, ws=ws) for _ in range(3)]
+        assert ws.status() == 0
+        assert _rel_err(host_bf16_to_f64(ys[0]), y_ref) <= TOL, (M, N, K, mode)
+        for y in ys[1:]:
+            assert torch.equal(y.view(torch.int16), ys[0].view(torch.int16))
+
+
 def test_plan_is_bit_exact():
     ml = needs_gpu()
     g = np.random.default_rng(2)

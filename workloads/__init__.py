@@ -203,12 +203,37 @@ def projection_weights(cfg: LayerConfig, p: int, seed: int = 0, r_max: int | Non
     return W, A, B, ranks
 
 
+# Projections of one transformer block that read the same input rows: q, k
+# and v read the normalised hidden state, gate and up the normalised output of
+# attention; o and down each read their own.
+_SHARED_INPUT = (("q", "k", "v"), ("gate", "up"))
+
+
+def input_groups(cfg: LayerConfig) -> list:
+    """Projection indices grouped by the input rows they read, in order:
+    [(0, 1, 2), (3,), (4, 5), (6,)] for the 8B and 32B shapes."""
+    names = [n for n, _, _ in cfg.projections]
+    groups, seen = [], set()
+    for i, n in enumerate(names):
+        if i in seen:
+            continue
+        g = (i,)
+        for shared in _SHARED_INPUT:
+            if n == shared[0] and all(x in names for x in shared):
+                g = tuple(names.index(x) for x in shared)
+        seen.update(g)
+        groups.append(g)
+    return groups
+
+
 def activations(cfg: LayerConfig, p: int, mode: str, k: int | None = None, seed: int = 0) -> np.ndarray:
-    """bf16 bits of x [M, K], entries N(0, 1)."""
+    """bf16 bits of x [M, K], entries N(0, 1).  Projections of one input group
+    (see input_groups) get the same rows."""
     _, K, _ = cfg.projections[p]
     M = cfg.rows(mode, k)
     kk = cfg.draft_lengths[0] if k is None else k
-    return _normal_bf16(rng(seed, "x", p, _MODE[mode], kk), (M, K), 1.0)
+    first = next(g[0] for g in input_groups(cfg) if p in g)
+    return _normal_bf16(rng(seed, "x", first, _MODE[mode], kk), (M, K), 1.0)
 
 
 # ----------------------------------------------------------------------------
