@@ -225,18 +225,23 @@ static mlora_status linear_impl(const mlora_bf16 *x, int M, int K, const mlora_b
   g.status = status;
   g.tw = verify ? tw : nullptr;
   int err = 0;
-  // The persistent stream-K GEMM takes batches of up to 256 rows in draft
-  // mode, and in verify mode when the tensor-core expand is certain to apply
-  // (every (adapter, 16-rank block) pair the plan can list fits the budget
-  // expand blocks x 128 <= K); otherwise the cluster split-K GEMM runs.
+  // Two GEMM kernels.  The cluster split-K kernel wins when its tiles fill at
+  // least 80% of the SMs in a single wave: the weights then stream at the
+  // full HBM rate and its on-chip reduction is the shortest tail.  Otherwise
+  // (a partial last wave, or idle SMs) the persistent stream-K kernel runs,
+  // if it can: batches of up to 256 rows in draft mode, and in verify mode
+  // when the tensor-core expand is certain to apply (every (adapter, 16-rank
+  // block) pair the plan can list fits the budget expand blocks x 128 <= K).
+  const GemmShape gs = gemm_shape(M, N, K, sms);
+  const bool cluster_full = gs.waves == 1 && (long long)gs.n_units * gs.C * 5 >= (long long)sms * 4;
   const SkShape sk = sk_shape(M, N, K, sms);
   const long long max_blocks = (long long)(M < n_ad ? M : n_ad) * ((r_max + 15) / 16);
   const bool sk_fits = sk.ok && L.sk != 0 && (!verify || (tw != nullptr && max_blocks * 128 <= K));
-  if (sk_fits) {
+  if (sk_fits && !cluster_full) {
     e = launch_gemm_sk(g, sk, reinterpret_cast<float *>(ws + L.sk), reinterpret_cast<uint32_t *>(ws + SK_FLAGS_OFF), s,
                        &err);
   } else {
-    e = launch_gemm(g, gemm_shape(M, N, K, sms), s, &err);
+    e = launch_gemm(g, gs, s, &err);
   }
   if (err) return MLORA_ERR_ARG;
   return cuda_status(e);

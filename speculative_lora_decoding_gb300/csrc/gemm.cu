@@ -837,7 +837,10 @@ GemmShape gemm_shape(int M, int N, int K, int num_sms) {
   const bool attrs = ensure_attributes();
   int bestC = 1;
   double best = 1e30;
-  for (int C = 1; C <= MAX_CLUSTER && C <= s.kblocks; ++C) {
+  // Powers of two only: measured, clusters of 3 ran slower than the
+  // persistent stream-K kernel that takes those shapes instead.
+  int bestW = 1;
+  for (int C = 1; C <= MAX_CLUSTER && C <= s.kblocks; C <<= 1) {
     const int red = C > 1 ? RED_BYTES : 0;
     const int st = stages_for(Mb, red);
     if (st < 2) continue;
@@ -857,9 +860,11 @@ GemmShape gemm_shape(int M, int N, int K, int num_sms) {
     if (cost < best - 1e-9) {
       best = cost;
       bestC = C;
+      bestW = (int)waves;
     }
   }
   s.C = bestC;
+  s.waves = bestW;
   s.red_bytes = bestC > 1 ? RED_BYTES : 0;
   s.stages = stages_for(Mb, s.red_bytes);
   s.grid = s.n_units * bestC;

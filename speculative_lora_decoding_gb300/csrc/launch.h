@@ -52,6 +52,7 @@ cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, in
 struct GemmShape {
   int Mb, nsub, sub_n, n_tgroups, n_units, kblocks, total_iters, stages, nbuf, tmem_cols, grid;
   int C;          // CTAs per cluster splitting K (1: no split)
+  int waves;      // rounds of resident clusters the launch takes
   int red_bytes;  // shared memory for the cluster reduction
   size_t smem_bytes, partial_floats;
 };

@@ -115,11 +115,19 @@ def test_nan_rank_padding_in_expand_shapes(M, N, K, n_ad, ranks):
     assert _rel_err(y, y_ref) <= TOL
 
 
-@pytest.mark.parametrize("M,N,K", [(64, 1024, 8192), (128, 4096, 4096), (200, 640, 2048), (1, 8, 512)])
+@pytest.mark.parametrize("M,N,K", [
+    (64, 1024, 8192),    # cluster split-K over 16 CTAs
+    (128, 4096, 4096),   # cluster split-K over 4 CTAs, one full wave
+    (200, 640, 2048),    # stream-K, every tile split 4 ways
+    (64, 6144, 4096),    # stream-K, the fused q|k|v shape
+    (128, 14336, 4096),  # stream-K, the gate shape in verify mode
+    (16, 28672, 4096),   # stream-K, the fused gate|up shape, few rows
+    (1, 8, 512),         # stream-K, a single CTA
+])
 def test_split_tiles_oracle_and_determinism(M, N, K):
-    """Shapes whose tiles are shared by many CTAs (up to 16 partial sums per
-    tile): oracle parity, identical bits on repeated calls, and consecutive
-    calls on one workspace (each call consumes the partial-sum flags it sets)."""
+    """Shapes whose tiles are shared by several CTAs, through both GEMM
+    kernels: oracle parity, identical bits on repeated calls, and consecutive
+    calls on one workspace (stream-K consumes the partial-sum flags it sets)."""
     ml = needs_gpu()
     x, W, A, B, rk, idx = _random_case(M + N + K, M, N, K, 4, (16, 16, 8, 12), r_max=16, nan_pad=True)
     ws = ml.Workspace(ml.linear_workspace_bytes(M, N, K, 4))
