@@ -27,6 +27,7 @@ Under torchrun (N > 1) every rank runs its own replica on its own requests
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -71,6 +72,38 @@ def layer_bytes_flops(M, K, N, active_ranks, verify, n_proj=1):
         b += sum(2 * r * K * n_proj + 2 * N * r for r in active_ranks)
         f += 2 * M * int(np.mean(active_ranks) if active_ranks else 0) * (K * n_proj + N)
     return b, f
+
+
+# DRAM traffic per launch of a kernel, from a committed ncu summary; valid
+# only while the kernel's sources are the ones the counters were taken on.
+TRAFFIC_SOURCES = {
+    "gemm_sk_kernel": ("gemm_sk.cu", "common.cuh", "launch.h"),
+    "gemm_kernel": ("gemm.cu", "common.cuh", "launch.h"),
+}
+
+
+def sources_hash(kernel):
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "speculative_lora_decoding_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel):
+    """(bytes per launch, note) from profiles/<kernel>_traffic_llama8b.md, or
+    (None, why) when there is none or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic_llama8b.md")
+    if not os.path.exists(path):
+        return None, "no ncu traffic summary"
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith(("sources_sha256", "dram_bytes_per_launch")):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("sources_sha256") != sources_hash(kernel):
+        return None, "kernel changed since the ncu capture"
+    return float(fields["dram_bytes_per_launch"]), f"ncu capture, {os.path.relpath(path, ROOT)}"
 
 
 def accept_bytes(B, V, accepted, k):
@@ -389,25 +422,45 @@ def run_gpu(args):
     active_ranks = [int(wl.ranks[a]) for a in active]
     draft_b = draft_t = verify_b = verify_t = 0.0
     draft_f = verify_f = 0.0
+    per_kernel = {}  # GEMM kernel -> draft bytes, draft ms, draft launches, ms over both passes
     for P in wl.proj:
         b, f = layer_bytes_flops(wl.Md, P["K"], P["N"], [], False)
         draft_b += b
         draft_f += f
         draft_t += op_ms[f"draft.{P['name']}"]
+        kd = ml.gemm_kernel_name(wl.Md, P["N"], P["K"], CFG.n_adapters, CFG.r_max, ml.DRAFT)
+        e = per_kernel.setdefault(kd, {"bytes": 0.0, "ms": 0.0, "launches": 0, "ops": [], "both_ms": 0.0})
+        e["bytes"] += b
+        e["ms"] += op_ms[f"draft.{P['name']}"]
+        e["launches"] += 1
+        e["ops"].append(P["name"])
+        e["both_ms"] += op_ms[f"draft.{P['name']}"]
         b, f = layer_bytes_flops(wl.Mv, P["K"], P["N"], active_ranks, True, P["n_proj"])
         verify_b += b
         verify_f += f
         verify_t += op_ms[f"verify.{P['name']}"]
+        kv = ml.gemm_kernel_name(wl.Mv, P["N"], P["K"], CFG.n_adapters, CFG.r_max, ml.VERIFY)
+        per_kernel.setdefault(kv, {"bytes": 0.0, "ms": 0.0, "launches": 0, "ops": [], "both_ms": 0.0})
+        per_kernel[kv]["both_ms"] += op_ms[f"verify.{P['name']}"]
     acc_host = wl.accepted.cpu().numpy()
     acc_b = accept_bytes(CFG.n_requests, CFG.vocab, acc_host, K_DRAFT)
-    achieved = draft_b / (draft_t * 1e-3) / 1e9          # draft layer calls: one GEMM kernel each
+    # The dominant kernel: the GEMM kernel with the most time over both
+    # passes; its roofline from its draft-pass launches, where a layer call is
+    # that one kernel (a verify call also runs the shrink).
+    dom = max((k for k in per_kernel if per_kernel[k]["launches"]), key=lambda k: per_kernel[k]["both_ms"])
+    d = per_kernel[dom]
+    achieved = d["bytes"] / (d["ms"] * 1e-3) / 1e9
+    traffic, traffic_note = profiled_traffic(dom)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
-                "traffic": None,
-                "kernel": f"gemm_kernel (draft pass, {len(wl.proj)} launches: "
-                          + ", ".join(P["name"] for P in wl.proj) + ", M=64)",
+                "traffic": traffic,
+                "kernel": f"{dom} (draft pass: {', '.join(d['ops'])}; M={wl.Md})",
                 "peak_kind": f"{peak_kind} hbm_gbs",
-                "algorithmic_bytes_per_launch": draft_b / len(wl.proj),
-                "avg_launch_us": 1e3 * draft_t / len(wl.proj)}
+                "algorithmic_bytes_per_launch": d["bytes"] / d["launches"],
+                "avg_launch_us": 1e3 * d["ms"] / d["launches"],
+                "traffic_source": traffic_note,
+                "other_kernels": {k: {"draft_GBps": v["bytes"] / (v["ms"] * 1e-3) / 1e9 if v["ms"] else None,
+                                      "draft_ops": v["ops"], "ms_both_passes": v["both_ms"]}
+                                  for k, v in per_kernel.items() if k != dom}}
     modes = {
         "draft_layer": {"us": 1e3 * draft_t, "tokens_per_s": wl.Md / (draft_t * 1e-3),
                         "GBps": draft_b / (draft_t * 1e-3) / 1e9, "frac_hbm": draft_b / (draft_t * 1e-3) / 1e9 / hbm_gbs},

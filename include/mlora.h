@@ -225,6 +225,14 @@ MLORA_API mlora_status mlora_linear_sliced(const mlora_bf16 *x, int M, int K, co
                                            const int32_t *seg_offsets, float scale, int mode, mlora_bf16 *y,
                                            void *workspace, size_t ws_bytes, mlora_stream stream);
 
+/* Which GEMM kernel a layer call of this shape runs on the current device
+ * (the choice is made on the host from the sizes alone): 0 = the cluster
+ * split-K kernel, 1 = the persistent stream-K kernel, -1 = sizes or mode
+ * outside the supported ranges (or no CUDA device).  For observability and
+ * profiling; the results of a call do not depend on it beyond fp32
+ * summation order.  n_adapters and r_max matter in verify mode only. */
+MLORA_API int mlora_linear_gemm_kernel(int M, int N, int K, int n_adapters, int r_max, int mode);
+
 /* Allocation-free variant of mlora_linear.  The paper has no counterpart;
  * this is for callers that cannot allocate device memory for a workspace (a
  * plugin inside a host framework that owns every device buffer, or code

@@ -66,6 +66,7 @@ _SIGNATURES = {
                                      _c_ptr, _c_size, _c_ptr]),
     "mlora_linear_noalloc": (_c_int, [_c_ptr, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int,
                                       _c_ptr, _c_ptr, _c_float, _c_int, _c_ptr, _c_ptr]),
+    "mlora_linear_gemm_kernel": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "mlora_status_string": (ctypes.c_char_p, [_c_int]),
     "mlora_device_supported": (_c_int, []),
     "mlora_launch_count": (ctypes.c_uint64, []),
@@ -137,6 +138,15 @@ def device_supported() -> bool:
 def launch_count() -> int:
     """Kernels the library has launched in this process."""
     return int(_load().mlora_launch_count())
+
+
+def gemm_kernel_name(M: int, N: int, K: int, n_adapters: int, r_max: int, mode: int) -> str:
+    """The GEMM kernel a layer call of this shape runs: "gemm_kernel" (cluster
+    split-K) or "gemm_sk_kernel" (persistent stream-K)."""
+    k = int(_load().mlora_linear_gemm_kernel(M, N, K, n_adapters, r_max, int(mode)))
+    if k < 0:
+        raise ValueError("sizes or mode outside the supported ranges")
+    return ("gemm_kernel", "gemm_sk_kernel")[k]
 
 
 def linear_workspace_bytes(M: int, N: int, K: int, n_adapters: int) -> int:

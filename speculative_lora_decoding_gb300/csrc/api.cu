@@ -78,6 +78,24 @@ static bool linear_sizes_ok(int M, int N, int K, int n_ad) {
 
 static mlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLORA_OK : MLORA_ERR_CUDA; }
 
+// Which GEMM kernel a layer call runs.  The cluster split-K kernel wins when
+// its tiles fill at least 80% of the SMs in a single wave: the weights then
+// stream at the full HBM rate and its on-chip reduction is the shortest
+// tail.  Otherwise (a partial last wave, or idle SMs) the persistent
+// stream-K kernel runs, if it can: batches of up to 256 rows in draft mode,
+// and in verify mode when the tensor-core expand is certain to apply (every
+// (adapter, 16-rank block) pair the plan can list fits the budget
+// expand blocks x 128 <= K, and the masked operand exists: M <= 256).
+static bool use_stream_k(int M, int N, int K, int n_ad, int r_max, bool verify, bool have_tw, bool have_sk, int sms,
+                         const GemmShape &gs, SkShape *sk_out) {
+  const bool cluster_full = gs.waves == 1 && (long long)gs.n_units * gs.C * 5 >= (long long)sms * 4;
+  const SkShape sk = sk_shape(M, N, K, sms);
+  if (sk_out) *sk_out = sk;
+  const long long max_blocks = (long long)(M < n_ad ? M : n_ad) * ((r_max + 15) / 16);
+  const bool fits = sk.ok && have_sk && (!verify || (have_tw && max_blocks * 128 <= K));
+  return fits && !cluster_full;
+}
+
 }  // namespace mlora
 
 using namespace mlora;
@@ -225,19 +243,9 @@ static mlora_status linear_impl(const mlora_bf16 *x, int M, int K, const mlora_b
   g.status = status;
   g.tw = verify ? tw : nullptr;
   int err = 0;
-  // Two GEMM kernels.  The cluster split-K kernel wins when its tiles fill at
-  // least 80% of the SMs in a single wave: the weights then stream at the
-  // full HBM rate and its on-chip reduction is the shortest tail.  Otherwise
-  // (a partial last wave, or idle SMs) the persistent stream-K kernel runs,
-  // if it can: batches of up to 256 rows in draft mode, and in verify mode
-  // when the tensor-core expand is certain to apply (every (adapter, 16-rank
-  // block) pair the plan can list fits the budget expand blocks x 128 <= K).
   const GemmShape gs = gemm_shape(M, N, K, sms);
-  const bool cluster_full = gs.waves == 1 && (long long)gs.n_units * gs.C * 5 >= (long long)sms * 4;
-  const SkShape sk = sk_shape(M, N, K, sms);
-  const long long max_blocks = (long long)(M < n_ad ? M : n_ad) * ((r_max + 15) / 16);
-  const bool sk_fits = sk.ok && L.sk != 0 && (!verify || (tw != nullptr && max_blocks * 128 <= K));
-  if (sk_fits && !cluster_full) {
+  SkShape sk;
+  if (use_stream_k(M, N, K, n_ad, r_max, verify, tw != nullptr, L.sk != 0, sms, gs, &sk)) {
     e = launch_gemm_sk(g, sk, reinterpret_cast<float *>(ws + L.sk), reinterpret_cast<uint32_t *>(ws + SK_FLAGS_OFF), s,
                        &err);
   } else {
@@ -263,6 +271,20 @@ mlora_status mlora_linear_sliced(const mlora_bf16 *x, int M, int K, const mlora_
                                  size_t ws_bytes, mlora_stream stream) {
   return linear_impl(x, M, K, W, N, n_slices, slice_end, A_stack, B_stack, n_adapters, r_max, rank_of, adapter_idx,
                      seg_offsets, scale, mode, y, workspace, ws_bytes, stream);
+}
+
+int mlora_linear_gemm_kernel(int M, int N, int K, int n_adapters, int r_max, int mode) {
+  const int base_mode = mode & ~MLORA_PREFETCH_WEIGHTS;
+  if (base_mode != MLORA_DRAFT && base_mode != MLORA_VERIFY) return -1;
+  const bool verify = base_mode == MLORA_VERIFY;
+  const int n_ad = verify ? n_adapters : 0;
+  if (!linear_sizes_ok(M, N, K, n_ad)) return -1;
+  if (verify && (n_ad < 1 || r_max < 8 || r_max > MLORA_MAX_RANK || (r_max % 8) != 0)) return -1;
+  const int sms = device_sms();
+  if (sms <= 0) return -1;
+  const LinearLayout L = linear_layout(M, n_ad, 1, sms);
+  const GemmShape gs = gemm_shape(M, N, K, sms);
+  return use_stream_k(M, N, K, n_ad, r_max, verify, L.tw != 0, L.sk != 0, sms, gs, nullptr) ? 1 : 0;
 }
 
 mlora_status mlora_verify_accept(const float *p_target, const float *q_draft, const int32_t *draft_tok,

@@ -145,3 +145,21 @@ def test_fused_groups_full_size_sampled(cfg):
                                                         f(Bs[s]), ranks, idx, cfg.scale, mode)
                 n0 = n1
             assert np.max(np.abs(got - want)) <= TOL * max(np.max(np.abs(want)), 1e-30), (cfg.name, group, name)
+
+
+def test_gemm_kernel_query():
+    """mlora_linear_gemm_kernel names one of the two GEMM kernels for valid
+    shapes and refuses invalid ones; on a 152-SM GB300 the decode step's
+    4-tile-per-SM shapes (o, down) take the cluster kernel and the others
+    the stream-K kernel."""
+    ml = needs_gpu()
+    for M, N, K in [(64, 6144, 4096), (64, 4096, 4096), (64, 28672, 4096), (64, 4096, 14336), (700, 512, 512)]:
+        for mode in (ml.DRAFT, ml.VERIFY):
+            assert ml.gemm_kernel_name(M, N, K, 16, 16, mode) in ("gemm_kernel", "gemm_sk_kernel")
+    with pytest.raises(ValueError):
+        ml.gemm_kernel_name(64, 4096, 4097, 16, 16, ml.DRAFT)
+    assert ml.gemm_kernel_name(700, 512, 512, 16, 16, ml.DRAFT) == "gemm_kernel"  # more than 256 rows
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert ml.gemm_kernel_name(64, 4096, 4096, 16, 16, ml.DRAFT) == "gemm_kernel"
+        assert ml.gemm_kernel_name(64, 28672, 4096, 16, 16, ml.DRAFT) == "gemm_sk_kernel"
+        assert ml.gemm_kernel_name(128, 6144, 4096, 16, 16, ml.VERIFY) == "gemm_sk_kernel"
