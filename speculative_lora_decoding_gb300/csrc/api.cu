@@ -92,7 +92,7 @@ static bool use_stream_k(int M, int N, int K, int n_ad, int r_max, bool verify, 
   const SkShape sk = sk_shape(M, N, K, sms);
   if (sk_out) *sk_out = sk;
   const long long max_blocks = (long long)(M < n_ad ? M : n_ad) * ((r_max + 15) / 16);
-  const bool fits = sk.ok && have_sk && (!verify || (have_tw && max_blocks * 128 <= K));
+  const bool fits = sk.ok && have_sk && (!verify || (have_tw && max_blocks * 128 <= K && max_blocks <= SK_EXPAND_TABLE));
   return fits && !cluster_full;
 }
 

@@ -1,5 +1,5 @@
-// Steps a3 + a4: the base GEMM acc = x W^T on the tcgen05 tensor cores and
-// the low-rank expand fused into its epilogue:
+// Steps a3 + a4, cluster split-K kernel: the base GEMM acc = x W^T on the
+// tcgen05 tensor cores plus the low-rank expand:
 //
 //   draft  (LoRA off): y[m, n] = bf16(acc[m, n])
 //   verify (LoRA on):  y[m, n] = bf16(acc[m, n] + scale * sum_{j<r} T[m, j] B_a[n, j]),  a = adapter of row m
@@ -17,10 +17,15 @@
 //  * A unit is 128 W rows x up to 512 tokens.  When there are too few units
 //    to cover the SMs, the C CTAs of one thread-block cluster split the unit's
 //    K range (split-K).  Their fp32 accumulators meet in distributed shared
-//    memory: each CTA copies its accumulator, 32 columns at a time, out of
-//    tensor memory into its own shared memory, and then sums rows
-//    [rank*128/C, (rank+1)*128/C) over all C CTAs in rank order.  The
-//    reduction stays on chip, runs on all C CTAs at once and is deterministic.
+//    memory: each CTA sums rows [rank*128/C, (rank+1)*128/C) over all C CTAs
+//    in rank order.  The reduction stays on chip, runs on all C CTAs at once
+//    and is deterministic.
+//  * The expand, when its (adapter, 16-rank block) pairs are few against K:
+//    one MMA per block, B_a[n0:n0+128, block] x Tmask_block^T, added to the
+//    accumulator after the K loop, the blocks shared out over the cluster's
+//    CTAs, four per ring stage; Tmask holds scale * T on the adapter's rows
+//    and 0 elsewhere (written by the shrink).  Otherwise the epilogue walks
+//    the plan's adapter buckets on the CUDA cores.
 //  * Warp roles: warp 0 issues TMA loads of W and x tiles (128-byte swizzle)
 //    into a ring of shared-memory stages; warp 1 owns tensor memory and issues
 //    tcgen05.mma from one thread; warps 2..5 drain the accumulator with
@@ -47,7 +52,12 @@ constexpr int CHUNK = 32;                             // accumulator columns per
 constexpr int RED_BYTES = 2 * CHUNK * BLOCK_N * 4;    // double-buffered reduction tile, 32 KB
 constexpr int MAX_CLUSTER = 16;
 constexpr size_t SMEM_LIMIT = 220 * 1024;             // leaves room for a co-resident shrink CTA
-constexpr size_t SMEM_FIXED = 1024 + 256;             // alignment slack + barriers
+constexpr int EXPAND_TABLE = 256;                     // expand blocks staged in shared memory
+// Expand blocks per ring stage: a block takes 128 x 16 bf16 of B (4 KB) and
+// Mb x 16 of the masked operand (Mb * 32 B), and 4 * (4096 + 32 Mb) is
+// exactly a stage (16 KB of W + Mb x 64 of x), so four share one stage.
+constexpr int EXPAND_PER_STAGE = 4;
+constexpr size_t SMEM_FIXED = 1024 + 256 + EXPAND_TABLE * 8;  // alignment slack, barriers, expand table
 
 struct GemmArgs {
   int M, N, K;
@@ -61,6 +71,7 @@ struct GemmArgs {
   float scale;
   uint16_t *y;
   const uint16_t *B_stack;
+  const uint16_t *tw;  // masked expand operand, rows already in the 32-byte-swizzled layout
   int r_max, n_ad;
   const float *T;  // [n_slices][M][T_STRIDE]
   const int32_t *plan;
@@ -85,6 +96,7 @@ struct SmemPtrs {
   int *abort_flag;
   int *acc_ready;
   int *zero_word;  // stays 0: for waits that only a time limit may end
+  int2 *exp_tab;   // [EXPAND_TABLE] (adapter, first rank) of each expand block
 };
 
 __device__ __forceinline__ SmemPtrs carve_smem(uint8_t *base, int stages, int stage_bytes, int red_bytes) {
@@ -101,6 +113,7 @@ __device__ __forceinline__ SmemPtrs carve_smem(uint8_t *base, int stages, int st
   p.abort_flag = reinterpret_cast<int *>(w + 1);
   p.acc_ready = reinterpret_cast<int *>(w + 2);
   p.zero_word = reinterpret_cast<int *>(w + 3);
+  p.exp_tab = reinterpret_cast<int2 *>(w + 4);
   return p;
 }
 
@@ -340,8 +353,8 @@ __device__ __forceinline__ void verify_walk(const GemmArgs &a, const PlanLayout 
 
 // Tensor-core expand: after the base K loop, one MMA per (adapter, 16-rank
 // slice) adds B_a[n0:n0+128, slice] x Tmask[:, slice]^T, where Tmask holds
-// scale * T for the adapter's own rows and 0 elsewhere (written by the plan
-// and shrink kernels).  Worth it while the slices' MMA work stays small
+// scale * T for the adapter's own rows and 0 elsewhere (written by the
+// shrink kernel).  Worth it while the slices' MMA work stays small
 // against the base GEMM (slices * 16 <= K / 8), and while every active rank
 // is a multiple of 16 or r_max: a 16-wide block of B columns must not reach
 // the caller's padding inside r_max (it may hold NaN, and NaN * 0 is NaN).
@@ -351,13 +364,12 @@ __device__ __forceinline__ int expand_slices_tc(const GemmArgs &a, const PlanLay
   if (!a.use_tw || a.mode != MLORA_VERIFY) return -1;
   if (a.plan[L.hdr + 5] != 1) return -1;
   const int ns = a.plan[L.hdr + 4];
-  return (ns * 16 * 8 <= a.K) ? ns : -1;
+  return (ns * 16 * 8 <= a.K && ns <= EXPAND_TABLE) ? ns : -1;
 }
 
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
-                const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_tw,
-                const GemmArgs args) {
+                const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align_smem_1024(smem_raw);
   const int S = args.stages;
@@ -391,10 +403,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_w);
     tma_prefetch_desc(&tmap_x);
-    if (args.use_tw) {
-      tma_prefetch_desc(&tmap_b);
-      tma_prefetch_desc(&tmap_tw);
-    }
+    if (args.use_tw) tma_prefetch_desc(&tmap_b);
   }
   if (warp == 1) {
     tmem_alloc(sp.tmem_slot, args.tmem_cols);
@@ -452,20 +461,47 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       }
       const PlanLayout Lp = plan_layout(args.M, args.n_ad);
-      const int ns = (rank == 0 && !*abort_flag) ? expand_slices_tc(args, Lp) : -1;
-      if (ns > 0) {
+      // The expand blocks are shared out over the cluster's C CTAs (the
+      // reduction adds every CTA's accumulator, so any CTA may add any
+      // block): CTA `rank` takes blocks [rank*ns/C, (rank+1)*ns/C).
+      const int ns = !*abort_flag ? expand_slices_tc(args, Lp) : -1;
+      const int blo = ns > 0 ? (int)((long long)rank * ns / C) : 0;
+      const int bhi = ns > 0 ? (int)((long long)(rank + 1) * ns / C) : 0;
+      if (bhi > blo) {
         grid_dependency_wait();  // the masked operand comes from the shrink kernel just before
-        for (int sl = 0; sl < ns; ++sl) {
-          const int ad = args.plan[Lp.slices + 2 * sl], j0 = args.plan[Lp.slices + 2 * sl + 1];
+        // This CTA's part of the expand list comes from the plan 16 entries
+        // per round of independent loads into a shared-memory table, so the
+        // stage loop waits on no global load.
+        for (int b0 = blo; b0 < bhi; b0 += 16) {
+          int ad_b[16], j0_b[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            ad_b[u] = b0 + u < bhi ? args.plan[Lp.slices + 2 * (b0 + u)] : 0;
+            j0_b[u] = b0 + u < bhi ? args.plan[Lp.slices + 2 * (b0 + u) + 1] : 0;
+          }
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            if (b0 + u < bhi) sp.exp_tab[b0 + u] = make_int2(ad_b[u], j0_b[u]);
+        }
+        // Four blocks per stage: B tiles at 4 KB steps, then the masked
+        // operand tiles at Mb * 32 B steps.
+        for (int sl0 = blo; sl0 < bhi; sl0 += EXPAND_PER_STAGE) {
+          const int gn = min(EXPAND_PER_STAGE, bhi - sl0);
           if (!mbar_wait_bounded(&sp.empty[stage], phase ^ 1u, abort_flag)) {
             signal_abort(sp, args.status);
             break;
           }
           uint8_t *st = sp.stage0 + (size_t)stage * stage_bytes;
-          mbar_arrive_expect_tx(&sp.full[stage], (uint32_t)(BLOCK_N * 32 + args.sub_n * 32));
-          tma_load_2d(st, &tmap_b, &sp.full[stage], j0, ad * args.N + n_tile * BLOCK_N, pol_w);
-          tma_load_2d(st + BLOCK_N * 32, &tmap_tw, &sp.full[stage], 0,
-                      slice * args.tw_slice_rows + sl * args.Mpad + m0, pol_x);
+          mbar_arrive_expect_tx(&sp.full[stage], (uint32_t)(gn * (BLOCK_N * 32 + args.sub_n * 32)));
+          for (int g = 0; g < gn; ++g) {
+            const int2 e = sp.exp_tab[sl0 + g];
+            tma_load_2d(st + g * BLOCK_N * 32, &tmap_b, &sp.full[stage], e.y, e.x * args.N + n_tile * BLOCK_N, pol_w);
+          }
+          // The blocks' masked-operand tiles are consecutive (one token
+          // group: Mpad == Mb rows each, m0 == 0): one bulk copy.
+          bulk_load(st + EXPAND_PER_STAGE * BLOCK_N * 32,
+                    args.tw + ((size_t)slice * args.tw_slice_rows + (size_t)sl0 * args.Mpad) * 16,
+                    (uint32_t)(gn * args.Mpad * 32), &sp.full[stage]);
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -529,8 +565,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       }
       const PlanLayout Lm = plan_layout(args.M, args.n_ad);
-      const int ns = (ok && rank == 0) ? expand_slices_tc(args, Lm) : -1;
-      for (int sl = 0; sl < ns; ++sl) {
+      const int ns = ok ? expand_slices_tc(args, Lm) : -1;
+      const int blo = ns > 0 ? (int)((long long)rank * ns / C) : 0;
+      const int bhi = ns > 0 ? (int)((long long)(rank + 1) * ns / C) : 0;
+      for (int sl0 = blo; sl0 < bhi; sl0 += EXPAND_PER_STAGE) {
+        const int gn = min(EXPAND_PER_STAGE, bhi - sl0);
         if (!mbar_wait_bounded(&sp.full[stage], phase, abort_flag)) {
           signal_abort(sp, args.status);
           ok = false;
@@ -538,7 +577,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         tc_fence_after_sync();
         const uint32_t a_addr = smem_addr(sp.stage0 + (size_t)stage * stage_bytes);
-        mma_bf16_ss(tmem_base, smem_desc_kmajor_sw32(a_addr), smem_desc_kmajor_sw32(a_addr + BLOCK_N * 32), idesc, 1u);
+        for (int g = 0; g < gn; ++g)
+          mma_bf16_ss(tmem_base, smem_desc_kmajor_sw32(a_addr + g * BLOCK_N * 32),
+                      smem_desc_kmajor_sw32(a_addr + EXPAND_PER_STAGE * BLOCK_N * 32 + g * args.sub_n * 32), idesc, 1u);
         mma_commit(&sp.empty[stage]);
         if (++stage == S) {
           stage = 0;
@@ -907,7 +948,7 @@ static bool make_map(CUtensorMap *map, const void *base, long long rows, int col
 
 cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s, int *err_code) {
   *err_code = 0;
-  CUtensorMap tw, tx, tb, tt;
+  CUtensorMap tw, tx, tb;
   if (!make_map(&tw, g.W, g.N, g.K, BLOCK_N) || !make_map(&tx, g.x, g.M, g.K, sh.sub_n)) {
     *err_code = 1;
     return cudaErrorInvalidValue;
@@ -915,11 +956,8 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
   // The tensor-core expand needs one token group loaded by one MMA.
   const int use_tw = (g.mode == MLORA_VERIFY && g.tw != nullptr && sh.nsub == 1 && sh.n_tgroups == 1) ? 1 : 0;
   tb = tw;
-  tt = tw;
   if (use_tw) {
-    if (!make_map(&tb, g.B_stack, (long long)g.n_ad * g.N, g.r_max, BLOCK_N, 16) ||
-        !make_map(&tt, g.tw, (long long)g.n_slices * max_expand_slices(g.M, g.n_ad) * expand_rows(g.M), 16, sh.sub_n,
-                  16)) {
+    if (!make_map(&tb, g.B_stack, (long long)g.n_ad * g.N, g.r_max, BLOCK_N, 16)) {
       *err_code = 1;
       return cudaErrorInvalidValue;
     }
@@ -949,6 +987,7 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
   a.scale = g.scale;
   a.y = g.y;
   a.B_stack = g.B_stack;
+  a.tw = g.tw;
   a.r_max = g.r_max;
   a.n_ad = g.n_ad;
   a.T = g.T;
@@ -974,7 +1013,7 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel, tw, tx, tb, tt, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel, tw, tx, tb, a);
   note_launch();
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

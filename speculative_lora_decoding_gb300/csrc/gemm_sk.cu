@@ -39,10 +39,14 @@ constexpr int SK_BK = 64;                        // K per stage: 128 bytes of bf
 constexpr int SK_WTILE = SK_BN * SK_BK * 2;      // 16 KB
 constexpr int SK_CHUNK = 32;                     // accumulator columns per tensor-memory load
 constexpr size_t SK_SMEM_LIMIT = 220 * 1024;     // leaves room for a co-resident shrink CTA
-constexpr size_t SK_SMEM_FIXED = 1024 + 256;     // alignment slack + barriers
+constexpr size_t SK_SMEM_FIXED = 1024 + 256 + SK_EXPAND_TABLE * 16;  // alignment slack, barriers, expand table
 constexpr int SK_MIN_SHARE = 8;                  // k-blocks per CTA at least
 constexpr int SK_MAX_PARTIALS = 8;               // contributors per tile besides its owner, at most
 constexpr int SK_MAX_ROWS = 256;                 // token rows: two accumulators fit in tensor memory
+// Expand blocks per ring stage: a block takes 128 x 16 bf16 of B (4 KB) and
+// Mb x 16 of the masked operand (Mb * 32 B); 4 * (4096 + 32 Mb) is exactly a
+// stage (16 KB of W + Mb x 64 of x).
+constexpr int SK_EXPAND_PER_STAGE = 4;
 
 struct SkArgs {
   int M, N, K, Mb, kblocks, total, P, stages, cols;
@@ -50,6 +54,7 @@ struct SkArgs {
   int n_slices, slice_end[MLORA_MAX_SLICES], tw_slice_rows;
   int n_ad;
   uint16_t *y;
+  const uint16_t *tw;  // masked expand operand, rows already in the 32-byte-swizzled layout
   const int32_t *plan;
   uint32_t *status;
   float *partials;  // [P][Mb][128]: a contributor's partial sums, token-major
@@ -92,13 +97,15 @@ __device__ __forceinline__ void zero_tail_columns_sw32(uint8_t *tile, int c0, in
 
 __global__ void __launch_bounds__(SK_THREADS, 1)
     gemm_sk_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
-                   const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_tw,
-                   const SkArgs args) {
+                   const __grid_constant__ CUtensorMap tmap_b, const SkArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *ring = align_smem_1024(smem_raw);
   const int S = args.stages;
   const int stage_bytes = SK_WTILE + args.Mb * SK_BK * 2;
-  uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)S * stage_bytes);
+  // Expand table: (adapter, first rank, rank columns in the block) per
+  // (adapter, 16-rank block), filled once by the producer from the plan.
+  int4 *exp_tab = reinterpret_cast<int4 *>(ring + (size_t)S * stage_bytes);
+  uint64_t *full = reinterpret_cast<uint64_t *>(exp_tab + SK_EXPAND_TABLE);
   uint64_t *empty = full + S;
   uint64_t *acc_full = empty + S;     // [2]: MMA commit -> epilogue
   uint64_t *acc_empty = acc_full + 2; // [2]: epilogue warps -> MMA issuer
@@ -136,10 +143,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_w);
     tma_prefetch_desc(&tmap_x);
-    if (tc) {
-      tma_prefetch_desc(&tmap_b);
-      tma_prefetch_desc(&tmap_tw);
-    }
+    if (tc) tma_prefetch_desc(&tmap_b);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 2 * args.cols);
@@ -175,8 +179,60 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       int stage = 0, issued = 0, i = 0, ns = -1;
       uint32_t phase = 0;
       bool ok = true;
+      // The expand blocks of an owned tile (verify mode): their operands go
+      // into the ring before the tile's last S k-blocks, so that they land
+      // while those stream instead of after the whole tile.
+      auto issue_expand = [&](int t) -> bool {
+        if (!waited) {
+          grid_dependency_wait();  // the masked operand comes from the shrink kernel just before
+          waited = true;
+        }
+        if (ns < 0) {
+          // The plan's expand list into shared memory, 16 entries per
+          // round of independent loads: the loops below then wait on no
+          // global load per block.  The MMA warp reads the table after its
+          // wait on the first expand stage, which this thread's arrival
+          // (release) on that stage orders after these stores.
+          ns = min(args.plan[L.hdr + 4], SK_EXPAND_TABLE);
+          for (int b0 = 0; b0 < ns; b0 += 16) {
+            int ad[16], j0[16], rk[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              ad[u] = b0 + u < ns ? args.plan[L.slices + 2 * (b0 + u)] : 0;
+              j0[u] = b0 + u < ns ? args.plan[L.slices + 2 * (b0 + u) + 1] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) rk[u] = b0 + u < ns ? args.plan[L.rank_eff + ad[u]] : 0;
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+              if (b0 + u < ns) exp_tab[b0 + u] = make_int4(ad[u], j0[u], rk[u] - j0[u], 0);
+          }
+        }
+        const int row0 = sk_slice_of(args, t * SK_BN) * args.tw_slice_rows;
+        for (int sl0 = 0; sl0 < ns; sl0 += SK_EXPAND_PER_STAGE) {
+          const int gn = min(SK_EXPAND_PER_STAGE, ns - sl0);
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, ab)) return false;
+          uint8_t *st = ring + (size_t)stage * stage_bytes;
+          mbar_arrive_expect_tx(&full[stage], tx_expand * (uint32_t)gn);
+          for (int g = 0; g < gn; ++g) {
+            const int4 e = exp_tab[sl0 + g];
+            tma_load_2d(st + g * SK_BN * 32, &tmap_b, &full[stage], e.y, e.x * args.N + t * SK_BN, pol_w);
+          }
+          // The blocks' masked-operand tiles are consecutive (Mpad == Mb
+          // rows each): one bulk copy brings all of them.
+          bulk_load(st + SK_EXPAND_PER_STAGE * SK_BN * 32, args.tw + ((size_t)row0 + (size_t)sl0 * args.Mpad) * 16,
+                    (uint32_t)(gn * args.Mpad * 32), &full[stage]);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        return true;
+      };
       for (int g = g0; g < g1 && ok;) {
         const int t = g / KB, kb0 = g - t * KB, kb1 = min(KB, g1 - t * KB);
+        const int ins = (tc && kb0 == 0) ? max(kb0, kb1 - 1 - S) : -1;  // expand after this k-block
         for (int kb = kb0; kb < kb1; ++kb, ++i) {
           uint8_t *st = ring + (size_t)stage * stage_bytes;
           if (i >= early) {
@@ -193,29 +249,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             stage = 0;
             phase ^= 1u;
           }
-        }
-        if (ok && tc && kb0 == 0) {
-          if (!waited) {
-            grid_dependency_wait();  // the masked operand comes from the shrink kernel just before
-            waited = true;
-          }
-          if (ns < 0) ns = args.plan[L.hdr + 4];
-          const int row0 = sk_slice_of(args, t * SK_BN) * args.tw_slice_rows;
-          for (int sl = 0; sl < ns; ++sl) {
-            const int ad = args.plan[L.slices + 2 * sl], j0 = args.plan[L.slices + 2 * sl + 1];
-            if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, ab)) {
-              ok = false;
-              break;
-            }
-            uint8_t *st = ring + (size_t)stage * stage_bytes;
-            mbar_arrive_expect_tx(&full[stage], tx_expand);
-            tma_load_2d(st, &tmap_b, &full[stage], j0, ad * args.N + t * SK_BN, pol_w);
-            tma_load_2d(st + SK_BN * 32, &tmap_tw, &full[stage], 0, row0 + sl * args.Mpad, pol_x);
-            ++issued;
-            if (++stage == S) {
-              stage = 0;
-              phase ^= 1u;
-            }
+          if (kb == ins && !issue_expand(t)) {
+            ok = false;
+            break;
           }
         }
         g = t * KB + kb1;
@@ -248,11 +284,12 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       const int t = g / KB, kb0 = g - t * KB, kb1 = min(KB, g1 - t * KB);
       const int buf = seg & 1;
       const uint32_t acc = tmem_base + (uint32_t)(buf * args.cols);
-      if (lane == 0) {
-        // The accumulator's previous use (segment seg - 2) must be drained.
-        if (seg >= 2 && !mbar_wait_bounded(&acc_empty[buf], (uint32_t)(((seg >> 1) - 1) & 1), ab)) ok = false;
-        tc_fence_after_sync();
-        for (int kb = kb0; kb < kb1 && ok; ++kb) {
+      // The same order as the producer: k-blocks up to `ins`, the expand
+      // stages (owned tile, verify mode), then the remaining k-blocks.
+      const bool expand_here = tc && kb0 == 0;
+      const int ins = expand_here ? max(kb0, kb1 - 1 - S) : kb1 - 1;
+      auto mma_kblocks = [&](int from, int to) {  // lane 0: k-blocks [from, to)
+        for (int kb = from; kb < to && ok; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, ab)) {
             ok = false;
             break;
@@ -271,33 +308,46 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             phase ^= 1u;
           }
         }
+      };
+      if (lane == 0) {
+        // The accumulator's previous use (segment seg - 2) must be drained.
+        if (seg >= 2 && !mbar_wait_bounded(&acc_empty[buf], (uint32_t)(((seg >> 1) - 1) & 1), ab)) ok = false;
+        tc_fence_after_sync();
+        mma_kblocks(kb0, ins + 1);
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       stage = __shfl_sync(0xffffffffu, stage, 0);
       phase = __shfl_sync(0xffffffffu, phase, 0);
-      if (ok && tc && kb0 == 0) {
+      if (ok && expand_here) {
         if (ns < 0) {
           grid_dependency_wait();  // the plan and the masked operand come from earlier kernels
-          ns = args.plan[L.hdr + 4];
+          ns = min(args.plan[L.hdr + 4], SK_EXPAND_TABLE);
         }
-        for (int sl = 0; sl < ns && ok; ++sl) {
+        for (int sl0 = 0; sl0 < ns && ok; sl0 += SK_EXPAND_PER_STAGE) {
+          const int gn = min(SK_EXPAND_PER_STAGE, ns - sl0);
           if (lane == 0 && !mbar_wait_bounded(&full[stage], phase, ab)) ok = false;
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
-          const int ad = args.plan[L.slices + 2 * sl], j0 = args.plan[L.slices + 2 * sl + 1];
-          const int c0 = args.plan[L.rank_eff + ad] - j0;  // rank columns of this 16-wide block
           uint8_t *st = ring + (size_t)stage * stage_bytes;
-          if (c0 < 16) {
-            // B columns past the rank hold the caller's padding (maybe NaN;
-            // NaN * 0 would still be NaN): zero them before the MMA reads.
-            zero_tail_columns_sw32(st, c0, lane);
-            fence_proxy_async_smem();
+          bool zeroed = false;
+          for (int g = 0; g < gn; ++g) {
+            const int c0 = exp_tab[sl0 + g].z;  // rank columns of this 16-wide block
+            if (c0 < 16) {
+              // B columns past the rank hold the caller's padding (maybe NaN;
+              // NaN * 0 would still be NaN): zero them before the MMA reads.
+              zero_tail_columns_sw32(st + g * SK_BN * 32, c0, lane);
+              zeroed = true;
+            }
           }
+          if (zeroed) fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             tc_fence_after_sync();
             const uint32_t a_addr = smem_addr(st);
-            mma_bf16_ss(acc, smem_desc_kmajor_sw32(a_addr), smem_desc_kmajor_sw32(a_addr + SK_BN * 32), idesc, 1u);
+            for (int g = 0; g < gn; ++g)
+              mma_bf16_ss(acc, smem_desc_kmajor_sw32(a_addr + g * SK_BN * 32),
+                          smem_desc_kmajor_sw32(a_addr + SK_EXPAND_PER_STAGE * SK_BN * 32 + g * args.Mb * 32), idesc,
+                          1u);
             mma_commit(&empty[stage]);
           }
           if (++stage == S) {
@@ -306,6 +356,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
           }
         }
       }
+      if (lane == 0) mma_kblocks(ins + 1, kb1);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      stage = __shfl_sync(0xffffffffu, stage, 0);
+      phase = __shfl_sync(0xffffffffu, phase, 0);
       if (lane == 0 && ok) mma_commit(&acc_full[buf]);
       __syncwarp();
       g = t * KB + kb1;
@@ -572,18 +626,15 @@ cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partia
       return cudaErrorInvalidValue;
     attr_done[dev] = 1;
   }
-  CUtensorMap tw, tx, tb, tt;
+  CUtensorMap tw, tx, tb;
   if (!sk_map(&tw, g.W, g.N, g.K, SK_BN, SK_BK) || !sk_map(&tx, g.x, g.M, g.K, sh.Mb, SK_BK)) {
     *err_code = 1;
     return cudaErrorInvalidValue;
   }
   const int use_tw = (g.mode == MLORA_VERIFY && g.tw != nullptr) ? 1 : 0;
   tb = tw;
-  tt = tw;
   if (use_tw) {
-    if (!sk_map(&tb, g.B_stack, (long long)g.n_ad * g.N, g.r_max, SK_BN, 16) ||
-        !sk_map(&tt, g.tw, (long long)g.n_slices * max_expand_slices(g.M, g.n_ad) * expand_rows(g.M), 16, sh.Mb,
-                16)) {
+    if (!sk_map(&tb, g.B_stack, (long long)g.n_ad * g.N, g.r_max, SK_BN, 16)) {
       *err_code = 1;
       return cudaErrorInvalidValue;
     }
@@ -608,11 +659,12 @@ cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partia
   a.tw_slice_rows = max_expand_slices(g.M, g.n_ad) * expand_rows(g.M);
   a.n_ad = g.n_ad;
   a.y = g.y;
+  a.tw = g.tw;
   a.plan = g.plan;
   a.status = g.status;
   a.partials = partials;
   a.flags = flags;
-  cudaError_t e = launch_pdl(gemm_sk_kernel, dim3(sh.P), dim3(SK_THREADS), sh.smem_bytes, s, tw, tx, tb, tt, a);
+  cudaError_t e = launch_pdl(gemm_sk_kernel, dim3(sh.P), dim3(SK_THREADS), sh.smem_bytes, s, tw, tx, tb, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -82,6 +82,7 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
 // equal shares of the (tile, k-block) pairs, at most 256 token rows, draft mode
 // or verify mode with the tensor-core expand.  Needs sk_partial_bytes(M, SMs)
 // of scratch for partial sums and one flag word per CTA (zero between calls).
+constexpr int SK_EXPAND_TABLE = 256;  // expand blocks the stream-K kernel stages in shared memory
 struct SkShape {
   bool ok;
   int Mb, cols, stages, n_tiles, kblocks, total, P;

@@ -23,7 +23,10 @@
 // values scale * T[m, j0:j0+16] if m belongs to a and 0 otherwise.  The work
 // items write the member entries of the rank columns below ceil8(rank); a
 // grid-stride pass writes zeros to exactly the other 16-byte halves, so the
-// two never touch the same bytes and no earlier zeroing is needed.
+// two never touch the same bytes and no earlier zeroing is needed.  Rows are
+// stored as the GEMM's shared memory wants them for a 32-byte-swizzled
+// operand (the two 16-byte halves of row m swapped when bit 2 of m is set),
+// so that the GEMM fetches them with one plain bulk copy.
 #include "common.cuh"
 #include "launch.h"
 
@@ -97,7 +100,8 @@ __global__ void __launch_bounds__(SHRINK_THREADS)
       const int a = plan[L.slices + 2 * e], j0 = plan[L.slices + 2 * e + 1];
       const bool member = m < M && plan[L.row_adapter + m] == a;
       if (!(member && j0 + 8 * h < plan[L.rank_eff + a]))
-        *reinterpret_cast<uint4 *>(tw + ((size_t)e * Mpad + m) * 16 + 8 * h) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(tw + ((size_t)e * Mpad + m) * 16 + 8 * (h ^ ((m >> 2) & 1))) =
+            make_uint4(0u, 0u, 0u, 0u);
     }
   }
 
@@ -167,7 +171,9 @@ __global__ void __launch_bounds__(SHRINK_THREADS)
         if (tw) {
           // Member row of the masked operand: slice (j0 + j) / 16 of adapter a.
           const int slice = plan[L.slice_off + a] + (j0 + j) / 16;
-          tw[((size_t)slice * Mpad + rows[t]) * 16 + (j0 + j) % 16] = float_to_bf16_bits(scale * v);
+          const int c = (j0 + j) % 16, m = rows[t];
+          const int pc = (((c >> 3) ^ ((m >> 2) & 1)) << 3) | (c & 7);  // swizzled column
+          tw[((size_t)slice * Mpad + m) * 16 + pc] = float_to_bf16_bits(scale * v);
         }
       }
     }
