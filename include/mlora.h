@@ -275,7 +275,7 @@ MLORA_API mlora_status mlora_linear_noalloc(const mlora_bf16 *x, int M, int K, c
  *   draft_tok int32 [B, k]         uniforms fp32 [B, k+1] in [0, 1)
  *   out_tok   int32 [B, k+1] out:  kept drafts, the drawn token, then -1
  *   accepted  int32 [B] out:       n in [0, k]
- * k in [1, 16], V in [1, 2^24].  Fallbacks: probability NaN/negative -> 0,
+ * B in [1, 32768], k in [1, 16], V in [1, 2^24].  Fallbacks: probability NaN/negative -> 0,
  * above 1 -> 1 (MLORA_DEV_BAD_PROB); uniform NaN/negative -> 0, >= 1 -> the
  * largest float below 1; a draft token outside [0, V) is rejected at its
  * position (MLORA_DEV_BAD_TOKEN); zero residual mass draws from p_n, and zero

@@ -11,16 +11,23 @@
 //   token = smallest v with sum_{v' <= v} w(v') > floor(U * S / 2^32),
 //           S = sum_v w(v), U = floor(u_k * 2^32)
 //
-// Layout: each request's vocabulary row is cut into `slices` contiguous
-// slices, one CTA each, so a small batch still spreads over every SM; each
-// slice is cut into one contiguous sub-range per warp.  A warp reads its
-// sub-range once (coalesced 16-byte loads) and publishes two exact uint64
-// sums (residual mass and target mass).  The last CTA of a request to arrive
-// (atomic counter, no spinning) scans the per-warp sums in vocabulary order,
-// picks the sub-range holding the draw, re-reads only that sub-range in one
-// round (a contiguous run per thread) and locates the token with a block-wide
-// prefix scan.  All sums are integers, so the order of addition cannot change
-// a result.
+// Layout: a request's vocabulary row is cut into chunks of CHUNK = 4096
+// entries, one CTA each, so that a small batch still gives every SM several
+// CTAs and each SM has many 16-byte loads in flight.  Every CTA of a request
+// repeats the accept test (its k gathers hit L2), one lane per draft
+// position.  Because almost every draft is accepted, the CTA requests its
+// chunk of the bonus row p_k before the test resolves; when a draft was
+// rejected it reads p_n and q_n instead.  It publishes the chunk's exact
+// uint64 sums (residual mass and target mass); the last CTA of the request
+// to arrive (atomic counter, no spinning) scans the chunk sums, computes the
+// draw, re-reads only the chunk holding it (one round, a contiguous run per
+// thread) and locates the token with a block-wide prefix scan.  All sums are
+// integers, so the order of addition cannot change a result.
+//
+// Q(f) = floor(f * 2^40) is one fp32 multiply (exact: a power-of-two scale of
+// a value in [0, 1]) and one conversion rounding toward minus infinity to an
+// unsigned 64-bit integer (exact: the scaled value is representable and its
+// integer part is below 2^41).
 #include "common.cuh"
 #include "launch.h"
 
@@ -28,8 +35,10 @@ namespace mlora {
 
 constexpr int ACC_THREADS = 256;
 constexpr int ACC_WARPS = ACC_THREADS / 32;
-constexpr int MIN_SLICE = 4096;
+constexpr int CHUNK = 4096;                       // vocabulary entries per CTA
+constexpr int PER_THREAD = CHUNK / ACC_THREADS;   // 16: four float4 per thread
 constexpr float TWO_POW_32 = 4294967296.0f;
+constexpr float TWO_POW_40 = 1099511627776.0f;
 
 __device__ __forceinline__ float sanitize_prob(float f, uint32_t &flags) {
   if (!(f >= 0.f)) {  // NaN or negative
@@ -55,44 +64,17 @@ __device__ __forceinline__ float sanitize_uniform(float u, uint32_t &flags) {
   return u;
 }
 
-// Q(f) = floor(f * 2^40) for f in [0, 1], from the IEEE-754 fields: a normal
-// f is (2^23 + mantissa) * 2^(exponent - 150), so Q(f) is that 24-bit integer
-// shifted left by (exponent - 110) or, for smaller exponents, right by
-// (110 - exponent) (the right shift is the floor).  Below 2^-40 the result
-// is 0; subnormals are far below that.  Integer operations only.
-__device__ __forceinline__ uint64_t fixq(float f) {
-  const uint32_t bits = __float_as_uint(f);
-  const int e = (int)(bits >> 23) & 0xFF;
-  const uint32_t m = (bits & 0x7FFFFFu) | 0x800000u;
-  const int sh = e - 110;  // e <= 127 for f <= 1, so sh <= 17
-  const uint64_t up = (uint64_t)m << (sh > 0 ? sh : 0);
-  const uint64_t down = (uint64_t)(m >> min(-sh, 31));  // m < 2^24: shifts of 24 or more give 0
-  return sh >= 0 ? up : down;
+// Clamp to [0, 1] (NaN and negatives to 0) and note an out-of-range value.
+__device__ __forceinline__ float clamp_prob(float f, bool &bad) {
+  const float c = fminf(fmaxf(f, 0.f), 1.f);  // fmaxf(NaN, 0) = 0
+  bad |= !(c == f);
+  return c;
 }
 
-// Clamp to [0, 1] (NaN and negatives to 0) and note whether the value was
-// out of range.
-__device__ __forceinline__ float clamp_prob(float f, uint32_t &flags) {
-  if (!(f >= 0.f && f <= 1.f)) flags |= MLORA_DEV_BAD_PROB;
-  return fminf(fmaxf(f, 0.f), 1.f);
-}
+// Q(f) = floor(f * 2^40) for f in [0, 1].
+__device__ __forceinline__ uint64_t fixq(float f) { return __float2ull_rd(f * TWO_POW_40); }
 
-struct Weights {
-  uint64_t res, tgt;
-};
-
-__device__ __forceinline__ Weights weight_of(float p, float q, bool residual, uint32_t &flags) {
-  Weights w;
-  const uint64_t qp = fixq(sanitize_prob(p, flags));
-  w.tgt = qp;
-  if (residual) {
-    const uint64_t qq = fixq(sanitize_prob(q, flags));
-    w.res = qp > qq ? qp - qq : 0ull;
-  } else {
-    w.res = 0ull;
-  }
-  return w;
-}
+__device__ __forceinline__ uint64_t res_weight(uint64_t qp, uint64_t qq) { return qp > qq ? qp - qq : 0ull; }
 
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
 #pragma unroll
@@ -128,121 +110,133 @@ __device__ __forceinline__ uint64_t block_excl_scan_u64(uint64_t v, uint64_t *sh
   return before + inc - v;
 }
 
-// Exact sums over [w0, w1) of one vocabulary row: the target mass sum Q(p)
-// and, when a draft was rejected, the residual mass sum max(0, Q(p) - Q(q)).
-// Eight 16-byte loads per operand are in flight per lane before any is used.
-template <bool RESIDUAL>
-__device__ __forceinline__ void pass1_sums(const float *prow, const float *qrow, int w0, int w1, int lane, int vec,
-                                           uint32_t &flags, uint64_t &s_res, uint64_t &s_tgt) {
-  auto add = [&](float pf, float qf) {
-    const uint64_t qp = fixq(clamp_prob(pf, flags));
-    s_tgt += qp;
-    if (RESIDUAL) {
-      const uint64_t qq = fixq(clamp_prob(qf, flags));
-      s_res += qp > qq ? qp - qq : 0ull;
-    }
-  };
-  if (vec) {
-    const float4 *p4 = reinterpret_cast<const float4 *>(prow);
-    const float4 *q4 = reinterpret_cast<const float4 *>(qrow);
-    const int e0 = w0 >> 2, e1 = w1 >> 2;  // w0, V multiples of 4 on this path
-    int e = e0 + lane;
-    for (; e + 7 * 32 < e1; e += 8 * 32) {
-      float4 pv[8], qv[8];
+// The 16 entries thread `tid` covers in the chunk starting at v0: with
+// 16-byte loads, four float4 at v0 + 4 * (tid + 256 j), j < 4 (a warp reads
+// 512 contiguous bytes per load); otherwise v0 + tid + 256 j, j < 16.  All
+// loads are issued before any value is used.  Entries at or past V read as
+// 0: in range, weight 0.
+__device__ __forceinline__ void load_chunk(const float *row, int v0, int V, int tid, bool vec, float (&f)[PER_THREAD]) {
+  if (vec && v0 + CHUNK <= V) {
+    const float4 *r4 = reinterpret_cast<const float4 *>(row + v0);
+    float4 t[4];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        pv[r] = __ldcs(p4 + e + 32 * r);
-        if (RESIDUAL) qv[r] = __ldcs(q4 + e + 32 * r);
-      }
+    for (int j = 0; j < 4; ++j) t[j] = __ldcs(r4 + tid + ACC_THREADS * j);
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        add(pv[r].x, RESIDUAL ? qv[r].x : 0.f);
-        add(pv[r].y, RESIDUAL ? qv[r].y : 0.f);
-        add(pv[r].z, RESIDUAL ? qv[r].z : 0.f);
-        add(pv[r].w, RESIDUAL ? qv[r].w : 0.f);
-      }
-    }
-    for (; e < e1; e += 32) {
-      const float4 pv = __ldcs(p4 + e);
-      const float4 qv = RESIDUAL ? __ldcs(q4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-      add(pv.x, qv.x);
-      add(pv.y, qv.y);
-      add(pv.z, qv.z);
-      add(pv.w, qv.w);
+    for (int j = 0; j < 4; ++j) {
+      f[4 * j + 0] = t[j].x;
+      f[4 * j + 1] = t[j].y;
+      f[4 * j + 2] = t[j].z;
+      f[4 * j + 3] = t[j].w;
     }
   } else {
-    for (int v = w0 + lane; v < w1; v += 32) add(prow[v], RESIDUAL ? qrow[v] : 0.f);
+#pragma unroll
+    for (int j = 0; j < PER_THREAD; ++j) {
+      const int v = v0 + tid + ACC_THREADS * j;
+      f[j] = v < V ? __ldcs(row + v) : 0.f;
+    }
   }
 }
 
-// Vocabulary row of request b: slices of slice_len (one CTA each), each slice
-// cut into ACC_WARPS contiguous sub-ranges of sub_len (one warp each).
 __global__ void __launch_bounds__(ACC_THREADS)
     accept_kernel(const float *__restrict__ p, const float *__restrict__ q, const int32_t *__restrict__ draft_tok,
-                  const float *__restrict__ uni, int B, int k, int V, int slices, int slice_len, int vec,
+                  const float *__restrict__ uni, int B, int k, int V, int chunks, int vec,
                   int32_t *__restrict__ out_tok, int32_t *__restrict__ accepted, uint32_t *counters,
                   uint64_t *sums, uint32_t *status) {
   __shared__ uint64_t sh_scan[ACC_WARPS];
-  __shared__ int sh_n, sh_last, sh_tok, sh_mode, sh_entry;
-  __shared__ uint32_t sh_flags;
+  __shared__ uint64_t sh_red[2][ACC_WARPS];
+  __shared__ int sh_n, sh_last, sh_tok, sh_mode, sh_chunk;
+  __shared__ uint32_t sh_flags, sh_uflags;
+  __shared__ float sh_uk;
   __shared__ uint64_t sh_T, sh_Tloc;
 
   grid_launch_dependents();
   grid_dependency_wait();
-  const int b = blockIdx.x / slices, g = blockIdx.x % slices;
+  const int b = blockIdx.x / chunks, c = blockIdx.x % chunks;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k1 = k + 1;
-  const int sub_len = slice_len / ACC_WARPS;
-  uint32_t flags = 0;
+  const int v0 = c * CHUNK;
+  const bool vec_ok = vec != 0;
 
-  // Step a5: accept tests (cheap gathers; every CTA of the request agrees).
-  if (tid == 0) {
-    sh_flags = 0;
-    int n = k;
-    for (int i = 0; i < k; ++i) {
-      const int x = draft_tok[(size_t)b * k + i];
+  // Speculatively request this chunk of the bonus row p_k.
+  float fp[PER_THREAD];
+  load_chunk(p + ((size_t)b * k1 + k) * V, v0, V, tid, vec_ok, fp);
+
+  // Step a5: the accept tests, position i on lane i of warp 0 (k <= 16).
+  // The result is what the sequential rule gives: n = the first position
+  // whose draft token is out of range or fails u*q < p, or k; flags come
+  // from positions up to and including n only.
+  if (warp == 0) {
+    uint32_t f = 0;
+    bool pass = true;
+    if (lane < k) {
+      const int x = draft_tok[(size_t)b * k + lane];
       if (x < 0 || x >= V) {
-        flags |= MLORA_DEV_BAD_TOKEN;
-        n = i;
-        break;
-      }
-      const float pi = sanitize_prob(p[((size_t)b * k1 + i) * V + x], flags);
-      const float qi = sanitize_prob(q[((size_t)b * k + i) * V + x], flags);
-      const float ui = sanitize_uniform(uni[(size_t)b * k1 + i], flags);
-      if (!((double)ui * (double)qi < (double)pi)) {
-        n = i;
-        break;
+        f |= MLORA_DEV_BAD_TOKEN;
+        pass = false;
+      } else {
+        const float pi = sanitize_prob(p[((size_t)b * k1 + lane) * V + x], f);
+        const float qi = sanitize_prob(q[((size_t)b * k + lane) * V + x], f);
+        const float ui = sanitize_uniform(uni[(size_t)b * k1 + lane], f);
+        pass = (double)ui * (double)qi < (double)pi;
       }
     }
-    sh_n = n;
+    const uint32_t fail = __ballot_sync(0xffffffffu, lane < k && !pass);
+    const int n = fail ? __ffs(fail) - 1 : k;
+    const uint32_t fl = __reduce_or_sync(0xffffffffu, (lane <= n && lane < k) ? f : 0u);
+    if (lane == 0) {
+      sh_n = n;
+      sh_flags = fl;
+    }
+    if (lane == k) {  // the draw's uniform, needed by the last CTA only, read early
+      uint32_t fu = 0;
+      sh_uk = sanitize_uniform(uni[(size_t)b * k1 + k], fu);
+      sh_uflags = fu;
+    }
   }
+  // Step a6, pass 1, on the bonus row while the accept tests resolve: exact
+  // sums over this chunk (kept only if every draft was accepted).
+  bool bad = false;
+  uint64_t s_res = 0, s_tgt = 0;
+#pragma unroll
+  for (int j = 0; j < PER_THREAD; ++j) s_tgt += fixq(clamp_prob(fp[j], bad));
   block_sync();
   const int n = sh_n;
   const bool residual = n < k;
-  const float *prow = p + ((size_t)b * k1 + n) * V;
-  const float *qrow = residual ? q + ((size_t)b * k + n) * V : prow;
-
-  // Step a6, pass 1: exact sums over this warp's sub-range.
-  const int w0 = min(V, g * slice_len + warp * sub_len), w1 = min(V, w0 + sub_len);
-  uint64_t s_res = 0, s_tgt = 0;
-  if (residual)
-    pass1_sums<true>(prow, qrow, w0, w1, lane, vec, flags, s_res, s_tgt);
-  else
-    pass1_sums<false>(prow, qrow, w0, w1, lane, vec, flags, s_res, s_tgt);
+  if (residual) {
+    bad = false;
+    s_tgt = 0;
+    float fq[PER_THREAD];
+    load_chunk(p + ((size_t)b * k1 + n) * V, v0, V, tid, vec_ok, fp);
+    load_chunk(q + ((size_t)b * k + n) * V, v0, V, tid, vec_ok, fq);
+#pragma unroll
+    for (int j = 0; j < PER_THREAD; ++j) {
+      const uint64_t qp = fixq(clamp_prob(fp[j], bad));
+      const uint64_t qq = fixq(clamp_prob(fq[j], bad));
+      s_tgt += qp;
+      s_res += res_weight(qp, qq);
+    }
+  }
   s_res = warp_sum_u64(s_res);
   s_tgt = warp_sum_u64(s_tgt);
-  const size_t entries = (size_t)slices * ACC_WARPS;
   if (lane == 0) {
-    const size_t at = ((size_t)b * entries + (size_t)g * ACC_WARPS + warp) * 2;
-    sums[at + 0] = s_res;
-    sums[at + 1] = s_tgt;
-    __threadfence();
+    sh_red[0][warp] = s_res;
+    sh_red[1][warp] = s_tgt;
   }
-  if (flags) atomicOr(&sh_flags, flags);
+  if (bad) atomicOr(&sh_flags, MLORA_DEV_BAD_PROB);
   block_sync();
   if (tid == 0) {
+    uint64_t a = 0, t = 0;
+#pragma unroll
+    for (int w = 0; w < ACC_WARPS; ++w) {
+      a += sh_red[0][w];
+      t += sh_red[1][w];
+    }
+    const size_t at = ((size_t)b * chunks + c) * 2;
+    sums[at + 0] = a;
+    sums[at + 1] = t;
+    __threadfence();
     const uint32_t old = atomicAdd(&counters[b], 1u);
-    sh_last = (old == (uint32_t)(slices - 1));
+    sh_last = (old == (uint32_t)(chunks - 1));
   }
   block_sync();
   if (!sh_last) {
@@ -250,16 +244,19 @@ __global__ void __launch_bounds__(ACC_THREADS)
     return;
   }
 
-  // Last CTA of this request: scan the per-warp sums (vocabulary order),
-  // choose the weights and the draw, and find the sub-range holding it.
+  // Last CTA of this request: scan the chunk sums (vocabulary order), choose
+  // the weights and the draw, and find the chunk holding it.
   __threadfence();
-  const int per = (int)((entries + ACC_THREADS - 1) / ACC_THREADS);
-  const int c0 = min((int)entries, tid * per), c1 = min((int)entries, c0 + per);
+  const int per = (chunks + ACC_THREADS - 1) / ACC_THREADS;
+  const int c0 = min(chunks, tid * per), c1 = min(chunks, c0 + per);
   uint64_t my_res = 0, my_tgt = 0;
-  for (int c = c0; c < c1; ++c) {
-    my_res += __ldcg(&sums[((size_t)b * entries + c) * 2 + 0]);
-    my_tgt += __ldcg(&sums[((size_t)b * entries + c) * 2 + 1]);
+  for (int e = c0; e < c1; ++e) {
+    my_res += __ldcg(&sums[((size_t)b * chunks + e) * 2 + 0]);
+    my_tgt += __ldcg(&sums[((size_t)b * chunks + e) * 2 + 1]);
   }
+  // With one chunk per thread (chunks <= 256) the search below needs no
+  // second read of the sums.
+  const bool one_each = per == 1;
   uint64_t S_res, S_tgt;
   const uint64_t ex_res = block_excl_scan_u64(my_res, sh_scan, &S_res);
   const uint64_t ex_tgt = block_excl_scan_u64(my_tgt, sh_scan, &S_tgt);
@@ -272,9 +269,10 @@ __global__ void __launch_bounds__(ACC_THREADS)
       mode = 1;
     }
     const uint64_t S = mode == 0 ? S_res : S_tgt;
-    const float uk = sanitize_uniform(uni[(size_t)b * k1 + k], f2);
+    const float uk = sh_uk;
+    f2 |= sh_uflags;
     sh_tok = -1;
-    sh_entry = -1;
+    sh_chunk = -1;
     if (S == 0) {
       f2 |= MLORA_DEV_ZERO_MASS;
       sh_tok = 0;
@@ -291,11 +289,11 @@ __global__ void __launch_bounds__(ACC_THREADS)
   if (sh_tok < 0) {
     const uint64_t T = sh_T;
     uint64_t run = mode == 0 ? ex_res : ex_tgt;
-    for (int c = c0; c < c1; ++c) {
-      const uint64_t w = __ldcg(&sums[((size_t)b * entries + c) * 2 + mode]);
+    for (int e = c0; e < c1; ++e) {
+      const uint64_t w = one_each ? (mode == 0 ? my_res : my_tgt) : __ldcg(&sums[((size_t)b * chunks + e) * 2 + mode]);
       if (run <= T && T < run + w) {
-        sh_entry = c;
-        sh_Tloc = T - run;  // the draw inside the entry; exactly one thread gets here
+        sh_chunk = e;
+        sh_Tloc = T - run;  // the draw inside the chunk; exactly one thread gets here
       }
       run += w;
     }
@@ -303,31 +301,41 @@ __global__ void __launch_bounds__(ACC_THREADS)
   block_sync();
 
   if (sh_tok < 0) {
-    // Pass 2: one round over the chosen sub-range, a contiguous run per thread.
-    const int ent = sh_entry;
+    // Pass 2: one round over the chosen chunk, a contiguous run of 16
+    // entries per thread (entries past V weigh 0).
+    const int cv0 = sh_chunk * CHUNK + tid * PER_THREAD;
     const uint64_t T = sh_Tloc;
-    const int gs = ent / ACC_WARPS, ws = ent % ACC_WARPS;
-    const int r0 = min(V, gs * slice_len + ws * sub_len), r1 = min(V, r0 + sub_len);
-    const int len = r1 - r0;
-    const int per2 = (len + ACC_THREADS - 1) / ACC_THREADS;
-    const int t0 = min(len, tid * per2), t1 = min(len, t0 + per2);
-    uint64_t mine = 0;
-    uint32_t dummy = 0;
-    for (int v = r0 + t0; v < r0 + t1; ++v) {
-      const Weights w = weight_of(prow[v], residual ? qrow[v] : 0.f, mode == 0, dummy);
-      mine += mode == 0 ? w.res : w.tgt;
+    const float *prow = p + ((size_t)b * k1 + n) * V;
+    const float *qrow = q + ((size_t)b * k + (residual ? n : 0)) * V;
+    const bool use_q = mode == 0;
+    uint64_t w[PER_THREAD];
+    {
+      float a[PER_THREAD], bq[PER_THREAD];
+#pragma unroll
+      for (int j = 0; j < PER_THREAD; ++j) {
+        a[j] = cv0 + j < V ? __ldcg(prow + cv0 + j) : 0.f;
+        bq[j] = (use_q && cv0 + j < V) ? __ldcg(qrow + cv0 + j) : 0.f;
+      }
+      bool dummy = false;
+#pragma unroll
+      for (int j = 0; j < PER_THREAD; ++j) {
+        const uint64_t qp = fixq(clamp_prob(a[j], dummy));
+        w[j] = use_q ? res_weight(qp, fixq(clamp_prob(bq[j], dummy))) : qp;
+      }
     }
+    uint64_t mine = 0;
+#pragma unroll
+    for (int j = 0; j < PER_THREAD; ++j) mine += w[j];
     uint64_t tot;
     uint64_t run = block_excl_scan_u64(mine, sh_scan, &tot);
     if (run <= T && T < run + mine) {
-      for (int v = r0 + t0; v < r0 + t1; ++v) {
-        const Weights w = weight_of(prow[v], residual ? qrow[v] : 0.f, mode == 0, dummy);
-        const uint64_t wv = mode == 0 ? w.res : w.tgt;
-        if (T < run + wv) {
-          sh_tok = v;
+#pragma unroll
+      for (int j = 0; j < PER_THREAD; ++j) {
+        if (T < run + w[j]) {
+          sh_tok = cv0 + j;
           break;
         }
-        run += wv;
+        run += w[j];
       }
     }
   }
@@ -347,18 +355,12 @@ __global__ void __launch_bounds__(ACC_THREADS)
 
 AcceptShape accept_shape(int B, int k, int V, int num_sms) {
   (void)k;
+  (void)num_sms;
   AcceptShape s;
-  int want = (2 * num_sms + B - 1) / B;  // about two CTAs per SM
-  const int max_slices = (V + MIN_SLICE - 1) / MIN_SLICE;
-  if (want > max_slices) want = max_slices;
-  if (want < 1) want = 1;
-  const int quantum = 4 * ACC_WARPS;  // every warp sub-range starts on a float4
-  int len = (V + want - 1) / want;
-  len = (len + quantum - 1) / quantum * quantum;
-  s.slice_len = len;
-  s.slices = (V + len - 1) / len;
+  s.slice_len = CHUNK;
+  s.slices = (V + CHUNK - 1) / CHUNK;
   s.threads = ACC_THREADS;
-  s.scratch_bytes = (size_t)B * s.slices * ACC_WARPS * 2 * sizeof(uint64_t);
+  s.scratch_bytes = (size_t)B * s.slices * 2 * sizeof(uint64_t);
   return s;
 }
 
@@ -369,8 +371,8 @@ cudaError_t launch_accept(const float *p, const float *q, const int32_t *draft_t
                   ((reinterpret_cast<uintptr_t>(q) & 15) == 0);
   const long long grid = (long long)B * sh.slices;
   cudaError_t e = launch_pdl(accept_kernel, dim3((unsigned)grid), dim3(ACC_THREADS), 0, s, p, q, draft_tok, u, B, k, V,
-                             sh.slices, sh.slice_len, vec, out_tok, accepted, counters,
-                             reinterpret_cast<uint64_t *>(scratch), status);
+                             sh.slices, vec, out_tok, accepted, counters, reinterpret_cast<uint64_t *>(scratch),
+                             status);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -117,7 +117,7 @@ size_t mlora_linear_sliced_workspace_bytes(int M, int N, int K, int n_adapters, 
 }
 
 size_t mlora_accept_workspace_bytes(int B, int k, int V) {
-  if (B < 1 || B > (int)WS_MAX_COUNTERS || k < 1 || k > 16 || V < 1 || V > MLORA_MAX_VOCAB) return 0;
+  if (B < 1 || B > (int)WS_MAX_COUNTERS / 2 || k < 1 || k > 16 || V < 1 || V > MLORA_MAX_VOCAB) return 0;
   int sms = device_sms();
   if (sms <= 0) sms = 160;
   return align_up(WS_SCRATCH_OFF + accept_shape(B, k, V, sms).scratch_bytes, 256);
@@ -291,7 +291,8 @@ mlora_status mlora_verify_accept(const float *p_target, const float *q_draft, co
                                  const float *uniforms, int B, int k, int V, int32_t *out_tok, int32_t *accepted,
                                  void *workspace, size_t ws_bytes, mlora_stream stream) {
   if (!p_target || !q_draft || !draft_tok || !uniforms || !out_tok || !accepted) return MLORA_ERR_ARG;
-  if (B < 1 || B > (int)WS_MAX_COUNTERS || k < 1 || k > 16 || V < 1 || V > MLORA_MAX_VOCAB) return MLORA_ERR_SHAPE;
+  // B <= half the counters: the other half holds the stream-K GEMM's flags.
+  if (B < 1 || B > (int)WS_MAX_COUNTERS / 2 || k < 1 || k > 16 || V < 1 || V > MLORA_MAX_VOCAB) return MLORA_ERR_SHAPE;
   if (!workspace || !aligned(workspace, 256)) return MLORA_ERR_WORKSPACE;
   const int sms = device_sms();
   if (sms <= 0) return MLORA_ERR_CUDA;
