@@ -96,6 +96,7 @@ cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partia
 // Steps a5 + a6.
 struct AcceptShape {
   int slices, slice_len, threads;
+  int ring_grid;  // CTAs of the streaming form (rows of aligned float4)
   size_t scratch_bytes;
 };
 AcceptShape accept_shape(int B, int k, int V, int num_sms);

@@ -94,3 +94,47 @@ def test_invalid_inputs_match_oracle_status():
     p[4, :, :] = 0.0          # zero mass
     q[4, :, :] = 0.0
     _check(ml, p, q, tok, u)
+
+
+def _offset_copy(a):
+    """The same values in a device buffer whose start is 4 bytes past a
+    16-byte boundary (rows of aligned float4 are then unavailable)."""
+    flat = torch.empty(a.size + 1, dtype=torch.float32, device="cuda")
+    view = flat[1:].view(a.shape)
+    view.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+    assert view.data_ptr() % 16 == 4
+    return view
+
+
+def test_streaming_and_per_chunk_forms_agree():
+    """Aligned rows take the streaming form, rows starting off a 16-byte
+    boundary the per-chunk form; both must give the oracle's tokens."""
+    ml = needs_gpu()
+    p, q, tok, u = WL.accept_inputs(12288, 40, 2, seed=8)
+    u[::3, 0] = np.float32(0.999999)   # rejections at position 0 in every third request
+    out_r, acc_r, st_r = OA.verify_accept(p, q, tok, u)
+    for mk in (dev, _offset_copy):
+        ws = ml.Workspace(ml.accept_workspace_bytes(40, 2, 12288))
+        out, acc = ml.verify_accept(mk(p), mk(q), dev(tok), dev(u), ws=ws)
+        assert np.array_equal(acc.cpu().numpy(), acc_r) and np.array_equal(out.cpu().numpy(), out_r)
+        assert ws.status() == st_r
+
+
+def test_streaming_form_ranges_touching_many_requests():
+    """One chunk per request and more requests than 31 per SM: the streaming
+    form's CTA ranges then cover up to 32 requests each (and more CTAs than
+    SMs are launched)."""
+    ml = needs_gpu()
+    p, q, tok, u = WL.accept_inputs(1024, 6000, 1, sigma=0.5, seed=9)
+    _check(ml, p, q, tok, u)
+
+
+def test_mixed_rejections_full_vocabulary():
+    """A 128256-entry vocabulary with about half the requests rejected: the
+    streaming form's ranges mix bonus and residual rows, and speculative
+    bonus chunks of rejected requests are dropped."""
+    ml = needs_gpu()
+    p, q, tok, u = WL.accept_inputs(128256, 80, 2, sigma=0.5, seed=10)
+    u[::2, 1] = np.float32(0.999999)
+    acc = _check(ml, p, q, tok, u)
+    assert (acc < 2).sum() >= 30
