@@ -120,18 +120,18 @@ def test_streaming_and_per_chunk_forms_agree():
         assert ws.status() == st_r
 
 
-def test_streaming_form_ranges_touching_many_requests():
-    """One chunk per request and more requests than 31 per SM: the streaming
-    form's CTA ranges then cover up to 32 requests each (and more CTAs than
-    SMs are launched)."""
+def test_streaming_form_many_units_per_cta():
+    """Two chunks per request (the second 8 entries long) and 20000 units:
+    more than 128 units per SM, so the streaming form launches more CTAs
+    than SMs, each owning up to 128 units of as many requests."""
     ml = needs_gpu()
-    p, q, tok, u = WL.accept_inputs(1024, 6000, 1, sigma=0.5, seed=9)
+    p, q, tok, u = WL.accept_inputs(4104, 10000, 1, sigma=0.5, seed=9)
     _check(ml, p, q, tok, u)
 
 
 def test_mixed_rejections_full_vocabulary():
     """A 128256-entry vocabulary with about half the requests rejected: the
-    streaming form's ranges mix bonus and residual rows, and speculative
+    streaming form's CTAs mix bonus and residual rows, and the speculative
     bonus chunks of rejected requests are dropped."""
     ml = needs_gpu()
     p, q, tok, u = WL.accept_inputs(128256, 80, 2, sigma=0.5, seed=10)
