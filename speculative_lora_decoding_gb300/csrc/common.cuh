@@ -335,6 +335,16 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t caddr) {
   return v;
 }
 
+// 16 bytes from a peer CTA's shared memory (caddr 16-byte aligned).
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t caddr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(caddr)
+               : "memory");
+  return v;
+}
+
 // Programmatic dependent launch: wait for the preceding grid's memory, and
 // allow the next grid in the stream to begin launching.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -367,6 +367,86 @@ __device__ __forceinline__ int expand_slices_tc(const GemmArgs &a, const PlanLay
   return (ns * 16 * 8 <= a.K && ns <= EXPAND_TABLE) ? ns : -1;
 }
 
+// Split-K reduction through distributed shared memory: sums rows [r0, r0 + R)
+// of columns [0, ncols) over the C_ peers' fp32 tiles laid out [column][128]
+// at cluster addresses peer[p] (+ base), four rows per 16-byte load, eight
+// loads in flight per thread (two rounds of DSMEM latency for C_ = 4 and 64
+// columns).  Peers are added in rank order.  out(c, i, v) receives rows
+// r0 + i .. r0 + i + 3 of column c.
+template <int C_, class Out>
+__device__ __forceinline__ void cluster_reduce_rows(const uint32_t *peer, uint32_t base, int r0, int R, int ncols,
+                                                    int et, Out &&out) {
+  constexpr int PG = C_ < 8 ? C_ : 8;  // peers per group of loads
+  constexpr int NV = 8 / PG;           // units per round
+  const int R4 = R / 4, total = ncols * R4;
+#pragma unroll 1
+  for (int e0 = et; e0 < total; e0 += 128 * NV) {
+    float4 t[NV];
+#pragma unroll
+    for (int g0 = 0; g0 < C_; g0 += PG) {
+      float4 w[NV][PG];
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int e = e0 + v * 128;
+        if (e < total) {
+          const int c = e / R4, i4 = e - c * R4;
+          const uint32_t off = base + (uint32_t)((c * BLOCK_N + r0 + 4 * i4) * 4);
+#pragma unroll
+          for (int p = 0; p < PG; ++p) w[v][p] = ld_dsmem_f32x4(peer[g0 + p] + off);
+        }
+      }
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+#pragma unroll
+        for (int p = 0; p < PG; ++p) {
+          if (g0 + p == 0) {
+            t[v] = w[v][0];
+          } else {
+            t[v].x += w[v][p].x;
+            t[v].y += w[v][p].y;
+            t[v].z += w[v][p].z;
+            t[v].w += w[v][p].w;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const int e = e0 + v * 128;
+      if (e < total) {
+        const int c = e / R4;
+        out(c, 4 * (e - c * R4), t[v]);
+      }
+    }
+  }
+}
+
+template <class Out>
+__device__ __forceinline__ void cluster_reduce_rows_c(int C, const uint32_t *peer, uint32_t base, int r0, int R,
+                                                      int ncols, int et, Out &&out) {
+  switch (C) {
+    case 2: cluster_reduce_rows<2>(peer, base, r0, R, ncols, et, out); break;
+    case 4: cluster_reduce_rows<4>(peer, base, r0, R, ncols, et, out); break;
+    case 8: cluster_reduce_rows<8>(peer, base, r0, R, ncols, et, out); break;
+    default: cluster_reduce_rows<16>(peer, base, r0, R, ncols, et, out); break;
+  }
+}
+
+// Four bf16 outputs y[row, n .. n + 3] (columns past N dropped).
+__device__ __forceinline__ void store_bf16x4(uint16_t *y, int N, size_t row, int n, float4 v) {
+  uint16_t *dst = y + row * (size_t)N + n;
+  if ((N & 3) == 0 && n + 3 < N) {
+    const uint32_t lo = (uint32_t)float_to_bf16_bits(v.x) | ((uint32_t)float_to_bf16_bits(v.y) << 16);
+    const uint32_t hi = (uint32_t)float_to_bf16_bits(v.z) | ((uint32_t)float_to_bf16_bits(v.w) << 16);
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(lo, hi);
+  } else {
+    const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (n + j < N) dst[j] = float_to_bf16_bits(f[j]);
+  }
+}
+
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
@@ -690,37 +770,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       }
       cluster_sync_all();
-      if (epi) {
-        // Rows [r0, r1) of every column, two elements (2C loads) in flight.
-        const int total = R * mcount;
-#pragma unroll 1
-        for (int e0 = et; e0 < total; e0 += 2 * 128) {
-          float w[2][MAX_CLUSTER];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int e = e0 + u * 128;
-            const int i = e % R, c = e / R;
-            const uint32_t off = (uint32_t)((c * BLOCK_N + r0 + i) * 4);
-            if (e < total) {
-#pragma unroll
-              for (int p = 0; p < MAX_CLUSTER; ++p)
-                if (p < C) w[u][p] = ld_dsmem_f32(peer[p] + off);
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int e = e0 + u * 128;
-            if (e >= total) continue;
-            const int i = e % R, c = e / R;
-            float v = w[u][0];
-#pragma unroll
-            for (int p = 1; p < MAX_CLUSTER; ++p)
-              if (p < C) v += w[u][p];
-            const int n = n_tile * BLOCK_N + r0 + i;
-            if (n < args.N) args.y[(size_t)(m0 + c) * args.N + n] = float_to_bf16_bits(v);
-          }
-        }
-      }
+      if (epi)
+        cluster_reduce_rows_c(C, peer, 0u, r0, R, mcount, et, [&](int c, int i, float4 v) {
+          store_bf16x4(args.y, args.N, (size_t)(m0 + c), n_tile * BLOCK_N + r0 + i, v);
+        });
     } else {
       const uint32_t red_local = smem_addr(sp.red);
       uint32_t peer[MAX_CLUSTER];
@@ -742,26 +795,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         cluster_sync_all();
         if (epi) {
-          for (int e = et; e < R * CHUNK; e += 128) {
-            const int i = e % R, c = e / R;
-            const int col = ch * CHUNK + c;
-            if (col >= mcount) continue;
-            const uint32_t off = (uint32_t)((buf * CHUNK * BLOCK_N + c * BLOCK_N + r0 + i) * 4);
-            float w[MAX_CLUSTER];
-  #pragma unroll
-            for (int p = 0; p < MAX_CLUSTER; ++p)
-              if (p < C) w[p] = ld_dsmem_f32(peer[p] + off);
-            float v = w[0];
-  #pragma unroll
-            for (int p = 1; p < MAX_CLUSTER; ++p)
-              if (p < C) v += w[p];
-            const int n = n_tile * BLOCK_N + r0 + i;
-            if (verify) {
-              fin[col * R + i] = v;
-            } else if (n < args.N) {
-              args.y[(size_t)(m0 + col) * args.N + n] = float_to_bf16_bits(v);
-            }
-          }
+          const int ncols = min(CHUNK, mcount - ch * CHUNK);
+          cluster_reduce_rows_c(C, peer, (uint32_t)(buf * CHUNK * BLOCK_N * 4), r0, R, ncols, et,
+                                [&](int c, int i, float4 v) {
+                                  const int col = ch * CHUNK + c;
+                                  if (verify) {
+                                    *reinterpret_cast<float4 *>(&fin[col * R + i]) = v;
+                                  } else {
+                                    store_bf16x4(args.y, args.N, (size_t)(m0 + col), n_tile * BLOCK_N + r0 + i, v);
+                                  }
+                                });
         }
       }
     }
