@@ -447,7 +447,9 @@ __device__ __forceinline__ void store_bf16x4(uint16_t *y, int N, size_t row, int
   }
 }
 
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+// Shared memory allows one CTA per SM; the second block in the bounds caps
+// registers (at 170) so that a shrink CTA still fits beside this one.
+__global__ void __launch_bounds__(GEMM_THREADS, 2)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];

@@ -14,9 +14,11 @@
 // shared-memory copy.  Warp sums are combined in a fixed order, so T is
 // deterministic.  Rank rows past rank_of[a] are never loaded.
 //
-// Output slices (blockIdx.y): a call may cover several projections that read
-// the same rows x (q, k and v; gate and up), each with its own A stack; slice
-// s reads A + s * n_ad * r_max * K and writes T + s * M * t_stride.
+// Output slices: a call may cover several projections that read the same
+// rows x (q, k and v; gate and up), each with its own A stack; slice s reads
+// A + s * n_ad * r_max * K and writes T + s * M * t_stride.  The grid has at
+// most one CTA per SM, each taking (slice, item) units in turn, so that every
+// SM keeps registers for the GEMM CTA that streams beside it.
 //
 // The masked operand of the tensor-core expand, when requested: for each
 // expand slice e = (adapter a, 16-rank block j0) and token row m, 16 bf16
@@ -69,10 +71,13 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[32]) {
   return v[0];
 }
 
-__global__ void __launch_bounds__(SHRINK_THREADS)
+#ifndef SHRINK_MIN_BLOCKS
+#define SHRINK_MIN_BLOCKS 3  // caps registers at 170: one CTA fits beside a GEMM CTA
+#endif
+__global__ void __launch_bounds__(SHRINK_THREADS, SHRINK_MIN_BLOCKS)
     shrink_kernel(const uint16_t *__restrict__ x, int M, int K, const uint16_t *__restrict__ A_all, int n_ad, int r_max,
                   const int32_t *__restrict__ plan, float *__restrict__ T_all, int t_stride,
-                  uint16_t *__restrict__ tw_all, float scale) {
+                  uint16_t *__restrict__ tw_all, float scale, int n_slices) {
   __shared__ float red[SHRINK_WARPS][SHRINK_J * SHRINK_TOK];
   // Wait for the preceding kernel first, then let the GEMM that follows
   // launch: by then everything the GEMM's mainloop reads (x, W) is complete,
@@ -84,17 +89,16 @@ __global__ void __launch_bounds__(SHRINK_THREADS)
   const int total_items = plan[L.hdr + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kchunks = K >> 3;  // 16-byte pieces per row
-  const int sl = blockIdx.y;
-  const uint16_t *A = A_all + (size_t)sl * n_ad * r_max * K;
-  float *T = T_all + (size_t)sl * M * t_stride;
   const int Mpad = expand_rows(M);
-  uint16_t *tw = tw_all ? tw_all + (size_t)sl * max_expand_slices(M, n_ad) * Mpad * 16 : nullptr;
 
-  if (tw) {
-    // Zero halves: (expand slice e, row m, half h) not written by an item.
+  if (tw_all) {
+    // Zero halves: (slice, expand block e, row m, half h) not written by an item.
     const int n_exp = plan[L.hdr + 4];
     const int halves = n_exp * Mpad * 2;
-    for (int hh = blockIdx.x * SHRINK_THREADS + threadIdx.x; hh < halves; hh += gridDim.x * SHRINK_THREADS) {
+    for (int hs = blockIdx.x * SHRINK_THREADS + threadIdx.x; hs < halves * n_slices;
+         hs += gridDim.x * SHRINK_THREADS) {
+      const int sl = hs / halves, hh = hs - sl * halves;
+      uint16_t *tw = tw_all + (size_t)sl * max_expand_slices(M, n_ad) * Mpad * 16;
       const int e = hh / (2 * Mpad), rem = hh - e * 2 * Mpad;
       const int m = rem >> 1, h = rem & 1;
       const int a = plan[L.slices + 2 * e], j0 = plan[L.slices + 2 * e + 1];
@@ -105,7 +109,12 @@ __global__ void __launch_bounds__(SHRINK_THREADS)
     }
   }
 
-  for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+  // Work units (slice, item), slice-major, one CTA each in turn.
+  for (int wu = blockIdx.x; wu < total_items * n_slices; wu += gridDim.x) {
+    const int sl = wu / total_items, item = wu - sl * total_items;
+    const uint16_t *A = A_all + (size_t)sl * n_ad * r_max * K;
+    float *T = T_all + (size_t)sl * M * t_stride;
+    uint16_t *tw = tw_all ? tw_all + (size_t)sl * max_expand_slices(M, n_ad) * Mpad * 16 : nullptr;
     const int4 *rec = reinterpret_cast<const int4 *>(plan + L.items + (size_t)item * ITEM_WORDS);
     const int4 h = rec[0], rw = rec[1];
     const int a = h.x, j0 = h.y, nrow = h.z, ntok = h.w;
@@ -191,10 +200,11 @@ cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, in
   // Upper bound on work items: ceil(r_max/J) * (ceil(M/TOK) + min(M, n_ad)).
   const long long bound =
       (long long)((r_max + SHRINK_J - 1) / SHRINK_J) * ((M + SHRINK_TOK - 1) / SHRINK_TOK + min(M, n_ad));
-  (void)n_ad;
-  const int grid = (int)max(1LL, min(bound, (long long)num_sms * 8));
-  cudaError_t e = launch_pdl(shrink_kernel, dim3(grid, n_slices), dim3(SHRINK_THREADS), 0, s, x, M, K, A, n_ad, r_max,
-                             plan, T, t_stride, tw, scale);
+  // At most one CTA per SM in all: the GEMM that follows streams beside
+  // these CTAs, and an SM holding two of them has no registers left for it.
+  const int grid = (int)max(1LL, min(bound * n_slices, (long long)num_sms));
+  cudaError_t e = launch_pdl(shrink_kernel, dim3(grid), dim3(SHRINK_THREADS), 0, s, x, M, K, A, n_ad, r_max, plan, T,
+                             t_stride, tw, scale, n_slices);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
