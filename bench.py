@@ -17,7 +17,8 @@ step captured as one CUDA graph.  The W working set (436 MB per pass, read
 twice per step) is larger than L2, so weights stream from HBM every launch.
 `e2e` is the same metric through the Python C-ABI binding with pinned host
 buffers: each step copies that step's activations and probabilities to the
-device and reads every output back.
+device and reads every output back; the copy-in of the next step overlaps
+the current step on a second stream.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -567,7 +568,12 @@ def per_op_durations(torch, wl, stream, args):
 
 
 def run_e2e(torch, ml, wl, stream, side, args, world):
-    """Host buffers in, host buffers out, through the public binding."""
+    """Host buffers in, host buffers out, through the public binding.  Every
+    step copies its activations, adapter indices and probabilities from
+    pinned host memory and reads every output back.  The copy-in of step s+1
+    runs on a second stream while step s computes (two device input sets,
+    each with its own captured graph of the same binding calls); the
+    read-back follows each step on the compute stream."""
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     h_x = [(pin(P["xd_h"].view(np.int16)), pin(P["xv_h"].view(np.int16))) for P in wl.proj]
     p, q, tok, u = wl.acc_h
@@ -581,39 +587,91 @@ def run_e2e(torch, ml, wl, stream, side, args, world):
         a.numel() * a.element_size() for a in h_acc) + h_idx.numel() * 4
     d2h = sum(a.numel() * 2 for a in h_yd + h_yv) + h_out.numel() * 4 + h_acc_out.numel() * 4
 
-    def one():
-        for P, (hd, hv) in zip(wl.proj, h_x):
-            P["xd"].view(torch.int16).copy_(hd, non_blocking=True)
-            P["xv"].view(torch.int16).copy_(hv, non_blocking=True)
-        wl.adx_v.copy_(h_idx, non_blocking=True)
-        for d, h in zip((wl.p, wl.q, wl.tok, wl.u), h_acc):
+    # Two sets of device inputs: the workload's own tensors and a copy.
+    def current():
+        return {"x": [(P["xd"], P["xv"]) for P in wl.proj], "idx": wl.adx_v, "acc": [wl.p, wl.q, wl.tok, wl.u]}
+
+    def use(st):
+        for P, (xd, xv) in zip(wl.proj, st["x"]):
+            P["xd"], P["xv"] = xd, xv
+        wl.adx_v = st["idx"]
+        wl.p, wl.q, wl.tok, wl.u = st["acc"]
+
+    set0 = current()
+    set1 = {"x": [(torch.empty_like(xd), torch.empty_like(xv)) for xd, xv in set0["x"]],
+            "idx": torch.empty_like(set0["idx"]), "acc": [torch.empty_like(a) for a in set0["acc"]]}
+    sets = (set0, set1)
+
+    def copy_in(st):
+        for (xd, xv), (hd, hv) in zip(st["x"], h_x):
+            xd.view(torch.int16).copy_(hd, non_blocking=True)
+            xv.view(torch.int16).copy_(hv, non_blocking=True)
+        st["idx"].copy_(h_idx, non_blocking=True)
+        for d, h in zip(st["acc"], h_acc):
             d.copy_(h, non_blocking=True)
-        wl.step(side)
+
+    def read_back():
         for P, hd, hv in zip(wl.proj, h_yd, h_yv):
             hd.copy_(P["yd"].view(torch.int16), non_blocking=True)
             hv.copy_(P["yv"].view(torch.int16), non_blocking=True)
         h_out.copy_(wl.out_tok, non_blocking=True)
         h_acc_out.copy_(wl.accepted, non_blocking=True)
 
+    graphs = []
+    with torch.cuda.stream(stream):
+        for st in sets:
+            use(st)
+            copy_in(st)
+            wl.step(side)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                wl.step(side)
+            graphs.append(g)
+    use(set0)
+    copy = torch.cuda.Stream(device=wl.p.device)
+    ready = [torch.cuda.Event(), torch.cuda.Event()]
+    free = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def run(n):
+        copy.wait_stream(stream)
+        with torch.cuda.stream(copy):
+            copy_in(sets[0])
+            ready[0].record(copy)
+        for s in range(n):
+            cur, nxt = s % 2, (s + 1) % 2
+            if s + 1 < n:
+                if s >= 1:
+                    copy.wait_event(free[nxt])  # step s-1 has read that set
+                with torch.cuda.stream(copy):
+                    copy_in(sets[nxt])
+                    ready[nxt].record(copy)
+            stream.wait_event(ready[cur])
+            graphs[cur].replay()
+            free[cur].record(stream)
+            read_back()
+
     steps = max(3, min(args.steps, 50))
     with torch.cuda.stream(stream):
-        for _ in range(2):
-            one()
+        run(3)
         stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(steps):
-            one()
+        run(steps)
         e1.record(stream)
     e1.synchronize()
+    torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    if wl.ws.status() != 0:
+        raise RuntimeError("device status bits raised during the end-to-end run")
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([ms], device=wl.p.device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     return {"value": wl.Mv * world / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": steps}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": steps,
+            "overlap": "copy-in of step s+1 on a second stream during step s; read-back after each step"}
 
 
 def main():
