@@ -299,6 +299,33 @@ def prepare_oracle(seed=0):
     return ranks, idx_d, idx_v, proj, acc
 
 
+# ---------------------------------------------------------------------------
+# Ranks (one process per GPU, replicas only)
+# ---------------------------------------------------------------------------
+
+
+def rank_env():
+    """(world size, rank, local rank) from the launcher's environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(torch, value, world, device):
+    """The slowest rank's value: every rank times the same number of steps on
+    its own requests, so the job's time per step is the maximum."""
+    if world <= 1:
+        return float(value)
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank, world, ms_per_step):
+    """Whole-job tokens per second: every rank's tokens over the slowest time."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -312,7 +339,7 @@ def cpu_cores():
 
 
 def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
+    _, rank, _ = rank_env()
     if rank != 0:
         return 0
     prepared = prepare_oracle(0)
@@ -349,9 +376,7 @@ def run_gpu(args):
     import torch
     import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
@@ -405,13 +430,9 @@ def run_gpu(args):
     barrier()
     ms = ev0.elapsed_time(ev1)
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, ms, world, device)
     ms_per_step = ms / args.steps
-    tokens_per_step = wl.Mv * world
-    value = tokens_per_step / (ms_per_step * 1e-3)
+    value = job_throughput(wl.Mv, world, ms_per_step)
     if wl.ws.status() != 0:
         raise RuntimeError("device status bits raised during the timed region")
 
@@ -664,12 +685,8 @@ def run_e2e(torch, ml, wl, stream, side, args, world):
     ms = e0.elapsed_time(e1) / steps
     if wl.ws.status() != 0:
         raise RuntimeError("device status bits raised during the end-to-end run")
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=wl.p.device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": wl.Mv * world / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+    ms = max_over_ranks(torch, ms, world, wl.p.device)
+    return {"value": job_throughput(wl.Mv, world, ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": steps,
             "overlap": "copy-in of step s+1 on a second stream during step s; read-back after each step"}
 
