@@ -271,6 +271,13 @@ MLORA_API mlora_status mlora_linear_noalloc(const mlora_bf16 *x, int M, int K, c
  * Every decision is exact integer / exact float64 arithmetic, so results are
  * bit-reproducible.
  *
+ * Launches: when V % 4 == 0 and p_target and q_draft are 16-byte aligned, a
+ * streaming kernel (one CTA per SM, bulk copies through shared memory) and a
+ * dependent draw kernel; otherwise one kernel with a CTA per (request,
+ * 4096-entry chunk).  Both give the same tokens, status bits and counts.
+ * All pointers are device memory owned by the caller; the call is
+ * asynchronous on `stream`; workspace: mlora_accept_workspace_bytes(B, k, V).
+ *
  *   p_target  fp32 [B, k+1, V]     q_draft  fp32 [B, k, V]
  *   draft_tok int32 [B, k]         uniforms fp32 [B, k+1] in [0, 1)
  *   out_tok   int32 [B, k+1] out:  kept drafts, the drawn token, then -1
