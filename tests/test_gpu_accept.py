@@ -59,7 +59,8 @@ def test_full_sweep_bit_exact(k):
     assert 0 < acc.mean() <= k
 
 
-@pytest.mark.parametrize("B,k,V", [(1, 1, 1), (3, 2, 5), (7, 1, 1001), (64, 1, 128256), (2, 3, 32000), (5, 16, 4099)])
+@pytest.mark.parametrize("B,k,V", [(1, 1, 1), (3, 2, 5), (7, 1, 1001), (64, 1, 128256), (2, 3, 32000), (5, 16, 4099),
+                                   (37, 16, 4100), (19, 5, 8200), (45, 3, 12292)])
 def test_ragged_sizes(B, k, V):
     ml = needs_gpu()
     p, q, tok, u = WL.accept_inputs(V, B, k, sigma=0.5, seed=B + k)
