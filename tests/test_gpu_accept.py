@@ -94,6 +94,10 @@ def test_invalid_inputs_match_oracle_status():
     u[3, 2] = np.float32(1.5)
     p[4, :, :] = 0.0          # zero mass
     q[4, :, :] = 0.0
+    u[5, :2] = np.float32(0.0)  # request 5 keeps both drafts: its bonus row holds a value above 1
+    p[5, 2, 33] = np.float32(1.5)
+    u[6, :2] = np.float32(0.0)  # request 6: a negative zero in its bonus row (valid, no status bit)
+    p[6, 2, 7] = np.float32(-0.0)
     _check(ml, p, q, tok, u)
 
 
