@@ -500,6 +500,10 @@ def run_gpu(args):
 
     # End to end through the binding with pinned host buffers.
     e2e = run_e2e(torch, ml, wl, stream, side, args, world)
+    try:
+        tensor = tensor_probe(torch, ml, device, stream, bf16_tf, peak_kind)
+    except Exception as exc:  # the probe is context; it does not void the step measurement
+        tensor = {"failed": str(exc)}
 
     cpu = None
     if rank == 0 and world == 1:
@@ -534,6 +538,7 @@ def run_gpu(args):
             "roofline": roofline,
             "modes": modes,
             "e2e": e2e,
+            "tensor_bound_verify": tensor,
             "cpu_baseline": cpu,
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                        "samples": clk["samples"]},
@@ -586,6 +591,66 @@ def per_op_durations(torch, wl, stream, args):
     torch.cuda.synchronize()
     return ({name: float(np.median([evs[r][i].elapsed_time(evs[r][i + 1]) for r in range(reps)]))
              for i, (name, _) in enumerate(op_graphs)}, "one graph per op")
+
+
+def tensor_probe(torch, ml, device, stream, bf16_tf, peak_kind):
+    """The verify base GEMM where the tensor cores bound it: the fused gate|up
+    call of the 32B-shaped block with k = 4 drafts (128 requests x 5 = 640
+    rows, 64 rank-16 adapters, ids uniform), random weights on the device,
+    timed over 20 replays of a captured graph with CUDA events: once without
+    the adapters (the base GEMM alone) and once as the full verify call."""
+    cfg = WL.QWEN32B_R16
+    dims = {name: (k_in, n_out) for name, k_in, n_out in cfg.projections}
+    K = dims["gate"][0]
+    N = dims["gate"][1] + dims["up"][1]
+    M, n_ad, r = cfg.rows("verify", 4), cfg.n_adapters, cfg.r_max
+    g = torch.Generator(device=device)
+    g.manual_seed(5)
+    W = (torch.randn(N, K, device=device, generator=g) * 0.02).bfloat16()
+    x = torch.randn(M, K, device=device, generator=g).bfloat16()
+    A = (torch.randn(2, n_ad, r, K, device=device, generator=g) * 0.02).bfloat16()
+    B = (torch.randn(n_ad, N, r, device=device, generator=g) * 0.25).bfloat16()
+    rank_of = torch.full((n_ad,), r, dtype=torch.int32, device=device)
+    idx = torch.randint(0, n_ad, (M,), dtype=torch.int32, device=device, generator=g)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+    ends = [dims["gate"][1], N]
+    ws = ml.Workspace(ml.linear_sliced_workspace_bytes(M, N, K, n_ad, 2), device=device)
+
+    def timed(call):
+        reps = 20
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call()
+            stream.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                call()
+            graph.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    us_base = timed(lambda: ml.linear_sliced(x, W, ends, None, None, None, None, 1.0, ml.DRAFT, ws=ws, y=y))
+    us_ver = timed(lambda: ml.linear_sliced(x, W, ends, A, B, rank_of, idx, cfg.scale, ml.VERIFY, ws=ws, y=y))
+    if ws.status() != 0:
+        raise RuntimeError("device status bits raised in the tensor-bound probe")
+    base = 2.0 * M * N * K
+    lora = 2.0 * M * r * (2 * K + N)  # shrink + expand
+    tf_base = base / (us_base * 1e-6) / 1e12
+    tf_ver = (base + lora) / (us_ver * 1e-6) / 1e12
+    out = {"call": f"gate|up, 32B shapes, k=4: M={M} N={N} K={K}, {n_ad} rank-{r} adapters",
+           "kernel": ml.gemm_kernel_name(M, N, K, n_ad, r, ml.VERIFY), "peak_TFLOPs": bf16_tf,
+           "peak_kind": f"{peak_kind} bf16_tflops_sustained",
+           "base_gemm": {"us_per_call": us_base, "TFLOPs": tf_base, "frac": tf_base / bf16_tf},
+           "verify_call": {"us_per_call": us_ver, "TFLOPs": tf_ver, "frac": tf_ver / bf16_tf,
+                           "expand": "CUDA-core bucket walk (64 blocks x 128 > K rules out the tensor-core expand)"}}
+    del W, x, A, B, y, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(torch, ml, wl, stream, side, args, world):
