@@ -647,7 +647,7 @@ def tensor_probe(torch, ml, device, stream, bf16_tf, peak_kind):
            "peak_kind": f"{peak_kind} bf16_tflops_sustained",
            "base_gemm": {"us_per_call": us_base, "TFLOPs": tf_base, "frac": tf_base / bf16_tf},
            "verify_call": {"us_per_call": us_ver, "TFLOPs": tf_ver, "frac": tf_ver / bf16_tf,
-                           "expand": "CUDA-core bucket walk (64 blocks x 128 > K rules out the tensor-core expand)"}}
+                           "expand": "CUDA-core bucket walk (the tensor-core expand's masked operand covers at most 256 rows)"}}
     del W, x, A, B, y, ws
     torch.cuda.empty_cache()
     return out

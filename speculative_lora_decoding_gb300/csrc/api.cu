@@ -85,14 +85,14 @@ static mlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLORA
 // stream-K kernel runs, if it can: batches of up to 256 rows in draft mode,
 // and in verify mode when the tensor-core expand is certain to apply (every
 // (adapter, 16-rank block) pair the plan can list fits the budget
-// expand blocks x 128 <= K, and the masked operand exists: M <= 256).
+// expand blocks x 32 <= K, and the masked operand exists: M <= 256).
 static bool use_stream_k(int M, int N, int K, int n_ad, int r_max, bool verify, bool have_tw, bool have_sk, int sms,
                          const GemmShape &gs, SkShape *sk_out) {
   const bool cluster_full = gs.waves == 1 && (long long)gs.n_units * gs.C * 5 >= (long long)sms * 4;
   const SkShape sk = sk_shape(M, N, K, sms);
   if (sk_out) *sk_out = sk;
   const long long max_blocks = (long long)(M < n_ad ? M : n_ad) * ((r_max + 15) / 16);
-  const bool fits = sk.ok && have_sk && (!verify || (have_tw && max_blocks * 128 <= K && max_blocks <= SK_EXPAND_TABLE));
+  const bool fits = sk.ok && have_sk && (!verify || (have_tw && max_blocks * 32 <= K && max_blocks <= SK_EXPAND_TABLE));
   return fits && !cluster_full;
 }
 

@@ -354,8 +354,9 @@ __device__ __forceinline__ void verify_walk(const GemmArgs &a, const PlanLayout 
 // Tensor-core expand: after the base K loop, one MMA per (adapter, 16-rank
 // slice) adds B_a[n0:n0+128, slice] x Tmask[:, slice]^T, where Tmask holds
 // scale * T for the adapter's own rows and 0 elsewhere (written by the
-// shrink kernel).  Worth it while the slices' MMA work stays small
-// against the base GEMM (slices * 16 <= K / 8), and while every active rank
+// shrink kernel).  Used up to slices * 16 <= K / 2 (a quarter of the
+// base GEMM's MMA work; measured, the bucket walk below costs 3.5-4.7x the
+// base GEMM at 64 slices, far more than these MMAs), and while every active rank
 // is a multiple of 16 or r_max: a 16-wide block of B columns must not reach
 // the caller's padding inside r_max (it may hold NaN, and NaN * 0 is NaN).
 // Otherwise the epilogue bucket walk adds the low-rank term on the CUDA
@@ -364,7 +365,7 @@ __device__ __forceinline__ int expand_slices_tc(const GemmArgs &a, const PlanLay
   if (!a.use_tw || a.mode != MLORA_VERIFY) return -1;
   if (a.plan[L.hdr + 5] != 1) return -1;
   const int ns = a.plan[L.hdr + 4];
-  return (ns * 16 * 8 <= a.K && ns <= EXPAND_TABLE) ? ns : -1;
+  return (ns * 32 <= a.K && ns <= EXPAND_TABLE) ? ns : -1;
 }
 
 // Split-K reduction through distributed shared memory: sums rows [r0, r0 + R)

@@ -56,7 +56,7 @@ def _run_sliced(ml, x, W, A, B, ranks, idx, ends, scale, mode, ws=None, seg=None
 
 
 @pytest.mark.parametrize("M,widths,K,n_ad,ranks", [
-    # tensor-core expand (M <= 256, slices * 128 <= K)
+    # tensor-core expand (M <= 256, slices * 32 <= K)
     (16, (256, 128, 130), 2048, 4, (8, 16, 24, 0)),
     (128, (512, 128, 128), 4096, 16, (16,) * 16),
     # more expand slices than the tensor-core rule allows: CUDA-core epilogue
