@@ -39,8 +39,10 @@ def test_hand_worked_examples():
         q = np.asarray(c["q"], np.float32)
         tok = np.asarray(c["draft_tok"], np.int32)
         u = np.asarray(c["u"], np.float32)
-        out, acc = _gpu(ml, p, q, tok, u)
+        ws = ml.Workspace(ml.accept_workspace_bytes(*tok.shape, p.shape[-1]))
+        out, acc = _gpu(ml, p, q, tok, u, ws)
         assert out.tolist() == c["out_tok"] and acc.tolist() == c["accepted"], c["why"]
+        assert ws.status() == c.get("status", 0), c["why"]
 
 
 def test_tiny_workload():
