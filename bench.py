@@ -1,26 +1,35 @@
-"""Benchmark of the multi-LoRA decode hot path on GB300.
+"""Benchmark of the multi-LoRA speculative decode hot path on GB300.
 
-One step = one InvisibleLoRA decode cycle through one transformer block's
-seven projections on the Llama-3-8B-shaped workload (64 requests, 16
-resident rank-16 adapters with Zipf(1.1) popularity, 1 draft token per
-request, vocabulary 128256).  Projections that read the same rows go through
-one sliced layer call (q|k|v, gate|up), as a block computes them:
+One step = one InvisibleLoRA decode cycle of one transformer block's seven
+projections ("InvisibleLoRA: Fast Multi-LoRA Serving Without Per-Token LoRA
+Decoding", abstract): k LoRA-off draft passes, one LoRA-on pass that
+verifies the committed token and the k drafts of every request, and the
+accept / resample step.  Projections that read the same rows go through one
+sliced layer call (q|k|v, gate|up), as a block computes them:
 
-    plan (a1, on a second stream, beside the draft pass)
-    draft pass:  4 layer calls (q|k|v, o, gate|up, down), M = 64 rows, LoRA off (a3)
-    verify pass: 4 x (shrink a2 + GEMM a3 + fused expand a4), M = 128 rows
-    accept / resample for 64 requests (a5, a6)
+    plan (a1, on a second stream, beside the draft passes)
+    k draft passes: 4 layer calls each (q|k|v, o, gate|up, down), one row per request, LoRA off (a3)
+    verify pass:    4 x (row gather + shrink a2 + GEMM a3 with the fused expand a4), (k+1) rows per request
+    accept / resample for every request (a5, a6)
 
-`value` is verified tokens (M = 128 per step, summed over ranks) per second
-with every input resident in HBM, from CUDA events around K replays of the
-step captured as one CUDA graph.  The W working set (436 MB per pass, read
-twice per step) is larger than L2, so weights stream from HBM every launch.
+The headline is the largest single-GPU workload: the 32B-class shapes, 128
+requests, 64 rank-16 adapters with uniform popularity and k = 4 drafts (640
+verify rows).  `value` is verified tokens (rows of the LoRA-on pass, summed
+over ranks) per second with every input resident in HBM, from CUDA events
+around K replays of the step captured as one CUDA graph; the W working set
+(1 GB per pass) is far larger than L2, so weights stream from HBM every pass.
 `e2e` is the same metric through the Python C-ABI binding with pinned host
-buffers: each step copies that step's activations and probabilities to the
-device and reads every output back; the copy-in of the next step overlaps
-the current step on a second stream.
+buffers: each step copies that step's activations, adapter indices and
+probabilities to the device and reads every output back.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+The same JSON line carries, under "configs", the other layer workloads (the
+tiny 512x512 layer, the Llama-3-8B-shaped block with 16 rank-16 adapters and
+with 128 heterogeneous-rank adapters, the 32B block at k = 1 and 2) and,
+under "accept_sweep", the accept step alone at batch 256, vocabulary 128256,
+k = 1..4, each with its roofline fraction and the float64 oracle timed on the
+host cores beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--extra all|none] [--impl reference]
 
 Under torchrun (N > 1) every rank runs its own replica on its own requests
 (weak scaling, no collective on the data path); rank 0 prints one JSON line.
@@ -30,6 +39,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -44,19 +54,30 @@ sys.path.insert(0, ROOT)
 
 import workloads as WL  # noqa: E402
 
-CFG = WL.LLAMA8B_R16
-K_DRAFT = 1
-METRIC = "multi-LoRA decode-step tokens/s (draft+verify layer x7 projections + accept)"
+# Layer workloads: (layer config, draft length k).
+LAYER_RUNS = {
+    "tiny": (WL.TINY, 1),
+    "llama8b-r16": (WL.LLAMA8B_R16, 1),
+    "llama8b-het": (WL.LLAMA8B_HET, 1),
+    "32b-k1": (WL.QWEN32B_R16, 1),
+    "32b-k2": (WL.QWEN32B_R16, 2),
+    "32b-k4": (WL.QWEN32B_R16, 4),
+}
+HEADLINE = "32b-k4"
+ACCEPT_SWEEP_K = (1, 2, 3, 4)
+METRIC = "multi-LoRA decode-step verified tokens/s (k draft passes + 1 verify pass of one block's 7 projections + accept)"
 UNIT = "tokens/s"
+L2_BYTES = 126 * 1024 * 1024
 
 
 def _peaks():
+    """(HBM GB/s, bf16 burst TF/s, bf16 sustained TF/s, kind)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops_sustained"]), "measured"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
     except Exception:
-        return 6800.0, 1700.0, "fallback"
+        return 6800.0, 1900.0, 1700.0, "fallback"
 
 
 # ---------------------------------------------------------------------------
@@ -78,8 +99,9 @@ def layer_bytes_flops(M, K, N, active_ranks, verify, n_proj=1):
 # DRAM traffic per launch of a kernel, from a committed ncu summary; valid
 # only while the kernel's sources are the ones the counters were taken on.
 TRAFFIC_SOURCES = {
-    "gemm_sk_kernel": ("gemm_sk.cu", "common.cuh", "launch.h"),
-    "gemm_kernel": ("gemm.cu", "common.cuh", "launch.h"),
+    "gemm_sk_kernel": ("gemm_sk.cu", "expand.cuh", "common.cuh", "launch.h"),
+    "gemm_kernel": ("gemm.cu", "expand.cuh", "common.cuh", "launch.h"),
+    "accept_stream_kernel": ("accept.cu", "common.cuh", "launch.h"),
 }
 
 
@@ -91,12 +113,12 @@ def sources_hash(kernel):
     return h.hexdigest()
 
 
-def profiled_traffic(kernel):
-    """(bytes per launch, note) from profiles/<kernel>_traffic_llama8b.md, or
-    (None, why) when there is none or the kernel changed since."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic_llama8b.md")
+def profiled_traffic(kernel, workload):
+    """(bytes per launch, note) from profiles/<kernel>_traffic_<workload>.md,
+    or (None, why) when there is none or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic_{workload}.md")
     if not os.path.exists(path):
-        return None, "no ncu traffic summary"
+        return None, "no ncu traffic summary for this kernel and workload"
     fields = {}
     for line in open(path):
         if ":" in line and line.strip().startswith(("sources_sha256", "dram_bytes_per_launch")):
@@ -164,95 +186,146 @@ class Clocks:
 
 
 # ---------------------------------------------------------------------------
-# Workload on the device
+# Synthetic inputs on the device (the recipe of `workloads`, drawn with
+# torch's generator on the device so that the 32B-shaped block is ready in
+# seconds; the float64 oracle baseline reads host copies of these tensors)
 # ---------------------------------------------------------------------------
 
 
-def _bf16(torch, bits, device):
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+def _gen(torch, device, seed, *key):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(hashlib.sha256(repr((seed,) + key).encode()).hexdigest()[:15], 16))
+    return g
 
 
-class DeviceWorkload:
-    def __init__(self, torch, ml, device, seed):
-        self.torch, self.ml = torch, ml
-        cfg = CFG
+def _normal_bf16(torch, shape, std, g, device):
+    return (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
+
+
+def accept_inputs_device(torch, V, B, k, device, seed=0, sigma=WL.ACCEPT_SIGMA, target_std=2.0):
+    """p [B, k+1, V], q [B, k, V] fp32 (float64 softmax of target logits
+    N(0, target_std^2) and of the same logits + N(0, sigma^2)), draft tokens
+    [B, k] drawn from q, uniforms [B, k+1] in [0, 1)."""
+    g = _gen(torch, device, seed, "accept", V, B, k)
+    p = torch.empty((B, k + 1, V), dtype=torch.float32, device=device)
+    q = torch.empty((B, k, V), dtype=torch.float32, device=device)
+    step = max(1, (1 << 27) // ((2 * k + 1) * V))  # bound the float64 temporaries
+    for b0 in range(0, B, step):
+        b1 = min(B, b0 + step)
+        z = torch.randn((b1 - b0, k + 1, V), generator=g, device=device, dtype=torch.float64) * target_std
+        p[b0:b1] = torch.softmax(z, dim=-1).float()
+        zq = z[:, :k] + torch.randn((b1 - b0, k, V), generator=g, device=device, dtype=torch.float64) * sigma
+        q[b0:b1] = torch.softmax(zq, dim=-1).float()
+        del z, zq
+    tok = torch.multinomial(q.reshape(B * k, V), 1, generator=g).reshape(B, k).to(torch.int32).contiguous()
+    u = torch.rand((B, k + 1), generator=g, device=device, dtype=torch.float32)
+    return p, q, tok, u
+
+
+class StepWorkload:
+    """Device tensors of one decode-step workload: per input group (q|k|v, o,
+    gate|up, down) the stacked W, A and B, one activation block per draft
+    pass and one for the verify pass; adapter indices; accept inputs."""
+
+    def __init__(self, torch, ml, device, name, seed):
+        self.torch, self.ml, self.name = torch, ml, name
+        cfg, k = LAYER_RUNS[name]
+        self.cfg, self.k = cfg, k
         self.ranks = WL.adapter_ranks(cfg, seed)
         self.idx_d = WL.row_adapters(cfg, "draft", seed=seed)
-        self.idx_v = WL.row_adapters(cfg, "verify", k=K_DRAFT, seed=seed)
+        self.idx_v = WL.row_adapters(cfg, "verify", k=k, seed=seed)
         self.Md, self.Mv = len(self.idx_d), len(self.idx_v)
-        # One entry per input group: the projections' W stacked along N, their
-        # A stacks side by side, their B stacks along N, the shared rows x.
         self.proj = []
+        rk = torch.from_numpy(self.ranks.astype(np.int64)).to(device)
+        r_max = cfg.r_max
         for group in WL.input_groups(cfg):
             Ws, As, Bs = [], [], []
-            for p in group:
-                W, A, B, _ = WL.projection_weights(cfg, p, seed=seed)
-                Ws.append(W)
-                As.append(A)
-                Bs.append(B)
             K = cfg.projections[group[0]][1]
+            for p in group:
+                _, Kp, N = cfg.projections[p]
+                g = _gen(torch, device, seed, "W", p)
+                Ws.append(_normal_bf16(torch, (N, Kp), 1.0 / math.sqrt(Kp), g, device))
+                A = _normal_bf16(torch, (cfg.n_adapters, r_max, Kp), 1.0 / math.sqrt(Kp), _gen(torch, device, seed, "A", p),
+                                 device)
+                A *= (torch.arange(r_max, device=device)[None, :] < rk[:, None]).to(torch.bfloat16)[:, :, None]
+                Bm = torch.randn((cfg.n_adapters, N, r_max), generator=_gen(torch, device, seed, "B", p), device=device)
+                Bm = Bm / torch.sqrt(torch.clamp(rk, min=1).float())[:, None, None]
+                Bm = (Bm * (torch.arange(r_max, device=device)[None, None, :] < rk[:, None, None])).to(torch.bfloat16)
+                As.append(A)
+                Bs.append(Bm)
             ends = [int(e) for e in np.cumsum([w.shape[0] for w in Ws])]
             N = ends[-1]
-            name = "_".join(cfg.projections[p][0] for p in group)
-            xd = WL.activations(cfg, group[0], "draft", seed=seed)
-            xv = WL.activations(cfg, group[0], "verify", k=K_DRAFT, seed=seed)
-            self.proj.append(dict(name=name, K=K, N=N, ends=ends, n_proj=len(group),
-                                  W=_bf16(torch, np.concatenate(Ws, axis=0), device),
-                                  A=_bf16(torch, np.stack(As), device),
-                                  B=_bf16(torch, np.concatenate(Bs, axis=1), device),
-                                  xd=_bf16(torch, xd, device), xv=_bf16(torch, xv, device), xd_h=xd, xv_h=xv,
+            gname = "_".join(cfg.projections[p][0] for p in group)
+            xd = [_normal_bf16(torch, (self.Md, K), 1.0, _gen(torch, device, seed, "xd", group[0], d), device)
+                  for d in range(k)]
+            xv = _normal_bf16(torch, (self.Mv, K), 1.0, _gen(torch, device, seed, "xv", group[0]), device)
+            self.proj.append(dict(name=gname, K=K, N=N, ends=ends, n_proj=len(group), W=torch.cat(Ws, 0).contiguous(),
+                                  A=torch.stack(As).contiguous(), B=torch.cat(Bs, 1).contiguous(), xd=xd, xv=xv,
                                   yd=torch.empty((self.Md, N), dtype=torch.bfloat16, device=device),
-                                  yv=torch.empty((self.Mv, N), dtype=torch.bfloat16, device=device)))
+                                  yv=torch.empty((self.Mv, N), dtype=torch.bfloat16, device=device),
+                                  yb=torch.empty((self.Mv, N), dtype=torch.bfloat16, device=device)))
+            del Ws, As, Bs
         self.rank_of = torch.from_numpy(self.ranks).to(device)
-        self.adx_d = torch.from_numpy(self.idx_d).to(device)
         self.adx_v = torch.from_numpy(self.idx_v).to(device)
-        p, q, tok, u = WL.accept_inputs(cfg.vocab, cfg.n_requests, K_DRAFT, seed=seed)
-        self.acc_h = (p, q, tok, u)
-        self.p, self.q, self.tok, self.u = (torch.from_numpy(a).to(device) for a in (p, q, tok, u))
-        self.out_tok = torch.empty((cfg.n_requests, K_DRAFT + 1), dtype=torch.int32, device=device)
-        self.accepted = torch.empty((cfg.n_requests,), dtype=torch.int32, device=device)
+        B = cfg.n_requests
+        self.p, self.q, self.tok, self.u = accept_inputs_device(torch, cfg.vocab, B, k, device, seed=seed)
+        self.out_tok = torch.empty((B, k + 1), dtype=torch.int32, device=device)
+        self.accepted = torch.empty((B,), dtype=torch.int32, device=device)
         ws_bytes = max(ml.linear_sliced_workspace_bytes(self.Mv, P["N"], P["K"], cfg.n_adapters, len(P["ends"]))
                        for P in self.proj)
-        ws_bytes = max(ws_bytes, ml.accept_workspace_bytes(cfg.n_requests, K_DRAFT, cfg.vocab))
+        ws_bytes = max(ws_bytes, ml.accept_workspace_bytes(B, k, cfg.vocab))
         self.ws = ml.Workspace(ws_bytes, device=device)
         self.seg = None
+        self.w_bytes_per_pass = sum(2 * P["N"] * P["K"] for P in self.proj)
 
-    # individual ops of one step, in order
-    def ops(self):
-        ml, cfg = self.ml, CFG
+    @property
+    def workload(self):
+        return f"{self.cfg.name}/k={self.k}/vocab={self.cfg.vocab}"
+
+    def ops(self, with_base=False):
+        """The step's ops in stream order (name, kind, group, callable);
+        with_base adds, after the step, a draft-mode call of each group at the
+        verify rows (the base GEMM alone at that shape, for comparison)."""
+        ml, cfg = self.ml, self.cfg
         out = []
 
         def plan():
             self.seg, _ = ml.plan_segments(self.adx_v, self.rank_of, cfg.n_adapters, cfg.r_max, self.ws)
-        out.append(("plan", plan))
+        out.append(("plan", "plan", None, plan))
+        for d in range(self.k):
+            for P in self.proj:
+                out.append((f"draft{d}.{P['name']}", "draft", P, lambda P=P, d=d: ml.linear_sliced(
+                    P["xd"][d], P["W"], P["ends"], None, None, None, None, cfg.scale, ml.DRAFT | ml.PREFETCH_WEIGHTS,
+                    ws=self.ws, y=P["yd"])))
         for P in self.proj:
-            out.append((f"draft.{P['name']}", lambda P=P: ml.linear_sliced(
-                P["xd"], P["W"], P["ends"], None, None, None, None, cfg.scale, ml.DRAFT | ml.PREFETCH_WEIGHTS,
-                ws=self.ws, y=P["yd"])))
-        for P in self.proj:
-            out.append((f"verify.{P['name']}", lambda P=P: ml.linear_sliced(
+            out.append((f"verify.{P['name']}", "verify", P, lambda P=P: ml.linear_sliced(
                 P["xv"], P["W"], P["ends"], P["A"], P["B"], self.rank_of, self.adx_v, cfg.scale,
                 ml.VERIFY | ml.PREFETCH_WEIGHTS, ws=self.ws, y=P["yv"], seg_offsets_ptr=self.seg)))
-        out.append(("accept", lambda: ml.verify_accept(self.p, self.q, self.tok, self.u, ws=self.ws,
-                                                      out_tok=self.out_tok, accepted=self.accepted)))
+        out.append(("accept", "accept", None, lambda: ml.verify_accept(
+            self.p, self.q, self.tok, self.u, ws=self.ws, out_tok=self.out_tok, accepted=self.accepted)))
+        if with_base:
+            for P in self.proj:
+                out.append((f"base.{P['name']}", "base", P, lambda P=P: ml.linear_sliced(
+                    P["xv"], P["W"], P["ends"], None, None, None, None, cfg.scale, ml.DRAFT | ml.PREFETCH_WEIGHTS,
+                    ws=self.ws, y=P["yb"])))
         return out
 
     def step(self, side=None):
         """One step in stream order.  With `side` (a second stream) the plan,
         which needs only the adapter indices, runs on it concurrently with the
-        draft pass, and the verify pass waits for it."""
+        draft passes, and the verify pass waits for it."""
         ops = self.ops()
         if side is None:
-            for _, f in ops:
+            for _, _, _, f in ops:
                 f()
             return
         torch = self.torch
         main = torch.cuda.current_stream()
         side.wait_stream(main)
         with torch.cuda.stream(side):
-            ops[0][1]()
-        for name, f in ops[1:]:
-            if name.startswith("verify.") and side is not None:
+            ops[0][3]()
+        for _, kind, _, f in ops[1:]:
+            if kind == "verify" and side is not None:
                 main.wait_stream(side)
                 side = None
             f()
@@ -263,40 +336,68 @@ class DeviceWorkload:
 # ---------------------------------------------------------------------------
 
 
-def oracle_sample_step(requests, seed=0, prepared=None):
-    """Run the oracle over `requests` requests of the workload (all 7
-    projections, draft and verify rows, then accept).  Returns (seconds,
-    verify tokens)."""
+def _f64(torch, t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def oracle_sample(torch, wl, requests):
+    """Host float64 copies of what the oracle needs for `requests` requests
+    of the workload: every group's full W, the A and B of the adapters those
+    requests use (relabelled 0..), their rows, and their accept inputs."""
+    cfg, k = wl.cfg, wl.k
+    req = np.arange(requests)
+    ads = sorted({int(a) for a in wl.idx_d[req] if a >= 0})
+    remap = {a: i for i, a in enumerate(ads)}
+    sub = lambda arr: np.array([remap.get(int(a), -1) for a in arr], dtype=np.int32)  # noqa: E731
+    rows_v = np.concatenate([np.arange(r * (k + 1), (r + 1) * (k + 1)) for r in req])
+    sel = torch.tensor(ads if ads else [0], dtype=torch.long, device=wl.p.device)
+    groups = []
+    for P in wl.proj:
+        ends = [0] + P["ends"]
+        W = _f64(torch, P["W"])
+        A = _f64(torch, P["A"][:, sel]) if ads else None
+        B = _f64(torch, P["B"][sel]) if ads else None
+        per_slice = [(W[ends[s]:ends[s + 1]], A[s] if ads else None, B[:, ends[s]:ends[s + 1]] if ads else None)
+                     for s in range(len(P["ends"]))]
+        xd = [_f64(torch, P["xd"][d][req]) for d in range(k)]
+        xv = _f64(torch, P["xv"][torch.from_numpy(rows_v).to(wl.p.device)])
+        groups.append((per_slice, xd, xv))
+    ranks = wl.ranks[ads] if ads else np.zeros(1, np.int32)
+    acc = tuple(t[:requests].cpu().numpy() for t in (wl.p, wl.q, wl.tok, wl.u))
+    return dict(groups=groups, ranks=ranks, idx_v=sub(wl.idx_v[rows_v]), acc=acc, rows_v=len(rows_v),
+                scale=cfg.scale)
+
+
+def oracle_step(sample):
+    """The oracle over the sample: k draft passes and the verify pass of every
+    projection, then the accept step.  Returns (seconds, verified tokens)."""
     from oracle import accept as OA
     from oracle import layer as OL
-    cfg = CFG
-    if prepared is None:
-        prepared = prepare_oracle(seed)
-    ranks, idx_d, idx_v, proj, acc = prepared
-    rows_d = np.arange(requests)
-    rows_v = np.arange(requests * (K_DRAFT + 1))
     t0 = time.perf_counter()
-    for (W, A, B, xd, xv) in proj:
-        OL.mlora_linear(xd[rows_d], W, None, None, None, None, cfg.scale, OL.DRAFT)
-        OL.mlora_linear(xv[rows_v], W, A, B, ranks, idx_v[rows_v], cfg.scale, OL.VERIFY)
-    p, q, tok, u = acc
-    OA.verify_accept(p[:requests], q[:requests], tok[:requests], u[:requests])
-    return time.perf_counter() - t0, len(rows_v)
+    for per_slice, xd, xv in sample["groups"]:
+        for W, A, B in per_slice:
+            for x in xd:
+                OL.mlora_linear(x, W, None, None, None, None, sample["scale"], OL.DRAFT)
+            if A is not None:
+                OL.mlora_linear(xv, W, A, B, sample["ranks"], sample["idx_v"], sample["scale"], OL.VERIFY)
+            else:
+                OL.mlora_linear(xv, W, None, None, None, None, sample["scale"], OL.DRAFT)
+    OA.verify_accept(*sample["acc"])
+    return time.perf_counter() - t0, sample["rows_v"]
 
 
-def prepare_oracle(seed=0):
-    cfg = CFG
-    f = WL.bf16_to_f64
-    ranks = WL.adapter_ranks(cfg, seed)
-    idx_d = WL.row_adapters(cfg, "draft", seed=seed)
-    idx_v = WL.row_adapters(cfg, "verify", k=K_DRAFT, seed=seed)
-    proj = []
-    for p in range(len(cfg.projections)):
-        W, A, B, _ = WL.projection_weights(cfg, p, seed=seed)
-        proj.append((f(W), f(A), f(B), f(WL.activations(cfg, p, "draft", seed=seed)),
-                     f(WL.activations(cfg, p, "verify", k=K_DRAFT, seed=seed))))
-    acc = WL.accept_inputs(cfg.vocab, 8, K_DRAFT, seed=seed)
-    return ranks, idx_d, idx_v, proj, acc
+def time_oracle(torch, wl, seconds, requests=1):
+    sample = oracle_sample(torch, wl, requests)
+    oracle_step(sample)  # first call: BLAS start-up
+    secs, toks, nrep = 0.0, 0, 0
+    while secs < seconds and nrep < 50:
+        t, n = oracle_step(sample)
+        secs += t
+        toks += n
+        nrep += 1
+    return {"value": toks / secs, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{nrep} x {requests} request(s) ({wl.k} draft rows + {wl.k + 1} verify rows each) through the "
+                      f"7 projections + accept, float64 numpy on the host cores, BLAS default threads"}
 
 
 # ---------------------------------------------------------------------------
@@ -342,29 +443,45 @@ def run_reference(args):
     _, rank, _ = rank_env()
     if rank != 0:
         return 0
-    prepared = prepare_oracle(0)
-    req = 1
+    import torch
+    name = getattr(args, "config", None) or HEADLINE
+    wl = StepWorkload(torch, _NoLib(), torch.device("cpu"), name, seed=0)
+    sample = oracle_sample(torch, wl, 1)
     for _ in range(args.warmup):
-        oracle_sample_step(req, prepared=prepared)
+        oracle_step(sample)
     times, toks = [], 0
     for _ in range(args.steps):
-        t, n = oracle_sample_step(req, prepared=prepared)
+        t, n = oracle_step(sample)
         times.append(t)
         toks += n
     total = sum(times)
     value = toks / total
-    cores = cpu_cores()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": CFG.name + f"/k={K_DRAFT}/vocab={CFG.vocab}", "requests_per_step": req},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{req} request per step: 7 projections draft+verify rows + accept, float64 numpy"},
+        "config": {"workload": wl.workload, "requests_per_step": 1},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"1 request per step ({wl.k} draft rows + {wl.k + 1} verify rows through the 7 "
+                                   "projections + accept), float64 numpy"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
     return 0
+
+
+class _NoLib:
+    """Stands in for the library when the reference arm builds the workload
+    on the CPU: only the workspace sizing is asked, and no workspace is made."""
+
+    def linear_sliced_workspace_bytes(self, *a):
+        return 0
+
+    def accept_workspace_bytes(self, *a):
+        return 0
+
+    def Workspace(self, *a, **k):
+        return None
 
 
 # ---------------------------------------------------------------------------
@@ -372,349 +489,264 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 
 
-def run_gpu(args):
-    import torch
-    import torch.distributed as dist
-
-    world, rank, local = rank_env()
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-
-    import speculative_lora_decoding_gb300 as ml
-    if not os.path.exists(ml.LIB_PATH):
-        import __graft_entry__
-        __graft_entry__.build()
-    if not ml.device_supported():
-        raise RuntimeError("this benchmark needs a compute capability 10.3 GPU")
-
-    wl = DeviceWorkload(torch, ml, device, seed=rank)
-    stream = torch.cuda.Stream(device)
-    side = torch.cuda.Stream(device)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
-            wl.step(side)
-    stream.synchronize()
-    if wl.ws.status() != 0:
-        raise RuntimeError("device status bits raised during warm-up")
-
-    # Whole step as one CUDA graph.
-    graph = torch.cuda.CUDAGraph()
-    n0 = ml.launch_count()
-    with torch.cuda.graph(graph, stream=stream):
-        wl.step(side)
-    launches_per_step = ml.launch_count() - n0
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    clocks = Clocks(local)
-    clocks.start()
-    time.sleep(0.3)
-    barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        ev1.record(stream)
-    ev1.synchronize()
-    torch.cuda.synchronize()
-    barrier()
-    ms = ev0.elapsed_time(ev1)
-    clk = clocks.stop()
-    ms = max_over_ranks(torch, ms, world, device)
-    ms_per_step = ms / args.steps
-    value = job_throughput(wl.Mv, world, ms_per_step)
-    if wl.ws.status() != 0:
-        raise RuntimeError("device status bits raised during the timed region")
-
-    op_ms, timing_kind = per_op_durations(torch, wl, stream, args)
-
-    # Algorithmic work.
-    hbm_gbs, bf16_tf, peak_kind = _peaks()
-    active = sorted(set(int(a) for a in wl.idx_v if a >= 0))
-    active_ranks = [int(wl.ranks[a]) for a in active]
-    draft_b = draft_t = verify_b = verify_t = 0.0
-    draft_f = verify_f = 0.0
-    per_kernel = {}  # GEMM kernel -> draft bytes, draft ms, draft launches, ms over both passes
-    for P in wl.proj:
-        b, f = layer_bytes_flops(wl.Md, P["K"], P["N"], [], False)
-        draft_b += b
-        draft_f += f
-        draft_t += op_ms[f"draft.{P['name']}"]
-        kd = ml.gemm_kernel_name(wl.Md, P["N"], P["K"], CFG.n_adapters, CFG.r_max, ml.DRAFT)
-        e = per_kernel.setdefault(kd, {"bytes": 0.0, "ms": 0.0, "launches": 0, "ops": [], "both_ms": 0.0})
-        e["bytes"] += b
-        e["ms"] += op_ms[f"draft.{P['name']}"]
-        e["launches"] += 1
-        e["ops"].append(P["name"])
-        e["both_ms"] += op_ms[f"draft.{P['name']}"]
-        b, f = layer_bytes_flops(wl.Mv, P["K"], P["N"], active_ranks, True, P["n_proj"])
-        verify_b += b
-        verify_f += f
-        verify_t += op_ms[f"verify.{P['name']}"]
-        kv = ml.gemm_kernel_name(wl.Mv, P["N"], P["K"], CFG.n_adapters, CFG.r_max, ml.VERIFY)
-        per_kernel.setdefault(kv, {"bytes": 0.0, "ms": 0.0, "launches": 0, "ops": [], "both_ms": 0.0})
-        per_kernel[kv]["both_ms"] += op_ms[f"verify.{P['name']}"]
-    acc_host = wl.accepted.cpu().numpy()
-    acc_b = accept_bytes(CFG.n_requests, CFG.vocab, acc_host, K_DRAFT)
-    # The dominant kernel: the GEMM kernel with the most time over both
-    # passes; its roofline from its draft-pass launches, where a layer call is
-    # that one kernel (a verify call also runs the shrink).
-    dom = max((k for k in per_kernel if per_kernel[k]["launches"]), key=lambda k: per_kernel[k]["both_ms"])
-    d = per_kernel[dom]
-    achieved = d["bytes"] / (d["ms"] * 1e-3) / 1e9
-    traffic, traffic_note = profiled_traffic(dom)
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
-                "traffic": traffic,
-                "kernel": f"{dom} (draft pass: {', '.join(d['ops'])}; M={wl.Md})",
-                "peak_kind": f"{peak_kind} hbm_gbs",
-                "algorithmic_bytes_per_launch": d["bytes"] / d["launches"],
-                "avg_launch_us": 1e3 * d["ms"] / d["launches"],
-                "traffic_source": traffic_note,
-                "other_kernels": {k: {"draft_GBps": v["bytes"] / (v["ms"] * 1e-3) / 1e9 if v["ms"] else None,
-                                      "draft_ops": v["ops"], "ms_both_passes": v["both_ms"]}
-                                  for k, v in per_kernel.items() if k != dom}}
-    modes = {
-        "draft_layer": {"us": 1e3 * draft_t, "tokens_per_s": wl.Md / (draft_t * 1e-3),
-                        "GBps": draft_b / (draft_t * 1e-3) / 1e9, "frac_hbm": draft_b / (draft_t * 1e-3) / 1e9 / hbm_gbs},
-        "verify_layer": {"us": 1e3 * verify_t, "tokens_per_s": wl.Mv / (verify_t * 1e-3),
-                         "GBps": verify_b / (verify_t * 1e-3) / 1e9,
-                         "frac_hbm": verify_b / (verify_t * 1e-3) / 1e9 / hbm_gbs,
-                         "TFLOPs": verify_f / (verify_t * 1e-3) / 1e12},
-        "accept": {"us": 1e3 * op_ms["accept"], "rows_per_s": CFG.n_requests / (op_ms["accept"] * 1e-3),
-                   "GBps": acc_b / (op_ms["accept"] * 1e-3) / 1e9,
-                   "mean_accepted": float(acc_host.mean())},
-        "plan_us": 1e3 * op_ms["plan"],
-        "per_op_timing": timing_kind,
-        "per_op_us": {k: 1e3 * v for k, v in op_ms.items()},
-    }
-
-    # End to end through the binding with pinned host buffers.
-    e2e = run_e2e(torch, ml, wl, stream, side, args, world)
-    try:
-        tensor = tensor_probe(torch, ml, device, stream, bf16_tf, peak_kind)
-    except Exception as exc:  # the probe is context; it does not void the step measurement
-        tensor = {"failed": str(exc)}
-
-    cpu = None
-    if rank == 0 and world == 1:
-        try:
-            prepared = prepare_oracle(0)
-            oracle_sample_step(1, prepared=prepared)
-            secs, toks, nrep = 0.0, 0, 0
-            while secs < 10.0 and nrep < 50:
-                t, n = oracle_sample_step(8, prepared=prepared)
-                secs += t
-                toks += n
-                nrep += 1
-            cpu = {"value": toks / secs, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                   "sample": f"{nrep} x 8 requests (16 verify + 8 draft rows) through 7 projections + accept, "
-                             "float64 numpy, BLAS default threads"}
-        except Exception as exc:  # a baseline that fails does not void the GPU number
-            cpu = {"value": None, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": f"failed: {exc}"}
-
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": CFG.name + f"/k={K_DRAFT}/vocab={CFG.vocab}", "requests": CFG.n_requests,
-                       "draft_rows": wl.Md, "verify_rows": wl.Mv,
-                       "projections": [p[0] for p in CFG.projections],
-                       "layer_calls": [p["name"] for p in wl.proj],
-                       "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2: 436 MB of W streamed per pass, two passes per step",
-                       "graph": "one CUDA graph per step; the plan runs on a second stream beside the draft pass"},
-            "gpu_launches": launches_per_step * args.steps,
-            "roofline": roofline,
-            "modes": modes,
-            "e2e": e2e,
-            "tensor_bound_verify": tensor,
-            "cpu_baseline": cpu,
-            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
-                       "samples": clk["samples"]},
-        }
-        print(json.dumps(line))
-    if world > 1:
-        dist.destroy_process_group()
-    return 0
+def graph_of(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
 
 
-def per_op_durations(torch, wl, stream, args):
-    """Median duration of every op of the step, from CUDA events on the
-    launching stream.  Preferred: one step graph with an event node between
-    consecutive ops (external events), replayed and read back step by step.
-    Fallback: each op in its own graph, replayed back to back."""
-    ops = wl.ops()
-    reps = max(10, min(args.steps, 200))
-    try:
-        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(ops) + 1)]
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            evs[0].record(stream)
-            for i, (_, fn) in enumerate(ops):
-                fn()
-                evs[i + 1].record(stream)
-        torch.cuda.synchronize()
-        samples = [[] for _ in ops]
-        for _ in range(reps):
-            g.replay()
-            torch.cuda.synchronize()
-            for i in range(len(ops)):
-                samples[i].append(evs[i].elapsed_time(evs[i + 1]))
-        return {name: float(np.median(samples[i])) for i, (name, _) in enumerate(ops)}, "events inside the step graph"
-    except Exception:
-        pass
-    op_graphs = []
-    for name, fn in ops:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            fn()
-        op_graphs.append((name, g))
-    torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(op_graphs) + 1)] for _ in range(reps)]
-    with torch.cuda.stream(stream):
-        for r in range(reps):
-            evs[r][0].record(stream)
-            for i, (_, g) in enumerate(op_graphs):
-                g.replay()
-                evs[r][i + 1].record(stream)
-    torch.cuda.synchronize()
-    return ({name: float(np.median([evs[r][i].elapsed_time(evs[r][i + 1]) for r in range(reps)]))
-             for i, (name, _) in enumerate(op_graphs)}, "one graph per op")
-
-
-def tensor_probe(torch, ml, device, stream, bf16_tf, peak_kind):
-    """The verify base GEMM where the tensor cores bound it: the fused gate|up
-    call of the 32B-shaped block with k = 4 drafts (128 requests x 5 = 640
-    rows, 64 rank-16 adapters, ids uniform), random weights on the device,
-    timed over 20 replays of a captured graph with CUDA events: once without
-    the adapters (the base GEMM alone) and once as the full verify call."""
-    cfg = WL.QWEN32B_R16
-    dims = {name: (k_in, n_out) for name, k_in, n_out in cfg.projections}
-    K = dims["gate"][0]
-    N = dims["gate"][1] + dims["up"][1]
-    M, n_ad, r = cfg.rows("verify", 4), cfg.n_adapters, cfg.r_max
-    g = torch.Generator(device=device)
-    g.manual_seed(5)
-    W = (torch.randn(N, K, device=device, generator=g) * 0.02).bfloat16()
-    x = torch.randn(M, K, device=device, generator=g).bfloat16()
-    A = (torch.randn(2, n_ad, r, K, device=device, generator=g) * 0.02).bfloat16()
-    B = (torch.randn(n_ad, N, r, device=device, generator=g) * 0.25).bfloat16()
-    rank_of = torch.full((n_ad,), r, dtype=torch.int32, device=device)
-    idx = torch.randint(0, n_ad, (M,), dtype=torch.int32, device=device, generator=g)
-    y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
-    ends = [dims["gate"][1], N]
-    ws = ml.Workspace(ml.linear_sliced_workspace_bytes(M, N, K, n_ad, 2), device=device)
-
-    def timed(call):
-        reps = 20
+def time_replays(torch, graph, stream, reps, flush=None):
+    """ms per replay.  Without `flush`: events around `reps` back-to-back
+    replays.  With it: the flush (a write larger than L2) runs before every
+    replay and only the replays are timed (one event pair each)."""
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
-            for _ in range(3):
-                call()
-            stream.synchronize()
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                call()
-            graph.replay()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for _ in range(reps):
                 graph.replay()
             e1.record(stream)
         e1.synchronize()
-        return e0.elapsed_time(e1) * 1e3 / reps
+        return e0.elapsed_time(e1) / reps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            flush()
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return float(np.median([a.elapsed_time(b) for a, b in evs]))
 
-    us_base = timed(lambda: ml.linear_sliced(x, W, ends, None, None, None, None, 1.0, ml.DRAFT, ws=ws, y=y))
-    us_ver = timed(lambda: ml.linear_sliced(x, W, ends, A, B, rank_of, idx, cfg.scale, ml.VERIFY, ws=ws, y=y))
-    if ws.status() != 0:
-        raise RuntimeError("device status bits raised in the tensor-bound probe")
-    base = 2.0 * M * N * K
-    lora = 2.0 * M * r * (2 * K + N)  # shrink + expand
-    tf_base = base / (us_base * 1e-6) / 1e12
-    tf_ver = (base + lora) / (us_ver * 1e-6) / 1e12
-    out = {"call": f"gate|up, 32B shapes, k=4: M={M} N={N} K={K}, {n_ad} rank-{r} adapters",
-           "kernel": ml.gemm_kernel_name(M, N, K, n_ad, r, ml.VERIFY), "peak_TFLOPs": bf16_tf,
-           "peak_kind": f"{peak_kind} bf16_tflops_sustained",
-           "base_gemm": {"us_per_call": us_base, "TFLOPs": tf_base, "frac": tf_base / bf16_tf},
-           "verify_call": {"us_per_call": us_ver, "TFLOPs": tf_ver, "frac": tf_ver / bf16_tf,
-                           "expand": "CUDA-core bucket walk (the tensor-core expand's masked operand covers at most 256 rows)"}}
-    del W, x, A, B, y, ws
-    torch.cuda.empty_cache()
+
+def per_op_durations(torch, ops, stream, reps):
+    """Median duration of every op, from CUDA events on the launching stream
+    between consecutive ops inside one captured graph (external events),
+    replayed and read back one replay at a time."""
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(ops) + 1)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        evs[0].record(stream)
+        for i, op in enumerate(ops):
+            op[3]()
+            evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    samples = [[] for _ in ops]
+    for _ in range(reps):
+        g.replay()
+        torch.cuda.synchronize()
+        for i in range(len(ops)):
+            samples[i].append(evs[i].elapsed_time(evs[i + 1]))
+    return {op[0]: float(np.median(samples[i])) for i, op in enumerate(ops)}
+
+
+def measure_layer(torch, ml, wl, stream, side, steps, peaks, flush):
+    """Step time, per-op breakdown, roofline figures of one workload."""
+    hbm_gbs, bf16_burst, bf16_sus, peak_kind = peaks
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            wl.step(side)
+    stream.synchronize()
+    if wl.ws.status() != 0:
+        raise RuntimeError(f"{wl.name}: device status bits raised during warm-up")
+    n0 = ml.launch_count()
+    graph = graph_of(torch, lambda: wl.step(side), stream)
+    launches = ml.launch_count() - n0
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    use_flush = wl.w_bytes_per_pass < 2 * L2_BYTES
+    ms_step = time_replays(torch, graph, stream, steps, flush if use_flush else None)
+    if wl.ws.status() != 0:
+        raise RuntimeError(f"{wl.name}: device status bits raised during the timed region")
+    op_ms = per_op_durations(torch, wl.ops(with_base=True), stream, max(10, min(steps, 100)))
+
+    cfg, k = wl.cfg, wl.k
+    active = sorted(set(int(a) for a in wl.idx_v if a >= 0))
+    active_ranks = [int(wl.ranks[a]) for a in active]
+    draft_b = draft_t = verify_b = verify_t = verify_f = 0.0
+    kernels = {}  # GEMM kernel -> {bytes, flops, ms, launches, ops, kind}
+    calls = {}
+    for P in wl.proj:
+        bd, fd = layer_bytes_flops(wl.Md, P["K"], P["N"], [], False)
+        kd = ml.gemm_kernel_name(wl.Md, P["N"], P["K"], cfg.n_adapters, cfg.r_max, ml.DRAFT)
+        td = sum(op_ms[f"draft{d}.{P['name']}"] for d in range(k))
+        draft_b += k * bd
+        draft_t += td
+        e = kernels.setdefault(kd, {"draft_bytes": 0.0, "draft_ms": 0.0, "draft_launches": 0, "draft_ops": [],
+                                    "verify_flops": 0.0, "verify_ms": 0.0, "verify_ops": []})
+        e["draft_bytes"] += k * bd
+        e["draft_ms"] += td
+        e["draft_launches"] += k
+        e["draft_ops"].append(P["name"])
+        bv, fv = layer_bytes_flops(wl.Mv, P["K"], P["N"], active_ranks, True, P["n_proj"])
+        tv = op_ms[f"verify.{P['name']}"]
+        tb = op_ms[f"base.{P['name']}"]
+        verify_b += bv
+        verify_f += fv
+        verify_t += tv
+        kv = ml.gemm_kernel_name(wl.Mv, P["N"], P["K"], cfg.n_adapters, cfg.r_max, ml.VERIFY)
+        e = kernels.setdefault(kv, {"draft_bytes": 0.0, "draft_ms": 0.0, "draft_launches": 0, "draft_ops": [],
+                                    "verify_flops": 0.0, "verify_ms": 0.0, "verify_ops": []})
+        e["verify_flops"] += fv
+        e["verify_ms"] += tv
+        e["verify_ops"].append(P["name"])
+        base_f = 2.0 * wl.Mv * P["N"] * P["K"]
+        calls[P["name"]] = {
+            "M_verify": wl.Mv, "N": P["N"], "K": P["K"], "verify_kernel": kv, "draft_kernel": kd,
+            "verify_us": 1e3 * tv, "verify_TFLOPs": fv / (tv * 1e-3) / 1e12,
+            "base_at_verify_rows_us": 1e3 * tb, "base_TFLOPs": base_f / (tb * 1e-3) / 1e12,
+            "verify_over_base": tv / tb, "draft_us_per_pass": 1e3 * td / k,
+            "draft_GBps": k * bd / (td * 1e-3) / 1e9}
+    acc_host = wl.accepted.cpu().numpy()
+    acc_b = accept_bytes(cfg.n_requests, cfg.vocab, acc_host, k)
+    t_acc = op_ms["accept"]
+    # The dominant kernel: the GEMM kernel with the most time over the step.
+    dom = max(kernels, key=lambda n: kernels[n]["draft_ms"] + kernels[n]["verify_ms"])
+    d = kernels[dom]
+    if d["draft_launches"]:
+        achieved = d["draft_bytes"] / (d["draft_ms"] * 1e-3) / 1e9
+        traffic, note = profiled_traffic(dom, wl.name)
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
+                "traffic": traffic, "kernel": f"{dom} (draft passes: {', '.join(d['draft_ops'])}; M={wl.Md})",
+                "peak_kind": f"{peak_kind} hbm_gbs",
+                "algorithmic_bytes_per_launch": d["draft_bytes"] / d["draft_launches"],
+                "avg_launch_us": 1e3 * d["draft_ms"] / d["draft_launches"], "traffic_source": note}
+    else:
+        achieved = d["verify_flops"] / (d["verify_ms"] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_sus, "unit": "TFLOP/s", "frac": achieved / bf16_sus,
+                "traffic": None, "kernel": f"{dom} (verify pass: {', '.join(d['verify_ops'])}; M={wl.Mv})",
+                "peak_kind": f"{peak_kind} bf16_tflops_sustained"}
+    others = {}
+    for n, e in kernels.items():
+        if n == dom:
+            continue
+        o = {}
+        if e["draft_ms"]:
+            o["draft_GBps"] = e["draft_bytes"] / (e["draft_ms"] * 1e-3) / 1e9
+            o["draft_frac_hbm"] = o["draft_GBps"] / hbm_gbs
+        if e["verify_ms"]:
+            o["verify_TFLOPs"] = e["verify_flops"] / (e["verify_ms"] * 1e-3) / 1e12
+            o["verify_frac_bf16_sustained"] = o["verify_TFLOPs"] / bf16_sus
+        o["ops"] = {"draft": e["draft_ops"], "verify": e["verify_ops"]}
+        others[n] = o
+    roof["other_kernels"] = others
+    modes = {
+        "draft_pass": {"passes": k, "us_per_pass": 1e3 * draft_t / k, "tokens_per_s": wl.Md * k / (draft_t * 1e-3),
+                       "GBps": draft_b / (draft_t * 1e-3) / 1e9,
+                       "frac_hbm": draft_b / (draft_t * 1e-3) / 1e9 / hbm_gbs},
+        "verify_pass": {"us": 1e3 * verify_t, "tokens_per_s": wl.Mv / (verify_t * 1e-3),
+                        "GBps": verify_b / (verify_t * 1e-3) / 1e9, "frac_hbm": verify_b / (verify_t * 1e-3) / 1e9 / hbm_gbs,
+                        "TFLOPs": verify_f / (verify_t * 1e-3) / 1e12,
+                        "frac_bf16_sustained": verify_f / (verify_t * 1e-3) / 1e12 / bf16_sus},
+        "accept": {"us": 1e3 * t_acc, "requests": cfg.n_requests, "rows_per_s": cfg.n_requests / (t_acc * 1e-3),
+                   "GBps": acc_b / (t_acc * 1e-3) / 1e9, "frac_hbm": acc_b / (t_acc * 1e-3) / 1e9 / hbm_gbs,
+                   "mean_accepted": float(acc_host.mean())},
+        "plan_us": 1e3 * op_ms["plan"],
+        "per_op_timing": "events between the ops inside one step graph (breaks the launch overlap at each boundary)",
+        "per_op_us": {n: 1e3 * v for n, v in op_ms.items()},
+        "calls": calls,
+    }
+    return {"ms_per_step": ms_step, "tokens_per_s": wl.Mv / (ms_step * 1e-3), "launches_per_step": launches,
+            "roofline": roof, "modes": modes,
+            "l2": ("L2 flushed before each timed step (W smaller than 2x L2)" if use_flush else
+                   f"inputs larger than L2: {wl.w_bytes_per_pass / 1e6:.0f} MB of W streamed per pass, "
+                   f"{k + 1} passes per step")}
+
+
+def measure_accept_sweep(torch, ml, device, stream, reps, peaks, flush, oracle_seconds):
+    """The accept step alone at batch 256, vocabulary 128256, k = 1..4."""
+    from oracle import accept as OA
+    hbm_gbs = peaks[0]
+    cfg = WL.ACCEPT_SWEEP
+    out = {"workload": f"{cfg.name}: B={cfg.batch} V={cfg.vocab} k=1..4, target logits N(0, 2^2), draft logits + "
+                       f"N(0, {WL.ACCEPT_SIGMA}^2)", "l2": "L2 flushed before each timed call", "k": {}}
+    for k in ACCEPT_SWEEP_K:
+        p, q, tok, u = accept_inputs_device(torch, cfg.vocab, cfg.batch, k, device, seed=17)
+        ws = ml.Workspace(ml.accept_workspace_bytes(cfg.batch, k, cfg.vocab), device=device)
+        out_tok = torch.empty((cfg.batch, k + 1), dtype=torch.int32, device=device)
+        accepted = torch.empty((cfg.batch,), dtype=torch.int32, device=device)
+        call = lambda: ml.verify_accept(p, q, tok, u, ws=ws, out_tok=out_tok, accepted=accepted)  # noqa: E731
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call()
+        stream.synchronize()
+        g = graph_of(torch, call, stream)
+        ms = time_replays(torch, g, stream, reps, flush)
+        if ws.status() != 0:
+            raise RuntimeError("device status bits raised in the accept sweep")
+        acc = accepted.cpu().numpy()
+        b = accept_bytes(cfg.batch, cfg.vocab, acc, k)
+        host = tuple(t[:4].cpu().numpy() for t in (p, q, tok, u))
+        OA.verify_accept(*host)
+        secs, rows = 0.0, 0
+        while secs < oracle_seconds:
+            t0 = time.perf_counter()
+            OA.verify_accept(*host)
+            secs += time.perf_counter() - t0
+            rows += 4
+        out["k"][str(k)] = {"us": 1e3 * ms, "rows_per_s": cfg.batch / (ms * 1e-3), "GBps": b / (ms * 1e-3) / 1e9,
+                            "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm_gbs, "algorithmic_bytes": b,
+                            "mean_accepted": float(acc.mean()),
+                            "oracle": {"rows_per_s": rows / secs, "cores": cpu_cores(),
+                                       "sample": f"{rows} requests, float64/integer numpy"}}
+        del p, q, tok, u, ws, g
+        torch.cuda.empty_cache()
     return out
 
 
-def run_e2e(torch, ml, wl, stream, side, args, world):
+def run_e2e(torch, ml, wl, stream, side, steps, world):
     """Host buffers in, host buffers out, through the public binding.  Every
     step copies its activations, adapter indices and probabilities from
     pinned host memory and reads every output back.  The copy-in of step s+1
     runs on a second stream while step s computes (two device input sets,
     each with its own captured graph of the same binding calls); the
     read-back follows each step on the compute stream."""
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    h_x = [(pin(P["xd_h"].view(np.int16)), pin(P["xv_h"].view(np.int16))) for P in wl.proj]
-    p, q, tok, u = wl.acc_h
-    h_acc = [pin(p), pin(q), pin(tok), pin(u)]
-    h_idx = pin(wl.idx_v)
-    h_yd = [torch.empty(tuple(P["yd"].shape), dtype=torch.int16).pin_memory() for P in wl.proj]
-    h_yv = [torch.empty(tuple(P["yv"].shape), dtype=torch.int16).pin_memory() for P in wl.proj]
-    h_out = torch.empty(tuple(wl.out_tok.shape), dtype=torch.int32).pin_memory()
-    h_acc_out = torch.empty(tuple(wl.accepted.shape), dtype=torch.int32).pin_memory()
-    h2d = sum(a.numel() * a.element_size() for pair in h_x for a in pair) + sum(
-        a.numel() * a.element_size() for a in h_acc) + h_idx.numel() * 4
-    d2h = sum(a.numel() * 2 for a in h_yd + h_yv) + h_out.numel() * 4 + h_acc_out.numel() * 4
+    def pin_like(t):
+        return torch.empty(tuple(t.shape), dtype=t.dtype).pin_memory()
 
-    # Two sets of device inputs: the workload's own tensors and a copy.
-    def current():
-        return {"x": [(P["xd"], P["xv"]) for P in wl.proj], "idx": wl.adx_v, "acc": [wl.p, wl.q, wl.tok, wl.u]}
+    def inputs_of():
+        return [x for P in wl.proj for x in P["xd"]] + [P["xv"] for P in wl.proj] + [wl.adx_v, wl.p, wl.q, wl.tok, wl.u]
 
-    def use(st):
-        for P, (xd, xv) in zip(wl.proj, st["x"]):
-            P["xd"], P["xv"] = xd, xv
-        wl.adx_v = st["idx"]
-        wl.p, wl.q, wl.tok, wl.u = st["acc"]
+    def set_inputs(lst):
+        i = 0
+        for P in wl.proj:
+            P["xd"] = lst[i:i + wl.k]
+            i += wl.k
+        for P in wl.proj:
+            P["xv"] = lst[i]
+            i += 1
+        wl.adx_v, wl.p, wl.q, wl.tok, wl.u = lst[i:i + 5]
 
-    set0 = current()
-    set1 = {"x": [(torch.empty_like(xd), torch.empty_like(xv)) for xd, xv in set0["x"]],
-            "idx": torch.empty_like(set0["idx"]), "acc": [torch.empty_like(a) for a in set0["acc"]]}
+    set0 = inputs_of()
+    host_in = [pin_like(t) for t in set0]
+    for h, t in zip(host_in, set0):
+        h.copy_(t)
+    set1 = [torch.empty_like(t) for t in set0]
     sets = (set0, set1)
+    outs = [P["yd"] for P in wl.proj] + [P["yv"] for P in wl.proj] + [wl.out_tok, wl.accepted]
+    host_out = [pin_like(t) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
 
     def copy_in(st):
-        for (xd, xv), (hd, hv) in zip(st["x"], h_x):
-            xd.view(torch.int16).copy_(hd, non_blocking=True)
-            xv.view(torch.int16).copy_(hv, non_blocking=True)
-        st["idx"].copy_(h_idx, non_blocking=True)
-        for d, h in zip(st["acc"], h_acc):
+        for d, h in zip(st, host_in):
             d.copy_(h, non_blocking=True)
 
     def read_back():
-        for P, hd, hv in zip(wl.proj, h_yd, h_yv):
-            hd.copy_(P["yd"].view(torch.int16), non_blocking=True)
-            hv.copy_(P["yv"].view(torch.int16), non_blocking=True)
-        h_out.copy_(wl.out_tok, non_blocking=True)
-        h_acc_out.copy_(wl.accepted, non_blocking=True)
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
 
     graphs = []
     with torch.cuda.stream(stream):
         for st in sets:
-            use(st)
+            set_inputs(st)
             copy_in(st)
             wl.step(side)
             stream.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                wl.step(side)
-            graphs.append(g)
-    use(set0)
+            graphs.append(graph_of(torch, lambda: wl.step(side), stream))
+    set_inputs(set0)
     copy = torch.cuda.Stream(device=wl.p.device)
     ready = [torch.cuda.Event(), torch.cuda.Event()]
     free = [torch.cuda.Event(), torch.cuda.Event()]
@@ -737,7 +769,6 @@ def run_e2e(torch, ml, wl, stream, side, args, world):
             free[cur].record(stream)
             read_back()
 
-    steps = max(3, min(args.steps, 50))
     with torch.cuda.stream(stream):
         run(3)
         stream.synchronize()
@@ -756,11 +787,125 @@ def run_e2e(torch, ml, wl, stream, side, args, world):
             "overlap": "copy-in of step s+1 on a second stream during step s; read-back after each step"}
 
 
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = rank_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    import speculative_lora_decoding_gb300 as ml
+    if not os.path.exists(ml.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    if not ml.device_supported():
+        raise RuntimeError("this benchmark needs a compute capability 10.3 GPU")
+
+    peaks = _peaks()
+    stream = torch.cuda.Stream(device)
+    side = torch.cuda.Stream(device)
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    flush = lambda: flush_buf.fill_(1.0)  # noqa: E731
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- headline workload
+    wl = StepWorkload(torch, ml, device, args.config, seed=rank)
+    head = measure_layer(torch, ml, wl, stream, side, min(args.steps, 200), peaks, flush)
+    # the timed headline run: K replays, clocks sampled meanwhile
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            wl.step(side)
+    stream.synchronize()
+    graph = graph_of(torch, lambda: wl.step(side), stream)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    ms = time_replays(torch, graph, stream, args.steps)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    if wl.ws.status() != 0:
+        raise RuntimeError("device status bits raised during the timed region")
+    ms = max_over_ranks(torch, ms, world, device)
+    value = job_throughput(wl.Mv, world, ms)
+    e2e = run_e2e(torch, ml, wl, stream, side, max(3, min(args.steps, 50)), world)
+    cpu = None
+    if rank == 0 and world == 1:
+        try:
+            cpu = time_oracle(torch, wl, 10.0)
+        except Exception as exc:  # a baseline that fails does not void the GPU number
+            cpu = {"value": None, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": f"failed: {exc}"}
+    head_workload, head_cfg = wl.workload, wl.cfg
+    head_rows = (wl.Md, wl.Mv, [P["name"] for P in wl.proj], wl.k)
+    del wl, graph
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads (rank 0 of a single-GPU run reports them)
+    extra, sweep = {}, None
+    if args.extra == "all" and world == 1:
+        for name in LAYER_RUNS:
+            if name == args.config:
+                continue
+            try:
+                w2 = StepWorkload(torch, ml, device, name, seed=0)
+                r = measure_layer(torch, ml, w2, stream, side, max(20, min(args.steps, 100)), peaks, flush)
+                r["workload"] = w2.workload
+                r["cpu_baseline"] = time_oracle(torch, w2, 3.0, requests=min(4, w2.cfg.n_requests))
+                extra[name] = r
+                del w2
+            except Exception as exc:
+                extra[name] = {"failed": f"{type(exc).__name__}: {exc}"}
+            torch.cuda.empty_cache()
+        try:
+            sweep = measure_accept_sweep(torch, ml, device, stream, 30, peaks, flush, 2.0)
+        except Exception as exc:
+            sweep = {"failed": f"{type(exc).__name__}: {exc}"}
+
+    if rank == 0:
+        Md, Mv, calls, k = head_rows
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": head_workload, "requests": head_cfg.n_requests, "draft_len": k,
+                       "draft_rows_per_pass": Md, "verify_rows": Mv,
+                       "projections": [p[0] for p in head_cfg.projections], "layer_calls": calls,
+                       "parallelism": f"replicas x{world}", "l2": head["l2"],
+                       "graph": "one CUDA graph per step; the plan runs on a second stream beside the draft passes"},
+            "gpu_launches": head["launches_per_step"] * args.steps,
+            "roofline": head["roofline"],
+            "modes": head["modes"],
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                       "samples": clk["samples"]},
+            "configs": extra,
+            "accept_sweep": sweep,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=HEADLINE, choices=sorted(LAYER_RUNS))
+    ap.add_argument("--extra", default="all", choices=["all", "none"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     args = ap.parse_args()
     if args.impl == "reference":

@@ -104,8 +104,10 @@ typedef enum {
 
 /* Bytes of workspace mlora_plan_segments / mlora_shrink / mlora_linear need for
  * M rows, N outputs, K inputs and n_adapters resident adapters, on the
- * current device.  One workspace sized for the largest (M, N, K) of a set of
- * projections serves all of them.  Returns 0 for sizes outside the ranges. */
+ * current device (it grows with M * K: verify mode keeps a copy of the token
+ * rows in adapter-sorted order).  One workspace sized for the largest
+ * (M, N, K) of a set of projections serves all of them.  Returns 0 for sizes
+ * outside the ranges. */
 MLORA_API size_t mlora_linear_workspace_bytes(int M, int N, int K, int n_adapters);
 
 /* Bytes of workspace mlora_linear_sliced needs with n_slices output slices
@@ -232,6 +234,20 @@ MLORA_API mlora_status mlora_linear_sliced(const mlora_bf16 *x, int M, int K, co
  * profiling; the results of a call do not depend on it beyond fp32
  * summation order.  n_adapters and r_max matter in verify mode only. */
 MLORA_API int mlora_linear_gemm_kernel(int M, int N, int K, int n_adapters, int r_max, int mode);
+
+/* Test hook for the failure path of the stream-K GEMM's cross-CTA wait (no
+ * counterpart on the pages).  With ns > 0, every later layer call that runs
+ * the stream-K kernel (see mlora_linear_gemm_kernel) makes the owner of each
+ * split tile wait up to ns nanoseconds on flag words that no CTA sets,
+ * instead of on its contributors' flags: the wait gives up, the tile is
+ * finished without the contributors' partial sums (wrong values) and
+ * MLORA_DEV_TIMEOUT is raised in the workspace status word.  The
+ * contributors' own flags stay set, so the caller must run
+ * mlora_workspace_init before the workspace's next call.  ns = 0 (the default)
+ * restores normal operation.  Process-wide; not for use while other threads
+ * issue layer calls.  Nothing waits on a peer that cannot arrive, so no call
+ * hangs or faults. */
+MLORA_API void mlora_debug_set_flag_wait_ns(uint32_t ns);
 
 /* Allocation-free variant of mlora_linear.  The paper has no counterpart;
  * this is for callers that cannot allocate device memory for a workspace (a

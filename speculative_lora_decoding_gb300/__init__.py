@@ -67,6 +67,7 @@ _SIGNATURES = {
     "mlora_linear_noalloc": (_c_int, [_c_ptr, _c_int, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int,
                                       _c_ptr, _c_ptr, _c_float, _c_int, _c_ptr, _c_ptr]),
     "mlora_linear_gemm_kernel": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "mlora_debug_set_flag_wait_ns": (None, [ctypes.c_uint32]),
     "mlora_status_string": (ctypes.c_char_p, [_c_int]),
     "mlora_device_supported": (_c_int, []),
     "mlora_launch_count": (ctypes.c_uint64, []),

@@ -21,16 +21,18 @@ static int device_sms() {
 static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct LinearLayout {
-  size_t plan, T, tw, sk, total;  // tw == 0: no masked operand; sk == 0: no stream-K scratch
+  size_t plan, T, tw, xs, sk, total;  // tw == 0: no token windows (draft only); sk == 0: no stream-K scratch
 };
 
 // Flag words of the stream-K GEMM: the upper half of the counter array.
 constexpr size_t SK_FLAGS_OFF = WS_COUNTERS_OFF + 4 * (WS_MAX_COUNTERS / 2);
 
-// Workspace of a layer call with n_slices output slices: the plan (at the
-// same offset for every call, so one plan serves all of them), then T and the
-// masked low-rank operand of the tensor-core expand, one of each per slice.
-static LinearLayout linear_layout(int M, int n_ad, int n_slices, int sms) {
+// Workspace of a layer call with n_slices output slices and K inputs: the
+// plan (at the same offset for every call, so one plan serves all of them),
+// then T (fp32, one per slice), the token windows of the tensor-core expand
+// (one buffer per slice) and the token rows in adapter-sorted order, then
+// the stream-K GEMM's partial sums.
+static LinearLayout linear_layout(int M, int K, int n_ad, int n_slices, int sms) {
   LinearLayout L;
   const PlanLayout P = plan_layout(M, n_ad);
   size_t o = WS_SCRATCH_OFF;
@@ -38,11 +40,13 @@ static LinearLayout linear_layout(int M, int n_ad, int n_slices, int sms) {
   o = align_up(o + P.words * 4, 256);
   L.T = o;
   o = align_up(o + (size_t)n_slices * M * T_STRIDE * 4, 256);
-  // Masked operand: one token group of at most 256 rows, loaded by a single MMA.
   L.tw = 0;
-  if (M <= 256 && n_ad > 0) {
+  L.xs = 0;
+  if (n_ad > 0) {
     L.tw = o;
-    o = align_up(o + (size_t)n_slices * max_expand_slices(M, n_ad) * expand_rows(M) * 32, 256);
+    o = align_up(o + (size_t)n_slices * max_window_rows(M, n_ad) * 32, 256);
+    L.xs = o;
+    o = align_up(o + (size_t)M * K * 2, 256);
   }
   // Partial sums of the stream-K GEMM (one tile's worth per SM).
   L.sk = 0;
@@ -54,6 +58,10 @@ static LinearLayout linear_layout(int M, int n_ad, int n_slices, int sms) {
   L.total = o;
   return L;
 }
+
+// Test knob (mlora_debug_set_flag_wait_ns): nonzero makes the stream-K GEMM's
+// tile owners wait that long on flags nothing sets.
+static std::atomic<uint32_t> g_test_flag_wait_ns{0};
 
 // Slice ends: increasing, every one but the last a multiple of 128 (the
 // GEMM's tile height), the last equal to N.
@@ -82,17 +90,14 @@ static mlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLORA
 // its tiles fill at least 80% of the SMs in a single wave: the weights then
 // stream at the full HBM rate and its on-chip reduction is the shortest
 // tail.  Otherwise (a partial last wave, or idle SMs) the persistent
-// stream-K kernel runs, if it can: batches of up to 256 rows in draft mode,
-// and in verify mode when the tensor-core expand is certain to apply (every
-// (adapter, 16-rank block) pair the plan can list fits the budget
-// expand blocks x 32 <= K, and the masked operand exists: M <= 256).
-static bool use_stream_k(int M, int N, int K, int n_ad, int r_max, bool verify, bool have_tw, bool have_sk, int sms,
-                         const GemmShape &gs, SkShape *sk_out) {
+// stream-K kernel runs, if it can: batches of up to 256 rows whose CTAs fit
+// on every SM at once, in verify mode with the token windows.
+static bool use_stream_k(int M, int N, int K, bool verify, bool have_tw, bool have_sk, int sms, const GemmShape &gs,
+                         SkShape *sk_out) {
   const bool cluster_full = gs.waves == 1 && (long long)gs.n_units * gs.C * 5 >= (long long)sms * 4;
   const SkShape sk = sk_shape(M, N, K, sms);
   if (sk_out) *sk_out = sk;
-  const long long max_blocks = (long long)(M < n_ad ? M : n_ad) * ((r_max + 15) / 16);
-  const bool fits = sk.ok && have_sk && (!verify || (have_tw && max_blocks * 32 <= K && max_blocks <= SK_EXPAND_TABLE));
+  const bool fits = sk.ok && have_sk && (!verify || have_tw);
   return fits && !cluster_full;
 }
 
@@ -106,14 +111,14 @@ size_t mlora_linear_workspace_bytes(int M, int N, int K, int n_adapters) {
   if (!linear_sizes_ok(M, N, K, n_adapters)) return 0;
   int sms = device_sms();
   if (sms <= 0) sms = 160;
-  return linear_layout(M, n_adapters, 1, sms).total;
+  return linear_layout(M, K, n_adapters, 1, sms).total;
 }
 
 size_t mlora_linear_sliced_workspace_bytes(int M, int N, int K, int n_adapters, int n_slices) {
   if (!linear_sizes_ok(M, N, K, n_adapters) || n_slices < 1 || n_slices > MLORA_MAX_SLICES) return 0;
   int sms = device_sms();
   if (sms <= 0) sms = 160;
-  return linear_layout(M, n_adapters, n_slices, sms).total;
+  return linear_layout(M, K, n_adapters, n_slices, sms).total;
 }
 
 size_t mlora_accept_workspace_bytes(int B, int k, int V) {
@@ -201,7 +206,7 @@ static mlora_status linear_impl(const mlora_bf16 *x, int M, int K, const mlora_b
   if (sms <= 0) return MLORA_ERR_CUDA;
   const int n_ad = verify ? n_adapters : 0;
   const int S = verify ? n_slices : 1;  // the draft pass is one plain GEMM over all slices
-  const LinearLayout L = linear_layout(M, n_ad, S, sms);
+  const LinearLayout L = linear_layout(M, K, n_ad, S, sms);
   if (ws_bytes < L.total) return MLORA_ERR_WORKSPACE;
 
   cudaStream_t s = (cudaStream_t)stream;
@@ -210,6 +215,7 @@ static mlora_status linear_impl(const mlora_bf16 *x, int M, int K, const mlora_b
   int32_t *plan = reinterpret_cast<int32_t *>(ws + L.plan);
   float *T = reinterpret_cast<float *>(ws + L.T);
   uint16_t *tw = L.tw ? reinterpret_cast<uint16_t *>(ws + L.tw) : nullptr;
+  uint16_t *xs = L.xs ? reinterpret_cast<uint16_t *>(ws + L.xs) : nullptr;
   cudaError_t e;
   if (verify) {
     const PlanLayout P = plan_layout(M, n_ad);
@@ -219,11 +225,15 @@ static mlora_status linear_impl(const mlora_bf16 *x, int M, int K, const mlora_b
     } else if (seg_offsets != plan + P.seg_offsets) {
       return MLORA_ERR_ARG;
     }
+    // Token rows in adapter-sorted order for the GEMM, then T and the
+    // windows of the tensor-core expand.
+    e = launch_gather_rows(x, M, K, plan + P.perm, xs, sms, s);
+    if (e != cudaSuccess) return MLORA_ERR_CUDA;
     e = launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, tw, scale, S, s);
     if (e != cudaSuccess) return MLORA_ERR_CUDA;
   }
   GemmLaunch g;
-  g.x = x;
+  g.x = verify ? xs : x;
   g.W = W;
   g.M = M;
   g.N = N;
@@ -242,10 +252,11 @@ static mlora_status linear_impl(const mlora_bf16 *x, int M, int K, const mlora_b
   g.plan = plan;
   g.status = status;
   g.tw = verify ? tw : nullptr;
+  g.test_flag_wait_ns = g_test_flag_wait_ns.load(std::memory_order_relaxed);
   int err = 0;
   const GemmShape gs = gemm_shape(M, N, K, sms);
   SkShape sk;
-  if (use_stream_k(M, N, K, n_ad, r_max, verify, tw != nullptr, L.sk != 0, sms, gs, &sk)) {
+  if (use_stream_k(M, N, K, verify, tw != nullptr, L.sk != 0, sms, gs, &sk)) {
     e = launch_gemm_sk(g, sk, reinterpret_cast<float *>(ws + L.sk), reinterpret_cast<uint32_t *>(ws + SK_FLAGS_OFF), s,
                        &err);
   } else {
@@ -282,10 +293,12 @@ int mlora_linear_gemm_kernel(int M, int N, int K, int n_adapters, int r_max, int
   if (verify && (n_ad < 1 || r_max < 8 || r_max > MLORA_MAX_RANK || (r_max % 8) != 0)) return -1;
   const int sms = device_sms();
   if (sms <= 0) return -1;
-  const LinearLayout L = linear_layout(M, n_ad, 1, sms);
+  const LinearLayout L = linear_layout(M, K, n_ad, 1, sms);
   const GemmShape gs = gemm_shape(M, N, K, sms);
-  return use_stream_k(M, N, K, n_ad, r_max, verify, L.tw != 0, L.sk != 0, sms, gs, nullptr) ? 1 : 0;
+  return use_stream_k(M, N, K, verify, L.tw != 0, L.sk != 0, sms, gs, nullptr) ? 1 : 0;
 }
+
+void mlora_debug_set_flag_wait_ns(uint32_t ns) { g_test_flag_wait_ns.store(ns, std::memory_order_relaxed); }
 
 mlora_status mlora_verify_accept(const float *p_target, const float *q_draft, const int32_t *draft_tok,
                                  const float *uniforms, int B, int k, int V, int32_t *out_tok, int32_t *accepted,

@@ -27,10 +27,13 @@ constexpr int T_STRIDE = 64;                  // row stride of the internal fp32
 
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Shrink work items: (adapter, block of SHRINK_J rank rows, chunk of SHRINK_TOK rows).
+// Shrink work items: (adapter, block of SHRINK_J rank rows, chunk of SHRINK_TOK
+// rows), one 32-byte record each: {adapter, j0 | nrow << 8 | ntok << 16,
+// sorted position of the first token, first expand block of the adapter},
+// then the four token rows (original row indices).
 constexpr int SHRINK_J = 8;
 constexpr int SHRINK_TOK = 4;
-constexpr int ITEM_WORDS = 8;  // {adapter, j0, nrow, ntok, row0..row3}
+constexpr int ITEM_WORDS = 8;
 
 // Upper bound on shrink items for M rows and n_ad adapters (rank <= 64).
 __host__ __device__ inline size_t max_shrink_items(int M, int n_ad) {
@@ -38,27 +41,44 @@ __host__ __device__ inline size_t max_shrink_items(int M, int n_ad) {
   return (size_t)(64 / SHRINK_J) * ((M + SHRINK_TOK - 1) / SHRINK_TOK + m_ad);
 }
 
-// Upper bound on (adapter, 16-rank slice) pairs: at most min(M, n_ad) active
-// adapters of rank <= 64.
+// Upper bound on expand blocks, (adapter, 16-rank block) pairs: at most
+// min(M, n_ad) active adapters of rank <= 64.
 __host__ __device__ inline int max_expand_slices(int M, int n_ad) { return (M < n_ad ? M : n_ad) * 4; }
 
-// Rows of the masked low-rank operand (tokens padded to 16).
-__host__ __device__ inline int expand_rows(int M) { return (M + 15) / 16 * 16; }
+// Expand blocks and their token windows.  In verify mode the GEMM reads the
+// token rows in adapter-sorted order, so the rows of adapter a occupy the
+// contiguous sorted positions [s0, s1) and, in tensor memory, the
+// accumulator columns of those positions.  The window of a is [w0, w0 + W)
+// with w0 = s0 rounded down and w0 + W = s1 rounded up to 16 (the MMA's
+// column granularity); each of its 16-rank blocks gets its own copy of the
+// window in the low-rank operand buffer, W rows of 16 bf16: scale * T on
+// a's rows, 0 on the rows of the neighbouring adapters the rounding takes
+// in.  A block's record in the plan is EXP_WORDS int32:
+//   {adapter, first rank j0, rank columns in the block (1..16),
+//    first row of its window in the operand buffer, w0, W, 0, 0}.
+constexpr int EXP_WORDS = 8;
+
+// Rows of the operand buffer (per output slice): every active adapter has at
+// most 4 blocks and a window of at most s_a + 30 rows.
+__host__ __device__ inline size_t max_window_rows(int M, int n_ad) {
+  const int m_ad = M < n_ad ? M : n_ad;
+  return (size_t)4 * ((size_t)M + 32 * (size_t)m_ad);
+}
 
 // Plan layout inside scratch (int32 words), for M rows and n_ad adapters.
 struct PlanLayout {
   size_t hdr;         // [0] n_active, [1] shrink items, [2] rows, [3] largest active rank,
-                      // [4] expand slices (adapter, 16-rank block) over the active adapters,
-                      // [5] 1 if every active rank is a multiple of 16 or r_max (16-wide
-                      //     blocks of B then read no padding column inside r_max)
+                      // [4] expand blocks (adapter, 16-rank block) over the active adapters,
+                      // [5] 1 if every active rank is a multiple of 16 or r_max,
+                      // [6] window rows of one slice's operand buffer
   size_t seg_offsets; // [n_ad + 2]
   size_t perm;        // [M]
   size_t row_adapter; // [M]   validated adapter per row (-1: none)
   size_t rank_eff;    // [n_ad] validated ranks
   size_t active;      // [n_ad] adapters with rows, increasing
   size_t item_off;    // [n_ad + 1] prefix of shrink items over the active list
-  size_t slice_off;   // [n_ad] first expand slice of each adapter
-  size_t slices;      // [max_expand_slices][2] (adapter, first rank of the slice)
+  size_t slice_off;   // [n_ad] first expand block of each adapter
+  size_t slices;      // [max_expand_slices][EXP_WORDS] expand block records
   size_t items;       // [max_shrink_items][ITEM_WORDS], 16-byte aligned
   size_t words;       // total int32 words
 };
@@ -74,7 +94,7 @@ __host__ __device__ inline PlanLayout plan_layout(int M, int n_ad) {
   L.active = o;       o += align_up(n_ad, 16);
   L.item_off = o;     o += align_up(n_ad + 1, 16);
   L.slice_off = o;    o += align_up(n_ad, 16);
-  L.slices = o;       o += align_up((size_t)max_expand_slices(M, n_ad) * 2, 16);
+  L.slices = o;       o += align_up((size_t)max_expand_slices(M, n_ad) * EXP_WORDS, 16);
   L.items = o;        o += max_shrink_items(M, n_ad) * ITEM_WORDS;
   L.words = o;
   return L;

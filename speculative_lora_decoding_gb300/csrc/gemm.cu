@@ -20,12 +20,14 @@
 //    memory: each CTA sums rows [rank*128/C, (rank+1)*128/C) over all C CTAs
 //    in rank order.  The reduction stays on chip, runs on all C CTAs at once
 //    and is deterministic.
-//  * The expand, when its (adapter, 16-rank block) pairs are few against K:
-//    one MMA per block, B_a[n0:n0+128, block] x Tmask_block^T, added to the
-//    accumulator after the K loop, the blocks shared out over the cluster's
-//    CTAs, four per ring stage; Tmask holds scale * T on the adapter's rows
-//    and 0 elsewhere (written by the shrink).  Otherwise the epilogue walks
-//    the plan's adapter buckets on the CUDA cores.
+//  * The verify expand (expand.cuh): the token rows come in adapter-sorted
+//    order (x_sorted), so each adapter's rows are adjacent accumulator
+//    columns; after the K loop one MMA per (adapter, 16-rank block) adds
+//    B_a[n0:n0+128, block] x Twin^T over the adapter's token window only,
+//    the blocks shared out over the cluster's CTAs, and the epilogue stores
+//    column c to row perm[c].  Without the sorted rows (the allocation-free
+//    entry point) the epilogue walks the plan's adapter buckets on the CUDA
+//    cores instead.
 //  * Warp roles: warp 0 issues TMA loads of W and x tiles (128-byte swizzle)
 //    into a ring of shared-memory stages; warp 1 owns tensor memory and issues
 //    tcgen05.mma from one thread; warps 2..5 drain the accumulator with
@@ -39,6 +41,7 @@
 //    MLORA_DEV_TIMEOUT, drains its own copies and MMAs, still takes part in
 //    every cluster barrier, frees its tensor memory and returns.
 #include "common.cuh"
+#include "expand.cuh"
 #include "launch.h"
 
 namespace mlora {
@@ -52,26 +55,22 @@ constexpr int CHUNK = 32;                             // accumulator columns per
 constexpr int RED_BYTES = 2 * CHUNK * BLOCK_N * 4;    // double-buffered reduction tile, 32 KB
 constexpr int MAX_CLUSTER = 16;
 constexpr size_t SMEM_LIMIT = 220 * 1024;             // leaves room for a co-resident shrink CTA
-constexpr int EXPAND_TABLE = 256;                     // expand blocks staged in shared memory
-// Expand blocks per ring stage: a block takes 128 x 16 bf16 of B (4 KB) and
-// Mb x 16 of the masked operand (Mb * 32 B), and 4 * (4096 + 32 Mb) is
-// exactly a stage (16 KB of W + Mb x 64 of x), so four share one stage.
-constexpr int EXPAND_PER_STAGE = 4;
-constexpr size_t SMEM_FIXED = 1024 + 256 + EXPAND_TABLE * 8;  // alignment slack, barriers, expand table
+constexpr int MAX_STAGES = 8;
+constexpr size_t SMEM_FIXED = 1024 + 256 + expand_smem_bytes(MAX_STAGES);  // alignment slack, barriers, expand records
 
 struct GemmArgs {
   int M, N, K;
   int Mb, nsub, sub_n, n_tgroups, kblocks, C, stages, tmem_cols, red_bytes;
   int mode, prefetch_w;
   int after_shrink;  // launched right after this library's shrink kernel: x and W are ready
-  int use_tw, Mpad;  // tensor-core expand allowed (masked operand present), its token rows
-  int n_slices;      // output slices: tile rows [slice_end[s-1], slice_end[s]) use T and masked operand s
+  int sorted;        // verify mode with x in adapter-sorted order and the token windows (tensor-core expand)
+  int n_slices;      // output slices: tile rows [slice_end[s-1], slice_end[s]) use T and windows of slice s
   int slice_end[MLORA_MAX_SLICES];
-  int tw_slice_rows; // rows of one slice's masked operand (expand slices x Mpad)
+  size_t tw_slice;   // bf16 elements of one slice's window buffer
   float scale;
   uint16_t *y;
   const uint16_t *B_stack;
-  const uint16_t *tw;  // masked expand operand, rows already in the 32-byte-swizzled layout
+  const uint16_t *tw;  // token windows of the expand blocks, rows in the 32-byte-swizzled order
   int r_max, n_ad;
   const float *T;  // [n_slices][M][T_STRIDE]
   const int32_t *plan;
@@ -91,19 +90,23 @@ __device__ __forceinline__ int slice_of(const GemmArgs &a, int n0) {
 struct SmemPtrs {
   uint8_t *stage0;
   float *red;
+  ExpandStage *meta;  // [stages] what an expand stage holds
+  int4 *chunk;        // [EXP_CHUNK] the producer's staged plan records
   uint64_t *full, *empty, *tfull, *drain;
   uint32_t *tmem_slot;
   int *abort_flag;
   int *acc_ready;
   int *zero_word;  // stays 0: for waits that only a time limit may end
-  int2 *exp_tab;   // [EXPAND_TABLE] (adapter, first rank) of each expand block
 };
 
 __device__ __forceinline__ SmemPtrs carve_smem(uint8_t *base, int stages, int stage_bytes, int red_bytes) {
   SmemPtrs p;
   p.stage0 = base;
   p.red = reinterpret_cast<float *>(base + (size_t)stages * stage_bytes);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(base + (size_t)stages * stage_bytes + red_bytes);
+  uint8_t *after = base + (size_t)stages * stage_bytes + red_bytes;
+  p.meta = reinterpret_cast<ExpandStage *>(after);
+  p.chunk = reinterpret_cast<int4 *>(after + (size_t)stages * sizeof(ExpandStage));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(after + expand_smem_bytes(stages));
   p.full = bars;
   p.empty = bars + stages;
   p.tfull = bars + 2 * stages;
@@ -113,7 +116,6 @@ __device__ __forceinline__ SmemPtrs carve_smem(uint8_t *base, int stages, int st
   p.abort_flag = reinterpret_cast<int *>(w + 1);
   p.acc_ready = reinterpret_cast<int *>(w + 2);
   p.zero_word = reinterpret_cast<int *>(w + 3);
-  p.exp_tab = reinterpret_cast<int2 *>(w + 4);
   return p;
 }
 
@@ -351,21 +353,11 @@ __device__ __forceinline__ void verify_walk(const GemmArgs &a, const PlanLayout 
   }
 }
 
-// Tensor-core expand: after the base K loop, one MMA per (adapter, 16-rank
-// slice) adds B_a[n0:n0+128, slice] x Tmask[:, slice]^T, where Tmask holds
-// scale * T for the adapter's own rows and 0 elsewhere (written by the
-// shrink kernel).  Used up to slices * 16 <= K / 2 (a quarter of the
-// base GEMM's MMA work; measured, the bucket walk below costs 3.5-4.7x the
-// base GEMM at 64 slices, far more than these MMAs), and while every active rank
-// is a multiple of 16 or r_max: a 16-wide block of B columns must not reach
-// the caller's padding inside r_max (it may hold NaN, and NaN * 0 is NaN).
-// Otherwise the epilogue bucket walk adds the low-rank term on the CUDA
-// cores, masking per element.
-__device__ __forceinline__ int expand_slices_tc(const GemmArgs &a, const PlanLayout &L) {
-  if (!a.use_tw || a.mode != MLORA_VERIFY) return -1;
-  if (a.plan[L.hdr + 5] != 1) return -1;
-  const int ns = a.plan[L.hdr + 4];
-  return (ns * 32 <= a.K && ns <= EXPAND_TABLE) ? ns : -1;
+// Expand blocks of the tensor-core expand (verify mode with sorted rows), or
+// -1 when the epilogue's bucket walk adds the low-rank term instead.
+__device__ __forceinline__ int expand_blocks(const GemmArgs &a, const PlanLayout &L) {
+  if (!a.sorted || a.mode != MLORA_VERIFY) return -1;
+  return a.plan[L.hdr + 4];
 }
 
 // Split-K reduction through distributed shared memory: sums rows [r0, r0 + R)
@@ -486,7 +478,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_w);
     tma_prefetch_desc(&tmap_x);
-    if (args.use_tw) tma_prefetch_desc(&tmap_b);
+    if (args.sorted) tma_prefetch_desc(&tmap_b);
   }
   if (warp == 1) {
     tmem_alloc(sp.tmem_slot, args.tmem_cols);
@@ -498,10 +490,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
   const uint32_t tmem_base = *sp.tmem_slot;
   volatile int *abort_flag = sp.abort_flag;
 
+  // Expand blocks of this CTA, read from the plan after griddepcontrol.wait:
+  // the cluster's CTAs share them out (the reduction adds every CTA's
+  // accumulator, so any CTA may add any block), CTA `rank` taking blocks
+  // [rank*ns/C, (rank+1)*ns/C).
+  const PlanLayout L = plan_layout(args.M, args.n_ad);
+  const bool sorted_verify = args.sorted && args.mode == MLORA_VERIFY;
+  auto expand_range = [&](int &blo, int &bhi) {
+    const int ns = expand_blocks(args, L);
+    blo = ns > 0 ? (int)((long long)rank * ns / C) : 0;
+    bhi = ns > 0 ? (int)((long long)(rank + 1) * ns / C) : 0;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    int stage = 0, issued = 0, early = 0;
+    uint32_t phase = 0;
+    const uint64_t pol_w = policy_evict_first();
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       const int nkb = kb_hi - kb_lo;
       // Loop constants in registers (the copies below are asm with memory
@@ -512,18 +518,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
       const uint32_t tx_bytes = (uint32_t)stage_bytes;
       // With static weights, the first ring of W tiles is requested before the
       // wait for the preceding kernel; x always comes after it.
-      const int early = (args.prefetch_w && !args.after_shrink) ? min(nkb, S) : 0;
+      early = (args.prefetch_w && !args.after_shrink) ? min(nkb, S) : 0;
       for (int i = 0; i < early; ++i) {
         mbar_arrive_expect_tx(&sp.full[i], tx_bytes);
         tma_load_2d(sp.stage0 + (size_t)i * stage_bytes, &tmap_w, &sp.full[i], (kb_lo + i) * BLOCK_K, w_row, pol_w);
       }
       // After this library's shrink kernel nothing the mainloop reads can
       // still be in flight (the shrink released this grid only after its own
-      // predecessor had finished), so only the epilogue waits for T.
+      // predecessor had finished), so only the expand and the epilogue wait
+      // for the shrink's output.
       if (!args.after_shrink) grid_dependency_wait();
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
       for (int i = 0; i < nkb; ++i) {
         const int kb = kb_lo + i;
         uint8_t *st = sp.stage0 + (size_t)stage * stage_bytes;
@@ -543,71 +547,41 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
           phase ^= 1u;
         }
       }
-      const PlanLayout Lp = plan_layout(args.M, args.n_ad);
-      // The expand blocks are shared out over the cluster's C CTAs (the
-      // reduction adds every CTA's accumulator, so any CTA may add any
-      // block): CTA `rank` takes blocks [rank*ns/C, (rank+1)*ns/C).
-      const int ns = !*abort_flag ? expand_slices_tc(args, Lp) : -1;
-      const int blo = ns > 0 ? (int)((long long)rank * ns / C) : 0;
-      const int bhi = ns > 0 ? (int)((long long)(rank + 1) * ns / C) : 0;
-      if (bhi > blo) {
-        grid_dependency_wait();  // the masked operand comes from the shrink kernel just before
-        // This CTA's part of the expand list comes from the plan 16 entries
-        // per round of independent loads into a shared-memory table, so the
-        // stage loop waits on no global load.
-        for (int b0 = blo; b0 < bhi; b0 += 16) {
-          int ad_b[16], j0_b[16];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            ad_b[u] = b0 + u < bhi ? args.plan[Lp.slices + 2 * (b0 + u)] : 0;
-            j0_b[u] = b0 + u < bhi ? args.plan[Lp.slices + 2 * (b0 + u) + 1] : 0;
-          }
-#pragma unroll
-          for (int u = 0; u < 16; ++u)
-            if (b0 + u < bhi) sp.exp_tab[b0 + u] = make_int2(ad_b[u], j0_b[u]);
-        }
-        // Four blocks per stage: B tiles at 4 KB steps, then the masked
-        // operand tiles at Mb * 32 B steps.
-        for (int sl0 = blo; sl0 < bhi; sl0 += EXPAND_PER_STAGE) {
-          const int gn = min(EXPAND_PER_STAGE, bhi - sl0);
-          if (!mbar_wait_bounded(&sp.empty[stage], phase ^ 1u, abort_flag)) {
-            signal_abort(sp, args.status);
-            break;
-          }
-          uint8_t *st = sp.stage0 + (size_t)stage * stage_bytes;
-          mbar_arrive_expect_tx(&sp.full[stage], (uint32_t)(gn * (BLOCK_N * 32 + args.sub_n * 32)));
-          for (int g = 0; g < gn; ++g) {
-            const int2 e = sp.exp_tab[sl0 + g];
-            tma_load_2d(st + g * BLOCK_N * 32, &tmap_b, &sp.full[stage], e.y, e.x * args.N + n_tile * BLOCK_N, pol_w);
-          }
-          // The blocks' masked-operand tiles are consecutive (one token
-          // group: Mpad == Mb rows each, m0 == 0): one bulk copy.
-          bulk_load(st + EXPAND_PER_STAGE * BLOCK_N * 32,
-                    args.tw + ((size_t)slice * args.tw_slice_rows + (size_t)sl0 * args.Mpad) * 16,
-                    (uint32_t)(gn * args.Mpad * 32), &sp.full[stage]);
-          ++issued;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
+    }
+    stage = __shfl_sync(0xffffffffu, stage, 0);
+    phase = __shfl_sync(0xffffffffu, phase, 0);
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    early = __shfl_sync(0xffffffffu, early, 0);
+    __syncwarp();
+    int blo = 0, bhi = 0;
+    if (sorted_verify && !*abort_flag) {
+      grid_dependency_wait();  // the plan and the token windows come from the kernels just before
+      expand_range(blo, bhi);
+    }
+    if (bhi > blo) {
+      const bool ok = expand_produce(args.plan + L.slices, blo, bhi, m0, args.Mb, n_tile * BLOCK_N, args.N, &tmap_b,
+                                     args.tw + (size_t)slice * args.tw_slice, sp.stage0, stage_bytes, S, sp.full,
+                                     sp.empty, sp.meta, sp.chunk, stage, phase, issued, abort_flag, pol_w, lane);
+      if (!ok && lane == 0) signal_abort(sp, args.status);
+    }
+    if (lane == 0 && *abort_flag) {
+      // Let this CTA's own copies land before shared memory goes away.
+      const int n = issued < S ? issued : S;
+      for (int i = issued - n; i < issued; ++i) {
+        mbar_wait_bounded(&sp.full[i % S], (uint32_t)((i / S) & 1), sp.zero_word);
       }
-      if (*abort_flag) {
-        // Let this CTA's own copies land before shared memory goes away.
-        const int n = issued < S ? issued : S;
-        for (int i = issued - n; i < issued; ++i) {
-          mbar_wait_bounded(&sp.full[i % S], (uint32_t)((i / S) & 1), sp.zero_word);
-        }
-        if (early > issued) {
-          for (int i = issued; i < early; ++i) {
-            mbar_wait_bounded(&sp.full[i], 0u, sp.zero_word);  // W half only: never completes, bounded
-          }
+      if (early > issued) {
+        for (int i = issued; i < early; ++i) {
+          mbar_wait_bounded(&sp.full[i], 0u, sp.zero_word);  // W half only: never completes, bounded
         }
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    bool mma_ok = false;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true, issued_any = false;
     if (lane == 0) {
       // Everything the loop needs is in registers before it starts: this one
       // thread issues every MMA of the CTA, so the issue path is kept to a
@@ -620,9 +594,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
       const uint32_t ring0 = smem_addr(sp.stage0);
       const uint32_t sbytes = (uint32_t)stage_bytes;
       const int k_lo = kb_lo, k_hi = kb_hi;
-      int stage = 0;
-      uint32_t phase = 0;
-      bool issued_any = false, ok = true;
       for (int kb = k_lo; kb < k_hi; ++kb) {
         if (!mbar_wait_bounded(&sp.full[stage], phase, abort_flag)) {
           signal_abort(sp, args.status);
@@ -647,28 +618,29 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
           phase ^= 1u;
         }
       }
-      const PlanLayout Lm = plan_layout(args.M, args.n_ad);
-      const int ns = ok ? expand_slices_tc(args, Lm) : -1;
-      const int blo = ns > 0 ? (int)((long long)rank * ns / C) : 0;
-      const int bhi = ns > 0 ? (int)((long long)(rank + 1) * ns / C) : 0;
-      for (int sl0 = blo; sl0 < bhi; sl0 += EXPAND_PER_STAGE) {
-        const int gn = min(EXPAND_PER_STAGE, bhi - sl0);
-        if (!mbar_wait_bounded(&sp.full[stage], phase, abort_flag)) {
-          signal_abort(sp, args.status);
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t a_addr = smem_addr(sp.stage0 + (size_t)stage * stage_bytes);
-        for (int g = 0; g < gn; ++g)
-          mma_bf16_ss(tmem_base, smem_desc_kmajor_sw32(a_addr + g * BLOCK_N * 32),
-                      smem_desc_kmajor_sw32(a_addr + EXPAND_PER_STAGE * BLOCK_N * 32 + g * args.sub_n * 32), idesc, 1u);
-        mma_commit(&sp.empty[stage]);
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    issued_any = __shfl_sync(0xffffffffu, issued_any ? 1 : 0, 0) != 0;
+    stage = __shfl_sync(0xffffffffu, stage, 0);
+    phase = __shfl_sync(0xffffffffu, phase, 0);
+    __syncwarp();
+    int blo = 0, bhi = 0;
+    if (sorted_verify) {
+      grid_dependency_wait();  // the plan comes from a kernel earlier in the stream
+      expand_range(blo, bhi);
+    }
+    if (ok && bhi > blo && !*abort_flag) {
+      // The producer issues at least one expand stage whenever bhi > blo
+      // and it has not given up.
+      ok = expand_consume(sp.stage0, stage_bytes, S, sp.full, sp.empty, sp.meta, tmem_base, stage, phase, abort_flag,
+                          lane);
+      if (!ok && lane == 0) signal_abort(sp, args.status);
+      issued_any = true;
+    } else if (ok && bhi > blo) {
+      ok = false;  // the producer gave up before the expand
+    }
+    bool mma_ok = false;
+    if (lane == 0) {
       if (ok) {
         mma_commit(sp.tfull);
       } else if (issued_any) {
@@ -699,21 +671,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
   const bool epi = warp >= 2;
   const int quad = warp & 3;
   const int et = threadIdx.x - 64;
-  const PlanLayout L = plan_layout(args.M, args.n_ad);
   bool have_acc = false;
-  bool expand_done = false;  // the low-rank term is already in the accumulator
   if (epi) {
     named_bar_sync(2, 160);  // released by the MMA warp once the accumulator is complete
     tc_fence_after_sync();
     have_acc = *reinterpret_cast<volatile int *>(sp.acc_ready) != 0;
     grid_dependency_wait();  // the plan and T come from kernels earlier in the stream
-    expand_done = expand_slices_tc(args, L) >= 0;
   }
   const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
   const int nchunks = (mcount + CHUNK - 1) / CHUNK;
 
   // Verify work left for the epilogue: none once the tensor cores added it.
-  const bool verify = args.mode == MLORA_VERIFY && !expand_done;
+  const bool verify = args.mode == MLORA_VERIFY && !args.sorted;
+  // Output row of accumulator column c: with sorted rows, perm[m0 + c].
+  const int32_t *perm = args.sorted ? args.plan + L.perm : nullptr;
+  auto out_row = [&](int c) -> size_t { return perm ? (size_t)__ldg(perm + m0 + c) : (size_t)(m0 + c); };
 
   if (C == 1) {
     if (epi && have_acc) {
@@ -722,12 +694,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
         for (int ch = 0; ch < nchunks; ++ch) {
           uint32_t r[32];
           tmem_ld_acc_x32(taddr + ch * CHUNK, r);
-          if (n < args.N) {
+          // Lane j holds the output row of column ch * 32 + j.
+          const int myc = ch * CHUNK + lane;
+          const int myrow = myc < mcount ? (int)out_row(myc) : 0;
 #pragma unroll
-            for (int j = 0; j < CHUNK; ++j) {
-              const int col = ch * CHUNK + j;
-              if (col < mcount) args.y[(size_t)(m0 + col) * args.N + n] = float_to_bf16_bits(__uint_as_float(r[j]));
-            }
+          for (int j = 0; j < CHUNK; ++j) {
+            const int col = ch * CHUNK + j;
+            const int row = __shfl_sync(0xffffffffu, myrow, j);
+            if (n < args.N && col < mcount) args.y[(size_t)row * args.N + n] = float_to_bf16_bits(__uint_as_float(r[j]));
           }
         }
       } else {
@@ -775,7 +749,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
       cluster_sync_all();
       if (epi)
         cluster_reduce_rows_c(C, peer, 0u, r0, R, mcount, et, [&](int c, int i, float4 v) {
-          store_bf16x4(args.y, args.N, (size_t)(m0 + c), n_tile * BLOCK_N + r0 + i, v);
+          store_bf16x4(args.y, args.N, out_row(c), n_tile * BLOCK_N + r0 + i, v);
         });
     } else {
       const uint32_t red_local = smem_addr(sp.red);
@@ -805,7 +779,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
                                   if (verify) {
                                     *reinterpret_cast<float4 *>(&fin[col * R + i]) = v;
                                   } else {
-                                    store_bf16x4(args.y, args.N, (size_t)(m0 + col), n_tile * BLOCK_N + r0 + i, v);
+                                    store_bf16x4(args.y, args.N, out_row(col), n_tile * BLOCK_N + r0 + i, v);
                                   }
                                 });
         }
@@ -847,7 +821,7 @@ static size_t smem_for(int Mb, int stages, int red_bytes) {
 static int stages_for(int Mb, int red_bytes) {
   const int stage_bytes = W_TILE_BYTES + Mb * BLOCK_K * 2;
   int s = (int)((SMEM_LIMIT - SMEM_FIXED - red_bytes) / stage_bytes);
-  return s > 8 ? 8 : s;
+  return s > MAX_STAGES ? MAX_STAGES : s;
 }
 
 // Clusters of size C that can be resident at once (one CTA per SM).
@@ -999,10 +973,11 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
     *err_code = 1;
     return cudaErrorInvalidValue;
   }
-  // The tensor-core expand needs one token group loaded by one MMA.
-  const int use_tw = (g.mode == MLORA_VERIFY && g.tw != nullptr && sh.nsub == 1 && sh.n_tgroups == 1) ? 1 : 0;
+  // Verify mode with the token windows: x is in adapter-sorted order and the
+  // tensor cores add the low-rank term.
+  const int sorted = (g.mode == MLORA_VERIFY && g.tw != nullptr) ? 1 : 0;
   tb = tw;
-  if (use_tw) {
+  if (sorted) {
     if (!make_map(&tb, g.B_stack, (long long)g.n_ad * g.N, g.r_max, BLOCK_N, 16)) {
       *err_code = 1;
       return cudaErrorInvalidValue;
@@ -1025,11 +1000,10 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
   a.mode = g.mode;
   a.prefetch_w = g.prefetch_w;
   a.after_shrink = g.after_shrink;
-  a.use_tw = use_tw;
-  a.Mpad = expand_rows(g.M);
+  a.sorted = sorted;
   a.n_slices = g.n_slices;
   for (int i = 0; i < MLORA_MAX_SLICES; ++i) a.slice_end[i] = i < g.n_slices ? g.slice_end[i] : g.N;
-  a.tw_slice_rows = max_expand_slices(g.M, g.n_ad) * expand_rows(g.M);
+  a.tw_slice = max_window_rows(g.M, g.n_ad) * 16;
   a.scale = g.scale;
   a.y = g.y;
   a.B_stack = g.B_stack;

@@ -3,11 +3,14 @@
 // (verify mode), for batches of up to 256 token rows:
 //
 //   draft  (LoRA off): y[m, n] = bf16(acc[m, n])
-//   verify (LoRA on):  y[m, n] = bf16(acc[m, n] + sum_s B_a[n, slice s] . Tmask_s[m, :])
+//   verify (LoRA on):  y[perm[c], n] = bf16(acc[c, n] + sum_blocks B_a[n, block] . Twin[c, :])
 //
-// where Tmask_s holds scale * T on the rows of adapter a and 0 elsewhere
-// ("output = W·x + scale · B(A·x)", "Multi-LoRA Serving in Practice", section
-// "Core Principle: Shared Base Model, Per-Request Adapter Selection").
+// In verify mode the token rows come in adapter-sorted order (column c is row
+// perm[c]) and each expand block (adapter a, 16-rank block) adds its MMA over
+// a's token window only (expand.cuh), where the window holds scale * T on a's
+// rows and 0 elsewhere ("output = W·x + scale · B(A·x)", "Multi-LoRA Serving
+// in Practice", section "Core Principle: Shared Base Model, Per-Request
+// Adapter Selection").
 //
 // Work split.  The (tile of 128 W rows, 64-wide k-block) pairs are laid out
 // tile by tile and cut into one contiguous, equal share per CTA, one CTA per
@@ -22,6 +25,11 @@
 // are resident at once, so the waits always end; every wait is bounded
 // nevertheless.  Partials are added in CTA order: results are deterministic.
 //
+// Residency: the waits above end only if every CTA of the grid is resident at
+// once.  The host launches one CTA per SM only when the occupancy query says
+// a CTA fits on every SM; each wait is bounded in any case, and a wait that
+// gives up raises MLORA_DEV_TIMEOUT.
+//
 // Warp roles: warp 0 issues the TMA loads of W and x tiles (128-byte swizzle)
 // and of the expand operands into a ring of stages that runs across segment
 // boundaries; warp 1 owns tensor memory, issues tcgen05.mma from one thread
@@ -29,6 +37,7 @@
 // adapter's rank in shared memory before an expand MMA reads them; warps 2..5
 // drain one accumulator while the MMAs fill the other.
 #include "common.cuh"
+#include "expand.cuh"
 #include "launch.h"
 
 namespace mlora {
@@ -39,22 +48,21 @@ constexpr int SK_BK = 64;                        // K per stage: 128 bytes of bf
 constexpr int SK_WTILE = SK_BN * SK_BK * 2;      // 16 KB
 constexpr int SK_CHUNK = 32;                     // accumulator columns per tensor-memory load
 constexpr size_t SK_SMEM_LIMIT = 220 * 1024;     // leaves room for a co-resident shrink CTA
-constexpr size_t SK_SMEM_FIXED = 1024 + 256 + SK_EXPAND_TABLE * 16;  // alignment slack, barriers, expand table
+constexpr int SK_MAX_STAGES = 8;
+constexpr size_t SK_SMEM_FIXED = 1024 + 256 + expand_smem_bytes(SK_MAX_STAGES);  // alignment slack, barriers, expand records
 constexpr int SK_MIN_SHARE = 8;                  // k-blocks per CTA at least
 constexpr int SK_MAX_PARTIALS = 8;               // contributors per tile besides its owner, at most
 constexpr int SK_MAX_ROWS = 256;                 // token rows: two accumulators fit in tensor memory
-// Expand blocks per ring stage: a block takes 128 x 16 bf16 of B (4 KB) and
-// Mb x 16 of the masked operand (Mb * 32 B); 4 * (4096 + 32 Mb) is exactly a
-// stage (16 KB of W + Mb x 64 of x).
-constexpr int SK_EXPAND_PER_STAGE = 4;
-
 struct SkArgs {
   int M, N, K, Mb, kblocks, total, P, stages, cols;
-  int mode, prefetch_w, after_shrink, use_tw, Mpad;
-  int n_slices, slice_end[MLORA_MAX_SLICES], tw_slice_rows;
+  int mode, prefetch_w, after_shrink;
+  int sorted;  // verify mode: x in adapter-sorted order, token windows present
+  int n_slices, slice_end[MLORA_MAX_SLICES];
+  size_t tw_slice;  // bf16 elements of one slice's window buffer
   int n_ad;
+  uint32_t test_flag_wait_ns;  // nonzero: owners poll never-set flags for this long (a test of the timeout path)
   uint16_t *y;
-  const uint16_t *tw;  // masked expand operand, rows already in the 32-byte-swizzled layout
+  const uint16_t *tw;  // token windows of the expand blocks, rows in the 32-byte-swizzled order
   const int32_t *plan;
   uint32_t *status;
   float *partials;  // [P][Mb][128]: a contributor's partial sums, token-major
@@ -79,22 +87,6 @@ __device__ __forceinline__ int sk_slice_of(const SkArgs &a, int n0) {
   return s;
 }
 
-// Zero logical columns [c0, 16) of a 128-row x 16-column bf16 tile written by
-// TMA with 32-byte swizzling (row i at byte 32 i; its two 16-byte halves are
-// swapped when bit 2 of i is set).  Each lane of the warp takes 4 rows.
-__device__ __forceinline__ void zero_tail_columns_sw32(uint8_t *tile, int c0, int lane) {
-#pragma unroll 1
-  for (int q = 0; q < 4; ++q) {
-    const int i = lane * 4 + q;
-    uint8_t *row = tile + i * 32;
-    const int flip = (i >> 2) & 1;
-    for (int c = c0; c < 16; ++c) {
-      const int chunk = (c >> 3) ^ flip;
-      *reinterpret_cast<uint16_t *>(row + chunk * 16 + (c & 7) * 2) = 0;
-    }
-  }
-}
-
 __global__ void __launch_bounds__(SK_THREADS, 1)
     gemm_sk_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_b, const SkArgs args) {
@@ -102,10 +94,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   uint8_t *ring = align_smem_1024(smem_raw);
   const int S = args.stages;
   const int stage_bytes = SK_WTILE + args.Mb * SK_BK * 2;
-  // Expand table: (adapter, first rank, rank columns in the block) per
-  // (adapter, 16-rank block), filled once by the producer from the plan.
-  int4 *exp_tab = reinterpret_cast<int4 *>(ring + (size_t)S * stage_bytes);
-  uint64_t *full = reinterpret_cast<uint64_t *>(exp_tab + SK_EXPAND_TABLE);
+  // Expand records (one per stage) and the producer's staged plan records.
+  ExpandStage *meta = reinterpret_cast<ExpandStage *>(ring + (size_t)S * stage_bytes);
+  int4 *chunk = reinterpret_cast<int4 *>(meta + S);
+  uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)S * stage_bytes + expand_smem_bytes(S));
   uint64_t *empty = full + S;
   uint64_t *acc_full = empty + S;     // [2]: MMA commit -> epilogue
   uint64_t *acc_empty = acc_full + 2; // [2]: epilogue warps -> MMA issuer
@@ -120,7 +112,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   const int cta = blockIdx.x;
   const int KB = args.kblocks;
   const int g0 = sk_begin(args, cta), g1 = sk_begin(args, cta + 1);
-  const bool tc = args.use_tw != 0 && args.mode == MLORA_VERIFY;
+  const bool tc = args.sorted != 0 && args.mode == MLORA_VERIFY;
   const PlanLayout L = plan_layout(args.M, args.n_ad);
 
   if (threadIdx.x == 0) {
@@ -158,15 +150,20 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Lane 0 issues the k-blocks; at an owned tile's expand point the whole
+    // warp stages the plan's expand records (expand_produce).  Every lane
+    // keeps the same ring position.
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_x = policy_evict_last();
+    const uint32_t tx = (uint32_t)stage_bytes;
+    int stage = 0, issued = 0, i = 0, early = 0, ns = -1;
+    uint32_t phase = 0;
+    bool ok = true;
+    bool waited = !args.after_shrink;
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_x = policy_evict_last();
-      const uint32_t tx = (uint32_t)stage_bytes;
-      const uint32_t tx_expand = (uint32_t)(SK_BN * 32 + args.Mb * 32);
       // With static weights the first ring of W tiles is requested before the
       // wait for the preceding kernel; x always comes after it.  (Not with the
       // expand: its operands would take ring stages between those k-blocks.)
-      int early = 0;
       if (args.prefetch_w && !args.after_shrink && !tc) {
         for (int g = g0; g < g1 && early < S; ++g, ++early) {
           const int t = g / KB, kb = g - t * KB;
@@ -174,88 +171,62 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
           tma_load_2d(ring + (size_t)early * stage_bytes, &tmap_w, &full[early], kb * SK_BK, t * SK_BN, pol_w);
         }
       }
-      bool waited = !args.after_shrink;
       if (waited) grid_dependency_wait();
-      int stage = 0, issued = 0, i = 0, ns = -1;
-      uint32_t phase = 0;
-      bool ok = true;
-      // The expand blocks of an owned tile (verify mode): their operands go
-      // into the ring before the tile's last S k-blocks, so that they land
-      // while those stream instead of after the whole tile.
-      auto issue_expand = [&](int t) -> bool {
-        if (!waited) {
-          grid_dependency_wait();  // the masked operand comes from the shrink kernel just before
-          waited = true;
-        }
-        if (ns < 0) {
-          // The plan's expand list into shared memory, 16 entries per
-          // round of independent loads: the loops below then wait on no
-          // global load per block.  The MMA warp reads the table after its
-          // wait on the first expand stage, which this thread's arrival
-          // (release) on that stage orders after these stores.
-          ns = min(args.plan[L.hdr + 4], SK_EXPAND_TABLE);
-          for (int b0 = 0; b0 < ns; b0 += 16) {
-            int ad[16], j0[16], rk[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              ad[u] = b0 + u < ns ? args.plan[L.slices + 2 * (b0 + u)] : 0;
-              j0[u] = b0 + u < ns ? args.plan[L.slices + 2 * (b0 + u) + 1] : 0;
-            }
-#pragma unroll
-            for (int u = 0; u < 16; ++u) rk[u] = b0 + u < ns ? args.plan[L.rank_eff + ad[u]] : 0;
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-              if (b0 + u < ns) exp_tab[b0 + u] = make_int4(ad[u], j0[u], rk[u] - j0[u], 0);
-          }
-        }
-        const int row0 = sk_slice_of(args, t * SK_BN) * args.tw_slice_rows;
-        for (int sl0 = 0; sl0 < ns; sl0 += SK_EXPAND_PER_STAGE) {
-          const int gn = min(SK_EXPAND_PER_STAGE, ns - sl0);
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, ab)) return false;
-          uint8_t *st = ring + (size_t)stage * stage_bytes;
-          mbar_arrive_expect_tx(&full[stage], tx_expand * (uint32_t)gn);
-          for (int g = 0; g < gn; ++g) {
-            const int4 e = exp_tab[sl0 + g];
-            tma_load_2d(st + g * SK_BN * 32, &tmap_b, &full[stage], e.y, e.x * args.N + t * SK_BN, pol_w);
-          }
-          // The blocks' masked-operand tiles are consecutive (Mpad == Mb
-          // rows each): one bulk copy brings all of them.
-          bulk_load(st + SK_EXPAND_PER_STAGE * SK_BN * 32, args.tw + ((size_t)row0 + (size_t)sl0 * args.Mpad) * 16,
-                    (uint32_t)(gn * args.Mpad * 32), &full[stage]);
-          ++issued;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        return true;
-      };
-      for (int g = g0; g < g1 && ok;) {
-        const int t = g / KB, kb0 = g - t * KB, kb1 = min(KB, g1 - t * KB);
-        const int ins = (tc && kb0 == 0) ? max(kb0, kb1 - 1 - S) : -1;  // expand after this k-block
-        for (int kb = kb0; kb < kb1; ++kb, ++i) {
-          uint8_t *st = ring + (size_t)stage * stage_bytes;
-          if (i >= early) {
-            if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, ab)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&full[stage], tx);
-            tma_load_2d(st, &tmap_w, &full[stage], kb * SK_BK, t * SK_BN, pol_w);
-          }
-          tma_load_2d(st + SK_WTILE, &tmap_x, &full[stage], kb * SK_BK, 0, pol_x);
-          ++issued;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          if (kb == ins && !issue_expand(t)) {
+    }
+    early = __shfl_sync(0xffffffffu, early, 0);
+    // k-blocks [from, to) of tile t, lane 0 only.
+    auto issue_kblocks = [&](int t, int from, int to) {
+      for (int kb = from; kb < to; ++kb, ++i) {
+        uint8_t *st = ring + (size_t)stage * stage_bytes;
+        if (i >= early) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, ab)) {
             ok = false;
             break;
           }
+          mbar_arrive_expect_tx(&full[stage], tx);
+          tma_load_2d(st, &tmap_w, &full[stage], kb * SK_BK, t * SK_BN, pol_w);
         }
-        g = t * KB + kb1;
+        tma_load_2d(st + SK_WTILE, &tmap_x, &full[stage], kb * SK_BK, 0, pol_x);
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
+    };
+    auto sync_state = [&]() {
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      stage = __shfl_sync(0xffffffffu, stage, 0);
+      phase = __shfl_sync(0xffffffffu, phase, 0);
+      issued = __shfl_sync(0xffffffffu, issued, 0);
+      i = __shfl_sync(0xffffffffu, i, 0);
+      __syncwarp();
+    };
+    for (int g = g0; g < g1 && ok;) {
+      const int t = g / KB, kb0 = g - t * KB, kb1 = min(KB, g1 - t * KB);
+      // The expand operands of an owned tile (verify mode) go into the ring
+      // before the tile's last S k-blocks, so that they land while those
+      // stream instead of after the whole tile.
+      const int ins = (tc && kb0 == 0) ? max(kb0, kb1 - 1 - S) : -1;
+      const int split = ins >= 0 ? ins + 1 : kb1;
+      if (lane == 0) issue_kblocks(t, kb0, split);
+      sync_state();
+      if (ok && ins >= 0) {
+        if (!waited) {
+          grid_dependency_wait();  // the token windows come from the shrink kernel just before
+          waited = true;
+        }
+        if (ns < 0) ns = args.plan[L.hdr + 4];
+        if (ns > 0)
+          ok = expand_produce(args.plan + L.slices, 0, ns, 0, args.Mb, t * SK_BN, args.N, &tmap_b,
+                              args.tw + (size_t)sk_slice_of(args, t * SK_BN) * args.tw_slice, ring, stage_bytes, S,
+                              full, empty, meta, chunk, stage, phase, issued, ab, pol_w, lane);
+      }
+      if (lane == 0 && ok) issue_kblocks(t, split, kb1);
+      sync_state();
+      g = t * KB + kb1;
+    }
+    if (lane == 0) {
       if (!ok) {
         *reinterpret_cast<volatile int *>(abort_flag) = 1;
         raise_status(args.status, MLORA_DEV_TIMEOUT);
@@ -318,45 +289,18 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       stage = __shfl_sync(0xffffffffu, stage, 0);
       phase = __shfl_sync(0xffffffffu, phase, 0);
+      __syncwarp();
       if (ok && expand_here) {
         if (ns < 0) {
-          grid_dependency_wait();  // the plan and the masked operand come from earlier kernels
-          ns = min(args.plan[L.hdr + 4], SK_EXPAND_TABLE);
+          grid_dependency_wait();  // the plan and the token windows come from earlier kernels
+          ns = args.plan[L.hdr + 4];
         }
-        for (int sl0 = 0; sl0 < ns && ok; sl0 += SK_EXPAND_PER_STAGE) {
-          const int gn = min(SK_EXPAND_PER_STAGE, ns - sl0);
-          if (lane == 0 && !mbar_wait_bounded(&full[stage], phase, ab)) ok = false;
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-          uint8_t *st = ring + (size_t)stage * stage_bytes;
-          bool zeroed = false;
-          for (int g = 0; g < gn; ++g) {
-            const int c0 = exp_tab[sl0 + g].z;  // rank columns of this 16-wide block
-            if (c0 < 16) {
-              // B columns past the rank hold the caller's padding (maybe NaN;
-              // NaN * 0 would still be NaN): zero them before the MMA reads.
-              zero_tail_columns_sw32(st + g * SK_BN * 32, c0, lane);
-              zeroed = true;
-            }
-          }
-          if (zeroed) fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tc_fence_after_sync();
-            const uint32_t a_addr = smem_addr(st);
-            for (int g = 0; g < gn; ++g)
-              mma_bf16_ss(acc, smem_desc_kmajor_sw32(a_addr + g * SK_BN * 32),
-                          smem_desc_kmajor_sw32(a_addr + SK_EXPAND_PER_STAGE * SK_BN * 32 + g * args.Mb * 32), idesc,
-                          1u);
-            mma_commit(&empty[stage]);
-          }
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        if (ns > 0) {
+          ok = expand_consume(ring, stage_bytes, S, full, empty, meta, acc, stage, phase, ab, lane);
+          issued_any = true;
         }
       }
-      if (lane == 0) mma_kblocks(ins + 1, kb1);
+      if (lane == 0 && ok) mma_kblocks(ins + 1, kb1);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       stage = __shfl_sync(0xffffffffu, stage, 0);
       phase = __shfl_sync(0xffffffffu, phase, 0);
@@ -364,6 +308,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       __syncwarp();
       g = t * KB + kb1;
     }
+    issued_any = __shfl_sync(0xffffffffu, issued_any ? 1 : 0, 0) != 0 || issued_any;
     if (lane == 0 && !ok) {
       *reinterpret_cast<volatile int *>(abort_flag) = 1;
       raise_status(args.status, MLORA_DEV_TIMEOUT);
@@ -379,6 +324,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     // Warp w reads tensor-memory lanes 32*(w%4)..+31: tile rows.
     const int quad = warp & 3, et = threadIdx.x - 64;
     const int row = quad * 32 + lane;
+    const int32_t *perm = tc ? args.plan + L.perm : nullptr;  // output row of each accumulator column
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     grid_dependency_wait();  // y and the flags may still be in use by the preceding kernel
     int seg = 0;
@@ -432,12 +378,17 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         bool have = true;
         if (nc > 0) {
           if (et == 0) {
+            // The timeout test polls flag words past the grid's, which no CTA
+            // sets, for test_flag_wait_ns instead of the contributors' flags.
+            const bool probe = args.test_flag_wait_ns != 0;
+            const uint64_t limit = probe ? (uint64_t)args.test_flag_wait_ns : WAIT_LIMIT_NS;
             for (int j = cta + 1; j <= last; ++j) {
-              bool seen = ld_acquire_gpu(&args.flags[j]) == 1u;
+              const uint32_t *flag = &args.flags[probe ? args.P + j : j];
+              bool seen = ld_acquire_gpu(flag) == 1u;
               if (!seen) {
                 const uint64_t t0 = global_timer_ns();
-                while (!(seen = ld_acquire_gpu(&args.flags[j]) == 1u)) {
-                  if (global_timer_ns() - t0 > WAIT_LIMIT_NS) break;
+                while (!(seen = ld_acquire_gpu(flag) == 1u)) {
+                  if (global_timer_ns() - t0 > limit) break;
                   sleep_ns(64);
                 }
               }
@@ -508,16 +459,15 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                 }
               }
             }
-            if (n < args.N) {
-              uint16_t *yp = args.y + (size_t)cb * args.N + n;
-              if (whole) {
+            // Output row of column cb + j: perm[cb + j] with sorted rows (lane
+            // j fetches it), else cb + j.
+            const int myc = cb + lane;
+            const int myrow = perm ? (myc < args.M ? __ldg(perm + myc) : 0) : myc;
+            uint16_t *yn = args.y + n;
 #pragma unroll
-                for (int j = 0; j < SK_CHUNK; ++j) yp[(size_t)j * args.N] = float_to_bf16_bits(v[j]);
-              } else {
-#pragma unroll
-                for (int j = 0; j < SK_CHUNK; ++j)
-                  if (cb + j < q1) yp[(size_t)j * args.N] = float_to_bf16_bits(v[j]);
-              }
+            for (int j = 0; j < SK_CHUNK; ++j) {
+              const int row = __shfl_sync(0xffffffffu, myrow, j);
+              if (n < args.N && (whole || cb + j < q1)) yn[(size_t)row * args.N] = float_to_bf16_bits(v[j]);
             }
           }
           if (fetch) named_bar_sync(1, 128);  // the ring is refilled only after every thread read it
@@ -550,6 +500,28 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   }
 }
 
+// One CTA of this shared-memory size fits on an SM (so a grid of one CTA per
+// SM is resident at once on an otherwise idle GPU).  Cached per device.
+static bool sk_resident(size_t smem) {
+  static int attr_done[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (!attr_done[dev]) {
+    if (cudaFuncSetAttribute(gemm_sk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SK_SMEM_LIMIT) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    attr_done[dev] = 1;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_sk_kernel, SK_THREADS, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return n >= 1;
+}
+
 SkShape sk_shape(int M, int N, int K, int num_sms) {
   SkShape s = {};
   s.ok = false;
@@ -560,7 +532,7 @@ SkShape sk_shape(int M, int N, int K, int num_sms) {
   s.cols = cols;
   const int stage_bytes = SK_WTILE + s.Mb * SK_BK * 2;
   int st = (int)((SK_SMEM_LIMIT - SK_SMEM_FIXED) / stage_bytes);
-  s.stages = st > 8 ? 8 : st;
+  s.stages = st > SK_MAX_STAGES ? SK_MAX_STAGES : st;
   if (s.stages < 2) return s;
   s.n_tiles = (N + SK_BN - 1) / SK_BN;
   s.kblocks = (K + SK_BK - 1) / SK_BK;
@@ -574,7 +546,7 @@ SkShape sk_shape(int M, int N, int K, int num_sms) {
   if (P < 1) P = 1;
   s.P = P;
   s.smem_bytes = SK_SMEM_FIXED + (size_t)s.stages * stage_bytes;
-  s.ok = true;
+  s.ok = sk_resident(s.smem_bytes);
   return s;
 }
 
@@ -617,23 +589,15 @@ static bool sk_map(CUtensorMap *map, const void *base, long long rows, int cols,
 cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partials, uint32_t *flags, cudaStream_t s,
                            int *err_code) {
   *err_code = 0;
-  static int attr_done[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidValue;
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(gemm_sk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SK_SMEM_LIMIT) !=
-        cudaSuccess)
-      return cudaErrorInvalidValue;
-    attr_done[dev] = 1;
-  }
+  if (!sh.ok) return cudaErrorInvalidValue;  // sk_shape set the kernel's attributes when it said ok
   CUtensorMap tw, tx, tb;
   if (!sk_map(&tw, g.W, g.N, g.K, SK_BN, SK_BK) || !sk_map(&tx, g.x, g.M, g.K, sh.Mb, SK_BK)) {
     *err_code = 1;
     return cudaErrorInvalidValue;
   }
-  const int use_tw = (g.mode == MLORA_VERIFY && g.tw != nullptr) ? 1 : 0;
+  const int sorted = (g.mode == MLORA_VERIFY && g.tw != nullptr) ? 1 : 0;
   tb = tw;
-  if (use_tw) {
+  if (sorted) {
     if (!sk_map(&tb, g.B_stack, (long long)g.n_ad * g.N, g.r_max, SK_BN, 16)) {
       *err_code = 1;
       return cudaErrorInvalidValue;
@@ -652,11 +616,11 @@ cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partia
   a.mode = g.mode;
   a.prefetch_w = g.prefetch_w;
   a.after_shrink = g.after_shrink;
-  a.use_tw = use_tw;
-  a.Mpad = expand_rows(g.M);
+  a.sorted = sorted;
   a.n_slices = g.n_slices;
   for (int i = 0; i < MLORA_MAX_SLICES; ++i) a.slice_end[i] = i < g.n_slices ? g.slice_end[i] : g.N;
-  a.tw_slice_rows = max_expand_slices(g.M, g.n_ad) * expand_rows(g.M);
+  a.tw_slice = max_window_rows(g.M, g.n_ad) * 16;
+  a.test_flag_wait_ns = g.test_flag_wait_ns;
   a.n_ad = g.n_ad;
   a.y = g.y;
   a.tw = g.tw;

@@ -38,12 +38,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 cudaError_t launch_plan(const int32_t *adapter_idx, int M, const int32_t *rank_of, int n_ad, int r_max,
                         int32_t *plan, uint32_t *status, cudaStream_t s);
 
+// The verify pass's token rows in adapter-sorted order: xs[p] = x[perm[p]]
+// for p < M (bf16 [M, K]).
+cudaError_t launch_gather_rows(const uint16_t *x, int M, int K, const int32_t *perm, uint16_t *xs, int num_sms,
+                               cudaStream_t s);
+
 // Step a2: T[m, j] for j < rank (fp32, row stride t_stride), for n_slices
 // output slices (A: [n_slices][n_ad][r_max][K]; T: [n_slices][M][t_stride]).
 // `zero_first` clears T first so that padding and rows without an adapter
-// read 0.  With `tw` non-null it also writes the whole masked operand of the
-// tensor-core expand, [n_slices][max_expand_slices(M, n_ad)][expand_rows(M)][16]
-// bf16: scale * T on member rows, 0 elsewhere.
+// read 0.  With `tw` non-null it also writes the token windows of the
+// tensor-core expand, [n_slices][max_window_rows(M, n_ad)][16] bf16 (see
+// common.cuh): scale * T on member rows, 0 elsewhere.
 cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, int n_ad, int r_max,
                           const int32_t *plan, float *T, int t_stride, bool zero_first, int num_sms, uint16_t *tw,
                           float scale, int n_slices, cudaStream_t s);
@@ -74,7 +79,9 @@ struct GemmLaunch {
   const float *T;      // [n_slices][M][T_STRIDE]
   const int32_t *plan;
   uint32_t *status;
-  const uint16_t *tw;  // masked low-rank operand [n_slices][...], or null (bucket-walk epilogue only)
+  const uint16_t *tw;  // token windows [n_slices][max_window_rows][16] with x in sorted order, or null
+                       // (x in row order, bucket-walk epilogue)
+  uint32_t test_flag_wait_ns;  // stream-K only: nonzero makes owners wait on never-set flags (timeout test)
 };
 cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s, int *err_code);
 
@@ -82,7 +89,8 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
 // equal shares of the (tile, k-block) pairs, at most 256 token rows, draft mode
 // or verify mode with the tensor-core expand.  Needs sk_partial_bytes(M, SMs)
 // of scratch for partial sums and one flag word per CTA (zero between calls).
-constexpr int SK_EXPAND_TABLE = 256;  // expand blocks the stream-K kernel stages in shared memory
+// `ok` is false when a CTA of that shape would not fit on every SM at once
+// (the cross-CTA waits need the whole grid resident).
 struct SkShape {
   bool ok;
   int Mb, cols, stages, n_tiles, kblocks, total, P;

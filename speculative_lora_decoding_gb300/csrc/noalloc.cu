@@ -123,6 +123,7 @@ extern "C" MLORA_API mlora_status mlora_linear_noalloc(const mlora_bf16 *x, int 
   g.plan = plan;
   g.status = status;
   g.tw = nullptr;
+  g.test_flag_wait_ns = 0;
   int err = 0;
   const cudaError_t e = launch_gemm(g, gemm_shape(M, N, K, sms), s, &err);
   if (err) return MLORA_ERR_ARG;

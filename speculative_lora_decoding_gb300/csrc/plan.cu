@@ -8,7 +8,8 @@
 // keeps each adapter's B row in registers across its group.
 //
 // One CTA of 256 threads: histogram in shared memory, block-wide scans for
-// the offsets, the active-adapter list and the shrink work list, then a
+// the offsets, the active-adapter list, the shrink work list and the expand
+// blocks with their token windows (see common.cuh), then a
 // warp-sequential ranking (match_any within a warp, warps in order) that
 // keeps rows of one bucket in increasing row order, and finally the shrink
 // work items written out in full, so that a shrink CTA finds its adapter,
@@ -116,10 +117,13 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
   }
   block_sync();
 
-  // Active adapters (rows > 0) and the shrink work list over them.
+  // Active adapters (rows > 0), the shrink work list and the expand blocks
+  // over them.  Adapter a's rows sit at sorted positions [s0, s1) = [cnt[a],
+  // cnt[a] + running[a]); its token window is [w0, w1) = [s0 & ~15,
+  // (s1 + 15) & ~15), one copy per 16-rank block in the operand buffer.
   {
     const int a0 = min(tid * per, n_ad), a1 = min(a0 + per, n_ad);
-    int nact = 0, nitems = 0, rmax = 0;
+    int nact = 0, nitems = 0, rmax = 0, nsl = 0, nwin = 0;
     for (int a = a0; a < a1; ++a) {
       const int c = running[a];
       if (c > 0) {
@@ -130,30 +134,35 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
         // caller padding (possibly NaN); past r_max it reads as zero.
         if ((r % 16) != 0 && r != r_max) partial_block = 1;
         nitems += ((r + SHRINK_J - 1) / SHRINK_J) * ((c + SHRINK_TOK - 1) / SHRINK_TOK);
+        const int nblk = (r + 15) / 16;
+        const int w0 = cnt[a] & ~15, w1 = (cnt[a] + c + 15) & ~15;
+        nsl += nblk;
+        nwin += nblk * (w1 - w0);
       }
     }
     if (rmax > 0) atomicMax(&max_rank, rmax);
-    int nsl = 0;
-    for (int a = a0; a < a1; ++a)
-      if (running[a] > 0) nsl += (plan[L.rank_eff + a] + 15) / 16;
-    int tot_act, tot_items, tot_sl;
+    int tot_act, tot_items, tot_sl, tot_win;
     int pa = block_excl_scan(nact, scan_sh, &tot_act);
     int pi = block_excl_scan(nitems, scan_sh, &tot_items);
     int ps = block_excl_scan(nsl, scan_sh, &tot_sl);
+    int pw = block_excl_scan(nwin, scan_sh, &tot_win);
     for (int a = a0; a < a1; ++a) {
       const int c = running[a];
       if (c > 0) {
         const int r = plan[L.rank_eff + a];
+        const int w0 = cnt[a] & ~15, W = ((cnt[a] + c + 15) & ~15) - w0;
         plan[L.active + pa] = a;
         plan[L.item_off + pa] = pi;
         plan[L.slice_off + a] = ps;
         for (int j = 0; j * 16 < r; ++j) {
-          plan[L.slices + 2 * (ps + j)] = a;
-          plan[L.slices + 2 * (ps + j) + 1] = 16 * j;
+          int4 *rec = reinterpret_cast<int4 *>(plan + L.slices + (size_t)(ps + j) * EXP_WORDS);
+          rec[0] = make_int4(a, 16 * j, min(16, r - 16 * j), pw + j * W);
+          rec[1] = make_int4(w0, W, 0, 0);
         }
         ++pa;
         pi += ((r + SHRINK_J - 1) / SHRINK_J) * ((c + SHRINK_TOK - 1) / SHRINK_TOK);
         ps += (r + 15) / 16;
+        pw += ((r + 15) / 16) * W;
       }
     }
     if (tid == 0) {
@@ -162,6 +171,7 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
       plan[L.hdr + 1] = tot_items;
       plan[L.hdr + 2] = M;
       plan[L.hdr + 4] = tot_sl;
+      plan[L.hdr + 6] = tot_win;
     }
   }
   block_sync();
@@ -216,12 +226,12 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1)
     const int j0 = (local % nj) * SHRINK_J;
     const int t0 = (local / nj) * SHRINK_TOK;
     const int ntok = min(SHRINK_TOK, c - t0);
-    int4 w0 = make_int4(a, j0, min(SHRINK_J, r - j0), ntok);
+    const int nrow = min(SHRINK_J, r - j0);
     int rows[SHRINK_TOK];
 #pragma unroll
     for (int t = 0; t < SHRINK_TOK; ++t) rows[t] = (t < ntok) ? plan[L.perm + s0 + t0 + t] : 0;
     int4 *rec = reinterpret_cast<int4 *>(plan + L.items + (size_t)it * ITEM_WORDS);
-    rec[0] = w0;
+    rec[0] = make_int4(a, j0 | (nrow << 8) | (ntok << 16), s0 + t0, plan[L.slice_off + a]);
     rec[1] = make_int4(rows[0], rows[1], rows[2], rows[3]);
   }
   block_sync();

@@ -20,15 +20,21 @@
 // most one CTA per SM, each taking (slice, item) units in turn, so that every
 // SM keeps registers for the GEMM CTA that streams beside it.
 //
-// The masked operand of the tensor-core expand, when requested: for each
-// expand slice e = (adapter a, 16-rank block j0) and token row m, 16 bf16
-// values scale * T[m, j0:j0+16] if m belongs to a and 0 otherwise.  The work
-// items write the member entries of the rank columns below ceil8(rank); a
-// grid-stride pass writes zeros to exactly the other 16-byte halves, so the
-// two never touch the same bytes and no earlier zeroing is needed.  Rows are
-// stored as the GEMM's shared memory wants them for a 32-byte-swizzled
-// operand (the two 16-byte halves of row m swapped when bit 2 of m is set),
-// so that the GEMM fetches them with one plain bulk copy.
+// The low-rank operand of the tensor-core expand, when requested (tw):
+// for each expand block (adapter a, 16-rank block j0) the window of sorted
+// positions [w0, w0 + W) that covers a's rows (see common.cuh), W rows of
+// 16 bf16: scale * T[row, j0:j0+16] on a's rows and 0 on the others.  The
+// work items write the member entries of the rank columns below ceil8(rank);
+// a pass over the windows writes zeros to exactly the other 16-byte halves,
+// so the two never touch the same bytes and no earlier zeroing is needed.
+// Rows are stored as the GEMM's shared memory wants them for a
+// 32-byte-swizzled operand (the two 16-byte halves of window row i swapped
+// when bit 2 of i is set), so that the GEMM fetches a window with one plain
+// bulk copy.
+//
+// gather_rows_kernel: the verify pass's token rows in adapter-sorted order,
+// xs[p] = x[perm[p]], which the GEMM reads so that each adapter's rows are
+// adjacent accumulator columns.
 #include "common.cuh"
 #include "launch.h"
 
@@ -89,23 +95,26 @@ __global__ void __launch_bounds__(SHRINK_THREADS, SHRINK_MIN_BLOCKS)
   const int total_items = plan[L.hdr + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kchunks = K >> 3;  // 16-byte pieces per row
-  const int Mpad = expand_rows(M);
+  const size_t tw_slice = max_window_rows(M, n_ad) * 16;  // bf16 elements of one slice's operand buffer
 
   if (tw_all) {
-    // Zero halves: (slice, expand block e, row m, half h) not written by an item.
+    // Zero halves: (slice, block, window row i, half h) not written by an item.
     const int n_exp = plan[L.hdr + 4];
-    const int halves = n_exp * Mpad * 2;
-    for (int hs = blockIdx.x * SHRINK_THREADS + threadIdx.x; hs < halves * n_slices;
-         hs += gridDim.x * SHRINK_THREADS) {
-      const int sl = hs / halves, hh = hs - sl * halves;
-      uint16_t *tw = tw_all + (size_t)sl * max_expand_slices(M, n_ad) * Mpad * 16;
-      const int e = hh / (2 * Mpad), rem = hh - e * 2 * Mpad;
-      const int m = rem >> 1, h = rem & 1;
-      const int a = plan[L.slices + 2 * e], j0 = plan[L.slices + 2 * e + 1];
-      const bool member = m < M && plan[L.row_adapter + m] == a;
-      if (!(member && j0 + 8 * h < plan[L.rank_eff + a]))
-        *reinterpret_cast<uint4 *>(tw + ((size_t)e * Mpad + m) * 16 + 8 * (h ^ ((m >> 2) & 1))) =
-            make_uint4(0u, 0u, 0u, 0u);
+    for (int bu = blockIdx.x; bu < n_exp * n_slices; bu += gridDim.x) {
+      const int sl = bu / n_exp, b = bu - sl * n_exp;
+      const int4 e0 = *reinterpret_cast<const int4 *>(plan + L.slices + (size_t)b * EXP_WORDS);
+      const int4 e1 = *reinterpret_cast<const int4 *>(plan + L.slices + (size_t)b * EXP_WORDS + 4);
+      const int a = e0.x, j0 = e0.y, win = e0.w, w0 = e1.x, W = e1.y;
+      const int s0 = plan[L.seg_offsets + a], s1 = plan[L.seg_offsets + a + 1];
+      const int r = plan[L.rank_eff + a];
+      uint16_t *tw = tw_all + (size_t)sl * tw_slice + (size_t)win * 16;
+      for (int hh = threadIdx.x; hh < 2 * W; hh += SHRINK_THREADS) {
+        const int i = hh >> 1, h = hh & 1;
+        const int p = w0 + i;
+        const bool member = p >= s0 && p < s1;
+        if (!(member && j0 + 8 * h < r))
+          *reinterpret_cast<uint4 *>(tw + (size_t)i * 16 + 8 * (h ^ ((i >> 2) & 1))) = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
   }
 
@@ -114,10 +123,11 @@ __global__ void __launch_bounds__(SHRINK_THREADS, SHRINK_MIN_BLOCKS)
     const int sl = wu / total_items, item = wu - sl * total_items;
     const uint16_t *A = A_all + (size_t)sl * n_ad * r_max * K;
     float *T = T_all + (size_t)sl * M * t_stride;
-    uint16_t *tw = tw_all ? tw_all + (size_t)sl * max_expand_slices(M, n_ad) * Mpad * 16 : nullptr;
+    uint16_t *tw = tw_all ? tw_all + (size_t)sl * tw_slice : nullptr;
     const int4 *rec = reinterpret_cast<const int4 *>(plan + L.items + (size_t)item * ITEM_WORDS);
     const int4 h = rec[0], rw = rec[1];
-    const int a = h.x, j0 = h.y, nrow = h.z, ntok = h.w;
+    const int a = h.x, j0 = h.y & 0xFF, nrow = (h.y >> 8) & 0xFF, ntok = h.y >> 16;
+    const int pos0 = h.z, blk0 = h.w;
     const int rows[SHRINK_TOK] = {rw.x, rw.y, rw.z, rw.w};
 
     const uint16_t *Abase = A + ((size_t)a * r_max + j0) * (size_t)K;
@@ -151,14 +161,14 @@ __global__ void __launch_bounds__(SHRINK_THREADS, SHRINK_MIN_BLOCKS)
         }
       }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int hh = 0; hh < 2; ++hh) {
         float xf[SHRINK_TOK][8];
 #pragma unroll
-        for (int t = 0; t < SHRINK_TOK; ++t) bf16x8_to_f32(xv[h][t], xf[t]);
+        for (int t = 0; t < SHRINK_TOK; ++t) bf16x8_to_f32(xv[hh][t], xf[t]);
 #pragma unroll
         for (int j = 0; j < SHRINK_J; ++j) {
           float af[8];
-          bf16x8_to_f32(av[h][j], af);
+          bf16x8_to_f32(av[hh][j], af);
 #pragma unroll
           for (int t = 0; t < SHRINK_TOK; ++t)
 #pragma unroll
@@ -178,16 +188,56 @@ __global__ void __launch_bounds__(SHRINK_THREADS, SHRINK_MIN_BLOCKS)
         const float v = (j < nrow) ? s : 0.f;
         T[(size_t)rows[t] * t_stride + j0 + j] = v;
         if (tw) {
-          // Member row of the masked operand: slice (j0 + j) / 16 of adapter a.
-          const int slice = plan[L.slice_off + a] + (j0 + j) / 16;
-          const int c = (j0 + j) % 16, m = rows[t];
-          const int pc = (((c >> 3) ^ ((m >> 2) & 1)) << 3) | (c & 7);  // swizzled column
-          tw[((size_t)slice * Mpad + m) * 16 + pc] = float_to_bf16_bits(scale * v);
+          // Member row of the window of block (j0 + j) / 16 of adapter a.
+          const int b = blk0 + (j0 + j) / 16;
+          const int win = plan[L.slices + (size_t)b * EXP_WORDS + 3];
+          const int w0 = plan[L.slices + (size_t)b * EXP_WORDS + 4];
+          const int c = (j0 + j) % 16, i = pos0 + t - w0;
+          const int pc = (((c >> 3) ^ ((i >> 2) & 1)) << 3) | (c & 7);  // swizzled column
+          tw[((size_t)win + i) * 16 + pc] = float_to_bf16_bits(scale * v);
         }
       }
     }
     block_sync();
   }
+}
+
+// xs[p, :] = x[perm[p], :] for p < M (16-byte pieces, four in flight per
+// thread).  Waits for the plan, then lets the shrink kernel launch.
+__global__ void __launch_bounds__(256)
+    gather_rows_kernel(const uint16_t *__restrict__ x, int M, int K, const int32_t *__restrict__ perm,
+                       uint16_t *__restrict__ xs) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int kv = K >> 3;
+  const long long total = (long long)M * kv;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 4 * stride) {
+    uint4 v[4];
+    long long dst[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const long long i = i0 + u * stride;
+      dst[u] = -1;
+      if (i < total) {
+        const int p = (int)(i / kv), c = (int)(i - (long long)p * kv);
+        v[u] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)perm[p] * K) + c);
+        dst[u] = (long long)p * kv + c;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (dst[u] >= 0) reinterpret_cast<uint4 *>(xs)[dst[u]] = v[u];
+  }
+}
+
+cudaError_t launch_gather_rows(const uint16_t *x, int M, int K, const int32_t *perm, uint16_t *xs, int num_sms,
+                               cudaStream_t s) {
+  const long long pieces = (long long)M * (K >> 3);
+  const long long want = (pieces + 4 * 256 - 1) / (4 * 256);
+  const int grid = (int)max(1LL, min(want, (long long)num_sms * 4));
+  cudaError_t e = launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, s, x, M, K, perm, xs);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, int n_ad, int r_max,

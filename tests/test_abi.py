@@ -49,8 +49,10 @@ def test_workspace_sizes(lib):
     b = lib.mlora_linear_workspace_bytes(256, 4096, 4096, 16)
     c = lib.mlora_linear_workspace_bytes(512, 14336, 4096, 128)
     assert 0 < a < b and c > 0
-    # one workspace serves every projection of a step: the size depends on M and n_adapters only
-    assert lib.mlora_linear_workspace_bytes(128, 1024, 14336, 16) == a
+    # one workspace sized for the largest K serves every projection of a step: the verify pass keeps the
+    # token rows in adapter-sorted order (M x K bf16), so the size grows with K and not with N
+    assert lib.mlora_linear_workspace_bytes(128, 1024, 4096, 16) == a
+    assert lib.mlora_linear_workspace_bytes(128, 4096, 14336, 16) >= a + 128 * (14336 - 4096) * 2
     assert lib.mlora_linear_workspace_bytes(128, 4096, 4097, 16) == 0      # K % 8 != 0
     assert lib.mlora_linear_workspace_bytes(0, 4096, 4096, 16) == 0
     assert lib.mlora_accept_workspace_bytes(256, 4, 128256) > 0

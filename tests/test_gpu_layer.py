@@ -4,6 +4,8 @@ Tolerance: max |y - y_ref| <= 1e-2 * max |y_ref| per call (bf16 inputs, fp32
 accumulation, one bf16 rounding of the output).  Integer work (the plan) and
 the small-integer case are compared bit for bit.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -99,13 +101,14 @@ def test_ragged_shapes_against_oracle(M, N, K, n_ad, ranks):
 
 
 @pytest.mark.parametrize("M,N,K,n_ad,ranks", [
-    (16, 256, 2048, 4, (8, 16, 24, 0)),    # ranks inside a 16-wide block: CUDA-core expand
-    (64, 384, 4096, 4, (16, 32, 48, 64)),  # multiples of 16: tensor-core expand, padding never read
+    (16, 256, 2048, 4, (8, 16, 24, 0)),    # ranks inside a 16-wide block: B columns zeroed before the MMA
+    (64, 384, 4096, 4, (16, 32, 48, 64)),  # multiples of 16: padding never inside a block
     (128, 1024, 4096, 16, (16,) * 15 + (40,)),
+    (128, 1024, 1024, 32, (16,) * 32),     # 32 blocks against a 1024-deep K loop
 ])
 def test_nan_rank_padding_in_expand_shapes(M, N, K, n_ad, ranks):
-    """Shapes where the tensor-core expand is allowed, with NaN in every
-    padding entry of A and B past each adapter's rank."""
+    """NaN in every padding entry of A and B past each adapter's rank never
+    reaches y."""
     ml = needs_gpu()
     x, W, A, B, rk, idx = _random_case(M + N + K, M, N, K, n_ad, ranks, r_max=64, nan_pad=True)
     y_ref, _ = _oracle(x, W, A, B, rk, idx, 2.0, OL.VERIFY)
@@ -113,6 +116,72 @@ def test_nan_rank_padding_in_expand_shapes(M, N, K, n_ad, ranks):
     y = host_bf16_to_f64(_run(ml, x, W, A, B, rk, idx, 2.0, OL.VERIFY, ws=ws))
     assert ws.status() == 0 and np.isfinite(y).all()
     assert _rel_err(y, y_ref) <= TOL
+
+
+def _zipf_idx(seed, M, n_ad, s=1.1):
+    g = np.random.default_rng(seed)
+    w = np.arange(1, n_ad + 1, dtype=np.float64) ** -s
+    return g.choice(n_ad, M, p=w / w.sum()).astype(np.int32)
+
+
+@pytest.mark.parametrize("M,N,K,n_ad,ranks,zipf", [
+    # more than 256 rows: cluster kernel, two MMAs per k-step, sorted rows and token windows
+    (384, 1024, 1024, 16, (8, 16, 32, 64) * 4, False),
+    (512, 640, 2048, 128, tuple([8, 16, 32, 64] * 32), True),    # heterogeneous ranks, Zipf: large and single rows
+    (640, 768, 1536, 64, (16,) * 64, False),                      # two token groups of 320 rows
+    (1000, 256, 512, 40, tuple([8, 24, 40, 56, 64] * 8), True),   # windows crossing the token-group boundary
+    # stream-K verify (at most 256 rows) with hundreds of expand blocks and ranks inside 16-wide blocks
+    (256, 6144, 1024, 128, (64,) * 128, False),
+    (200, 640, 2048, 64, (8, 24, 40, 56) * 16, True),
+    (48, 1280, 4096, 300, tuple([1, 9, 17, 33, 63] * 60), False),
+])
+def test_windowed_expand_against_oracle(M, N, K, n_ad, ranks, zipf):
+    """The tensor-core expand over each adapter's token window, with NaN in
+    every padding entry of A and B past each adapter's rank."""
+    ml = needs_gpu()
+    x, W, A, B, rk, idx = _random_case(M + 3 * N + K, M, N, K, n_ad, ranks, r_max=64, nan_pad=True)
+    if zipf:
+        idx = _zipf_idx(M + n_ad, M, n_ad)
+        idx[::11] = -1
+    ws = ml.Workspace(ml.linear_workspace_bytes(M, N, K, n_ad))
+    y_ref, _ = _oracle(x, W, A, B, rk, idx, 2.0, OL.VERIFY)
+    y = host_bf16_to_f64(_run(ml, x, W, A, B, rk, idx, 2.0, OL.VERIFY, ws=ws))
+    assert ws.status() == 0 and np.isfinite(y).all()
+    assert _rel_err(y, y_ref) <= TOL, (M, N, K, n_ad, ml.gemm_kernel_name(M, N, K, n_ad, 64, ml.VERIFY))
+    # every output row is written (rows come back through the permutation)
+    yd = host_bf16_to_f64(_run(ml, x, W, A, B, rk, idx, 2.0, OL.DRAFT, ws=ws))
+    y_ref_d, _ = _oracle(x, W, A, B, rk, idx, 2.0, OL.DRAFT)
+    assert _rel_err(yd, y_ref_d) <= TOL
+
+
+def test_stream_k_flag_wait_gives_up_and_workspace_recovers():
+    """The stream-K GEMM's cross-CTA wait, made to run out on purpose: with
+    the test hook the tile owners wait 2 microseconds on flag words nothing
+    sets, give up, finish their tiles without the partial sums and raise the
+    timeout bit; the call returns and the context stays usable.  After
+    mlora_workspace_init the next call is back to oracle parity."""
+    ml = needs_gpu()
+    lib = ml.library()
+    M, N, K = 64, 6144, 4096
+    if ml.gemm_kernel_name(M, N, K, 4, 16, ml.DRAFT) != "gemm_sk_kernel":
+        pytest.skip("this device runs the cluster kernel for the shape")
+    x, W, A, B, rk, idx = _random_case(21, M, N, K, 4, (16, 16, 8, 12), r_max=16, nan_pad=False)
+    ws = ml.Workspace(ml.linear_workspace_bytes(M, N, K, 4))
+    lib.mlora_debug_set_flag_wait_ns(2000)
+    try:
+        _run(ml, x, W, A, B, rk, idx, 2.0, OL.DRAFT, ws=ws)
+    finally:
+        lib.mlora_debug_set_flag_wait_ns(0)
+    bits = ctypes.c_uint32(0)
+    st = lib.mlora_read_device_status(ws.ptr, ctypes.byref(bits), 1, torch.cuda.current_stream().cuda_stream)
+    assert st == 6 and bits.value & ml.DEV_TIMEOUT  # MLORA_ERR_TIMEOUT
+    assert lib.mlora_workspace_init(ws.ptr, ws.nbytes, torch.cuda.current_stream().cuda_stream) == 0
+    y_ref, _ = _oracle(x, W, A, B, rk, idx, 2.0, OL.DRAFT)
+    for mode in (OL.DRAFT, OL.VERIFY):
+        y_ref, _ = _oracle(x, W, A, B, rk, idx, 2.0, mode)
+        y = host_bf16_to_f64(_run(ml, x, W, A, B, rk, idx, 2.0, mode, ws=ws))
+        assert ws.status() == 0
+        assert _rel_err(y, y_ref) <= TOL
 
 
 @pytest.mark.parametrize("M,N,K", [

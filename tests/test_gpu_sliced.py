@@ -56,13 +56,14 @@ def _run_sliced(ml, x, W, A, B, ranks, idx, ends, scale, mode, ws=None, seg=None
 
 
 @pytest.mark.parametrize("M,widths,K,n_ad,ranks", [
-    # tensor-core expand (M <= 256, slices * 32 <= K)
+    # stream-K or cluster kernel, up to 256 rows
     (16, (256, 128, 130), 2048, 4, (8, 16, 24, 0)),
     (128, (512, 128, 128), 4096, 16, (16,) * 16),
-    # more expand slices than the tensor-core rule allows: CUDA-core epilogue
+    # more expand blocks than k-blocks
     (40, (128, 200), 256, 6, (8, 16, 32, 64, 24, 40)),
-    # more than 256 rows: no masked operand, CUDA-core epilogue
+    # more than 256 rows: cluster kernel, two MMAs per k-step
     (300, (384, 256), 512, 5, (64, 8, 33, 17, 1)),
+    (640, (256, 512, 128), 1024, 24, tuple([8, 16, 32, 64, 48, 24] * 4)),
     # four slices
     (64, (128, 128, 256, 72), 1024, 3, (16, 32, 8)),
 ])
@@ -87,8 +88,8 @@ def test_one_slice_is_mlora_linear_bitwise():
         assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
 
 
-def test_masked_operand_is_rewritten_for_every_plan():
-    """The shrink writes the whole masked operand (member entries and zeros),
+def test_windows_are_rewritten_for_every_plan():
+    """The shrink writes every token window whole (member entries and zeros),
     so a second plan with other adapter rows on the same workspace sees none
     of the first plan's entries."""
     ml = needs_gpu()
@@ -106,10 +107,12 @@ def test_masked_operand_is_rewritten_for_every_plan():
     assert ws.status() == 0
 
 
-@pytest.mark.parametrize("cfg", [WL.LLAMA8B_R16, WL.QWEN32B_R16], ids=lambda c: c.name)
-def test_fused_groups_full_size_sampled(cfg):
-    """The decode-step grouping (q|k|v, o, gate|up, down) at full size: 512
-    sampled outputs per call against the oracle, one output at a time."""
+@pytest.mark.parametrize("cfg,k", [(WL.LLAMA8B_R16, 1), (WL.LLAMA8B_HET, 1), (WL.QWEN32B_R16, 1), (WL.QWEN32B_R16, 2),
+                                   (WL.QWEN32B_R16, 4)], ids=lambda v: getattr(v, "name", f"k={v}"))
+def test_fused_groups_full_size_sampled(cfg, k):
+    """The decode-step grouping (q|k|v, o, gate|up, down) at full size, for
+    every layer workload and draft length: 512 sampled outputs per call
+    against the oracle, one output at a time."""
     ml = needs_gpu()
     ranks = WL.adapter_ranks(cfg)
     f = WL.bf16_to_f64
@@ -126,8 +129,8 @@ def test_fused_groups_full_size_sampled(cfg):
         ends = list(np.cumsum([w.shape[0] for w in Ws]))
         N, K = W.shape
         for mode, name in ((OL.DRAFT, "draft"), (OL.VERIFY, "verify")):
-            x = WL.activations(cfg, group[0], name)
-            idx = WL.row_adapters(cfg, name)
+            x = WL.activations(cfg, group[0], name, k=k)
+            idx = WL.row_adapters(cfg, name, k=k)
             M = x.shape[0]
             ws = ml.Workspace(ml.linear_sliced_workspace_bytes(M, N, K, cfg.n_adapters, len(group)))
             y = host_bf16_to_f64(ml.linear_sliced(dev_bf16(x), dev_bf16(W), ends, dev_bf16(A), dev_bf16(B),

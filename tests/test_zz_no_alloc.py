@@ -39,18 +39,34 @@ def _rel(a, b):
     return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
 
 
+def _oracle(case, mode):
+    import workloads as WL
+    from oracle import layer as OL
+    x, W, A, B, rk, idx = case
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731  (bf16 values, exact in float64)
+    y, _ = OL.mlora_linear(f(x), f(W), f(A), f(B), rk.cpu().numpy(), idx.cpu().numpy(), 2.0, mode)
+    return y
+
+
+def _rel_np(a, b):
+    a = a.float().cpu().numpy().astype(np.float64)
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
+
+
 @pytest.mark.parametrize("mode_name", ["draft", "verify"])
 def test_noalloc_matches_workspace_entry_point_on_two_calls(mode_name):
     ml = needs_gpu()
     mode = ml.DRAFT if mode_name == "draft" else ml.VERIFY
-    cases = [_case(1, 128, 1024, 4096, 16, 16), _case(2, 96, 4096, 1024, 8, 16)]
+    # the second case has more than 512 rows: the GEMM takes two token groups
+    cases = [_case(1, 128, 1024, 4096, 16, 16), _case(2, 700, 1024, 1024, 8, 16)]
     refs = []
     for x, W, A, B, rk, idx in cases:
         refs.append(ml.linear(x, W, A, B, rk, idx, 2.0, mode))
     outs = [ml.linear_noalloc(x, W, A, B, rk, idx, 2.0, mode) for (x, W, A, B, rk, idx) in cases]
     torch.cuda.synchronize()
-    for y, y_ref in zip(outs, refs):
+    for case, y, y_ref in zip(cases, outs, refs):
         assert _rel(y, y_ref) <= TOL
+        assert _rel_np(y, _oracle(case, mode)) <= TOL
 
 
 def test_noalloc_refuses_sizes_beyond_its_array():
