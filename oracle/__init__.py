@@ -22,7 +22,8 @@ Sources:
     speculative sampling (Leviathan, Kalman & Matias 2023; Chen et al. 2023)
     with an exact fixed-point residual draw (see ``oracle.accept``).
 
-Modules: ``oracle.layer`` (segment plan, shrink, layer output) and
-``oracle.accept`` (accept test, residual/bonus sample).  Every function is
-pinned by tests under ``-m "not gpu"``; none is marked "parity unpinned".
+Modules: ``oracle.layer`` (segment plan, shrink, layer output),
+``oracle.accept`` (accept test, residual/bonus sample) and ``oracle.softmax``
+(logits to probabilities, draft-token draw).  Every function is pinned by
+tests under ``-m "not gpu"``; none is marked "parity unpinned".
 """
