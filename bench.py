@@ -275,6 +275,10 @@ class StepWorkload:
                        for P in self.proj)
         ws_bytes = max(ws_bytes, ml.accept_workspace_bytes(B, k, cfg.vocab))
         self.ws = ml.Workspace(ws_bytes, device=device)
+        # The draft passes run beside the plan (second stream): a workspace of their own.
+        self.ws_draft = ml.Workspace(max(ml.linear_sliced_workspace_bytes(self.Md, P["N"], P["K"], 0, len(P["ends"]))
+                                         for P in self.proj), device=device)
+        torch.cuda.synchronize(device) if device.type == "cuda" else None
         self.seg = None
         self.w_bytes_per_pass = sum(2 * P["N"] * P["K"] for P in self.proj)
 
@@ -296,7 +300,7 @@ class StepWorkload:
             for P in self.proj:
                 out.append((f"draft{d}.{P['name']}", "draft", P, lambda P=P, d=d: ml.linear_sliced(
                     P["xd"][d], P["W"], P["ends"], None, None, None, None, cfg.scale, ml.DRAFT | ml.PREFETCH_WEIGHTS,
-                    ws=self.ws, y=P["yd"])))
+                    ws=self.ws_draft, y=P["yd"])))
         for P in self.proj:
             out.append((f"verify.{P['name']}", "verify", P, lambda P=P: ml.linear_sliced(
                 P["xv"], P["W"], P["ends"], P["A"], P["B"], self.rank_of, self.adx_v, cfg.scale,
@@ -483,6 +487,9 @@ class _NoLib:
     def Workspace(self, *a, **k):
         return None
 
+    def __getattr__(self, name):
+        raise RuntimeError(f"the reference arm does not call the library ({name})")
+
 
 # ---------------------------------------------------------------------------
 # GPU arm
@@ -548,7 +555,7 @@ def measure_layer(torch, ml, wl, stream, side, steps, peaks, flush):
         for _ in range(3):
             wl.step(side)
     stream.synchronize()
-    if wl.ws.status() != 0:
+    if wl.ws.status() != 0 or wl.ws_draft.status() != 0:
         raise RuntimeError(f"{wl.name}: device status bits raised during warm-up")
     n0 = ml.launch_count()
     graph = graph_of(torch, lambda: wl.step(side), stream)
@@ -558,7 +565,7 @@ def measure_layer(torch, ml, wl, stream, side, steps, peaks, flush):
     torch.cuda.synchronize()
     use_flush = wl.w_bytes_per_pass < 2 * L2_BYTES
     ms_step = time_replays(torch, graph, stream, steps, flush if use_flush else None)
-    if wl.ws.status() != 0:
+    if wl.ws.status() != 0 or wl.ws_draft.status() != 0:
         raise RuntimeError(f"{wl.name}: device status bits raised during the timed region")
     op_ms = per_op_durations(torch, wl.ops(with_base=True), stream, max(10, min(steps, 100)))
 

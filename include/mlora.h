@@ -38,10 +38,10 @@
  * mlora_workspace_init once after allocating it (and after any call that
  * returned MLORA_ERR_TIMEOUT).  Kernels leave the counters at zero when they
  * finish, so one workspace serves any sequence of calls on one stream.  Calls
- * that use the same workspace must not overlap in time (e.g. on two streams),
- * with one exception: draft-mode layer calls touch nothing in the workspace
- * but the status word, so they may overlap mlora_plan_segments on another
- * stream (a decode step can plan the verify pass while it drafts).
+ * that use the same workspace must not overlap in time (e.g. on two streams):
+ * layer calls of either mode may use its scratch (the stream-K GEMM keeps
+ * partial sums there).  A decode step that plans its verify pass on a second
+ * stream while it drafts gives the draft calls a workspace of their own.
  */
 #ifndef MLORA_H
 #define MLORA_H
@@ -90,6 +90,9 @@ typedef enum {
 #define MLORA_DEV_BAD_TOKEN   (1u << 3) /* a draft token outside [0, V): rejected at its position */
 #define MLORA_DEV_ZERO_MASS   (1u << 4) /* residual mass 0: drew from p_n, or emitted token 0     */
 #define MLORA_DEV_TIMEOUT     (1u << 5) /* a bounded wait inside a kernel gave up                 */
+#define MLORA_DEV_BAD_PLAN    (1u << 6) /* a plan entry read by a layer kernel was out of range (the
+                                           workspace's plan was overwritten, or made for other
+                                           sizes): the access was skipped, outputs are wrong    */
 
 /* Supported ranges. */
 #define MLORA_MAX_RANK 64          /* r_max <= 64, r_max % 8 == 0 */

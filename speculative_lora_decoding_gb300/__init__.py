@@ -38,6 +38,7 @@ DEV_BAD_PROB = 1 << 2
 DEV_BAD_TOKEN = 1 << 3
 DEV_ZERO_MASS = 1 << 4
 DEV_TIMEOUT = 1 << 5
+DEV_BAD_PLAN = 1 << 6
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmlora.so")
 HEADER_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mlora.h")
@@ -171,6 +172,8 @@ class Workspace:
         self.nbytes = int(nbytes)
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
         _check(_load().mlora_workspace_init(self.buf.data_ptr(), self.nbytes, _stream(stream)), "workspace_init")
+        # The zeroing is asynchronous on `stream`; calls may come on any stream.
+        (torch.cuda.current_stream(self.buf.device) if stream is None else stream).synchronize()
 
     @property
     def ptr(self) -> int:

@@ -80,6 +80,17 @@ __device__ __forceinline__ float clamp_prob(float f, bool &bad) {
 // Q(f) = floor(f * 2^40) for f in [0, 1].
 __device__ __forceinline__ uint64_t fixq(float f) { return __float2ull_rd(f * TWO_POW_40); }
 
+// Logits mode (LG): rows hold logits z and the probability of an entry is
+// expf(z - m) / S with the row's statistics st = (m, S) from row_stats, the
+// one expression softmax.cu uses everywhere (so the decisions equal the ones
+// taken on the probabilities mlora_softmax writes).  Otherwise rows hold
+// probabilities and are read as they are.
+template <bool LG>
+__device__ __forceinline__ float as_prob(float f, float2 st) {
+  if (LG) return expf(f - st.x) / st.y;
+  return f;
+}
+
 __device__ __forceinline__ uint64_t res_weight(uint64_t qp, uint64_t qq) { return qp > qq ? qp - qq : 0ull; }
 
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
@@ -120,19 +131,34 @@ __device__ __forceinline__ uint64_t block_excl_scan_u64(uint64_t v, uint64_t *sh
 // 256 j, j < 16 (each warp load is 128 contiguous bytes).  All loads are
 // issued before any value is used.  Entries at or past V read as 0: in
 // range, weight 0.
-__device__ __forceinline__ void load_chunk(const float *row, int v0, int V, int tid, float (&f)[PER_THREAD]) {
+template <bool LG>
+__device__ __forceinline__ void load_chunk(const float *row, int v0, int V, int tid, float (&f)[PER_THREAD],
+                                           float2 st) {
 #pragma unroll
   for (int j = 0; j < PER_THREAD; ++j) {
     const int v = v0 + tid + ACC_THREADS * j;
     f[j] = v < V ? __ldcs(row + v) : 0.f;
   }
+  if (LG) {
+#pragma unroll
+    for (int j = 0; j < PER_THREAD; ++j)
+      if (v0 + tid + ACC_THREADS * j < V) f[j] = as_prob<LG>(f[j], st);
+  }
 }
 
+// Statistics of row `row` (zeros when not in logits mode).
+template <bool LG>
+__device__ __forceinline__ float2 row_st(const float2 *st, size_t row) {
+  if (LG) return st[row];
+  return make_float2(0.f, 1.f);
+}
+
+template <bool LG>
 __global__ void __launch_bounds__(ACC_THREADS)
     accept_kernel(const float *__restrict__ p, const float *__restrict__ q, const int32_t *__restrict__ draft_tok,
                   const float *__restrict__ uni, int B, int k, int V, int chunks,
                   int32_t *__restrict__ out_tok, int32_t *__restrict__ accepted, uint32_t *counters,
-                  uint64_t *sums, uint32_t *status) {
+                  uint64_t *sums, uint32_t *status, const float2 *__restrict__ sp, const float2 *__restrict__ sq) {
   __shared__ uint64_t sh_scan[ACC_WARPS];
   __shared__ uint64_t sh_red[2][ACC_WARPS];
   __shared__ int sh_n, sh_last, sh_tok, sh_mode, sh_chunk;
@@ -149,7 +175,7 @@ __global__ void __launch_bounds__(ACC_THREADS)
 
   // Speculatively request this chunk of the bonus row p_k.
   float fp[PER_THREAD];
-  load_chunk(p + ((size_t)b * k1 + k) * V, v0, V, tid, fp);
+  load_chunk<LG>(p + ((size_t)b * k1 + k) * V, v0, V, tid, fp, row_st<LG>(sp, (size_t)b * k1 + k));
 
   // Step a5: the accept tests, position i on lane i of warp 0 (k <= 16).
   // The result is what the sequential rule gives: n = the first position
@@ -164,8 +190,10 @@ __global__ void __launch_bounds__(ACC_THREADS)
         f |= MLORA_DEV_BAD_TOKEN;
         pass = false;
       } else {
-        const float pi = sanitize_prob(p[((size_t)b * k1 + lane) * V + x], f);
-        const float qi = sanitize_prob(q[((size_t)b * k + lane) * V + x], f);
+        const float pi = sanitize_prob(
+            as_prob<LG>(p[((size_t)b * k1 + lane) * V + x], row_st<LG>(sp, (size_t)b * k1 + lane)), f);
+        const float qi = sanitize_prob(
+            as_prob<LG>(q[((size_t)b * k + lane) * V + x], row_st<LG>(sq, (size_t)b * k + lane)), f);
         const float ui = sanitize_uniform(uni[(size_t)b * k1 + lane], f);
         pass = (double)ui * (double)qi < (double)pi;
       }
@@ -196,8 +224,8 @@ __global__ void __launch_bounds__(ACC_THREADS)
     bad = false;
     s_tgt = 0;
     float fq[PER_THREAD];
-    load_chunk(p + ((size_t)b * k1 + n) * V, v0, V, tid, fp);
-    load_chunk(q + ((size_t)b * k + n) * V, v0, V, tid, fq);
+    load_chunk<LG>(p + ((size_t)b * k1 + n) * V, v0, V, tid, fp, row_st<LG>(sp, (size_t)b * k1 + n));
+    load_chunk<LG>(q + ((size_t)b * k + n) * V, v0, V, tid, fq, row_st<LG>(sq, (size_t)b * k + n));
 #pragma unroll
     for (int j = 0; j < PER_THREAD; ++j) {
       const uint64_t qp = fixq(clamp_prob(fp[j], bad));
@@ -298,13 +326,15 @@ __global__ void __launch_bounds__(ACC_THREADS)
     const float *prow = p + ((size_t)b * k1 + n) * V;
     const float *qrow = q + ((size_t)b * k + (residual ? n : 0)) * V;
     const bool use_q = mode == 0;
+    const float2 stp = row_st<LG>(sp, (size_t)b * k1 + n);
+    const float2 stq = row_st<LG>(sq, (size_t)b * k + (residual ? n : 0));
     uint64_t w[PER_THREAD];
     {
       float a[PER_THREAD], bq[PER_THREAD];
 #pragma unroll
       for (int j = 0; j < PER_THREAD; ++j) {
-        a[j] = cv0 + j < V ? __ldcg(prow + cv0 + j) : 0.f;
-        bq[j] = (use_q && cv0 + j < V) ? __ldcg(qrow + cv0 + j) : 0.f;
+        a[j] = cv0 + j < V ? as_prob<LG>(__ldcg(prow + cv0 + j), stp) : 0.f;
+        bq[j] = (use_q && cv0 + j < V) ? as_prob<LG>(__ldcg(qrow + cv0 + j), stq) : 0.f;
       }
       bool dummy = false;
 #pragma unroll
@@ -406,10 +436,12 @@ __device__ __forceinline__ void ring_abort(RingShared &rs, uint32_t *status) {
 
 // blk: [B * chunks units][8 blocks][2] uint64 (residual, target);
 // n_out: [B] accepted count, written by the unit holding chunk 0.
+template <bool LG>
 __global__ void __launch_bounds__(RING_THREADS, 1)
     accept_stream_kernel(const float *__restrict__ p, const float *__restrict__ q,
                          const int32_t *__restrict__ draft_tok, const float *__restrict__ uni, int B, int k, int V,
-                         int chunks, uint64_t *__restrict__ blk, int32_t *__restrict__ n_out, uint32_t *status) {
+                         int chunks, uint64_t *__restrict__ blk, int32_t *__restrict__ n_out, uint32_t *status,
+                         const float2 *__restrict__ sp, const float2 *__restrict__ sq) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = align_smem_1024(smem_raw);
   float *stages = reinterpret_cast<float *>(smem);
@@ -518,8 +550,10 @@ __global__ void __launch_bounds__(RING_THREADS, 1)
           f |= MLORA_DEV_BAD_TOKEN;
           pass = false;
         } else {
-          const float pi = sanitize_prob(p[((size_t)b * k1 + pos) * V + x], f);
-          const float qi = sanitize_prob(q[((size_t)b * k + pos) * V + x], f);
+          const float pi = sanitize_prob(
+              as_prob<LG>(p[((size_t)b * k1 + pos) * V + x], row_st<LG>(sp, (size_t)b * k1 + pos)), f);
+          const float qi = sanitize_prob(
+              as_prob<LG>(q[((size_t)b * k + pos) * V + x], row_st<LG>(sq, (size_t)b * k + pos)), f);
           const float ui = sanitize_uniform(uni[(size_t)b * k1 + pos], f);
           pass = (double)ui * (double)qi < (double)pi;
         }
@@ -576,9 +610,11 @@ __global__ void __launch_bounds__(RING_THREADS, 1)
     const float4 *a4 = reinterpret_cast<const float4 *>(stages + (size_t)s0 * STAGE_FLOATS);
     const float4 *c4 = reinterpret_cast<const float4 *>(stages + (size_t)s1 * STAGE_FLOATS);
     float pa[16], qa[16];
+    bool inr[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e4 = warp * (BLOCK / 4) + lane + 32 * j;  // entries past V read as 0 (weight 0)
+      inr[j] = e4 < len4;
       const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
       const float4 a = e4 < len4 ? a4[e4] : z4;
       const float4 cq = (resid && e4 < len4) ? c4[e4] : z4;
@@ -589,6 +625,19 @@ __global__ void __launch_bounds__(RING_THREADS, 1)
     if (lane == 0) {
       mbar_arrive(&rs.empty[s0]);
       if (resid) mbar_arrive(&rs.empty[s1]);
+    }
+    if (LG) {
+      // Logits to probabilities (entries past V stay 0).
+      const int b = u / chunks, prow = resid ? rs.n[i] : k;
+      const float2 stp = sp[(size_t)b * k1 + prow];
+      const float2 stq = resid ? sq[(size_t)b * k + prow] : make_float2(0.f, 1.f);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        if (inr[e >> 2]) {
+          pa[e] = as_prob<LG>(pa[e], stp);
+          if (resid) qa[e] = as_prob<LG>(qa[e], stq);
+        }
+      }
     }
     uint32_t mx = 0, sy = 0, sz = 0, my = 0, mz = 0;
 #pragma unroll
@@ -645,11 +694,13 @@ __global__ void __launch_bounds__(RING_THREADS, 1)
 // weights (residual, else target), T = floor(U * S / 2^32), the chunk
 // holding T (32 chunks per round, lane e summing chunk e's 8 blocks), the
 // block within it, then the block's entries, 16 contiguous per lane.
+template <bool LG>
 __global__ void __launch_bounds__(DRAW_WARPS * 32)
     accept_draw_kernel(const float *__restrict__ p, const float *__restrict__ q,
                        const int32_t *__restrict__ draft_tok, const float *__restrict__ uni, int B, int k, int V,
                        int chunks, const uint64_t *blk, const int32_t *n_in, int32_t *__restrict__ out_tok,
-                       int32_t *__restrict__ accepted, uint32_t *status) {
+                       int32_t *__restrict__ accepted, uint32_t *status, const float2 *__restrict__ sp,
+                       const float2 *__restrict__ sq) {
   grid_launch_dependents();
   grid_dependency_wait();
   const int lane = threadIdx.x & 31;
@@ -743,6 +794,17 @@ __global__ void __launch_bounds__(DRAW_WARPS * 32)
           a[4 * j + 0] = t4.x, a[4 * j + 1] = t4.y, a[4 * j + 2] = t4.z, a[4 * j + 3] = t4.w;
           c[4 * j + 0] = u4.x, c[4 * j + 1] = u4.y, c[4 * j + 2] = u4.z, c[4 * j + 3] = u4.w;
         }
+        if (LG) {
+          const float2 stp = sp[(size_t)b * k1 + n];
+          const float2 stq = use_q ? sq[(size_t)b * k + n] : make_float2(0.f, 1.f);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (v0 + j < V) {
+              a[j] = as_prob<LG>(a[j], stp);
+              if (use_q) c[j] = as_prob<LG>(c[j], stq);
+            }
+          }
+        }
         uint64_t wv[16];
         uint64_t mine = 0;
         bool dummy = false;
@@ -801,9 +863,11 @@ AcceptShape accept_shape(int B, int k, int V, int num_sms) {
   return s;
 }
 
-cudaError_t launch_accept(const float *p, const float *q, const int32_t *draft_tok, const float *u, int B, int k, int V,
-                          int32_t *out_tok, int32_t *accepted, uint32_t *counters, void *scratch, uint32_t *status,
-                          const AcceptShape &sh, cudaStream_t s) {
+template <bool LG>
+static cudaError_t launch_accept_t(const float *p, const float *q, const int32_t *draft_tok, const float *u, int B,
+                                   int k, int V, int32_t *out_tok, int32_t *accepted, uint32_t *counters, void *scratch,
+                                   uint32_t *status, const AcceptShape &sh, const float2 *sp, const float2 *sq,
+                                   cudaStream_t s) {
   const bool vec = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(p) & 15) == 0) &&
                    ((reinterpret_cast<uintptr_t>(q) & 15) == 0);
   uint64_t *sums = reinterpret_cast<uint64_t *>(scratch);
@@ -813,23 +877,33 @@ cudaError_t launch_accept(const float *p, const float *q, const int32_t *draft_t
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidValue;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-      e = cudaFuncSetAttribute(accept_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RING_SMEM);
+      e = cudaFuncSetAttribute(accept_stream_kernel<LG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RING_SMEM);
       if (e != cudaSuccess) return e;
       attr_done[dev] = 1;
     }
     int32_t *n_buf = reinterpret_cast<int32_t *>(sums + (size_t)B * sh.slices * RING_CONSUMERS * 2);
-    e = launch_pdl(accept_stream_kernel, dim3((unsigned)sh.ring_grid), dim3(RING_THREADS), RING_SMEM, s, p, q,
-                   draft_tok, u, B, k, V, sh.slices, sums, n_buf, status);
+    e = launch_pdl(accept_stream_kernel<LG>, dim3((unsigned)sh.ring_grid), dim3(RING_THREADS), RING_SMEM, s, p, q,
+                   draft_tok, u, B, k, V, sh.slices, sums, n_buf, status, sp, sq);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(accept_draw_kernel, dim3((unsigned)((B + DRAW_WARPS - 1) / DRAW_WARPS)), dim3(DRAW_WARPS * 32), 0,
-                   s, p, q, draft_tok, u, B, k, V, sh.slices, (const uint64_t *)sums, (const int32_t *)n_buf, out_tok,
-                   accepted, status);
+    e = launch_pdl(accept_draw_kernel<LG>, dim3((unsigned)((B + DRAW_WARPS - 1) / DRAW_WARPS)),
+                   dim3(DRAW_WARPS * 32), 0, s, p, q, draft_tok, u, B, k, V, sh.slices, (const uint64_t *)sums,
+                   (const int32_t *)n_buf, out_tok, accepted, status, sp, sq);
   } else {
     const long long grid = (long long)B * sh.slices;
-    e = launch_pdl(accept_kernel, dim3((unsigned)grid), dim3(ACC_THREADS), 0, s, p, q, draft_tok, u, B, k, V,
-                   sh.slices, out_tok, accepted, counters, sums, status);
+    e = launch_pdl(accept_kernel<LG>, dim3((unsigned)grid), dim3(ACC_THREADS), 0, s, p, q, draft_tok, u, B, k, V,
+                   sh.slices, out_tok, accepted, counters, sums, status, sp, sq);
   }
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_accept(const float *p, const float *q, const int32_t *draft_tok, const float *u, int B, int k, int V,
+                          int32_t *out_tok, int32_t *accepted, uint32_t *counters, void *scratch, uint32_t *status,
+                          const AcceptShape &sh, const float2 *stats_p, const float2 *stats_q, cudaStream_t s) {
+  if (stats_p && stats_q)
+    return launch_accept_t<true>(p, q, draft_tok, u, B, k, V, out_tok, accepted, counters, scratch, status, sh,
+                                 stats_p, stats_q, s);
+  return launch_accept_t<false>(p, q, draft_tok, u, B, k, V, out_tok, accepted, counters, scratch, status, sh, nullptr,
+                                nullptr, s);
 }
 
 }  // namespace mlora

@@ -181,7 +181,8 @@ mlora_status mlora_shrink(const mlora_bf16 *x, int M, int K, const mlora_bf16 *A
   const int sms = device_sms();
   if (sms <= 0) return MLORA_ERR_CUDA;
   cudaError_t e =
-      launch_shrink(x, M, K, A_stack, n_adapters, r_max, plan, T, r_max, true, sms, nullptr, 1.f, 1, (cudaStream_t)stream);
+      launch_shrink(x, M, K, A_stack, n_adapters, r_max, plan, T, r_max, true, sms, nullptr, 1.f, 1,
+                    reinterpret_cast<uint32_t *>((uint8_t *)workspace + WS_STATUS_OFF), (cudaStream_t)stream);
   return cuda_status(e);
 }
 
@@ -227,9 +228,9 @@ static mlora_status linear_impl(const mlora_bf16 *x, int M, int K, const mlora_b
     }
     // Token rows in adapter-sorted order for the GEMM, then T and the
     // windows of the tensor-core expand.
-    e = launch_gather_rows(x, M, K, plan + P.perm, xs, sms, s);
+    e = launch_gather_rows(x, M, K, plan + P.perm, xs, sms, status, s);
     if (e != cudaSuccess) return MLORA_ERR_CUDA;
-    e = launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, tw, scale, S, s);
+    e = launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, tw, scale, S, status, s);
     if (e != cudaSuccess) return MLORA_ERR_CUDA;
   }
   GemmLaunch g;

@@ -66,11 +66,15 @@ __device__ __forceinline__ void zero_tail_columns_sw32(uint8_t *tile, int c0, in
 // row n0, with the windows clipped to token columns [m0, m0 + mcols).  Lane 0
 // waits and issues; every lane keeps the same stage / phase / issued count.
 // Returns false if a wait gave up.
+// A record out of range (n_ad adapters, tw_rows rows in the window buffer)
+// means the plan was overwritten or made for other sizes: the block is
+// dropped and MLORA_DEV_BAD_PLAN raised.
 __device__ __forceinline__ bool expand_produce(const int32_t *blocks, int blo, int bhi, int m0, int mcols, int n0,
                                                int N, const CUtensorMap *tmap_b, const uint16_t *tw, uint8_t *ring,
                                                int stage_bytes, int S, uint64_t *full, uint64_t *empty,
                                                ExpandStage *meta, int4 *chunk, int &stage, uint32_t &phase,
-                                               int &issued, volatile int *abort, uint64_t pol, int lane) {
+                                               int &issued, volatile int *abort, uint64_t pol, int lane, int n_ad,
+                                               long long tw_rows, uint32_t *status) {
   bool ok = true;
   for (int c0 = blo; c0 < bhi && ok; c0 += EXP_CHUNK) {
     const int n = min(EXP_CHUNK, bhi - c0);
@@ -79,8 +83,12 @@ __device__ __forceinline__ bool expand_produce(const int32_t *blocks, int blo, i
       const int4 e0 = *reinterpret_cast<const int4 *>(blocks + (size_t)(c0 + lane) * EXP_WORDS);
       const int4 e1 = *reinterpret_cast<const int4 *>(blocks + (size_t)(c0 + lane) * EXP_WORDS + 4);
       const int w0 = e1.x, W = e1.y;
+      const bool valid = (unsigned)e0.x < (unsigned)n_ad && (e0.y & 15) == 0 && (unsigned)e0.y < 64u &&
+                         e0.z >= 1 && e0.z <= 16 && e0.w >= 0 && w0 >= 0 && (w0 & 15) == 0 && W >= 0 &&
+                         (W & 15) == 0 && (long long)e0.w + W <= tw_rows;
+      if (!valid) raise_status(status, MLORA_DEV_BAD_PLAN);
       const int cs = max(w0, m0), ce = min(w0 + W, m0 + mcols);
-      const int rows = ce > cs ? ce - cs : 0;
+      const int rows = (valid && ce > cs) ? ce - cs : 0;
       // {adapter, j0 | rank columns << 8, first window row, column | rows << 16}
       chunk[lane] = make_int4(e0.x, e0.y | (e0.z << 8), e0.w + (rows ? cs - w0 : 0), rows ? ((cs - m0) | (rows << 16)) : 0);
     }

@@ -561,7 +561,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
     if (bhi > blo) {
       const bool ok = expand_produce(args.plan + L.slices, blo, bhi, m0, args.Mb, n_tile * BLOCK_N, args.N, &tmap_b,
                                      args.tw + (size_t)slice * args.tw_slice, sp.stage0, stage_bytes, S, sp.full,
-                                     sp.empty, sp.meta, sp.chunk, stage, phase, issued, abort_flag, pol_w, lane);
+                                     sp.empty, sp.meta, sp.chunk, stage, phase, issued, abort_flag, pol_w, lane,
+                                     args.n_ad, (long long)(args.tw_slice / 16), args.status);
       if (!ok && lane == 0) signal_abort(sp, args.status);
     }
     if (lane == 0 && *abort_flag) {
@@ -685,7 +686,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
   const bool verify = args.mode == MLORA_VERIFY && !args.sorted;
   // Output row of accumulator column c: with sorted rows, perm[m0 + c].
   const int32_t *perm = args.sorted ? args.plan + L.perm : nullptr;
-  auto out_row = [&](int c) -> size_t { return perm ? (size_t)__ldg(perm + m0 + c) : (size_t)(m0 + c); };
+  // A permutation entry out of range (a plan overwritten or made for other
+  // sizes) maps to -1: the store is skipped and MLORA_DEV_BAD_PLAN raised.
+  auto out_row = [&](int c) -> long long {
+    if (!perm) return (long long)(m0 + c);
+    const int r = __ldg(perm + m0 + c);
+    if ((unsigned)r < (unsigned)args.M) return r;
+    raise_status(args.status, MLORA_DEV_BAD_PLAN);
+    return -1;
+  };
 
   if (C == 1) {
     if (epi && have_acc) {
@@ -696,12 +705,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
           tmem_ld_acc_x32(taddr + ch * CHUNK, r);
           // Lane j holds the output row of column ch * 32 + j.
           const int myc = ch * CHUNK + lane;
-          const int myrow = myc < mcount ? (int)out_row(myc) : 0;
+          const int myrow = myc < mcount ? (int)out_row(myc) : -1;
 #pragma unroll
           for (int j = 0; j < CHUNK; ++j) {
             const int col = ch * CHUNK + j;
             const int row = __shfl_sync(0xffffffffu, myrow, j);
-            if (n < args.N && col < mcount) args.y[(size_t)row * args.N + n] = float_to_bf16_bits(__uint_as_float(r[j]));
+            if (n < args.N && col < mcount && row >= 0)
+              args.y[(size_t)row * args.N + n] = float_to_bf16_bits(__uint_as_float(r[j]));
           }
         }
       } else {
@@ -726,7 +736,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
     // One round when the whole accumulator fits the freed stage ring and no
     // bucket walk needs the ring afterwards; otherwise 32 columns at a time
     // through the double-buffered reduction tile.
-    const bool oneshot = !verify && (size_t)args.Mb * BLOCK_N * 4 <= ring;
+    // (The epilogue writes whole 32-column chunks: round Mb up.)
+    const bool oneshot = !verify && (size_t)((args.Mb + CHUNK - 1) / CHUNK * CHUNK) * BLOCK_N * 4 <= ring;
     if (oneshot) {
       float *acc_all = reinterpret_cast<float *>(sp.stage0);  // [Mb][128], one column of 128 rows after another
       const uint32_t ring_local = smem_addr(sp.stage0);
@@ -749,7 +760,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
       cluster_sync_all();
       if (epi)
         cluster_reduce_rows_c(C, peer, 0u, r0, R, mcount, et, [&](int c, int i, float4 v) {
-          store_bf16x4(args.y, args.N, out_row(c), n_tile * BLOCK_N + r0 + i, v);
+          const long long row = out_row(c);
+          if (row >= 0) store_bf16x4(args.y, args.N, (size_t)row, n_tile * BLOCK_N + r0 + i, v);
         });
     } else {
       const uint32_t red_local = smem_addr(sp.red);
@@ -779,7 +791,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
                                   if (verify) {
                                     *reinterpret_cast<float4 *>(&fin[col * R + i]) = v;
                                   } else {
-                                    store_bf16x4(args.y, args.N, out_row(col), n_tile * BLOCK_N + r0 + i, v);
+                                    const long long row = out_row(col);
+                                    if (row >= 0) store_bf16x4(args.y, args.N, (size_t)row, n_tile * BLOCK_N + r0 + i, v);
                                   }
                                 });
         }

@@ -220,7 +220,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         if (ns > 0)
           ok = expand_produce(args.plan + L.slices, 0, ns, 0, args.Mb, t * SK_BN, args.N, &tmap_b,
                               args.tw + (size_t)sk_slice_of(args, t * SK_BN) * args.tw_slice, ring, stage_bytes, S,
-                              full, empty, meta, chunk, stage, phase, issued, ab, pol_w, lane);
+                              full, empty, meta, chunk, stage, phase, issued, ab, pol_w, lane, args.n_ad,
+                              (long long)(args.tw_slice / 16), args.status);
       }
       if (lane == 0 && ok) issue_kblocks(t, split, kb1);
       sync_state();
@@ -461,13 +462,22 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             }
             // Output row of column cb + j: perm[cb + j] with sorted rows (lane
             // j fetches it), else cb + j.
+            // An entry out of range (a plan overwritten or made for other
+            // sizes) skips the store and raises MLORA_DEV_BAD_PLAN.
             const int myc = cb + lane;
-            const int myrow = perm ? (myc < args.M ? __ldg(perm + myc) : 0) : myc;
+            int myrow = myc;
+            if (perm) {
+              myrow = myc < args.M ? __ldg(perm + myc) : -1;
+              if (myc < args.M && (unsigned)myrow >= (unsigned)args.M) {
+                raise_status(args.status, MLORA_DEV_BAD_PLAN);
+                myrow = -1;
+              }
+            }
             uint16_t *yn = args.y + n;
 #pragma unroll
             for (int j = 0; j < SK_CHUNK; ++j) {
               const int row = __shfl_sync(0xffffffffu, myrow, j);
-              if (n < args.N && (whole || cb + j < q1)) yn[(size_t)row * args.N] = float_to_bf16_bits(v[j]);
+              if (n < args.N && (whole || cb + j < q1) && row >= 0) yn[(size_t)row * args.N] = float_to_bf16_bits(v[j]);
             }
           }
           if (fetch) named_bar_sync(1, 128);  // the ring is refilled only after every thread read it

@@ -41,7 +41,7 @@ cudaError_t launch_plan(const int32_t *adapter_idx, int M, const int32_t *rank_o
 // The verify pass's token rows in adapter-sorted order: xs[p] = x[perm[p]]
 // for p < M (bf16 [M, K]).
 cudaError_t launch_gather_rows(const uint16_t *x, int M, int K, const int32_t *perm, uint16_t *xs, int num_sms,
-                               cudaStream_t s);
+                               uint32_t *status, cudaStream_t s);
 
 // Step a2: T[m, j] for j < rank (fp32, row stride t_stride), for n_slices
 // output slices (A: [n_slices][n_ad][r_max][K]; T: [n_slices][M][t_stride]).
@@ -51,7 +51,7 @@ cudaError_t launch_gather_rows(const uint16_t *x, int M, int K, const int32_t *p
 // common.cuh): scale * T on member rows, 0 elsewhere.
 cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, int n_ad, int r_max,
                           const int32_t *plan, float *T, int t_stride, bool zero_first, int num_sms, uint16_t *tw,
-                          float scale, int n_slices, cudaStream_t s);
+                          float scale, int n_slices, uint32_t *status, cudaStream_t s);
 
 // Steps a3 + a4: base GEMM on tcgen05 with the expand epilogue.
 struct GemmShape {

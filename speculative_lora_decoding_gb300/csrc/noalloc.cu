@@ -100,7 +100,8 @@ extern "C" MLORA_API mlora_status mlora_linear_noalloc(const mlora_bf16 *x, int 
   if (verify) {
     if (launch_plan(adapter_idx, M, rank_of, n_ad, r_max, plan, status, s) != cudaSuccess)
       return MLORA_ERR_CUDA;
-    if (launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, nullptr, 1.f, 1, s) != cudaSuccess)
+    if (launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, nullptr, 1.f, 1, status, s) !=
+        cudaSuccess)
       return MLORA_ERR_CUDA;
   }
   GemmLaunch g;

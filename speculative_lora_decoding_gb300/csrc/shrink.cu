@@ -83,7 +83,7 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[32]) {
 __global__ void __launch_bounds__(SHRINK_THREADS, SHRINK_MIN_BLOCKS)
     shrink_kernel(const uint16_t *__restrict__ x, int M, int K, const uint16_t *__restrict__ A_all, int n_ad, int r_max,
                   const int32_t *__restrict__ plan, float *__restrict__ T_all, int t_stride,
-                  uint16_t *__restrict__ tw_all, float scale, int n_slices) {
+                  uint16_t *__restrict__ tw_all, float scale, int n_slices, uint32_t *status) {
   __shared__ float red[SHRINK_WARPS][SHRINK_J * SHRINK_TOK];
   // Wait for the preceding kernel first, then let the GEMM that follows
   // launch: by then everything the GEMM's mainloop reads (x, W) is complete,
@@ -95,16 +95,22 @@ __global__ void __launch_bounds__(SHRINK_THREADS, SHRINK_MIN_BLOCKS)
   const int total_items = plan[L.hdr + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kchunks = K >> 3;  // 16-byte pieces per row
-  const size_t tw_slice = max_window_rows(M, n_ad) * 16;  // bf16 elements of one slice's operand buffer
+  const size_t tw_rows = max_window_rows(M, n_ad);
+  const size_t tw_slice = tw_rows * 16;  // bf16 elements of one slice's operand buffer
+  const int n_exp = plan[L.hdr + 4];
 
   if (tw_all) {
     // Zero halves: (slice, block, window row i, half h) not written by an item.
-    const int n_exp = plan[L.hdr + 4];
     for (int bu = blockIdx.x; bu < n_exp * n_slices; bu += gridDim.x) {
       const int sl = bu / n_exp, b = bu - sl * n_exp;
       const int4 e0 = *reinterpret_cast<const int4 *>(plan + L.slices + (size_t)b * EXP_WORDS);
       const int4 e1 = *reinterpret_cast<const int4 *>(plan + L.slices + (size_t)b * EXP_WORDS + 4);
       const int a = e0.x, j0 = e0.y, win = e0.w, w0 = e1.x, W = e1.y;
+      // A record out of range (a plan overwritten or made for other sizes) is skipped.
+      if ((unsigned)a >= (unsigned)n_ad || win < 0 || W < 0 || (size_t)win + W > tw_rows) {
+        if (threadIdx.x == 0) raise_status(status, MLORA_DEV_BAD_PLAN);
+        continue;
+      }
       const int s0 = plan[L.seg_offsets + a], s1 = plan[L.seg_offsets + a + 1];
       const int r = plan[L.rank_eff + a];
       uint16_t *tw = tw_all + (size_t)sl * tw_slice + (size_t)win * 16;
@@ -129,6 +135,15 @@ __global__ void __launch_bounds__(SHRINK_THREADS, SHRINK_MIN_BLOCKS)
     const int a = h.x, j0 = h.y & 0xFF, nrow = (h.y >> 8) & 0xFF, ntok = h.y >> 16;
     const int pos0 = h.z, blk0 = h.w;
     const int rows[SHRINK_TOK] = {rw.x, rw.y, rw.z, rw.w};
+    // A record out of range (a plan overwritten or made for other sizes) is skipped.
+    bool rec_ok = (unsigned)a < (unsigned)n_ad && j0 + nrow <= r_max && nrow <= SHRINK_J && ntok <= SHRINK_TOK &&
+                  pos0 >= 0 && pos0 + ntok <= M;
+#pragma unroll
+    for (int t = 0; t < SHRINK_TOK; ++t) rec_ok &= t >= ntok || (unsigned)rows[t] < (unsigned)M;
+    if (!rec_ok) {
+      if (threadIdx.x == 0) raise_status(status, MLORA_DEV_BAD_PLAN);
+      continue;
+    }
 
     const uint16_t *Abase = A + ((size_t)a * r_max + j0) * (size_t)K;
     float acc[SHRINK_J * SHRINK_TOK];
@@ -190,11 +205,16 @@ __global__ void __launch_bounds__(SHRINK_THREADS, SHRINK_MIN_BLOCKS)
         if (tw) {
           // Member row of the window of block (j0 + j) / 16 of adapter a.
           const int b = blk0 + (j0 + j) / 16;
-          const int win = plan[L.slices + (size_t)b * EXP_WORDS + 3];
-          const int w0 = plan[L.slices + (size_t)b * EXP_WORDS + 4];
+          const int win = b >= 0 && b < n_exp ? plan[L.slices + (size_t)b * EXP_WORDS + 3] : -1;
+          const int w0 = b >= 0 && b < n_exp ? plan[L.slices + (size_t)b * EXP_WORDS + 4] : 0;
+          const int W = b >= 0 && b < n_exp ? plan[L.slices + (size_t)b * EXP_WORDS + 5] : 0;
           const int c = (j0 + j) % 16, i = pos0 + t - w0;
-          const int pc = (((c >> 3) ^ ((i >> 2) & 1)) << 3) | (c & 7);  // swizzled column
-          tw[((size_t)win + i) * 16 + pc] = float_to_bf16_bits(scale * v);
+          if (win >= 0 && i >= 0 && i < W && (size_t)win + W <= tw_rows) {
+            const int pc = (((c >> 3) ^ ((i >> 2) & 1)) << 3) | (c & 7);  // swizzled column
+            tw[((size_t)win + i) * 16 + pc] = float_to_bf16_bits(scale * v);
+          } else {
+            raise_status(status, MLORA_DEV_BAD_PLAN);
+          }
         }
       }
     }
@@ -206,7 +226,7 @@ __global__ void __launch_bounds__(SHRINK_THREADS, SHRINK_MIN_BLOCKS)
 // thread).  Waits for the plan, then lets the shrink kernel launch.
 __global__ void __launch_bounds__(256)
     gather_rows_kernel(const uint16_t *__restrict__ x, int M, int K, const int32_t *__restrict__ perm,
-                       uint16_t *__restrict__ xs) {
+                       uint16_t *__restrict__ xs, uint32_t *status) {
   grid_dependency_wait();
   grid_launch_dependents();
   const int kv = K >> 3;
@@ -221,8 +241,13 @@ __global__ void __launch_bounds__(256)
       dst[u] = -1;
       if (i < total) {
         const int p = (int)(i / kv), c = (int)(i - (long long)p * kv);
-        v[u] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)perm[p] * K) + c);
-        dst[u] = (long long)p * kv + c;
+        const int m = perm[p];
+        if ((unsigned)m < (unsigned)M) {
+          v[u] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)m * K) + c);
+          dst[u] = (long long)p * kv + c;
+        } else {
+          raise_status(status, MLORA_DEV_BAD_PLAN);  // a permutation entry out of range: skipped
+        }
       }
     }
 #pragma unroll
@@ -232,17 +257,17 @@ __global__ void __launch_bounds__(256)
 }
 
 cudaError_t launch_gather_rows(const uint16_t *x, int M, int K, const int32_t *perm, uint16_t *xs, int num_sms,
-                               cudaStream_t s) {
+                               uint32_t *status, cudaStream_t s) {
   const long long pieces = (long long)M * (K >> 3);
   const long long want = (pieces + 4 * 256 - 1) / (4 * 256);
   const int grid = (int)max(1LL, min(want, (long long)num_sms * 4));
-  cudaError_t e = launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, s, x, M, K, perm, xs);
+  cudaError_t e = launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, s, x, M, K, perm, xs, status);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, int n_ad, int r_max,
                           const int32_t *plan, float *T, int t_stride, bool zero_first, int num_sms, uint16_t *tw,
-                          float scale, int n_slices, cudaStream_t s) {
+                          float scale, int n_slices, uint32_t *status, cudaStream_t s) {
   if (zero_first) {
     cudaError_t e = cudaMemsetAsync(T, 0, (size_t)n_slices * M * t_stride * sizeof(float), s);
     if (e != cudaSuccess) return e;
@@ -254,7 +279,7 @@ cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, in
   // these CTAs, and an SM holding two of them has no registers left for it.
   const int grid = (int)max(1LL, min(bound * n_slices, (long long)num_sms));
   cudaError_t e = launch_pdl(shrink_kernel, dim3(grid), dim3(SHRINK_THREADS), 0, s, x, M, K, A, n_ad, r_max, plan, T,
-                             t_stride, tw, scale, n_slices);
+                             t_stride, tw, scale, n_slices, status);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
