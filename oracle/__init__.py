@@ -23,7 +23,8 @@ Sources:
     with an exact fixed-point residual draw (see ``oracle.accept``).
 
 Modules: ``oracle.layer`` (segment plan, shrink, layer output),
-``oracle.accept`` (accept test, residual/bonus sample) and ``oracle.softmax``
-(logits to probabilities, draft-token draw).  Every function is pinned by
+``oracle.accept`` (accept test, residual/bonus sample), ``oracle.softmax``
+(logits to probabilities, draft-token draw) and ``oracle.gate`` (the run-time
+draft gate's cost model).  Every function is pinned by
 tests under ``-m "not gpu"``; none is marked "parity unpinned".
 """
