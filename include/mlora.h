@@ -310,6 +310,81 @@ MLORA_API mlora_status mlora_verify_accept(const float *p_target, const float *q
                                  const float *uniforms, int B, int k, int V, int32_t *out_tok, int32_t *accepted,
                                  void *workspace, size_t ws_bytes, mlora_stream stream);
 
+/* The same step taking logits instead of probabilities: z_target [B, k+1, V]
+ * are the LoRA-on pass's logits, z_draft [B, k, V] the LoRA-off passes'.  The
+ * softmax is fused into the accept kernels: every probability they read is
+ * expf(z - m) / S of its row, with the row statistics of mlora_softmax, so the
+ * decisions are exactly those mlora_verify_accept takes on the probabilities
+ * mlora_softmax writes for the same logits.  Everything else as
+ * mlora_verify_accept; workspace mlora_accept_workspace_bytes(B, k, V).  The
+ * pages give no formula for the distributions; the softmax of the logits at
+ * temperature 1 is the plain reading of a language model's output. */
+MLORA_API mlora_status mlora_verify_accept_logits(const float *z_target, const float *z_draft,
+                                                  const int32_t *draft_tok, const float *uniforms, int B, int k, int V,
+                                                  int32_t *out_tok, int32_t *accepted, void *workspace,
+                                                  size_t ws_bytes, mlora_stream stream);
+
+/* ------------------------------------------------------------------------- */
+/* Softmax and the draft draw (the steps on either side of the accept step)  */
+/* ------------------------------------------------------------------------- */
+
+/* p[r, v] = expf(z[r, v] - m_r) / S_r for `rows` rows of V fp32 logits, with
+ * m_r the row maximum and S_r the row's sum of expf(z - m_r) (accumulated in a
+ * fixed order in fp32: the results are deterministic).  CUDA's expf, IEEE
+ * division.  The InvisibleLoRA abstract has both passes end in a distribution
+ * over the vocabulary; the softmax of the logits is the plain reading.
+ *   z, p   fp32 [rows, V] device (p may not alias z); rows in [1, 65536],
+ *          V in [1, 2^24]; workspace mlora_softmax_workspace_bytes(rows, V). */
+MLORA_API size_t mlora_softmax_workspace_bytes(int rows, int V);
+MLORA_API mlora_status mlora_softmax(const float *z, int rows, int V, float *p, void *workspace, size_t ws_bytes,
+                                     mlora_stream stream);
+
+/* The draft token of each request from its LoRA-off logits (the InvisibleLoRA
+ * abstract: the LoRA-off pass proposes the next token for every request):
+ * q = softmax(z_draft[b]) as mlora_softmax computes it, then the exact integer
+ * inverse CDF of Q(q) = floor(q * 2^40) with U = floor(uniforms[b] * 2^32),
+ * the same draw the accept step uses for its residual.
+ *   z_draft  fp32 [B, V] logits;  uniforms fp32 [B];  draft_tok int32 [B] out;
+ *   q_out    fp32 [B, V] out, or NULL: the probabilities the draw used (what
+ *            mlora_verify_accept takes as q; mlora_verify_accept_logits takes
+ *            the logits instead).
+ * Uniforms outside [0, 1) are clamped as in the accept step
+ * (MLORA_DEV_BAD_PROB); a row of zero mass draws token 0 (MLORA_DEV_ZERO_MASS).
+ * Workspace mlora_draft_sample_workspace_bytes(B, V). */
+MLORA_API size_t mlora_draft_sample_workspace_bytes(int B, int V);
+MLORA_API mlora_status mlora_draft_sample(const float *z_draft, int B, int V, const float *uniforms,
+                                          int32_t *draft_tok, float *q_out, void *workspace, size_t ws_bytes,
+                                          mlora_stream stream);
+
+/* ------------------------------------------------------------------------- */
+/* Run-time draft gate (host functions; no GPU needed)                        */
+/* ------------------------------------------------------------------------- */
+
+/* The InvisibleLoRA abstract has a run-time gate skip drafting on steps where
+ * the adapter cost cannot repay a draft pass.  The cost model (a reading; the
+ * pages give none) is speculative decoding's: with draft length k and each
+ * draft kept with probability alpha, a decode cycle emits on average
+ * E(alpha, k) = 1 + alpha + ... + alpha^k tokens per request. */
+
+/* E(alpha, k) for alpha in [0, 1], k >= 0; 0 for arguments outside. */
+MLORA_API double mlora_expected_tokens(double alpha, int k);
+
+/* The draft length to use: t_cycle (HOST, [k_max + 1], entry 0 unused) holds
+ * the measured time of a decode cycle with k drafts (k LoRA-off passes, the
+ * LoRA-on pass over k + 1 rows per request, the accept step), t_plain the
+ * time of one plain LoRA-on decode step of the same requests.  Returns the k
+ * in [1, k_max] with the highest rate E(alpha, k) / t_cycle[k] if it beats
+ * 1 / t_plain (the smallest such k on ties), else 0 (skip drafting); *gain
+ * (optional) receives that best rate times t_plain.  Returns -1 for null
+ * t_cycle, k_max outside [1, 64], a time that is not positive or alpha outside
+ * [0, 1]. */
+MLORA_API int mlora_draft_gate(const double *t_cycle, int k_max, double t_plain, double alpha, double *gain);
+
+/* Maximum-likelihood acceptance rate from the kept-draft counts (HOST array
+ * accepted[B], as mlora_verify_accept returns them, each clamped to [0, k]):
+ * sum n / (sum n + number of requests with n < k); 0 when undefined. */
+MLORA_API double mlora_estimate_acceptance(const int32_t *accepted, int B, int k);
+
 /* ------------------------------------------------------------------------- */
 /* Misc                                                                       */
 /* ------------------------------------------------------------------------- */

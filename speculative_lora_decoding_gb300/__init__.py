@@ -9,6 +9,8 @@ device is not compute capability 10.3, the calls raise.
     linear(x, W, A_stack, B_stack, rank_of, adapter_idx, scale, mode)   steps a1-a4
     linear_sliced(x, W, slice_end, A_stack, B_stack, ...)               the same, projections sharing x
     verify_accept(p, q, draft_tok, uniforms)                             steps a5-a6
+    verify_accept_logits(z_p, z_q, draft_tok, uniforms)                  the same on logits (softmax fused)
+    softmax(z), draft_sample(z_q, uniforms)                              logits -> probabilities; draft draw
     plan_segments(...), shrink(...)                                      steps a1, a2 alone
 
 The layer is y = W x (draft, LoRA off) or y = W x + scale * B_a (A_a x)
@@ -69,6 +71,16 @@ _SIGNATURES = {
                                       _c_ptr, _c_ptr, _c_float, _c_int, _c_ptr, _c_ptr]),
     "mlora_linear_gemm_kernel": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "mlora_debug_set_flag_wait_ns": (None, [ctypes.c_uint32]),
+    "mlora_verify_accept_logits": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr, _c_ptr,
+                                            _c_ptr, _c_size, _c_ptr]),
+    "mlora_softmax_workspace_bytes": (_c_size, [_c_int, _c_int]),
+    "mlora_softmax": (_c_int, [_c_ptr, _c_int, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "mlora_draft_sample_workspace_bytes": (_c_size, [_c_int, _c_int]),
+    "mlora_draft_sample": (_c_int, [_c_ptr, _c_int, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "mlora_expected_tokens": (ctypes.c_double, [ctypes.c_double, _c_int]),
+    "mlora_draft_gate": (_c_int, [ctypes.POINTER(ctypes.c_double), _c_int, ctypes.c_double, ctypes.c_double,
+                                  ctypes.POINTER(ctypes.c_double)]),
+    "mlora_estimate_acceptance": (ctypes.c_double, [ctypes.POINTER(ctypes.c_int32), _c_int, _c_int]),
     "mlora_status_string": (ctypes.c_char_p, [_c_int]),
     "mlora_device_supported": (_c_int, []),
     "mlora_launch_count": (ctypes.c_uint64, []),
@@ -314,6 +326,85 @@ def verify_accept(p: torch.Tensor, q: torch.Tensor, draft_tok: torch.Tensor, uni
                                      _need(accepted, "accepted", torch.int32, 1), ws.ptr, ws.nbytes, _stream(stream))
     _check(st, "verify_accept")
     return out_tok, accepted
+
+
+def verify_accept_logits(z_target: torch.Tensor, z_draft: torch.Tensor, draft_tok: torch.Tensor,
+                         uniforms: torch.Tensor, ws: Workspace = None, out_tok: torch.Tensor = None,
+                         accepted: torch.Tensor = None, stream=None):
+    """Steps a5-a6 on logits (softmax fused).  Returns (out_tok, accepted)."""
+    B, k1, V = z_target.shape
+    k = k1 - 1
+    if tuple(z_draft.shape) != (B, k, V) or tuple(draft_tok.shape) != (B, k) or tuple(uniforms.shape) != (B, k1):
+        raise ValueError("z_target [B,k+1,V], z_draft [B,k,V], draft_tok [B,k], uniforms [B,k+1] shapes disagree")
+    if ws is None:
+        ws = Workspace(accept_workspace_bytes(B, k, V), device=z_target.device, stream=stream)
+    if out_tok is None:
+        out_tok = torch.empty((B, k1), dtype=torch.int32, device=z_target.device)
+    if accepted is None:
+        accepted = torch.empty((B,), dtype=torch.int32, device=z_target.device)
+    st = _load().mlora_verify_accept_logits(_need(z_target, "z_target", torch.float32, 3),
+                                            _need(z_draft, "z_draft", torch.float32, 3),
+                                            _need(draft_tok, "draft_tok", torch.int32, 2),
+                                            _need(uniforms, "uniforms", torch.float32, 2), B, k, V,
+                                            _need(out_tok, "out_tok", torch.int32, 2),
+                                            _need(accepted, "accepted", torch.int32, 1), ws.ptr, ws.nbytes,
+                                            _stream(stream))
+    _check(st, "verify_accept_logits")
+    return out_tok, accepted
+
+
+def softmax(z: torch.Tensor, ws: Workspace = None, p: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Row softmax of fp32 logits [..., V] (the library's one definition of a probability)."""
+    V = z.shape[-1]
+    rows = z.numel() // V
+    if ws is None:
+        ws = Workspace(int(_load().mlora_softmax_workspace_bytes(rows, V)), device=z.device, stream=stream)
+    if p is None:
+        p = torch.empty_like(z)
+    st = _load().mlora_softmax(_need(z, "z", torch.float32), rows, V, _need(p, "p", torch.float32), ws.ptr, ws.nbytes,
+                               _stream(stream))
+    _check(st, "softmax")
+    return p
+
+
+def draft_sample(z_draft: torch.Tensor, uniforms: torch.Tensor, ws: Workspace = None, tok: torch.Tensor = None,
+                 q: torch.Tensor = None, want_q: bool = True, stream=None):
+    """Draft tokens from LoRA-off logits [B, V]: returns (tok int32 [B], q fp32 [B, V] or None)."""
+    B, V = z_draft.shape
+    if tuple(uniforms.shape) != (B,):
+        raise ValueError("uniforms must have B entries")
+    if ws is None:
+        ws = Workspace(int(_load().mlora_draft_sample_workspace_bytes(B, V)), device=z_draft.device, stream=stream)
+    if tok is None:
+        tok = torch.empty((B,), dtype=torch.int32, device=z_draft.device)
+    if q is None and want_q:
+        q = torch.empty_like(z_draft)
+    st = _load().mlora_draft_sample(_need(z_draft, "z_draft", torch.float32, 2), B, V,
+                                    _need(uniforms, "uniforms", torch.float32, 1), _need(tok, "tok", torch.int32, 1),
+                                    _need(q, "q", torch.float32, 2) if q is not None else None, ws.ptr, ws.nbytes,
+                                    _stream(stream))
+    _check(st, "draft_sample")
+    return tok, q
+
+
+def draft_gate(t_cycle: dict, t_plain: float, alpha: float):
+    """The run-time draft gate: t_cycle {k: measured cycle time} for k = 1..k_max,
+    t_plain the plain LoRA-on step time, alpha the acceptance rate.  Returns
+    (k, gain) with k = 0 meaning "skip drafting"."""
+    k_max = max(t_cycle)
+    arr = (ctypes.c_double * (k_max + 1))(*([0.0] + [float(t_cycle.get(k, 0.0)) for k in range(1, k_max + 1)]))
+    gain = ctypes.c_double(0.0)
+    k = int(_load().mlora_draft_gate(arr, k_max, float(t_plain), float(alpha), ctypes.byref(gain)))
+    if k < 0:
+        raise ValueError("draft gate: invalid times or acceptance rate (every k in 1..k_max needs a positive time)")
+    return k, gain.value
+
+
+def estimate_acceptance(accepted, k: int) -> float:
+    """Maximum-likelihood acceptance rate from kept-draft counts (host ints)."""
+    a = [int(v) for v in accepted]
+    arr = (ctypes.c_int32 * max(len(a), 1))(*a)
+    return float(_load().mlora_estimate_acceptance(arr, len(a), int(k)))
 
 
 def linear_noalloc(x: torch.Tensor, W: torch.Tensor, A_stack, B_stack, rank_of, adapter_idx, scale: float, mode: int,

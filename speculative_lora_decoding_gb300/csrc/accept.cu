@@ -845,7 +845,6 @@ __global__ void __launch_bounds__(DRAW_WARPS * 32)
 }
 
 AcceptShape accept_shape(int B, int k, int V, int num_sms) {
-  (void)k;
   AcceptShape s;
   s.slice_len = CHUNK;
   s.slices = (V + CHUNK - 1) / CHUNK;
@@ -853,7 +852,8 @@ AcceptShape accept_shape(int B, int k, int V, int num_sms) {
   // Per-chunk form: chunk sums (residual, target).  Streaming form: the 8
   // block sums of every chunk, then the accepted count of every request.
   const size_t units = (size_t)B * s.slices;
-  s.scratch_bytes = units * RING_CONSUMERS * 2 * sizeof(uint64_t) + align_up((size_t)B * 4, 256);
+  s.stats_off = units * RING_CONSUMERS * 2 * sizeof(uint64_t) + align_up((size_t)B * 4, 256);
+  s.scratch_bytes = s.stats_off + align_up((size_t)B * (2 * k + 1) * sizeof(float2), 256);
   // Streaming form: one CTA per SM, more when a CTA would own more than
   // RING_MAX_UNITS units.
   long long g = (long long)units < num_sms ? (long long)units : num_sms;

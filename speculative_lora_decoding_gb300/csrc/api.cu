@@ -301,10 +301,10 @@ int mlora_linear_gemm_kernel(int M, int N, int K, int n_adapters, int r_max, int
 
 void mlora_debug_set_flag_wait_ns(uint32_t ns) { g_test_flag_wait_ns.store(ns, std::memory_order_relaxed); }
 
-mlora_status mlora_verify_accept(const float *p_target, const float *q_draft, const int32_t *draft_tok,
-                                 const float *uniforms, int B, int k, int V, int32_t *out_tok, int32_t *accepted,
-                                 void *workspace, size_t ws_bytes, mlora_stream stream) {
-  if (!p_target || !q_draft || !draft_tok || !uniforms || !out_tok || !accepted) return MLORA_ERR_ARG;
+static mlora_status accept_impl(const float *p, const float *q, const int32_t *draft_tok, const float *uniforms, int B,
+                                int k, int V, int32_t *out_tok, int32_t *accepted, void *workspace, size_t ws_bytes,
+                                mlora_stream stream, bool logits) {
+  if (!p || !q || !draft_tok || !uniforms || !out_tok || !accepted) return MLORA_ERR_ARG;
   // B <= half the counters: the other half holds the stream-K GEMM's flags.
   if (B < 1 || B > (int)WS_MAX_COUNTERS / 2 || k < 1 || k > 16 || V < 1 || V > MLORA_MAX_VOCAB) return MLORA_ERR_SHAPE;
   if (!workspace || !aligned(workspace, 256)) return MLORA_ERR_WORKSPACE;
@@ -313,10 +313,111 @@ mlora_status mlora_verify_accept(const float *p_target, const float *q_draft, co
   const AcceptShape sh = accept_shape(B, k, V, sms);
   if (ws_bytes < WS_SCRATCH_OFF + sh.scratch_bytes) return MLORA_ERR_WORKSPACE;
   uint8_t *ws = (uint8_t *)workspace;
-  cudaError_t e = launch_accept(p_target, q_draft, draft_tok, uniforms, B, k, V, out_tok, accepted,
+  cudaStream_t s = (cudaStream_t)stream;
+  float2 *sp = nullptr, *sq = nullptr;
+  if (logits) {
+    // Row statistics of the target rows, then of the draft rows.
+    sp = reinterpret_cast<float2 *>(ws + WS_SCRATCH_OFF + sh.stats_off);
+    sq = sp + (size_t)B * (k + 1);
+    cudaError_t e = launch_row_stats(p, B * (k + 1), V, sp, sms, s);
+    if (e == cudaSuccess) e = launch_row_stats(q, B * k, V, sq, sms, s);
+    if (e != cudaSuccess) return MLORA_ERR_CUDA;
+  }
+  cudaError_t e = launch_accept(p, q, draft_tok, uniforms, B, k, V, out_tok, accepted,
                                 reinterpret_cast<uint32_t *>(ws + WS_COUNTERS_OFF), ws + WS_SCRATCH_OFF,
-                                reinterpret_cast<uint32_t *>(ws + WS_STATUS_OFF), sh, (cudaStream_t)stream);
+                                reinterpret_cast<uint32_t *>(ws + WS_STATUS_OFF), sh, sp, sq, s);
   return cuda_status(e);
+}
+
+mlora_status mlora_verify_accept(const float *p_target, const float *q_draft, const int32_t *draft_tok,
+                                 const float *uniforms, int B, int k, int V, int32_t *out_tok, int32_t *accepted,
+                                 void *workspace, size_t ws_bytes, mlora_stream stream) {
+  return accept_impl(p_target, q_draft, draft_tok, uniforms, B, k, V, out_tok, accepted, workspace, ws_bytes, stream,
+                     false);
+}
+
+mlora_status mlora_verify_accept_logits(const float *z_target, const float *z_draft, const int32_t *draft_tok,
+                                        const float *uniforms, int B, int k, int V, int32_t *out_tok,
+                                        int32_t *accepted, void *workspace, size_t ws_bytes, mlora_stream stream) {
+  return accept_impl(z_target, z_draft, draft_tok, uniforms, B, k, V, out_tok, accepted, workspace, ws_bytes, stream,
+                     true);
+}
+
+size_t mlora_softmax_workspace_bytes(int rows, int V) {
+  if (rows < 1 || rows > MLORA_MAX_ROWS || V < 1 || V > MLORA_MAX_VOCAB) return 0;
+  return align_up(WS_SCRATCH_OFF + (size_t)rows * sizeof(float2), 256);
+}
+
+mlora_status mlora_softmax(const float *z, int rows, int V, float *p, void *workspace, size_t ws_bytes,
+                           mlora_stream stream) {
+  if (!z || !p) return MLORA_ERR_ARG;
+  if (rows < 1 || rows > MLORA_MAX_ROWS || V < 1 || V > MLORA_MAX_VOCAB) return MLORA_ERR_SHAPE;
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < mlora_softmax_workspace_bytes(rows, V))
+    return MLORA_ERR_WORKSPACE;
+  const int sms = device_sms();
+  if (sms <= 0) return MLORA_ERR_CUDA;
+  float2 *stats = reinterpret_cast<float2 *>((uint8_t *)workspace + WS_SCRATCH_OFF);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_row_stats(z, rows, V, stats, sms, s);
+  if (e == cudaSuccess) e = launch_softmax_write(z, rows, V, stats, p, sms, s);
+  return cuda_status(e);
+}
+
+size_t mlora_draft_sample_workspace_bytes(int B, int V) {
+  if (B < 1 || B > MLORA_MAX_ROWS || V < 1 || V > MLORA_MAX_VOCAB) return 0;
+  return align_up(WS_SCRATCH_OFF + align_up((size_t)B * sizeof(float2), 256) + draft_sample_scratch_bytes(B, V), 256);
+}
+
+mlora_status mlora_draft_sample(const float *z_draft, int B, int V, const float *uniforms, int32_t *draft_tok,
+                                float *q_out, void *workspace, size_t ws_bytes, mlora_stream stream) {
+  if (!z_draft || !uniforms || !draft_tok) return MLORA_ERR_ARG;
+  if (B < 1 || B > MLORA_MAX_ROWS || V < 1 || V > MLORA_MAX_VOCAB) return MLORA_ERR_SHAPE;
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < mlora_draft_sample_workspace_bytes(B, V))
+    return MLORA_ERR_WORKSPACE;
+  const int sms = device_sms();
+  if (sms <= 0) return MLORA_ERR_CUDA;
+  uint8_t *ws = (uint8_t *)workspace;
+  float2 *stats = reinterpret_cast<float2 *>(ws + WS_SCRATCH_OFF);
+  void *blk = ws + WS_SCRATCH_OFF + align_up((size_t)B * sizeof(float2), 256);
+  cudaError_t e = launch_draft_sample(z_draft, B, V, uniforms, draft_tok, stats, q_out, blk,
+                                      reinterpret_cast<uint32_t *>(ws + WS_STATUS_OFF), sms, (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+double mlora_expected_tokens(double alpha, int k) {
+  if (k < 0 || !(alpha >= 0.0 && alpha <= 1.0)) return 0.0;
+  // 1 + alpha + ... + alpha^k by Horner's rule (stable as alpha -> 1).
+  double e = 1.0;
+  for (int i = 0; i < k; ++i) e = 1.0 + alpha * e;
+  return e;
+}
+
+int mlora_draft_gate(const double *t_cycle, int k_max, double t_plain, double alpha, double *gain) {
+  if (!t_cycle || k_max < 1 || k_max > 64 || !(t_plain > 0.0) || !(alpha >= 0.0 && alpha <= 1.0)) return -1;
+  for (int k = 1; k <= k_max; ++k)
+    if (!(t_cycle[k] > 0.0)) return -1;
+  int best_k = 0;
+  double best_rate = 1.0 / t_plain;
+  for (int k = 1; k <= k_max; ++k) {
+    const double rate = mlora_expected_tokens(alpha, k) / t_cycle[k];
+    if (rate > best_rate) {
+      best_k = k;
+      best_rate = rate;
+    }
+  }
+  if (gain) *gain = best_rate * t_plain;
+  return best_k;
+}
+
+double mlora_estimate_acceptance(const int32_t *accepted, int B, int k) {
+  if (!accepted || B < 1 || k < 1) return 0.0;
+  long long kept = 0, short_ = 0;
+  for (int b = 0; b < B; ++b) {
+    const int n = accepted[b] < 0 ? 0 : (accepted[b] > k ? k : accepted[b]);
+    kept += n;
+    short_ += n < k ? 1 : 0;
+  }
+  return kept + short_ == 0 ? 0.0 : (double)kept / (double)(kept + short_);
 }
 
 const char *mlora_status_string(mlora_status s) {

@@ -101,15 +101,26 @@ size_t sk_partial_bytes(int M, int num_sms);
 cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partials, uint32_t *flags, cudaStream_t s,
                            int *err_code);
 
-// Steps a5 + a6.
+// Steps a5 + a6.  With stats_p and stats_q non-null, p and q hold logits and
+// the kernels read probabilities expf(z - m) / S from the rows' statistics.
 struct AcceptShape {
   int slices, slice_len, threads;
   int ring_grid;  // CTAs of the streaming form (rows of aligned float4)
+  size_t stats_off;      // scratch offset of the row statistics (logits form): float2 [B(k+1) + Bk]
   size_t scratch_bytes;
 };
 AcceptShape accept_shape(int B, int k, int V, int num_sms);
 cudaError_t launch_accept(const float *p, const float *q, const int32_t *draft_tok, const float *u, int B, int k, int V,
                           int32_t *out_tok, int32_t *accepted, uint32_t *counters, void *scratch, uint32_t *status,
-                          const AcceptShape &sh, cudaStream_t s);
+                          const AcceptShape &sh, const float2 *stats_p, const float2 *stats_q, cudaStream_t s);
+
+// Softmax of logit rows (softmax.cu): stats[r] = (max, sum) of row r; the
+// probabilities expf(z - max) / sum written out; the draft draw.
+cudaError_t launch_row_stats(const float *z, int R, int V, float2 *stats, int num_sms, cudaStream_t s);
+cudaError_t launch_softmax_write(const float *z, int R, int V, const float2 *stats, float *p, int num_sms,
+                                 cudaStream_t s);
+size_t draft_sample_scratch_bytes(int B, int V);
+cudaError_t launch_draft_sample(const float *z, int B, int V, const float *u, int32_t *tok, float2 *stats, float *q,
+                                void *scratch, uint32_t *status, int num_sms, cudaStream_t s);
 
 }  // namespace mlora

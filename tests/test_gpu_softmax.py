@@ -1,0 +1,139 @@
+"""GPU parity of the softmax, the draft draw and the accept step on logits.
+
+The kernels compute a probability as expf(z - m) / S in fp32 (CUDA's expf,
+IEEE division, a row sum accumulated in a fixed order); the oracle is the
+float64 softmax.  Tolerance: per entry |p - p_ref| <= REL * p_ref with
+REL = 1e-4, from the fp32 arithmetic: expf is within 2 ulp (2.4e-7
+relative), the rounding of z - m moves the exponent by |z - m| 2^-24 (under
+2.4e-6 for the |z - m| <= 40 of these inputs), and the row sum of at most
+~260 terms per thread plus 9 merge levels and the rescalings errs by under
+3e-5 relative; the division adds half an ulp.
+
+The draw and the accept decisions are integers decided by those fp32 values,
+so they are compared with the oracle run on the float64 probabilities
+rounded to fp32: they must agree on every request whose decision lies
+outside the rounding margin (an accept test with |u q - p| <= REL (p + q), or
+a draw whose threshold T lies within the weights' possible shift of a
+cumulative boundary); the tests count the marginal ones, which must be rare.
+Inside the CUDA path the logits form must equal, bit for bit, the probability
+form fed with the probabilities mlora_softmax writes (one formula for every
+entry).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as WL
+from oracle import accept as OA
+from oracle import softmax as OS
+from tests.gpu_util import dev, needs_gpu
+
+pytestmark = pytest.mark.gpu
+REL = 1e-4
+
+
+def _check_probs(p_gpu, z):
+    p_ref = OS.softmax(np.asarray(z, np.float64))
+    p = p_gpu.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(p - p_ref) <= REL * p_ref + 1e-30), float(np.max(np.abs(p - p_ref) / np.maximum(p_ref, 1e-30)))
+
+
+def _draw_margin(w, U):
+    """Distance from T = floor(U S / 2^32) to the nearest cumulative boundary."""
+    S = int(w.sum(dtype=np.uint64))
+    if S == 0:
+        return np.inf
+    T = (int(U) * S) >> 32
+    c = np.cumsum(w.astype(np.float64))
+    return float(np.min(np.abs(c - T)))
+
+
+def _weights_shift(V, n_rows):
+    # Q(p) = floor(p 2^40): each weight moves by at most REL p 2^40 + 1 per row read,
+    # so a cumulative sum (and the total S, hence T) by at most REL 2^40 + V per row.
+    return n_rows * (REL * 2.0 ** 40 + V)
+
+
+@pytest.mark.parametrize("rows,V", [(1, 1), (3, 5), (8, 1000), (5, 4099), (16, 128256)])
+def test_softmax_matches_float64(rows, V):
+    ml = needs_gpu()
+    g = np.random.default_rng(rows + V)
+    z = (g.standard_normal((rows, V)) * 3).astype(np.float32)
+    if V > 3:
+        z[0, 2] = -np.inf          # a masked token: probability exactly 0
+        z[-1, 1] = np.float32(200.0)  # one logit that dominates its row
+    p = ml.softmax(dev(z))
+    assert p.cpu().numpy()[0, 2] == 0.0 if V > 3 else True
+    _check_probs(p, z)
+    assert torch.equal(p, ml.softmax(dev(z)))  # deterministic
+
+
+@pytest.mark.parametrize("B,V", [(256, 128256), (9, 1000), (7, 4099)])
+def test_draft_sample_against_oracle(B, V):
+    ml = needs_gpu()
+    zq = WL.accept_logits(V, B, 1, seed=B)[1][:, 0].copy()
+    u = np.random.default_rng(V).random(B, dtype=np.float32)
+    u[0] = np.float32(0.0)
+    tok, q = ml.draft_sample(dev(zq), dev(u))
+    _check_probs(q, zq)
+    assert torch.equal(q, ml.softmax(dev(zq)))  # the draw used the library's probabilities
+    q_ref32 = OS.softmax(zq.astype(np.float64)).astype(np.float32)
+    tok_ref = OS.draft_sample(q_ref32, u)
+    tok = tok.cpu().numpy()
+    marginal = 0
+    for b in range(B):
+        U = int(np.floor(np.float64(u[b]) * 2.0 ** 32))
+        if _draw_margin(OA.quantize(q_ref32[b]), U) <= 2 * _weights_shift(V, 1):
+            marginal += 1
+            continue
+        assert tok[b] == tok_ref[b], b
+    assert marginal <= max(2, B // 50), marginal
+
+
+def _offset_copy(a):
+    flat = torch.empty(a.size + 1, dtype=torch.float32, device="cuda")
+    view = flat[1:].view(a.shape)
+    view.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+    return view
+
+
+@pytest.mark.parametrize("B,k,V", [(64, 1, 128256), (32, 3, 128256), (16, 2, 4099), (8, 4, 1000), (3, 1, 5)])
+def test_accept_on_logits(B, k, V):
+    ml = needs_gpu()
+    zp, zq, tok, u = WL.accept_logits(V, B, k, sigma=0.3, seed=V + k)
+    u[::5, 0] = np.float32(0.999)  # some rejections at position 0
+    # Inside the CUDA path: the logits form equals the probability form on mlora_softmax's output.
+    for mk in (dev, _offset_copy):
+        ws = ml.Workspace(ml.accept_workspace_bytes(B, k, V))
+        out, acc = ml.verify_accept_logits(mk(zp), mk(zq), dev(tok), dev(u), ws=ws)
+        st = ws.status()
+        p_gpu, q_gpu = ml.softmax(dev(zp)), ml.softmax(dev(zq))
+        ws2 = ml.Workspace(ml.accept_workspace_bytes(B, k, V))
+        out2, acc2 = ml.verify_accept(p_gpu, q_gpu, dev(tok), dev(u), ws=ws2)
+        assert torch.equal(out, out2) and torch.equal(acc, acc2) and st == ws2.status()
+    out, acc = out.cpu().numpy(), acc.cpu().numpy()
+    # Against the oracle on the float64 probabilities rounded to fp32.
+    p32 = OS.softmax(zp.astype(np.float64)).astype(np.float32)
+    q32 = OS.softmax(zq.astype(np.float64)).astype(np.float32)
+    out_r, acc_r, _ = OA.verify_accept(p32, q32, tok, u)
+    marginal = 0
+    for b in range(B):
+        close = False
+        for i in range(min(int(acc_r[b]) + 1, k)):
+            x = int(tok[b, i])
+            pi, qi = float(p32[b, i, x]), float(q32[b, i, x])
+            close |= abs(float(u[b, i]) * qi - pi) <= REL * (pi + qi) + 1e-30
+        n = int(acc_r[b])
+        if n < k:
+            w = np.maximum(OA.quantize(p32[b, n]).astype(np.int64) - OA.quantize(q32[b, n]).astype(np.int64), 0)
+            shift = _weights_shift(V, 2)
+        else:
+            w = OA.quantize(p32[b, k]).astype(np.int64)
+            shift = _weights_shift(V, 1)
+        U = int(np.floor(np.float64(min(u[b, k], np.float32(1) - np.float32(2 ** -24))) * 2.0 ** 32))
+        close |= _draw_margin(w.astype(np.uint64), U) <= 2 * shift
+        if close:
+            marginal += 1
+            continue
+        assert acc[b] == acc_r[b] and np.array_equal(out[b], out_r[b]), b
+    assert marginal <= max(2, B // 20), marginal

@@ -271,3 +271,22 @@ def accept_inputs(V: int, B: int, k: int, sigma: float = ACCEPT_SIGMA, target_st
             tok[b, i] = min(t, V - 1)
     u = gu.random((B, k + 1), dtype=np.float32)
     return p, q, tok, u
+
+
+def accept_logits(V: int, B: int, k: int, sigma: float = ACCEPT_SIGMA, target_std: float = 2.0, seed: int = 0):
+    """Logits for the accept step and the draft draw: target logits z_p
+    [B, k+1, V] ~ N(0, target_std^2), draft logits z_q [B, k, V] = z_p[:, :k] +
+    N(0, sigma^2), both rounded to fp32; draft tokens [B, k] drawn from the fp32
+    probabilities of z_q (float64 softmax, float64 cumulative sum, their own
+    uniform stream); uniforms [B, k+1] in [0, 1) as fp32."""
+    gz, gn, gd, gu = (rng(seed, c, V, k, 1) for c in ("z", "noise", "draft_u", "u"))
+    zp = (gz.standard_normal((B, k + 1, V)) * target_std).astype(np.float32)
+    zq = (zp[:, :k].astype(np.float64) + gn.standard_normal((B, k, V)) * sigma).astype(np.float32)
+    tok = np.empty((B, k), dtype=np.int32)
+    for b in range(B):
+        q = _softmax_f32(zq[b].astype(np.float64))
+        for i in range(k):
+            c = np.cumsum(q[i].astype(np.float64))
+            tok[b, i] = min(int(np.searchsorted(c, gd.random() * c[-1], side="right")), V - 1)
+    u = gu.random((B, k + 1), dtype=np.float32)
+    return zp, zq, tok, u
