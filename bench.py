@@ -222,6 +222,19 @@ def accept_inputs_device(torch, V, B, k, device, seed=0, sigma=WL.ACCEPT_SIGMA, 
     return p, q, tok, u
 
 
+def accept_logits_device(torch, V, B, k, device, seed=0, sigma=WL.ACCEPT_SIGMA, target_std=2.0):
+    """Logits for the softmax row: z_p [B, k+1, V] ~ N(0, target_std^2) and
+    z_q [B, k, V] = z_p[:, :k] + N(0, sigma^2) in fp32; draft tokens drawn from
+    softmax(z_q); uniforms [B, k+1] in [0, 1)."""
+    g = _gen(torch, device, seed, "logits", V, B, k)
+    zp = torch.randn((B, k + 1, V), generator=g, device=device, dtype=torch.float32) * target_std
+    zq = zp[:, :k] + torch.randn((B, k, V), generator=g, device=device, dtype=torch.float32) * sigma
+    tok = torch.multinomial(torch.softmax(zq.reshape(B * k, V).double(), -1).float(), 1, generator=g)
+    tok = tok.reshape(B, k).to(torch.int32).contiguous()
+    u = torch.rand((B, k + 1), generator=g, device=device, dtype=torch.float32)
+    return zp.contiguous(), zq.contiguous(), tok, u
+
+
 class StepWorkload:
     """Device tensors of one decode-step workload: per input group (q|k|v, o,
     gate|up, down) the stacked W, A and B, one activation block per draft
@@ -267,6 +280,7 @@ class StepWorkload:
             del Ws, As, Bs
         self.rank_of = torch.from_numpy(self.ranks).to(device)
         self.adx_v = torch.from_numpy(self.idx_v).to(device)
+        self.adx_d = torch.from_numpy(self.idx_d).to(device)
         B = cfg.n_requests
         self.p, self.q, self.tok, self.u = accept_inputs_device(torch, cfg.vocab, B, k, device, seed=seed)
         self.out_tok = torch.empty((B, k + 1), dtype=torch.int32, device=device)
@@ -278,6 +292,10 @@ class StepWorkload:
         # The draft passes run beside the plan (second stream): a workspace of their own.
         self.ws_draft = ml.Workspace(max(ml.linear_sliced_workspace_bytes(self.Md, P["N"], P["K"], 0, len(P["ends"]))
                                          for P in self.proj), device=device)
+        self.ws_plain = ml.Workspace(max(ml.linear_sliced_workspace_bytes(self.Md, P["N"], P["K"], cfg.n_adapters,
+                                                                          len(P["ends"])) for P in self.proj),
+                                     device=device)
+        self.seg_plain = None
         torch.cuda.synchronize(device) if device.type == "cuda" else None
         self.seg = None
         self.w_bytes_per_pass = sum(2 * P["N"] * P["K"] for P in self.proj)
@@ -312,6 +330,15 @@ class StepWorkload:
                 out.append((f"base.{P['name']}", "base", P, lambda P=P: ml.linear_sliced(
                     P["xv"], P["W"], P["ends"], None, None, None, None, cfg.scale, ml.DRAFT | ml.PREFETCH_WEIGHTS,
                     ws=self.ws, y=P["yb"])))
+            # Plain multi-LoRA decoding: one LoRA-on pass over one row per request.
+            def plain_plan():
+                self.seg_plain, _ = ml.plan_segments(self.adx_d, self.rank_of, cfg.n_adapters, cfg.r_max,
+                                                     self.ws_plain)
+            out.append(("plain.plan", "plain", None, plain_plan))
+            for P in self.proj:
+                out.append((f"plain.{P['name']}", "plain", P, lambda P=P: ml.linear_sliced(
+                    P["xd"][0], P["W"], P["ends"], P["A"], P["B"], self.rank_of, self.adx_d, cfg.scale,
+                    ml.VERIFY | ml.PREFETCH_WEIGHTS, ws=self.ws_plain, y=P["yd"], seg_offsets_ptr=self.seg_plain)))
         return out
 
     def step(self, side=None):
@@ -650,6 +677,9 @@ def measure_layer(torch, ml, wl, stream, side, steps, peaks, flush):
         "accept": {"us": 1e3 * t_acc, "requests": cfg.n_requests, "rows_per_s": cfg.n_requests / (t_acc * 1e-3),
                    "GBps": acc_b / (t_acc * 1e-3) / 1e9, "frac_hbm": acc_b / (t_acc * 1e-3) / 1e9 / hbm_gbs,
                    "mean_accepted": float(acc_host.mean())},
+        "plain_lora_on_pass": {"us": 1e3 * sum(op_ms[f"plain.{P['name']}"] for P in wl.proj) + 1e3 * op_ms["plain.plan"],
+                               "rows": wl.Md,
+                               "note": "plain multi-LoRA decoding: one LoRA-on pass over one row per request (plan + 4 calls)"},
         "plan_us": 1e3 * op_ms["plan"],
         "per_op_timing": "events between the ops inside one step graph (breaks the launch overlap at each boundary)",
         "per_op_us": {n: 1e3 * v for n, v in op_ms.items()},
@@ -701,6 +731,55 @@ def measure_accept_sweep(torch, ml, device, stream, reps, peaks, flush, oracle_s
         del p, q, tok, u, ws, g
         torch.cuda.empty_cache()
     return out
+
+
+def measure_softmax_row(torch, ml, wl, device, stream, reps, peaks, flush):
+    """The steps beside the accept step at the workload's sizes: the draft
+    draw from LoRA-off logits (one per draft pass) and the accept step on
+    logits (softmax fused), each from CUDA events around graph replays with
+    L2 flushed before each."""
+    hbm_gbs = peaks[0]
+    cfg, k = wl.cfg, wl.k
+    B, V = cfg.n_requests, cfg.vocab
+    zp, zq, tok, u = accept_logits_device(torch, V, B, k, device, seed=23)
+    ws_s = ml.Workspace(int(ml.library().mlora_draft_sample_workspace_bytes(B, V)), device=device)
+    ws_a = ml.Workspace(ml.accept_workspace_bytes(B, k, V), device=device)
+    zq0 = zq[:, 0].contiguous()
+    u0 = u[:, 0].contiguous()
+    t_s = torch.empty((B,), dtype=torch.int32, device=device)
+    out_tok = torch.empty((B, k + 1), dtype=torch.int32, device=device)
+    accepted = torch.empty((B,), dtype=torch.int32, device=device)
+    sample = lambda: ml.draft_sample(zq0, u0, ws=ws_s, tok=t_s, want_q=False)  # noqa: E731
+    acc = lambda: ml.verify_accept_logits(zp, zq, tok, u, ws=ws_a, out_tok=out_tok, accepted=accepted)  # noqa: E731
+    res = {}
+    for name, fn in (("draft_sample", sample), ("accept_logits", acc)):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        g = graph_of(torch, fn, stream)
+        res[name] = time_replays(torch, g, stream, reps, flush)
+    if ws_s.status() != 0 or ws_a.status() != 0:
+        raise RuntimeError("device status bits raised in the softmax-row measurement")
+    acc_h = accepted.cpu().numpy()
+    rej = int((acc_h < k).sum())
+    # Bytes the design reads: the draw reads its logit row twice (statistics,
+    # then weights); the accept reads every target and draft row once for the
+    # statistics, then the scanned row (p_n, and q_n on a rejection).
+    b_sample = 2 * 4 * V * B
+    b_acc = (2 * k + 1) * 4 * V * B + 4 * V * (B + rej)
+    return {
+        "sizes": f"B={B} V={V} k={k}",
+        "draft_sample": {"us": 1e3 * res["draft_sample"], "rows_per_s": B / (res["draft_sample"] * 1e-3),
+                         "GBps": b_sample / (res["draft_sample"] * 1e-3) / 1e9,
+                         "frac_hbm": b_sample / (res["draft_sample"] * 1e-3) / 1e9 / hbm_gbs,
+                         "bytes": b_sample, "per_draft_pass": True},
+        "accept_logits": {"us": 1e3 * res["accept_logits"], "rows_per_s": B / (res["accept_logits"] * 1e-3),
+                          "GBps": b_acc / (res["accept_logits"] * 1e-3) / 1e9,
+                          "frac_hbm": b_acc / (res["accept_logits"] * 1e-3) / 1e9 / hbm_gbs, "bytes": b_acc,
+                          "mean_accepted": float(acc_h.mean())},
+        "l2": "L2 flushed before each timed call",
+    }
 
 
 def run_e2e(torch, ml, wl, stream, side, steps, world):
@@ -847,6 +926,11 @@ def run_gpu(args):
     ms = max_over_ranks(torch, ms, world, device)
     value = job_throughput(wl.Mv, world, ms)
     e2e = run_e2e(torch, ml, wl, stream, side, max(3, min(args.steps, 50)), world)
+    try:
+        softmax_row = measure_softmax_row(torch, ml, wl, device, stream, 30, peaks, flush)
+    except Exception as exc:
+        softmax_row = {"failed": f"{type(exc).__name__}: {exc}"}
+    alpha_hat = ml.estimate_acceptance(wl.accepted.cpu().numpy(), wl.k)
     cpu = None
     if rank == 0 and world == 1:
         try:
@@ -879,6 +963,34 @@ def run_gpu(args):
         except Exception as exc:
             sweep = {"failed": f"{type(exc).__name__}: {exc}"}
 
+    # The run-time draft gate on the measured cycle times: a cycle with k
+    # drafts costs the measured step plus k draft draws; plain decoding costs
+    # one LoRA-on pass over one row per request plus one draw.
+    gate = None
+    try:
+        t_draw = softmax_row["draft_sample"]["us"] if "draft_sample" in softmax_row else 0.0
+        t_plain = head["modes"]["plain_lora_on_pass"]["us"] + t_draw
+        cycles = {head_rows[3]: 1e3 * ms + head_rows[3] * t_draw}
+        for name, r in extra.items():
+            if "failed" not in r and LAYER_RUNS[name][0] is head_cfg:
+                kk = LAYER_RUNS[name][1]
+                cycles[kk] = 1e3 * r["ms_per_step"] + kk * t_draw
+        full = {kk: cycles[kk] for kk in sorted(cycles)}
+        kmax = max(full)
+        if all(kk in full for kk in range(1, kmax + 1)):
+            kk, gain = ml.draft_gate(full, t_plain, alpha_hat)
+        else:
+            # only some draft lengths measured: the gate over those, by its formula
+            rates = {kk: ml.library().mlora_expected_tokens(alpha_hat, kk) / t for kk, t in full.items()}
+            best = max(rates, key=rates.get)
+            kk, gain = (best, rates[best] * t_plain) if rates[best] > 1.0 / t_plain else (0, 1.0)
+        gate = {"alpha_estimate": alpha_hat, "t_plain_us": t_plain, "t_cycle_us": full, "k": kk,
+                "tokens_per_plain_step_time": gain,
+                "expected_tokens": {str(j): ml.library().mlora_expected_tokens(alpha_hat, j) for j in full},
+                "note": "k = 0 would skip drafting; gain = emitted tokens per request in the time of one plain step"}
+    except Exception as exc:
+        gate = {"failed": f"{type(exc).__name__}: {exc}"}
+
     if rank == 0:
         Md, Mv, calls, k = head_rows
         line = {
@@ -899,6 +1011,8 @@ def run_gpu(args):
                        "samples": clk["samples"]},
             "configs": extra,
             "accept_sweep": sweep,
+            "softmax_and_draft_draw": softmax_row,
+            "draft_gate": gate,
         }
         print(json.dumps(line))
     if world > 1:
@@ -913,11 +1027,33 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=HEADLINE, choices=sorted(LAYER_RUNS))
     ap.add_argument("--extra", default="all", choices=["all", "none"])
+    ap.add_argument("--only", default=None, choices=["accept"],
+                    help="run only the accept sweep (batch 256, vocabulary 128256, k = 1..4) and print its results")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.only == "accept":
+        return run_accept_only(args)
     return run_gpu(args)
+
+
+def run_accept_only(args):
+    """The accept sweep alone (for profiling the accept kernels): one JSON
+    line with the sweep's results, not a bench line."""
+    import torch
+    import speculative_lora_decoding_gb300 as ml
+    if not os.path.exists(ml.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream(device)
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    sweep = measure_accept_sweep(torch, ml, device, stream, max(3, min(args.steps, 30)), _peaks(),
+                                 lambda: flush_buf.fill_(1.0), 0.5)
+    print(json.dumps({"accept_sweep": sweep}))
+    return 0
 
 
 if __name__ == "__main__":
