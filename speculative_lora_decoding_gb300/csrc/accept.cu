@@ -34,6 +34,8 @@
 // conversion rounding toward minus infinity to an unsigned 64-bit integer
 // (exact: the scaled value is representable and its integer part is below
 // 2^41); in the streaming form's sums, three fused multiply-adds (q_bits).
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -853,7 +855,9 @@ AcceptShape accept_shape(int B, int k, int V, int num_sms) {
   // block sums of every chunk, then the accepted count of every request.
   const size_t units = (size_t)B * s.slices;
   s.stats_off = units * RING_CONSUMERS * 2 * sizeof(uint64_t) + align_up((size_t)B * 4, 256);
-  s.scratch_bytes = s.stats_off + align_up((size_t)B * (2 * k + 1) * sizeof(float2), 256);
+  s.part_off = s.stats_off + align_up((size_t)B * (2 * k + 1) * sizeof(float2), 256);
+  const size_t rows_per_launch = std::min((size_t)B * (k + 1), (size_t)WS_MAX_COUNTERS);
+  s.scratch_bytes = s.part_off + row_stats_scratch_bytes((int)rows_per_launch, V);
   // Streaming form: one CTA per SM, more when a CTA would own more than
   // RING_MAX_UNITS units.
   long long g = (long long)units < num_sms ? (long long)units : num_sms;

@@ -1,5 +1,6 @@
 // C-ABI front end: argument checks, workspace layout and kernel launches.
 // Nothing here computes a result; every step runs in the CUDA kernels.
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 
@@ -316,11 +317,22 @@ static mlora_status accept_impl(const float *p, const float *q, const int32_t *d
   cudaStream_t s = (cudaStream_t)stream;
   float2 *sp = nullptr, *sq = nullptr;
   if (logits) {
-    // Row statistics of the target rows, then of the draft rows.
+    // Row statistics of the target rows, then of the draft rows, at most
+    // WS_MAX_COUNTERS rows per launch (one arrival counter per row).
     sp = reinterpret_cast<float2 *>(ws + WS_SCRATCH_OFF + sh.stats_off);
     sq = sp + (size_t)B * (k + 1);
-    cudaError_t e = launch_row_stats(p, B * (k + 1), V, sp, sms, s);
-    if (e == cudaSuccess) e = launch_row_stats(q, B * k, V, sq, sms, s);
+    uint32_t *counters = reinterpret_cast<uint32_t *>(ws + WS_COUNTERS_OFF);
+    void *part = ws + WS_SCRATCH_OFF + sh.part_off;
+    auto stats_of = [&](const float *z, long long rows, float2 *out) -> cudaError_t {
+      for (long long r0 = 0; r0 < rows; r0 += (long long)WS_MAX_COUNTERS) {
+        const int n = (int)std::min<long long>((long long)WS_MAX_COUNTERS, rows - r0);
+        cudaError_t e = launch_row_stats(z + (size_t)r0 * V, n, V, out + r0, part, counters, s);
+        if (e != cudaSuccess) return e;
+      }
+      return cudaSuccess;
+    };
+    cudaError_t e = stats_of(p, (long long)B * (k + 1), sp);
+    if (e == cudaSuccess) e = stats_of(q, (long long)B * k, sq);
     if (e != cudaSuccess) return MLORA_ERR_CUDA;
   }
   cudaError_t e = launch_accept(p, q, draft_tok, uniforms, B, k, V, out_tok, accepted,
@@ -345,7 +357,8 @@ mlora_status mlora_verify_accept_logits(const float *z_target, const float *z_dr
 
 size_t mlora_softmax_workspace_bytes(int rows, int V) {
   if (rows < 1 || rows > MLORA_MAX_ROWS || V < 1 || V > MLORA_MAX_VOCAB) return 0;
-  return align_up(WS_SCRATCH_OFF + (size_t)rows * sizeof(float2), 256);
+  return align_up(WS_SCRATCH_OFF + align_up((size_t)rows * sizeof(float2), 256) + row_stats_scratch_bytes(rows, V),
+                  256);
 }
 
 mlora_status mlora_softmax(const float *z, int rows, int V, float *p, void *workspace, size_t ws_bytes,
@@ -356,22 +369,24 @@ mlora_status mlora_softmax(const float *z, int rows, int V, float *p, void *work
     return MLORA_ERR_WORKSPACE;
   const int sms = device_sms();
   if (sms <= 0) return MLORA_ERR_CUDA;
-  float2 *stats = reinterpret_cast<float2 *>((uint8_t *)workspace + WS_SCRATCH_OFF);
+  uint8_t *ws = (uint8_t *)workspace;
+  float2 *stats = reinterpret_cast<float2 *>(ws + WS_SCRATCH_OFF);
+  void *part = ws + WS_SCRATCH_OFF + align_up((size_t)rows * sizeof(float2), 256);
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_row_stats(z, rows, V, stats, sms, s);
+  cudaError_t e = launch_row_stats(z, rows, V, stats, part, reinterpret_cast<uint32_t *>(ws + WS_COUNTERS_OFF), s);
   if (e == cudaSuccess) e = launch_softmax_write(z, rows, V, stats, p, sms, s);
   return cuda_status(e);
 }
 
 size_t mlora_draft_sample_workspace_bytes(int B, int V) {
-  if (B < 1 || B > MLORA_MAX_ROWS || V < 1 || V > MLORA_MAX_VOCAB) return 0;
+  if (B < 1 || B > (int)WS_MAX_COUNTERS || V < 1 || V > MLORA_MAX_VOCAB) return 0;
   return align_up(WS_SCRATCH_OFF + align_up((size_t)B * sizeof(float2), 256) + draft_sample_scratch_bytes(B, V), 256);
 }
 
 mlora_status mlora_draft_sample(const float *z_draft, int B, int V, const float *uniforms, int32_t *draft_tok,
                                 float *q_out, void *workspace, size_t ws_bytes, mlora_stream stream) {
   if (!z_draft || !uniforms || !draft_tok) return MLORA_ERR_ARG;
-  if (B < 1 || B > MLORA_MAX_ROWS || V < 1 || V > MLORA_MAX_VOCAB) return MLORA_ERR_SHAPE;
+  if (B < 1 || B > (int)WS_MAX_COUNTERS || V < 1 || V > MLORA_MAX_VOCAB) return MLORA_ERR_SHAPE;
   if (!workspace || !aligned(workspace, 256) || ws_bytes < mlora_draft_sample_workspace_bytes(B, V))
     return MLORA_ERR_WORKSPACE;
   const int sms = device_sms();
@@ -380,7 +395,8 @@ mlora_status mlora_draft_sample(const float *z_draft, int B, int V, const float 
   float2 *stats = reinterpret_cast<float2 *>(ws + WS_SCRATCH_OFF);
   void *blk = ws + WS_SCRATCH_OFF + align_up((size_t)B * sizeof(float2), 256);
   cudaError_t e = launch_draft_sample(z_draft, B, V, uniforms, draft_tok, stats, q_out, blk,
-                                      reinterpret_cast<uint32_t *>(ws + WS_STATUS_OFF), sms, (cudaStream_t)stream);
+                                      reinterpret_cast<uint32_t *>(ws + WS_COUNTERS_OFF),
+                                      reinterpret_cast<uint32_t *>(ws + WS_STATUS_OFF), (cudaStream_t)stream);
   return cuda_status(e);
 }
 

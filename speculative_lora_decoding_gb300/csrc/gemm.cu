@@ -502,38 +502,38 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
     bhi = ns > 0 ? (int)((long long)(rank + 1) * ns / C) : 0;
   };
 
+  // k-blocks before the expand: verify mode puts the expand's operand loads
+  // into the ring before the last S k-blocks, so that they land while those
+  // stream (the expand MMAs then add into the accumulator before the last
+  // k-blocks do; the order of additions into it is free).  Not when the first
+  // ring of W was requested early (those stages are already taken).
+  const int nkb = kb_hi - kb_lo;
+  const int early_n = (args.prefetch_w && !args.after_shrink) ? min(nkb, S) : 0;
+  const int split = (sorted_verify && early_n == 0) ? max(1, nkb - S) : nkb;
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int stage = 0, issued = 0, early = 0;
+    int stage = 0, issued = 0;
     uint32_t phase = 0;
+    bool ok = true;
+    const int early = early_n;
     const uint64_t pol_w = policy_evict_first();
-    if (lane == 0) {
-      const uint64_t pol_x = policy_evict_last();
-      const int nkb = kb_hi - kb_lo;
-      // Loop constants in registers (the copies below are asm with memory
-      // clobbers, after which kernel parameters would be re-read).
-      const bool two = args.nsub == 2;
-      const int w_row = n_tile * BLOCK_N, x_row1 = m0 + args.sub_n;
-      const uint32_t x1_bytes = (uint32_t)(args.sub_n * BLOCK_K * 2);
-      const uint32_t tx_bytes = (uint32_t)stage_bytes;
-      // With static weights, the first ring of W tiles is requested before the
-      // wait for the preceding kernel; x always comes after it.
-      early = (args.prefetch_w && !args.after_shrink) ? min(nkb, S) : 0;
-      for (int i = 0; i < early; ++i) {
-        mbar_arrive_expect_tx(&sp.full[i], tx_bytes);
-        tma_load_2d(sp.stage0 + (size_t)i * stage_bytes, &tmap_w, &sp.full[i], (kb_lo + i) * BLOCK_K, w_row, pol_w);
-      }
-      // After this library's shrink kernel nothing the mainloop reads can
-      // still be in flight (the shrink released this grid only after its own
-      // predecessor had finished), so only the expand and the epilogue wait
-      // for the shrink's output.
-      if (!args.after_shrink) grid_dependency_wait();
-      for (int i = 0; i < nkb; ++i) {
+    const uint64_t pol_x = policy_evict_last();
+    // Loop constants in registers (the copies below are asm with memory
+    // clobbers, after which kernel parameters would be re-read).
+    const bool two = args.nsub == 2;
+    const int w_row = n_tile * BLOCK_N, x_row1 = m0 + args.sub_n;
+    const uint32_t x1_bytes = (uint32_t)(args.sub_n * BLOCK_K * 2);
+    const uint32_t tx_bytes = (uint32_t)stage_bytes;
+    // k-blocks [from, to) of this CTA's range, lane 0 only.
+    auto issue = [&](int from, int to) {
+      for (int i = from; i < to; ++i) {
         const int kb = kb_lo + i;
         uint8_t *st = sp.stage0 + (size_t)stage * stage_bytes;
         if (i >= early) {
           if (!mbar_wait_bounded(&sp.empty[stage], phase ^ 1u, abort_flag)) {
             signal_abort(sp, args.status);
+            ok = false;
             break;
           }
           mbar_arrive_expect_tx(&sp.full[stage], tx_bytes);
@@ -547,24 +547,43 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
           phase ^= 1u;
         }
       }
+    };
+    auto sync_state = [&]() {
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      stage = __shfl_sync(0xffffffffu, stage, 0);
+      phase = __shfl_sync(0xffffffffu, phase, 0);
+      issued = __shfl_sync(0xffffffffu, issued, 0);
+      __syncwarp();
+    };
+    if (lane == 0) {
+      // With static weights, the first ring of W tiles is requested before the
+      // wait for the preceding kernel; x always comes after it.
+      for (int i = 0; i < early; ++i) {
+        mbar_arrive_expect_tx(&sp.full[i], tx_bytes);
+        tma_load_2d(sp.stage0 + (size_t)i * stage_bytes, &tmap_w, &sp.full[i], (kb_lo + i) * BLOCK_K, w_row, pol_w);
+      }
+      // After this library's shrink kernel nothing the mainloop reads can
+      // still be in flight (the shrink released this grid only after its own
+      // predecessor had finished), so only the expand and the epilogue wait
+      // for the shrink's output.
+      if (!args.after_shrink) grid_dependency_wait();
+      issue(0, split);
     }
-    stage = __shfl_sync(0xffffffffu, stage, 0);
-    phase = __shfl_sync(0xffffffffu, phase, 0);
-    issued = __shfl_sync(0xffffffffu, issued, 0);
-    early = __shfl_sync(0xffffffffu, early, 0);
-    __syncwarp();
-    int blo = 0, bhi = 0;
-    if (sorted_verify && !*abort_flag) {
+    sync_state();
+    if (ok && sorted_verify && !*abort_flag) {
       grid_dependency_wait();  // the plan and the token windows come from the kernels just before
+      int blo = 0, bhi = 0;
       expand_range(blo, bhi);
+      if (bhi > blo) {
+        ok = expand_produce(args.plan + L.slices, blo, bhi, m0, args.Mb, n_tile * BLOCK_N, args.N, &tmap_b,
+                            args.tw + (size_t)slice * args.tw_slice, sp.stage0, stage_bytes, S, sp.full, sp.empty,
+                            sp.meta, sp.chunk, stage, phase, issued, abort_flag, pol_w, lane, args.n_ad,
+                            (long long)(args.tw_slice / 16), args.status);
+        if (!ok && lane == 0) signal_abort(sp, args.status);
+      }
     }
-    if (bhi > blo) {
-      const bool ok = expand_produce(args.plan + L.slices, blo, bhi, m0, args.Mb, n_tile * BLOCK_N, args.N, &tmap_b,
-                                     args.tw + (size_t)slice * args.tw_slice, sp.stage0, stage_bytes, S, sp.full,
-                                     sp.empty, sp.meta, sp.chunk, stage, phase, issued, abort_flag, pol_w, lane,
-                                     args.n_ad, (long long)(args.tw_slice / 16), args.status);
-      if (!ok && lane == 0) signal_abort(sp, args.status);
-    }
+    if (lane == 0 && ok && !*abort_flag) issue(split, nkb);
+    sync_state();
     if (lane == 0 && *abort_flag) {
       // Let this CTA's own copies land before shared memory goes away.
       const int n = issued < S ? issued : S;
@@ -583,19 +602,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true, issued_any = false;
-    if (lane == 0) {
-      // Everything the loop needs is in registers before it starts: this one
-      // thread issues every MMA of the CTA, so the issue path is kept to a
-      // few integer adds per instruction (descriptor start addresses step by
-      // 32 bytes, i.e. 2 in the descriptor's 16-byte units, per 16-wide K step).
-      const uint32_t idesc = idesc_bf16_f32(BLOCK_N, args.sub_n);
-      const bool two = args.nsub == 2;
-      const uint32_t d1 = tmem_base + (uint32_t)args.sub_n;
-      const uint64_t x1_off = (uint64_t)((args.sub_n * BLOCK_K * 2) >> 4);
-      const uint32_t ring0 = smem_addr(sp.stage0);
-      const uint32_t sbytes = (uint32_t)stage_bytes;
-      const int k_lo = kb_lo, k_hi = kb_hi;
-      for (int kb = k_lo; kb < k_hi; ++kb) {
+    // Everything the loop needs is in registers before it starts: this one
+    // thread issues every MMA of the CTA, so the issue path is kept to a few
+    // integer adds per instruction (descriptor start addresses step by 32
+    // bytes, i.e. 2 in the descriptor's 16-byte units, per 16-wide K step).
+    const uint32_t idesc = idesc_bf16_f32(BLOCK_N, args.sub_n);
+    const bool two = args.nsub == 2;
+    const uint32_t d1 = tmem_base + (uint32_t)args.sub_n;
+    const uint64_t x1_off = (uint64_t)((args.sub_n * BLOCK_K * 2) >> 4);
+    const uint32_t ring0 = smem_addr(sp.stage0);
+    const uint32_t sbytes = (uint32_t)stage_bytes;
+    auto mma_kblocks = [&](int from, int to) {  // lane 0: k-blocks [kb_lo + from, kb_lo + to)
+      for (int kb = kb_lo + from; kb < kb_lo + to; ++kb) {
         if (!mbar_wait_bounded(&sp.full[stage], phase, abort_flag)) {
           signal_abort(sp, args.status);
           ok = false;
@@ -605,7 +623,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
         const uint32_t a_addr = ring0 + (uint32_t)stage * sbytes;
         const uint64_t ad = smem_desc_kmajor_sw128(a_addr);
         const uint64_t bd = smem_desc_kmajor_sw128(a_addr + W_TILE_BYTES);
-        const uint32_t first = kb > k_lo ? 1u : 0u;
+        const uint32_t first = kb > kb_lo ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
           const uint32_t accum = kk > 0 ? 1u : first;
@@ -619,27 +637,33 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
           phase ^= 1u;
         }
       }
-    }
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    issued_any = __shfl_sync(0xffffffffu, issued_any ? 1 : 0, 0) != 0;
-    stage = __shfl_sync(0xffffffffu, stage, 0);
-    phase = __shfl_sync(0xffffffffu, phase, 0);
-    __syncwarp();
-    int blo = 0, bhi = 0;
-    if (sorted_verify) {
+    };
+    auto sync_state = [&]() {
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      issued_any = __shfl_sync(0xffffffffu, issued_any ? 1 : 0, 0) != 0;
+      stage = __shfl_sync(0xffffffffu, stage, 0);
+      phase = __shfl_sync(0xffffffffu, phase, 0);
+      __syncwarp();
+    };
+    if (lane == 0) mma_kblocks(0, split);
+    sync_state();
+    if (ok && sorted_verify) {
       grid_dependency_wait();  // the plan comes from a kernel earlier in the stream
+      int blo = 0, bhi = 0;
       expand_range(blo, bhi);
+      if (bhi > blo && !*abort_flag) {
+        // The producer issues at least one expand stage whenever bhi > blo
+        // and it has not given up.
+        ok = expand_consume(sp.stage0, stage_bytes, S, sp.full, sp.empty, sp.meta, tmem_base, stage, phase,
+                            abort_flag, lane);
+        if (!ok && lane == 0) signal_abort(sp, args.status);
+        issued_any = true;
+      } else if (bhi > blo) {
+        ok = false;  // the producer gave up before the expand
+      }
     }
-    if (ok && bhi > blo && !*abort_flag) {
-      // The producer issues at least one expand stage whenever bhi > blo
-      // and it has not given up.
-      ok = expand_consume(sp.stage0, stage_bytes, S, sp.full, sp.empty, sp.meta, tmem_base, stage, phase, abort_flag,
-                          lane);
-      if (!ok && lane == 0) signal_abort(sp, args.status);
-      issued_any = true;
-    } else if (ok && bhi > blo) {
-      ok = false;  // the producer gave up before the expand
-    }
+    if (lane == 0 && ok) mma_kblocks(split, nkb);
+    sync_state();
     bool mma_ok = false;
     if (lane == 0) {
       if (ok) {

@@ -107,6 +107,7 @@ struct AcceptShape {
   int slices, slice_len, threads;
   int ring_grid;  // CTAs of the streaming form (rows of aligned float4)
   size_t stats_off;      // scratch offset of the row statistics (logits form): float2 [B(k+1) + Bk]
+  size_t part_off;       // scratch offset of the statistics' chunk partials (logits form)
   size_t scratch_bytes;
 };
 AcceptShape accept_shape(int B, int k, int V, int num_sms);
@@ -116,11 +117,16 @@ cudaError_t launch_accept(const float *p, const float *q, const int32_t *draft_t
 
 // Softmax of logit rows (softmax.cu): stats[r] = (max, sum) of row r; the
 // probabilities expf(z - max) / sum written out; the draft draw.
-cudaError_t launch_row_stats(const float *z, int R, int V, float2 *stats, int num_sms, cudaStream_t s);
+// Row statistics use one CTA per (row, 4096-entry chunk), chunk partials in
+// `scratch` (row_stats_scratch_bytes) and one arrival counter per row
+// (counters[0, R), zero before and after; R <= WS_MAX_COUNTERS).
+size_t row_stats_scratch_bytes(int R, int V);
+cudaError_t launch_row_stats(const float *z, int R, int V, float2 *stats, void *scratch, uint32_t *counters,
+                             cudaStream_t s);
 cudaError_t launch_softmax_write(const float *z, int R, int V, const float2 *stats, float *p, int num_sms,
                                  cudaStream_t s);
 size_t draft_sample_scratch_bytes(int B, int V);
 cudaError_t launch_draft_sample(const float *z, int B, int V, const float *u, int32_t *tok, float2 *stats, float *q,
-                                void *scratch, uint32_t *status, int num_sms, cudaStream_t s);
+                                void *scratch, uint32_t *counters, uint32_t *status, cudaStream_t s);
 
 }  // namespace mlora

@@ -11,10 +11,13 @@ relative), the rounding of z - m moves the exponent by |z - m| 2^-24 (under
 
 The draw and the accept decisions are integers decided by those fp32 values,
 so they are compared with the oracle run on the float64 probabilities
-rounded to fp32: they must agree on every request whose decision lies
-outside the rounding margin (an accept test with |u q - p| <= REL (p + q), or
-a draw whose threshold T lies within the weights' possible shift of a
-cumulative boundary); the tests count the marginal ones, which must be rare.
+rounded to fp32: every request on which the two disagree must lie inside
+the rounding margin (an accept test with |u q - p| <= REL (p + q), or a draw
+whose threshold T lies within the weights' largest possible shift of a
+cumulative boundary), and disagreements must be rare.  (The margin is a
+worst case that adds every entry's error in one direction; on a flat
+128256-entry row most draws lie inside it, so it decides only which
+disagreements are allowed, not which requests are compared.)
 Inside the CUDA path the logits form must equal, bit for bit, the probability
 form fed with the probabilities mlora_softmax writes (one formula for every
 entry).
@@ -80,14 +83,11 @@ def test_draft_sample_against_oracle(B, V):
     q_ref32 = OS.softmax(zq.astype(np.float64)).astype(np.float32)
     tok_ref = OS.draft_sample(q_ref32, u)
     tok = tok.cpu().numpy()
-    marginal = 0
-    for b in range(B):
+    differ = [b for b in range(B) if tok[b] != tok_ref[b]]
+    for b in differ:  # a disagreement is allowed only inside the rounding margin
         U = int(np.floor(np.float64(u[b]) * 2.0 ** 32))
-        if _draw_margin(OA.quantize(q_ref32[b]), U) <= 2 * _weights_shift(V, 1):
-            marginal += 1
-            continue
-        assert tok[b] == tok_ref[b], b
-    assert marginal <= max(2, B // 50), marginal
+        assert _draw_margin(OA.quantize(q_ref32[b]), U) <= 2 * _weights_shift(V, 1), b
+    assert len(differ) <= max(1, B // 100), differ
 
 
 def _offset_copy(a):
@@ -116,8 +116,8 @@ def test_accept_on_logits(B, k, V):
     p32 = OS.softmax(zp.astype(np.float64)).astype(np.float32)
     q32 = OS.softmax(zq.astype(np.float64)).astype(np.float32)
     out_r, acc_r, _ = OA.verify_accept(p32, q32, tok, u)
-    marginal = 0
-    for b in range(B):
+    differ = [b for b in range(B) if acc[b] != acc_r[b] or not np.array_equal(out[b], out_r[b])]
+    for b in differ:  # a disagreement is allowed only inside the rounding margin
         close = False
         for i in range(min(int(acc_r[b]) + 1, k)):
             x = int(tok[b, i])
@@ -132,8 +132,5 @@ def test_accept_on_logits(B, k, V):
             shift = _weights_shift(V, 1)
         U = int(np.floor(np.float64(min(u[b, k], np.float32(1) - np.float32(2 ** -24))) * 2.0 ** 32))
         close |= _draw_margin(w.astype(np.uint64), U) <= 2 * shift
-        if close:
-            marginal += 1
-            continue
-        assert acc[b] == acc_r[b] and np.array_equal(out[b], out_r[b]), b
-    assert marginal <= max(2, B // 20), marginal
+        assert close, b
+    assert len(differ) <= max(1, B // 50), differ
