@@ -99,9 +99,9 @@ def layer_bytes_flops(M, K, N, active_ranks, verify, n_proj=1):
 # DRAM traffic per launch of a kernel, from a committed ncu summary; valid
 # only while the kernel's sources are the ones the counters were taken on.
 TRAFFIC_SOURCES = {
-    "gemm_sk_kernel": ("gemm_sk.cu", "expand.cuh", "common.cuh", "launch.h"),
-    "gemm_kernel": ("gemm.cu", "expand.cuh", "common.cuh", "launch.h"),
-    "accept_stream_kernel": ("accept.cu", "common.cuh", "launch.h"),
+    "gemm_sk_kernel": ("gemm_sk.cu", "expand.cuh", "common.cuh"),
+    "gemm_kernel": ("gemm.cu", "expand.cuh", "common.cuh"),
+    "accept_stream_kernel": ("accept.cu", "common.cuh"),
 }
 
 
