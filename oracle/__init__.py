@@ -25,7 +25,8 @@ Sources:
 Modules: ``oracle.layer`` (segment plan, shrink, layer output),
 ``oracle.accept`` (accept test, residual/bonus sample), ``oracle.softmax``
 (logits to probabilities, draft-token draw), ``oracle.gate`` (the run-time
-draft gate's cost model) and ``oracle.kvcache`` (where each pass's K/V rows
-go in the paged cache the two passes share).  Every function is pinned by
+draft gate's cost model), ``oracle.kvcache`` (where each pass's K/V rows
+go in the paged cache the two passes share) and ``oracle.fp8`` (E4M3
+rounding, per-row scales and the draft layer on FP8 weights).  Every function is pinned by
 tests under ``-m "not gpu"``; none is marked "parity unpinned".
 """
