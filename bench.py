@@ -782,6 +782,76 @@ def measure_softmax_row(torch, ml, wl, device, stream, reps, peaks, flush):
     }
 
 
+KV_HEAD_DIM = 128  # head size of the 32B- and 8B-class shapes (q 5120 = 40 x 128, k/v 1024 = 8 x 128)
+
+
+def measure_kv_cache(torch, ml, wl, device, stream, reps, peaks, flush):
+    """The hybrid KV cache at the workload's sizes: one draft step's K/V rows
+    (one per request), the verify pass's (k + 1 per request) and the commit,
+    from the fused q|k|v output into a paged cache of 16-token blocks; CUDA
+    events around graph replays with L2 flushed before each.  The oracle's
+    copy of the same rows is timed beside it."""
+    import numpy as np
+    from oracle import kvcache as OK
+    hbm_gbs = peaks[0]
+    cfg, k = wl.cfg, wl.k
+    P = wl.proj[0]
+    if P["n_proj"] != 3:
+        return {"skipped": "the workload has no fused q|k|v projection"}
+    ends = [int(e) for e in P["ends"]]
+    Nq, Nkv = ends[0], ends[1] - ends[0]
+    D = KV_HEAD_DIM if Nkv % KV_HEAD_DIM == 0 else Nkv
+    H = Nkv // D
+    B, bs, max_blocks = cfg.n_requests, 16, 64
+    num_blocks = B * max_blocks
+    g = torch.Generator(device=device)
+    g.manual_seed(31)
+    bt = torch.randperm(num_blocks, generator=g, device=device).to(torch.int32).view(B, max_blocks)
+    seq0 = torch.randint(0, max_blocks * bs - 2 * k - 2, (B,), generator=g, device=device, dtype=torch.int32)
+    seq = seq0.clone()
+    kc = torch.zeros((num_blocks, bs, H, D), dtype=torch.bfloat16, device=device)
+    vc = torch.zeros_like(kc)
+    yd = torch.randn((wl.Md, P["N"]), generator=g, device=device).to(torch.bfloat16)
+    yv = torch.randn((wl.Mv, P["N"]), generator=g, device=device).to(torch.bfloat16)
+    acc = torch.randint(0, k + 1, (B,), generator=g, device=device, dtype=torch.int32)
+    ws = ml.Workspace(ml.kv_workspace_bytes(), device=device)
+    calls = {
+        "draft_step": lambda: ml.kv_write(yd, Nq, Nq + Nkv, H, D, bt, seq, 1, 0, kc, vc, ws=ws),
+        "verify_pass": lambda: ml.kv_write(yv, Nq, Nq + Nkv, H, D, bt, seq, k + 1, 0, kc, vc, ws=ws),
+    }
+    res = {}
+    for name, fn in calls.items():
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        gr = graph_of(torch, fn, stream)
+        ms = time_replays(torch, gr, stream, reps, flush)
+        rows = wl.Md if name == "draft_step" else wl.Mv
+        nbytes = rows * 2 * H * D * 2 * 2  # K and V rows read from y and written to the cache
+        res[name] = {"rows": rows, "us": 1e3 * ms, "GBps": nbytes / (ms * 1e-3) / 1e9,
+                     "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm_gbs, "bytes": nbytes}
+    with torch.cuda.stream(stream):
+        ml.kv_commit(acc, seq, stream=stream)
+    stream.synchronize()
+    if not torch.equal(seq, seq0 + acc + 1) or ws.status() != 0:
+        raise RuntimeError("KV cache measurement: commit or status check failed")
+    # the oracle on the verify pass's rows (host, numpy)
+    yh = yv.view(torch.int16).cpu().numpy().view(np.uint16)
+    bth, sh = bt.cpu().numpy(), seq0.cpu().numpy()
+    kh = np.zeros((num_blocks, bs, H, D), np.uint16)
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < 2.0:
+        OK.kv_write(yh, Nq, Nq + Nkv, H, D, bth, sh, k + 1, 0, kh, kh)
+        n += 1
+    secs = time.perf_counter() - t0
+    return {"sizes": f"B={B} k={k} H={H} D={D} block_size={bs}", **res,
+            "oracle": {"rows_per_s": n * wl.Mv / secs, "cores": 1, "sample": f"{n} verify passes, numpy"},
+            "note": "a copy of a few MB: launch latency bounds it, not HBM",
+            "l2": "L2 flushed before each timed call"}
+
+
 def run_e2e(torch, ml, wl, stream, side, steps, world):
     """Host buffers in, host buffers out, through the public binding.  Every
     step copies its activations, adapter indices and probabilities from
@@ -930,6 +1000,10 @@ def run_gpu(args):
         softmax_row = measure_softmax_row(torch, ml, wl, device, stream, 30, peaks, flush)
     except Exception as exc:
         softmax_row = {"failed": f"{type(exc).__name__}: {exc}"}
+    try:
+        kv_cache = measure_kv_cache(torch, ml, wl, device, stream, 30, peaks, flush)
+    except Exception as exc:
+        kv_cache = {"failed": f"{type(exc).__name__}: {exc}"}
     alpha_hat = ml.estimate_acceptance(wl.accepted.cpu().numpy(), wl.k)
     cpu = None
     if rank == 0 and world == 1:
@@ -1012,6 +1086,7 @@ def run_gpu(args):
             "configs": extra,
             "accept_sweep": sweep,
             "softmax_and_draft_draw": softmax_row,
+            "kv_cache": kv_cache,
             "draft_gate": gate,
         }
         print(json.dumps(line))

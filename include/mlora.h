@@ -93,6 +93,8 @@ typedef enum {
 #define MLORA_DEV_BAD_PLAN    (1u << 6) /* a plan entry read by a layer kernel was out of range (the
                                            workspace's plan was overwritten, or made for other
                                            sizes): the access was skipped, outputs are wrong    */
+#define MLORA_DEV_BAD_SLOT    (1u << 7) /* a KV row's slot was outside the cache or the request's
+                                           block table: the row was not written                 */
 
 /* Supported ranges. */
 #define MLORA_MAX_RANK 64          /* r_max <= 64, r_max % 8 == 0 */
@@ -355,6 +357,54 @@ MLORA_API size_t mlora_draft_sample_workspace_bytes(int B, int V);
 MLORA_API mlora_status mlora_draft_sample(const float *z_draft, int B, int V, const float *uniforms,
                                           int32_t *draft_tok, float *q_out, void *workspace, size_t ws_bytes,
                                           mlora_stream stream);
+
+/* ------------------------------------------------------------------------- */
+/* Hybrid KV cache                                                            */
+/* ------------------------------------------------------------------------- */
+
+/* The InvisibleLoRA abstract has one KV cache for both passes: the LoRA-off
+ * drafter writes its speculative K/V entries into the cache of the LoRA-on
+ * target, and the verification pass overwrites them, so the drafter reads
+ * LoRA-conditioned K/V for the committed prefix and needs no cache of its
+ * own.  The pages give no layout; this one is a paged cache:
+ *   k_cache, v_cache  bf16 [num_blocks, block_size, H, D] each (caller-owned,
+ *                     16-byte aligned for the vectorised copy, else a slower
+ *                     word-by-word copy);
+ *   block_table       int32 [B, max_blocks]: request b's position pos lives in
+ *                     block block_table[b][pos / block_size] at offset
+ *                     pos % block_size;
+ *   seq_len           int32 [B]: request b's committed tokens (K/V in the cache
+ *                     with LoRA-on values); negative = unused request slot.
+ *
+ * mlora_kv_write copies the K and V rows of one pass:
+ *   y       bf16 [M, ld]: the fused q|k|v projection's output (mlora_linear
+ *           or mlora_linear_sliced); K of row m = y[m, k_col : k_col + H*D],
+ *           V = y[m, v_col : v_col + H*D], H heads of D contiguous values;
+ *   rows_per_req  1 for a draft step (one row per request), k + 1 for the
+ *           verify pass: row m is request m / rows_per_req at step
+ *           t = m % rows_per_req (M <= B * rows_per_req);
+ *   t0      the draft step (0 .. k-1) in the draft pass, 0 in the verify pass:
+ *           row m goes to position seq_len[b] + t0 + t.
+ * So in one decode cycle draft step t writes position L + t (L = seq_len[b]),
+ * the verify pass writes L .. L + k over them, and mlora_kv_commit then sets
+ * seq_len[b] = L + accepted[b] + 1 (the pending token and the kept drafts);
+ * slots past it are stale and the next cycle overwrites them.
+ * A slot outside [0, num_blocks) or past the table is not written and raises
+ * MLORA_DEV_BAD_SLOT; rows of unused request slots are skipped.  Asynchronous
+ * on `stream`; the workspace (any of this library's, at least
+ * mlora_kv_workspace_bytes() bytes) holds only the status word.  Returns
+ * MLORA_ERR_SHAPE for sizes outside the ranges (column ranges past ld,
+ * M > B * rows_per_req, H*D > 2^20), MLORA_ERR_ARG for a null pointer (y may
+ * be NULL when M = 0). */
+MLORA_API size_t mlora_kv_workspace_bytes(void);
+MLORA_API mlora_status mlora_kv_write(const void *y, int M, int ld, int k_col, int v_col, int H, int D,
+                                      const int32_t *block_table, int B, int max_blocks, const int32_t *seq_len,
+                                      int rows_per_req, int t0, void *k_cache, void *v_cache, int num_blocks,
+                                      int block_size, void *workspace, size_t ws_bytes, mlora_stream stream);
+
+/* seq_len[b] += accepted[b] + 1 for every used request slot (seq_len[b] >= 0);
+ * accepted as the accept step writes it (0..k).  Asynchronous on `stream`. */
+MLORA_API mlora_status mlora_kv_commit(const int32_t *accepted, int B, int32_t *seq_len, mlora_stream stream);
 
 /* ------------------------------------------------------------------------- */
 /* Run-time draft gate (host functions; no GPU needed)                        */

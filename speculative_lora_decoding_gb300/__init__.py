@@ -11,6 +11,7 @@ device is not compute capability 10.3, the calls raise.
     verify_accept(p, q, draft_tok, uniforms)                             steps a5-a6
     verify_accept_logits(z_p, z_q, draft_tok, uniforms)                  the same on logits (softmax fused)
     softmax(z), draft_sample(z_q, uniforms)                              logits -> probabilities; draft draw
+    kv_write(y, ...), kv_commit(accepted, seq_len)                       hybrid KV cache (paged)
     plan_segments(...), shrink(...)                                      steps a1, a2 alone
 
 The layer is y = W x (draft, LoRA off) or y = W x + scale * B_a (A_a x)
@@ -41,6 +42,7 @@ DEV_BAD_TOKEN = 1 << 3
 DEV_ZERO_MASS = 1 << 4
 DEV_TIMEOUT = 1 << 5
 DEV_BAD_PLAN = 1 << 6
+DEV_BAD_SLOT = 1 << 7
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmlora.so")
 HEADER_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mlora.h")
@@ -81,6 +83,10 @@ _SIGNATURES = {
     "mlora_draft_gate": (_c_int, [ctypes.POINTER(ctypes.c_double), _c_int, ctypes.c_double, ctypes.c_double,
                                   ctypes.POINTER(ctypes.c_double)]),
     "mlora_estimate_acceptance": (ctypes.c_double, [ctypes.POINTER(ctypes.c_int32), _c_int, _c_int]),
+    "mlora_kv_workspace_bytes": (_c_size, []),
+    "mlora_kv_write": (_c_int, [_c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr, _c_int, _c_int,
+                                _c_ptr, _c_int, _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_ptr, _c_size, _c_ptr]),
+    "mlora_kv_commit": (_c_int, [_c_ptr, _c_int, _c_ptr, _c_ptr]),
     "mlora_status_string": (ctypes.c_char_p, [_c_int]),
     "mlora_device_supported": (_c_int, []),
     "mlora_launch_count": (ctypes.c_uint64, []),
@@ -385,6 +391,46 @@ def draft_sample(z_draft: torch.Tensor, uniforms: torch.Tensor, ws: Workspace = 
                                     _stream(stream))
     _check(st, "draft_sample")
     return tok, q
+
+
+def kv_workspace_bytes() -> int:
+    return int(_load().mlora_kv_workspace_bytes())
+
+
+def kv_write(y: torch.Tensor, k_col: int, v_col: int, H: int, D: int, block_table: torch.Tensor,
+             seq_len: torch.Tensor, rows_per_req: int, t0: int, k_cache: torch.Tensor, v_cache: torch.Tensor,
+             ws: Workspace = None, stream=None):
+    """Hybrid KV cache: the K and V rows of one pass (y bf16 [M, ld], the fused
+    q|k|v output) into the paged caches k_cache, v_cache bf16
+    [num_blocks, block_size, H, D].  Row m is request m // rows_per_req at step
+    m % rows_per_req and goes to position seq_len[b] + t0 + step."""
+    M, ld = y.shape
+    B, max_blocks = block_table.shape
+    num_blocks, block_size = k_cache.shape[0], k_cache.shape[1]
+    if tuple(k_cache.shape) != (num_blocks, block_size, H, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must both be [num_blocks, block_size, H, D]")
+    if seq_len.numel() != B:
+        raise ValueError("seq_len must have one entry per block-table row")
+    if ws is None:
+        ws = Workspace(kv_workspace_bytes(), device=y.device, stream=stream)
+    st = _load().mlora_kv_write(_need(y, "y", torch.bfloat16, 2), M, ld, int(k_col), int(v_col), int(H), int(D),
+                                _need(block_table, "block_table", torch.int32, 2), B, max_blocks,
+                                _need(seq_len, "seq_len", torch.int32, 1), int(rows_per_req), int(t0),
+                                _need(k_cache, "k_cache", torch.bfloat16, 4), _need(v_cache, "v_cache", torch.bfloat16, 4),
+                                num_blocks, block_size, ws.ptr, ws.nbytes, _stream(stream))
+    _check(st, "kv_write")
+    return k_cache, v_cache
+
+
+def kv_commit(accepted: torch.Tensor, seq_len: torch.Tensor, stream=None) -> torch.Tensor:
+    """seq_len[b] += accepted[b] + 1 for every used request slot (in place)."""
+    B = seq_len.numel()
+    if accepted.numel() != B:
+        raise ValueError("accepted and seq_len must have the same length")
+    st = _load().mlora_kv_commit(_need(accepted, "accepted", torch.int32, 1), B, _need(seq_len, "seq_len", torch.int32, 1),
+                                 _stream(stream))
+    _check(st, "kv_commit")
+    return seq_len
 
 
 def draft_gate(t_cycle: dict, t_plain: float, alpha: float):

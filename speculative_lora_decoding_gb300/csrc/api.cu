@@ -400,6 +400,48 @@ mlora_status mlora_draft_sample(const float *z_draft, int B, int V, const float 
   return cuda_status(e);
 }
 
+size_t mlora_kv_workspace_bytes(void) { return WS_INIT_BYTES; }
+
+mlora_status mlora_kv_write(const void *y, int M, int ld, int k_col, int v_col, int H, int D,
+                            const int32_t *block_table, int B, int max_blocks, const int32_t *seq_len,
+                            int rows_per_req, int t0, void *k_cache, void *v_cache, int num_blocks, int block_size,
+                            void *workspace, size_t ws_bytes, mlora_stream stream) {
+  if (M < 0 || M > MLORA_MAX_ROWS || B < 1 || B > MLORA_MAX_ROWS || rows_per_req < 1 ||
+      (long long)M > (long long)B * rows_per_req || H < 1 || D < 1 || (long long)H * D > (1 << 20) || t0 < 0 ||
+      max_blocks < 1 || num_blocks < 1 || block_size < 1 || k_col < 0 || v_col < 0 ||
+      (long long)k_col + (long long)H * D > ld || (long long)v_col + (long long)H * D > ld)
+    return MLORA_ERR_SHAPE;
+  if ((M > 0 && !y) || !block_table || !seq_len || !k_cache || !v_cache) return MLORA_ERR_ARG;  // y may be empty
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < mlora_kv_workspace_bytes()) return MLORA_ERR_WORKSPACE;
+  const int sms = device_sms();
+  if (sms <= 0) return MLORA_ERR_CUDA;
+  KvWrite a;
+  a.y = (const uint16_t *)y;
+  a.M = M;
+  a.ld = ld;
+  a.k_col = k_col;
+  a.v_col = v_col;
+  a.HD = H * D;
+  a.block_table = block_table;
+  a.B = B;
+  a.max_blocks = max_blocks;
+  a.seq_len = seq_len;
+  a.rows_per_req = rows_per_req;
+  a.t0 = t0;
+  a.k_cache = (uint16_t *)k_cache;
+  a.v_cache = (uint16_t *)v_cache;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.status = reinterpret_cast<uint32_t *>((uint8_t *)workspace + WS_STATUS_OFF);
+  return cuda_status(launch_kv_write(a, sms, (cudaStream_t)stream));
+}
+
+mlora_status mlora_kv_commit(const int32_t *accepted, int B, int32_t *seq_len, mlora_stream stream) {
+  if (B < 1 || B > MLORA_MAX_ROWS) return MLORA_ERR_SHAPE;
+  if (!accepted || !seq_len) return MLORA_ERR_ARG;
+  return cuda_status(launch_kv_commit(accepted, B, seq_len, (cudaStream_t)stream));
+}
+
 double mlora_expected_tokens(double alpha, int k) {
   if (k < 0 || !(alpha >= 0.0 && alpha <= 1.0)) return 0.0;
   // 1 + alpha + ... + alpha^k by Horner's rule (stable as alpha -> 1).

@@ -129,4 +129,20 @@ size_t draft_sample_scratch_bytes(int B, int V);
 cudaError_t launch_draft_sample(const float *z, int B, int V, const float *u, int32_t *tok, float2 *stats, float *q,
                                 void *scratch, uint32_t *counters, uint32_t *status, cudaStream_t s);
 
+// Hybrid KV cache (kvcache.cu): the K/V rows of one pass into the paged
+// cache, and the committed lengths after the accept step.
+struct KvWrite {
+  const uint16_t *y;
+  int M, ld, k_col, v_col, HD;
+  const int32_t *block_table;
+  int B, max_blocks;
+  const int32_t *seq_len;
+  int rows_per_req, t0;
+  uint16_t *k_cache, *v_cache;
+  int num_blocks, block_size;
+  uint32_t *status;
+};
+cudaError_t launch_kv_write(const KvWrite &a, int num_sms, cudaStream_t s);
+cudaError_t launch_kv_commit(const int32_t *accepted, int B, int32_t *seq_len, cudaStream_t s);
+
 }  // namespace mlora

@@ -77,3 +77,28 @@ def test_sliced_host_checks(lib):
     assert lib.mlora_linear_sliced_workspace_bytes(128, 6144, 4096, 16, 3) > \
         lib.mlora_linear_sliced_workspace_bytes(128, 6144, 4096, 16, 1) == lib.mlora_linear_workspace_bytes(128, 6144, 4096, 16)
     assert lib.mlora_linear_sliced_workspace_bytes(128, 6144, 4096, 16, 5) == 0
+
+
+def test_kv_host_checks(lib):
+    """Sizes and pointers of the KV-cache calls are checked on the host, before any CUDA call."""
+    p = ctypes.c_void_p(256)
+    SHAPE, ARG, WS = 2, 1, 3
+    big = 1 << 20
+
+    def call(y=p, M=4, ld=48, k_col=16, v_col=32, H=2, D=8, B=2, max_blocks=4, rpr=2, t0=0, nb=8, bs=16, ws=p,
+             wsb=big):
+        return lib.mlora_kv_write(y, M, ld, k_col, v_col, H, D, p, B, max_blocks, p, rpr, t0, p, p, nb, bs, ws, wsb,
+                                  None)
+
+    assert call(M=5) == SHAPE                  # more rows than B * rows_per_req
+    assert call(v_col=33) == SHAPE             # V columns past ld
+    assert call(k_col=-1) == SHAPE
+    assert call(H=0) == SHAPE
+    assert call(t0=-1) == SHAPE
+    assert call(bs=0) == SHAPE
+    assert call(y=None) == ARG
+    assert call(ws=None) == WS
+    assert call(wsb=16) == WS
+    assert lib.mlora_kv_workspace_bytes() > 0
+    assert lib.mlora_kv_commit(None, 4, None, None) == ARG
+    assert lib.mlora_kv_commit(p, 0, p, None) == SHAPE
