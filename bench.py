@@ -299,6 +299,19 @@ class StepWorkload:
         torch.cuda.synchronize(device) if device.type == "cuda" else None
         self.seg = None
         self.w_bytes_per_pass = sum(2 * P["N"] * P["K"] for P in self.proj)
+        self.fp8 = False
+        self.ws_fp8 = None
+
+    def enable_fp8(self):
+        """Draft passes on E4M3 copies of W (quantized once, per output row)."""
+        ml = self.ml
+        for P in self.proj:
+            if "W8" not in P:
+                P["W8"], P["sw"] = ml.quantize_rows_fp8(P["W"])
+        if self.ws_fp8 is None:
+            self.ws_fp8 = ml.Workspace(max(ml.linear_fp8_workspace_bytes(self.Md, P["N"], P["K"]) for P in self.proj),
+                                       device=self.p.device)
+        self.fp8 = True
 
     @property
     def workload(self):
@@ -316,6 +329,10 @@ class StepWorkload:
         out.append(("plan", "plan", None, plan))
         for d in range(self.k):
             for P in self.proj:
+                if self.fp8:
+                    out.append((f"draft{d}.{P['name']}", "draft", P, lambda P=P, d=d: ml.linear_fp8(
+                        P["xd"][d], P["W8"], P["sw"], ml.PREFETCH_WEIGHTS, ws=self.ws_fp8, y=P["yd"])))
+                    continue
                 out.append((f"draft{d}.{P['name']}", "draft", P, lambda P=P, d=d: ml.linear_sliced(
                     P["xd"][d], P["W"], P["ends"], None, None, None, None, cfg.scale, ml.DRAFT | ml.PREFETCH_WEIGHTS,
                     ws=self.ws_draft, y=P["yd"])))
@@ -782,6 +799,47 @@ def measure_softmax_row(torch, ml, wl, device, stream, reps, peaks, flush):
     }
 
 
+def measure_fp8_draft(torch, ml, wl, stream, side, steps, peaks, flush, bf16_step_ms, bf16_draft_us):
+    """The same decode step with the draft passes on E4M3 weights: step time,
+    draft-pass time and bytes (W codes + x + its codes + y), and the quality
+    of each draft projection against its bf16 output (relative error)."""
+    hbm_gbs = peaks[0]
+    wl.enable_fp8()
+    try:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                wl.step(side)
+        stream.synchronize()
+        graph = graph_of(torch, lambda: wl.step(side), stream)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        ms = time_replays(torch, graph, stream, steps)
+        op_ms = per_op_durations(torch, wl.ops(), stream, max(10, min(steps, 50)))
+        if wl.ws_fp8.status() != 0 or wl.ws.status() != 0:
+            raise RuntimeError("device status bits raised in the FP8 draft measurement")
+        k = wl.k
+        t_draft = sum(op_ms[f"draft{d}.{P['name']}"] for d in range(k) for P in wl.proj)
+        nbytes = k * sum(P["N"] * P["K"] + 4 * wl.Md * P["K"] + 2 * wl.Md * P["N"] for P in wl.proj)
+        quality = {}
+        for P in wl.proj:
+            y8 = ml.linear_fp8(P["xd"][0], P["W8"], P["sw"], ws=wl.ws_fp8).float()
+            y16 = ml.linear_sliced(P["xd"][0], P["W"], P["ends"], None, None, None, None, 1.0, ml.DRAFT,
+                                   ws=wl.ws_draft).float()
+            quality[P["name"]] = float(torch.linalg.norm(y8 - y16) / torch.linalg.norm(y16))
+        torch.cuda.synchronize()
+    finally:
+        wl.fp8 = False
+    return {"ms_per_step": ms, "tokens_per_s": wl.Mv / (ms * 1e-3), "speedup_vs_bf16_step": bf16_step_ms / ms,
+            "draft_pass": {"us_per_pass": 1e3 * t_draft / k, "GBps": nbytes / (t_draft * 1e-3) / 1e9,
+                           "frac_hbm": nbytes / (t_draft * 1e-3) / 1e9 / hbm_gbs,
+                           "speedup_vs_bf16_pass": bf16_draft_us / (1e3 * t_draft / k),
+                           "bytes_per_pass": nbytes / k},
+            "quality_rel_error_vs_bf16": quality,
+            "note": "draft passes on E4M3 W (per-row scales) and per-token E4M3 activations; verify pass and "
+                    "accept unchanged (bf16), so emitted tokens keep the target distribution"}
+
+
 KV_HEAD_DIM = 128  # head size of the 32B- and 8B-class shapes (q 5120 = 40 x 128, k/v 1024 = 8 x 128)
 
 
@@ -1004,6 +1062,11 @@ def run_gpu(args):
         kv_cache = measure_kv_cache(torch, ml, wl, device, stream, 30, peaks, flush)
     except Exception as exc:
         kv_cache = {"failed": f"{type(exc).__name__}: {exc}"}
+    try:
+        fp8_draft = measure_fp8_draft(torch, ml, wl, stream, side, min(args.steps, 100), peaks, flush, ms,
+                                      head["modes"]["draft_pass"]["us_per_pass"])
+    except Exception as exc:
+        fp8_draft = {"failed": f"{type(exc).__name__}: {exc}"}
     alpha_hat = ml.estimate_acceptance(wl.accepted.cpu().numpy(), wl.k)
     cpu = None
     if rank == 0 and world == 1:
@@ -1087,6 +1150,7 @@ def run_gpu(args):
             "accept_sweep": sweep,
             "softmax_and_draft_draw": softmax_row,
             "kv_cache": kv_cache,
+            "fp8_draft": fp8_draft,
             "draft_gate": gate,
         }
         print(json.dumps(line))

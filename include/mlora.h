@@ -359,6 +359,44 @@ MLORA_API mlora_status mlora_draft_sample(const float *z_draft, int B, int V, co
                                           mlora_stream stream);
 
 /* ------------------------------------------------------------------------- */
+/* FP8 base weights for the draft pass                                        */
+/* ------------------------------------------------------------------------- */
+
+/* The "LoRA Inference" glossary lists quantizing the base weights to 8 bits
+ * (INT8/FP8) among the serving optimisations that go with LoRA.  The
+ * InvisibleLoRA draft pass runs the base model alone (LoRA off), so it can
+ * read an E4M3 copy of W: half the bytes of the HBM-bound pass.  Drafts only
+ * propose tokens; the LoRA-on verify pass (bf16 W) and the accept step decide
+ * what is emitted, so the output distribution stays exact and only the
+ * acceptance rate can change.  Format and rounding (a reading; the pages fix
+ * neither): E4M3 (4 exponent bits, bias 7, 3 mantissa bits, largest finite
+ * 448), round to nearest with ties to even, saturating at 448; one fp32 scale
+ * per row, scale = amax / 448, code = E4M3(v / scale) (IEEE fp32 division);
+ * a zero row gets scale 1 and +0 codes.  Inputs must be finite. */
+
+/* Quantize bf16 rows src [R, K] (row-major) to E4M3 codes q [R, K] and fp32
+ * scales [R]: W once, per output row, before the draft passes.  K % 16 == 0;
+ * src and q 16-byte aligned.  Asynchronous on `stream`. */
+MLORA_API mlora_status mlora_quantize_rows_fp8(const mlora_bf16 *src, int R, int K, uint8_t *q, float *scale,
+                                               mlora_stream stream);
+
+/* The draft (LoRA-off) layer on FP8 weights:
+ *   y[m, n] = bf16_rn(x_scale[m] * w_scale[n] * sum_k Xq[m, k] * Wq[n, k])
+ * with x quantized per token row into the workspace by the same rule, W8 and
+ * w_scale from mlora_quantize_rows_fp8, products exact and sums in fp32 on
+ * the tensor cores (kind::f8f6f4).  x bf16 [M, K], W8 uint8 [N, K], y bf16
+ * [M, N]; 1 <= M <= 256, K % 16 == 0; x and W8 16-byte aligned.  flags: 0 or
+ * MLORA_PREFETCH_WEIGHTS (W8 is constant: its first tiles may stream before
+ * the preceding kernel ends).  Workspace: mlora_linear_fp8_workspace_bytes
+ * (M, N, K), initialised once with mlora_workspace_init; calls sharing it
+ * must not overlap.  MLORA_ERR_UNSUPPORTED if a CTA of the shape cannot be
+ * resident on every SM at once. */
+MLORA_API size_t mlora_linear_fp8_workspace_bytes(int M, int N, int K);
+MLORA_API mlora_status mlora_linear_fp8(const mlora_bf16 *x, int M, int K, const uint8_t *W8, const float *w_scale,
+                                        int N, mlora_bf16 *y, int flags, void *workspace, size_t ws_bytes,
+                                        mlora_stream stream);
+
+/* ------------------------------------------------------------------------- */
 /* Hybrid KV cache                                                            */
 /* ------------------------------------------------------------------------- */
 

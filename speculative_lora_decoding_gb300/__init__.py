@@ -12,6 +12,7 @@ device is not compute capability 10.3, the calls raise.
     verify_accept_logits(z_p, z_q, draft_tok, uniforms)                  the same on logits (softmax fused)
     softmax(z), draft_sample(z_q, uniforms)                              logits -> probabilities; draft draw
     kv_write(y, ...), kv_commit(accepted, seq_len)                       hybrid KV cache (paged)
+    quantize_rows_fp8(W), linear_fp8(x, W8, w_scale)                     draft pass on E4M3 weights
     plan_segments(...), shrink(...)                                      steps a1, a2 alone
 
 The layer is y = W x (draft, LoRA off) or y = W x + scale * B_a (A_a x)
@@ -83,6 +84,10 @@ _SIGNATURES = {
     "mlora_draft_gate": (_c_int, [ctypes.POINTER(ctypes.c_double), _c_int, ctypes.c_double, ctypes.c_double,
                                   ctypes.POINTER(ctypes.c_double)]),
     "mlora_estimate_acceptance": (ctypes.c_double, [ctypes.POINTER(ctypes.c_int32), _c_int, _c_int]),
+    "mlora_quantize_rows_fp8": (_c_int, [_c_ptr, _c_int, _c_int, _c_ptr, _c_ptr, _c_ptr]),
+    "mlora_linear_fp8_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "mlora_linear_fp8": (_c_int, [_c_ptr, _c_int, _c_int, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int, _c_ptr, _c_size,
+                                  _c_ptr]),
     "mlora_kv_workspace_bytes": (_c_size, []),
     "mlora_kv_write": (_c_int, [_c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr, _c_int, _c_int,
                                 _c_ptr, _c_int, _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_ptr, _c_size, _c_ptr]),
@@ -391,6 +396,41 @@ def draft_sample(z_draft: torch.Tensor, uniforms: torch.Tensor, ws: Workspace = 
                                     _stream(stream))
     _check(st, "draft_sample")
     return tok, q
+
+
+def quantize_rows_fp8(src: torch.Tensor, q: torch.Tensor = None, scale: torch.Tensor = None, stream=None):
+    """E4M3 codes (uint8 [R, K]) and fp32 row scales [R] of bf16 rows [R, K]."""
+    R, K = src.shape
+    if q is None:
+        q = torch.empty((R, K), dtype=torch.uint8, device=src.device)
+    if scale is None:
+        scale = torch.empty((R,), dtype=torch.float32, device=src.device)
+    st = _load().mlora_quantize_rows_fp8(_need(src, "src", torch.bfloat16, 2), R, K, _need(q, "q", torch.uint8, 2),
+                                         _need(scale, "scale", torch.float32, 1), _stream(stream))
+    _check(st, "quantize_rows_fp8")
+    return q, scale
+
+
+def linear_fp8_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(_load().mlora_linear_fp8_workspace_bytes(M, N, K))
+
+
+def linear_fp8(x: torch.Tensor, W8: torch.Tensor, w_scale: torch.Tensor, flags: int = 0, ws: Workspace = None,
+               y: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Draft (LoRA-off) layer on E4M3 weights from quantize_rows_fp8: bf16 [M, N]."""
+    M, K = x.shape
+    N, K2 = W8.shape
+    if K2 != K or w_scale.numel() != N:
+        raise ValueError("W8 [N, K] / w_scale [N] disagree with x [M, K]")
+    if ws is None:
+        ws = Workspace(linear_fp8_workspace_bytes(M, N, K), device=x.device, stream=stream)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    st = _load().mlora_linear_fp8(_need(x, "x", torch.bfloat16, 2), M, K, _need(W8, "W8", torch.uint8, 2),
+                                  _need(w_scale, "w_scale", torch.float32, 1), N, _need(y, "y", torch.bfloat16, 2),
+                                  int(flags), ws.ptr, ws.nbytes, _stream(stream))
+    _check(st, "linear_fp8")
+    return y
 
 
 def kv_workspace_bytes() -> int:

@@ -400,6 +400,82 @@ mlora_status mlora_draft_sample(const float *z_draft, int B, int V, const float 
   return cuda_status(e);
 }
 
+mlora_status mlora_quantize_rows_fp8(const mlora_bf16 *src, int R, int K, uint8_t *q, float *scale,
+                                     mlora_stream stream) {
+  if (R < 1 || K < 16 || (K % 16) != 0) return MLORA_ERR_SHAPE;
+  if (!src || !q || !scale) return MLORA_ERR_ARG;
+  if (!aligned(src, 16) || !aligned(q, 16)) return MLORA_ERR_ARG;
+  const int sms = device_sms();
+  if (sms <= 0) return MLORA_ERR_CUDA;
+  return cuda_status(launch_quantize_rows_e4m3((const uint16_t *)src, R, K, q, scale, sms, (cudaStream_t)stream));
+}
+
+// Workspace of the FP8 draft layer: the activations' codes and scales, then
+// the stream-K GEMM's partial sums.
+struct F8Layout {
+  size_t x8, xs, sk, total;
+};
+static F8Layout f8_layout(int M, int K, int sms) {
+  F8Layout L;
+  size_t o = WS_SCRATCH_OFF;
+  L.x8 = o;
+  o = align_up(o + (size_t)M * K, 256);
+  L.xs = o;
+  o = align_up(o + (size_t)M * 4, 256);
+  L.sk = o;
+  o = align_up(o + sk_partial_bytes(M, sms), 256);
+  L.total = o;
+  return L;
+}
+
+static bool f8_sizes_ok(int M, int N, int K) {
+  return M >= 1 && M <= 256 && N >= 1 && K >= 16 && (K % 16) == 0;
+}
+
+size_t mlora_linear_fp8_workspace_bytes(int M, int N, int K) {
+  if (!f8_sizes_ok(M, N, K)) return 0;
+  int sms = device_sms();
+  if (sms <= 0) sms = 160;
+  return f8_layout(M, K, sms).total;
+}
+
+mlora_status mlora_linear_fp8(const mlora_bf16 *x, int M, int K, const uint8_t *W8, const float *w_scale, int N,
+                              mlora_bf16 *y, int flags, void *workspace, size_t ws_bytes, mlora_stream stream) {
+  if (!f8_sizes_ok(M, N, K)) return MLORA_ERR_SHAPE;
+  if (!x || !W8 || !w_scale || !y) return MLORA_ERR_ARG;
+  if ((flags & ~MLORA_PREFETCH_WEIGHTS) != 0) return MLORA_ERR_ARG;
+  if (!aligned(x, 16) || !aligned(W8, 16)) return MLORA_ERR_ARG;
+  if (!workspace || !aligned(workspace, 256)) return MLORA_ERR_WORKSPACE;
+  const int sms = device_sms();
+  if (sms <= 0) return MLORA_ERR_CUDA;
+  const F8Layout L = f8_layout(M, K, sms);
+  if (ws_bytes < L.total) return MLORA_ERR_WORKSPACE;
+  const SkShape sk = sk_shape(M, N, K, sms, true);
+  if (!sk.ok) return MLORA_ERR_UNSUPPORTED;  // a CTA of this shape does not fit on every SM
+  uint8_t *ws = (uint8_t *)workspace;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t *x8 = ws + L.x8;
+  float *xs = reinterpret_cast<float *>(ws + L.xs);
+  cudaError_t e = launch_quantize_rows_e4m3((const uint16_t *)x, M, K, x8, xs, sms, s);
+  if (e != cudaSuccess) return MLORA_ERR_CUDA;
+  F8Launch g;
+  g.x8 = x8;
+  g.W8 = W8;
+  g.x_scale = xs;
+  g.w_scale = w_scale;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.prefetch_w = (flags & MLORA_PREFETCH_WEIGHTS) ? 1 : 0;
+  g.y = (uint16_t *)y;
+  g.status = reinterpret_cast<uint32_t *>(ws + WS_STATUS_OFF);
+  int err = 0;
+  e = launch_gemm_sk_f8(g, sk, reinterpret_cast<float *>(ws + L.sk), reinterpret_cast<uint32_t *>(ws + SK_FLAGS_OFF), s,
+                        &err);
+  if (err) return MLORA_ERR_ARG;
+  return cuda_status(e);
+}
+
 size_t mlora_kv_workspace_bytes(void) { return WS_INIT_BYTES; }
 
 mlora_status mlora_kv_write(const void *y, int M, int ld, int k_col, int v_col, int H, int D,

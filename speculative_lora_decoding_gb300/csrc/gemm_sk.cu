@@ -44,7 +44,7 @@ namespace mlora {
 
 constexpr int SK_THREADS = 192;
 constexpr int SK_BN = 128;                       // W rows per tile (MMA M)
-constexpr int SK_BK = 64;                        // K per stage: 128 bytes of bf16
+constexpr int SK_BK = 64;                        // K per stage: 128 bytes of bf16 (128 E4M3 values)
 constexpr int SK_WTILE = SK_BN * SK_BK * 2;      // 16 KB
 constexpr int SK_CHUNK = 32;                     // accumulator columns per tensor-memory load
 constexpr size_t SK_SMEM_LIMIT = 220 * 1024;     // leaves room for a co-resident shrink CTA
@@ -67,6 +67,8 @@ struct SkArgs {
   uint32_t *status;
   float *partials;  // [P][Mb][128]: a contributor's partial sums, token-major
   uint32_t *flags;  // [P]: 1 once CTA i's partial is written; the owner sets it back to 0
+  const float *w_scale;  // E4M3 operands: per W row and per token row scales of the codes
+  const float *x_scale;
 };
 
 __device__ __forceinline__ int sk_begin(const SkArgs &a, int i) { return (int)((long long)i * a.total / a.P); }
@@ -87,6 +89,10 @@ __device__ __forceinline__ int sk_slice_of(const SkArgs &a, int n0) {
   return s;
 }
 
+// F8: W and x are E4M3 codes (draft mode only): 128 values per 128-byte
+// k-block row, kind::f8f6f4 MMAs, and the epilogue applies the row scales,
+// y = bf16(acc * w_scale[n] * x_scale[m]).
+template <bool F8>
 __global__ void __launch_bounds__(SK_THREADS, 1)
     gemm_sk_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                    const __grid_constant__ CUtensorMap tmap_b, const SkArgs args) {
@@ -94,6 +100,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   uint8_t *ring = align_smem_1024(smem_raw);
   const int S = args.stages;
   const int stage_bytes = SK_WTILE + args.Mb * SK_BK * 2;
+  constexpr int KBE = F8 ? 2 * SK_BK : SK_BK;  // values per k-block (the TMA coordinate unit)
   // Expand records (one per stage) and the producer's staged plan records.
   ExpandStage *meta = reinterpret_cast<ExpandStage *>(ring + (size_t)S * stage_bytes);
   int4 *chunk = reinterpret_cast<int4 *>(meta + S);
@@ -112,7 +119,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   const int cta = blockIdx.x;
   const int KB = args.kblocks;
   const int g0 = sk_begin(args, cta), g1 = sk_begin(args, cta + 1);
-  const bool tc = args.sorted != 0 && args.mode == MLORA_VERIFY;
+  const bool tc = !F8 && args.sorted != 0 && args.mode == MLORA_VERIFY;
   const PlanLayout L = plan_layout(args.M, args.n_ad);
 
   if (threadIdx.x == 0) {
@@ -168,7 +175,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         for (int g = g0; g < g1 && early < S; ++g, ++early) {
           const int t = g / KB, kb = g - t * KB;
           mbar_arrive_expect_tx(&full[early], tx);
-          tma_load_2d(ring + (size_t)early * stage_bytes, &tmap_w, &full[early], kb * SK_BK, t * SK_BN, pol_w);
+          tma_load_2d(ring + (size_t)early * stage_bytes, &tmap_w, &full[early], kb * KBE, t * SK_BN, pol_w);
         }
       }
       if (waited) grid_dependency_wait();
@@ -184,9 +191,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[stage], tx);
-          tma_load_2d(st, &tmap_w, &full[stage], kb * SK_BK, t * SK_BN, pol_w);
+          tma_load_2d(st, &tmap_w, &full[stage], kb * KBE, t * SK_BN, pol_w);
         }
-        tma_load_2d(st + SK_WTILE, &tmap_x, &full[stage], kb * SK_BK, 0, pol_x);
+        tma_load_2d(st + SK_WTILE, &tmap_x, &full[stage], kb * KBE, 0, pol_x);
         ++issued;
         if (++stage == S) {
           stage = 0;
@@ -246,7 +253,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idesc = idesc_bf16_f32(SK_BN, args.Mb);
+    const uint32_t idesc = F8 ? idesc_e4m3_f32(SK_BN, args.Mb) : idesc_bf16_f32(SK_BN, args.Mb);
     const uint32_t ring0 = smem_addr(ring);
     const uint32_t sbytes = (uint32_t)stage_bytes;
     int stage = 0, seg = 0, ns = -1;
@@ -272,7 +279,12 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
           const uint64_t bd = smem_desc_kmajor_sw128(a_addr + SK_WTILE);
           const uint32_t first = kb > kb0 ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < SK_BK / 16; ++kk) mma_bf16_ss(acc, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : first);
+          for (int kk = 0; kk < SK_BK / 16; ++kk) {  // 32 bytes of K per instruction
+            if (F8)
+              mma_e4m3_ss(acc, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : first);
+            else
+              mma_bf16_ss(acc, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : first);
+          }
           mma_commit(&empty[stage]);
           issued_any = true;
           if (++stage == S) {
@@ -474,10 +486,17 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
               }
             }
             uint16_t *yn = args.y + n;
+            float wsn = 1.f, myxs = 1.f;  // E4M3: the scales of this thread's W row and of lane's token row
+            if (F8) {
+              wsn = n < args.N ? __ldg(args.w_scale + n) : 0.f;
+              myxs = myc < args.M ? __ldg(args.x_scale + myc) : 0.f;
+            }
 #pragma unroll
             for (int j = 0; j < SK_CHUNK; ++j) {
               const int row = __shfl_sync(0xffffffffu, myrow, j);
-              if (n < args.N && (whole || cb + j < q1) && row >= 0) yn[(size_t)row * args.N] = float_to_bf16_bits(v[j]);
+              const float xs = F8 ? __shfl_sync(0xffffffffu, myxs, j) : 1.f;
+              if (n < args.N && (whole || cb + j < q1) && row >= 0)
+                yn[(size_t)row * args.N] = float_to_bf16_bits(F8 ? v[j] * wsn * xs : v[j]);
             }
           }
           if (fetch) named_bar_sync(1, 128);  // the ring is refilled only after every thread read it
@@ -512,12 +531,13 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
 
 // One CTA of this shared-memory size fits on an SM (so a grid of one CTA per
 // SM is resident at once on an otherwise idle GPU).  Cached per device.
+template <bool F8>
 static bool sk_resident(size_t smem) {
   static int attr_done[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(gemm_sk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SK_SMEM_LIMIT) !=
+    if (cudaFuncSetAttribute(gemm_sk_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SK_SMEM_LIMIT) !=
         cudaSuccess) {
       cudaGetLastError();
       return false;
@@ -525,14 +545,14 @@ static bool sk_resident(size_t smem) {
     attr_done[dev] = 1;
   }
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_sk_kernel, SK_THREADS, smem) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemm_sk_kernel<F8>, SK_THREADS, smem) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
   return n >= 1;
 }
 
-SkShape sk_shape(int M, int N, int K, int num_sms) {
+SkShape sk_shape(int M, int N, int K, int num_sms, bool f8) {
   SkShape s = {};
   s.ok = false;
   if (M < 1 || M > SK_MAX_ROWS || num_sms <= 0) return s;
@@ -545,7 +565,8 @@ SkShape sk_shape(int M, int N, int K, int num_sms) {
   s.stages = st > SK_MAX_STAGES ? SK_MAX_STAGES : st;
   if (s.stages < 2) return s;
   s.n_tiles = (N + SK_BN - 1) / SK_BN;
-  s.kblocks = (K + SK_BK - 1) / SK_BK;
+  const int kbe = f8 ? 2 * SK_BK : SK_BK;  // values per 128-byte k-block row
+  s.kblocks = (K + kbe - 1) / kbe;
   s.total = s.n_tiles * s.kblocks;
   // Shares of at least ceil(kblocks / SK_MAX_PARTIALS) k-blocks: a tile then
   // meets at most SK_MAX_PARTIALS + 1 CTAs.
@@ -556,7 +577,7 @@ SkShape sk_shape(int M, int N, int K, int num_sms) {
   if (P < 1) P = 1;
   s.P = P;
   s.smem_bytes = SK_SMEM_FIXED + (size_t)s.stages * stage_bytes;
-  s.ok = sk_resident(s.smem_bytes);
+  s.ok = f8 ? sk_resident<true>(s.smem_bytes) : sk_resident<false>(s.smem_bytes);
   return s;
 }
 
@@ -583,15 +604,18 @@ static SkEncodeFn sk_encode_fn() {
 
 // Row-major bf16 [rows, cols] read in boxes of box_rows x box_cols (64 columns
 // with 128-byte swizzling, or 16 with 32-byte swizzling); out of range reads 0.
-static bool sk_map(CUtensorMap *map, const void *base, long long rows, int cols, int box_rows, int box_cols) {
+// bytes1: one-byte elements (E4M3 codes), boxes of 128 columns, 128-byte swizzle.
+static bool sk_map(CUtensorMap *map, const void *base, long long rows, int cols, int box_rows, int box_cols,
+                   bool bytes1 = false) {
   SkEncodeFn fn = sk_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * (bytes1 ? 1 : 2)};
   cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapSwizzle sw = box_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B;
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+  return fn(map, bytes1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -638,7 +662,44 @@ cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partia
   a.status = g.status;
   a.partials = partials;
   a.flags = flags;
-  cudaError_t e = launch_pdl(gemm_sk_kernel, dim3(sh.P), dim3(SK_THREADS), sh.smem_bytes, s, tw, tx, tb, a);
+  a.w_scale = nullptr;
+  a.x_scale = nullptr;
+  cudaError_t e = launch_pdl(gemm_sk_kernel<false>, dim3(sh.P), dim3(SK_THREADS), sh.smem_bytes, s, tw, tx, tb, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_gemm_sk_f8(const F8Launch &g, const SkShape &sh, float *partials, uint32_t *flags, cudaStream_t s,
+                              int *err_code) {
+  *err_code = 0;
+  if (!sh.ok) return cudaErrorInvalidValue;
+  CUtensorMap tw, tx;
+  if (!sk_map(&tw, g.W8, g.N, g.K, SK_BN, 2 * SK_BK, true) || !sk_map(&tx, g.x8, g.M, g.K, sh.Mb, 2 * SK_BK, true)) {
+    *err_code = 1;
+    return cudaErrorInvalidValue;
+  }
+  SkArgs a = {};
+  a.M = g.M;
+  a.N = g.N;
+  a.K = g.K;
+  a.Mb = sh.Mb;
+  a.kblocks = sh.kblocks;
+  a.total = sh.total;
+  a.P = sh.P;
+  a.stages = sh.stages;
+  a.cols = sh.cols;
+  a.mode = MLORA_DRAFT;
+  a.prefetch_w = g.prefetch_w;
+  a.after_shrink = 0;
+  a.sorted = 0;
+  a.n_slices = 1;
+  for (int i = 0; i < MLORA_MAX_SLICES; ++i) a.slice_end[i] = g.N;
+  a.y = g.y;
+  a.status = g.status;
+  a.partials = partials;
+  a.flags = flags;
+  a.w_scale = g.w_scale;
+  a.x_scale = g.x_scale;
+  cudaError_t e = launch_pdl(gemm_sk_kernel<true>, dim3(sh.P), dim3(SK_THREADS), sh.smem_bytes, s, tw, tx, tw, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -96,10 +96,26 @@ struct SkShape {
   int Mb, cols, stages, n_tiles, kblocks, total, P;
   size_t smem_bytes;
 };
-SkShape sk_shape(int M, int N, int K, int num_sms);
+SkShape sk_shape(int M, int N, int K, int num_sms, bool f8 = false);
 size_t sk_partial_bytes(int M, int num_sms);
 cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partials, uint32_t *flags, cudaStream_t s,
                            int *err_code);
+
+// The draft layer on E4M3 codes (fp8.cu quantizes; the stream-K kernel with
+// kind::f8f6f4 MMAs multiplies): y = bf16(acc * w_scale[n] * x_scale[m]).
+struct F8Launch {
+  const uint8_t *x8, *W8;
+  const float *x_scale, *w_scale;
+  int M, N, K, prefetch_w;
+  uint16_t *y;
+  uint32_t *status;
+};
+cudaError_t launch_gemm_sk_f8(const F8Launch &g, const SkShape &sh, float *partials, uint32_t *flags, cudaStream_t s,
+                              int *err_code);
+// Per-row E4M3 quantization of bf16 rows [R, K]: scale[r] = amax / 448,
+// q[r, k] = e4m3_rn_satfinite(src[r, k] / scale[r]); a zero row gets scale 1.
+cudaError_t launch_quantize_rows_e4m3(const uint16_t *src, int R, int K, uint8_t *q, float *scale, int num_sms,
+                                      cudaStream_t s);
 
 // Steps a5 + a6.  With stats_p and stats_q non-null, p and q hold logits and
 // the kernels read probabilities expf(z - m) / S from the rows' statistics.

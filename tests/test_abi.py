@@ -102,3 +102,17 @@ def test_kv_host_checks(lib):
     assert lib.mlora_kv_workspace_bytes() > 0
     assert lib.mlora_kv_commit(None, 4, None, None) == ARG
     assert lib.mlora_kv_commit(p, 0, p, None) == SHAPE
+
+
+def test_fp8_host_checks(lib):
+    p = ctypes.c_void_p(256)
+    SHAPE, ARG, WS = 2, 1, 3
+    assert lib.mlora_linear_fp8_workspace_bytes(128, 5120, 5120) > 0
+    assert lib.mlora_linear_fp8_workspace_bytes(257, 5120, 5120) == 0   # the stream-K kernel's 256 rows
+    assert lib.mlora_linear_fp8_workspace_bytes(128, 5120, 5128) == 0   # K % 16 != 0
+    assert lib.mlora_linear_fp8(p, 128, 5128, p, p, 64, p, 0, p, 1 << 30, None) == SHAPE
+    assert lib.mlora_linear_fp8(None, 128, 512, p, p, 64, p, 0, p, 1 << 30, None) == ARG
+    assert lib.mlora_linear_fp8(p, 128, 512, p, p, 64, p, 7, p, 1 << 30, None) == ARG   # unknown flag
+    assert lib.mlora_linear_fp8(p, 128, 512, p, p, 64, p, 0, None, 0, None) == WS
+    assert lib.mlora_quantize_rows_fp8(p, 4, 24, p, p, None) == SHAPE
+    assert lib.mlora_quantize_rows_fp8(None, 4, 32, p, p, None) == ARG
