@@ -376,43 +376,34 @@ __global__ void __launch_bounds__(ACC_THREADS)
 }
 
 // ---------------------------------------------------------------------------
-// Streaming form, for rows of 16-byte aligned float4 (V % 4 == 0), in two
-// kernels.
+// Streaming form, for rows of 16-byte aligned float4 (V % 4 == 0), in three
+// kernels chained by programmatic dependent launch.
 //
-// accept_stream_kernel: one CTA per SM at most; CTA g owns the units
-// (request, chunk) u = g + i G, so a rejected request's reloads spread over
-// many SMs.  Warp 8 streams chunks into a ring of RING_STAGES shared-memory
-// stages with bulk copies; warps 0-7 run the accept tests of the units'
-// requests, then each takes its own 512-entry block of every ring item and
-// writes the block's exact sums.  Every wait is on an mbarrier, bounded,
-// and taken in order by every thread that takes it (so each parity wait is
-// on its current phase).
+// accept_test_kernel: step a5 for every request (kp = k rounded up to a
+// power of two lanes per request, 32 / kp requests per warp): n_out[b] = the
+// first rejected position, or k.
 //
-// accept_draw_kernel (programmatic dependent launch, one warp per request):
-// the block sums give the totals, the chunk and then the block holding the
-// draw; one read of that block's 512 entries finds the token.
+// accept_blocks_kernel: one CTA of 8 warps per unit (request, 4096-entry
+// chunk); warp w sums block w (512 entries, 16 per lane loaded as four
+// 16-byte pieces before any is used) of the row the draw needs: p_k (bonus)
+// when all k drafts were kept, else p_n and q_n (residual).  Every unit's
+// loads are in flight at once across the resident CTAs (no shared-memory
+// staging: the latency is hidden by the number of warps, not by a ring), and
+// bonus and residual units take separate code paths, so neither issues the
+// other's instructions.  Its output: the exact fixed-point sums of each
+// block, (residual, target).
+//
+// accept_draw_kernel (one warp per request): the block sums give the totals,
+// the chunk and then the block holding the draw; one read of that block's
+// 512 entries finds the token.
 // ---------------------------------------------------------------------------
-constexpr int RING_STAGES = 14;
-constexpr int RING_CONSUMERS = 8;
-constexpr int PRODUCER_WARP = RING_CONSUMERS;
-constexpr int RING_THREADS = (RING_CONSUMERS + 1) * 32;
-constexpr int BLOCK = CHUNK / RING_CONSUMERS;  // 512 entries of an item per consumer warp
-constexpr int RING_MAX_UNITS = 128;            // units of one CTA
-constexpr int STAGE_FLOATS = CHUNK;
-constexpr int DRAW_WARPS = 4;  // small CTAs: they fit beside a streaming CTA while they wait
+constexpr int BLK_WARPS = 8;
+constexpr int BLK_THREADS = BLK_WARPS * 32;
+constexpr int BLOCK = CHUNK / BLK_WARPS;  // 512 entries of a unit per warp
+constexpr int TEST_THREADS = 256;
+constexpr int DRAW_WARPS = 4;
 constexpr uint32_t ONE_BITS = 0x3F800000u;  // bit pattern of 1.0f: every f in [0, 1] has bits <= it
 constexpr uint32_t BIAS_BITS = 0x4B000000u; // bit pattern of 2^23
-
-enum : int { ITEM_DISCARD = 0, ITEM_BONUS = 1, ITEM_RESIDUAL = 2 };
-
-struct RingShared {
-  uint64_t full[RING_STAGES], empty[RING_STAGES];
-  uint64_t a5_done;
-  int n[RING_MAX_UNITS];  // accepted count of each unit's request
-  int abort_flag, zero_word;
-};
-constexpr size_t RING_SMEM = (size_t)RING_STAGES * STAGE_FLOATS * 4 + sizeof(RingShared) + 1024;
-static_assert(RING_SMEM <= 232448, "ring exceeds the shared memory of a CTA");
 
 // Q(f) = floor(f * 2^40) for f in [0, 1] as hi * 2^23 + lo, with FP32
 // operations only: y = 2^23 + floor(f 2^17) (fused multiply-add rounding
@@ -431,265 +422,158 @@ __device__ __forceinline__ QBits q_bits(float f) {
   return {__float_as_uint(y), __float_as_uint(z)};
 }
 
-__device__ __forceinline__ void ring_abort(RingShared &rs, uint32_t *status) {
-  *reinterpret_cast<volatile int *>(&rs.abort_flag) = 1;
-  raise_status(status, MLORA_DEV_TIMEOUT);
+template <bool LG>
+__global__ void __launch_bounds__(TEST_THREADS)
+    accept_test_kernel(const float *__restrict__ p, const float *__restrict__ q,
+                       const int32_t *__restrict__ draft_tok, const float *__restrict__ uni, int B, int k, int V,
+                       int32_t *__restrict__ n_out, uint32_t *status, const float2 *__restrict__ sp,
+                       const float2 *__restrict__ sq) {
+  grid_launch_dependents();
+  grid_dependency_wait();
+  const int lane = threadIdx.x & 31;
+  const int k1 = k + 1;
+  const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));
+  const int per = 32 / kp, slot = lane / kp, pos = lane % kp;
+  const int b = (blockIdx.x * TEST_THREADS + threadIdx.x) / 32 * per + slot;
+  const bool live = b < B && pos < k;
+  uint32_t f = 0;
+  bool pass = true;
+  if (live) {
+    const int x = draft_tok[(size_t)b * k + pos];
+    if (x < 0 || x >= V) {
+      f |= MLORA_DEV_BAD_TOKEN;
+      pass = false;
+    } else {
+      const float pi =
+          sanitize_prob(as_prob<LG>(p[((size_t)b * k1 + pos) * V + x], row_st<LG>(sp, (size_t)b * k1 + pos)), f);
+      const float qi =
+          sanitize_prob(as_prob<LG>(q[((size_t)b * k + pos) * V + x], row_st<LG>(sq, (size_t)b * k + pos)), f);
+      const float ui = sanitize_uniform(uni[(size_t)b * k1 + pos], f);
+      pass = (double)ui * (double)qi < (double)pi;
+    }
+  }
+  // n = the first failing position of this lane's request, else k; flags
+  // count from positions up to and including n only.
+  const uint32_t fails = __ballot_sync(0xffffffffu, live && !pass);
+  const uint32_t mine = kp == 32 ? fails : (fails >> (slot * kp)) & ((1u << kp) - 1u);
+  const int n = mine ? __ffs(mine) - 1 : k;
+  if (live && pos <= n && f) raise_status(status, f);
+  if (b < B && pos == 0) n_out[b] = n;
 }
 
-// blk: [B * chunks units][8 blocks][2] uint64 (residual, target);
-// n_out: [B] accepted count, written by the unit holding chunk 0.
+// The four 16-byte pieces of lane `lane` in block `w` of the chunk at float4
+// index c4 of `row` (entries past V read as 0: weight 0).
 template <bool LG>
-__global__ void __launch_bounds__(RING_THREADS, 1)
-    accept_stream_kernel(const float *__restrict__ p, const float *__restrict__ q,
-                         const int32_t *__restrict__ draft_tok, const float *__restrict__ uni, int B, int k, int V,
-                         int chunks, uint64_t *__restrict__ blk, int32_t *__restrict__ n_out, uint32_t *status,
-                         const float2 *__restrict__ sp, const float2 *__restrict__ sq) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t *smem = align_smem_1024(smem_raw);
-  float *stages = reinterpret_cast<float *>(smem);
-  RingShared &rs = *reinterpret_cast<RingShared *>(smem + (size_t)RING_STAGES * STAGE_FLOATS * 4);
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int k1 = k + 1;
-  const int U = B * chunks, G = gridDim.x, g = blockIdx.x;
-  const int nU = g < U ? (U - g + G - 1) / G : 0;
-  if (nU <= 0) return;
-  if (nU > RING_MAX_UNITS) {  // excluded by the host's choice of grid
-    if (tid == 0) raise_status(status, MLORA_DEV_TIMEOUT);
-    return;
+__device__ __forceinline__ void load_block(const float *row, int c4, int len4, int w, int lane, float (&a)[16],
+                                           float2 st) {
+  const float4 *r4 = reinterpret_cast<const float4 *>(row) + c4;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e4 = w * (BLOCK / 4) + lane + 32 * j;
+    const float4 v = e4 < len4 ? __ldcs(r4 + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    a[4 * j + 0] = v.x, a[4 * j + 1] = v.y, a[4 * j + 2] = v.z, a[4 * j + 3] = v.w;
   }
-  const int R = min(RING_STAGES, nU);
-
-  if (tid == 0) {
-    for (int s = 0; s < RING_STAGES; ++s) {
-      mbar_init(&rs.full[s], 1);
-      mbar_init(&rs.empty[s], RING_CONSUMERS);
-    }
-    mbar_init(&rs.a5_done, RING_CONSUMERS);
-    rs.abort_flag = 0;
-    rs.zero_word = 0;
-    fence_mbar_init();
-  }
-  grid_launch_dependents();
-  block_sync();
-  grid_dependency_wait();
-  volatile int *ab = &rs.abort_flag;
-
-  // The issue order (and the order producer and consumers walk the items
-  // in), over this CTA's units i < nU:
-  //  1. the bonus chunks of units i < R, before the tests resolve;
-  //  2. p_n and q_n chunks of those units whose request was rejected (their
-  //     bonus chunks are dropped);
-  //  3. units i >= R: the bonus chunk, or p_n and q_n.
-  // ITEM_RESIDUAL items take two consecutive slots, the others one.
-  auto rejected = [&](int i) { return rs.n[i] < k; };
-  auto walk = [&](auto &&f) {
-    for (int i = 0; i < R; ++i)
-      if (!f(i, rejected(i) ? ITEM_DISCARD : ITEM_BONUS)) return;
-    for (int i = 0; i < R; ++i)
-      if (rejected(i) && !f(i, ITEM_RESIDUAL)) return;
-    for (int i = R; i < nU; ++i)
-      if (!f(i, rejected(i) ? ITEM_RESIDUAL : ITEM_BONUS)) return;
-  };
-
-  if (warp == PRODUCER_WARP) {
-    // Phase 1, lane i: unit i into stage i (no stage is in use yet).
-    if (lane < R) {
-      const int u = g + lane * G, b = u / chunks, c = u - b * chunks;
-      const uint32_t bytes = (uint32_t)min(CHUNK, V - c * CHUNK) * 4u;
-      mbar_arrive_expect_tx(&rs.full[lane], bytes);
-      bulk_load(stages + (size_t)lane * STAGE_FLOATS, p + ((size_t)b * k1 + k) * V + (size_t)c * CHUNK, bytes,
-                &rs.full[lane]);
-    }
-    if (lane != 0) return;
-    int issued = R, st = R == RING_STAGES ? 0 : R;
-    uint32_t ph = R == RING_STAGES ? 1u : 0u;
-    auto issue = [&](const float *row, int c) -> bool {
-      if (issued >= RING_STAGES && !mbar_wait_bounded(&rs.empty[st], ph ^ 1u, ab)) return false;
-      const uint32_t bytes = (uint32_t)min(CHUNK, V - c * CHUNK) * 4u;
-      mbar_arrive_expect_tx(&rs.full[st], bytes);
-      bulk_load(stages + (size_t)st * STAGE_FLOATS, row + (size_t)c * CHUNK, bytes, &rs.full[st]);
-      ++issued;
-      if (++st == RING_STAGES) {
-        st = 0;
-        ph ^= 1u;
-      }
-      return true;
-    };
-    bool ok = mbar_wait_bounded(&rs.a5_done, 0u, ab);
-    if (ok) {
-      int item = 0;
-      walk([&](int i, int kind) -> bool {
-        if (item++ < R) return true;  // phase 1, issued above
-        const int u = g + i * G, b = u / chunks, c = u - b * chunks, n = rs.n[i];
-        if (kind == ITEM_BONUS) return ok = issue(p + ((size_t)b * k1 + k) * V, c);
-        return ok = issue(p + ((size_t)b * k1 + n) * V, c) && issue(q + ((size_t)b * k + n) * V, c);
-      });
-    }
-    if (!ok) ring_abort(rs, status);
-    // Copies still in flight land before the CTA may exit.
-    for (int s = max(0, issued - RING_STAGES); s < issued; ++s)
-      if (!mbar_wait_bounded(&rs.full[s % RING_STAGES], (uint32_t)(s / RING_STAGES) & 1u, &rs.zero_word))
-        raise_status(status, MLORA_DEV_TIMEOUT);
-    return;
-  }
-
-  // Step a5 for every unit's request: kp = k rounded up to a power of two
-  // lanes per request, 32 / kp requests per warp and round.
-  {
-    const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));
-    const int per = 32 / kp, slot = lane / kp, pos = lane % kp;
-    for (int i0 = warp * per; i0 < nU; i0 += RING_CONSUMERS * per) {
-      const int i = i0 + slot;
-      const bool live = i < nU && pos < k;
-      uint32_t f = 0;
-      bool pass = true;
-      int b = 0;
-      if (i < nU) b = (g + i * G) / chunks;
-      if (live) {
-        const int x = draft_tok[(size_t)b * k + pos];
-        if (x < 0 || x >= V) {
-          f |= MLORA_DEV_BAD_TOKEN;
-          pass = false;
-        } else {
-          const float pi = sanitize_prob(
-              as_prob<LG>(p[((size_t)b * k1 + pos) * V + x], row_st<LG>(sp, (size_t)b * k1 + pos)), f);
-          const float qi = sanitize_prob(
-              as_prob<LG>(q[((size_t)b * k + pos) * V + x], row_st<LG>(sq, (size_t)b * k + pos)), f);
-          const float ui = sanitize_uniform(uni[(size_t)b * k1 + pos], f);
-          pass = (double)ui * (double)qi < (double)pi;
-        }
-      }
-      // n = the first failing position of this lane's request, else k;
-      // flags count from positions up to and including n only.
-      const uint32_t fails = __ballot_sync(0xffffffffu, live && !pass);
-      const uint32_t mine = kp == 32 ? fails : (fails >> (slot * kp)) & ((1u << kp) - 1u);
-      const int n = mine ? __ffs(mine) - 1 : k;
-      if (live && pos <= n && f) raise_status(status, f);
-      if (i < nU && pos == 0) {
-        rs.n[i] = n;
-        if ((g + i * G) - b * chunks == 0) n_out[b] = n;
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&rs.a5_done);
-  }
-  if (!mbar_wait_bounded(&rs.a5_done, 0u, ab)) {
-    if (lane == 0) ring_abort(rs, status);
-    return;
-  }
-
-  // Consumer: this warp's block [512 warp, 512 warp + 512) of every item.
-  int st = 0;
-  uint32_t ph = 0;
-  auto next_stage = [&](int &s, uint32_t &parity) {
-    s = st;
-    parity = ph;
-    if (++st == RING_STAGES) {
-      st = 0;
-      ph ^= 1u;
-    }
-  };
-  walk([&](int i, int kind) -> bool {
-    int s0, s1 = 0;
-    uint32_t p0, p1 = 0;
-    next_stage(s0, p0);
-    const bool resid = kind == ITEM_RESIDUAL;
-    if (resid) next_stage(s1, p1);
-    bool landed = mbar_wait_bounded(&rs.full[s0], p0, ab);
-    if (landed && resid) landed = mbar_wait_bounded(&rs.full[s1], p1, ab);
-    if (!__all_sync(0xffffffffu, landed)) {
-      if (lane == 0) ring_abort(rs, status);
-      return false;
-    }
-    if (kind == ITEM_DISCARD) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&rs.empty[s0]);
-      return true;
-    }
-    const int u = g + i * G, c = u % chunks;
-    const int len4 = min(CHUNK, V - c * CHUNK) / 4;
-    const float4 *a4 = reinterpret_cast<const float4 *>(stages + (size_t)s0 * STAGE_FLOATS);
-    const float4 *c4 = reinterpret_cast<const float4 *>(stages + (size_t)s1 * STAGE_FLOATS);
-    float pa[16], qa[16];
-    bool inr[4];
+  if (LG) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int e4 = warp * (BLOCK / 4) + lane + 32 * j;  // entries past V read as 0 (weight 0)
-      inr[j] = e4 < len4;
-      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 a = e4 < len4 ? a4[e4] : z4;
-      const float4 cq = (resid && e4 < len4) ? c4[e4] : z4;
-      pa[4 * j + 0] = a.x, pa[4 * j + 1] = a.y, pa[4 * j + 2] = a.z, pa[4 * j + 3] = a.w;
-      qa[4 * j + 0] = cq.x, qa[4 * j + 1] = cq.y, qa[4 * j + 2] = cq.z, qa[4 * j + 3] = cq.w;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&rs.empty[s0]);
-      if (resid) mbar_arrive(&rs.empty[s1]);
-    }
-    if (LG) {
-      // Logits to probabilities (entries past V stay 0).
-      const int b = u / chunks, prow = resid ? rs.n[i] : k;
-      const float2 stp = sp[(size_t)b * k1 + prow];
-      const float2 stq = resid ? sq[(size_t)b * k + prow] : make_float2(0.f, 1.f);
+      if (w * (BLOCK / 4) + lane + 32 * j < len4) {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        if (inr[e >> 2]) {
-          pa[e] = as_prob<LG>(pa[e], stp);
-          if (resid) qa[e] = as_prob<LG>(qa[e], stq);
-        }
+        for (int i = 0; i < 4; ++i) a[4 * j + i] = as_prob<LG>(a[4 * j + i], st);
       }
     }
+  }
+}
+
+// blk: [B * chunks units][8 blocks][2] uint64 (residual, target).
+template <bool LG>
+__global__ void __launch_bounds__(BLK_THREADS)
+    accept_blocks_kernel(const float *__restrict__ p, const float *__restrict__ q, int B, int k, int V, int chunks,
+                         const int32_t *__restrict__ n_in, uint64_t *__restrict__ blk, uint32_t *status,
+                         const float2 *__restrict__ sp, const float2 *__restrict__ sq) {
+  grid_launch_dependents();
+  grid_dependency_wait();  // the accepted counts come from accept_test_kernel
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int k1 = k + 1;
+  const int U = B * chunks;
+  for (int u = blockIdx.x; u < U; u += gridDim.x) {
+    const int b = u / chunks, c = u - b * chunks;
+    const int n = __ldcg(n_in + b);
+    const bool resid = n < k;
+    const int len4 = min(CHUNK, V - c * CHUNK) / 4;
+    const size_t prow = (size_t)b * k1 + (resid ? n : k);
+    float pa[16];
     uint32_t mx = 0, sy = 0, sz = 0, my = 0, mz = 0;
+    if (!resid) {
+      load_block<LG>(p + prow * V, c * (CHUNK / 4), len4, w, lane, pa, row_st<LG>(sp, prow));
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      mx = max(mx, __float_as_uint(pa[e]));
-      const QBits t = q_bits(pa[e]);
-      sy += t.y;
-      sz += t.z;
-      if (resid) {
-        mx = max(mx, __float_as_uint(qa[e]));
+      for (int e = 0; e < 16; ++e) {
+        mx = max(mx, __float_as_uint(pa[e]));
+        const QBits t = q_bits(pa[e]);
+        sy += t.y;
+        sz += t.z;
+      }
+    } else {
+      const size_t qrow = (size_t)b * k + n;
+      float qa[16];
+      load_block<LG>(p + prow * V, c * (CHUNK / 4), len4, w, lane, pa, row_st<LG>(sp, prow));
+      load_block<LG>(q + qrow * V, c * (CHUNK / 4), len4, w, lane, qa, row_st<LG>(sq, qrow));
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        mx = max(mx, max(__float_as_uint(pa[e]), __float_as_uint(qa[e])));
+        const QBits t = q_bits(pa[e]);
+        sy += t.y;
+        sz += t.z;
         const QBits m = q_bits(fminf(pa[e], qa[e]));  // Q is monotone: Q(min(p, q)) = min(Q(p), Q(q))
         my += m.y;
         mz += m.z;
       }
+      if (__any_sync(0xffffffffu, mx > ONE_BITS)) {
+        // An entry outside [0, 1] or NaN: clamp every entry and note it, as
+        // the per-chunk form does (here, where qa is in scope).
+        bool bad = false;
+        uint64_t s_res = 0, s_tgt = 0;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint64_t qp = fixq(clamp_prob(pa[e], bad));
+          s_tgt += qp;
+          s_res += res_weight(qp, fixq(clamp_prob(qa[e], bad)));
+        }
+        s_res = warp_sum_u64(s_res);
+        s_tgt = warp_sum_u64(s_tgt);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(status, MLORA_DEV_BAD_PROB);
+        if (lane == 0) {
+          blk[((size_t)u * BLK_WARPS + w) * 2 + 0] = s_res;
+          blk[((size_t)u * BLK_WARPS + w) * 2 + 1] = s_tgt;
+        }
+        continue;
+      }
     }
-    uint64_t s_res, s_tgt;
+    uint64_t s_res = 0, s_tgt = 0;
     if (!__any_sync(0xffffffffu, mx > ONE_BITS)) {
       // Per lane the sums of hi stay <= 16 * 2^17 and of lo < 16 * 2^23, so
       // the warp sums stay below 2^32.
       const uint32_t bias16 = 16u * BIAS_BITS;
       s_tgt = ((uint64_t)__reduce_add_sync(0xffffffffu, sy - bias16) << 23) +
               __reduce_add_sync(0xffffffffu, sz - bias16);
-      s_res = 0;
       if (resid) {
         const uint64_t s_min = ((uint64_t)__reduce_add_sync(0xffffffffu, my - bias16) << 23) +
                                __reduce_add_sync(0xffffffffu, mz - bias16);
         s_res = s_tgt - s_min;
       }
     } else {
-      // An entry outside [0, 1] or NaN: clamp every entry and note it, as the
-      // per-chunk form does.
+      // A bonus-row entry outside [0, 1] or NaN: clamp every entry and note
+      // it, as the per-chunk form does.
       bool bad = false;
-      s_res = 0;
-      s_tgt = 0;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const uint64_t qp = fixq(clamp_prob(pa[e], bad));
-        s_tgt += qp;
-        if (resid) s_res += res_weight(qp, fixq(clamp_prob(qa[e], bad)));
-      }
-      s_res = warp_sum_u64(s_res);
+      for (int e = 0; e < 16; ++e) s_tgt += fixq(clamp_prob(pa[e], bad));
       s_tgt = warp_sum_u64(s_tgt);
       if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(status, MLORA_DEV_BAD_PROB);
     }
     if (lane == 0) {
-      blk[((size_t)u * RING_CONSUMERS + warp) * 2 + 0] = s_res;
-      blk[((size_t)u * RING_CONSUMERS + warp) * 2 + 1] = s_tgt;
+      blk[((size_t)u * BLK_WARPS + w) * 2 + 0] = s_res;
+      blk[((size_t)u * BLK_WARPS + w) * 2 + 1] = s_tgt;
     }
-    return true;
-  });
+  }
 }
 
 // The draw of request b by one warp, from the block sums: the totals, the
@@ -716,17 +600,17 @@ __global__ void __launch_bounds__(DRAW_WARPS * 32)
   if (lane == 0) uk = sanitize_uniform(uni[(size_t)b * k1 + k], fl);
   int dt = -1;
   if (lane < k) dt = draft_tok[(size_t)b * k + lane];
-  const ulonglong2 *bb = reinterpret_cast<const ulonglong2 *>(blk) + (size_t)b * chunks * RING_CONSUMERS;
+  const ulonglong2 *bb = reinterpret_cast<const ulonglong2 *>(blk) + (size_t)b * chunks * BLK_WARPS;
   // Group 0's block sums stay in registers (chunks <= 32 needs no reload).
-  ulonglong2 g0[RING_CONSUMERS];
+  ulonglong2 g0[BLK_WARPS];
   uint64_t S_res = 0, S_tgt = 0;
   for (int e0 = 0; e0 < chunks; e0 += 32) {
     const int e = e0 + lane;
-    ulonglong2 v[RING_CONSUMERS];
+    ulonglong2 v[BLK_WARPS];
 #pragma unroll
-    for (int j = 0; j < RING_CONSUMERS; ++j) v[j] = e < chunks ? __ldcg(bb + (size_t)e * RING_CONSUMERS + j) : make_ulonglong2(0, 0);
+    for (int j = 0; j < BLK_WARPS; ++j) v[j] = e < chunks ? __ldcg(bb + (size_t)e * BLK_WARPS + j) : make_ulonglong2(0, 0);
 #pragma unroll
-    for (int j = 0; j < RING_CONSUMERS; ++j) {
+    for (int j = 0; j < BLK_WARPS; ++j) {
       S_res += v[j].x;
       S_tgt += v[j].y;
       if (e0 == 0) g0[j] = v[j];
@@ -751,13 +635,13 @@ __global__ void __launch_bounds__(DRAW_WARPS * 32)
     uint64_t base = 0;
     for (int e0 = 0; e0 < chunks && found < 0; e0 += 32) {
       const int e = e0 + lane;
-      ulonglong2 v[RING_CONSUMERS];
+      ulonglong2 v[BLK_WARPS];
 #pragma unroll
-      for (int j = 0; j < RING_CONSUMERS; ++j)
-        v[j] = e0 == 0 ? g0[j] : (e < chunks ? __ldcg(bb + (size_t)e * RING_CONSUMERS + j) : make_ulonglong2(0, 0));
+      for (int j = 0; j < BLK_WARPS; ++j)
+        v[j] = e0 == 0 ? g0[j] : (e < chunks ? __ldcg(bb + (size_t)e * BLK_WARPS + j) : make_ulonglong2(0, 0));
       uint64_t w = 0;
 #pragma unroll
-      for (int j = 0; j < RING_CONSUMERS; ++j) w += mode == 0 ? v[j].x : v[j].y;
+      for (int j = 0; j < BLK_WARPS; ++j) w += mode == 0 ? v[j].x : v[j].y;
       const uint64_t inc = warp_incl_scan_u64(w);
       uint64_t run = base + inc - w;
       const uint32_t hit = __ballot_sync(0xffffffffu, run <= T && T < run + w);
@@ -769,7 +653,7 @@ __global__ void __launch_bounds__(DRAW_WARPS * 32)
         if (lane == h) {
           uint64_t t = T - run;
 #pragma unroll
-          for (int j = 0; j < RING_CONSUMERS; ++j) {
+          for (int j = 0; j < BLK_WARPS; ++j) {
             const uint64_t wj = mode == 0 ? v[j].x : v[j].y;
             if (t < wj) {
               blkid = j;
@@ -854,16 +738,15 @@ AcceptShape accept_shape(int B, int k, int V, int num_sms) {
   // Per-chunk form: chunk sums (residual, target).  Streaming form: the 8
   // block sums of every chunk, then the accepted count of every request.
   const size_t units = (size_t)B * s.slices;
-  s.stats_off = units * RING_CONSUMERS * 2 * sizeof(uint64_t) + align_up((size_t)B * 4, 256);
+  s.stats_off = units * BLK_WARPS * 2 * sizeof(uint64_t) + align_up((size_t)B * 4, 256);
   s.part_off = s.stats_off + align_up((size_t)B * (2 * k + 1) * sizeof(float2), 256);
   const size_t rows_per_launch = std::min((size_t)B * (k + 1), (size_t)WS_MAX_COUNTERS);
   s.scratch_bytes = s.part_off + row_stats_scratch_bytes((int)rows_per_launch, V);
-  // Streaming form: one CTA per SM, more when a CTA would own more than
-  // RING_MAX_UNITS units.
-  long long g = (long long)units < num_sms ? (long long)units : num_sms;
-  const long long g_units = ((long long)units + RING_MAX_UNITS - 1) / RING_MAX_UNITS;
-  if (g < g_units) g = g_units;
-  s.ring_grid = (int)(g > 0 ? g : 1);
+  // Streaming form: one CTA per unit, up to 64 per SM (a grid-stride loop
+  // takes the rest).
+  const long long cap = (long long)(num_sms > 0 ? num_sms : 1) * 64;
+  const long long g = (long long)units < cap ? (long long)units : cap;
+  s.blocks_grid = (int)(g > 0 ? g : 1);
   return s;
 }
 
@@ -877,17 +760,14 @@ static cudaError_t launch_accept_t(const float *p, const float *q, const int32_t
   uint64_t *sums = reinterpret_cast<uint64_t *>(scratch);
   cudaError_t e;
   if (vec) {
-    static int attr_done[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidValue;
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-      e = cudaFuncSetAttribute(accept_stream_kernel<LG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RING_SMEM);
-      if (e != cudaSuccess) return e;
-      attr_done[dev] = 1;
-    }
-    int32_t *n_buf = reinterpret_cast<int32_t *>(sums + (size_t)B * sh.slices * RING_CONSUMERS * 2);
-    e = launch_pdl(accept_stream_kernel<LG>, dim3((unsigned)sh.ring_grid), dim3(RING_THREADS), RING_SMEM, s, p, q,
-                   draft_tok, u, B, k, V, sh.slices, sums, n_buf, status, sp, sq);
+    int32_t *n_buf = reinterpret_cast<int32_t *>(sums + (size_t)B * sh.slices * BLK_WARPS * 2);
+    const int kp = k <= 1 ? 1 : 1 << (32 - __builtin_clz((unsigned)(k - 1)));
+    const long long test_threads = (long long)(B + 32 / kp - 1) / (32 / kp) * 32;
+    e = launch_pdl(accept_test_kernel<LG>, dim3((unsigned)((test_threads + TEST_THREADS - 1) / TEST_THREADS)),
+                   dim3(TEST_THREADS), 0, s, p, q, draft_tok, u, B, k, V, n_buf, status, sp, sq);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(accept_blocks_kernel<LG>, dim3((unsigned)sh.blocks_grid), dim3(BLK_THREADS), 0, s, p, q, B, k, V,
+                   sh.slices, (const int32_t *)n_buf, sums, status, sp, sq);
     if (e != cudaSuccess) return e;
     e = launch_pdl(accept_draw_kernel<LG>, dim3((unsigned)((B + DRAW_WARPS - 1) / DRAW_WARPS)),
                    dim3(DRAW_WARPS * 32), 0, s, p, q, draft_tok, u, B, k, V, sh.slices, (const uint64_t *)sums,

@@ -121,7 +121,7 @@ cudaError_t launch_quantize_rows_e4m3(const uint16_t *src, int R, int K, uint8_t
 // the kernels read probabilities expf(z - m) / S from the rows' statistics.
 struct AcceptShape {
   int slices, slice_len, threads;
-  int ring_grid;  // CTAs of the streaming form (rows of aligned float4)
+  int blocks_grid;  // CTAs of the streaming form's block sums (rows of aligned float4)
   size_t stats_off;      // scratch offset of the row statistics (logits form): float2 [B(k+1) + Bk]
   size_t part_off;       // scratch offset of the statistics' chunk partials (logits form)
   size_t scratch_bytes;
