@@ -18,12 +18,15 @@
 // (no partial last wave).  A CTA's share is a sequence of segments: the tail
 // of a tile begun by the CTA before it, whole tiles, and the head of a tile
 // that the CTAs after it finish.  The CTA that holds a tile's first k-block
-// owns the tile: it adds the expand MMAs, waits for the fp32 partial sums of
-// the other contributors (each publishes its single non-owned segment first,
-// so by the time the owner reaches the end of its share they are ready) and
-// writes y.  Waits only ever point to CTAs with a larger index, and all CTAs
-// are resident at once, so the waits always end; every wait is bounded
-// nevertheless.  Partials are added in CTA order: results are deterministic.
+// owns the tile and adds the expand MMAs.  A split tile is finished by its
+// participants together: each publishes its segment's fp32 partial sums and
+// counts itself in on the tile's arrival word; those whose shares end inside
+// the tile (the owner, and the CTAs whose whole share lies in it) then each
+// add up every partial for an equal slice of the token columns and store y.
+// A CTA waits at most once, in its last segment, after publishing all its
+// earlier segments, and all CTAs are resident at once, so the waits always
+// end; every wait is bounded nevertheless.  Partials are added in CTA order:
+// results are deterministic.
 //
 // Residency: the waits above end only if every CTA of the grid is resident at
 // once.  The host launches one CTA per SM only when the occupancy query says
@@ -65,8 +68,8 @@ struct SkArgs {
   const uint16_t *tw;  // token windows of the expand blocks, rows in the 32-byte-swizzled order
   const int32_t *plan;
   uint32_t *status;
-  float *partials;  // [P][Mb][128]: a contributor's partial sums, token-major
-  uint32_t *flags;  // [P]: 1 once CTA i's partial is written; the owner sets it back to 0
+  float *partials;  // [P][2][Mb][128]: a CTA's partial sums of its first and of a later split segment, token-major
+  uint32_t *flags;  // [P] arrivals and [P] finished reducers of the split tile owned by CTA i (zero between calls)
   const float *w_scale;  // E4M3 operands: per W row and per token row scales of the codes
   const float *x_scale;
 };
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   uint64_t *acc_full = empty + S;     // [2]: MMA commit -> epilogue
   uint64_t *acc_empty = acc_full + 2; // [2]: epilogue warps -> MMA issuer
   uint64_t *drain = acc_empty + 2;
-  uint64_t *fix_bar = drain + 1;      // partial sums copied into the ring (owner fix-up)
+  uint64_t *fix_bar = drain + 1;      // other participants' partial sums copied into the ring (reducers)
   uint64_t *epi_done = fix_bar + 1;   // every epilogue warp is done with tensor memory
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi_done + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
@@ -358,88 +361,144 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       tc_fence_after_sync();
       const uint32_t acc = tmem_base + (uint32_t)(buf * args.cols) + lane_off;
       const int nchunks = (args.M + SK_CHUNK - 1) / SK_CHUNK;
-      if (kb0 > 0) {
-        // Contributor: publish this segment's partial sums, then the flag.
-        float *part = args.partials + (size_t)cta * args.Mb * SK_BN;
-        for (int ch = 0; ch < nchunks; ++ch) {
-          uint32_t r[32];
-          tmem_ld_x32(acc + ch * SK_CHUNK, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < SK_CHUNK; ++j) {
-            const int col = ch * SK_CHUNK + j;
-            if (col < args.M) part[(size_t)col * SK_BN + row] = __uint_as_float(r[j]);
+      const int n = t * SK_BN + row;
+      // y for accumulator columns [cb, min(cb + 32, c_end)) from v: output
+      // row perm[c] with sorted rows (lane j fetches it), else c.  An entry
+      // out of range (a plan overwritten or made for other sizes) skips the
+      // store and raises MLORA_DEV_BAD_PLAN.
+      auto store_y = [&](int cb, int c_end, const float (&v)[SK_CHUNK]) {
+        const int myc = cb + lane;
+        int myrow = myc;
+        if (perm) {
+          myrow = myc < args.M ? __ldg(perm + myc) : -1;
+          if (myc < args.M && (unsigned)myrow >= (unsigned)args.M) {
+            raise_status(args.status, MLORA_DEV_BAD_PLAN);
+            myrow = -1;
           }
+        }
+        uint16_t *yn = args.y + n;
+        float wsn = 1.f, myxs = 1.f;  // E4M3: the scales of this thread's W row and of lane's token row
+        if (F8) {
+          wsn = n < args.N ? __ldg(args.w_scale + n) : 0.f;
+          myxs = myc < args.M ? __ldg(args.x_scale + myc) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < SK_CHUNK; ++j) {
+          const int orow = __shfl_sync(0xffffffffu, myrow, j);
+          const float xs = F8 ? __shfl_sync(0xffffffffu, myxs, j) : 1.f;
+          if (n < args.N && cb + j < c_end && orow >= 0)
+            yn[(size_t)orow * args.N] = float_to_bf16_bits(F8 ? v[j] * wsn * xs : v[j]);
+        }
+      };
+      if (kb0 == 0 && kb1 == KB) {
+        // A whole tile: round once and store y straight from tensor memory.
+        for (int cb = 0; cb < args.M; cb += SK_CHUNK) {
+          uint32_t r[32];
+          tmem_ld_x32(acc + cb, r);
+          tmem_ld_wait();
+          float v[SK_CHUNK];
+#pragma unroll
+          for (int j = 0; j < SK_CHUNK; ++j) v[j] = __uint_as_float(r[j]);
+          store_y(cb, args.M, v);
         }
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      } else {
+        // A split tile.  Every participant (the CTAs first..last holding its
+        // k-blocks) publishes its fp32 partial sums, then counts itself in on
+        // the tile's arrival word.  The participants whose shares end inside
+        // the tile (all but a last one that continues past it) then reduce
+        // it together: each takes an equal slice of the token columns, adds
+        // every participant's partial for them in CTA order and stores y.
+        // Only a CTA's last segment can reduce, and it publishes every
+        // earlier split segment first, so all arrivals come before any wait;
+        // all CTAs are resident at once, so the waits end (and are bounded).
+        const int first = sk_cta_of(args, t * KB), last = sk_cta_of(args, (t + 1) * KB - 1);
+        const int npart = last - first + 1;
+        const int r_last = sk_begin(args, last + 1) <= (t + 1) * KB ? last : last - 1;
+        const bool reducer = sk_begin(args, cta + 1) <= (t + 1) * KB;
+        // Partial slot: 0 for a CTA's first segment, 1 for a later one.
+        auto part_of = [&](int pc) {
+          return args.partials + ((size_t)pc * 2 + (sk_begin(args, pc) >= t * KB ? 0 : 1)) * args.Mb * SK_BN;
+        };
+        // A reducer adds its own sums straight from tensor memory; it writes
+        // them out only when other reducers need them.
+        const int nred = r_last - first + 1;
+        const bool publish = !reducer || nred > 1;
+        if (publish) {
+          float *part = part_of(cta);
+          for (int ch = 0; ch < nchunks; ++ch) {
+            uint32_t r[32];
+            tmem_ld_x32(acc + ch * SK_CHUNK, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < SK_CHUNK; ++j) {
+              const int col = ch * SK_CHUNK + j;
+              if (col < args.M) part[(size_t)col * SK_BN + row] = __uint_as_float(r[j]);
+            }
+          }
+        }
+        if (!reducer) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);  // the accumulator is free: the partial holds it
+        }
         named_bar_sync(1, 128);
         if (et == 0) {
-          __threadfence();
-          st_release_gpu(&args.flags[cta], 1u);
+          __threadfence();  // after the barrier: covers the partial sums every thread stored
+          atomic_add_release_gpu(&args.flags[first], 1u);
         }
         __syncwarp();
-      } else {
-        // Owner: wait for the contributors of this tile, add their partials
-        // in CTA order, round once and store y.  A tile with contributors is
-        // always this CTA's last segment, so the stage ring is idle (every
-        // load landed and every MMA that read it completed): the partials
-        // come into it with bulk copies, a round trip for many columns.
-        const int last = kb1 < KB ? sk_cta_of(args, (t + 1) * KB - 1) : cta;
-        const int nc = last - cta;
-        bool have = true;
-        if (nc > 0) {
+        if (reducer) {
+          bool have = true;
           if (et == 0) {
-            // The timeout test polls flag words past the grid's, which no CTA
-            // sets, for test_flag_wait_ns instead of the contributors' flags.
+            // The timeout test polls a word past the grid's, which no CTA
+            // sets, for test_flag_wait_ns instead of the tile's arrivals.
             const bool probe = args.test_flag_wait_ns != 0;
             const uint64_t limit = probe ? (uint64_t)args.test_flag_wait_ns : WAIT_LIMIT_NS;
-            for (int j = cta + 1; j <= last; ++j) {
-              const uint32_t *flag = &args.flags[probe ? args.P + j : j];
-              bool seen = ld_acquire_gpu(flag) == 1u;
-              if (!seen) {
-                const uint64_t t0 = global_timer_ns();
-                while (!(seen = ld_acquire_gpu(flag) == 1u)) {
-                  if (global_timer_ns() - t0 > limit) break;
-                  sleep_ns(64);
-                }
-              }
-              if (seen) {
-                args.flags[j] = 0u;
-              } else {
-                have = false;
-                raise_status(args.status, MLORA_DEV_TIMEOUT);
+            const uint32_t *word = &args.flags[probe ? 2 * args.P + first : first];
+            bool seen = ld_acquire_gpu(word) >= (uint32_t)npart;
+            if (!seen) {
+              const uint64_t t0 = global_timer_ns();
+              while (!(seen = ld_acquire_gpu(word) >= (uint32_t)npart)) {
+                if (global_timer_ns() - t0 > limit) break;
+                sleep_ns(32);
               }
             }
-            fence_proxy_async_global();
+            if (!seen) {
+              have = false;
+              raise_status(args.status, MLORA_DEV_TIMEOUT);
+            }
+            fence_proxy_async_global();  // the bulk copies below read what generic stores wrote
           }
           __syncwarp();  // warps reach a barrier converged (bar.* counts whole warps)
           have = named_bar_and(1, 128, have);
-        }
-        const int n = t * SK_BN + row;
-        // Columns per round: every contributor's slice of them fits the ring
-        // (the host bounds nc so that at least SK_CHUNK columns always do).
-        const size_t ring_bytes = (size_t)S * stage_bytes;
-        int per = nc > 0 ? (int)(ring_bytes / ((size_t)nc * SK_BN * 4)) / SK_CHUNK * SK_CHUNK : args.M;
-        if (nc > 0 && per < SK_CHUNK) {
-          per = SK_CHUNK;
-          if (have && et == 0) raise_status(args.status, MLORA_DEV_TIMEOUT);
-          have = false;  // cannot happen within the host's bound; never copy past the ring
-        }
-        const float *sp = reinterpret_cast<const float *>(ring);
-        uint32_t fix_phase = 0;
-        for (int q0 = 0; q0 < args.M; q0 += per) {
-          const int q1 = min(args.M, q0 + per);
-          const int qn = q1 - q0;
-          const bool fetch = nc > 0 && have;
-          if (fetch) {
+          const int ri = cta - first;
+          const int per = ((args.M + nred - 1) / nred + SK_CHUNK - 1) / SK_CHUNK * SK_CHUNK;
+          const int c0 = ri * per, c1 = min(args.M, c0 + per);
+          // The other participants' partials for the slice come into the
+          // stage ring (idle in a CTA's last segment: every load landed and
+          // every MMA that read it completed) with bulk copies, in rounds of
+          // columns that fit it; this CTA's own sums come from tensor memory.
+          const int nother = npart - 1;
+          const size_t ring_bytes = (size_t)S * stage_bytes;
+          int round_cols = (int)(ring_bytes / ((size_t)nother * SK_BN * 4)) / SK_CHUNK * SK_CHUNK;
+          if (round_cols < SK_CHUNK) {  // excluded by the host's bound on participants
+            if (have && et == 0) raise_status(args.status, MLORA_DEV_TIMEOUT);
+            have = false;
+          }
+          const float *ringf = reinterpret_cast<const float *>(ring);
+          uint32_t fix_phase = 0;
+          for (int q0 = c0; have && q0 < c1; q0 += round_cols) {
+            const int q1 = min(c1, q0 + round_cols), qn = q1 - q0;
             if (et == 0) {
               const uint32_t bytes = (uint32_t)qn * SK_BN * 4;
-              mbar_arrive_expect_tx(fix_bar, bytes * (uint32_t)nc);
-              for (int c = 0; c < nc; ++c)
-                bulk_load(ring + (size_t)c * qn * SK_BN * 4,
-                          args.partials + ((size_t)(cta + 1 + c) * args.Mb + q0) * SK_BN, bytes, fix_bar);
+              mbar_arrive_expect_tx(fix_bar, bytes * (uint32_t)nother);
+              int o = 0;
+              for (int pc = first; pc <= last; ++pc)
+                if (pc != cta) bulk_load(ring + (size_t)(o++) * qn * SK_BN * 4, part_of(pc) + (size_t)q0 * SK_BN, bytes,
+                                         fix_bar);
             }
             __syncwarp();
             // Not cut short by the abort flag: the copies must land before
@@ -449,61 +508,45 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             if (!landed) {
               if (et == 0) raise_status(args.status, MLORA_DEV_TIMEOUT);
               have = false;
+              break;
             }
-          }
-          for (int cb = q0; cb < q1; cb += SK_CHUNK) {
-            uint32_t r[32];
-            tmem_ld_x32(acc + cb, r);
-            tmem_ld_wait();
-            float v[32];
+            for (int cb = q0; cb < q1; cb += SK_CHUNK) {
+              uint32_t r[32];
+              tmem_ld_x32(acc + cb, r);
+              tmem_ld_wait();
+              float v[SK_CHUNK];
 #pragma unroll
-            for (int j = 0; j < SK_CHUNK; ++j) v[j] = __uint_as_float(r[j]);
-            const bool whole = cb + SK_CHUNK <= q1;  // no column past q1 in this chunk
-            if (fetch && have) {
-              for (int c = 0; c < nc; ++c) {
-                const float *pc = sp + ((size_t)c * qn + (cb - q0)) * SK_BN + row;
-                if (whole) {
+              for (int j = 0; j < SK_CHUNK; ++j) v[j] = 0.f;
+              int o = 0;
+              for (int pc = first; pc <= last; ++pc) {
+                if (pc == cta) {
 #pragma unroll
-                  for (int j = 0; j < SK_CHUNK; ++j) v[j] += pc[j * SK_BN];
-                } else {
-#pragma unroll
-                  for (int j = 0; j < SK_CHUNK; ++j)
-                    if (cb + j < q1) v[j] += pc[j * SK_BN];
+                  for (int j = 0; j < SK_CHUNK; ++j) v[j] += __uint_as_float(r[j]);
+                  continue;
                 }
-              }
-            }
-            // Output row of column cb + j: perm[cb + j] with sorted rows (lane
-            // j fetches it), else cb + j.
-            // An entry out of range (a plan overwritten or made for other
-            // sizes) skips the store and raises MLORA_DEV_BAD_PLAN.
-            const int myc = cb + lane;
-            int myrow = myc;
-            if (perm) {
-              myrow = myc < args.M ? __ldg(perm + myc) : -1;
-              if (myc < args.M && (unsigned)myrow >= (unsigned)args.M) {
-                raise_status(args.status, MLORA_DEV_BAD_PLAN);
-                myrow = -1;
-              }
-            }
-            uint16_t *yn = args.y + n;
-            float wsn = 1.f, myxs = 1.f;  // E4M3: the scales of this thread's W row and of lane's token row
-            if (F8) {
-              wsn = n < args.N ? __ldg(args.w_scale + n) : 0.f;
-              myxs = myc < args.M ? __ldg(args.x_scale + myc) : 0.f;
-            }
+                const float *pp = ringf + ((size_t)(o++) * qn + (cb - q0)) * SK_BN + row;
 #pragma unroll
-            for (int j = 0; j < SK_CHUNK; ++j) {
-              const int row = __shfl_sync(0xffffffffu, myrow, j);
-              const float xs = F8 ? __shfl_sync(0xffffffffu, myxs, j) : 1.f;
-              if (n < args.N && (whole || cb + j < q1) && row >= 0)
-                yn[(size_t)row * args.N] = float_to_bf16_bits(F8 ? v[j] * wsn * xs : v[j]);
+                for (int j = 0; j < SK_CHUNK; ++j)
+                  if (cb + j < q1) v[j] += pp[j * SK_BN];
+              }
+              store_y(cb, q1, v);
+            }
+            named_bar_sync(1, 128);  // the ring is refilled only after every thread read it
+          }
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          // The last reducer to finish puts the tile's words back to zero.
+          named_bar_sync(1, 128);
+          if (et == 0) {
+            const uint32_t prev = atomicAdd(&args.flags[args.P + first], 1u);
+            if (prev == (uint32_t)(nred - 1)) {
+              args.flags[first] = 0u;
+              args.flags[args.P + first] = 0u;
             }
           }
-          if (fetch) named_bar_sync(1, 128);  // the ring is refilled only after every thread read it
+          __syncwarp();
         }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[buf]);
       }
       g = t * KB + kb1;
     }
@@ -583,7 +626,7 @@ SkShape sk_shape(int M, int N, int K, int num_sms, bool f8) {
 
 size_t sk_partial_bytes(int M, int num_sms) {
   if (M < 1 || M > SK_MAX_ROWS) return 0;
-  return (size_t)num_sms * ((M + 15) / 16 * 16) * SK_BN * sizeof(float);
+  return (size_t)num_sms * 2 * ((M + 15) / 16 * 16) * SK_BN * sizeof(float);
 }
 
 typedef CUresult (*SkEncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
