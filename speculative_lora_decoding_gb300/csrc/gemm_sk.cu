@@ -1,6 +1,6 @@
 // Steps a3 + a4 as a persistent stream-K kernel: the base GEMM acc = x W^T on
 // the tcgen05 tensor cores with the low-rank expand added by tensor-core MMAs
-// (verify mode), for batches of up to 256 token rows:
+// (verify mode), for batches of up to 1024 token rows:
 //
 //   draft  (LoRA off): y[m, n] = bf16(acc[m, n])
 //   verify (LoRA on):  y[perm[c], n] = bf16(acc[c, n] + sum_blocks B_a[n, block] . Twin[c, :])
@@ -12,17 +12,20 @@
 // in Practice", section "Core Principle: Shared Base Model, Per-Request
 // Adapter Selection").
 //
-// Work split.  The (tile of 128 W rows, 64-wide k-block) pairs are laid out
-// tile by tile and cut into one contiguous, equal share per CTA, one CTA per
-// SM, so every SM streams the same number of W bytes whatever the tile count
-// (no partial last wave).  A CTA's share is a sequence of segments: the tail
-// of a tile begun by the CTA before it, whole tiles, and the head of a tile
-// that the CTAs after it finish.  The CTA that holds a tile's first k-block
-// owns the tile and adds the expand MMAs.  A split tile is finished by its
-// participants together: each publishes its segment's fp32 partial sums and
-// counts itself in on the tile's arrival word; those whose shares end inside
-// the tile (the owner, and the CTAs whose whole share lies in it) then each
-// add up every partial for an equal slice of the token columns and store y.
+// Work split.  The token rows form up to four groups of at most 256 (Mb
+// rows each); a unit is a tile of 128 W rows with one token group, units go
+// tile by tile (the groups of a tile side by side, so a W tile read from
+// DRAM serves them all from L2).  The (unit, 64-wide k-block) pairs are cut
+// into one contiguous, equal share per CTA, one CTA per SM, so every SM
+// streams the same number of bytes whatever the unit count (no partial last
+// wave).  A CTA's share is a sequence of segments: the tail of a unit begun
+// by the CTA before it, whole units, and the head of a unit that the CTAs
+// after it finish.  The CTA that holds a unit's first k-block owns the unit
+// and adds the expand MMAs.  A split unit is finished by its participants
+// together: each publishes its segment's fp32 partial sums and counts itself
+// in on the unit's arrival word; those whose shares end inside the unit (the
+// owner, and the CTAs whose whole share lies in it) then each add up every
+// partial for an equal slice of the unit's token columns and store y.
 // A CTA waits at most once, in its last segment, after publishing all its
 // earlier segments, and all CTAs are resident at once, so the waits always
 // end; every wait is bounded nevertheless.  Partials are added in CTA order:
@@ -55,9 +58,11 @@ constexpr int SK_MAX_STAGES = 8;
 constexpr size_t SK_SMEM_FIXED = 1024 + 256 + expand_smem_bytes(SK_MAX_STAGES);  // alignment slack, barriers, expand records
 constexpr int SK_MIN_SHARE = 8;                  // k-blocks per CTA at least
 constexpr int SK_MAX_PARTIALS = 8;               // contributors per tile besides its owner, at most
-constexpr int SK_MAX_ROWS = 256;                 // token rows: two accumulators fit in tensor memory
+constexpr int SK_GROUP_ROWS = 256;               // token rows of a group: two accumulators fit in tensor memory
+constexpr int SK_MAX_GROUPS = 4;                 // token groups of a call (M <= 1024)
 struct SkArgs {
   int M, N, K, Mb, kblocks, total, P, stages, cols;
+  int n_tg;  // token groups: unit u is (W tile u / n_tg, token rows [(u % n_tg) Mb, +Mb))
   int mode, prefetch_w, after_shrink;
   int sorted;  // verify mode: x in adapter-sorted order, token windows present
   int n_slices, slice_end[MLORA_MAX_SLICES];
@@ -176,16 +181,18 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       // expand: its operands would take ring stages between those k-blocks.)
       if (args.prefetch_w && !args.after_shrink && !tc) {
         for (int g = g0; g < g1 && early < S; ++g, ++early) {
-          const int t = g / KB, kb = g - t * KB;
+          const int u = g / KB, kb = g - u * KB;
           mbar_arrive_expect_tx(&full[early], tx);
-          tma_load_2d(ring + (size_t)early * stage_bytes, &tmap_w, &full[early], kb * KBE, t * SK_BN, pol_w);
+          tma_load_2d(ring + (size_t)early * stage_bytes, &tmap_w, &full[early], kb * KBE, (u / args.n_tg) * SK_BN,
+                      pol_w);
         }
       }
       if (waited) grid_dependency_wait();
     }
     early = __shfl_sync(0xffffffffu, early, 0);
-    // k-blocks [from, to) of tile t, lane 0 only.
-    auto issue_kblocks = [&](int t, int from, int to) {
+    // k-blocks [from, to) of unit u, lane 0 only.
+    auto issue_kblocks = [&](int u, int from, int to) {
+      const int w_row = (u / args.n_tg) * SK_BN, x_row = (u % args.n_tg) * args.Mb;
       for (int kb = from; kb < to; ++kb, ++i) {
         uint8_t *st = ring + (size_t)stage * stage_bytes;
         if (i >= early) {
@@ -194,9 +201,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[stage], tx);
-          tma_load_2d(st, &tmap_w, &full[stage], kb * KBE, t * SK_BN, pol_w);
+          tma_load_2d(st, &tmap_w, &full[stage], kb * KBE, w_row, pol_w);
         }
-        tma_load_2d(st + SK_WTILE, &tmap_x, &full[stage], kb * KBE, 0, pol_x);
+        tma_load_2d(st + SK_WTILE, &tmap_x, &full[stage], kb * KBE, x_row, pol_x);
         ++issued;
         if (++stage == S) {
           stage = 0;
@@ -213,13 +220,14 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       __syncwarp();
     };
     for (int g = g0; g < g1 && ok;) {
-      const int t = g / KB, kb0 = g - t * KB, kb1 = min(KB, g1 - t * KB);
-      // The expand operands of an owned tile (verify mode) go into the ring
-      // before the tile's last S k-blocks, so that they land while those
-      // stream instead of after the whole tile.
+      const int u = g / KB, kb0 = g - u * KB, kb1 = min(KB, g1 - u * KB);
+      const int t = u / args.n_tg, m0 = (u % args.n_tg) * args.Mb;
+      // The expand operands of an owned unit (verify mode) go into the ring
+      // before the unit's last S k-blocks, so that they land while those
+      // stream instead of after the whole unit.
       const int ins = (tc && kb0 == 0) ? max(kb0, kb1 - 1 - S) : -1;
       const int split = ins >= 0 ? ins + 1 : kb1;
-      if (lane == 0) issue_kblocks(t, kb0, split);
+      if (lane == 0) issue_kblocks(u, kb0, split);
       sync_state();
       if (ok && ins >= 0) {
         if (!waited) {
@@ -228,14 +236,14 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         }
         if (ns < 0) ns = args.plan[L.hdr + 4];
         if (ns > 0)
-          ok = expand_produce(args.plan + L.slices, 0, ns, 0, args.Mb, t * SK_BN, args.N, &tmap_b,
+          ok = expand_produce(args.plan + L.slices, 0, ns, m0, args.Mb, t * SK_BN, args.N, &tmap_b,
                               args.tw + (size_t)sk_slice_of(args, t * SK_BN) * args.tw_slice, ring, stage_bytes, S,
                               full, empty, meta, chunk, stage, phase, issued, ab, pol_w, lane, args.n_ad,
                               (long long)(args.tw_slice / 16), args.status);
       }
-      if (lane == 0 && ok) issue_kblocks(t, split, kb1);
+      if (lane == 0 && ok) issue_kblocks(u, split, kb1);
       sync_state();
-      g = t * KB + kb1;
+      g = u * KB + kb1;
     }
     if (lane == 0) {
       if (!ok) {
@@ -263,7 +271,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     uint32_t phase = 0;
     bool ok = true, issued_any = false;
     for (int g = g0; g < g1 && ok; ++seg) {
-      const int t = g / KB, kb0 = g - t * KB, kb1 = min(KB, g1 - t * KB);
+      const int u = g / KB, kb0 = g - u * KB, kb1 = min(KB, g1 - u * KB);
       const int buf = seg & 1;
       const uint32_t acc = tmem_base + (uint32_t)(buf * args.cols);
       // The same order as the producer: k-blocks up to `ins`, the expand
@@ -322,7 +330,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       phase = __shfl_sync(0xffffffffu, phase, 0);
       if (lane == 0 && ok) mma_commit(&acc_full[buf]);
       __syncwarp();
-      g = t * KB + kb1;
+      g = u * KB + kb1;
     }
     issued_any = __shfl_sync(0xffffffffu, issued_any ? 1 : 0, 0) != 0 || issued_any;
     if (lane == 0 && !ok) {
@@ -345,7 +353,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     grid_dependency_wait();  // y and the flags may still be in use by the preceding kernel
     int seg = 0;
     for (int g = g0; g < g1; ++seg) {
-      const int t = g / KB, kb0 = g - t * KB, kb1 = min(KB, g1 - t * KB);
+      const int u = g / KB, kb0 = g - u * KB, kb1 = min(KB, g1 - u * KB);
+      const int t = u / args.n_tg, m0 = (u % args.n_tg) * args.Mb;
+      const int gcols = min(args.Mb, args.M - m0);  // token columns of this unit
       const int buf = seg & 1;
       // All 128 threads agree on the outcome before any of them branches, so
       // the named barriers below are always reached by every thread.
@@ -360,14 +370,15 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       }
       tc_fence_after_sync();
       const uint32_t acc = tmem_base + (uint32_t)(buf * args.cols) + lane_off;
-      const int nchunks = (args.M + SK_CHUNK - 1) / SK_CHUNK;
+      const int nchunks = (gcols + SK_CHUNK - 1) / SK_CHUNK;
       const int n = t * SK_BN + row;
-      // y for accumulator columns [cb, min(cb + 32, c_end)) from v: output
-      // row perm[c] with sorted rows (lane j fetches it), else c.  An entry
-      // out of range (a plan overwritten or made for other sizes) skips the
-      // store and raises MLORA_DEV_BAD_PLAN.
+      // y for accumulator columns [cb, min(cb + 32, c_end)) from v: column c
+      // is token position m0 + c, output row perm[m0 + c] with sorted rows
+      // (lane j fetches it), else m0 + c.  An entry out of range (a plan
+      // overwritten or made for other sizes) skips the store and raises
+      // MLORA_DEV_BAD_PLAN.
       auto store_y = [&](int cb, int c_end, const float (&v)[SK_CHUNK]) {
-        const int myc = cb + lane;
+        const int myc = m0 + cb + lane;
         int myrow = myc;
         if (perm) {
           myrow = myc < args.M ? __ldg(perm + myc) : -1;
@@ -391,15 +402,15 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         }
       };
       if (kb0 == 0 && kb1 == KB) {
-        // A whole tile: round once and store y straight from tensor memory.
-        for (int cb = 0; cb < args.M; cb += SK_CHUNK) {
+        // A whole unit: round once and store y straight from tensor memory.
+        for (int cb = 0; cb < gcols; cb += SK_CHUNK) {
           uint32_t r[32];
           tmem_ld_x32(acc + cb, r);
           tmem_ld_wait();
           float v[SK_CHUNK];
 #pragma unroll
           for (int j = 0; j < SK_CHUNK; ++j) v[j] = __uint_as_float(r[j]);
-          store_y(cb, args.M, v);
+          store_y(cb, gcols, v);
         }
         tc_fence_before_sync();
         __syncwarp();
@@ -414,13 +425,13 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         // Only a CTA's last segment can reduce, and it publishes every
         // earlier split segment first, so all arrivals come before any wait;
         // all CTAs are resident at once, so the waits end (and are bounded).
-        const int first = sk_cta_of(args, t * KB), last = sk_cta_of(args, (t + 1) * KB - 1);
+        const int first = sk_cta_of(args, u * KB), last = sk_cta_of(args, (u + 1) * KB - 1);
         const int npart = last - first + 1;
-        const int r_last = sk_begin(args, last + 1) <= (t + 1) * KB ? last : last - 1;
-        const bool reducer = sk_begin(args, cta + 1) <= (t + 1) * KB;
+        const int r_last = sk_begin(args, last + 1) <= (u + 1) * KB ? last : last - 1;
+        const bool reducer = sk_begin(args, cta + 1) <= (u + 1) * KB;
         // Partial slot: 0 for a CTA's first segment, 1 for a later one.
         auto part_of = [&](int pc) {
-          return args.partials + ((size_t)pc * 2 + (sk_begin(args, pc) >= t * KB ? 0 : 1)) * args.Mb * SK_BN;
+          return args.partials + ((size_t)pc * 2 + (sk_begin(args, pc) >= u * KB ? 0 : 1)) * args.Mb * SK_BN;
         };
         // A reducer adds its own sums straight from tensor memory; it writes
         // them out only when other reducers need them.
@@ -435,7 +446,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < SK_CHUNK; ++j) {
               const int col = ch * SK_CHUNK + j;
-              if (col < args.M) part[(size_t)col * SK_BN + row] = __uint_as_float(r[j]);
+              if (col < gcols) part[(size_t)col * SK_BN + row] = __uint_as_float(r[j]);
             }
           }
         }
@@ -475,8 +486,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
           __syncwarp();  // warps reach a barrier converged (bar.* counts whole warps)
           have = named_bar_and(1, 128, have);
           const int ri = cta - first;
-          const int per = ((args.M + nred - 1) / nred + SK_CHUNK - 1) / SK_CHUNK * SK_CHUNK;
-          const int c0 = ri * per, c1 = min(args.M, c0 + per);
+          const int per = ((gcols + nred - 1) / nred + SK_CHUNK - 1) / SK_CHUNK * SK_CHUNK;
+          const int c0 = ri * per, c1 = min(gcols, c0 + per);
           // The other participants' partials for the slice come into the
           // stage ring (idle in a CTA's last segment: every load landed and
           // every MMA that read it completed) with bulk copies, in rounds of
@@ -548,7 +559,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
           __syncwarp();
         }
       }
-      g = t * KB + kb1;
+      g = u * KB + kb1;
     }
     tc_fence_before_sync();
     __syncwarp();
@@ -595,11 +606,19 @@ static bool sk_resident(size_t smem) {
   return n >= 1;
 }
 
+// Token groups of M rows: as few as keep a group within SK_GROUP_ROWS, of
+// equal size rounded up to 16 (the MMA's N granularity).
+static void sk_groups(int M, int *n_tg, int *Mb) {
+  const int g = (M + SK_GROUP_ROWS - 1) / SK_GROUP_ROWS;
+  *n_tg = g;
+  *Mb = ((M + g - 1) / g + 15) / 16 * 16;
+}
+
 SkShape sk_shape(int M, int N, int K, int num_sms, bool f8) {
   SkShape s = {};
   s.ok = false;
-  if (M < 1 || M > SK_MAX_ROWS || num_sms <= 0) return s;
-  s.Mb = (M + 15) / 16 * 16;
+  if (M < 1 || M > SK_GROUP_ROWS * SK_MAX_GROUPS || num_sms <= 0) return s;
+  sk_groups(M, &s.n_tg, &s.Mb);
   int cols = 32;
   while (cols < s.Mb) cols <<= 1;
   s.cols = cols;
@@ -610,8 +629,8 @@ SkShape sk_shape(int M, int N, int K, int num_sms, bool f8) {
   s.n_tiles = (N + SK_BN - 1) / SK_BN;
   const int kbe = f8 ? 2 * SK_BK : SK_BK;  // values per 128-byte k-block row
   s.kblocks = (K + kbe - 1) / kbe;
-  s.total = s.n_tiles * s.kblocks;
-  // Shares of at least ceil(kblocks / SK_MAX_PARTIALS) k-blocks: a tile then
+  s.total = s.n_tiles * s.n_tg * s.kblocks;
+  // Shares of at least ceil(kblocks / SK_MAX_PARTIALS) k-blocks: a unit then
   // meets at most SK_MAX_PARTIALS + 1 CTAs.
   int share = (s.kblocks + SK_MAX_PARTIALS - 1) / SK_MAX_PARTIALS;
   if (share < SK_MIN_SHARE) share = SK_MIN_SHARE;
@@ -625,8 +644,10 @@ SkShape sk_shape(int M, int N, int K, int num_sms, bool f8) {
 }
 
 size_t sk_partial_bytes(int M, int num_sms) {
-  if (M < 1 || M > SK_MAX_ROWS) return 0;
-  return (size_t)num_sms * 2 * ((M + 15) / 16 * 16) * SK_BN * sizeof(float);
+  if (M < 1 || M > SK_GROUP_ROWS * SK_MAX_GROUPS) return 0;
+  int n_tg = 0, Mb = 0;
+  sk_groups(M, &n_tg, &Mb);
+  return (size_t)num_sms * 2 * Mb * SK_BN * sizeof(float);
 }
 
 typedef CUresult (*SkEncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -685,6 +706,7 @@ cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partia
   a.N = g.N;
   a.K = g.K;
   a.Mb = sh.Mb;
+  a.n_tg = sh.n_tg;
   a.kblocks = sh.kblocks;
   a.total = sh.total;
   a.P = sh.P;
@@ -725,6 +747,7 @@ cudaError_t launch_gemm_sk_f8(const F8Launch &g, const SkShape &sh, float *parti
   a.N = g.N;
   a.K = g.K;
   a.Mb = sh.Mb;
+  a.n_tg = sh.n_tg;
   a.kblocks = sh.kblocks;
   a.total = sh.total;
   a.P = sh.P;

@@ -86,14 +86,15 @@ struct GemmLaunch {
 cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s, int *err_code);
 
 // Steps a3 + a4 as a persistent stream-K kernel (gemm_sk.cu): one CTA per SM,
-// equal shares of the (tile, k-block) pairs, at most 256 token rows, draft mode
+// equal shares of the (tile, token group, k-block) triples, at most 1024 token
+// rows in groups of at most 256, draft mode
 // or verify mode with the tensor-core expand.  Needs sk_partial_bytes(M, SMs)
 // of scratch for partial sums and one flag word per CTA (zero between calls).
 // `ok` is false when a CTA of that shape would not fit on every SM at once
 // (the cross-CTA waits need the whole grid resident).
 struct SkShape {
   bool ok;
-  int Mb, cols, stages, n_tiles, kblocks, total, P;
+  int Mb, n_tg, cols, stages, n_tiles, kblocks, total, P;  // Mb rows in each of n_tg token groups
   size_t smem_bytes;
 };
 SkShape sk_shape(int M, int N, int K, int num_sms, bool f8 = false);

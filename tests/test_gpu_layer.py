@@ -125,11 +125,13 @@ def _zipf_idx(seed, M, n_ad, s=1.1):
 
 
 @pytest.mark.parametrize("M,N,K,n_ad,ranks,zipf", [
-    # more than 256 rows: cluster kernel, two MMAs per k-step, sorted rows and token windows
-    (384, 1024, 1024, 16, (8, 16, 32, 64) * 4, False),
+    # more than 256 rows: stream-K over token groups of at most 256 rows, sorted rows and token windows
+    (384, 1024, 1024, 16, (8, 16, 32, 64) * 4, False),            # two groups of 192
     (512, 640, 2048, 128, tuple([8, 16, 32, 64] * 32), True),    # heterogeneous ranks, Zipf: large and single rows
-    (640, 768, 1536, 64, (16,) * 64, False),                      # two token groups of 320 rows
-    (1000, 256, 512, 40, tuple([8, 24, 40, 56, 64] * 8), True),   # windows crossing the token-group boundary
+    (640, 768, 1536, 64, (16,) * 64, False),                      # three groups of 224
+    (1000, 256, 512, 40, tuple([8, 24, 40, 56, 64] * 8), True),   # four groups; windows crossing group boundaries
+    # more than 256 rows with full cluster waves: cluster kernel, two MMAs per k-step, 320-row token groups
+    (640, 18432, 512, 64, (16,) * 64, False),
     # stream-K verify (at most 256 rows) with hundreds of expand blocks and ranks inside 16-wide blocks
     (256, 6144, 1024, 128, (64,) * 128, False),
     (200, 640, 2048, 64, (8, 24, 40, 56) * 16, True),
@@ -192,6 +194,9 @@ def test_stream_k_flag_wait_gives_up_and_workspace_recovers():
     (128, 14336, 4096),  # stream-K, the gate shape in verify mode
     (16, 28672, 4096),   # stream-K, the fused gate|up shape, few rows
     (1, 8, 512),         # stream-K, a single CTA
+    (640, 640, 1024),    # stream-K, three token groups of 224 rows
+    (384, 384, 2048),    # stream-K, two token groups of 192 rows
+    (1024, 256, 512),    # stream-K, four token groups of 256 rows
 ])
 def test_split_tiles_oracle_and_determinism(M, N, K):
     """Shapes whose tiles are shared by several CTAs, through both GEMM
