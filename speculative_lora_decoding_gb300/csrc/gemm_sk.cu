@@ -13,12 +13,13 @@
 // Adapter Selection").
 //
 // Work split.  The token rows form up to four groups of at most 256 (Mb
-// rows each); a unit is a tile of 128 W rows with one token group, units go
-// tile by tile (the groups of a tile side by side, so a W tile read from
-// DRAM serves them all from L2).  The (unit, 64-wide k-block) pairs are cut
-// into one contiguous, equal share per CTA, one CTA per SM, so every SM
-// streams the same number of bytes whatever the unit count (no partial last
-// wave).  A CTA's share is a sequence of segments: the tail of a unit begun
+// rows each); every group gets the same number of CTAs (at most one per SM
+// in all), and a unit is a tile of 128 W rows with the CTAs' token group.
+// Within a group the (tile, 64-wide k-block) pairs are cut into one
+// contiguous, equal share per CTA, so every SM streams the same number of
+// bytes whatever the tile count (no partial last wave), and CTA j of every
+// group streams the same W k-blocks at about the same time: a W tile comes
+// from DRAM once and serves the other groups from L2.  A CTA's share is a sequence of segments: the tail of a unit begun
 // by the CTA before it, whole units, and the head of a unit that the CTAs
 // after it finish.  The CTA that holds a unit's first k-block owns the unit
 // and adds the expand MMAs.  A split unit is finished by its participants
@@ -62,7 +63,8 @@ constexpr int SK_GROUP_ROWS = 256;               // token rows of a group: two a
 constexpr int SK_MAX_GROUPS = 4;                 // token groups of a call (M <= 1024)
 struct SkArgs {
   int M, N, K, Mb, kblocks, total, P, stages, cols;
-  int n_tg;  // token groups: unit u is (W tile u / n_tg, token rows [(u % n_tg) Mb, +Mb))
+  int n_tg;  // token groups; CTAs [g Pg, (g + 1) Pg) serve group g (token rows [g Mb, +Mb))
+  int Pg;    // CTAs per token group; total = (tile, k-block) pairs of one group
   int mode, prefetch_w, after_shrink;
   int sorted;  // verify mode: x in adapter-sorted order, token windows present
   int n_slices, slice_end[MLORA_MAX_SLICES];
@@ -79,12 +81,14 @@ struct SkArgs {
   const float *x_scale;
 };
 
-__device__ __forceinline__ int sk_begin(const SkArgs &a, int i) { return (int)((long long)i * a.total / a.P); }
+// Shares within a token group's CTAs: local CTA i holds linear k-blocks
+// [sk_begin(i), sk_begin(i + 1)) of the group's (tile, k-block) pairs.
+__device__ __forceinline__ int sk_begin(const SkArgs &a, int i) { return (int)((long long)i * a.total / a.Pg); }
 
-// The CTA whose share holds linear k-block g.
+// The local CTA whose share holds linear k-block g.
 __device__ __forceinline__ int sk_cta_of(const SkArgs &a, int g) {
-  int i = (int)((long long)g * a.P / a.total);
-  while (i + 1 < a.P && sk_begin(a, i + 1) <= g) ++i;
+  int i = (int)((long long)g * a.Pg / a.total);
+  while (i + 1 < a.Pg && sk_begin(a, i + 1) <= g) ++i;
   while (i > 0 && sk_begin(a, i) > g) --i;
   return i;
 }
@@ -126,7 +130,12 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
   const int KB = args.kblocks;
-  const int g0 = sk_begin(args, cta), g1 = sk_begin(args, cta + 1);
+  // Token group of this CTA and its index among the group's CTAs: CTA j of
+  // every group streams the same W k-blocks at about the same time, so a W
+  // tile read from DRAM for one group serves the others from L2.
+  const int grp = cta / args.Pg, lc = cta - grp * args.Pg, cbase = grp * args.Pg;
+  const int m0 = grp * args.Mb;
+  const int g0 = sk_begin(args, lc), g1 = sk_begin(args, lc + 1);
   const bool tc = !F8 && args.sorted != 0 && args.mode == MLORA_VERIFY;
   const PlanLayout L = plan_layout(args.M, args.n_ad);
 
@@ -183,8 +192,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         for (int g = g0; g < g1 && early < S; ++g, ++early) {
           const int u = g / KB, kb = g - u * KB;
           mbar_arrive_expect_tx(&full[early], tx);
-          tma_load_2d(ring + (size_t)early * stage_bytes, &tmap_w, &full[early], kb * KBE, (u / args.n_tg) * SK_BN,
-                      pol_w);
+          tma_load_2d(ring + (size_t)early * stage_bytes, &tmap_w, &full[early], kb * KBE, u * SK_BN, pol_w);
         }
       }
       if (waited) grid_dependency_wait();
@@ -192,7 +200,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     early = __shfl_sync(0xffffffffu, early, 0);
     // k-blocks [from, to) of unit u, lane 0 only.
     auto issue_kblocks = [&](int u, int from, int to) {
-      const int w_row = (u / args.n_tg) * SK_BN, x_row = (u % args.n_tg) * args.Mb;
+      const int w_row = u * SK_BN, x_row = m0;
       for (int kb = from; kb < to; ++kb, ++i) {
         uint8_t *st = ring + (size_t)stage * stage_bytes;
         if (i >= early) {
@@ -221,7 +229,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     };
     for (int g = g0; g < g1 && ok;) {
       const int u = g / KB, kb0 = g - u * KB, kb1 = min(KB, g1 - u * KB);
-      const int t = u / args.n_tg, m0 = (u % args.n_tg) * args.Mb;
+      const int t = u;
       // The expand operands of an owned unit (verify mode) go into the ring
       // before the unit's last S k-blocks, so that they land while those
       // stream instead of after the whole unit.
@@ -354,7 +362,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     int seg = 0;
     for (int g = g0; g < g1; ++seg) {
       const int u = g / KB, kb0 = g - u * KB, kb1 = min(KB, g1 - u * KB);
-      const int t = u / args.n_tg, m0 = (u % args.n_tg) * args.Mb;
+      const int t = u;
       const int gcols = min(args.Mb, args.M - m0);  // token columns of this unit
       const int buf = seg & 1;
       // All 128 threads agree on the outcome before any of them branches, so
@@ -425,13 +433,13 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         // Only a CTA's last segment can reduce, and it publishes every
         // earlier split segment first, so all arrivals come before any wait;
         // all CTAs are resident at once, so the waits end (and are bounded).
-        const int first = sk_cta_of(args, u * KB), last = sk_cta_of(args, (u + 1) * KB - 1);
+        const int first = cbase + sk_cta_of(args, u * KB), last = cbase + sk_cta_of(args, (u + 1) * KB - 1);
         const int npart = last - first + 1;
-        const int r_last = sk_begin(args, last + 1) <= (u + 1) * KB ? last : last - 1;
-        const bool reducer = sk_begin(args, cta + 1) <= (u + 1) * KB;
+        const int r_last = sk_begin(args, last - cbase + 1) <= (u + 1) * KB ? last : last - 1;
+        const bool reducer = sk_begin(args, lc + 1) <= (u + 1) * KB;
         // Partial slot: 0 for a CTA's first segment, 1 for a later one.
         auto part_of = [&](int pc) {
-          return args.partials + ((size_t)pc * 2 + (sk_begin(args, pc) >= u * KB ? 0 : 1)) * args.Mb * SK_BN;
+          return args.partials + ((size_t)pc * 2 + (sk_begin(args, pc - cbase) >= u * KB ? 0 : 1)) * args.Mb * SK_BN;
         };
         // A reducer adds its own sums straight from tensor memory; it writes
         // them out only when other reducers need them.
@@ -629,15 +637,17 @@ SkShape sk_shape(int M, int N, int K, int num_sms, bool f8) {
   s.n_tiles = (N + SK_BN - 1) / SK_BN;
   const int kbe = f8 ? 2 * SK_BK : SK_BK;  // values per 128-byte k-block row
   s.kblocks = (K + kbe - 1) / kbe;
-  s.total = s.n_tiles * s.n_tg * s.kblocks;
+  s.total = s.n_tiles * s.kblocks;  // (tile, k-block) pairs of one token group
   // Shares of at least ceil(kblocks / SK_MAX_PARTIALS) k-blocks: a unit then
   // meets at most SK_MAX_PARTIALS + 1 CTAs.
   int share = (s.kblocks + SK_MAX_PARTIALS - 1) / SK_MAX_PARTIALS;
   if (share < SK_MIN_SHARE) share = SK_MIN_SHARE;
-  int P = s.total / share;
-  if (P > num_sms) P = num_sms;
-  if (P < 1) P = 1;
-  s.P = P;
+  // The same number of CTAs for each token group, all resident at once.
+  int Pg = s.total / share;
+  if (Pg > num_sms / s.n_tg) Pg = num_sms / s.n_tg;
+  if (Pg < 1) Pg = 1;
+  s.Pg = Pg;
+  s.P = Pg * s.n_tg;
   s.smem_bytes = SK_SMEM_FIXED + (size_t)s.stages * stage_bytes;
   s.ok = f8 ? sk_resident<true>(s.smem_bytes) : sk_resident<false>(s.smem_bytes);
   return s;
@@ -710,6 +720,7 @@ cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partia
   a.kblocks = sh.kblocks;
   a.total = sh.total;
   a.P = sh.P;
+  a.Pg = sh.Pg;
   a.stages = sh.stages;
   a.cols = sh.cols;
   a.mode = g.mode;
@@ -751,6 +762,7 @@ cudaError_t launch_gemm_sk_f8(const F8Launch &g, const SkShape &sh, float *parti
   a.kblocks = sh.kblocks;
   a.total = sh.total;
   a.P = sh.P;
+  a.Pg = sh.Pg;
   a.stages = sh.stages;
   a.cols = sh.cols;
   a.mode = MLORA_DRAFT;

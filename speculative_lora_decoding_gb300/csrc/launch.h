@@ -94,7 +94,7 @@ cudaError_t launch_gemm(const GemmLaunch &g, const GemmShape &sh, cudaStream_t s
 // (the cross-CTA waits need the whole grid resident).
 struct SkShape {
   bool ok;
-  int Mb, n_tg, cols, stages, n_tiles, kblocks, total, P;  // Mb rows in each of n_tg token groups
+  int Mb, n_tg, cols, stages, n_tiles, kblocks, total, P, Pg;  // Mb rows in each of n_tg groups, Pg CTAs per group
   size_t smem_bytes;
 };
 SkShape sk_shape(int M, int N, int K, int num_sms, bool f8 = false);
