@@ -101,7 +101,7 @@ def layer_bytes_flops(M, K, N, active_ranks, verify, n_proj=1):
 TRAFFIC_SOURCES = {
     "gemm_sk_kernel": ("gemm_sk.cu", "expand.cuh", "common.cuh"),
     "gemm_kernel": ("gemm.cu", "expand.cuh", "common.cuh"),
-    "accept_stream_kernel": ("accept.cu", "common.cuh"),
+    "accept_blocks_kernel": ("accept.cu", "common.cuh"),
 }
 
 
