@@ -88,21 +88,18 @@ static bool linear_sizes_ok(int M, int N, int K, int n_ad) {
 static mlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLORA_OK : MLORA_ERR_CUDA; }
 
 // Which GEMM kernel a layer call runs.  The cluster split-K kernel wins when
-// its tiles fill at least 80% of the SMs in a single wave: the weights then
-// stream at the full HBM rate and its on-chip reduction is the shortest
-// tail.  Past 256 rows it wins with one wave at least 70% full, or several
-// at least 90% full: its 320-row token groups read fewer bytes from L2 per
-// MMA than the stream-K kernel's groups of at most 256 (measured at 640 rows:
-// q|k|v, 112 CTAs in one wave, 119 us against 129 us).  Otherwise (a partial last wave, or idle
+// its tiles fill at least 80% of the SMs in a single wave (70% past 256 rows):
+// the weights then stream at the full HBM rate and its on-chip reduction is
+// the shortest tail.  Otherwise (a partial last wave, several waves, or idle
 // SMs) the persistent stream-K kernel runs, if it can: batches of up to 1024
 // rows whose CTAs fit on every SM at once, in verify mode with the token
-// windows.
+// windows.  Measured on the 32B block at 640 verify rows: q|k|v (112 cluster
+// CTAs in one wave) 100 us on the cluster kernel, 111 us on stream-K; gate|up
+// (5.7 cluster waves) 437 us against 377 us on stream-K.
 static bool use_stream_k(int M, int N, int K, bool verify, bool have_tw, bool have_sk, int sms, const GemmShape &gs,
                          SkShape *sk_out) {
   bool cluster_good = gs.waves == 1 && (long long)gs.n_units * gs.C * 5 >= (long long)sms * 4;
-  if (M > 256)
-    cluster_good = gs.waves == 1 ? (long long)gs.n_units * gs.C * 10 >= (long long)sms * 7
-                                 : (long long)gs.n_units * gs.C * 10 >= (long long)gs.waves * sms * 9;
+  if (M > 256) cluster_good = gs.waves == 1 && (long long)gs.n_units * gs.C * 10 >= (long long)sms * 7;
   const SkShape sk = sk_shape(M, N, K, sms);
   if (sk_out) *sk_out = sk;
   const bool fits = sk.ok && have_sk && (!verify || have_tw);

@@ -130,8 +130,8 @@ def _zipf_idx(seed, M, n_ad, s=1.1):
     (512, 640, 2048, 128, tuple([8, 16, 32, 64] * 32), True),    # heterogeneous ranks, Zipf: large and single rows
     (640, 768, 1536, 64, (16,) * 64, False),                      # three groups of 224
     (1000, 256, 512, 40, tuple([8, 24, 40, 56, 64] * 8), True),   # four groups; windows crossing group boundaries
-    # more than 256 rows with full cluster waves: cluster kernel, two MMAs per k-step, 320-row token groups
-    (640, 18432, 512, 64, (16,) * 64, False),
+    # more than 256 rows in one well-filled cluster wave: cluster kernel, two MMAs per k-step, 320-row groups
+    (640, 7168, 512, 64, (16,) * 64, False),
     # stream-K verify (at most 256 rows) with hundreds of expand blocks and ranks inside 16-wide blocks
     (256, 6144, 1024, 128, (64,) * 128, False),
     (200, 640, 2048, 64, (8, 24, 40, 56) * 16, True),

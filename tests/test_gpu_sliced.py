@@ -154,8 +154,8 @@ def test_gemm_kernel_query():
     """mlora_linear_gemm_kernel names one of the two GEMM kernels for valid
     shapes and refuses invalid ones; on a 152-SM GB300 the decode step's
     4-tile-per-SM shapes (o, down) take the cluster kernel and the others
-    the stream-K kernel; past 256 rows the cluster kernel only where its waves
-    are full."""
+    the stream-K kernel; past 256 rows the cluster kernel only for one wave
+    that fills 70% of the SMs."""
     ml = needs_gpu()
     for M, N, K in [(64, 6144, 4096), (64, 4096, 4096), (64, 28672, 4096), (64, 4096, 14336), (700, 512, 512)]:
         for mode in (ml.DRAFT, ml.VERIFY):
@@ -164,8 +164,8 @@ def test_gemm_kernel_query():
         ml.gemm_kernel_name(64, 4096, 4097, 16, 16, ml.DRAFT)
     assert ml.gemm_kernel_name(1100, 512, 512, 16, 16, ml.DRAFT) == "gemm_kernel"  # past the stream-K kernel's 1024 rows
     if torch.cuda.get_device_properties(0).multi_processor_count == 152:
-        # 640 verify rows (the 32B block at k = 4): gate|up fills its cluster waves, o and down do not
-        assert ml.gemm_kernel_name(640, 55296, 5120, 64, 16, ml.VERIFY) == "gemm_kernel"
+        # 640 verify rows (the 32B block at k = 4): only q|k|v has one well-filled cluster wave
+        assert ml.gemm_kernel_name(640, 55296, 5120, 64, 16, ml.VERIFY) == "gemm_sk_kernel"
         assert ml.gemm_kernel_name(640, 5120, 5120, 64, 16, ml.VERIFY) == "gemm_sk_kernel"
         assert ml.gemm_kernel_name(640, 5120, 27648, 64, 16, ml.VERIFY) == "gemm_sk_kernel"
         assert ml.gemm_kernel_name(640, 7168, 5120, 64, 16, ml.VERIFY) == "gemm_kernel"  # one wave, 74% full
