@@ -56,7 +56,9 @@ constexpr int SK_WTILE = SK_BN * SK_BK * 2;      // 16 KB
 constexpr int SK_CHUNK = 32;                     // accumulator columns per tensor-memory load
 constexpr size_t SK_SMEM_LIMIT = 220 * 1024;     // leaves room for a co-resident shrink CTA
 constexpr int SK_MAX_STAGES = 8;
-constexpr size_t SK_SMEM_FIXED = 1024 + 256 + expand_smem_bytes(SK_MAX_STAGES);  // alignment slack, barriers, expand records
+constexpr int SK_CACHE_BLOCKS = 256;             // expand block records kept in shared memory (8 KB)
+// Alignment slack, barriers, the expand stage records, the cached block records.
+constexpr size_t SK_SMEM_FIXED = 1024 + 256 + expand_smem_bytes(SK_MAX_STAGES) + SK_CACHE_BLOCKS * EXP_WORDS * 4;
 constexpr int SK_MIN_SHARE = 8;                  // k-blocks per CTA at least
 constexpr int SK_MAX_PARTIALS = 8;               // contributors per tile besides its owner, at most
 constexpr int SK_GROUP_ROWS = 256;               // token rows of a group: two accumulators fit in tensor memory
@@ -126,6 +128,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi_done + 1);
   int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
   int *zero_word = abort_flag + 1;    // stays 0: for waits that only a time limit may end
+  // The plan's expand block records, copied once per CTA (verify mode): every
+  // owned unit scans them, so the scans read shared memory, not L2.
+  int32_t *blk_cache = reinterpret_cast<int32_t *>(ring + (size_t)S * stage_bytes + expand_smem_bytes(S) + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -181,6 +186,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     const uint64_t pol_x = policy_evict_last();
     const uint32_t tx = (uint32_t)stage_bytes;
     int stage = 0, issued = 0, i = 0, early = 0, ns = -1;
+    bool cached = false;
     uint32_t phase = 0;
     bool ok = true;
     bool waited = !args.after_shrink;
@@ -243,8 +249,14 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
           waited = true;
         }
         if (ns < 0) ns = args.plan[L.hdr + 4];
+        if (ns > 0 && !cached && ns <= SK_CACHE_BLOCKS) {
+          const int4 *src = reinterpret_cast<const int4 *>(args.plan + L.slices);
+          for (int q = lane; q < ns * (EXP_WORDS / 4); q += 32) reinterpret_cast<int4 *>(blk_cache)[q] = src[q];
+          __syncwarp();
+          cached = true;
+        }
         if (ns > 0)
-          ok = expand_produce(args.plan + L.slices, 0, ns, m0, args.Mb, t * SK_BN, args.N, &tmap_b,
+          ok = expand_produce(cached ? blk_cache : args.plan + L.slices, 0, ns, m0, args.Mb, t * SK_BN, args.N, &tmap_b,
                               args.tw + (size_t)sk_slice_of(args, t * SK_BN) * args.tw_slice, ring, stage_bytes, S,
                               full, empty, meta, chunk, stage, phase, issued, ab, pol_w, lane, args.n_ad,
                               (long long)(args.tw_slice / 16), args.status);
