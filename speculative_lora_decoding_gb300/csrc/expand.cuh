@@ -135,7 +135,16 @@ __device__ __forceinline__ bool expand_produce(const int32_t *blocks, int blo, i
         for (int c = 0; c < cnt; ++c) {
           const int4 r = chunk[sel[c]];
           tma_load_2d(st + c * EXP_B_TILE, tmap_b, &full[stage], r.y & 0xFF, r.x * N + n0, pol);
-          bulk_load(st + m.blk[c].y, tw + (size_t)r.z * 16, (uint32_t)((r.w >> 16) * 32), &full[stage]);
+        }
+        // The windows of consecutive blocks usually sit back to back in the
+        // window buffer (the plan lays them out in block order): one bulk
+        // copy per run of contiguous windows, not one per block.
+        for (int c = 0; c < cnt;) {
+          const int4 r = chunk[sel[c]];
+          int rows = r.w >> 16, e = c + 1;
+          while (e < cnt && chunk[sel[e]].z == r.z + rows) rows += chunk[sel[e++]].w >> 16;
+          bulk_load(st + m.blk[c].y, tw + (size_t)r.z * 16, (uint32_t)(rows * 32), &full[stage]);
+          c = e;
         }
         emitted = true;
         ++issued;
