@@ -1017,6 +1017,7 @@ def run_gpu(args):
         __graft_entry__.build()
     if not ml.device_supported():
         raise RuntimeError("this benchmark needs a compute capability 10.3 GPU")
+    ml.set_shrink_path({"auto": ml.SHRINK_AUTO, "warp": ml.SHRINK_WARP, "tensor": ml.SHRINK_TENSOR}[args.shrink])
 
     peaks = _peaks()
     stream = torch.cuda.Stream(device)
@@ -1137,7 +1138,7 @@ def run_gpu(args):
             "config": {"workload": head_workload, "requests": head_cfg.n_requests, "draft_len": k,
                        "draft_rows_per_pass": Md, "verify_rows": Mv,
                        "projections": [p[0] for p in head_cfg.projections], "layer_calls": calls,
-                       "parallelism": f"replicas x{world}", "l2": head["l2"],
+                       "parallelism": f"replicas x{world}", "l2": head["l2"], "shrink": args.shrink,
                        "graph": "one CUDA graph per step; the plan runs on a second stream beside the draft passes"},
             "gpu_launches": head["launches_per_step"] * args.steps,
             "roofline": head["roofline"],
@@ -1169,6 +1170,8 @@ def main():
     ap.add_argument("--only", default=None, choices=["accept"],
                     help="run only the accept sweep (batch 256, vocabulary 128256, k = 1..4) and print its results")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--shrink", default="auto", choices=["auto", "warp", "tensor"],
+                    help="which kernel writes the verify pass's low-rank operand (default: the library's choice)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -254,6 +254,20 @@ MLORA_API int mlora_linear_gemm_kernel(int M, int N, int K, int n_adapters, int 
  * hangs or faults. */
 MLORA_API void mlora_debug_set_flag_wait_ns(uint32_t ns);
 
+/* Which kernel writes the low-rank operand (the token windows of
+ * bf16(scale * A_a x)) in later verify-mode layer calls (no counterpart on the
+ * pages, which compute the per-adapter product without naming a kernel):
+ *   MLORA_SHRINK_AUTO    the library's choice from the call's sizes (default);
+ *   MLORA_SHRINK_WARP    warp items of 8 rank rows x 4 tokens (CUDA cores);
+ *   MLORA_SHRINK_TENSOR  128-row tcgen05 tiles over 8 expand blocks' tokens.
+ * The two differ only in fp32 summation order.  Process-wide; not for use
+ * while other threads issue layer calls.  Returns MLORA_ERR_ARG for another
+ * value.  mlora_shrink (the T output) always runs the warp items. */
+#define MLORA_SHRINK_AUTO   0
+#define MLORA_SHRINK_WARP   1
+#define MLORA_SHRINK_TENSOR 2
+MLORA_API mlora_status mlora_set_shrink_path(int path);
+
 /* Allocation-free variant of mlora_linear.  The paper has no counterpart;
  * this is for callers that cannot allocate device memory for a workspace (a
  * plugin inside a host framework that owns every device buffer, or code

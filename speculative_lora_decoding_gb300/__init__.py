@@ -31,6 +31,7 @@ import torch
 DRAFT = 0
 VERIFY = 1
 PREFETCH_WEIGHTS = 0x100  # mode flag: W is constant; may be streamed before the preceding kernel ends
+SHRINK_AUTO, SHRINK_WARP, SHRINK_TENSOR = 0, 1, 2  # which kernel writes the verify pass's low-rank operand
 
 # Limits of mlora_linear_noalloc (its scratch is a fixed array in the library).
 NOALLOC_MAX_ROWS = 1024
@@ -74,6 +75,7 @@ _SIGNATURES = {
                                       _c_ptr, _c_ptr, _c_float, _c_int, _c_ptr, _c_ptr]),
     "mlora_linear_gemm_kernel": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "mlora_debug_set_flag_wait_ns": (None, [ctypes.c_uint32]),
+    "mlora_set_shrink_path": (_c_int, [_c_int]),
     "mlora_verify_accept_logits": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr, _c_ptr,
                                             _c_ptr, _c_size, _c_ptr]),
     "mlora_softmax_workspace_bytes": (_c_size, [_c_int, _c_int]),
@@ -172,6 +174,12 @@ def gemm_kernel_name(M: int, N: int, K: int, n_adapters: int, r_max: int, mode: 
     if k < 0:
         raise ValueError("sizes or mode outside the supported ranges")
     return ("gemm_kernel", "gemm_sk_kernel")[k]
+
+
+def set_shrink_path(path: int) -> None:
+    """Which kernel writes the verify pass's low-rank operand in later layer
+    calls: SHRINK_AUTO (the library's choice), SHRINK_WARP or SHRINK_TENSOR."""
+    _check(_load().mlora_set_shrink_path(int(path)), "mlora_set_shrink_path")
 
 
 def linear_workspace_bytes(M: int, N: int, K: int, n_adapters: int) -> int:

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmlora.so")
-SOURCES = ("api.cu", "plan.cu", "shrink.cu", "gemm.cu", "gemm_sk.cu", "accept.cu", "softmax.cu", "kvcache.cu", "fp8.cu", "noalloc.cu")
+SOURCES = ("api.cu", "plan.cu", "shrink.cu", "shrink_mma.cu", "gemm.cu", "gemm_sk.cu", "accept.cu", "softmax.cu", "kvcache.cu", "fp8.cu", "noalloc.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -63,6 +63,7 @@ static LinearLayout linear_layout(int M, int K, int n_ad, int n_slices, int sms)
 // Test knob (mlora_debug_set_flag_wait_ns): nonzero makes the stream-K GEMM's
 // tile owners wait that long on flags nothing sets.
 static std::atomic<uint32_t> g_test_flag_wait_ns{0};
+static std::atomic<int> g_shrink_path{MLORA_SHRINK_AUTO};
 
 // Slice ends: increasing, every one but the last a multiple of 128 (the
 // GEMM's tile height), the last equal to N.
@@ -104,6 +105,25 @@ static bool use_stream_k(int M, int N, int K, bool verify, bool have_tw, bool ha
   if (sk_out) *sk_out = sk;
   const bool fits = sk.ok && have_sk && (!verify || have_tw);
   return fits && !cluster_good;
+}
+
+// Which shrink writes the verify pass's token windows: the tensor-core tile
+// (launch_shrink_mma) or the warp items (launch_shrink), unless a path was
+// forced with mlora_set_shrink_path.  Both read each A row from DRAM once;
+// the warp items re-read it from L2 once per 4 tokens of its segment, the
+// tiles once per unit of 8 blocks, but the tiles use fewer SMs.  Measured on
+// GB300 (whole verify call, 640 and 512 rows, K 5120 and 14336): the tiles
+// win by 7-21% at rank 64 with 8..128 rows per adapter, lose by 4-44% with
+// fewer adapters (too few units to fill the SMs) or at rank 16 (little
+// re-reading to save), and by up to 8% with 4 rows per adapter.
+static bool shrink_on_tensor_cores(int M, int K, int n_ad, int r_max, int n_slices) {
+  const int forced = g_shrink_path.load(std::memory_order_relaxed);
+  if (forced == MLORA_SHRINK_WARP) return false;
+  if (forced == MLORA_SHRINK_TENSOR) return true;
+  (void)K, (void)n_slices;
+  const int m_ad = M < n_ad ? M : n_ad;
+  const int rows_per_adapter = M / m_ad;
+  return r_max >= 64 && M >= 512 && rows_per_adapter >= 8 && rows_per_adapter <= 128;
 }
 
 }  // namespace mlora
@@ -235,7 +255,11 @@ static mlora_status linear_impl(const mlora_bf16 *x, int M, int K, const mlora_b
     // windows of the tensor-core expand.
     e = launch_gather_rows(x, M, K, plan + P.perm, xs, sms, status, s);
     if (e != cudaSuccess) return MLORA_ERR_CUDA;
-    e = launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, tw, scale, S, status, s);
+    if (shrink_on_tensor_cores(M, K, n_ad, r_max, S)) {
+      e = launch_shrink_mma(xs, M, K, A_stack, n_ad, r_max, plan, tw, scale, S, sms, status, s);
+    } else {
+      e = launch_shrink(x, M, K, A_stack, n_ad, r_max, plan, T, T_STRIDE, false, sms, tw, scale, S, status, s);
+    }
     if (e != cudaSuccess) return MLORA_ERR_CUDA;
   }
   GemmLaunch g;
@@ -305,6 +329,12 @@ int mlora_linear_gemm_kernel(int M, int N, int K, int n_adapters, int r_max, int
 }
 
 void mlora_debug_set_flag_wait_ns(uint32_t ns) { g_test_flag_wait_ns.store(ns, std::memory_order_relaxed); }
+
+mlora_status mlora_set_shrink_path(int path) {
+  if (path != MLORA_SHRINK_AUTO && path != MLORA_SHRINK_WARP && path != MLORA_SHRINK_TENSOR) return MLORA_ERR_ARG;
+  g_shrink_path.store(path, std::memory_order_relaxed);
+  return MLORA_OK;
+}
 
 static mlora_status accept_impl(const float *p, const float *q, const int32_t *draft_tok, const float *uniforms, int B,
                                 int k, int V, int32_t *out_tok, int32_t *accepted, void *workspace, size_t ws_bytes,

@@ -53,6 +53,14 @@ cudaError_t launch_shrink(const uint16_t *x, int M, int K, const uint16_t *A, in
                           const int32_t *plan, float *T, int t_stride, bool zero_first, int num_sms, uint16_t *tw,
                           float scale, int n_slices, uint32_t *status, cudaStream_t s);
 
+// The token windows alone (as launch_shrink writes them into `tw`), on the
+// tensor cores: one 128 x (up to 256) MMA tile per 8 consecutive expand
+// blocks over their tokens in adapter-sorted order `xs` [M, K], split-K
+// over a thread-block cluster.  Reads the plan; writes no T.
+cudaError_t launch_shrink_mma(const uint16_t *xs, int M, int K, const uint16_t *A, int n_ad, int r_max,
+                              const int32_t *plan, uint16_t *tw, float scale, int n_slices, int num_sms,
+                              uint32_t *status, cudaStream_t s);
+
 // Steps a3 + a4: base GEMM on tcgen05 with the expand epilogue.
 struct GemmShape {
   int Mb, nsub, sub_n, n_tgroups, n_units, kblocks, total_iters, stages, nbuf, tmem_cols, grid;

@@ -231,15 +231,68 @@ def test_plan_is_bit_exact():
 
 def test_shrink_against_oracle():
     ml = needs_gpu()
-    for (M, K, n_ad, ranks) in [(16, 512, 4, (8, 8, 8, 8)), (512, 4096, 8, (8, 16, 32, 64, 1, 9, 63, 0)),
-                                (37, 14336, 3, (16, 16, 16))]:
+    for (M, K, n_ad, ranks, zipf) in [(16, 512, 4, (8, 8, 8, 8), False),
+                                      (512, 4096, 8, (8, 16, 32, 64, 1, 9, 63, 0), False),
+                                      (37, 14336, 3, (16, 16, 16), False),
+                                      (512, 14336, 128, _het_ranks(128, 3), True)]:
         x, W, A, B, rk, idx = _random_case(K + M, M, 8, K, n_ad, ranks, r_max=64)
+        if zipf:  # heterogeneous ranks under Zipf(1.1): one segment of 100+ rows at rank 64, many singletons
+            idx = _zipf_idx(M + n_ad, M, n_ad)
         T_ref, _ = OL.shrink(WL.bf16_to_f64(x), WL.bf16_to_f64(A), rk, idx)
         ws = ml.Workspace(ml.linear_workspace_bytes(M, 8, K, n_ad))
         seg_p, _ = ml.plan_segments(dev(idx), dev(rk), n_ad, 64, ws)
         T = ml.shrink(dev_bf16(x), dev_bf16(A), seg_p, ws).cpu().numpy().astype(np.float64)
         assert np.isfinite(T).all()
         assert np.max(np.abs(T - T_ref)) <= 1e-4 * max(np.max(np.abs(T_ref)), 1e-30)
+
+
+def _het_ranks(n_ad, seed):
+    rk = np.random.default_rng(seed).choice([8, 16, 32, 64], n_ad)
+    rk[0] = 64  # the most popular adapter under Zipf: a segment of 100+ rows at rank 64
+    return tuple(int(r) for r in rk)
+
+
+@pytest.mark.parametrize("path", ["warp", "tensor"])
+@pytest.mark.parametrize("M,K,n_ad,ranks,zipf", [
+    (512, 14336, 128, _het_ranks(128, 3), True),  # 8B-shaped down projection, heterogeneous ranks, Zipf(1.1)
+    (640, 5120, 64, (16,) * 64, False),           # 32B-shaped q|k|v input, draft length 4
+    (300, 1024, 5, (64, 8, 33, 17, 1), False),    # ranks inside 16-wide blocks, segments of ~60 rows
+    (1000, 512, 3, (64, 64, 16), False),          # segments of 300+ rows: windows wider than one MMA tile
+    (7, 64, 3, (8, 16, 8), False),                # one k-block: no split of K
+    (96, 2048, 40, tuple([1, 9, 17, 33, 63] * 8), True),
+])
+def test_lora_term_alone_both_shrink_paths(M, K, n_ad, ranks, zipf, path):
+    """W = 0: the output is scale * B_a (A_a x) alone, so the low-rank operand
+    (the shrink) is checked against the oracle at full relative weight, with
+    NaN in every padding entry of A and B past each adapter's rank; both
+    kernels that can write it (warp items, tensor-core tiles)."""
+    ml = needs_gpu()
+    N = 256
+    x, W, A, B, rk, idx = _random_case(M + K + n_ad, M, N, K, n_ad, ranks, r_max=64, nan_pad=True)
+    W[:] = 0
+    if zipf:
+        idx = _zipf_idx(M + n_ad, M, n_ad)
+        idx[::13] = -1
+    y_ref, _ = _oracle(x, W, A, B, rk, idx, 2.0, OL.VERIFY)
+    ws = ml.Workspace(ml.linear_workspace_bytes(M, N, K, n_ad))
+    ml.set_shrink_path(ml.SHRINK_WARP if path == "warp" else ml.SHRINK_TENSOR)
+    try:
+        y1 = _run(ml, x, W, A, B, rk, idx, 2.0, OL.VERIFY, ws=ws)
+        y2 = _run(ml, x, W, A, B, rk, idx, 2.0, OL.VERIFY, ws=ws)
+    finally:
+        ml.set_shrink_path(ml.SHRINK_AUTO)
+    assert ws.status() == 0
+    y = host_bf16_to_f64(y1)
+    assert np.isfinite(y).all() and np.abs(y_ref).max() > 0
+    assert _rel_err(y, y_ref) <= TOL, (M, K, n_ad, path)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))  # deterministic
+
+
+def test_set_shrink_path_rejects_unknown_values():
+    ml = needs_gpu()
+    with pytest.raises(ml.MLoraError):
+        ml.set_shrink_path(3)
+    ml.set_shrink_path(ml.SHRINK_AUTO)
 
 
 def test_zero_B_verify_equals_draft_bitwise():
