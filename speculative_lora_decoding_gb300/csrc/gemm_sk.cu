@@ -57,8 +57,12 @@ constexpr int SK_CHUNK = 32;                     // accumulator columns per tens
 constexpr size_t SK_SMEM_LIMIT = 220 * 1024;     // leaves room for a co-resident shrink CTA
 constexpr int SK_MAX_STAGES = 8;
 constexpr int SK_CACHE_BLOCKS = 256;             // expand block records kept in shared memory (8 KB)
-// Alignment slack, barriers, the expand stage records, the cached block records.
-constexpr size_t SK_SMEM_FIXED = 1024 + 256 + expand_smem_bytes(SK_MAX_STAGES) + SK_CACHE_BLOCKS * EXP_WORDS * 4;
+constexpr int SK_YROW = 40;                      // bf16 per token row of an epilogue warp's y staging (32 + pad)
+constexpr int SK_YSTAGE = 4 * 32 * SK_YROW * 2;  // y staging of the four epilogue warps: 10 KB
+// Alignment slack, barriers, the expand stage records, the cached block
+// records, the y staging.
+constexpr size_t SK_SMEM_FIXED =
+    1024 + 256 + expand_smem_bytes(SK_MAX_STAGES) + SK_CACHE_BLOCKS * EXP_WORDS * 4 + SK_YSTAGE;
 constexpr int SK_MIN_SHARE = 8;                  // k-blocks per CTA at least
 constexpr int SK_MAX_PARTIALS = 8;               // contributors per tile besides its owner, at most
 constexpr int SK_GROUP_ROWS = 256;               // token rows of a group: two accumulators fit in tensor memory
@@ -72,6 +76,7 @@ struct SkArgs {
   int n_slices, slice_end[MLORA_MAX_SLICES];
   size_t tw_slice;  // bf16 elements of one slice's window buffer
   int n_ad;
+  int vec_y;  // N % 8 == 0 and y 16-byte aligned: 16-byte stores of 8 outputs
   uint32_t test_flag_wait_ns;  // nonzero: owners poll never-set flags for this long (a test of the timeout path)
   uint16_t *y;
   const uint16_t *tw;  // token windows of the expand blocks, rows in the 32-byte-swizzled order
@@ -131,6 +136,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   // The plan's expand block records, copied once per CTA (verify mode): every
   // owned unit scans them, so the scans read shared memory, not L2.
   int32_t *blk_cache = reinterpret_cast<int32_t *>(ring + (size_t)S * stage_bytes + expand_smem_bytes(S) + 256);
+  // Per epilogue warp, its 32 W rows x 32 token columns of y in bf16, token-major.
+  uint16_t *ystage = reinterpret_cast<uint16_t *>(blk_cache + SK_CACHE_BLOCKS * EXP_WORDS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -412,6 +419,36 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         if (F8) {
           wsn = n < args.N ? __ldg(args.w_scale + n) : 0.f;
           myxs = myc < args.M ? __ldg(args.x_scale + myc) : 0.f;
+        }
+        if (args.vec_y) {
+          // Through shared memory: lane l writes its W row's 32 outputs as
+          // column l of the warp's token-major block, then owns token
+          // column l and stores its 32 outputs (this warp's 32 W rows) as
+          // four 16-byte pieces.  The rows are padded to 80 bytes, so
+          // neither side has bank conflicts.
+          uint16_t *sy = ystage + (size_t)(quad * 32) * SK_YROW;
+#pragma unroll
+          for (int j = 0; j < SK_CHUNK; ++j) {
+            const float xs = F8 ? __shfl_sync(0xffffffffu, myxs, j) : 1.f;
+            sy[j * SK_YROW + lane] = float_to_bf16_bits(F8 ? v[j] * wsn * xs : v[j]);
+          }
+          __syncwarp();
+          const int nb = t * SK_BN + quad * 32;  // first W row of this warp
+          if (cb + lane < c_end && myrow >= 0) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(sy + lane * SK_YROW);
+            uint16_t *dst = args.y + (size_t)myrow * args.N + nb;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (nb + 8 * q + 8 <= args.N) {
+                reinterpret_cast<uint4 *>(dst)[q] = src[q];
+              } else {
+                for (int e = 0; e < 8; ++e)
+                  if (nb + 8 * q + e < args.N) dst[8 * q + e] = sy[lane * SK_YROW + 8 * q + e];
+              }
+            }
+          }
+          __syncwarp();  // the block is rewritten by the next chunk
+          return;
         }
 #pragma unroll
         for (int j = 0; j < SK_CHUNK; ++j) {
@@ -745,6 +782,7 @@ cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partia
   a.test_flag_wait_ns = g.test_flag_wait_ns;
   a.n_ad = g.n_ad;
   a.y = g.y;
+  a.vec_y = (g.N % 8 == 0 && (reinterpret_cast<uintptr_t>(g.y) & 15) == 0) ? 1 : 0;
   a.tw = g.tw;
   a.plan = g.plan;
   a.status = g.status;
@@ -784,6 +822,7 @@ cudaError_t launch_gemm_sk_f8(const F8Launch &g, const SkShape &sh, float *parti
   a.n_slices = 1;
   for (int i = 0; i < MLORA_MAX_SLICES; ++i) a.slice_end[i] = g.N;
   a.y = g.y;
+  a.vec_y = (g.N % 8 == 0 && (reinterpret_cast<uintptr_t>(g.y) & 15) == 0) ? 1 : 0;
   a.status = g.status;
   a.partials = partials;
   a.flags = flags;
