@@ -425,6 +425,8 @@ __device__ __forceinline__ void cluster_reduce_rows_c(int C, const uint32_t *pee
   }
 }
 
+constexpr int Y_ROW = 40;  // bf16 per token row of an epilogue warp's y staging (32 + pad: no bank conflicts)
+
 // Four bf16 outputs y[row, n .. n + 3] (columns past N dropped).
 __device__ __forceinline__ void store_bf16x4(uint16_t *y, int N, size_t row, int n, float4 v) {
   uint16_t *dst = y + row * (size_t)N + n;
@@ -724,12 +726,39 @@ __global__ void __launch_bounds__(GEMM_THREADS, 2)
     if (epi && have_acc) {
       const int n = n_tile * BLOCK_N + quad * 32 + lane;
       if (!verify) {
+        // With N % 8 == 0 and y 16-byte aligned, each warp's 32 W rows x 32
+        // token columns go through a padded token-major block in the idle
+        // stage ring, and lane j stores token column j's 32 outputs as four
+        // 16-byte pieces; otherwise one two-byte store per output.
+        const bool vec = (args.N & 7) == 0 && (reinterpret_cast<uintptr_t>(args.y) & 15) == 0;
+        uint16_t *sy = reinterpret_cast<uint16_t *>(sp.stage0) + (size_t)quad * 32 * Y_ROW;
+        const int nb = n_tile * BLOCK_N + quad * 32;
         for (int ch = 0; ch < nchunks; ++ch) {
           uint32_t r[32];
           tmem_ld_acc_x32(taddr + ch * CHUNK, r);
           // Lane j holds the output row of column ch * 32 + j.
           const int myc = ch * CHUNK + lane;
           const int myrow = myc < mcount ? (int)out_row(myc) : -1;
+          if (vec) {
+#pragma unroll
+            for (int j = 0; j < CHUNK; ++j) sy[j * Y_ROW + lane] = float_to_bf16_bits(__uint_as_float(r[j]));
+            __syncwarp();
+            if (myrow >= 0) {
+              const uint4 *src = reinterpret_cast<const uint4 *>(sy + lane * Y_ROW);
+              uint16_t *dst = args.y + (size_t)myrow * args.N + nb;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                if (nb + 8 * q + 8 <= args.N) {
+                  reinterpret_cast<uint4 *>(dst)[q] = src[q];
+                } else {
+                  for (int e = 0; e < 8; ++e)
+                    if (nb + 8 * q + e < args.N) dst[8 * q + e] = sy[lane * Y_ROW + 8 * q + e];
+                }
+              }
+            }
+            __syncwarp();  // the block is rewritten by the next chunk
+            continue;
+          }
 #pragma unroll
           for (int j = 0; j < CHUNK; ++j) {
             const int col = ch * CHUNK + j;

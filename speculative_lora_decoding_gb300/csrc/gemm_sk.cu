@@ -58,7 +58,8 @@ constexpr size_t SK_SMEM_LIMIT = 220 * 1024;     // leaves room for a co-residen
 constexpr int SK_MAX_STAGES = 8;
 constexpr int SK_CACHE_BLOCKS = 256;             // expand block records kept in shared memory (8 KB)
 constexpr int SK_YROW = 40;                      // bf16 per token row of an epilogue warp's y staging (32 + pad)
-constexpr int SK_YSTAGE = 4 * 32 * SK_YROW * 2;  // y staging of the four epilogue warps: 10 KB
+constexpr int SK_YSTAGE = 4 * 32 * SK_YROW * 2;  // staging of the four epilogue warps (y, partial sums): 10 KB
+static_assert(4 * 16 * 36 * 4 <= SK_YSTAGE, "16 columns of a warp's fp32 partial sums fit its staging block");
 // Alignment slack, barriers, the expand stage records, the cached block
 // records, the y staging.
 constexpr size_t SK_SMEM_FIXED =
@@ -495,15 +496,29 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         const int nred = r_last - first + 1;
         const bool publish = !reducer || nred > 1;
         if (publish) {
+          // Through the warp's staging block, 16 columns at a time: each
+          // column's 32 rows (this warp's) as 36 floats, so that lane l
+          // stores rows 4 (l % 8) .. + 3 of column l / 8 + 4 q as one
+          // 16-byte piece (no bank conflicts on either side).
           float *part = part_of(cta);
+          float *sp = reinterpret_cast<float *>(ystage) + (size_t)quad * 16 * (32 + 4);
           for (int ch = 0; ch < nchunks; ++ch) {
             uint32_t r[32];
             tmem_ld_x32(acc + ch * SK_CHUNK, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < SK_CHUNK; ++j) {
-              const int col = ch * SK_CHUNK + j;
-              if (col < gcols) part[(size_t)col * SK_BN + row] = __uint_as_float(r[j]);
+            for (int h = 0; h < SK_CHUNK; h += 16) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) sp[j * 36 + lane] = __uint_as_float(r[h + j]);
+              __syncwarp();
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int jc = (lane >> 3) + 4 * q, col = ch * SK_CHUNK + h + jc;
+                if (col < gcols)
+                  *reinterpret_cast<float4 *>(part + (size_t)col * SK_BN + quad * 32 + 4 * (lane & 7)) =
+                      *reinterpret_cast<const float4 *>(sp + jc * 36 + 4 * (lane & 7));
+              }
+              __syncwarp();  // the block is rewritten by the next half
             }
           }
         }
@@ -592,10 +607,18 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                   for (int j = 0; j < SK_CHUNK; ++j) v[j] += __uint_as_float(r[j]);
                   continue;
                 }
+                // Sixteen independent loads, then their sums.  Columns past
+                // q1 read other bytes of the ring (inside it: qn <=
+                // round_cols) and are never stored.
                 const float *pp = ringf + ((size_t)(o++) * qn + (cb - q0)) * SK_BN + row;
 #pragma unroll
-                for (int j = 0; j < SK_CHUNK; ++j)
-                  if (cb + j < q1) v[j] += pp[j * SK_BN];
+                for (int h = 0; h < SK_CHUNK; h += 16) {
+                  float t[16];
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) t[j] = pp[(h + j) * SK_BN];
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) v[h + j] += t[j];
+                }
               }
               store_y(cb, q1, v);
             }
