@@ -65,6 +65,7 @@ LAYER_RUNS = {
 }
 HEADLINE = "32b-k4"
 ACCEPT_SWEEP_K = (1, 2, 3, 4)
+ACCEPT_CALLS = 8  # accept calls per graph in the sweep's back-to-back timing
 METRIC = "multi-LoRA decode-step verified tokens/s (k draft passes + 1 verify pass of one block's 7 projections + accept)"
 UNIT = "tokens/s"
 L2_BYTES = 126 * 1024 * 1024
@@ -571,6 +572,16 @@ def time_replays(torch, graph, stream, reps, flush=None):
     return float(np.median([a.elapsed_time(b) for a, b in evs]))
 
 
+def time_ops_graph(torch, ops, stream, reps, flush=None):
+    """ms for the ops in stream order, from replays of one graph of them (the
+    launches overlap at their boundaries as they do inside the step)."""
+    g = graph_of(torch, lambda: [op[3]() for op in ops], stream)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    return time_replays(torch, g, stream, reps, flush)
+
+
 def per_op_durations(torch, ops, stream, reps):
     """Median duration of every op, from CUDA events on the launching stream
     between consecutive ops inside one captured graph (external events),
@@ -612,6 +623,9 @@ def measure_layer(torch, ml, wl, stream, side, steps, peaks, flush):
     if wl.ws.status() != 0 or wl.ws_draft.status() != 0:
         raise RuntimeError(f"{wl.name}: device status bits raised during the timed region")
     op_ms = per_op_durations(torch, wl.ops(with_base=True), stream, max(10, min(steps, 100)))
+    # The k draft passes alone, from their own graph.
+    ms_draft = time_ops_graph(torch, [op for op in wl.ops() if op[1] == "draft"], stream, max(10, min(steps, 100)),
+                              flush if use_flush else None)
 
     cfg, k = wl.cfg, wl.k
     active = sorted(set(int(a) for a in wl.idx_v if a >= 0))
@@ -657,13 +671,20 @@ def measure_layer(torch, ml, wl, stream, side, steps, peaks, flush):
     dom = max(kernels, key=lambda n: kernels[n]["draft_ms"] + kernels[n]["verify_ms"])
     d = kernels[dom]
     if d["draft_launches"]:
-        achieved = d["draft_bytes"] / (d["draft_ms"] * 1e-3) / 1e9
+        # Every draft launch on this kernel: its time is the draft passes'
+        # graph time; otherwise the per-op times of its launches.
+        all_draft = d["draft_launches"] == k * len(wl.proj)
+        d_ms = ms_draft if all_draft else d["draft_ms"]
+        achieved = d["draft_bytes"] / (d_ms * 1e-3) / 1e9
         traffic, note = profiled_traffic(dom, wl.name)
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
                 "traffic": traffic, "kernel": f"{dom} (draft passes: {', '.join(d['draft_ops'])}; M={wl.Md})",
                 "peak_kind": f"{peak_kind} hbm_gbs",
                 "algorithmic_bytes_per_launch": d["draft_bytes"] / d["draft_launches"],
-                "avg_launch_us": 1e3 * d["draft_ms"] / d["draft_launches"], "traffic_source": note}
+                "avg_launch_us": 1e3 * d_ms / d["draft_launches"], "traffic_source": note,
+                "timing": ("events around replays of a graph of the k draft passes (all of this kernel's draft "
+                           "launches), divided by its launches" if all_draft else
+                           "events between the ops inside one step graph, summed over this kernel's draft launches")}
     else:
         achieved = d["verify_flops"] / (d["verify_ms"] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_sus, "unit": "TFLOP/s", "frac": achieved / bf16_sus,
@@ -684,9 +705,11 @@ def measure_layer(torch, ml, wl, stream, side, steps, peaks, flush):
         others[n] = o
     roof["other_kernels"] = others
     modes = {
-        "draft_pass": {"passes": k, "us_per_pass": 1e3 * draft_t / k, "tokens_per_s": wl.Md * k / (draft_t * 1e-3),
-                       "GBps": draft_b / (draft_t * 1e-3) / 1e9,
-                       "frac_hbm": draft_b / (draft_t * 1e-3) / 1e9 / hbm_gbs},
+        "draft_pass": {"passes": k, "us_per_pass": 1e3 * ms_draft / k, "tokens_per_s": wl.Md * k / (ms_draft * 1e-3),
+                       "GBps": draft_b / (ms_draft * 1e-3) / 1e9,
+                       "frac_hbm": draft_b / (ms_draft * 1e-3) / 1e9 / hbm_gbs,
+                       "us_per_pass_per_op_events": 1e3 * draft_t / k,
+                       "timing": "events around replays of a graph of the k draft passes"},
         "verify_pass": {"us": 1e3 * verify_t, "tokens_per_s": wl.Mv / (verify_t * 1e-3),
                         "GBps": verify_b / (verify_t * 1e-3) / 1e9, "frac_hbm": verify_b / (verify_t * 1e-3) / 1e9 / hbm_gbs,
                         "TFLOPs": verify_f / (verify_t * 1e-3) / 1e12,
@@ -710,29 +733,47 @@ def measure_layer(torch, ml, wl, stream, side, steps, peaks, flush):
 
 
 def measure_accept_sweep(torch, ml, device, stream, reps, peaks, flush, oracle_seconds):
-    """The accept step alone at batch 256, vocabulary 128256, k = 1..4."""
+    """The accept step alone at batch 256, vocabulary 128256, k = 1..4:
+    back-to-back calls alternating between two input sets, each larger than
+    L2 (so no call finds the previous one's rows in L2), from CUDA events
+    around replays of a graph of ACCEPT_CALLS calls; and one call alone after
+    an L2 flush (launch latency included) for reference."""
     from oracle import accept as OA
     hbm_gbs = peaks[0]
     cfg = WL.ACCEPT_SWEEP
     out = {"workload": f"{cfg.name}: B={cfg.batch} V={cfg.vocab} k=1..4, target logits N(0, 2^2), draft logits + "
-                       f"N(0, {WL.ACCEPT_SIGMA}^2)", "l2": "L2 flushed before each timed call", "k": {}}
+                       f"N(0, {WL.ACCEPT_SIGMA}^2)",
+           "l2": "inputs larger than L2: two input sets of p and q (394-1182 MB each) alternate between back-to-back "
+                 "calls; 'us_single' is one call after an L2 flush", "k": {}}
     for k in ACCEPT_SWEEP_K:
-        p, q, tok, u = accept_inputs_device(torch, cfg.vocab, cfg.batch, k, device, seed=17)
+        sets = []
+        for seed in (17, 18):
+            p, q, tok, u = accept_inputs_device(torch, cfg.vocab, cfg.batch, k, device, seed=seed)
+            sets.append(dict(p=p, q=q, tok=tok, u=u, out_tok=torch.empty((cfg.batch, k + 1), dtype=torch.int32,
+                                                                         device=device),
+                             accepted=torch.empty((cfg.batch,), dtype=torch.int32, device=device)))
         ws = ml.Workspace(ml.accept_workspace_bytes(cfg.batch, k, cfg.vocab), device=device)
-        out_tok = torch.empty((cfg.batch, k + 1), dtype=torch.int32, device=device)
-        accepted = torch.empty((cfg.batch,), dtype=torch.int32, device=device)
-        call = lambda: ml.verify_accept(p, q, tok, u, ws=ws, out_tok=out_tok, accepted=accepted)  # noqa: E731
+
+        def call(i):
+            st = sets[i % 2]
+            ml.verify_accept(st["p"], st["q"], st["tok"], st["u"], ws=ws, out_tok=st["out_tok"],
+                             accepted=st["accepted"])
         with torch.cuda.stream(stream):
-            for _ in range(3):
-                call()
+            for i in range(4):
+                call(i)
         stream.synchronize()
-        g = graph_of(torch, call, stream)
-        ms = time_replays(torch, g, stream, reps, flush)
+        g1 = graph_of(torch, lambda: call(0), stream)
+        ms_single = time_replays(torch, g1, stream, reps, flush)
+        gn = graph_of(torch, lambda: [call(i) for i in range(ACCEPT_CALLS)], stream)
+        with torch.cuda.stream(stream):
+            gn.replay()
+        ms = time_replays(torch, gn, stream, max(3, reps // 4)) / ACCEPT_CALLS
         if ws.status() != 0:
             raise RuntimeError("device status bits raised in the accept sweep")
-        acc = accepted.cpu().numpy()
-        b = accept_bytes(cfg.batch, cfg.vocab, acc, k)
-        host = tuple(t[:4].cpu().numpy() for t in (p, q, tok, u))
+        accs = [st["accepted"].cpu().numpy() for st in sets]
+        b = 0.5 * sum(accept_bytes(cfg.batch, cfg.vocab, a, k) for a in accs)
+        st = sets[0]
+        host = tuple(t[:4].cpu().numpy() for t in (st["p"], st["q"], st["tok"], st["u"]))
         OA.verify_accept(*host)
         secs, rows = 0.0, 0
         while secs < oracle_seconds:
@@ -740,12 +781,12 @@ def measure_accept_sweep(torch, ml, device, stream, reps, peaks, flush, oracle_s
             OA.verify_accept(*host)
             secs += time.perf_counter() - t0
             rows += 4
-        out["k"][str(k)] = {"us": 1e3 * ms, "rows_per_s": cfg.batch / (ms * 1e-3), "GBps": b / (ms * 1e-3) / 1e9,
-                            "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm_gbs, "algorithmic_bytes": b,
-                            "mean_accepted": float(acc.mean()),
+        out["k"][str(k)] = {"us": 1e3 * ms, "us_single": 1e3 * ms_single, "rows_per_s": cfg.batch / (ms * 1e-3),
+                            "GBps": b / (ms * 1e-3) / 1e9, "frac_hbm": b / (ms * 1e-3) / 1e9 / hbm_gbs,
+                            "algorithmic_bytes": int(b), "mean_accepted": float(np.mean([a.mean() for a in accs])),
                             "oracle": {"rows_per_s": rows / secs, "cores": cpu_cores(),
                                        "sample": f"{rows} requests, float64/integer numpy"}}
-        del p, q, tok, u, ws, g
+        del sets, ws, g1, gn
         torch.cuda.empty_cache()
     return out
 
@@ -815,11 +856,10 @@ def measure_fp8_draft(torch, ml, wl, stream, side, steps, peaks, flush, bf16_ste
             graph.replay()
         torch.cuda.synchronize()
         ms = time_replays(torch, graph, stream, steps)
-        op_ms = per_op_durations(torch, wl.ops(), stream, max(10, min(steps, 50)))
+        t_draft = time_ops_graph(torch, [op for op in wl.ops() if op[1] == "draft"], stream, max(10, min(steps, 50)))
         if wl.ws_fp8.status() != 0 or wl.ws.status() != 0:
             raise RuntimeError("device status bits raised in the FP8 draft measurement")
         k = wl.k
-        t_draft = sum(op_ms[f"draft{d}.{P['name']}"] for d in range(k) for P in wl.proj)
         nbytes = k * sum(P["N"] * P["K"] + 4 * wl.Md * P["K"] + 2 * wl.Md * P["N"] for P in wl.proj)
         quality = {}
         for P in wl.proj:
