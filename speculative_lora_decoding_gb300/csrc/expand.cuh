@@ -165,10 +165,46 @@ __device__ __forceinline__ bool expand_produce(const int32_t *blocks, int blo, i
   return ok;
 }
 
+// The MMAs of one expand stage whose barrier has completed (all 32 lanes of
+// the MMA warp): zero the B columns past each block's rank columns, then
+// lane 0 issues one MMA per block (two past 256 window rows) into the
+// accumulator columns of its window and commits the stage to `empty_bar`.
+// acc is the tensor-memory address of the accumulator's column 0 (the CTA's
+// first token column).
+__device__ __forceinline__ void expand_stage_mma(uint8_t *st, const ExpandStage &m, uint32_t acc, uint64_t *empty_bar,
+                                                 int lane) {
+  const int cnt = m.count;
+  bool zeroed = false;
+  for (int c = 0; c < cnt; ++c) {
+    const int cols = m.blk[c].w >> 16;
+    if (cols < 16) {
+      zero_tail_columns_sw32(st + m.blk[c].x, cols, lane);
+      zeroed = true;
+    }
+  }
+  if (zeroed) fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tc_fence_after_sync();
+    const uint32_t base = smem_addr(st);
+    for (int c = 0; c < cnt; ++c) {
+      const int4 b = m.blk[c];
+      const int rows = b.w & 0xFFFF;
+      const uint64_t bd = smem_desc_kmajor_sw32(base + (uint32_t)b.x);
+      for (int p = 0; p < rows; p += 256) {
+        const int nn = min(256, rows - p);
+        mma_bf16_ss(acc + (uint32_t)(b.z + p), bd, smem_desc_kmajor_sw32(base + (uint32_t)(b.y + p * 32)),
+                    idesc_bf16_f32(128, nn), 1u);
+      }
+    }
+    mma_commit(empty_bar);
+  }
+  __syncwarp();
+}
+
 // MMA side, called by all 32 lanes of the MMA warp after the producer has
 // issued at least one expand stage: run stages until the one flagged `last`.
-// acc is the tensor-memory address of the accumulator's column 0 (the CTA's
-// first token column).  Returns false if a wait gave up.
+// Returns false if a wait gave up.
 __device__ __forceinline__ bool expand_consume(uint8_t *ring, int stage_bytes, int S, uint64_t *full,
                                                uint64_t *empty, const ExpandStage *meta, uint32_t acc, int &stage,
                                                uint32_t &phase, volatile int *abort, int lane) {
@@ -180,35 +216,8 @@ __device__ __forceinline__ bool expand_consume(uint8_t *ring, int stage_bytes, i
     if (!ok) break;
     tc_fence_after_sync();
     const ExpandStage &m = meta[stage];
-    const int cnt = m.count;
     const bool last = m.last != 0;
-    uint8_t *st = ring + (size_t)stage * stage_bytes;
-    bool zeroed = false;
-    for (int c = 0; c < cnt; ++c) {
-      const int cols = m.blk[c].w >> 16;
-      if (cols < 16) {
-        zero_tail_columns_sw32(st + m.blk[c].x, cols, lane);
-        zeroed = true;
-      }
-    }
-    if (zeroed) fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tc_fence_after_sync();
-      const uint32_t base = smem_addr(st);
-      for (int c = 0; c < cnt; ++c) {
-        const int4 b = m.blk[c];
-        const int rows = b.w & 0xFFFF;
-        const uint64_t bd = smem_desc_kmajor_sw32(base + (uint32_t)b.x);
-        for (int p = 0; p < rows; p += 256) {
-          const int nn = min(256, rows - p);
-          mma_bf16_ss(acc + (uint32_t)(b.z + p), bd, smem_desc_kmajor_sw32(base + (uint32_t)(b.y + p * 32)),
-                      idesc_bf16_f32(128, nn), 1u);
-        }
-      }
-      mma_commit(&empty[stage]);
-    }
-    __syncwarp();
+    expand_stage_mma(ring + (size_t)stage * stage_bytes, m, acc, &empty[stage], lane);
     if (++stage == S) {
       stage = 0;
       phase ^= 1u;

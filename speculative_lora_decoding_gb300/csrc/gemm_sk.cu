@@ -109,13 +109,145 @@ __device__ __forceinline__ int sk_slice_of(const SkArgs &a, int n0) {
   return s;
 }
 
+// The expand operands' tensor maps: B_stack [n_ad][N][r_max] as a 2-D view
+// [n_ad N, r_max] (one 16-rank block of 128 rows per box), and as 3-D maps
+// {r_max, N, n_ad} whose boxes take the same block of 1, 2, 4 or 8
+// consecutive adapters at once.
+struct SkBMaps {
+  CUtensorMap b2;
+  CUtensorMap b3[4];
+};
+
+// A CTA's expand plan, built once from the cached block records: the blocks
+// whose windows meet the CTA's token group, in plan order, E[k] = {adapter,
+// j0 | rank columns << 8, first window row, first accumulator column | rows
+// << 16}, and their packing into ring stages, D[s] = {first block, blocks,
+// window bytes, last}.  Only the W tile (the B rows) changes from one owned
+// unit to the next, so each unit replays the plan.  Built in place over the
+// cached records (entry k, 16 bytes, never overtakes record k, 32 bytes).
+// Returns the stage count (at least 1, an empty stage when no block meets
+// the group: the MMA warp runs an owned unit's stages until `last`).
+__device__ __forceinline__ int sk_expand_plan(int32_t *cache, int ns, int m0, int mcols, int n_ad, long long tw_rows,
+                                              int stage_bytes, int lane, uint32_t *status) {
+  int4 *E = reinterpret_cast<int4 *>(cache);
+  int4 *D = reinterpret_cast<int4 *>(cache) + SK_CACHE_BLOCKS;
+  int ne = 0;
+  for (int c0 = 0; c0 < ns; c0 += 32) {
+    int4 ent = make_int4(0, 0, 0, 0);
+    bool keep = false;
+    if (c0 + lane < ns) {
+      const int4 e0 = reinterpret_cast<const int4 *>(cache)[(size_t)(c0 + lane) * 2];
+      const int4 e1 = reinterpret_cast<const int4 *>(cache)[(size_t)(c0 + lane) * 2 + 1];
+      const int w0 = e1.x, W = e1.y;
+      const bool valid = (unsigned)e0.x < (unsigned)n_ad && (e0.y & 15) == 0 && (unsigned)e0.y < 64u &&
+                         e0.z >= 1 && e0.z <= 16 && e0.w >= 0 && w0 >= 0 && (w0 & 15) == 0 && W >= 0 &&
+                         (W & 15) == 0 && (long long)e0.w + W <= tw_rows;
+      if (!valid) raise_status(status, MLORA_DEV_BAD_PLAN);
+      const int cs = max(w0, m0), ce = min(w0 + W, m0 + mcols);
+      keep = valid && ce > cs;
+      if (keep) ent = make_int4(e0.x, e0.y | (e0.z << 8), e0.w + (cs - w0), (cs - m0) | ((ce - cs) << 16));
+    }
+    const uint32_t kb = __ballot_sync(0xffffffffu, keep);
+    __syncwarp();  // every lane has read its record before any entry is written
+    if (keep) E[ne + __popc(kb & ((1u << lane) - 1u))] = ent;
+    ne += __popc(kb);
+    __syncwarp();
+  }
+  int nst = 0;
+  if (lane == 0) {
+    for (int k = 0; k < ne;) {
+      int cnt = 0, tbytes = 0;
+      while (k + cnt < ne && cnt < EXP_MAX_PER_STAGE) {
+        const int rows = E[k + cnt].w >> 16;  // <= 286: a block and its window always fit a stage
+        if ((cnt + 1) * EXP_B_TILE + tbytes + rows * 32 > stage_bytes) break;
+        tbytes += rows * 32;
+        ++cnt;
+      }
+      D[nst++] = make_int4(k, cnt, tbytes, 0);
+      k += cnt;
+    }
+    if (nst == 0) D[nst++] = make_int4(0, 0, 0, 0);
+    D[nst - 1].w = 1;
+  }
+  nst = __shfl_sync(0xffffffffu, nst, 0);
+  __syncwarp();
+  return nst;
+}
+
+// Stages [s_begin, s_end) of one owned unit's expand from the plan (producer
+// warp, all lanes):
+// per stage, lane c describes block c in the stage record, lane 0 arms the
+// barrier, then each lane that starts a run of consecutive adapters (same
+// 16-rank block) loads their B tiles with 3-D boxes, and each lane that
+// starts a run of back-to-back windows copies them with one bulk copy.
+__device__ __forceinline__ bool sk_expand_issue(const int32_t *cache, int s_begin, int s_end, const SkBMaps &bm, int n0,
+                                                const uint16_t *tw, uint8_t *ring, int stage_bytes, int S,
+                                                uint64_t *full, uint64_t *empty, ExpandStage *meta, int &stage,
+                                                uint32_t &phase, int &issued, volatile int *abort, uint64_t pol,
+                                                int lane) {
+  const int4 *E = reinterpret_cast<const int4 *>(cache);
+  const int4 *D = reinterpret_cast<const int4 *>(cache) + SK_CACHE_BLOCKS;
+  for (int s = s_begin; s < s_end; ++s) {
+    const int4 dsc = D[s];
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_bounded(&empty[stage], phase ^ 1u, abort);
+    if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) return false;
+    uint8_t *st = ring + (size_t)stage * stage_bytes;
+    ExpandStage &m = meta[stage];
+    const int cnt = dsc.y;
+    const bool mine = lane < cnt;
+    const int4 e = mine ? E[dsc.x + lane] : make_int4(0, 0, 0, 0);
+    const int rows = e.w >> 16;
+    int incl = rows * 32;  // window bytes of blocks 0..lane
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int toff = cnt * EXP_B_TILE + incl - rows * 32;
+    if (mine) m.blk[lane] = make_int4(lane * EXP_B_TILE, toff, e.w & 0xFFFF, rows | (((e.y >> 8) & 0xFF) << 16));
+    if (lane == 0) {
+      m.count = cnt;
+      m.last = dsc.w;
+    }
+    __syncwarp();
+    // The arrival releases the record; the copies complete the phase.
+    if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)(cnt * EXP_B_TILE + dsc.z));
+    __syncwarp();
+    const int pa = __shfl_up_sync(0xffffffffu, e.x, 1), py = __shfl_up_sync(0xffffffffu, e.y, 1);
+    const int pz = __shfl_up_sync(0xffffffffu, e.z, 1), pr = __shfl_up_sync(0xffffffffu, rows, 1);
+    const bool b_start = mine && (lane == 0 || e.x != pa + 1 || (e.y & 0xFF) != (py & 0xFF));
+    const bool w_start = mine && (lane == 0 || e.z != pz + pr);
+    const uint32_t bs = __ballot_sync(0xffffffffu, b_start) | (cnt < 32 ? (1u << cnt) : 0u);
+    const uint32_t ws = __ballot_sync(0xffffffffu, w_start) | (cnt < 32 ? (1u << cnt) : 0u);
+    const uint32_t above = lane < 31 ? ~((2u << lane) - 1u) : 0u;  // lanes after this one
+    if (b_start) {
+      const int len = __ffs(bs & above) - 1 - lane;
+      for (int o = 0; o < len;) {
+        const int lg = len - o >= 8 ? 3 : len - o >= 4 ? 2 : len - o >= 2 ? 1 : 0;
+        tma_load_3d(st + (lane + o) * EXP_B_TILE, &bm.b3[lg], &full[stage], e.y & 0xFF, n0, e.x + o, pol);
+        o += 1 << lg;
+      }
+    }
+    const int wend = __ffs(ws & above) - 1;  // first lane after this one's window run
+    const int wlast = __shfl_sync(0xffffffffu, incl, max(0, (w_start ? wend : lane + 1) - 1));
+    if (w_start) bulk_load(st + toff, tw + (size_t)e.z * 16, (uint32_t)(wlast - (incl - rows * 32)), &full[stage]);
+    ++issued;
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+  return true;
+}
+
 // F8: W and x are E4M3 codes (draft mode only): 128 values per 128-byte
 // k-block row, kind::f8f6f4 MMAs, and the epilogue applies the row scales,
 // y = bf16(acc * w_scale[n] * x_scale[m]).
 template <bool F8>
 __global__ void __launch_bounds__(SK_THREADS, 1)
     gemm_sk_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
-                   const __grid_constant__ CUtensorMap tmap_b, const SkArgs args) {
+                   const __grid_constant__ SkBMaps bm, const SkArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *ring = align_smem_1024(smem_raw);
   const int S = args.stages;
@@ -172,7 +304,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_w);
     tma_prefetch_desc(&tmap_x);
-    if (tc) tma_prefetch_desc(&tmap_b);
+    if (tc) {
+      tma_prefetch_desc(&bm.b2);
+      for (int q = 0; q < 4; ++q) tma_prefetch_desc(&bm.b3[q]);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 2 * args.cols);
@@ -193,7 +328,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
     const uint32_t tx = (uint32_t)stage_bytes;
-    int stage = 0, issued = 0, i = 0, early = 0, ns = -1;
+    int stage = 0, issued = 0, i = 0, early = 0, ns = -1, nst = 0;
     bool cached = false;
     uint32_t phase = 0;
     bool ok = true;
@@ -244,33 +379,44 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     for (int g = g0; g < g1 && ok;) {
       const int u = g / KB, kb0 = g - u * KB, kb1 = min(KB, g1 - u * KB);
       const int t = u;
-      // The expand operands of an owned unit (verify mode) go into the ring
-      // before the unit's last S k-blocks, so that they land while those
-      // stream instead of after the whole unit.
-      const int ins = (tc && kb0 == 0) ? max(kb0, kb1 - 1 - S) : -1;
-      const int split = ins >= 0 ? ins + 1 : kb1;
-      if (lane == 0) issue_kblocks(u, kb0, split);
-      sync_state();
-      if (ok && ins >= 0) {
-        if (!waited) {
-          grid_dependency_wait();  // the token windows come from the shrink kernel just before
-          waited = true;
+      const uint16_t *tws = args.tw + (size_t)sk_slice_of(args, t * SK_BN) * args.tw_slice;
+      if (!(tc && kb0 == 0)) {
+        if (lane == 0) issue_kblocks(u, kb0, kb1);
+        sync_state();
+      } else {
+        // An owned unit (verify mode): the expand operands go into the ring
+        // before the unit's last S k-blocks, so that they land while those
+        // stream; the first owned unit waits there for the kernels that wrote
+        // the plan and the windows, while its first k-blocks stream.
+        const int ins = max(kb0, kb1 - 1 - S);
+        const int split = ins + 1;
+        if (lane == 0) issue_kblocks(u, kb0, split);
+        sync_state();
+        if (ok) {
+          if (!waited) {
+            grid_dependency_wait();  // the token windows come from the shrink kernel just before
+            waited = true;
+          }
+          if (ns < 0) ns = args.plan[L.hdr + 4];
+          if (ns > 0 && !cached && ns <= SK_CACHE_BLOCKS) {
+            const int4 *src = reinterpret_cast<const int4 *>(args.plan + L.slices);
+            for (int q = lane; q < ns * (EXP_WORDS / 4); q += 32) reinterpret_cast<int4 *>(blk_cache)[q] = src[q];
+            __syncwarp();
+            nst = sk_expand_plan(blk_cache, ns, m0, args.Mb, args.n_ad, (long long)(args.tw_slice / 16),
+                                 stage_bytes, lane, args.status);
+            cached = true;
+          }
+          if (ns > 0 && cached)
+            ok = sk_expand_issue(blk_cache, 0, nst, bm, t * SK_BN, tws, ring, stage_bytes, S, full, empty, meta,
+                                 stage, phase, issued, ab, pol_w, lane);
+          else if (ns > 0)
+            ok = expand_produce(args.plan + L.slices, 0, ns, m0, args.Mb, t * SK_BN, args.N, &bm.b2, tws, ring,
+                                stage_bytes, S, full, empty, meta, chunk, stage, phase, issued, ab, pol_w, lane,
+                                args.n_ad, (long long)(args.tw_slice / 16), args.status);
         }
-        if (ns < 0) ns = args.plan[L.hdr + 4];
-        if (ns > 0 && !cached && ns <= SK_CACHE_BLOCKS) {
-          const int4 *src = reinterpret_cast<const int4 *>(args.plan + L.slices);
-          for (int q = lane; q < ns * (EXP_WORDS / 4); q += 32) reinterpret_cast<int4 *>(blk_cache)[q] = src[q];
-          __syncwarp();
-          cached = true;
-        }
-        if (ns > 0)
-          ok = expand_produce(cached ? blk_cache : args.plan + L.slices, 0, ns, m0, args.Mb, t * SK_BN, args.N, &tmap_b,
-                              args.tw + (size_t)sk_slice_of(args, t * SK_BN) * args.tw_slice, ring, stage_bytes, S,
-                              full, empty, meta, chunk, stage, phase, issued, ab, pol_w, lane, args.n_ad,
-                              (long long)(args.tw_slice / 16), args.status);
+        if (lane == 0 && ok) issue_kblocks(u, split, kb1);
+        sync_state();
       }
-      if (lane == 0 && ok) issue_kblocks(u, split, kb1);
-      sync_state();
       g = u * KB + kb1;
     }
     if (lane == 0) {
@@ -766,19 +912,42 @@ static bool sk_map(CUtensorMap *map, const void *base, long long rows, int cols,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// B_stack [n_ad][N][r_max] bf16 as a 3-D map {r_max, N, n_ad}: boxes of 16
+// ranks x 128 rows x `depth` consecutive adapters, 32-byte swizzle (each
+// adapter's 128 x 16 tile lands as with the 2-D view); out of range reads 0.
+static bool sk_map_b3(CUtensorMap *map, const void *base, int n_ad, int N, int r_max, int depth) {
+  SkEncodeFn fn = sk_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)r_max, (cuuint64_t)N, (cuuint64_t)n_ad};
+  cuuint64_t strides[2] = {(cuuint64_t)r_max * 2, (cuuint64_t)N * r_max * 2};
+  cuuint32_t box[3] = {16, (cuuint32_t)SK_BN, (cuuint32_t)depth};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partials, uint32_t *flags, cudaStream_t s,
                            int *err_code) {
   *err_code = 0;
   if (!sh.ok) return cudaErrorInvalidValue;  // sk_shape set the kernel's attributes when it said ok
-  CUtensorMap tw, tx, tb;
+  CUtensorMap tw, tx;
   if (!sk_map(&tw, g.W, g.N, g.K, SK_BN, SK_BK) || !sk_map(&tx, g.x, g.M, g.K, sh.Mb, SK_BK)) {
     *err_code = 1;
     return cudaErrorInvalidValue;
   }
   const int sorted = (g.mode == MLORA_VERIFY && g.tw != nullptr) ? 1 : 0;
-  tb = tw;
+  SkBMaps bm;
+  bm.b2 = tw;
+  for (int q = 0; q < 4; ++q) bm.b3[q] = tw;
   if (sorted) {
-    if (!sk_map(&tb, g.B_stack, (long long)g.n_ad * g.N, g.r_max, SK_BN, 16)) {
+    bool mapped = sk_map(&bm.b2, g.B_stack, (long long)g.n_ad * g.N, g.r_max, SK_BN, 16);
+    // A run of consecutive adapters never exceeds n_ad: deeper boxes than
+    // that are never used (a copy of the one-adapter map stands in).
+    for (int q = 0; q < 4 && mapped; ++q)
+      mapped = (1 << q) <= g.n_ad ? sk_map_b3(&bm.b3[q], g.B_stack, g.n_ad, g.N, g.r_max, 1 << q)
+                                  : (bm.b3[q] = bm.b3[0], true);
+    if (!mapped) {
       *err_code = 1;
       return cudaErrorInvalidValue;
     }
@@ -813,7 +982,7 @@ cudaError_t launch_gemm_sk(const GemmLaunch &g, const SkShape &sh, float *partia
   a.flags = flags;
   a.w_scale = nullptr;
   a.x_scale = nullptr;
-  cudaError_t e = launch_pdl(gemm_sk_kernel<false>, dim3(sh.P), dim3(SK_THREADS), sh.smem_bytes, s, tw, tx, tb, a);
+  cudaError_t e = launch_pdl(gemm_sk_kernel<false>, dim3(sh.P), dim3(SK_THREADS), sh.smem_bytes, s, tw, tx, bm, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -851,7 +1020,10 @@ cudaError_t launch_gemm_sk_f8(const F8Launch &g, const SkShape &sh, float *parti
   a.flags = flags;
   a.w_scale = g.w_scale;
   a.x_scale = g.x_scale;
-  cudaError_t e = launch_pdl(gemm_sk_kernel<true>, dim3(sh.P), dim3(SK_THREADS), sh.smem_bytes, s, tw, tx, tw, a);
+  SkBMaps bm;  // no expand in the E4M3 draft pass: placeholders
+  bm.b2 = tw;
+  for (int q = 0; q < 4; ++q) bm.b3[q] = tw;
+  cudaError_t e = launch_pdl(gemm_sk_kernel<true>, dim3(sh.P), dim3(SK_THREADS), sh.smem_bytes, s, tw, tx, bm, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
