@@ -64,7 +64,8 @@ __device__ __forceinline__ void zero_tail_columns_sw32(uint8_t *tile, int c0, in
 // Producer side, called by all 32 lanes of the producer warp: issue the
 // expand stages for plan blocks [blo, bhi) of the output tile starting at W
 // row n0, with the windows clipped to token columns [m0, m0 + mcols).  Lane 0
-// waits and issues; every lane keeps the same stage / phase / issued count.
+// packs the stages and issues the copies; every lane waits for each stage's
+// slot and keeps the same stage / phase / issued count.
 // Returns false if a wait gave up.
 // A record out of range (n_ad adapters, tw_rows rows in the window buffer)
 // means the plan was overwritten or made for other sizes: the block is
@@ -93,12 +94,16 @@ __device__ __forceinline__ bool expand_produce(const int32_t *blocks, int blo, i
       chunk[lane] = make_int4(e0.x, e0.y | (e0.z << 8), e0.w + (rows ? cs - w0 : 0), rows ? ((cs - m0) | (rows << 16)) : 0);
     }
     __syncwarp();
-    if (lane == 0) {
-      int i = 0;
-      bool emitted = false;  // a stage of this chunk was issued
-      while (true) {
-        int sel[EXP_MAX_PER_STAGE];
-        int cnt = 0, tbytes = 0, j = i;
+    // Lane 0 packs each stage; every lane waits for the stage's slot itself
+    // (a lane that waits behind another's suspended wait and a shuffle
+    // measured about 0.5 us a stage), so the loop stays warp-uniform.
+    int i = 0;
+    bool emitted = false;  // a stage of this chunk was issued
+    while (true) {
+      int sel[EXP_MAX_PER_STAGE];
+      int cnt = 0, tbytes = 0, j = i;
+      bool more = false;
+      if (lane == 0) {
         while (j < n && cnt < EXP_MAX_PER_STAGE) {
           const int rows = chunk[j].w >> 16;
           if (rows == 0) {
@@ -110,15 +115,19 @@ __device__ __forceinline__ bool expand_produce(const int32_t *blocks, int blo, i
           tbytes += rows * 32;
           ++j;
         }
-        bool more = false;
         for (int q = j; q < n; ++q) more |= (chunk[q].w >> 16) > 0;
-        // The last chunk always issues a stage, so the MMA warp sees `last`.
-        if (cnt == 0 && !(final_chunk && !emitted)) break;
-        const bool last = final_chunk && !more;
-        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort)) {
-          ok = false;
-          break;
-        }
+      }
+      cnt = __shfl_sync(0xffffffffu, cnt, 0);
+      j = __shfl_sync(0xffffffffu, j, 0);
+      more = __shfl_sync(0xffffffffu, more ? 1 : 0, 0) != 0;
+      // The last chunk always issues a stage, so the MMA warp sees `last`.
+      if (cnt == 0 && !(final_chunk && !emitted)) break;
+      const bool last = final_chunk && !more;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[stage], phase ^ 1u, abort))) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
         uint8_t *st = ring + (size_t)stage * stage_bytes;
         ExpandStage &m = meta[stage];
         int toff = cnt * EXP_B_TILE;
@@ -146,20 +155,17 @@ __device__ __forceinline__ bool expand_produce(const int32_t *blocks, int blo, i
           bulk_load(st + m.blk[c].y, tw + (size_t)r.z * 16, (uint32_t)(rows * 32), &full[stage]);
           c = e;
         }
-        emitted = true;
-        ++issued;
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        i = j;
-        if (!more) break;
       }
+      __syncwarp();
+      emitted = true;
+      ++issued;
+      if (++stage == S) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      i = j;
+      if (!more) break;
     }
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    stage = __shfl_sync(0xffffffffu, stage, 0);
-    phase = __shfl_sync(0xffffffffu, phase, 0);
-    issued = __shfl_sync(0xffffffffu, issued, 0);
     __syncwarp();  // the chunk table is rewritten only after lane 0 has read it
   }
   return ok;
@@ -210,9 +216,9 @@ __device__ __forceinline__ bool expand_consume(uint8_t *ring, int stage_bytes, i
                                                uint32_t &phase, volatile int *abort, int lane) {
   bool ok = true;
   while (true) {
-    if (lane == 0) ok = mbar_wait_bounded(&full[stage], phase, abort);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    __syncwarp();
+    // Every lane tests the barrier itself (no lane waits behind another's
+    // suspended wait); they agree on the outcome before going on.
+    ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[stage], phase, abort));
     if (!ok) break;
     tc_fence_after_sync();
     const ExpandStage &m = meta[stage];
