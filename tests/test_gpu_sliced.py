@@ -152,10 +152,10 @@ def test_fused_groups_full_size_sampled(cfg, k):
 
 def test_gemm_kernel_query():
     """mlora_linear_gemm_kernel names one of the two GEMM kernels for valid
-    shapes and refuses invalid ones; on a 152-SM GB300 the decode step's
-    4-tile-per-SM shapes (o, down) take the cluster kernel and the others
-    the stream-K kernel; past 256 rows the cluster kernel only for one wave
-    that fills 70% of the SMs."""
+    shapes and refuses invalid ones; on a 152-SM GB300 draft calls (LoRA
+    off) take the stream-K kernel up to its 1024 rows; verify calls take the
+    cluster kernel for one wave that fills 80% of the SMs (70% past 256
+    rows)."""
     ml = needs_gpu()
     for M, N, K in [(64, 6144, 4096), (64, 4096, 4096), (64, 28672, 4096), (64, 4096, 14336), (700, 512, 512)]:
         for mode in (ml.DRAFT, ml.VERIFY):
@@ -169,6 +169,7 @@ def test_gemm_kernel_query():
         assert ml.gemm_kernel_name(640, 5120, 5120, 64, 16, ml.VERIFY) == "gemm_sk_kernel"
         assert ml.gemm_kernel_name(640, 5120, 27648, 64, 16, ml.VERIFY) == "gemm_sk_kernel"
         assert ml.gemm_kernel_name(640, 7168, 5120, 64, 16, ml.VERIFY) == "gemm_kernel"  # one wave, 74% full
-        assert ml.gemm_kernel_name(64, 4096, 4096, 16, 16, ml.DRAFT) == "gemm_kernel"
+        assert ml.gemm_kernel_name(64, 4096, 4096, 16, 16, ml.DRAFT) == "gemm_sk_kernel"
+        assert ml.gemm_kernel_name(64, 4096, 14336, 16, 16, ml.DRAFT) == "gemm_sk_kernel"
         assert ml.gemm_kernel_name(64, 28672, 4096, 16, 16, ml.DRAFT) == "gemm_sk_kernel"
         assert ml.gemm_kernel_name(128, 6144, 4096, 16, 16, ml.VERIFY) == "gemm_sk_kernel"
