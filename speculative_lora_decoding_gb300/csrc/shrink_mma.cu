@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(SQ_THREADS, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tail + 72);
   int *abort_flag = reinterpret_cast<int *>(tail + 76);
   int *zero_word = reinterpret_cast<int *>(tail + 80);
+  int *acc_ready = reinterpret_cast<int *>(tail + 84);  // the MMA warp's verdict on the accumulator, per pass
   uint64_t *drain = reinterpret_cast<uint64_t *>(tail + 88);
   int4 *rec = reinterpret_cast<int4 *>(tail + 96);  // per block: {a, j0, rank columns (0: skip), win}, {w0, W, s0, s1}
   int *span = reinterpret_cast<int *>(tail + 96 + 2 * SQ_BLOCKS * 16);  // first row, end row of the windows
@@ -277,18 +278,29 @@ __global__ void __launch_bounds__(SQ_THREADS, 1)
       mma_any = __shfl_sync(0xffffffffu, mma_any ? 1 : 0, 0) != 0;
       stage = __shfl_sync(0xffffffffu, stage, 0);
       phase = __shfl_sync(0xffffffffu, phase, 0);
+      // The accumulator handoff: this warp waits for the last MMA, then
+      // releases the staging warps through named barrier 1, so that they
+      // sleep in hardware instead of polling an mbarrier during the K loop.
+      // It arrives in every pass, aborted or not.
+      if (lane == 0) {
+        const bool ready = ok && !*ab && mbar_wait_bounded(acc_full, acc_phase, ab);
+        if (ok && !ready && !*ab) {
+          *ab = 1;
+          raise_status(args.status, MLORA_DEV_TIMEOUT);
+        }
+        *reinterpret_cast<volatile int *>(acc_ready) = ready ? 1 : 0;
+      }
+      __syncwarp();
+      tc_fence_before_sync();
+      named_bar_arrive(1, 160);
     } else {
       // -------------------------------------------------------- stage D
       // Warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (rows of D) and
       // writes them transposed, Dt[c][row] (fp32, 128 rows per column), into
       // the ring, which no copy or MMA of this pass touches any more.
-      bool have = !*ab && mbar_wait_bounded(acc_full, acc_phase, ab);
-      have = __all_sync(0xffffffffu, have);
-      if (!have && !*ab) {
-        *ab = 1;
-        raise_status(args.status, MLORA_DEV_TIMEOUT);
-      }
+      named_bar_sync(1, 160);
       tc_fence_after_sync();
+      const bool have = *reinterpret_cast<volatile int *>(acc_ready) != 0;
       if (have) {
         const int quad = warp & 3, row = quad * 32 + lane;
         const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16);
