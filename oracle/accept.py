@@ -26,7 +26,7 @@ that a GPU can reproduce each decision bit for bit:
   4. Output tokens x_0..x_{n-1}, then the drawn token, then -1 padding;
      accepted = n.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   * accept test "u*q < p" (strict); u in [0, 1).
   * the residual in 2^-40 fixed point: its total-variation bias against the
     real-valued residual is below V * 2^-40.

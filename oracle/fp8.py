@@ -10,8 +10,7 @@ draft pass runs the base model alone (LoRA off), so its weights can be an FP8
 copy of W: half the bytes of the HBM-bound draft.  Drafts only propose
 tokens; the LoRA-on verify pass (bf16) and the accept step decide what is
 emitted, so FP8 drafts change the acceptance rate, never the output
-distribution.  The readings taken where the pages say nothing (also listed in
-DESIGN.md):
+distribution.  The readings taken where the pages say nothing:
 
   * Format E4M3 (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
     largest finite 448, smallest normal 2^-6, subnormals down to 2^-9; no

@@ -8,7 +8,7 @@ The InvisibleLoRA abstract describes one KV cache for both models: the
 LoRA-off drafter writes its speculative K/V entries into the target's cache,
 the LoRA-on verification pass overwrites those entries, and the drafter
 therefore reads LoRA-conditioned K/V for the committed prefix.  The pages give
-no layout; the readings taken (also listed in the design doc):
+no layout; the readings taken:
 
   * A paged cache: K and V each [num_blocks, block_size, H, D] of bf16 words;
     request b's position `pos` lives in block block_table[b, pos // block_size]

@@ -18,7 +18,7 @@ residual draw (``oracle.accept``): weights Q(q(v)) = floor(q(v) * 2^40),
 S = sum of the weights, U = floor(u * 2^32), T = floor(U * S / 2^32), and the
 token is the smallest v whose running sum of weights exceeds T.
 
-Readings where the pages are silent (also listed in the design doc):
+Readings where the pages are silent:
   * temperature 1, no top-k / top-p truncation;
   * the draw takes the fp32 probabilities the kernel hands to the accept
     step, so that the drawn token and the q the accept step tests it with are
