@@ -322,9 +322,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Lane 0 issues the k-blocks; at an owned tile's expand point the whole
-    // warp stages the plan's expand records (expand_produce).  Every lane
-    // keeps the same ring position.
+    // The whole warp runs the loop and keeps the same ring position; lane 0
+    // issues the k-blocks' copies, and at an owned tile's expand point the
+    // lanes issue the expand stages from the plan.
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
     const uint32_t tx = (uint32_t)stage_bytes;
@@ -347,20 +347,27 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       if (waited) grid_dependency_wait();
     }
     early = __shfl_sync(0xffffffffu, early, 0);
-    // k-blocks [from, to) of unit u, lane 0 only.
+    // k-blocks [from, to) of unit u, all lanes: every lane waits for each
+    // slot itself (a lane that waits alone while the others stand at a
+    // shuffle measured about 0.5 us a wait), lane 0 issues the copies.  An
+    // owned unit's k-block stages are marked in their record (count -1): the
+    // MMA warp reads the kind of each of its stages.
     auto issue_kblocks = [&](int u, int from, int to) {
       const int w_row = u * SK_BN, x_row = m0;
       for (int kb = from; kb < to; ++kb, ++i) {
         uint8_t *st = ring + (size_t)stage * stage_bytes;
         if (i >= early) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, ab)) {
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[stage], phase ^ 1u, ab))) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], tx);
-          tma_load_2d(st, &tmap_w, &full[stage], kb * KBE, w_row, pol_w);
+          if (lane == 0) {
+            if (tc) meta[stage].count = -1;
+            mbar_arrive_expect_tx(&full[stage], tx);
+            tma_load_2d(st, &tmap_w, &full[stage], kb * KBE, w_row, pol_w);
+          }
         }
-        tma_load_2d(st + SK_WTILE, &tmap_x, &full[stage], kb * KBE, x_row, pol_x);
+        if (lane == 0) tma_load_2d(st + SK_WTILE, &tmap_x, &full[stage], kb * KBE, x_row, pol_x);
         ++issued;
         if (++stage == S) {
           stage = 0;
@@ -368,21 +375,12 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         }
       }
     };
-    auto sync_state = [&]() {
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      stage = __shfl_sync(0xffffffffu, stage, 0);
-      phase = __shfl_sync(0xffffffffu, phase, 0);
-      issued = __shfl_sync(0xffffffffu, issued, 0);
-      i = __shfl_sync(0xffffffffu, i, 0);
-      __syncwarp();
-    };
     for (int g = g0; g < g1 && ok;) {
       const int u = g / KB, kb0 = g - u * KB, kb1 = min(KB, g1 - u * KB);
       const int t = u;
       const uint16_t *tws = args.tw + (size_t)sk_slice_of(args, t * SK_BN) * args.tw_slice;
       if (!(tc && kb0 == 0)) {
-        if (lane == 0) issue_kblocks(u, kb0, kb1);
-        sync_state();
+        issue_kblocks(u, kb0, kb1);
       } else {
         // An owned unit (verify mode): the expand operands go into the ring
         // before the unit's last S k-blocks, so that they land while those
@@ -390,15 +388,16 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         // the plan and the windows, while its first k-blocks stream.
         const int ins = max(kb0, kb1 - 1 - S);
         const int split = ins + 1;
-        if (lane == 0) issue_kblocks(u, kb0, split);
-        sync_state();
+        issue_kblocks(u, kb0, split);
         if (ok) {
           if (!waited) {
             grid_dependency_wait();  // the token windows come from the shrink kernel just before
             waited = true;
           }
           if (ns < 0) ns = args.plan[L.hdr + 4];
-          if (ns > 0 && !cached && ns <= SK_CACHE_BLOCKS) {
+          // Also with no blocks at all (an empty stage flagged `last`): the MMA
+          // warp runs every owned unit's stages until `last`.
+          if (!cached && ns <= SK_CACHE_BLOCKS) {
             const int4 *src = reinterpret_cast<const int4 *>(args.plan + L.slices);
             for (int q = lane; q < ns * (EXP_WORDS / 4); q += 32) reinterpret_cast<int4 *>(blk_cache)[q] = src[q];
             __syncwarp();
@@ -406,16 +405,15 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                                  stage_bytes, lane, args.status);
             cached = true;
           }
-          if (ns > 0 && cached)
+          if (cached)
             ok = sk_expand_issue(blk_cache, 0, nst, bm, t * SK_BN, tws, ring, stage_bytes, S, full, empty, meta,
                                  stage, phase, issued, ab, pol_w, lane);
-          else if (ns > 0)
+          else
             ok = expand_produce(args.plan + L.slices, 0, ns, m0, args.Mb, t * SK_BN, args.N, &bm.b2, tws, ring,
                                 stage_bytes, S, full, empty, meta, chunk, stage, phase, issued, ab, pol_w, lane,
                                 args.n_ad, (long long)(args.tw_slice / 16), args.status);
         }
-        if (lane == 0 && ok) issue_kblocks(u, split, kb1);
-        sync_state();
+        if (ok) issue_kblocks(u, split, kb1);
       }
       g = u * KB + kb1;
     }
@@ -441,67 +439,58 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     const uint32_t idesc = F8 ? idesc_e4m3_f32(SK_BN, args.Mb) : idesc_bf16_f32(SK_BN, args.Mb);
     const uint32_t ring0 = smem_addr(ring);
     const uint32_t sbytes = (uint32_t)stage_bytes;
-    int stage = 0, seg = 0, ns = -1;
+    int stage = 0, seg = 0;
     uint32_t phase = 0;
     bool ok = true, issued_any = false;
     for (int g = g0; g < g1 && ok; ++seg) {
       const int u = g / KB, kb0 = g - u * KB, kb1 = min(KB, g1 - u * KB);
       const int buf = seg & 1;
       const uint32_t acc = tmem_base + (uint32_t)(buf * args.cols);
-      // The same order as the producer: k-blocks up to `ins`, the expand
-      // stages (owned tile, verify mode), then the remaining k-blocks.
+      // The whole warp runs the segment's stages (every lane tests each
+      // barrier itself), lane 0 issues the MMAs.  An owned unit (verify
+      // mode) has its expand stages among its k-blocks wherever the producer
+      // put them: each stage's record says which it is (count < 0: a
+      // k-block), and the unit's stages end with its last k-block and the
+      // expand stage flagged `last`, in either order.
       const bool expand_here = tc && kb0 == 0;
-      const int ins = expand_here ? max(kb0, kb1 - 1 - S) : kb1 - 1;
-      auto mma_kblocks = [&](int from, int to) {  // lane 0: k-blocks [from, to)
-        for (int kb = from; kb < to && ok; ++kb) {
-          if (!mbar_wait_bounded(&full[stage], phase, ab)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          const uint32_t a_addr = ring0 + (uint32_t)stage * sbytes;
-          const uint64_t ad = smem_desc_kmajor_sw128(a_addr);
-          const uint64_t bd = smem_desc_kmajor_sw128(a_addr + SK_WTILE);
-          const uint32_t first = kb > kb0 ? 1u : 0u;
-#pragma unroll
-          for (int kk = 0; kk < SK_BK / 16; ++kk) {  // 32 bytes of K per instruction
-            if (F8)
-              mma_e4m3_ss(acc, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : first);
-            else
-              mma_bf16_ss(acc, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : first);
-          }
-          mma_commit(&empty[stage]);
-          issued_any = true;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
+      if (seg >= 2 && ok)  // the accumulator's previous use (segment seg - 2) must be drained
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_empty[buf], (uint32_t)(((seg >> 1) - 1) & 1), ab));
+      tc_fence_after_sync();
+      int kb = kb0;
+      bool seen_last = !expand_here;
+      while (ok && (kb < kb1 || !seen_last)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[stage], phase, ab))) {
+          ok = false;
+          break;
         }
-      };
-      if (lane == 0) {
-        // The accumulator's previous use (segment seg - 2) must be drained.
-        if (seg >= 2 && !mbar_wait_bounded(&acc_empty[buf], (uint32_t)(((seg >> 1) - 1) & 1), ab)) ok = false;
         tc_fence_after_sync();
-        mma_kblocks(kb0, ins + 1);
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      stage = __shfl_sync(0xffffffffu, stage, 0);
-      phase = __shfl_sync(0xffffffffu, phase, 0);
-      __syncwarp();
-      if (ok && expand_here) {
-        if (ns < 0) {
-          grid_dependency_wait();  // the plan and the token windows come from earlier kernels
-          ns = args.plan[L.hdr + 4];
+        if (!expand_here || meta[stage].count < 0) {
+          if (lane == 0) {
+            const uint32_t a_addr = ring0 + (uint32_t)stage * sbytes;
+            const uint64_t ad = smem_desc_kmajor_sw128(a_addr);
+            const uint64_t bd = smem_desc_kmajor_sw128(a_addr + SK_WTILE);
+            const uint32_t first = kb > kb0 ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < SK_BK / 16; ++kk) {  // 32 bytes of K per instruction
+              if (F8)
+                mma_e4m3_ss(acc, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : first);
+              else
+                mma_bf16_ss(acc, ad + 2 * kk, bd + 2 * kk, idesc, kk > 0 ? 1u : first);
+            }
+            mma_commit(&empty[stage]);
+          }
+          ++kb;
+        } else {
+          seen_last = meta[stage].last != 0;
+          expand_stage_mma(ring + (size_t)stage * stage_bytes, meta[stage], acc, &empty[stage], lane);
         }
-        if (ns > 0) {
-          ok = expand_consume(ring, stage_bytes, S, full, empty, meta, acc, stage, phase, ab, lane);
-          issued_any = true;
+        issued_any = true;
+        __syncwarp();
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      if (lane == 0 && ok) mma_kblocks(ins + 1, kb1);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      stage = __shfl_sync(0xffffffffu, stage, 0);
-      phase = __shfl_sync(0xffffffffu, phase, 0);
       if (lane == 0 && ok) mma_commit(&acc_full[buf]);
       __syncwarp();
       g = u * KB + kb1;
