@@ -355,15 +355,15 @@ static mlora_status accept_impl(const float *p, const float *q, const int32_t *d
   float2 *sp = nullptr, *sq = nullptr;
   if (logits) {
     // Row statistics of the target rows, then of the draft rows, at most
-    // WS_MAX_COUNTERS rows per launch (one arrival counter per row).
+    // WS_MAX_COUNTERS rows per launch (the block partials' scratch is sized
+    // for that many rows).
     sp = reinterpret_cast<float2 *>(ws + WS_SCRATCH_OFF + sh.stats_off);
     sq = sp + (size_t)B * (k + 1);
-    uint32_t *counters = reinterpret_cast<uint32_t *>(ws + WS_COUNTERS_OFF);
     void *part = ws + WS_SCRATCH_OFF + sh.part_off;
     auto stats_of = [&](const float *z, long long rows, float2 *out) -> cudaError_t {
       for (long long r0 = 0; r0 < rows; r0 += (long long)WS_MAX_COUNTERS) {
         const int n = (int)std::min<long long>((long long)WS_MAX_COUNTERS, rows - r0);
-        cudaError_t e = launch_row_stats(z + (size_t)r0 * V, n, V, out + r0, part, counters, s);
+        cudaError_t e = launch_row_stats(z + (size_t)r0 * V, n, V, out + r0, part, s);
         if (e != cudaSuccess) return e;
       }
       return cudaSuccess;
@@ -410,8 +410,8 @@ mlora_status mlora_softmax(const float *z, int rows, int V, float *p, void *work
   float2 *stats = reinterpret_cast<float2 *>(ws + WS_SCRATCH_OFF);
   void *part = ws + WS_SCRATCH_OFF + align_up((size_t)rows * sizeof(float2), 256);
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_row_stats(z, rows, V, stats, part, reinterpret_cast<uint32_t *>(ws + WS_COUNTERS_OFF), s);
-  if (e == cudaSuccess) e = launch_softmax_write(z, rows, V, stats, p, sms, s);
+  cudaError_t e = launch_row_stats(z, rows, V, stats, part, s);
+  if (e == cudaSuccess) e = launch_softmax_write(z, rows, V, stats, p, s);
   return cuda_status(e);
 }
 
@@ -432,7 +432,6 @@ mlora_status mlora_draft_sample(const float *z_draft, int B, int V, const float 
   float2 *stats = reinterpret_cast<float2 *>(ws + WS_SCRATCH_OFF);
   void *blk = ws + WS_SCRATCH_OFF + align_up((size_t)B * sizeof(float2), 256);
   cudaError_t e = launch_draft_sample(z_draft, B, V, uniforms, draft_tok, stats, q_out, blk,
-                                      reinterpret_cast<uint32_t *>(ws + WS_COUNTERS_OFF),
                                       reinterpret_cast<uint32_t *>(ws + WS_STATUS_OFF), (cudaStream_t)stream);
   return cuda_status(e);
 }

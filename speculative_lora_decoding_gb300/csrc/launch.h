@@ -142,17 +142,15 @@ cudaError_t launch_accept(const float *p, const float *q, const int32_t *draft_t
 
 // Softmax of logit rows (softmax.cu): stats[r] = (max, sum) of row r; the
 // probabilities expf(z - max) / sum written out; the draft draw.
-// Row statistics use one CTA per (row, 4096-entry chunk), chunk partials in
-// `scratch` (row_stats_scratch_bytes) and one arrival counter per row
-// (counters[0, R), zero before and after; R <= WS_MAX_COUNTERS).
+// Row statistics take one warp per (row, 512-entry block) and keep the
+// blocks' partial pairs in `scratch` (row_stats_scratch_bytes); a second
+// launch merges each row's pairs.
 size_t row_stats_scratch_bytes(int R, int V);
-cudaError_t launch_row_stats(const float *z, int R, int V, float2 *stats, void *scratch, uint32_t *counters,
-                             cudaStream_t s);
-cudaError_t launch_softmax_write(const float *z, int R, int V, const float2 *stats, float *p, int num_sms,
-                                 cudaStream_t s);
+cudaError_t launch_row_stats(const float *z, int R, int V, float2 *stats, void *scratch, cudaStream_t s);
+cudaError_t launch_softmax_write(const float *z, int R, int V, const float2 *stats, float *p, cudaStream_t s);
 size_t draft_sample_scratch_bytes(int B, int V);
 cudaError_t launch_draft_sample(const float *z, int B, int V, const float *u, int32_t *tok, float2 *stats, float *q,
-                                void *scratch, uint32_t *counters, uint32_t *status, cudaStream_t s);
+                                void *scratch, uint32_t *status, cudaStream_t s);
 
 // Hybrid KV cache (kvcache.cu): the K/V rows of one pass into the paged
 // cache, and the committed lengths after the accept step.

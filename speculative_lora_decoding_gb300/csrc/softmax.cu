@@ -9,20 +9,27 @@
 //   p(v) = expf(z(v) - m) / S,   m = max_w z(w),   S = the row sum below
 //
 // computed in fp32 with CUDA's expf and an IEEE division.  The row statistics
-// (m, S) come from row_stats (one CTA per row, online softmax: every thread
-// keeps a running maximum and a sum rescaled whenever the maximum grows, over
-// a fixed set of entries in a fixed order, and the partial results are merged
-// in a fixed tree), so they are deterministic; because every entry of p is
-// computed from (m, S) by the same expression, the probabilities the accept
-// step derives from logits are bit-identical to the ones softmax_write
-// writes.
+// (m, S) are built over 512-entry blocks: a lane takes the maximum of its 16
+// entries of the block, then the sum of expf(z - that maximum); the lanes'
+// pairs are merged in a fixed tree (the maximum first, then the partial sums
+// rescaled to it and added) into the block's pair, and a second kernel merges
+// a row's block pairs the same way in a fixed order.  Nothing depends on the
+// grid or on the other rows of the call, so a row's statistics are the same
+// in every call; because every entry of p is computed from (m, S) by the same
+// expression, the probabilities the accept step derives from logits are
+// bit-identical to the ones softmax_write writes.
 //
 // The draft draw uses the accept step's exact integer inverse CDF on
 // Q(q(v)) = floor(q(v) * 2^40): S_w = sum of the weights, U = floor(u * 2^32),
 // T = floor(U * S_w / 2^32), token = the smallest v whose running sum of
-// weights exceeds T.  Sums of the weights of 512-entry blocks are kept (exact
-// in uint64), the block holding T is found by a scan over them, then the token
-// inside it by a warp scan.
+// weights exceeds T.  Each block's weight sum is kept (exact in uint64, so the
+// order of the additions does not matter), the block holding T is found by a
+// scan over them, then the token inside it by a warp scan.
+//
+// The kernels that read whole rows are streaming kernels: one warp per
+// (row, 512-entry block) unit, each load instruction of a warp 512
+// contiguous bytes, no barrier, atomic or fence between the warps (the merges
+// run in the next kernel, ordered by the launch).
 #include <algorithm>
 
 #include "common.cuh"
@@ -30,132 +37,139 @@
 
 namespace mlora {
 
-constexpr int SM_THREADS = 256;
-constexpr int SM_WARPS = SM_THREADS / 32;
-constexpr int SM_CHUNK = 4096;   // vocabulary entries per (row, chunk) unit: 16 per thread
-constexpr int DRAW_BLOCK = 512;  // vocabulary entries per weight block of the draw
+constexpr int SM_BLOCK = 512;            // entries per (row, block) unit: 16 per lane
+constexpr int UNIT_WARPS = 8;            // units per CTA of the streaming kernels
+constexpr int ROW_WARPS = 4;             // rows per CTA of the per-row kernels
 constexpr float SM_TWO_POW_32 = 4294967296.0f;
 constexpr float SM_TWO_POW_40 = 1099511627776.0f;
 
 // The probability of an entry from its logit and the row's statistics.
 __device__ __forceinline__ float prob_of(float z, float2 st) { return expf(z - st.x) / st.y; }
 
-// Merge two (running maximum, sum relative to it) pairs.
-__device__ __forceinline__ void merge_stats(float &m, float &s, float m2, float s2) {
-  if (m2 == -INFINITY) return;
-  if (m == -INFINITY) {
-    m = m2;
-    s = s2;
-    return;
-  }
-  const float mm = fmaxf(m, m2);
-  s = s * expf(m - mm) + s2 * expf(m2 - mm);
-  m = mm;
+// The entries of block k a lane holds: lane l takes the block's four-entry
+// groups 4 l + 128 j (j < 4), so that v[4 j + i] holds entry
+// 512 k + 4 l + 128 j + i.
+__device__ __forceinline__ int lane_entry(int k, int j, int i) {
+  return SM_BLOCK * k + 4 * (threadIdx.x & 31) + 128 * j + i;
 }
 
-__device__ __forceinline__ void online_add(float &m, float &s, float z) {
-  if (z > m) {
-    s = (m == -INFINITY ? 0.f : s * expf(m - z)) + 1.f;
-    m = z;
-  } else if (m != -INFINITY) {  // z = -inf before any finite logit adds nothing
-    s += expf(z - m);
-  }
-}
-
-// Statistics of one (row, 4096-entry chunk) unit by a CTA of 256 threads:
-// thread t takes entries 4t + 1024 j, j < 4 (float4 loads when the row
-// allows), an online pass over its 16 entries in index order, then a fixed
-// butterfly over the warp and a fixed sequential merge of the eight warps.
-__device__ float2 chunk_stats(const float *row, int v0, int V, bool vec, float2 *sh) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float m = -INFINITY, s = 0.f;
-  float v[16];
-  if (vec) {
+// Loads a lane's 16 entries of block k of `row`; entries at or past V read
+// as `fill`.  vec: the row is 16-byte aligned and V a multiple of 4.  STREAM
+// marks the lines evict-first (the last read of the row).
+template <bool STREAM>
+__device__ __forceinline__ void load_block(const float *row, int k, int V, bool vec, float fill, float (&v)[16]) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = v0 + 4 * tid + 1024 * j;
-      const float4 f = e < V ? __ldcs(reinterpret_cast<const float4 *>(row + e))
-                             : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  for (int j = 0; j < 4; ++j) {
+    const int e = lane_entry(k, j, 0);
+    if (vec) {
+      float4 f = make_float4(fill, fill, fill, fill);
+      if (e < V) {
+        const float4 *p = reinterpret_cast<const float4 *>(row + e);
+        f = STREAM ? __ldcs(p) : __ldg(p);
+      }
       v[4 * j] = f.x, v[4 * j + 1] = f.y, v[4 * j + 2] = f.z, v[4 * j + 3] = f.w;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int e = v0 + 4 * tid + 1024 * (j >> 2) + (j & 3);
-      v[j] = e < V ? __ldcs(row + e) : -INFINITY;
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 16; ++j) online_add(m, s, v[j]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    // Both lanes of a pair merge the same two values in the same order.
-    if (lane & o) {
-      float mm = m2, ss = s2;
-      merge_stats(mm, ss, m, s);
-      m = mm;
-      s = ss;
     } else {
-      merge_stats(m, s, m2, s2);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[4 * j + i] = e + i < V ? (STREAM ? __ldcs(row + e + i) : __ldg(row + e + i)) : fill;
     }
   }
-  if (lane == 0) sh[warp] = make_float2(m, s);
-  __syncthreads();
-  float2 res = make_float2(0.f, 0.f);
-  if (tid == 0) {
-    float mt = sh[0].x, st = sh[0].y;
-    for (int w = 1; w < SM_WARPS; ++w) merge_stats(mt, st, sh[w].x, sh[w].y);
-    res = make_float2(mt, st);
-  }
-  return res;  // valid in thread 0
 }
 
-// stats[r] = (m, S) of row r of z [R, V].  One CTA per (row, chunk) unit;
-// each writes its chunk's (maximum, sum) to part[r][c], and the last unit of
-// the row to arrive (counter, no spinning) merges the chunks in chunk order,
-// so the result does not depend on which unit finishes last.  The counters
-// return to zero.
-__global__ void __launch_bounds__(SM_THREADS)
-    row_stats_kernel(const float *__restrict__ z, int R, int V, int chunks, float2 *__restrict__ part,
-                     uint32_t *counters, float2 *__restrict__ stats) {
-  __shared__ float2 sh[SM_WARPS];
-  __shared__ int last;
+// A partial sum s taken relative to the maximum m, rescaled to the maximum
+// M >= m (nothing when m is -inf: every entry behind it is masked).
+__device__ __forceinline__ float rescaled(float m, float s, float M) { return m == -INFINITY ? 0.f : s * expf(m - M); }
+
+// (maximum, sum of expf(z - maximum)) of a lane's 16 entries, in index order.
+__device__ __forceinline__ float2 lane_stats(const float (&v)[16]) {
+  float m = v[0];
+#pragma unroll
+  for (int j = 1; j < 16; ++j) m = fmaxf(m, v[j]);
+  float s = 0.f;
+  if (m != -INFINITY) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) s += expf(v[j] - m);
+  }
+  return make_float2(m, s);
+}
+
+// Merge the warp's pairs: the maximum over the lanes, then each lane's sum
+// rescaled to it and added in a fixed tree.  Valid in lane 0.
+__device__ __forceinline__ float2 warp_merge(float m, float s) {
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float t = rescaled(m, s, M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_down_sync(0xffffffffu, t, o);
+  return make_float2(M, t);
+}
+
+// part[r][k] = the pair of block k of row r of z [R, V].  Grid (R, groups of
+// UNIT_WARPS blocks); warp w of CTA (r, y) takes block k = UNIT_WARPS y + w.
+__global__ void __launch_bounds__(UNIT_WARPS * 32)
+    block_stats_kernel(const float *__restrict__ z, int V, int nblk, float2 *__restrict__ part) {
   grid_dependency_wait();
   grid_launch_dependents();
+  const int r = blockIdx.x, k = blockIdx.y * UNIT_WARPS + (threadIdx.x >> 5);
+  if (k >= nblk) return;
   const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(z) & 15) == 0;
-  const int r = blockIdx.x / chunks, c = blockIdx.x - r * chunks;
-  const float2 cs = chunk_stats(z + (size_t)r * V, c * SM_CHUNK, V, vec, sh);
-  if (threadIdx.x == 0) {
-    part[(size_t)r * chunks + c] = cs;
-    __threadfence();
-    last = atomicAdd(&counters[r], 1u) == (uint32_t)(chunks - 1);
-  }
-  __syncthreads();
-  if (last && threadIdx.x == 0) {
-    __threadfence();
-    float m = -INFINITY, sm = 0.f;
-    for (int k = 0; k < chunks; ++k) {
-      const float2 p2 = __ldcg(&part[(size_t)r * chunks + k]);
-      merge_stats(m, sm, p2.x, p2.y);
-    }
-    stats[r] = make_float2(m, sm);
-    counters[r] = 0u;
-  }
+  float v[16];
+  load_block<false>(z + (size_t)r * V, k, V, vec, -INFINITY, v);
+  const float2 t = lane_stats(v);
+  const float2 w = warp_merge(t.x, t.y);
+  if ((threadIdx.x & 31) == 0) part[(size_t)r * nblk + k] = w;
 }
 
-// p[r, v] = prob_of(z[r, v], stats[r]).
-__global__ void __launch_bounds__(256)
-    softmax_write_kernel(const float *__restrict__ z, int R, int V, const float2 *__restrict__ stats,
+// stats[r] = (m, S) of row r from its block pairs, one warp per row: the
+// maximum, then lane l adds the rescaled sums of blocks l, l + 32, ... in
+// that order and the lanes' sums are added in a fixed tree.
+__global__ void __launch_bounds__(ROW_WARPS * 32)
+    row_merge_kernel(const float2 *__restrict__ part, int R, int nblk, float2 *__restrict__ stats) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int r = blockIdx.x * ROW_WARPS + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= R) return;
+  const float2 *pr = part + (size_t)r * nblk;
+  float M = -INFINITY;
+  for (int k = lane; k < nblk; k += 32) M = fmaxf(M, pr[k].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float s = 0.f;
+  for (int k = lane; k < nblk; k += 32) {
+    const float2 p = pr[k];
+    s += rescaled(p.x, p.y, M);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+  if (lane == 0) stats[r] = make_float2(M, s);
+}
+
+// p[r, v] = prob_of(z[r, v], stats[r]), in the units of block_stats.
+__global__ void __launch_bounds__(UNIT_WARPS * 32)
+    softmax_write_kernel(const float *__restrict__ z, int V, int nblk, const float2 *__restrict__ stats,
                          float *__restrict__ p) {
   grid_dependency_wait();
   grid_launch_dependents();
-  const long long total = (long long)R * V;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int r = (int)(i / V);
-    p[i] = prob_of(__ldcs(z + i), stats[r]);
+  const int r = blockIdx.x, k = blockIdx.y * UNIT_WARPS + (threadIdx.x >> 5);
+  if (k >= nblk) return;
+  const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(z) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+  const float2 st = stats[r];
+  float v[16];
+  load_block<true>(z + (size_t)r * V, k, V, vec, 0.f, v);
+  float *pr = p + (size_t)r * V;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = lane_entry(k, j, 0);
+    if (vec) {
+      if (e < V)
+        __stcs(reinterpret_cast<float4 *>(pr + e), make_float4(prob_of(v[4 * j], st), prob_of(v[4 * j + 1], st),
+                                                               prob_of(v[4 * j + 2], st), prob_of(v[4 * j + 3], st)));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (e + i < V) pr[e + i] = prob_of(v[4 * j + i], st);
+    }
   }
 }
 
@@ -177,164 +191,170 @@ __device__ __forceinline__ uint64_t warp_incl_scan_u64_sm(uint64_t v) {
   return v;
 }
 
-// Draft draw.  One CTA per (request b, 4096-entry chunk) unit: warp w takes
-// the chunk's 512-entry block w (16 consecutive entries per lane), writes the
-// probabilities (when q_out is given) and the block's exact uint64 weight sum
-// blk[b][8 c + w].  The last unit of the request to arrive (counter) totals
-// the weights, finds the block holding T (a block scan over contiguous runs
-// of blocks) and then the token inside it (a warp scan), and writes it.
-__global__ void __launch_bounds__(SM_THREADS)
-    draft_sample_kernel(const float *__restrict__ z, int B, int V, int chunks, const float2 *__restrict__ stats,
-                        const float *__restrict__ u, int32_t *__restrict__ tok, float *__restrict__ q_out,
-                        uint64_t *__restrict__ blk, uint32_t *counters, uint32_t *status) {
-  __shared__ uint64_t shu[SM_WARPS];
-  __shared__ int sh_block, last;
-  __shared__ uint64_t sh_T, sh_Tloc;
+// Draft draw, first half: in the units of block_stats, the probabilities of
+// block k of row b (written to q_out when it is given) and the block's exact
+// weight sum blk[b][k] = sum of Q(q(v)).
+__global__ void __launch_bounds__(UNIT_WARPS * 32)
+    draw_weights_kernel(const float *__restrict__ z, int V, int nblk, const float2 *__restrict__ stats,
+                        float *__restrict__ q_out, uint64_t *__restrict__ blk) {
   grid_dependency_wait();
   grid_launch_dependents();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.x / chunks, c = blockIdx.x - b * chunks;
-  const int nblk = chunks * (SM_CHUNK / DRAW_BLOCK);
-  const float *row = z + (size_t)b * V;
+  const int b = blockIdx.x, k = blockIdx.y * UNIT_WARPS + (threadIdx.x >> 5);
+  if (k >= nblk) return;
+  const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(z) & 15) == 0;
+  const bool vec_q = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(q_out) & 15) == 0;
   const float2 st = stats[b];
-  uint64_t *bw = blk + (size_t)b * nblk;
-  {
-    const int k = c * (SM_CHUNK / DRAW_BLOCK) + warp;
-    const int v0 = k * DRAW_BLOCK + 16 * lane;
-    uint64_t w = 0;
+  float v[16];
+  load_block<true>(z + (size_t)b * V, k, V, vec, 0.f, v);
+  uint64_t w = 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int v = v0 + j;
-      if (v < V) {
-        const float q = prob_of(row[v], st);
-        if (q_out) q_out[(size_t)b * V + v] = q;
-        w += q40(q);
+  for (int j = 0; j < 16; ++j) {
+    v[j] = lane_entry(k, j >> 2, j & 3) < V ? prob_of(v[j], st) : 0.f;
+    w += q40(v[j]);
+  }
+  if (q_out) {
+    float *qr = q_out + (size_t)b * V;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = lane_entry(k, j, 0);
+      if (vec_q) {
+        if (e < V) *reinterpret_cast<float4 *>(qr + e) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (e + i < V) qr[e + i] = v[4 * j + i];
       }
     }
-    w = warp_sum_u64_sm(w);
-    if (lane == 0) bw[k] = w;
   }
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    last = atomicAdd(&counters[b], 1u) == (uint32_t)(chunks - 1);
-  }
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  // Total and the block holding T: thread t sums a contiguous run of blocks.
-  const int per = (nblk + SM_THREADS - 1) / SM_THREADS;
-  const int k0 = min(nblk, tid * per), k1 = min(nblk, k0 + per);
+  w = warp_sum_u64_sm(w);
+  if ((threadIdx.x & 31) == 0) blk[(size_t)b * nblk + k] = w;
+}
+
+// Draft draw, second half, one warp per request b, three searches that each
+// take one round of parallel loads: lane l sums a contiguous run of the
+// blocks' weights and a warp scan finds the run that holds T; the warp scans
+// that run 32 blocks at a time and finds the block; lane l recomputes the
+// weights of 16 consecutive entries of the block (the same expression) and a
+// last warp scan finds the token.
+__global__ void __launch_bounds__(ROW_WARPS * 32)
+    draw_token_kernel(const float *__restrict__ z, int B, int V, int nblk, const float2 *__restrict__ stats,
+                      const uint64_t *__restrict__ blk, const float *__restrict__ u, int32_t *__restrict__ tok,
+                      uint32_t *status) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int b = blockIdx.x * ROW_WARPS + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (b >= B) return;
+  const uint64_t *bw = blk + (size_t)b * nblk;
+  const int per = (nblk + 31) / 32;
+  const int k0 = min(nblk, lane * per), k1 = min(nblk, k0 + per);
   uint64_t mine = 0;
-  for (int k = k0; k < k1; ++k) mine += __ldcg(&bw[k]);
+  for (int k = k0; k < k1; ++k) mine += bw[k];
   const uint64_t inc = warp_incl_scan_u64_sm(mine);
-  if (lane == 31) shu[warp] = inc;
-  __syncthreads();
-  uint64_t before = 0, total = 0;
-  for (int w = 0; w < SM_WARPS; ++w) {
-    if (w < warp) before += shu[w];
-    total += shu[w];
+  const uint64_t total = __shfl_sync(0xffffffffu, inc, 31);
+  float uu = u[b];
+  uint32_t fl = 0;
+  if (!(uu >= 0.f)) {
+    uu = 0.f;
+    fl |= MLORA_DEV_BAD_PROB;
+  } else if (uu >= 1.f) {
+    uu = __uint_as_float(0x3F7FFFFFu);
+    fl |= MLORA_DEV_BAD_PROB;
   }
-  if (tid == 0) {
-    counters[b] = 0u;
-    sh_block = -1;
-    float uu = u[b];
-    uint32_t fl = 0;
-    if (!(uu >= 0.f)) {
-      uu = 0.f;
-      fl |= MLORA_DEV_BAD_PROB;
-    } else if (uu >= 1.f) {
-      uu = __uint_as_float(0x3F7FFFFFu);
-      fl |= MLORA_DEV_BAD_PROB;
-    }
-    if (total == 0) fl |= MLORA_DEV_ZERO_MASS;
-    const uint64_t U = __float2ull_rz(uu * SM_TWO_POW_32);
-    sh_T = total == 0 ? 0 : (__umul64hi(U, total) << 32) | ((U * total) >> 32);  // floor(U * S / 2^32) < S
-    if (fl) raise_status(status, fl);
-  }
-  __syncthreads();
-  const uint64_t T = sh_T;
-  if (total != 0) {
-    uint64_t run = before + inc - mine;
-    if (run <= T && T < run + mine) {
-      for (int k = k0; k < k1; ++k) {
-        const uint64_t w = __ldcg(&bw[k]);
-        if (T < run + w) {
-          sh_block = k;
-          sh_Tloc = T - run;
-          break;
-        }
-        run += w;
+  if (total == 0) fl |= MLORA_DEV_ZERO_MASS;
+  const uint64_t U = __float2ull_rz(uu * SM_TWO_POW_32);
+  const uint64_t T = total == 0 ? 0 : (__umul64hi(U, total) << 32) | ((U * total) >> 32);  // floor(U * S / 2^32) < S
+  const uint32_t hit = __ballot_sync(0xffffffffu, total != 0 && inc - mine <= T && T < inc);
+  int t = 0;
+  if (hit) {
+    const int src = __ffs(hit) - 1;
+    uint64_t run = __shfl_sync(0xffffffffu, inc - mine, src);
+    const int r0 = __shfl_sync(0xffffffffu, k0, src), r1 = __shfl_sync(0xffffffffu, k1, src);
+    int kb = -1;
+    uint64_t Tl = 0;
+    for (int base = r0; base < r1 && kb < 0; base += 32) {
+      const uint64_t w = base + lane < r1 ? bw[base + lane] : 0ull;
+      const uint64_t c = warp_incl_scan_u64_sm(w);
+      const uint32_t h = __ballot_sync(0xffffffffu, run + c - w <= T && T < run + c);
+      if (h) {
+        const int l = __ffs(h) - 1;
+        kb = base + l;
+        Tl = T - run - __shfl_sync(0xffffffffu, c - w, l);
+      } else {
+        run += __shfl_sync(0xffffffffu, c, 31);
       }
     }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int t = 0;
-    const int kb = sh_block;
-    if (kb >= 0) {
-      const uint64_t Tl = sh_Tloc;
-      const int v0 = kb * DRAW_BLOCK + 16 * lane;
-      uint64_t wv[16];
+    if (kb >= 0) {  // always, when the sums are consistent
+      const float *row = z + (size_t)b * V;
+      const float2 st = stats[b];
+      const int v0 = kb * SM_BLOCK + 16 * lane;
       uint64_t mw = 0;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        wv[j] = v0 + j < V ? q40(prob_of(row[v0 + j], st)) : 0ull;
-        mw += wv[j];
-      }
+      for (int j = 0; j < 16; ++j)
+        if (v0 + j < V) mw += q40(prob_of(__ldg(row + v0 + j), st));
       const uint64_t inc2 = warp_incl_scan_u64_sm(mw);
       uint64_t run2 = inc2 - mw;
-      const uint32_t hit = __ballot_sync(0xffffffffu, run2 <= Tl && Tl < run2 + mw);
+      const uint32_t hit2 = __ballot_sync(0xffffffffu, run2 <= Tl && Tl < run2 + mw);
       int found = -1;
-      if (hit && lane == __ffs(hit) - 1) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (found < 0 && Tl < run2 + wv[j]) found = v0 + j;
-          run2 += wv[j];
+      if (hit2 && lane == __ffs(hit2) - 1) {  // the lane's weights again, in order
+        for (int j = 0; j < 16 && v0 + j < V; ++j) {
+          run2 += q40(prob_of(__ldg(row + v0 + j), st));
+          if (Tl < run2) {
+            found = v0 + j;
+            break;
+          }
         }
       }
-      t = hit ? __shfl_sync(0xffffffffu, found, __ffs(hit) - 1) : 0;
+      t = hit2 ? __shfl_sync(0xffffffffu, found, __ffs(hit2) - 1) : 0;
       if (t < 0) t = 0;  // unreachable when the sums are consistent
     }
-    if (lane == 0) tok[b] = t;
+  }
+  if (lane == 0) {
+    tok[b] = t;
+    if (fl) raise_status(status, fl);
   }
 }
 
-static int chunks_of(int V) { return (V + SM_CHUNK - 1) / SM_CHUNK; }
+static int blocks_of(int V) { return (V + SM_BLOCK - 1) / SM_BLOCK; }
 
-size_t row_stats_scratch_bytes(int R, int V) { return align_up((size_t)R * chunks_of(V) * sizeof(float2), 256); }
+// The grid of the streaming kernels: x = row, y = group of UNIT_WARPS blocks.
+static dim3 unit_grid(int R, int nblk) { return dim3((unsigned)R, (unsigned)((nblk + UNIT_WARPS - 1) / UNIT_WARPS)); }
 
-cudaError_t launch_row_stats(const float *z, int R, int V, float2 *stats, void *scratch, uint32_t *counters,
-                             cudaStream_t s) {
-  const int chunks = chunks_of(V);
-  cudaError_t e = launch_pdl(row_stats_kernel, dim3((unsigned)((long long)R * chunks)), dim3(SM_THREADS), 0, s, z, R,
-                             V, chunks, reinterpret_cast<float2 *>(scratch), counters, stats);
+size_t row_stats_scratch_bytes(int R, int V) { return align_up((size_t)R * blocks_of(V) * sizeof(float2), 256); }
+
+cudaError_t launch_row_stats(const float *z, int R, int V, float2 *stats, void *scratch, cudaStream_t s) {
+  const int nblk = blocks_of(V);
+  float2 *part = reinterpret_cast<float2 *>(scratch);
+  cudaError_t e =
+      launch_pdl(block_stats_kernel, unit_grid(R, nblk), dim3(UNIT_WARPS * 32), 0, s, z, V, nblk, part);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(row_merge_kernel, dim3((unsigned)((R + ROW_WARPS - 1) / ROW_WARPS)), dim3(ROW_WARPS * 32), 0, s,
+                 (const float2 *)part, R, nblk, stats);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_softmax_write(const float *z, int R, int V, const float2 *stats, float *p, int num_sms,
-                                 cudaStream_t s) {
-  const long long total = (long long)R * V;
-  const int grid = (int)std::max<long long>(1, std::min<long long>((total + 255) / 256, (long long)num_sms * 8));
-  cudaError_t e = launch_pdl(softmax_write_kernel, dim3(grid), dim3(256), 0, s, z, R, V, stats, p);
+cudaError_t launch_softmax_write(const float *z, int R, int V, const float2 *stats, float *p, cudaStream_t s) {
+  const int nblk = blocks_of(V);
+  cudaError_t e = launch_pdl(softmax_write_kernel, unit_grid(R, nblk), dim3(UNIT_WARPS * 32), 0, s, z, V, nblk,
+                             stats, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-size_t draft_sample_scratch_bytes(int B, int V) {
-  return align_up((size_t)B * chunks_of(V) * (SM_CHUNK / DRAW_BLOCK) * sizeof(uint64_t), 256) +
-         row_stats_scratch_bytes(B, V);
-}
+static size_t draw_sums_bytes(int B, int V) { return align_up((size_t)B * blocks_of(V) * sizeof(uint64_t), 256); }
+
+size_t draft_sample_scratch_bytes(int B, int V) { return draw_sums_bytes(B, V) + row_stats_scratch_bytes(B, V); }
 
 cudaError_t launch_draft_sample(const float *z, int B, int V, const float *u, int32_t *tok, float2 *stats, float *q,
-                                void *scratch, uint32_t *counters, uint32_t *status, cudaStream_t s) {
-  const int chunks = chunks_of(V);
+                                void *scratch, uint32_t *status, cudaStream_t s) {
+  const int nblk = blocks_of(V);
   uint8_t *sc = static_cast<uint8_t *>(scratch);
   uint64_t *blk = reinterpret_cast<uint64_t *>(sc);
-  void *stats_scratch = sc + align_up((size_t)B * chunks * (SM_CHUNK / DRAW_BLOCK) * sizeof(uint64_t), 256);
-  cudaError_t e = launch_row_stats(z, B, V, stats, stats_scratch, counters, s);
+  cudaError_t e = launch_row_stats(z, B, V, stats, sc + draw_sums_bytes(B, V), s);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(draft_sample_kernel, dim3((unsigned)((long long)B * chunks)), dim3(SM_THREADS), 0, s, z, B, V,
-                 chunks, (const float2 *)stats, u, tok, q, blk, counters, status);
+  e = launch_pdl(draw_weights_kernel, unit_grid(B, nblk), dim3(UNIT_WARPS * 32), 0, s, z, V, nblk,
+                 (const float2 *)stats, q, blk);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(draw_token_kernel, dim3((unsigned)((B + ROW_WARPS - 1) / ROW_WARPS)), dim3(ROW_WARPS * 32), 0, s, z,
+                 B, V, nblk, (const float2 *)stats, (const uint64_t *)blk, u, tok, status);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
