@@ -254,6 +254,16 @@ MLORA_API int mlora_linear_gemm_kernel(int M, int N, int K, int n_adapters, int 
  * hangs or faults. */
 MLORA_API void mlora_debug_set_flag_wait_ns(uint32_t ns);
 
+/* Test hook for the draw's weights (no counterpart on the pages): the
+ * kernels compute Q(f) = floor(f * 2^40) of a probability clamped to [0, 1]
+ * from the bits of f with integer operations.  For the `count` fp32 bit
+ * patterns first_bits, first_bits + 1, ... this adds to *mismatches (device
+ * memory, caller-owned, caller-zeroed) the number whose Q differs from
+ * CUDA's round-down conversion of the clamped f * 2^40.  Asynchronous on
+ * `stream`.  MLORA_ERR_ARG when the range passes 2^32 or mismatches is NULL. */
+MLORA_API mlora_status mlora_debug_q40_mismatches(uint32_t first_bits, uint32_t count,
+                                                  unsigned long long *mismatches, mlora_stream stream);
+
 /* Which kernel writes the low-rank operand (the token windows of
  * bf16(scale * A_a x)) in later verify-mode layer calls (no counterpart on the
  * pages, which compute the per-adapter product without naming a kernel):

@@ -333,6 +333,15 @@ int mlora_linear_gemm_kernel(int M, int N, int K, int n_adapters, int r_max, int
 
 void mlora_debug_set_flag_wait_ns(uint32_t ns) { g_test_flag_wait_ns.store(ns, std::memory_order_relaxed); }
 
+mlora_status mlora_debug_q40_mismatches(uint32_t first_bits, uint32_t count, unsigned long long *mismatches,
+                                        mlora_stream stream) {
+  if (!mismatches || (uint64_t)first_bits + count > (1ull << 32)) return MLORA_ERR_ARG;
+  if (count == 0) return MLORA_OK;
+  const int sms = device_sms();
+  if (sms <= 0) return MLORA_ERR_CUDA;
+  return cuda_status(launch_q40_check(first_bits, count, mismatches, sms, (cudaStream_t)stream));
+}
+
 mlora_status mlora_set_shrink_path(int path) {
   if (path != MLORA_SHRINK_AUTO && path != MLORA_SHRINK_WARP && path != MLORA_SHRINK_TENSOR) return MLORA_ERR_ARG;
   g_shrink_path.store(path, std::memory_order_relaxed);

@@ -151,6 +151,8 @@ cudaError_t launch_softmax_write(const float *z, int R, int V, const float2 *sta
 size_t draft_sample_scratch_bytes(int B, int V);
 cudaError_t launch_draft_sample(const float *z, int B, int V, const float *u, int32_t *tok, float2 *stats, float *q,
                                 void *scratch, uint32_t *status, cudaStream_t s);
+cudaError_t launch_q40_check(uint32_t first, uint32_t count, unsigned long long *mismatches, int num_sms,
+                             cudaStream_t s);
 
 // Hybrid KV cache (kvcache.cu): the K/V rows of one pass into the paged
 // cache, and the committed lengths after the accept step.

@@ -41,7 +41,6 @@ constexpr int SM_BLOCK = 512;            // entries per (row, block) unit: 16 pe
 constexpr int UNIT_WARPS = 8;            // units per CTA of the streaming kernels
 constexpr int ROW_WARPS = 4;             // rows per CTA of the per-row kernels
 constexpr float SM_TWO_POW_32 = 4294967296.0f;
-constexpr float SM_TWO_POW_40 = 1099511627776.0f;
 
 // The probability of an entry from its logit and the row's statistics.
 __device__ __forceinline__ float prob_of(float z, float2 st) { return expf(z - st.x) / st.y; }
@@ -173,7 +172,20 @@ __global__ void __launch_bounds__(UNIT_WARPS * 32)
   }
 }
 
-__device__ __forceinline__ uint64_t q40(float f) { return __float2ull_rd(fminf(fmaxf(f, 0.f), 1.f) * SM_TWO_POW_40); }
+// Q(f) = floor(f * 2^40) of f clamped to [0, 1] (NaN to 0), from the bits
+// of f with integer operations only: f = M 2^(e - 23) with the 24-bit
+// significand M (implicit one included) and the unbiased exponent e <= 0, so
+// f 2^40 = M 2^(e + 17) is M shifted left by e + 17, or right by -(e + 17)
+// (nothing left once that is 24 or more).  Zero and subnormal f give 0
+// (f 2^40 < 2^-86).
+__device__ __forceinline__ uint64_t q40(float f) {
+  const uint32_t bits = __float_as_uint(fminf(fmaxf(f, 0.f), 1.f)) & 0x7FFFFFFFu;
+  const int e = (int)(bits >> 23) - 127;
+  if (e < -126) return 0ull;
+  const uint64_t M = (uint64_t)((bits & 0x7FFFFFu) | 0x800000u);
+  const int sh = e + 17;
+  return sh >= 0 ? M << sh : (sh > -24 ? M >> -sh : 0ull);
+}
 
 __device__ __forceinline__ uint64_t warp_sum_u64_sm(uint64_t v) {
 #pragma unroll
@@ -312,6 +324,27 @@ __global__ void __launch_bounds__(ROW_WARPS * 32)
     tok[b] = t;
     if (fl) raise_status(status, fl);
   }
+}
+
+// Test hook: counts the bit patterns first + i (i < count) whose q40 differs
+// from CUDA's round-down conversion of the clamped f * 2^40.
+__global__ void q40_check_kernel(uint32_t first, uint32_t count, unsigned long long *mismatches) {
+  unsigned long long bad = 0;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride) {
+    const float f = __uint_as_float(first + i);
+    const uint64_t ref = __float2ull_rd(fminf(fmaxf(f, 0.f), 1.f) * 1099511627776.0f);
+    bad += q40(f) != ref;
+    if (stride > count - i) break;  // the next i would wrap past 2^32
+  }
+  bad = warp_sum_u64_sm(bad);
+  if ((threadIdx.x & 31) == 0 && bad) atomicAdd(mismatches, bad);
+}
+
+cudaError_t launch_q40_check(uint32_t first, uint32_t count, unsigned long long *mismatches, int num_sms,
+                             cudaStream_t s) {
+  q40_check_kernel<<<std::max(num_sms, 1) * 8, 256, 0, s>>>(first, count, mismatches);
+  return cudaGetLastError();
 }
 
 static int blocks_of(int V) { return (V + SM_BLOCK - 1) / SM_BLOCK; }

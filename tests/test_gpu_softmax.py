@@ -140,3 +140,19 @@ def test_accept_on_logits(B, k, V):
         close |= _draw_margin(w.astype(np.uint64), U) <= 2 * shift
         assert close, b
     assert len(differ) <= max(1, B // 50), differ
+
+
+def test_q40_matches_cuda_conversion_on_every_float():
+    """The draw's Q(f) = floor(f 2^40), computed from the bits of f, equals
+    CUDA's round-down conversion of the clamped f 2^40 on all 2^32 fp32 bit
+    patterns (zeros, subnormals, values above 1, infinities and NaNs
+    included)."""
+    ml = needs_gpu()
+    lib = ml.library()
+    bad = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for first in (0, 1 << 31):
+        assert lib.mlora_debug_q40_mismatches(first, 1 << 31, bad.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    assert int(bad.item()) == 0
+    # The range check: first + count past 2^32 is refused.
+    assert lib.mlora_debug_q40_mismatches(2, 0xFFFFFFFF, bad.data_ptr(), None) != 0
