@@ -339,7 +339,7 @@ MLORA_API mlora_status mlora_verify_accept(const float *p_target, const float *q
 /* The same step taking logits instead of probabilities: z_target [B, k+1, V]
  * are the LoRA-on pass's logits, z_draft [B, k, V] the LoRA-off passes'.  The
  * softmax is fused into the accept kernels: every probability they read is
- * expf(z - m) / S of its row, with the row statistics of mlora_softmax, so the
+ * e^(z - m) * R of its row, with the row statistics of mlora_softmax, so the
  * decisions are exactly those mlora_verify_accept takes on the probabilities
  * mlora_softmax writes for the same logits.  Everything else as
  * mlora_verify_accept; workspace mlora_accept_workspace_bytes(B, k, V).  The
@@ -354,11 +354,13 @@ MLORA_API mlora_status mlora_verify_accept_logits(const float *z_target, const f
 /* Softmax and the draft draw (the steps on either side of the accept step)  */
 /* ------------------------------------------------------------------------- */
 
-/* p[r, v] = expf(z[r, v] - m_r) / S_r for `rows` rows of V fp32 logits, with
- * m_r the row maximum and S_r the row's sum of expf(z - m_r) (accumulated in a
- * fixed order in fp32: the results are deterministic).  CUDA's expf, IEEE
- * division.  The InvisibleLoRA abstract has both passes end in a distribution
- * over the vocabulary; the softmax of the logits is the plain reading.
+/* p[r, v] = e^(z[r, v] - m_r) * R_r for `rows` rows of V fp32 logits, with
+ * m_r the row maximum, S_r the row's sum of e^(z - m_r) (accumulated in a
+ * fixed order in fp32: the results are deterministic, and a row's values do
+ * not depend on the other rows of the call) and R_r = 1/S_r rounded once.
+ * e^d is computed as 2^(d log2 e) with the PTX ex2.approx instruction.  The
+ * InvisibleLoRA abstract has both passes end in a distribution over the
+ * vocabulary; the softmax of the logits is the plain reading.
  *   z, p   fp32 [rows, V] device (p may not alias z); rows in [1, 65536],
  *          V in [1, 2^24]; workspace mlora_softmax_workspace_bytes(rows, V). */
 MLORA_API size_t mlora_softmax_workspace_bytes(int rows, int V);

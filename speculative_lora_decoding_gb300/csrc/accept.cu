@@ -38,6 +38,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "prob.cuh"
 
 namespace mlora {
 
@@ -83,13 +84,13 @@ __device__ __forceinline__ float clamp_prob(float f, bool &bad) {
 __device__ __forceinline__ uint64_t fixq(float f) { return __float2ull_rd(f * TWO_POW_40); }
 
 // Logits mode (LG): rows hold logits z and the probability of an entry is
-// expf(z - m) / S with the row's statistics st = (m, S) from row_stats, the
-// one expression softmax.cu uses everywhere (so the decisions equal the ones
-// taken on the probabilities mlora_softmax writes).  Otherwise rows hold
-// probabilities and are read as they are.
+// prob_from_logit(z, st) with the row's pair st = (m, 1/S) from the row
+// statistics, the one expression the softmax uses everywhere (so the
+// decisions equal the ones taken on the probabilities mlora_softmax writes).
+// Otherwise rows hold probabilities and are read as they are.
 template <bool LG>
 __device__ __forceinline__ float as_prob(float f, float2 st) {
-  if (LG) return expf(f - st.x) / st.y;
+  if (LG) return prob_from_logit(f, st);
   return f;
 }
 

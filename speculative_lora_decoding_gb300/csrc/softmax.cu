@@ -4,20 +4,18 @@
 // abstract: a LoRA-off pass proposes the next token for every request, one
 // LoRA-on pass verifies the proposals).
 //
-// One definition of a probability serves every kernel of the library:
-//
-//   p(v) = expf(z(v) - m) / S,   m = max_w z(w),   S = the row sum below
-//
-// computed in fp32 with CUDA's expf and an IEEE division.  The row statistics
-// (m, S) are built over 512-entry blocks: a lane takes the maximum of its 16
-// entries of the block, then the sum of expf(z - that maximum); the lanes'
+// One definition of a probability serves every kernel of the library (the
+// functions of prob.cuh): p(v) = e^(z(v) - m) R, with m the row maximum and
+// R = 1/S the reciprocal of the row sum below, rounded once per row.  The row
+// statistics are built over 512-entry blocks: a lane takes the maximum of its
+// 16 entries of the block, then the sum of e^(z - that maximum); the lanes'
 // pairs are merged in a fixed tree (the maximum first, then the partial sums
 // rescaled to it and added) into the block's pair, and a second kernel merges
-// a row's block pairs the same way in a fixed order.  Nothing depends on the
-// grid or on the other rows of the call, so a row's statistics are the same
-// in every call; because every entry of p is computed from (m, S) by the same
-// expression, the probabilities the accept step derives from logits are
-// bit-identical to the ones softmax_write writes.
+// a row's block pairs the same way in a fixed order and stores (m, 1/S).
+// Nothing depends on the grid or on the other rows of the call, so a row's
+// statistics are the same in every call; because every entry of p is computed
+// from them by the same expression, the probabilities the accept step derives
+// from logits are bit-identical to the ones softmax_write writes.
 //
 // The draft draw uses the accept step's exact integer inverse CDF on
 // Q(q(v)) = floor(q(v) * 2^40): S_w = sum of the weights, U = floor(u * 2^32),
@@ -34,6 +32,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "prob.cuh"
 
 namespace mlora {
 
@@ -41,9 +40,6 @@ constexpr int SM_BLOCK = 512;            // entries per (row, block) unit: 16 pe
 constexpr int UNIT_WARPS = 8;            // units per CTA of the streaming kernels
 constexpr int ROW_WARPS = 4;             // rows per CTA of the per-row kernels
 constexpr float SM_TWO_POW_32 = 4294967296.0f;
-
-// The probability of an entry from its logit and the row's statistics.
-__device__ __forceinline__ float prob_of(float z, float2 st) { return expf(z - st.x) / st.y; }
 
 // The entries of block k a lane holds: lane l takes the block's four-entry
 // groups 4 l + 128 j (j < 4), so that v[4 j + i] holds entry
@@ -76,9 +72,9 @@ __device__ __forceinline__ void load_block(const float *row, int k, int V, bool 
 
 // A partial sum s taken relative to the maximum m, rescaled to the maximum
 // M >= m (nothing when m is -inf: every entry behind it is masked).
-__device__ __forceinline__ float rescaled(float m, float s, float M) { return m == -INFINITY ? 0.f : s * expf(m - M); }
+__device__ __forceinline__ float rescaled(float m, float s, float M) { return m == -INFINITY ? 0.f : s * exp_of(m - M); }
 
-// (maximum, sum of expf(z - maximum)) of a lane's 16 entries, in index order.
+// (maximum, sum of e^(z - maximum)) of a lane's 16 entries, in index order.
 __device__ __forceinline__ float2 lane_stats(const float (&v)[16]) {
   float m = v[0];
 #pragma unroll
@@ -86,7 +82,7 @@ __device__ __forceinline__ float2 lane_stats(const float (&v)[16]) {
   float s = 0.f;
   if (m != -INFINITY) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) s += expf(v[j] - m);
+    for (int j = 0; j < 16; ++j) s += exp_of(v[j] - m);
   }
   return make_float2(m, s);
 }
@@ -119,9 +115,10 @@ __global__ void __launch_bounds__(UNIT_WARPS * 32)
   if ((threadIdx.x & 31) == 0) part[(size_t)r * nblk + k] = w;
 }
 
-// stats[r] = (m, S) of row r from its block pairs, one warp per row: the
+// stats[r] = (m, 1/S) of row r from its block pairs, one warp per row: the
 // maximum, then lane l adds the rescaled sums of blocks l, l + 32, ... in
-// that order and the lanes' sums are added in a fixed tree.
+// that order, the lanes' sums are added in a fixed tree, and the total's
+// reciprocal is rounded once (IEEE).
 __global__ void __launch_bounds__(ROW_WARPS * 32)
     row_merge_kernel(const float2 *__restrict__ part, int R, int nblk, float2 *__restrict__ stats) {
   grid_dependency_wait();
@@ -140,10 +137,10 @@ __global__ void __launch_bounds__(ROW_WARPS * 32)
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
-  if (lane == 0) stats[r] = make_float2(M, s);
+  if (lane == 0) stats[r] = make_float2(M, __frcp_rn(s));
 }
 
-// p[r, v] = prob_of(z[r, v], stats[r]), in the units of block_stats.
+// p[r, v] = prob_from_logit(z[r, v], stats[r]), in the units of block_stats.
 __global__ void __launch_bounds__(UNIT_WARPS * 32)
     softmax_write_kernel(const float *__restrict__ z, int V, int nblk, const float2 *__restrict__ stats,
                          float *__restrict__ p) {
@@ -162,29 +159,27 @@ __global__ void __launch_bounds__(UNIT_WARPS * 32)
     const int e = lane_entry(k, j, 0);
     if (vec) {
       if (e < V)
-        __stcs(reinterpret_cast<float4 *>(pr + e), make_float4(prob_of(v[4 * j], st), prob_of(v[4 * j + 1], st),
-                                                               prob_of(v[4 * j + 2], st), prob_of(v[4 * j + 3], st)));
+        __stcs(reinterpret_cast<float4 *>(pr + e), make_float4(prob_from_logit(v[4 * j], st), prob_from_logit(v[4 * j + 1], st),
+                                                               prob_from_logit(v[4 * j + 2], st), prob_from_logit(v[4 * j + 3], st)));
     } else {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        if (e + i < V) pr[e + i] = prob_of(v[4 * j + i], st);
+        if (e + i < V) pr[e + i] = prob_from_logit(v[4 * j + i], st);
     }
   }
 }
 
-// Q(f) = floor(f * 2^40) of f clamped to [0, 1] (NaN to 0), from the bits
-// of f with integer operations only: f = M 2^(e - 23) with the 24-bit
-// significand M (implicit one included) and the unbiased exponent e <= 0, so
-// f 2^40 = M 2^(e + 17) is M shifted left by e + 17, or right by -(e + 17)
-// (nothing left once that is 24 or more).  Zero and subnormal f give 0
-// (f 2^40 < 2^-86).
+// Q(f) = floor(f * 2^40) of f clamped to [0, 1] (NaN to 0), with integer
+// operations on the bits of x = |f| 2^40 (exact): x = M 2^s with the 24-bit
+// significand M (implicit one included) and s = (biased exponent) - 150, so
+// floor(x) is M shifted left by s when s >= 0 and right by -s otherwise
+// (nothing is left once -s reaches 24: x < 1, zero and subnormals included).
 __device__ __forceinline__ uint64_t q40(float f) {
-  const uint32_t bits = __float_as_uint(fminf(fmaxf(f, 0.f), 1.f)) & 0x7FFFFFFFu;
-  const int e = (int)(bits >> 23) - 127;
-  if (e < -126) return 0ull;
-  const uint64_t M = (uint64_t)((bits & 0x7FFFFFu) | 0x800000u);
-  const int sh = e + 17;
-  return sh >= 0 ? M << sh : (sh > -24 ? M >> -sh : 0ull);
+  const float x = fabsf(fminf(fmaxf(f, 0.f), 1.f)) * 1099511627776.0f;
+  const uint32_t bits = __float_as_uint(x);
+  const uint32_t M = (bits & 0x7FFFFFu) | 0x800000u;
+  const int s = (int)(bits >> 23) - 150;
+  return s >= 0 ? (uint64_t)M << s : (uint64_t)(M >> min(-s, 31));
 }
 
 __device__ __forceinline__ uint64_t warp_sum_u64_sm(uint64_t v) {
@@ -219,10 +214,18 @@ __global__ void __launch_bounds__(UNIT_WARPS * 32)
   float v[16];
   load_block<true>(z + (size_t)b * V, k, V, vec, 0.f, v);
   uint64_t w = 0;
+  if ((k + 1) * SM_BLOCK <= V) {  // every block but a row's last
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    v[j] = lane_entry(k, j >> 2, j & 3) < V ? prob_of(v[j], st) : 0.f;
-    w += q40(v[j]);
+    for (int j = 0; j < 16; ++j) {
+      v[j] = prob_from_logit(v[j], st);
+      w += q40(v[j]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      v[j] = lane_entry(k, j >> 2, j & 3) < V ? prob_from_logit(v[j], st) : 0.f;
+      w += q40(v[j]);
+    }
   }
   if (q_out) {
     float *qr = q_out + (size_t)b * V;
@@ -302,14 +305,14 @@ __global__ void __launch_bounds__(ROW_WARPS * 32)
       uint64_t mw = 0;
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        if (v0 + j < V) mw += q40(prob_of(__ldg(row + v0 + j), st));
+        if (v0 + j < V) mw += q40(prob_from_logit(__ldg(row + v0 + j), st));
       const uint64_t inc2 = warp_incl_scan_u64_sm(mw);
       uint64_t run2 = inc2 - mw;
       const uint32_t hit2 = __ballot_sync(0xffffffffu, run2 <= Tl && Tl < run2 + mw);
       int found = -1;
       if (hit2 && lane == __ffs(hit2) - 1) {  // the lane's weights again, in order
         for (int j = 0; j < 16 && v0 + j < V; ++j) {
-          run2 += q40(prob_of(__ldg(row + v0 + j), st));
+          run2 += q40(prob_from_logit(__ldg(row + v0 + j), st));
           if (Tl < run2) {
             found = v0 + j;
             break;

@@ -1,14 +1,15 @@
 """GPU parity of the softmax, the draft draw and the accept step on logits.
 
-The kernels compute a probability as expf(z - m) / S in fp32 (CUDA's expf,
-IEEE division, a row sum accumulated in a fixed order); the oracle is the
-float64 softmax.  Tolerance: per entry |p - p_ref| <= REL * p_ref with
-REL = 1e-4, from the fp32 arithmetic: expf is within 2 ulp (2.4e-7
-relative), the rounding of z - m moves the exponent by |z - m| 2^-24 (under
-2.4e-6 for the |z - m| <= 40 of these inputs), and the row sum (16 terms per
-thread, 8 tree levels inside a chunk, a chunk's rescaling, then up to
-chunks / 32 terms per lane and 5 more levels) errs by under 1e-5 relative for
-V up to 2^20; the division adds half an ulp.
+The kernels compute a probability as e^(z - m) R in fp32 (e^d = 2^(d log2 e)
+by the ex2.approx instruction, R = 1/S rounded once per row); the oracle is
+the float64 softmax.  Tolerance: per entry |p - p_ref| <= REL * p_ref with
+REL = 1e-4, from the fp32 arithmetic: the rounding of z - m and of the
+product with log2 e move the exponent by under |z - m| 2^-23 (under 5e-6
+for the |z - m| <= 40 of these inputs), ex2.approx errs by about 2^-22
+relative, the row sum (16 terms per lane, 5 tree levels inside a block, a
+block's rescaling, then up to blocks / 32 terms per lane and 5 more levels)
+errs by under 1e-5 relative for V up to 2^20, and the reciprocal and the
+product add an ulp.
 
 The draw and the accept decisions are integers decided by those fp32 values,
 so they are compared with the oracle run on the float64 probabilities
