@@ -741,7 +741,7 @@ AcceptShape accept_shape(int B, int k, int V, int num_sms) {
   const size_t units = (size_t)B * s.slices;
   s.stats_off = units * BLK_WARPS * 2 * sizeof(uint64_t) + align_up((size_t)B * 4, 256);
   s.part_off = s.stats_off + align_up((size_t)B * (2 * k + 1) * sizeof(float2), 256);
-  const size_t rows_per_launch = std::min((size_t)B * (k + 1), (size_t)WS_MAX_COUNTERS);
+  const size_t rows_per_launch = std::min((size_t)B * (2 * k + 1), (size_t)WS_MAX_COUNTERS);
   s.scratch_bytes = s.part_off + row_stats_scratch_bytes((int)rows_per_launch, V);
   // Streaming form: one CTA per unit, up to 64 per SM (a grid-stride loop
   // takes the rest).

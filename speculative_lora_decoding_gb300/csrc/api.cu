@@ -363,22 +363,22 @@ static mlora_status accept_impl(const float *p, const float *q, const int32_t *d
   cudaStream_t s = (cudaStream_t)stream;
   float2 *sp = nullptr, *sq = nullptr;
   if (logits) {
-    // Row statistics of the target rows, then of the draft rows, at most
-    // WS_MAX_COUNTERS rows per launch (the block partials' scratch is sized
-    // for that many rows).
+    // Row statistics of the target rows followed by the draft rows (sq = sp +
+    // B (k + 1)), at most WS_MAX_COUNTERS rows per launch (the block
+    // partials' scratch is sized for that many rows).
     sp = reinterpret_cast<float2 *>(ws + WS_SCRATCH_OFF + sh.stats_off);
     sq = sp + (size_t)B * (k + 1);
     void *part = ws + WS_SCRATCH_OFF + sh.part_off;
-    auto stats_of = [&](const float *z, long long rows, float2 *out) -> cudaError_t {
-      for (long long r0 = 0; r0 < rows; r0 += (long long)WS_MAX_COUNTERS) {
-        const int n = (int)std::min<long long>((long long)WS_MAX_COUNTERS, rows - r0);
-        cudaError_t e = launch_row_stats(z + (size_t)r0 * V, n, V, out + r0, part, s);
-        if (e != cudaSuccess) return e;
-      }
-      return cudaSuccess;
-    };
-    cudaError_t e = stats_of(p, (long long)B * (k + 1), sp);
-    if (e == cudaSuccess) e = stats_of(q, (long long)B * k, sq);
+    const long long Rp = (long long)B * (k + 1), R = Rp + (long long)B * k;
+    cudaError_t e = cudaSuccess;
+    for (long long r0 = 0; r0 < R && e == cudaSuccess; r0 += (long long)WS_MAX_COUNTERS) {
+      const long long r1 = std::min(R, r0 + (long long)WS_MAX_COUNTERS);
+      const long long n1 = std::max(0ll, std::min(r1, Rp) - r0);  // target rows of this launch
+      const float *z1 = n1 > 0 ? p + (size_t)r0 * V : q + (size_t)(r0 - Rp) * V;
+      const long long q0 = std::max(r0, Rp) - Rp;                  // first draft row of this launch
+      e = n1 > 0 ? launch_row_stats(z1, (int)n1, q + (size_t)q0 * V, (int)(r1 - r0 - n1), V, sp + r0, part, s)
+                 : launch_row_stats(z1, (int)(r1 - r0), nullptr, 0, V, sp + r0, part, s);
+    }
     if (e != cudaSuccess) return MLORA_ERR_CUDA;
   }
   cudaError_t e = launch_accept(p, q, draft_tok, uniforms, B, k, V, out_tok, accepted,
@@ -419,7 +419,7 @@ mlora_status mlora_softmax(const float *z, int rows, int V, float *p, void *work
   float2 *stats = reinterpret_cast<float2 *>(ws + WS_SCRATCH_OFF);
   void *part = ws + WS_SCRATCH_OFF + align_up((size_t)rows * sizeof(float2), 256);
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_row_stats(z, rows, V, stats, part, s);
+  cudaError_t e = launch_row_stats(z, rows, nullptr, 0, V, stats, part, s);
   if (e == cudaSuccess) e = launch_softmax_write(z, rows, V, stats, p, s);
   return cuda_status(e);
 }

@@ -143,10 +143,13 @@ cudaError_t launch_accept(const float *p, const float *q, const int32_t *draft_t
 // Softmax of logit rows (softmax.cu): stats[r] = (max, sum) of row r; the
 // probabilities expf(z - max) / sum written out; the draft draw.
 // Row statistics take one warp per (row, 512-entry block) and keep the
-// blocks' partial pairs in `scratch` (row_stats_scratch_bytes); a second
-// launch merges each row's pairs.
+// blocks' partial pairs in `scratch` (row_stats_scratch_bytes(R1 + R2, V));
+// a second launch merges each row's pairs.  The rows are those of z1 [R1, V]
+// followed by those of z2 [R2, V] (z2 may be null when R2 = 0); stats gets
+// R1 + R2 pairs in that order.
 size_t row_stats_scratch_bytes(int R, int V);
-cudaError_t launch_row_stats(const float *z, int R, int V, float2 *stats, void *scratch, cudaStream_t s);
+cudaError_t launch_row_stats(const float *z1, int R1, const float *z2, int R2, int V, float2 *stats, void *scratch,
+                             cudaStream_t s);
 cudaError_t launch_softmax_write(const float *z, int R, int V, const float2 *stats, float *p, cudaStream_t s);
 size_t draft_sample_scratch_bytes(int B, int V);
 cudaError_t launch_draft_sample(const float *z, int B, int V, const float *u, int32_t *tok, float2 *stats, float *q,

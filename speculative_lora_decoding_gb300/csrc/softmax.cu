@@ -99,33 +99,32 @@ __device__ __forceinline__ float2 warp_merge(float m, float s) {
   return make_float2(M, t);
 }
 
-// part[r][k] = the pair of block k of row r of z [R, V].  Grid (R, groups of
-// UNIT_WARPS blocks); warp w of CTA (r, y) takes block k = UNIT_WARPS y + w.
+// part[r][k] = the pair of block k of row r, for the rows of two matrices
+// taken as one: rows r < R1 are rows of z1, the others rows r - R1 of z2
+// (R1 = all rows for one matrix).  Grid (rows, groups of UNIT_WARPS blocks);
+// warp w of CTA (r, y) takes block k = UNIT_WARPS y + w.
 __global__ void __launch_bounds__(UNIT_WARPS * 32)
-    block_stats_kernel(const float *__restrict__ z, int V, int nblk, float2 *__restrict__ part) {
+    block_stats_kernel(const float *__restrict__ z1, int R1, const float *__restrict__ z2, int V, int nblk,
+                       float2 *__restrict__ part) {
   grid_dependency_wait();
   grid_launch_dependents();
   const int r = blockIdx.x, k = blockIdx.y * UNIT_WARPS + (threadIdx.x >> 5);
   if (k >= nblk) return;
-  const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(z) & 15) == 0;
+  const float *row = r < R1 ? z1 + (size_t)r * V : z2 + (size_t)(r - R1) * V;
+  const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(r < R1 ? z1 : z2) & 15) == 0;
   float v[16];
-  load_block<false>(z + (size_t)r * V, k, V, vec, -INFINITY, v);
+  load_block<false>(row, k, V, vec, -INFINITY, v);
   const float2 t = lane_stats(v);
   const float2 w = warp_merge(t.x, t.y);
   if ((threadIdx.x & 31) == 0) part[(size_t)r * nblk + k] = w;
 }
 
-// stats[r] = (m, 1/S) of row r from its block pairs, one warp per row: the
+// A row's pair (m, 1/S) from its block pairs pr[0, nblk), by one warp: the
 // maximum, then lane l adds the rescaled sums of blocks l, l + 32, ... in
 // that order, the lanes' sums are added in a fixed tree, and the total's
-// reciprocal is rounded once (IEEE).
-__global__ void __launch_bounds__(ROW_WARPS * 32)
-    row_merge_kernel(const float2 *__restrict__ part, int R, int nblk, float2 *__restrict__ stats) {
-  grid_dependency_wait();
-  grid_launch_dependents();
-  const int r = blockIdx.x * ROW_WARPS + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (r >= R) return;
-  const float2 *pr = part + (size_t)r * nblk;
+// reciprocal is rounded once (IEEE).  Valid in lane 0.
+__device__ __forceinline__ float2 merge_row(const float2 *pr, int nblk) {
+  const int lane = threadIdx.x & 31;
   float M = -INFINITY;
   for (int k = lane; k < nblk; k += 32) M = fmaxf(M, pr[k].x);
 #pragma unroll
@@ -137,7 +136,18 @@ __global__ void __launch_bounds__(ROW_WARPS * 32)
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
-  if (lane == 0) stats[r] = make_float2(M, __frcp_rn(s));
+  return make_float2(M, __frcp_rn(s));
+}
+
+// stats[r] = merge_row of row r, one warp per row.
+__global__ void __launch_bounds__(ROW_WARPS * 32)
+    row_merge_kernel(const float2 *__restrict__ part, int R, int nblk, float2 *__restrict__ stats) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int r = blockIdx.x * ROW_WARPS + (threadIdx.x >> 5);
+  if (r >= R) return;
+  const float2 st = merge_row(part + (size_t)r * nblk, nblk);
+  if ((threadIdx.x & 31) == 0) stats[r] = st;
 }
 
 // p[r, v] = prob_from_logit(z[r, v], stats[r]), in the units of block_stats.
@@ -357,11 +367,12 @@ static dim3 unit_grid(int R, int nblk) { return dim3((unsigned)R, (unsigned)((nb
 
 size_t row_stats_scratch_bytes(int R, int V) { return align_up((size_t)R * blocks_of(V) * sizeof(float2), 256); }
 
-cudaError_t launch_row_stats(const float *z, int R, int V, float2 *stats, void *scratch, cudaStream_t s) {
-  const int nblk = blocks_of(V);
+cudaError_t launch_row_stats(const float *z1, int R1, const float *z2, int R2, int V, float2 *stats, void *scratch,
+                             cudaStream_t s) {
+  const int nblk = blocks_of(V), R = R1 + R2;
   float2 *part = reinterpret_cast<float2 *>(scratch);
   cudaError_t e =
-      launch_pdl(block_stats_kernel, unit_grid(R, nblk), dim3(UNIT_WARPS * 32), 0, s, z, V, nblk, part);
+      launch_pdl(block_stats_kernel, unit_grid(R, nblk), dim3(UNIT_WARPS * 32), 0, s, z1, R1, z2, V, nblk, part);
   if (e != cudaSuccess) return e;
   e = launch_pdl(row_merge_kernel, dim3((unsigned)((R + ROW_WARPS - 1) / ROW_WARPS)), dim3(ROW_WARPS * 32), 0, s,
                  (const float2 *)part, R, nblk, stats);
@@ -384,7 +395,7 @@ cudaError_t launch_draft_sample(const float *z, int B, int V, const float *u, in
   const int nblk = blocks_of(V);
   uint8_t *sc = static_cast<uint8_t *>(scratch);
   uint64_t *blk = reinterpret_cast<uint64_t *>(sc);
-  cudaError_t e = launch_row_stats(z, B, V, stats, sc + draw_sums_bytes(B, V), s);
+  cudaError_t e = launch_row_stats(z, B, nullptr, 0, V, stats, sc + draw_sums_bytes(B, V), s);
   if (e != cudaSuccess) return e;
   e = launch_pdl(draw_weights_kernel, unit_grid(B, nblk), dim3(UNIT_WARPS * 32), 0, s, z, V, nblk,
                  (const float2 *)stats, q, blk);

@@ -104,7 +104,10 @@ def _offset_copy(a):
     return view
 
 
-@pytest.mark.parametrize("B,k,V", [(64, 1, 128256), (32, 3, 128256), (16, 2, 4099), (8, 4, 1000), (3, 1, 5)])
+# (6000, 5, 5): 66000 statistics rows, more than one launch takes (65536), split
+# inside the draft rows.
+@pytest.mark.parametrize("B,k,V", [(64, 1, 128256), (32, 3, 128256), (16, 2, 4099), (8, 4, 1000), (3, 1, 5),
+                                   (6000, 5, 5)])
 def test_accept_on_logits(B, k, V):
     ml = needs_gpu()
     zp, zq, tok, u = WL.accept_logits(V, B, k, sigma=0.3, seed=V + k)
