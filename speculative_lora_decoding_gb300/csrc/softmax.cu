@@ -179,17 +179,33 @@ __global__ void __launch_bounds__(UNIT_WARPS * 32)
   }
 }
 
-// Q(f) = floor(f * 2^40) of f clamped to [0, 1] (NaN to 0), with integer
-// operations on the bits of x = |f| 2^40 (exact): x = M 2^s with the 24-bit
-// significand M (implicit one included) and s = (biased exponent) - 150, so
-// floor(x) is M shifted left by s when s >= 0 and right by -s otherwise
-// (nothing is left once -s reaches 24: x < 1, zero and subnormals included).
+// Q(f) = floor(f * 2^40) of f clamped to [0, 1] (NaN to 0), in two parts,
+// each from one float operation rounded down onto the integers of
+// [2^23, 2^24], whose bit patterns are 0x4B000000 plus the integer:
+//   h  = floor(c 2^23):          t1 = c 2^23 + 2^23 rounded down;
+//   lo = floor((c 2^23 - h) 2^17): c 2^23 - h (exact, in [0, 1)) times 2^17
+//                                  plus 2^23, rounded down;
+// and Q = h 2^17 + lo.  q40_parts returns the two bit patterns; a sum of n
+// of them, taken mod 2^32, less n * 0x4B000000 is the sum of the parts
+// exactly as long as that sum is below 2^32.
+constexpr uint32_t Q40_OFFSET = 0x4B000000u;  // the bit pattern of 2^23
+
+__device__ __forceinline__ void q40_parts(float f, uint32_t &hb, uint32_t &lb) {
+  const float c = fminf(fmaxf(f, 0.f), 1.f);
+  const float t1 = __fmaf_rd(c, 8388608.0f, 8388608.0f);
+  const float fr = __fmaf_rn(c, 8388608.0f, -(t1 - 8388608.0f));
+  const float t2 = __fmaf_rd(fr, 131072.0f, 8388608.0f);
+  hb = __float_as_uint(t1);
+  lb = __float_as_uint(t2);
+}
+
+// Q from the parts' sums (offsets removed): h 2^17 + lo.
+__device__ __forceinline__ uint64_t q40_join(uint32_t h, uint32_t lo) { return ((uint64_t)h << 17) + lo; }
+
 __device__ __forceinline__ uint64_t q40(float f) {
-  const float x = fabsf(fminf(fmaxf(f, 0.f), 1.f)) * 1099511627776.0f;
-  const uint32_t bits = __float_as_uint(x);
-  const uint32_t M = (bits & 0x7FFFFFu) | 0x800000u;
-  const int s = (int)(bits >> 23) - 150;
-  return s >= 0 ? (uint64_t)M << s : (uint64_t)(M >> min(-s, 31));
+  uint32_t hb, lb;
+  q40_parts(f, hb, lb);
+  return q40_join(hb - Q40_OFFSET, lb - Q40_OFFSET);
 }
 
 __device__ __forceinline__ uint64_t warp_sum_u64_sm(uint64_t v) {
@@ -223,20 +239,27 @@ __global__ void __launch_bounds__(UNIT_WARPS * 32)
   const float2 st = stats[b];
   float v[16];
   load_block<true>(z + (size_t)b * V, k, V, vec, 0.f, v);
-  uint64_t w = 0;
+  // The lane's 16 weights as sums of their parts' bit patterns (the h parts
+  // sum below 2^27, the lo parts below 2^21).
+  uint32_t sh = 0, sl = 0;
   if ((k + 1) * SM_BLOCK <= V) {  // every block but a row's last
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       v[j] = prob_from_logit(v[j], st);
-      w += q40(v[j]);
+      uint32_t hb, lb;
+      q40_parts(v[j], hb, lb);
+      sh += hb, sl += lb;
     }
   } else {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       v[j] = lane_entry(k, j >> 2, j & 3) < V ? prob_from_logit(v[j], st) : 0.f;
-      w += q40(v[j]);
+      uint32_t hb, lb;
+      q40_parts(v[j], hb, lb);
+      sh += hb, sl += lb;
     }
   }
+  uint64_t w = q40_join(sh - 16u * Q40_OFFSET, sl - 16u * Q40_OFFSET);
   if (q_out) {
     float *qr = q_out + (size_t)b * V;
 #pragma unroll
