@@ -116,3 +116,13 @@ def test_fp8_host_checks(lib):
     assert lib.mlora_linear_fp8(p, 128, 512, p, p, 64, p, 0, None, 0, None) == WS
     assert lib.mlora_quantize_rows_fp8(p, 4, 24, p, p, None) == SHAPE
     assert lib.mlora_quantize_rows_fp8(None, 4, 32, p, p, None) == ARG
+
+
+def test_q40_hook_host_checks(lib):
+    """The Q(f) check hook refuses a null counter and a range past 2^32
+    before any CUDA call; an empty range does nothing."""
+    dummy = ctypes.c_void_p(16)  # never dereferenced: these calls return before any launch
+    assert lib.mlora_debug_q40_mismatches(0, 1, None, None) == 1                 # MLORA_ERR_ARG
+    assert lib.mlora_debug_q40_mismatches(2, 0xFFFFFFFF, dummy, None) == 1       # past 2^32
+    assert lib.mlora_debug_q40_mismatches(0xFFFFFFFF, 2, dummy, None) == 1
+    assert lib.mlora_debug_q40_mismatches(5, 0, dummy, None) == 0                # MLORA_OK, nothing launched
