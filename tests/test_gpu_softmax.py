@@ -87,6 +87,11 @@ def test_draft_sample_against_oracle(B, V):
     assert torch.equal(q, ml.softmax(dev(zq)))  # the draw used the library's probabilities
     # On the kernel's own probabilities the draw is integer work: bit-exact.
     assert np.array_equal(tok.cpu().numpy(), OS.draft_sample(q.cpu().numpy(), u))
+    # The same logits through a view 4 bytes off 16-byte alignment (the
+    # kernels' scalar-load path) give the same probabilities and tokens.
+    tok2, q2 = ml.draft_sample(_offset_copy(zq), dev(u))
+    assert torch.equal(tok2, tok) and torch.equal(q2, q)
+    assert torch.equal(ml.softmax(_offset_copy(zq)), q)
     q_ref32 = OS.softmax(zq.astype(np.float64)).astype(np.float32)
     tok_ref = OS.draft_sample(q_ref32, u)
     tok = tok.cpu().numpy()
