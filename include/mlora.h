@@ -264,6 +264,17 @@ MLORA_API void mlora_debug_set_flag_wait_ns(uint32_t ns);
 MLORA_API mlora_status mlora_debug_q40_mismatches(uint32_t first_bits, uint32_t count,
                                                   unsigned long long *mismatches, mlora_stream stream);
 
+/* Test hook for the probability expression (no counterpart on the pages):
+ * the kernels compute e^d as 2^(d log2 e) with the PTX ex2.approx
+ * instruction.  For the `count` fp32 bit patterns first_bits,
+ * first_bits + 1, ... whose CUDA expf is a normal float, this raises
+ * *max_rel_bits (device memory, caller-owned, caller-zeroed; the bit pattern
+ * of a non-negative float) to the largest |e^d - expf(d)| / expf(d).
+ * Asynchronous on `stream`.  MLORA_ERR_ARG when the range passes 2^32 or the
+ * pointer is NULL. */
+MLORA_API mlora_status mlora_debug_exp_max_rel_error(uint32_t first_bits, uint32_t count, unsigned int *max_rel_bits,
+                                                     mlora_stream stream);
+
 /* Which kernel writes the low-rank operand (the token windows of
  * bf16(scale * A_a x)) in later verify-mode layer calls (no counterpart on the
  * pages, which compute the per-adapter product without naming a kernel):

@@ -76,6 +76,7 @@ _SIGNATURES = {
     "mlora_linear_gemm_kernel": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "mlora_debug_set_flag_wait_ns": (None, [ctypes.c_uint32]),
     "mlora_debug_q40_mismatches": (_c_int, [ctypes.c_uint32, ctypes.c_uint32, _c_ptr, _c_ptr]),
+    "mlora_debug_exp_max_rel_error": (_c_int, [ctypes.c_uint32, ctypes.c_uint32, _c_ptr, _c_ptr]),
     "mlora_set_shrink_path": (_c_int, [_c_int]),
     "mlora_verify_accept_logits": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr, _c_ptr,
                                             _c_ptr, _c_size, _c_ptr]),

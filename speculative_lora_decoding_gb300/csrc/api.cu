@@ -342,6 +342,15 @@ mlora_status mlora_debug_q40_mismatches(uint32_t first_bits, uint32_t count, uns
   return cuda_status(launch_q40_check(first_bits, count, mismatches, sms, (cudaStream_t)stream));
 }
 
+mlora_status mlora_debug_exp_max_rel_error(uint32_t first_bits, uint32_t count, unsigned int *max_rel_bits,
+                                          mlora_stream stream) {
+  if (!max_rel_bits || (uint64_t)first_bits + count > (1ull << 32)) return MLORA_ERR_ARG;
+  if (count == 0) return MLORA_OK;
+  const int sms = device_sms();
+  if (sms <= 0) return MLORA_ERR_CUDA;
+  return cuda_status(launch_exp_check(first_bits, count, max_rel_bits, sms, (cudaStream_t)stream));
+}
+
 mlora_status mlora_set_shrink_path(int path) {
   if (path != MLORA_SHRINK_AUTO && path != MLORA_SHRINK_WARP && path != MLORA_SHRINK_TENSOR) return MLORA_ERR_ARG;
   g_shrink_path.store(path, std::memory_order_relaxed);

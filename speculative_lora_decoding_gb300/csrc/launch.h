@@ -156,6 +156,8 @@ cudaError_t launch_draft_sample(const float *z, int B, int V, const float *u, in
                                 void *scratch, uint32_t *status, cudaStream_t s);
 cudaError_t launch_q40_check(uint32_t first, uint32_t count, unsigned long long *mismatches, int num_sms,
                              cudaStream_t s);
+cudaError_t launch_exp_check(uint32_t first, uint32_t count, unsigned int *max_rel_bits, int num_sms,
+                             cudaStream_t s);
 
 // Hybrid KV cache (kvcache.cu): the K/V rows of one pass into the paged
 // cache, and the committed lengths after the accept step.

@@ -383,6 +383,29 @@ cudaError_t launch_q40_check(uint32_t first, uint32_t count, unsigned long long 
   return cudaGetLastError();
 }
 
+// Test hook: the largest relative difference between exp_of(d) and CUDA's
+// expf(d) over the bit patterns first + i (i < count), where expf(d) is a
+// normal float; atomicMax on the bit pattern of the (non-negative) float.
+__global__ void exp_check_kernel(uint32_t first, uint32_t count, unsigned int *max_rel_bits) {
+  float worst = 0.f;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride) {
+    const float d = __uint_as_float(first + i);
+    const float ref = expf(d);
+    if (isfinite(d) && isfinite(ref) && ref >= 1.17549435e-38f) worst = fmaxf(worst, fabsf(exp_of(d) - ref) / ref);
+    if (stride > count - i) break;  // the next i would wrap past 2^32
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) worst = fmaxf(worst, __shfl_xor_sync(0xffffffffu, worst, o));
+  if ((threadIdx.x & 31) == 0 && worst > 0.f) atomicMax(max_rel_bits, __float_as_uint(worst));
+}
+
+cudaError_t launch_exp_check(uint32_t first, uint32_t count, unsigned int *max_rel_bits, int num_sms,
+                             cudaStream_t s) {
+  exp_check_kernel<<<std::max(num_sms, 1) * 8, 256, 0, s>>>(first, count, max_rel_bits);
+  return cudaGetLastError();
+}
+
 static int blocks_of(int V) { return (V + SM_BLOCK - 1) / SM_BLOCK; }
 
 // The grid of the streaming kernels: x = row, y = group of UNIT_WARPS blocks.

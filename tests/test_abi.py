@@ -126,3 +126,12 @@ def test_q40_hook_host_checks(lib):
     assert lib.mlora_debug_q40_mismatches(2, 0xFFFFFFFF, dummy, None) == 1       # past 2^32
     assert lib.mlora_debug_q40_mismatches(0xFFFFFFFF, 2, dummy, None) == 1
     assert lib.mlora_debug_q40_mismatches(5, 0, dummy, None) == 0                # MLORA_OK, nothing launched
+
+
+def test_exp_hook_host_checks(lib):
+    """The e^d check hook refuses a null result pointer and a range past 2^32
+    before any CUDA call; an empty range does nothing."""
+    dummy = ctypes.c_void_p(16)  # never dereferenced: these calls return before any launch
+    assert lib.mlora_debug_exp_max_rel_error(0, 1, None, None) == 1              # MLORA_ERR_ARG
+    assert lib.mlora_debug_exp_max_rel_error(2, 0xFFFFFFFF, dummy, None) == 1    # past 2^32
+    assert lib.mlora_debug_exp_max_rel_error(7, 0, dummy, None) == 0             # MLORA_OK, nothing launched

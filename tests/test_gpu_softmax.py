@@ -165,3 +165,35 @@ def test_q40_matches_cuda_conversion_on_every_float():
     assert int(bad.item()) == 0
     # The range check: first + count past 2^32 is refused.
     assert lib.mlora_debug_q40_mismatches(2, 0xFFFFFFFF, bad.data_ptr(), None) != 0
+
+
+def _exp_max_rel(lib, lo, hi):
+    """Largest relative difference between the kernels' e^d and CUDA's expf
+    over every fp32 d in [lo, hi] (lo <= hi <= 0)."""
+    import struct
+    bits = lambda f: struct.unpack("<I", struct.pack("<f", f))[0]  # noqa: E731
+    first, last = bits(float(hi)) if hi < 0 else 0x80000000, bits(float(lo))
+    out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert lib.mlora_debug_exp_max_rel_error(first, last - first + 1, out.data_ptr(), None) == 0
+    if hi >= 0:  # d = +0 as well
+        assert lib.mlora_debug_exp_max_rel_error(0, 1, out.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    return float(out.cpu().view(torch.float32).item())
+
+
+def test_exp_against_cuda_expf():
+    """e^d = 2^(d log2 e) by ex2.approx against CUDA's expf on every fp32 d in
+    [-87, 0].  The error comes from rounding y = d log2 e (half an ulp of y:
+    2^-18 for |y| < 128, 2^-19 for |y| < 64), from log2 e rounded to fp32
+    (1.3e-8 relative, so |y| * 1.3e-8 absolute), each moving e^d by ln 2 times
+    that, plus ex2.approx's and expf's own few-ulp errors: about 4.3e-6
+    relative over the whole range and 2.2e-6 for |d| <= 40.  The limits
+    below leave room for the two instructions' errors."""
+    ml = needs_gpu()
+    lib = ml.library()
+    near = _exp_max_rel(lib, -40.0, 0.0)
+    full = _exp_max_rel(lib, -87.0, 0.0)
+    assert 0.0 < near <= 4e-6, near
+    assert near <= full <= 8e-6, full
+    bad = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert lib.mlora_debug_exp_max_rel_error(2, 0xFFFFFFFF, bad.data_ptr(), None) != 0
