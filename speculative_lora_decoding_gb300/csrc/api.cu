@@ -103,7 +103,14 @@ static bool use_stream_k(int M, int N, int K, bool verify, bool have_tw, bool ha
   // fits: measured on the 8B shapes at 64 and 256 rows, o and down (one
   // cluster wave of 84%) took 121 -> 114 us and 158 -> 148 us per pass there.
   bool cluster_good = verify && gs.waves == 1 && (long long)gs.n_units * gs.C * 5 >= (long long)sms * 4;
-  if (M > 256) cluster_good = verify && gs.waves == 1 && (long long)gs.n_units * gs.C * 10 >= (long long)sms * 7;
+  // Past 256 rows the cluster kernel keeps up to 512 rows in one token group
+  // (two sub-accumulators).  Measured on GB300 at 384 rows (the 32B block at
+  // k = 2) it lost to the stream-K kernel's two groups of 192 (q|k|v 100 ->
+  // 70 us; o, gate|up and down within 2 us), while at 512 rows (8B o and
+  // down: 84 and 137 us against 95 and 143) and at 640 rows it held its own
+  // when one wave fills 70% of the SMs.
+  if (M > 256)
+    cluster_good = M > 384 && verify && gs.waves == 1 && (long long)gs.n_units * gs.C * 10 >= (long long)sms * 7;
   const SkShape sk = sk_shape(M, N, K, sms);
   if (sk_out) *sk_out = sk;
   const bool fits = sk.ok && have_sk && (!verify || have_tw);

@@ -169,6 +169,7 @@ def test_gemm_kernel_query():
         assert ml.gemm_kernel_name(640, 5120, 5120, 64, 16, ml.VERIFY) == "gemm_sk_kernel"
         assert ml.gemm_kernel_name(640, 5120, 27648, 64, 16, ml.VERIFY) == "gemm_sk_kernel"
         assert ml.gemm_kernel_name(640, 7168, 5120, 64, 16, ml.VERIFY) == "gemm_kernel"  # one wave, 74% full
+        assert ml.gemm_kernel_name(384, 7168, 5120, 64, 16, ml.VERIFY) == "gemm_sk_kernel"  # 257..384 rows
         assert ml.gemm_kernel_name(64, 4096, 4096, 16, 16, ml.DRAFT) == "gemm_sk_kernel"
         assert ml.gemm_kernel_name(64, 4096, 14336, 16, 16, ml.DRAFT) == "gemm_sk_kernel"
         assert ml.gemm_kernel_name(64, 28672, 4096, 16, 16, ml.DRAFT) == "gemm_sk_kernel"
