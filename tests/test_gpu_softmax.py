@@ -197,3 +197,27 @@ def test_exp_against_cuda_expf():
     assert near <= full <= 8e-6, full
     bad = torch.zeros(1, dtype=torch.int32, device="cuda")
     assert lib.mlora_debug_exp_max_rel_error(2, 0xFFFFFFFF, bad.data_ptr(), None) != 0
+
+
+def test_draft_sample_uniform_edge_cases():
+    """Uniforms outside [0, 1) are clamped as the accept step clamps them (NaN
+    and negatives to 0, 1 and above to the largest float below 1) and raise
+    MLORA_DEV_BAD_PROB; the tokens equal the oracle's on the kernel's own
+    probabilities, including the draws at the two ends of the range."""
+    ml = needs_gpu()
+    V, B = 1000, 6
+    zq = WL.accept_logits(V, B, 1, seed=5)[1][:, 0].copy()
+    below_one = np.nextafter(np.float32(1), np.float32(0))
+    u = np.array([np.nan, -1.0, 1.5, 1.0, below_one, 0.0], dtype=np.float32)
+    ws = ml.Workspace(int(ml.library().mlora_draft_sample_workspace_bytes(B, V)))
+    tok, q = ml.draft_sample(dev(zq), dev(u), ws=ws)
+    assert ws.status() & ml.DEV_BAD_PROB
+    assert np.array_equal(tok.cpu().numpy(), OS.draft_sample(q.cpu().numpy(), u))
+    # u = 0 draws the first token with weight; the largest u the last one.
+    w = OA.quantize(q.cpu().numpy())
+    assert tok[5].item() == int(np.flatnonzero(w[5])[0])
+    assert tok[4].item() == int(np.flatnonzero(w[4])[-1])
+    # Only valid uniforms: no status bit.
+    ws2 = ml.Workspace(int(ml.library().mlora_draft_sample_workspace_bytes(B, V)))
+    ml.draft_sample(dev(zq), dev(np.full(B, 0.5, dtype=np.float32)), ws=ws2)
+    assert ws2.status() == 0
