@@ -76,7 +76,7 @@ def test_softmax_matches_float64(rows, V):
     assert torch.equal(p[-1:], ml.softmax(dev(z[-1:])))
 
 
-@pytest.mark.parametrize("B,V", [(256, 128256), (9, 1000), (7, 4099), (3, 600000)])
+@pytest.mark.parametrize("B,V", [(256, 128256), (9, 1000), (7, 4099), (3, 600000), (1, 1 << 24)])
 def test_draft_sample_against_oracle(B, V):
     ml = needs_gpu()
     zq = WL.accept_logits(V, B, 1, seed=B)[1][:, 0].copy()
